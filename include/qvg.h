@@ -1,0 +1,163 @@
+/*
+ * qvg.h -- C ABI of libqvg, a GB300 (sm_103a) implementation of the KV-cache compression
+ * path of Quant VideoGen (arXiv 2602.02958).
+ *
+ * The method, as the pages state it:
+ *   - Semantic-Aware Smoothing ("Quant VideoGen" notes page, section Semantic-Aware
+ *     Smoothing; review page "Quant VideoGen: 基于2-Bit KV缓存量化的自回归长视频生成",
+ *     pipeline paragraph, steps (a)-(c)): the N tokens of a per-head tensor X in R^{N x d}
+ *     are clustered by k-means along the token axis into C groups, and each token has its
+ *     group's centroid (the group mean) subtracted.
+ *   - Progressive Residual Quantization (notes page, section Progressive Residual
+ *     Quantization; review page, pipeline paragraph): with R^(0) = X, stage t = 1..T
+ *     re-applies the smoothing to R^(t-1), producing R^(t), centroids C^(t) and
+ *     assignments pi^(t); only R^(T) is quantized.
+ *   - Q(R^(T)) is symmetric group integer quantization, INT2 or INT4, with one scale per
+ *     group stored as FP8 E4M3 (notes page, section Algorithm-System Co-design; explainer
+ *     "Quant VideoGen: Auto-Regressive Long Video Generation via 2-Bit KV-Cache
+ *     Quantization", section Step-by-step).
+ *   - Reconstruction dequantizes and adds the stages' assigned centroids back from stage T
+ *     down to stage 1, fused in one pass (notes page, sections Progressive Residual
+ *     Quantization and Algorithm-System Co-design).
+ *   - Streaming: the previous chunk's centroids initialise the next chunk's k-means
+ *     (notes page, section Algorithm-System Co-design).
+ *
+ * Conventions for every call:
+ *   - All data pointers are DEVICE pointers into memory the caller owns and keeps alive
+ *     until the work on `stream` has finished.  The library allocates no device memory and
+ *     keeps no mutable global state; scratch space is the caller's `workspace`.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).  Work
+ *     is enqueued asynchronously; a call returns once it is enqueued.
+ *   - Argument errors are detected on the host before anything is enqueued and returned as
+ *     QVG_ERR_INVALID_ARG / QVG_ERR_UNSUPPORTED / QVG_ERR_WORKSPACE.  A CUDA error reported
+ *     while enqueuing returns QVG_ERR_CUDA; work already enqueued may have run.
+ *   - Conditions only the device can see are OR-ed into *dev_status (a device uint32, may
+ *     be NULL) as QVG_DEV_* bits; read it after synchronising the stream.  No call aborts
+ *     the process or traps the device.
+ *   - Pointers must be 16-byte aligned.
+ *
+ * Supported shapes: d = 128; group in {16, 32, 64}; bits in {2, 4}; 1 <= C <= 256 and
+ * C <= N when T > 0; 0 <= T <= 8; iters >= 1; N >= 1.
+ */
+#ifndef QVG_H
+#define QVG_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    QVG_OK = 0,
+    QVG_ERR_INVALID_ARG = 1, /* NULL / misaligned pointer, negative or inconsistent size */
+    QVG_ERR_UNSUPPORTED = 2, /* a value outside the supported shapes listed above */
+    QVG_ERR_WORKSPACE = 3,   /* workspace NULL or smaller than qvg_quantize_workspace_bytes */
+    QVG_ERR_CUDA = 4,        /* a CUDA runtime call failed while enqueuing (no device, launch) */
+    QVG_ERR_DEVICE = 5       /* the current device is not an sm_103 (GB300-class) GPU */
+} qvg_status;
+
+/* Bits OR-ed into *dev_status by the device. */
+#define QVG_DEV_NONFINITE 0x1u /* X held a NaN or an infinity */
+#define QVG_DEV_TIMEOUT 0x2u   /* a pipeline wait in the assignment kernel gave up */
+#define QVG_DEV_BAD_INDEX 0x4u /* a stored cluster index was >= C; it was clamped to C-1 */
+
+typedef enum { QVG_F16 = 0, QVG_BF16 = 1, QVG_F32 = 2 } qvg_dtype;
+
+/* Parameters of one qvg_quantize call: n_tensors independent tensors of N tokens each. */
+typedef struct {
+    int32_t n_tensors;      /* H >= 1: independent (layer, head, K/V) tensors in this call */
+    int32_t d;              /* channels per token; must be 128 */
+    int64_t N;              /* tokens per tensor in this call */
+    int32_t C;              /* clusters per stage */
+    int32_t T;              /* smoothing stages (0 = plain group quantization) */
+    int32_t bits;           /* 2 or 4 */
+    int32_t group;          /* channels per scale group: 16, 32 or 64 */
+    int32_t iters;          /* Lloyd rounds (assign + mean update) per stage */
+    int32_t in_dtype;       /* qvg_dtype of X */
+    uint64_t seed;          /* cold-start seed */
+    int64_t tensor_id_base; /* tensor h of this call uses id tensor_id_base + h for seeding */
+    int64_t x_stride;       /* elements between consecutive tensors of X (0 = N*d) */
+    int64_t token_offset;   /* first token slot written in codes / scales / pi */
+    int64_t token_capacity; /* token slots per tensor in codes / scales / pi (0 = N) */
+    int32_t table_index;    /* centroid-table slot written by this call */
+    int32_t n_tables;       /* centroid-table slots per tensor (0 = 1) */
+    int64_t warm_stride;    /* floats between consecutive tensors of warm_centroids
+                               (0 = T*C*d) */
+} qvg_quant_params;
+
+/* The compressed cache.  Layouts (all row-major, caller-owned device memory):
+ *   codes     uint8 [H][token_capacity][d*bits/8]  channel k of a token sits at bits
+ *             (k*bits) mod 8 of byte (k*bits)/8 of its row; stored code u = q + 2^(bits-1)
+ *   scales    uint8 [H][token_capacity][d/group]   FP8 E4M3 bit patterns
+ *   pi        uint8 [H][T][token_capacity]         cluster index per stage and token
+ *   centroids float [H][n_tables][T][C][d]         one table per chunk of tokens
+ * For T = 0, pi and centroids are not touched and may be NULL. */
+typedef struct {
+    uint8_t *codes;
+    uint8_t *scales;
+    uint8_t *pi;
+    float *centroids;
+} qvg_buffers;
+
+/* Bytes of device scratch qvg_quantize needs for these parameters (0 if they are invalid).
+ * Depends only on n_tensors, N, C, T. */
+size_t qvg_quantize_workspace_bytes(const qvg_quant_params *params);
+
+/* Compress X: T smoothing stages of `iters` Lloyd rounds each, then group quantization of
+ * the last residual.  Writes codes/scales for tokens [token_offset, token_offset + N),
+ * pi^(1..T) for the same slots, and C^(1..T) into table slot table_index.
+ *   X               [H][N][d] of in_dtype, tensor h at X + h*x_stride elements
+ *   warm_centroids  NULL for a cold start (seeded distinct rows of R^(t-1) as the initial
+ *                   centroids of stage t), or fp32 [H][T][C][d] (tensor stride warm_stride)
+ *                   used as stage t's initial centroids -- the streaming warm start.  It
+ *                   may point into out->centroids (another table slot than table_index).
+ *   workspace       >= qvg_quantize_workspace_bytes(params) bytes, 256-byte aligned; its
+ *                   contents on entry do not matter.
+ * Calls that share a workspace must be ordered on one stream. */
+qvg_status qvg_quantize(const qvg_quant_params *params, const void *X,
+                        const float *warm_centroids, const qvg_buffers *out, void *workspace,
+                        size_t workspace_bytes, uint32_t *dev_status, void *stream);
+
+/* Assign every token's stage-T residual R^(T-1) to its nearest centroid of C^(T) as stored
+ * in out->centroids (table slot table_index), writing pi^(T).  This is one assignment step
+ * of the Lloyd iteration (notes page, section Semantic-Aware Smoothing, step 1), run on the
+ * state a preceding qvg_quantize call with the same params, X, out and workspace left
+ * behind: the residual planes of stage T stay in the workspace.  It lets the tensor-core
+ * assignment be timed and checked on its own.  Requires T >= 1.  The codes and scales
+ * are not updated. */
+qvg_status qvg_reassign(const qvg_quant_params *params, const void *X, const qvg_buffers *out,
+                        void *workspace, size_t workspace_bytes, uint32_t *dev_status,
+                        void *stream);
+
+/* Parameters of one qvg_dequantize call. */
+typedef struct {
+    int32_t n_tensors;      /* H */
+    int32_t d;              /* 128 */
+    int64_t N;              /* tokens to reconstruct per tensor, slots [0, N) */
+    int32_t C, T, bits, group;
+    int32_t out_dtype;      /* qvg_dtype of X_hat */
+    int64_t chunk_len;      /* tokens per centroid table: slot i uses table i / chunk_len
+                               (0 = N, one table) */
+    int64_t token_capacity; /* token slots per tensor in codes / scales / pi (0 = N) */
+    int32_t n_tables;       /* centroid-table slots per tensor (0 = 1) */
+    int64_t out_stride;     /* elements between consecutive tensors of X_hat (0 = N*d) */
+} qvg_dequant_params;
+
+/* Reconstruct X_hat[h][i] = s_q * (u - 2^(bits-1)) + C^(T)[pi^(T)_i] + ... + C^(1)[pi^(1)_i],
+ * added in that order (stage T first) in fp32 registers, rounded once to out_dtype. */
+qvg_status qvg_dequantize(const qvg_dequant_params *params, const qvg_buffers *in,
+                          void *X_hat, uint32_t *dev_status, void *stream);
+
+/* Static description of a status code. */
+const char *qvg_status_string(qvg_status status);
+
+/* Library version, (major << 16) | minor. */
+uint32_t qvg_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QVG_H */

@@ -55,6 +55,10 @@ def _load():
         lib.orc_e4m3_decode.argtypes = [c.c_uint8]
         lib.orc_e4m3_encode.restype = c.c_uint8
         lib.orc_e4m3_encode.argtypes = [c.c_double]
+        lib.orc_e4m3_encode_n.restype = None
+        lib.orc_e4m3_encode_n.argtypes = [_f64p, c.c_int64, _u8p]
+        lib.orc_e4m3_decode_n.restype = None
+        lib.orc_e4m3_decode_n.argtypes = [_u8p, c.c_int64, _f64p]
         lib.orc_init_indices.restype = c.c_int
         lib.orc_init_indices.argtypes = [c.c_uint64, c.c_int64, c.c_int, c.c_int64, c.c_int, _i64p]
         lib.orc_assign.restype = None
@@ -112,16 +116,17 @@ def num_cores() -> int:
 
 
 def e4m3_decode(b) -> np.ndarray:
-    lib = _load()
-    b = np.asarray(b, dtype=np.uint8)
-    return np.array([lib.orc_e4m3_decode(int(v)) for v in b.ravel()]).reshape(b.shape)
+    b = np.ascontiguousarray(b, dtype=np.uint8)
+    out = np.zeros(b.shape, dtype=np.float64)
+    _load().orc_e4m3_decode_n(b.reshape(-1), b.size, out.reshape(-1))
+    return out
 
 
 def e4m3_encode(x) -> np.ndarray:
-    lib = _load()
-    x = np.asarray(x, dtype=np.float64)
-    return np.array([lib.orc_e4m3_encode(float(v)) for v in x.ravel()],
-                    dtype=np.uint8).reshape(x.shape)
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    out = np.zeros(x.shape, dtype=np.uint8)
+    _load().orc_e4m3_encode_n(x.reshape(-1), x.size, out.reshape(-1))
+    return out
 
 
 def init_indices(seed: int, tensor_id: int, stage: int, N: int, C: int) -> np.ndarray:

@@ -89,6 +89,14 @@ uint8_t orc_e4m3_encode(double x) {
     return (uint8_t)(sign | best);
 }
 
+void orc_e4m3_encode_n(const double *x, int64_t n, uint8_t *out) {
+    for (int64_t i = 0; i < n; i++) out[i] = orc_e4m3_encode(x[i]);
+}
+
+void orc_e4m3_decode_n(const uint8_t *b, int64_t n, double *out) {
+    for (int64_t i = 0; i < n; i++) out[i] = orc_e4m3_decode(b[i]);
+}
+
 /* ------------------------------------------------------------------------------------ */
 /* Seeded cold start.                                                                     */
 /* ------------------------------------------------------------------------------------ */

@@ -1,0 +1,153 @@
+"""Comparison helpers for the GPU-vs-oracle parity tests.
+
+Tolerances (derived from the arithmetic; see the design notes for the derivations):
+  * codes and E4M3 scales, given the same assignments and centroids: bit-exact, except
+    groups whose exact scale max|r|/qmax lies within 2^-20 (relative) of an E4M3 rounding
+    midpoint and elements whose exact r/s_q lies within 2^-20 (relative) of a half-integer.
+    The GPU forms r as the fp32 value nearest the exact residual and divides in IEEE fp32,
+    so it can only differ from the fp64 oracle inside those bands.  Band cases are counted.
+  * centroids, given the same assignments: |C_gpu - C_exact| <= ulp32(C_exact) +
+    0.5 * max over the cluster of ulp32(r_i).  The GPU's mean is the correctly rounded mean
+    of the fp32-rounded residuals r_i (exact fixed-point sums), so it is off the exact mean
+    by at most the mean of the members' rounding errors plus one final rounding.  For stage
+    1 the residual is X itself (exact in fp32) and the second term is zero.
+  * reconstruction into fp32: |x_gpu - x_oracle| <= max(1e-3 * s_q, (T + 1) * ulp32(S)) with
+    S = |deQ| + sum_t |C^(t)[pi^(t)]|: the GPU adds T + 1 fp32 terms in sequence, each add
+    rounding by at most half an ulp of a partial sum bounded by S.
+  * assignments from two independent runs: >= 99.9 % agreement per stage; the Lloyd
+    objective within 1e-3 relative.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+import oracle
+
+
+def ulp32(x):
+    x = np.abs(np.asarray(x, dtype=np.float64)).astype(np.float32)
+    return np.spacing(np.maximum(x, np.float32(np.finfo(np.float32).tiny))).astype(np.float64)
+
+
+def unpack_codes(codes, bits):
+    codes = np.asarray(codes, dtype=np.uint8)
+    per = 8 // bits
+    mask = (1 << bits) - 1
+    u = np.stack([(codes >> (bits * k)) & mask for k in range(per)], axis=-1)
+    return u.reshape(*codes.shape[:-1], codes.shape[-1] * per).astype(np.int64)
+
+
+def compare_codes(R, codes_gpu, scales_gpu, bits, group, eps=2.0 ** -20):
+    """R: exact final residual [N][d] (fp64).  Returns counts; raises on a real mismatch."""
+    qmax = (1 << (bits - 1)) - 1
+    N, d = R.shape
+    ng = d // group
+    codes_o, scales_o = oracle.encode(R, bits, group)
+    a = np.abs(R.reshape(N, ng, group)).max(axis=2)
+    s = a / qmax
+    sb_lo = oracle.e4m3_encode(s * (1 - eps))
+    sb_hi = oracle.e4m3_encode(s * (1 + eps))
+    band_group = sb_lo != sb_hi
+    sq = oracle.e4m3_decode(scales_o)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        v = R / np.repeat(sq, group, axis=1)
+    frac = np.abs(np.abs(v - np.floor(v)) - 0.5)
+    band_elem = np.where(np.repeat(sq, group, axis=1) > 0,
+                         frac <= eps * np.maximum(np.abs(v), 1.0), False)
+    band_elem |= np.repeat(band_group, group, axis=1)
+    scales_gpu = np.asarray(scales_gpu)
+    bad_scales = (scales_gpu != scales_o) & ~band_group
+    u_o = unpack_codes(codes_o, bits)
+    u_g = unpack_codes(codes_gpu, bits)
+    bad_codes = (u_o != u_g) & ~band_elem
+    res = {"band_groups": int(band_group.sum()), "band_elems": int(band_elem.sum()),
+           "scale_mismatch": int(bad_scales.sum()), "code_mismatch": int(bad_codes.sum()),
+           "groups": int(band_group.size), "elems": int(band_elem.size)}
+    if res["scale_mismatch"] or res["code_mismatch"]:
+        i, g = np.argwhere(bad_scales)[0] if res["scale_mismatch"] else np.argwhere(bad_codes)[0]
+        raise AssertionError("code/scale mismatch outside the rounding band: %s; first at "
+                             "token %d group/elem %d" % (res, i, g))
+    return res
+
+
+def check_centroids(R_in, pi_t, cent_gpu, stage):
+    """Centroids of one stage against the exact means of R_in over pi_t."""
+    C = cent_gpu.shape[0]
+    pi_t = np.asarray(pi_t, dtype=np.int64)
+    counts = np.bincount(pi_t, minlength=C)
+    sums = np.zeros((C, R_in.shape[1]))
+    np.add.at(sums, pi_t, R_in)
+    nz = counts > 0
+    exact = sums[nz] / counts[nz, None]
+    if stage == 1:
+        slack = np.zeros(C)
+    else:
+        maxabs = np.zeros(C)
+        np.maximum.at(maxabs, pi_t, np.abs(R_in).max(axis=1))
+        slack = 0.5 * ulp32(maxabs)
+    tol = ulp32(exact) + slack[nz, None] + 1e-300
+    err = np.abs(cent_gpu[nz].astype(np.float64) - exact)
+    worst = float((err / tol).max()) if err.size else 0.0
+    if worst > 1.0:
+        j = np.argwhere(err > tol)[0]
+        raise AssertionError("stage %d centroid off by %.3g tolerances (cluster row %d, "
+                             "channel %d)" % (stage, worst, j[0], j[1]))
+    return {"clusters": int(nz.sum()), "empty": int((~nz).sum()), "worst_tol_frac": worst,
+            "exact_bits": int((cent_gpu[nz] == exact.astype(np.float32)).sum()),
+            "entries": int(exact.size)}
+
+
+def forced_check(X, codes, scales, pi, cent, bits, group):
+    """One tensor's GPU outputs against the oracle given the GPU's own assignments.
+    X [N][d] fp64; pi [T][N]; cent [T][C][d]."""
+    T = pi.shape[0]
+    out = {"stages": []}
+    R = np.array(X, dtype=np.float64)
+    for t in range(T):
+        out["stages"].append(check_centroids(R, pi[t], cent[t], t + 1))
+        R = oracle.subtract(R, pi[t].astype(np.int32), cent[t])
+    out["codes"] = compare_codes(R, codes, scales, bits, group)
+    return out
+
+
+def check_reconstruction(xhat_gpu, codes, scales, pi, cent, bits, group):
+    """fp32 GPU reconstruction against the oracle's decode of the same compressed data."""
+    T = pi.shape[0]
+    want = oracle.dequantize(codes, scales, pi, cent, bits, group)
+    deq = oracle.decode_codes(codes, scales, bits, group)
+    S = np.abs(deq)
+    for t in range(T):
+        S = S + np.abs(cent[t][pi[t].astype(np.int64)])
+    sq = np.repeat(oracle.e4m3_decode(scales), group, axis=1)
+    tol = np.maximum(1e-3 * sq, (T + 1) * ulp32(S))
+    err = np.abs(np.asarray(xhat_gpu, dtype=np.float64) - want)
+    if not np.all(err <= tol):
+        i, k = np.argwhere(err > tol)[0]
+        raise AssertionError("reconstruction off at token %d channel %d: got %r want %r tol %r"
+                             % (i, k, xhat_gpu[i, k], want[i, k], tol[i, k]))
+    return {"max_err_over_tol": float((err / tol).max())}
+
+
+def check_rounded_output(x16, x32, dtype):
+    """A 16-bit output must be the round-to-nearest-even of the fp32 output."""
+    import torch
+    want = torch.from_numpy(np.asarray(x32, dtype=np.float32)).to(dtype)
+    got = torch.as_tensor(x16).cpu()
+    assert torch.equal(got.view(torch.int16), want.view(torch.int16))
+
+
+def assignment_agreement(pi_gpu, pi_orc, R_stage_inputs, cent_orc):
+    """Per stage: fraction of equal assignments and, for every mismatch, the relative
+    distance gap against the oracle's centroids."""
+    res = []
+    for t in range(pi_gpu.shape[0]):
+        eq = pi_gpu[t] == pi_orc[t]
+        gaps = []
+        R = R_stage_inputs[t]
+        for i in np.flatnonzero(~eq):
+            dg = ((R[i] - cent_orc[t][pi_gpu[t][i]]) ** 2).sum()
+            do = ((R[i] - cent_orc[t][pi_orc[t][i]]) ** 2).sum()
+            gaps.append((dg - do) / max(do, 1e-12 * (R[i] ** 2).sum(), 1e-300))
+        res.append({"agree": float(eq.mean()), "mismatches": int((~eq).sum()),
+                    "max_gap": float(max(gaps)) if gaps else 0.0})
+    return res

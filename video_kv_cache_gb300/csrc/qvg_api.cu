@@ -1,0 +1,319 @@
+// C ABI of libqvg: argument checks, workspace layout and the stage / Lloyd-round loop of
+// the quantize path, plus the dequantize entry point.  Declarations and their contracts
+// are in include/qvg.h.
+#include <cstdint>
+#include <cstring>
+
+#include "internal.cuh"
+#include "qvg.h"
+
+namespace qvg {
+
+cudaError_t launch_init_indices(const QPlan &p, uint64_t seed, int64_t tid_base, cudaStream_t st);
+
+namespace {
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline int cpad_of(int C) { return C <= 16 ? 16 : (C + 15) / 16 * 16; }
+
+struct WsLayout {
+    size_t R32, A, rnorm, B, cn, mu, sums, counts, maxabs, init_idx, stats, rq_count, rq, total;
+};
+
+WsLayout ws_layout(int64_t H, int64_t N, int C, int T) {
+    WsLayout w{};
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        size_t at = off;
+        off = align_up(off + bytes, 256);
+        return at;
+    };
+    w.stats = take(64);
+    if (T > 0) {
+        const int Cpad = cpad_of(C);
+        w.R32 = take(T >= 2 ? (size_t)H * N * kD * 4 : 0);
+        w.A = take((size_t)H * 2 * N * kD * 2);
+        w.rnorm = take((size_t)H * N * 4);
+        w.B = take((size_t)H * 2 * Cpad * kD * 2);
+        w.cn = take((size_t)H * Cpad * 4);
+        w.mu = take((size_t)H * kD * 4);
+        w.sums = take((size_t)H * C * kD * 8);
+        w.counts = take((size_t)H * C * 4);
+        w.maxabs = take((size_t)H * 4);
+        w.init_idx = take((size_t)H * T * C * 4);
+        w.rq_count = take(4);
+        w.rq = take((size_t)H * N * sizeof(RefineReq));
+    }
+    w.total = off;
+    return w;
+}
+
+int elem_bytes(int dt) { return dt == QVG_F32 ? 4 : 2; }
+
+qvg_status check_quant(const qvg_quant_params *p) {
+    if (!p) return QVG_ERR_INVALID_ARG;
+    if (p->n_tensors < 1 || p->N < 1 || p->N >= (int64_t(1) << 31)) return QVG_ERR_INVALID_ARG;
+    if (p->d != kD) return QVG_ERR_UNSUPPORTED;
+    if (p->bits != 2 && p->bits != 4) return QVG_ERR_UNSUPPORTED;
+    if (p->group != 16 && p->group != 32 && p->group != 64) return QVG_ERR_UNSUPPORTED;
+    if (p->T < 0 || p->T > kMaxT) return QVG_ERR_UNSUPPORTED;
+    if (p->in_dtype < QVG_F16 || p->in_dtype > QVG_F32) return QVG_ERR_UNSUPPORTED;
+    if (p->T > 0) {
+        if (p->C < 1 || p->C > kMaxC) return QVG_ERR_UNSUPPORTED;
+        if (p->C > p->N) return QVG_ERR_INVALID_ARG;
+        if (p->iters < 1) return QVG_ERR_INVALID_ARG;
+    }
+    if (p->x_stride < 0 || p->token_offset < 0 || p->token_capacity < 0 || p->warm_stride < 0)
+        return QVG_ERR_INVALID_ARG;
+    if (p->x_stride != 0 && p->x_stride < p->N * kD) return QVG_ERR_INVALID_ARG;
+    if (p->x_stride * elem_bytes(p->in_dtype) % 16 != 0) return QVG_ERR_INVALID_ARG;
+    const int64_t cap = p->token_capacity ? p->token_capacity : p->N;
+    if (p->token_offset + p->N > cap) return QVG_ERR_INVALID_ARG;
+    const int n_tables = p->n_tables ? p->n_tables : 1;
+    if (n_tables < 1 || p->table_index < 0 || p->table_index >= n_tables) return QVG_ERR_INVALID_ARG;
+    if (p->warm_stride != 0 && p->warm_stride < (int64_t)p->T * p->C * kD) return QVG_ERR_INVALID_ARG;
+    if (p->warm_stride % 4 != 0) return QVG_ERR_INVALID_ARG;
+    return QVG_OK;
+}
+
+qvg_status device_info(int *num_sms) {
+    int dev = 0, major = 0, minor = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return QVG_ERR_CUDA;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return QVG_ERR_CUDA;
+    if (major != 10 || minor != 3) return QVG_ERR_DEVICE;
+    return QVG_OK;
+}
+
+#define QVG_CUDA(call)                                \
+    do {                                              \
+        if ((call) != cudaSuccess) {                  \
+            (void)cudaGetLastError();                 \
+            return QVG_ERR_CUDA;                      \
+        }                                             \
+    } while (0)
+
+qvg_status run_quantize(QPlan &p, const qvg_quant_params *prm, int num_sms, cudaStream_t st) {
+    if (p.T > 0) {
+        QVG_CUDA(cudaMemsetAsync(p.sums, 0, (size_t)p.H * p.C * kD * 8, st));
+        QVG_CUDA(cudaMemsetAsync(p.counts, 0, (size_t)p.H * p.C * 4, st));
+        if (!p.warm) QVG_CUDA(launch_init_indices(p, prm->seed, prm->tensor_id_base, st));
+        AssignMaps *maps = nullptr;
+        QVG_CUDA(assign_prepare(p, &maps));
+        qvg_status rc = QVG_OK;
+        for (int t = 1; t <= p.T && rc == QVG_OK; t++) {
+            auto step = [&](cudaError_t e) {
+                if (e != cudaSuccess && rc == QVG_OK) rc = QVG_ERR_CUDA;
+            };
+            step(cudaMemsetAsync(p.maxabs, 0, (size_t)p.H * 4, st));
+            if (t == 1) step(launch_init_centroids(p, t, st));
+            step(launch_centre(p, t, st));
+            step(launch_prep(p, t, st));
+            if (t >= 2) step(launch_init_centroids(p, t, st));
+            step(launch_centroid_planes(p, t, false, true, st));
+            for (int it = 1; it <= p.iters && rc == QVG_OK; it++) {
+                step(cudaMemsetAsync(p.rq_count, 0, 4, st));
+                step(launch_assign(p, maps, t, num_sms, st));
+                step(launch_refine(p, t, num_sms, st));
+                step(launch_update(p, t, num_sms, st));
+                step(launch_centroid_planes(p, t, true, it < p.iters, st));
+            }
+        }
+        assign_release(maps);
+        if (rc != QVG_OK) {
+            (void)cudaGetLastError();
+            return rc;
+        }
+    }
+    QVG_CUDA(launch_encode(p, st));
+    return QVG_OK;
+}
+
+QPlan make_plan(const qvg_quant_params *prm, const void *X, const float *warm,
+                     const qvg_buffers *out, void *workspace, const WsLayout &w,
+                     uint32_t *dev_status) {
+    unsigned char *ws = static_cast<unsigned char *>(workspace);
+    QPlan p{};
+    p.H = prm->n_tensors;
+    p.N = prm->N;
+    p.C = prm->T > 0 ? prm->C : 1;
+    p.Cpad = cpad_of(p.C);
+    p.T = prm->T;
+    p.bits = prm->bits;
+    p.group = prm->group;
+    p.iters = prm->iters;
+    p.in_dtype = prm->in_dtype;
+    p.x_stride = prm->x_stride ? prm->x_stride : prm->N * kD;
+    p.cap = prm->token_capacity ? prm->token_capacity : prm->N;
+    p.tok_off = prm->token_offset;
+    const int n_tables = prm->n_tables ? prm->n_tables : 1;
+    p.cent_tstride = (int64_t)n_tables * p.T * p.C * kD;
+    p.cent_off = (int64_t)prm->table_index * p.T * p.C * kD;
+    p.X = X;
+    p.codes = out->codes;
+    p.scales = out->scales;
+    p.pi = out->pi;
+    p.cent = out->centroids;
+    p.warm = warm;
+    p.warm_stride = prm->warm_stride ? prm->warm_stride : (int64_t)p.T * p.C * kD;
+    p.stats = reinterpret_cast<unsigned *>(ws + w.stats);
+    if (p.T > 0) {
+        p.R32 = p.T >= 2 ? reinterpret_cast<float *>(ws + w.R32) : nullptr;
+        p.A = reinterpret_cast<__nv_bfloat16 *>(ws + w.A);
+        p.rnorm = reinterpret_cast<float *>(ws + w.rnorm);
+        p.B = reinterpret_cast<__nv_bfloat16 *>(ws + w.B);
+        p.cn = reinterpret_cast<float *>(ws + w.cn);
+        p.mu = reinterpret_cast<float *>(ws + w.mu);
+        p.sums = reinterpret_cast<long long *>(ws + w.sums);
+        p.counts = reinterpret_cast<int *>(ws + w.counts);
+        p.maxabs = reinterpret_cast<unsigned *>(ws + w.maxabs);
+        p.init_idx = reinterpret_cast<int *>(ws + w.init_idx);
+        p.rq_count = reinterpret_cast<int *>(ws + w.rq_count);
+        p.rq = reinterpret_cast<RefineReq *>(ws + w.rq);
+    }
+    p.status = dev_status;
+    return p;
+}
+
+}  // namespace
+}  // namespace qvg
+
+using namespace qvg;
+
+extern "C" {
+
+size_t qvg_quantize_workspace_bytes(const qvg_quant_params *params) {
+    if (check_quant(params) != QVG_OK) return 0;
+    return ws_layout(params->n_tensors, params->N, params->C, params->T).total;
+}
+
+qvg_status qvg_quantize(const qvg_quant_params *prm, const void *X, const float *warm,
+                        const qvg_buffers *out, void *workspace, size_t workspace_bytes,
+                        uint32_t *dev_status, void *stream) {
+    qvg_status rc = check_quant(prm);
+    if (rc != QVG_OK) return rc;
+    if (!X || !out || !out->codes || !out->scales) return QVG_ERR_INVALID_ARG;
+    if (prm->T > 0 && (!out->pi || !out->centroids)) return QVG_ERR_INVALID_ARG;
+    if (!aligned16(X) || !aligned16(out->codes) || !aligned16(out->scales) ||
+        (prm->T > 0 && !aligned16(out->centroids)) || (warm && !aligned16(warm)))
+        return QVG_ERR_INVALID_ARG;
+    const WsLayout w = ws_layout(prm->n_tensors, prm->N, prm->C, prm->T);
+    if (!workspace || workspace_bytes < w.total) return QVG_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return QVG_ERR_INVALID_ARG;
+    int num_sms = 0;
+    rc = device_info(&num_sms);
+    if (rc != QVG_OK) return rc;
+
+    QPlan p = make_plan(prm, X, warm, out, workspace, w, dev_status);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(p.stats, 0, 64, st) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return QVG_ERR_CUDA;
+    }
+    return run_quantize(p, prm, num_sms, st);
+}
+
+qvg_status qvg_reassign(const qvg_quant_params *prm, const void *X, const qvg_buffers *out,
+                        void *workspace, size_t workspace_bytes, uint32_t *dev_status,
+                        void *stream) {
+    qvg_status rc = check_quant(prm);
+    if (rc != QVG_OK) return rc;
+    if (prm->T < 1) return QVG_ERR_INVALID_ARG;
+    if (!X || !out || !out->pi || !out->centroids) return QVG_ERR_INVALID_ARG;
+    if (!aligned16(X) || !aligned16(out->centroids)) return QVG_ERR_INVALID_ARG;
+    const WsLayout w = ws_layout(prm->n_tensors, prm->N, prm->C, prm->T);
+    if (!workspace || workspace_bytes < w.total) return QVG_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return QVG_ERR_INVALID_ARG;
+    int num_sms = 0;
+    rc = device_info(&num_sms);
+    if (rc != QVG_OK) return rc;
+    QPlan p = make_plan(prm, X, nullptr, out, workspace, w, dev_status);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    AssignMaps *maps = nullptr;
+    if (assign_prepare(p, &maps) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return QVG_ERR_CUDA;
+    }
+    cudaError_t e = launch_centroid_planes(p, p.T, false, true, st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(p.rq_count, 0, 4, st);
+    if (e == cudaSuccess) e = launch_assign(p, maps, p.T, num_sms, st);
+    if (e == cudaSuccess) e = launch_refine(p, p.T, num_sms, st);
+    assign_release(maps);
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        return QVG_ERR_CUDA;
+    }
+    return QVG_OK;
+}
+
+
+
+qvg_status qvg_dequantize(const qvg_dequant_params *prm, const qvg_buffers *in, void *X_hat,
+                          uint32_t *dev_status, void *stream) {
+    if (!prm || !in || !X_hat || !in->codes || !in->scales) return QVG_ERR_INVALID_ARG;
+    if (prm->n_tensors < 1 || prm->N < 1 || prm->N >= (int64_t(1) << 31)) return QVG_ERR_INVALID_ARG;
+    if (prm->d != kD) return QVG_ERR_UNSUPPORTED;
+    if (prm->bits != 2 && prm->bits != 4) return QVG_ERR_UNSUPPORTED;
+    if (prm->group != 16 && prm->group != 32 && prm->group != 64) return QVG_ERR_UNSUPPORTED;
+    if (prm->T < 0 || prm->T > kMaxT) return QVG_ERR_UNSUPPORTED;
+    if (prm->out_dtype < QVG_F16 || prm->out_dtype > QVG_F32) return QVG_ERR_UNSUPPORTED;
+    if (prm->T > 0 && (prm->C < 1 || prm->C > kMaxC)) return QVG_ERR_UNSUPPORTED;
+    if (prm->T > 0 && (!in->pi || !in->centroids)) return QVG_ERR_INVALID_ARG;
+    if (prm->chunk_len < 0 || prm->token_capacity < 0 || prm->n_tables < 0 || prm->out_stride < 0)
+        return QVG_ERR_INVALID_ARG;
+    const int64_t cap = prm->token_capacity ? prm->token_capacity : prm->N;
+    const int64_t chunk = prm->chunk_len ? prm->chunk_len : prm->N;
+    const int n_tables = prm->n_tables ? prm->n_tables : 1;
+    const int64_t ostride = prm->out_stride ? prm->out_stride : prm->N * kD;
+    if (cap < prm->N || ostride < prm->N * kD) return QVG_ERR_INVALID_ARG;
+    if (prm->T > 0 && (prm->N + chunk - 1) / chunk > n_tables) return QVG_ERR_INVALID_ARG;
+    if (ostride * elem_bytes(prm->out_dtype) % 16 != 0) return QVG_ERR_INVALID_ARG;
+    if (!aligned16(X_hat) || !aligned16(in->codes) || !aligned16(in->scales) ||
+        (prm->T > 0 && !aligned16(in->centroids)))
+        return QVG_ERR_INVALID_ARG;
+    int num_sms = 0;
+    qvg_status rc = device_info(&num_sms);
+    if (rc != QVG_OK) return rc;
+    DPlan p{};
+    p.H = prm->n_tensors;
+    p.N = prm->N;
+    p.C = prm->T > 0 ? prm->C : 1;
+    p.T = prm->T;
+    p.bits = prm->bits;
+    p.group = prm->group;
+    p.out_dtype = prm->out_dtype;
+    p.chunk_len = chunk;
+    p.cap = cap;
+    p.n_tables = n_tables;
+    p.out_stride = ostride;
+    p.codes = in->codes;
+    p.scales = in->scales;
+    p.pi = in->pi;
+    p.cent = in->centroids;
+    p.out = X_hat;
+    p.status = dev_status;
+    if (launch_dequant(p, num_sms, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return QVG_ERR_CUDA;
+    }
+    return QVG_OK;
+}
+
+const char *qvg_status_string(qvg_status s) {
+    switch (s) {
+        case QVG_OK: return "ok";
+        case QVG_ERR_INVALID_ARG: return "invalid argument (null, misaligned or inconsistent size)";
+        case QVG_ERR_UNSUPPORTED: return "unsupported shape or parameter value";
+        case QVG_ERR_WORKSPACE: return "workspace missing or too small";
+        case QVG_ERR_CUDA: return "CUDA error while enqueuing work";
+        case QVG_ERR_DEVICE: return "current device is not an sm_103 GPU";
+    }
+    return "unknown status";
+}
+
+uint32_t qvg_version(void) { return (1u << 16) | 0u; }
+
+}  // extern "C"

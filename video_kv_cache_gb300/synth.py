@@ -76,9 +76,9 @@ def _noise(seed: int, tid: int, gtok: torch.Tensor) -> torch.Tensor:
     base = (int(seed) * 0x9E3779B1 + int(tid) * 0x85EBCA77) & ((1 << 62) - 1)
     h1 = _mix(key + base)
     h2 = _mix(key + 1 + base)
-    u1 = (((h1 >> 8) & _MASK24).to(torch.float64) + 0.5) / float(1 << 24)
-    u2 = ((h2 >> 8) & _MASK24).to(torch.float64) / float(1 << 24)
-    return (torch.sqrt(-2.0 * torch.log(u1)) * torch.cos(2.0 * math.pi * u2)).to(torch.float32)
+    u1 = (((h1 >> 8) & _MASK24).to(torch.float32) + 0.5) / float(1 << 24)
+    u2 = ((h2 >> 8) & _MASK24).to(torch.float32) / float(1 << 24)
+    return torch.sqrt(-2.0 * torch.log(u1)) * torch.cos(2.0 * math.pi * u2)
 
 
 def kv_tensor(seed: int, tids: Sequence[int], f0: int, nf: int, gh: int, gw: int,
