@@ -51,8 +51,15 @@ struct QPlan {
     __nv_bfloat16 *B;      // [H][2][Cpad][128] bf16 hi / lo planes of the centred centroids
     float *cn;             // [H][Cpad] squared norm of the centred centroids
     float *mu;             // [H][128] centring vector of the current stage
-    long long *sums;       // [H][C][128] fixed-point centroid sums
-    int *counts;           // [H][C]
+    int *counts;           // [H][C] cluster sizes of the current assignment
+    int *offs;             // [H][C] first position of each cluster in `ids`
+    int *blockoff;         // [H][nsb][C] per token block: its first position per cluster
+    int *ids;              // [H][N] token indices grouped by cluster, increasing in a cluster
+    uint8_t *cid;          // [H][N] cluster of each sorted position
+    float *psum;           // [H][nchunk][2][2][128] (sum, error) of the runs that cross a
+                           // chunk boundary: [0] the run at the chunk start, [1] the last run
+    float *wsum;           // [H][C][2][128] (sum, error) of clusters inside one chunk
+    int nsb, nchunk;       // token blocks of the sort, 64-position chunks per tensor
     unsigned *maxabs;      // [H] max |r| of the current stage, as float bits
     int *init_idx;         // [H][T][C] cold-start rows
     unsigned *stats;       // [16] counters (see kStat*)
@@ -133,6 +140,27 @@ __device__ __forceinline__ int fixed_q(unsigned maxabs_bits, int64_t N) {
 
 __device__ __forceinline__ float pow2f(int q) { return __int_as_float((q + 127) << 23); }
 
+// x * 2^q rounded to nearest (ties to even) as a 64-bit integer, for |x * 2^q| < 2^62.
+// Integer-only: a float -> int64 conversion instruction would run on the FP64 pipe, which
+// is narrow on this GPU.
+__device__ __forceinline__ long long f2fix(float x, int q) {
+    const uint32_t b = __float_as_uint(x);
+    const int e = (int)((b >> 23) & 0xFFu);
+    const uint32_t m = (b & 0x7FFFFFu) | (e ? 0x800000u : 0u);
+    const int sh = (e ? e : 1) - 150 + q;  // |x| = m * 2^(e - 150) for normals
+    unsigned long long v;
+    if (sh >= 0) {
+        v = (unsigned long long)m << (sh < 63 ? sh : 63);
+    } else {
+        const int s = -sh < 31 ? -sh : 31;
+        const uint32_t kept = m >> s;
+        const uint32_t rem = m - (kept << s);
+        const uint32_t half = 1u << (s - 1);
+        v = kept + ((rem > half) || (rem == half && (kept & 1u)) ? 1u : 0u);
+    }
+    return (b >> 31) ? -(long long)v : (long long)v;
+}
+
 __device__ __forceinline__ void or_status(uint32_t *status, uint32_t bits) {
     if (status) atomicOr(status, bits);
 }
@@ -144,9 +172,10 @@ __device__ __forceinline__ void or_status(uint32_t *status, uint32_t bits) {
 cudaError_t launch_init_centroids(const QPlan &p, int t, cudaStream_t st);
 cudaError_t launch_centre(const QPlan &p, int t, cudaStream_t st);
 cudaError_t launch_prep(const QPlan &p, int t, cudaStream_t st);
-cudaError_t launch_centroid_planes(const QPlan &p, int t, bool from_sums, bool planes,
-                                   cudaStream_t st);
-cudaError_t launch_update(const QPlan &p, int t, int num_sms, cudaStream_t st);
+cudaError_t launch_centroid_planes(const QPlan &p, int t, cudaStream_t st);
+cudaError_t launch_cluster_means(const QPlan &p, int t, bool planes, cudaStream_t st);
+constexpr int kSortBlock = 256;  // tokens per block of the counting sort
+constexpr int kChunk = 64;       // sorted positions summed by one warp
 cudaError_t launch_encode(const QPlan &p, cudaStream_t st);
 
 struct AssignMaps;  // opaque: tensor maps for the assignment GEMM

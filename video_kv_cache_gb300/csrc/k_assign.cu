@@ -16,8 +16,8 @@
 //
 // Kernel structure (one persistent CTA per SM, 192 threads):
 //   warp 0   TMA producer: B (centroid planes, C x 128 x 2 planes) once per tensor, A
-//            (residual planes, 128 tokens x 128 x bf16, one 32 KB slot per plane) into a
-//            ring of smem slots.
+//            (residual planes of 128 tokens, four 16 KB blocks of 64 channels per tile)
+//            into a ring of smem slots.
 //   warp 1   TMEM allocator and MMA issuer (one thread): 3 x 8 tcgen05.mma of
 //            M=128, N=Cpad, K=16 per tile into one of two TMEM accumulators.
 //   warps 2-5 epilogue: warp w reads TMEM lanes 32*(w%4).. (one token row per thread),
@@ -39,10 +39,9 @@ struct AssignMaps {
 
 namespace {
 
-constexpr int kEpiWarps = 8;
-constexpr int kThreads = 64 + kEpiWarps * 32;  // producer, MMA, 8 epilogue warps
+constexpr int kEpiGroups = 2;                      // epilogue groups of 8 warps
+constexpr int kThreads = 64 + kEpiGroups * 8 * 32;  // producer, MMA, 16 epilogue warps
 constexpr int kTileM = 128;
-constexpr uint32_t kPlaneBytes = kTileM * kD * 2;  // 32 KB: one plane of a 128-token tile
 constexpr uint32_t kKBlockBytes = kTileM * 64 * 2;  // 16 KB: 64 channels of that plane
 constexpr uint32_t kSpinLimit = 1u << 22;
 
@@ -120,21 +119,6 @@ __device__ __forceinline__ void tc_mma(uint32_t d, uint64_t a, uint64_t b, uint3
         : "memory");
 }
 
-// Barrier over the epilogue warps that also ORs a flag across them, so that every
-// epilogue warp takes the same branch after a bounded wait.
-__device__ __forceinline__ bool epi_any(bool x, int nthreads) {
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\t"
-        "setp.ne.u32 p, %1, 0;\n\t"
-        "bar.red.or.pred q, 1, %2, p;\n\t"
-        "selp.u32 %0, 1, 0, q;\n\t}\n"
-        : "=r"(r)
-        : "r"((uint32_t)x), "r"(nthreads)
-        : "memory");
-    return r != 0u;
-}
-
 // 32 consecutive fp32 columns of this thread's TMEM lane.
 __device__ __forceinline__ void tc_ld32(uint32_t taddr, float v[32]) {
     uint32_t r[32];
@@ -184,16 +168,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t bsub = (uint32_t)Cpad * 128u;  // one (plane, 64-channel block) of B
     unsigned char *sB = sm;
     unsigned char *sA = sm + 4 * bsub;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sA + (size_t)nslots * kPlaneBytes);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sA + (size_t)nslots * kKBlockBytes);
     uint64_t *a_full = bars, *a_empty = bars + nslots;
     uint64_t *b_full = bars + 2 * nslots, *b_empty = b_full + 1;
-    uint64_t *acc_full = b_full + 2, *acc_empty = b_full + 4, *fin = b_full + 6;
+    uint64_t *acc_full = b_full + 2, *acc_empty = acc_full + kEpiGroups, *fin = acc_empty + kEpiGroups;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(fin + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
-    // per-row (best, second, index) of the upper half of the columns, for the merge
-    float *x_best = reinterpret_cast<float *>(tmem_slot + 4);
-    float *x_second = x_best + kTileM;
-    int *x_idx = reinterpret_cast<int *>(x_second + kTileM);
+    // per epilogue group: ||c||^2 of its current tensor and the column-half exchange
+    // 16-byte aligned: the epilogue reads it with 16-byte vector loads
+    float *cn_s = reinterpret_cast<float *>(
+        (reinterpret_cast<uintptr_t>(tmem_slot + 4) + 15) & ~static_cast<uintptr_t>(15));  // [kEpiGroups][Cpad]
+    float *x_best = cn_s + kEpiGroups * Cpad;                     // [kEpiGroups][128]
+    float *x_second = x_best + kEpiGroups * kTileM;
+    int *x_idx = reinterpret_cast<int *>(x_second + kEpiGroups * kTileM);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t total = (int64_t)p.H * tiles_per_tensor;
@@ -208,9 +195,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_init(smem_u32(b_full), 1);
         mbar_init(smem_u32(b_empty), 1);
-        for (int b = 0; b < 2; b++) {
-            mbar_init(smem_u32(acc_full + b), 1);
-            mbar_init(smem_u32(acc_empty + b), kEpiWarps);
+        for (int g = 0; g < kEpiGroups; g++) {
+            mbar_init(smem_u32(acc_full + g), 1);
+            mbar_init(smem_u32(acc_empty + g), 8);
         }
         mbar_init(smem_u32(fin), 1);
         *abort_flag = 0;
@@ -247,17 +234,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                     nb++;
                     cur_h = h;
                 }
+                // four 16 KB loads per tile: hi plane channels 0-63, 64-127, then lo plane
                 bool ok = true;
-                for (int pl = 0; pl < 2 && ok; pl++) {
-                    const uint32_t q = 2u * (uint32_t)lt + pl, s = q % nslots, ph = (q / nslots) & 1u;
+                for (int k = 0; k < 4; k++) {
+                    const uint32_t q = 4u * (uint32_t)lt + k, s = q % nslots, ph = (q / nslots) & 1u;
                     if (!mbar_wait(smem_u32(a_empty + s), ph ^ 1u, abort_flag)) {
                         ok = false;
                         break;
                     }
-                    mbar_expect_tx(smem_u32(a_full + s), kPlaneBytes);
-                    for (int kb = 0; kb < 2; kb++)
-                        tma_load_3d(smem_u32(sA + s * kPlaneBytes + kb * kKBlockBytes), &tmA,
-                                    kb * 64, m0, 2 * h + pl, smem_u32(a_full + s));
+                    mbar_expect_tx(smem_u32(a_full + s), kKBlockBytes);
+                    tma_load_3d(smem_u32(sA + s * kKBlockBytes), &tmA, (k & 1) * 64, m0,
+                                2 * h + (k >> 1), smem_u32(a_full + s));
                     issued = q + 1;
                 }
                 if (!ok) break;
@@ -283,33 +270,34 @@ __global__ void __launch_bounds__(kThreads, 1)
                     nb++;
                     cur_h = h;
                 }
-                const uint32_t buf = (uint32_t)lt & 1u, use = (uint32_t)lt >> 1;
-                if (!mbar_wait(smem_u32(acc_empty + buf), (use & 1u) ^ 1u, abort_flag)) break;
+                // tile lt goes to accumulator and epilogue group lt % 2, free once the
+                // group released its previous tile
+                const uint32_t buf = (uint32_t)lt & 1u, grp = buf, use = (uint32_t)lt >> 1;
+                if (!mbar_wait(smem_u32(acc_empty + grp), (use & 1u) ^ 1u, abort_flag)) break;
                 tc_fence_after();
                 const uint32_t d = tmem + buf * acc_stride;
-                // A hi plane against B hi and B lo
-                const uint32_t qh = 2u * (uint32_t)lt, sh = qh % nslots;
-                if (!mbar_wait(smem_u32(a_full + sh), (qh / nslots) & 1u, abort_flag)) break;
-                tc_fence_after();
-                const uint64_t dAh = sw128_desc(smem_u32(sA + sh * kPlaneBytes));
-                for (int bp = 0; bp < 2; bp++)
-                    for (int kb = 0; kb < 2; kb++)
+                // k = 0, 1: hi plane blocks against B hi and B lo; k = 2, 3: lo plane against
+                // B hi.  Each A block's slot is released as soon as its MMAs complete.
+                bool ok = true;
+                for (int k = 0; k < 4 && ok; k++) {
+                    const uint32_t q = 4u * (uint32_t)lt + k, s = q % nslots;
+                    if (!mbar_wait(smem_u32(a_full + s), (q / nslots) & 1u, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t dA = sw128_desc(smem_u32(sA + s * kKBlockBytes));
+                    const int kb = k & 1;
+                    const int nbp = k < 2 ? 2 : 1;
+                    for (int bp = 0; bp < nbp; bp++)
                         for (int kk = 0; kk < 4; kk++)
-                            tc_mma(d, dAh + (uint64_t)((kb * kKBlockBytes + kk * 32) >> 4),
+                            tc_mma(d, dA + (uint64_t)((kk * 32) >> 4),
                                    dB0 + (uint64_t)(((bp * 2 + kb) * bsub + kk * 32) >> 4), idesc,
-                                   (bp | kb | kk) != 0);
-                tc_commit(smem_u32(a_empty + sh));
-                // A lo plane against B hi
-                const uint32_t ql = qh + 1u, sl = ql % nslots;
-                if (!mbar_wait(smem_u32(a_full + sl), (ql / nslots) & 1u, abort_flag)) break;
-                tc_fence_after();
-                const uint64_t dAl = sw128_desc(smem_u32(sA + sl * kPlaneBytes));
-                for (int kb = 0; kb < 2; kb++)
-                    for (int kk = 0; kk < 4; kk++)
-                        tc_mma(d, dAl + (uint64_t)((kb * kKBlockBytes + kk * 32) >> 4),
-                               dB0 + (uint64_t)((kb * bsub + kk * 32) >> 4), idesc, 1u);
-                tc_commit(smem_u32(a_empty + sl));
-                tc_commit(smem_u32(acc_full + buf));
+                                   (k | bp | kk) != 0);
+                    tc_commit(smem_u32(a_empty + s));
+                }
+                if (!ok) break;
+                tc_commit(smem_u32(acc_full + grp));
             }
             // every MMA issued so far completes before TMEM is released
             tc_commit(smem_u32(fin));
@@ -317,36 +305,55 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ------------------------------------------------------------ epilogue
-        // 8 warps: warp w reads TMEM lanes 32*(w%4).. (its rows) and one half of the
-        // 32-column chunks; the lower half merges and writes the result.
-        const int quarter = warp & 3;
-        const int half = (warp - 2) >> 2;
+        // Two groups of 8 warps take turns: group g handles the tiles with lt % 2 == g, found
+        // in TMEM accumulator g.  Warp w reads TMEM lanes 32*(w%4).. (its 32 rows); the two
+        // warps of a group with the same lanes split the columns, and the lower-column warp
+        // merges the pair's results through shared memory.
+        const int e = warp - 2;
+        const int grp = e >> 3, half = (e >> 2) & 1, quarter = warp & 3;
         const int row = quarter * 32 + lane;
         const int C = p.C;
         const int nchunks = (Cpad + 31) >> 5;
         const int split = (nchunks + 1) >> 1;
         const int ch_lo = half ? split : 0, ch_hi = half ? nchunks : split;
+        const int pair_bar = 1 + grp * 4 + quarter;  // named barrier of the two warps of a row block
+        const int grp_bar = 9 + grp;                  // named barrier of the group's 8 warps
+        float *cns = cn_s + grp * Cpad;
+        float *xb = x_best + grp * kTileM, *xs = x_second + grp * kTileM;
+        int *xi = x_idx + grp * kTileM;
         int cur_h = -1;
         float cmax = 0.f, cmax2 = 0.f;
         unsigned n_ref_rows = 0;
-        for (int64_t tile = tb, lt = 0; tile < te; tile++, lt++) {
+        for (int64_t tile = tb + grp, lt = grp; tile < te; tile += kEpiGroups, lt += kEpiGroups) {
             const int h = (int)(tile / tiles_per_tensor);
             const int64_t i = (tile - (int64_t)h * tiles_per_tensor) * kTileM + row;
             const bool valid = i < p.N;
-            const float *cn = p.cn + (int64_t)h * Cpad;
+            const uint32_t buf = (uint32_t)grp, use = (uint32_t)lt >> 1;
+            const float rn = (half == 0 && valid) ? __ldg(p.rnorm + (int64_t)h * p.N + i) : 0.f;
+            const bool ok = mbar_wait(smem_u32(acc_full + grp), use & 1u, abort_flag);
+            // every warp of the group takes the same branch after the bounded wait; this is
+            // also the group barrier that ends the previous tile's reads of ||c||^2
+            uint32_t any_fail;
+            asm volatile(
+                "{\n\t.reg .pred p, q;\n\tsetp.eq.u32 p, %1, 0;\n\t"
+                "bar.red.or.pred q, %2, 256, p;\n\tselp.u32 %0, 1, 0, q;\n\t}\n"
+                : "=r"(any_fail)
+                : "r"((uint32_t)(ok ? 1 : 0)), "r"(grp_bar)
+                : "memory");
+            if (any_fail) break;
             if (h != cur_h) {
+                // the group's private copy of ||c||^2 for this tensor
                 cur_h = h;
+                const float *cn = p.cn + (int64_t)h * Cpad;
+                for (int j = e * 32 + lane - grp * 256; j < Cpad; j += 256) cns[j] = __ldg(cn + j);
+                asm volatile("bar.sync %0, 256;" ::"r"(grp_bar) : "memory");
                 cmax2 = 0.f;
-                for (int j = lane; j < C; j += 32) cmax2 = fmaxf(cmax2, __ldg(cn + j));
+                for (int j = lane; j < C; j += 32) cmax2 = fmaxf(cmax2, cns[j]);
 #pragma unroll
                 for (int o = 16; o >= 1; o >>= 1)
                     cmax2 = fmaxf(cmax2, __shfl_xor_sync(0xffffffffu, cmax2, o));
                 cmax = sqrtf(cmax2);
             }
-            const uint32_t buf = (uint32_t)lt & 1u, use = (uint32_t)lt >> 1;
-            const float rn = (half == 0 && valid) ? __ldg(p.rnorm + (int64_t)h * p.N + i) : 0.f;
-            const bool ok = mbar_wait(smem_u32(acc_full + buf), use & 1u, abort_flag);
-            if (epi_any(!ok, kEpiWarps * 32)) break;  // all epilogue warps leave together
             tc_fence_after();
             const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + buf * acc_stride;
             float best = INFINITY, second = INFINITY;
@@ -357,7 +364,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_ld32(taddr + cb * 32, v);
 #pragma unroll
                 for (int q = 0; q < 32; q += 4) {
-                    const float4 c4 = __ldg(reinterpret_cast<const float4 *>(cn + cb * 32 + q));
+                    const float4 c4 = *reinterpret_cast<const float4 *>(cns + cb * 32 + q);
                     const float cc[4] = {c4.x, c4.y, c4.z, c4.w};
 #pragma unroll
                     for (int u = 0; u < 4; u++) {
@@ -370,25 +377,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             if (half == 1) {
-                x_best[row] = best;
-                x_second[row] = second;
-                x_idx[row] = bj;
+                xb[row] = best;
+                xs[row] = second;
+                xi[row] = bj;
             }
-            asm volatile("bar.sync 1, %0;" ::"r"(kEpiWarps * 32) : "memory");
-            bool need = false;
-            float lim = 0.f;
+            asm volatile("bar.sync %0, 64;" ::"r"(pair_bar) : "memory");
             if (half == 0) {
-                const float ob = x_best[row], os = x_second[row];
-                const int oj = x_idx[row];
+                const float ob = xb[row], os = xs[row];
+                const int oj = xi[row];
                 second = fminf(fminf(second, os), fmaxf(best, ob));
-                if (ob < best) bj = oj;  // lower half wins ties: lowest cluster index
+                if (ob < best) bj = oj;  // the lower half wins ties: lowest cluster index
                 best = fminf(best, ob);
-                // |error of a score| <= 2^-12 ||r|| ||c_j|| + 2^-17 ||c_j||^2; two scores
-                // differ from their exact values by at most twice that.
-                const float margin = 2.f * (ldexpf(rn * cmax, -12) + ldexpf(cmax2, -17)) + 1e-30f;
-                lim = best + margin;
-                need = valid && second <= lim;
             }
+            // |error of a score| <= 2^-12 ||r|| ||c_j|| + 2^-17 ||c_j||^2; two scores differ
+            // from their exact values by at most twice that.
+            const float margin = 2.f * (ldexpf(rn * cmax, -12) + ldexpf(cmax2, -17)) + 1e-30f;
+            const float lim = best + margin;
+            const bool need = half == 0 && valid && second <= lim;
             uint32_t cand[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
             if (half == 0 && __any_sync(0xffffffffu, need)) {
 #pragma unroll
@@ -399,7 +404,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int q = 0; q < 32; q++) {
                             const int j = cb * 32 + q;
-                            const float s = __fmaf_rn(-2.f, v[q], __ldg(cn + j));
+                            const float s = __fmaf_rn(-2.f, v[q], cns[j]);
                             if (need && j < C && s <= lim) cand[cb] |= 1u << q;
                         }
                     }
@@ -407,9 +412,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(acc_empty + buf));
-            // the next tile's exchange must not overwrite this one before it is read
-            asm volatile("bar.sync 1, %0;" ::"r"(kEpiWarps * 32) : "memory");
+            if (lane == 0) mbar_arrive(smem_u32(acc_empty + grp));
             if (half == 0 && valid) {
                 p.pi[(int64_t)(h * p.T + t - 1) * p.cap + p.tok_off + i] = (uint8_t)bj;
                 if (need) {
@@ -520,23 +523,25 @@ static EncodeTiledFn encode_fn() {
 
 static const int kMaxSmem = 232448;  // opt-in shared memory per block on sm_100-class GPUs
 
-// barriers, TMEM slot, abort flag and the epilogue's per-row exchange
-static size_t assign_tail_bytes(int nslots) {
-    return (size_t)(2 * nslots + 7) * 8 + 16 + 3 * kTileM * 4;
+// barriers, TMEM slot, abort flag, and per epilogue group ||c||^2 and the column-half
+// exchange (best, second, index per row)
+static size_t assign_tail_bytes(int nslots, int Cpad) {
+    return (size_t)(2 * nslots + 3 + 2 * kEpiGroups) * 8 + 16 + 16 /* alignment */ +
+           (size_t)kEpiGroups * (Cpad + 3 * kTileM) * 4;
 }
 
 static int assign_slots(int Cpad) {
-    for (int n = 8; n >= 2; n--)
-        if ((size_t)1024 + 4 * (size_t)Cpad * 128 + (size_t)n * kPlaneBytes + assign_tail_bytes(n) <=
-            (size_t)kMaxSmem)
+    for (int n = 12; n >= 4; n--)
+        if ((size_t)1024 + 4 * (size_t)Cpad * 128 + (size_t)n * kKBlockBytes +
+                assign_tail_bytes(n, Cpad) <= (size_t)kMaxSmem)
             return n;
-    return 2;
+    return 4;
 }
 
 size_t assign_smem_bytes(int Cpad) {
     const int nslots = assign_slots(Cpad);
-    return (size_t)1024 + 4 * (size_t)Cpad * 128 + (size_t)nslots * kPlaneBytes +
-           assign_tail_bytes(nslots);
+    return (size_t)1024 + 4 * (size_t)Cpad * 128 + (size_t)nslots * kKBlockBytes +
+           assign_tail_bytes(nslots, Cpad);
 }
 
 cudaError_t assign_prepare(const QPlan &p, AssignMaps **out) {

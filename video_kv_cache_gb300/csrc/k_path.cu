@@ -230,203 +230,340 @@ cudaError_t launch_prep(const QPlan &p, int t, cudaStream_t st) {
 }
 
 // --------------------------------------------------------------------------------------
-// Centroid finalisation and GEMM planes.   grid (C, H), block 128.
-//   from_sums: C_j = fp32(exact fixed-point sum / count) for non-empty clusters (empty ones
-//              keep their value); the sums and counts are cleared for the next round.
-//   planes:    bf16 hi / lo split of C_j - mu and ||C_j - mu||^2 for the next assignment.
+// GEMM planes of the stage's initial centroids: bf16 hi / lo split of C_j - mu and
+// ||C_j - mu||^2.   grid (C, H), block 128.
 // --------------------------------------------------------------------------------------
-__global__ void k_centroid_planes(QPlan p, int t, int from_sums, int planes) {
+__global__ void k_centroid_planes(QPlan p, int t) {
     const int j = blockIdx.x, h = blockIdx.y, k = threadIdx.x;
-    float *c = p.cent + h * p.cent_tstride + p.cent_off + (int64_t)(t - 1) * p.C * kD +
-               (int64_t)j * kD;
-    float v = c[k];
-    __shared__ double inv_s;
-    __shared__ int cnt_s;
+    const float v = p.cent[h * p.cent_tstride + p.cent_off + (int64_t)(t - 1) * p.C * kD +
+                           (int64_t)j * kD + k];
     __shared__ float red[4];
-    if (from_sums) {
-        if (k == 0) {
-            const int cnt = p.counts[h * p.C + j];
-            cnt_s = cnt;
-            if (cnt > 0) inv_s = ldexp(1.0, -fixed_q(p.maxabs[h], p.N)) / (double)cnt;
-            p.counts[h * p.C + j] = 0;
-        }
-        __syncthreads();
-        long long *sp = p.sums + ((int64_t)h * p.C + j) * kD + k;
-        if (cnt_s > 0) {
-            v = (float)((double)(*sp) * inv_s);
-            c[k] = v;
-        }
-        *sp = 0;
-    }
-    if (planes) {
-        const float ct = __fsub_rn(v, p.mu[h * kD + k]);
-        const __nv_bfloat16 hi = __float2bfloat16_rn(ct);
-        const __nv_bfloat16 lo = __float2bfloat16_rn(__fsub_rn(ct, __bfloat162float(hi)));
-        p.B[((int64_t)(h * 2 + 0) * p.Cpad + j) * kD + k] = hi;
-        p.B[((int64_t)(h * 2 + 1) * p.Cpad + j) * kD + k] = lo;
-        float ss = ct * ct;
+    const float ct = __fsub_rn(v, p.mu[h * kD + k]);
+    const __nv_bfloat16 hi = __float2bfloat16_rn(ct);
+    const __nv_bfloat16 lo = __float2bfloat16_rn(__fsub_rn(ct, __bfloat162float(hi)));
+    p.B[((int64_t)(h * 2 + 0) * p.Cpad + j) * kD + k] = hi;
+    p.B[((int64_t)(h * 2 + 1) * p.Cpad + j) * kD + k] = lo;
+    float ss = ct * ct;
 #pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-        if ((k & 31) == 0) red[k >> 5] = ss;
-        __syncthreads();
-        if (k == 0) p.cn[(int64_t)h * p.Cpad + j] = (red[0] + red[1]) + (red[2] + red[3]);
-    }
+    for (int o = 16; o >= 1; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if ((k & 31) == 0) red[k >> 5] = ss;
+    __syncthreads();
+    if (k == 0) p.cn[(int64_t)h * p.Cpad + j] = (red[0] + red[1]) + (red[2] + red[3]);
 }
 
-cudaError_t launch_centroid_planes(const QPlan &p, int t, bool from_sums, bool planes,
-                                   cudaStream_t st) {
-    k_centroid_planes<<<dim3(p.C, p.H), kD, 0, st>>>(p, t, from_sums ? 1 : 0, planes ? 1 : 0);
+__global__ void k_pad_cn(QPlan p) {
+    // padded GEMM columns (C <= j < Cpad) never win the argmin
+    const int h = blockIdx.x;
+    for (int j = p.C + threadIdx.x; j < p.Cpad; j += blockDim.x) p.cn[(int64_t)h * p.Cpad + j] = INFINITY;
+}
+
+cudaError_t launch_centroid_planes(const QPlan &p, int t, cudaStream_t st) {
+    if (p.Cpad > p.C) k_pad_cn<<<p.H, 32, 0, st>>>(p);
+    k_centroid_planes<<<dim3(p.C, p.H), kD, 0, st>>>(p, t);
     return cudaGetLastError();
 }
 
 // --------------------------------------------------------------------------------------
-// Centroid sums.  Each CTA owns a token range of one tensor and a slab of CH = 32*CPL
-// channels, keeps int64 fixed-point bins [C][CH] in shared memory, and adds them to the
-// global bins once at the end.  A warp walks its tokens in order with lane l holding
-// channels l*CPL..; consecutive tokens of a run with the same cluster (frequent: the
-// grouping follows the video's spatial layout) are summed in registers and flushed to the
-// shared bins only when the cluster changes.  Integer adds make every order give the
-// same bits.
-//   SRC: 0 = X as 16-bit (fp16 / bf16), 1 = X as fp32, 2 = R32 (stages t >= 2)
-// grid (units per tensor, channel slabs, H), block 512.
+// Centroid update: C_j = mean of the residual rows assigned to j, for every non-empty j.
+//
+// 1. A stable counting sort groups the token indices by cluster, increasing within a
+//    cluster (histogram per block of 256 tokens, scans, scatter with in-block ranks).
+// 2. The sorted positions are cut into chunks of 64; one warp adds each run of equal
+//    cluster inside its chunk with error-free TwoSum accumulation (sum + running error,
+//    both fp32) in sorted order (lane l holds channels 4l..4l+3, 16 rows in flight).
+// 3. One warp per cluster adds its pieces (one, or one per chunk it spans) in chunk
+//    order, forms the mean, and writes the centroid with the bf16 hi / lo planes of
+//    C_j - mu and ||C_j - mu||^2 for the next assignment; empty clusters keep their
+//    centroid.
+// Every reduction has a fixed order, so repeated runs give identical bits; the
+// compensated sums carry about twice fp32's precision.
 // --------------------------------------------------------------------------------------
-constexpr int kUpdThreads = 512;
-constexpr int kUpdBatch = 16;  // tokens whose loads are in flight per warp
+__device__ __forceinline__ void acc_two_sum(float &s, float &e, float x) {
+    float err;
+    two_sum(s, x, s, err);
+    e = __fadd_rn(e, err);
+}
 
-template <int CPL, int SRC>
-__global__ void __launch_bounds__(kUpdThreads) k_update(QPlan p, int t, int64_t toks) {
-    extern __shared__ __align__(16) unsigned char smem_raw[];
-    constexpr int CH = 32 * CPL;
-    long long *bins = reinterpret_cast<long long *>(smem_raw);
-    unsigned *cnt = reinterpret_cast<unsigned *>(bins + (size_t)p.C * CH);
-    const int h = blockIdx.z, slab = blockIdx.y;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    constexpr int nw = kUpdThreads / 32;
-    for (int x = threadIdx.x; x < p.C * CH; x += kUpdThreads) bins[x] = 0;
-    for (int x = threadIdx.x; x < p.C; x += kUpdThreads) cnt[x] = 0;
+__global__ void __launch_bounds__(kSortBlock) k_sort_hist(QPlan p, int t) {
+    __shared__ int hist[kMaxC];
+    const int h = blockIdx.y, b = blockIdx.x;
+    for (int j = threadIdx.x; j < p.C; j += kSortBlock) hist[j] = 0;
     __syncthreads();
-
-    const float scale = pow2f(fixed_q(p.maxabs[h], p.N));
-    const int64_t t0 = (int64_t)blockIdx.x * toks;
-    const int64_t t1 = min(p.N, t0 + toks);
-    const int64_t span = (t1 - t0 + nw - 1) / nw;
-    const int64_t w0 = min(t1, t0 + warp * span), w1 = min(t1, w0 + span);
-    // lane l owns channels slab*CH + l + 32*c: every access of a warp is one contiguous run
-    const int ch = slab * CH + lane;
+    const int64_t i = (int64_t)b * kSortBlock + threadIdx.x;
     const uint8_t *pis = p.pi + (int64_t)(h * p.T + t - 1) * p.cap + p.tok_off;
-    const float *rsrc = SRC == 2 ? p.R32 + (int64_t)h * p.N * kD + ch : nullptr;
-    const float *xsrc32 = SRC == 1 ? static_cast<const float *>(p.X) + h * p.x_stride + ch : nullptr;
-    const uint16_t *xsrc16 = SRC == 0 ? static_cast<const uint16_t *>(p.X) + h * p.x_stride + ch : nullptr;
-
-    int run_p = -1;
-    unsigned run_n = 0;
-    long long acc[CPL];
-#pragma unroll
-    for (int c = 0; c < CPL; c++) acc[c] = 0;
-
-    auto flush = [&]() {
-        if (run_p >= 0) {
-#pragma unroll
-            for (int c = 0; c < CPL; c++)
-                atomicAdd(reinterpret_cast<unsigned long long *>(bins + run_p * CH + lane + 32 * c),
-                          static_cast<unsigned long long>(acc[c]));
-            if (lane == 0) atomicAdd(cnt + run_p, run_n);
-        }
-    };
-
-    for (int64_t base = w0; base < w1; base += 32) {
-        const int n = (int)min((int64_t)32, w1 - base);
-        int my_p = lane < n ? (int)pis[base + lane] : 0;
-        if (my_p >= p.C) {  // never produced by the assignment; counted, not accumulated
-            or_status(p.status, QVG_DEV_BAD_INDEX);
-            my_p = -1;
-        }
-        for (int jj = 0; jj < n; jj += kUpdBatch) {
-            float val[kUpdBatch][CPL];
-#pragma unroll
-            for (int u = 0; u < kUpdBatch; u++) {
-                const int64_t i = base + jj + u;
-                if (jj + u < n) {
-#pragma unroll
-                    for (int c = 0; c < CPL; c++) {
-                        if constexpr (SRC == 2) {
-                            val[u][c] = __ldg(rsrc + i * kD + 32 * c);
-                        } else if constexpr (SRC == 1) {
-                            val[u][c] = __ldg(xsrc32 + i * kD + 32 * c);
-                        } else {
-                            const uint32_t b = __ldg(reinterpret_cast<const unsigned short *>(xsrc16) + i * kD + 32 * c);
-                            val[u][c] = p.in_dtype == DT_BF16 ? __uint_as_float(b << 16)
-                                                              : __half2float(__ushort_as_half((unsigned short)b));
-                        }
-                    }
-                }
-            }
-#pragma unroll
-            for (int u = 0; u < kUpdBatch; u++) {
-                if (jj + u < n) {
-                    const int pj = __shfl_sync(0xffffffffu, my_p, jj + u);
-                    if (pj < 0) continue;
-                    if (pj != run_p) {
-                        flush();
-                        run_p = pj;
-                        run_n = 0;
-#pragma unroll
-                        for (int c = 0; c < CPL; c++) acc[c] = 0;
-                    }
-                    run_n++;
-#pragma unroll
-                    for (int c = 0; c < CPL; c++) acc[c] += __float2ll_rn(val[u][c] * scale);
-                }
-            }
-        }
+    if (i < p.N) {
+        const int j = pis[i];
+        if (j < p.C) atomicAdd(hist + j, 1);
+        else or_status(p.status, QVG_DEV_BAD_INDEX);
     }
-    flush();
     __syncthreads();
-    long long *gs = p.sums + (int64_t)h * p.C * kD + slab * CH;
-    for (int x = threadIdx.x; x < p.C * CH; x += kUpdThreads) {
-        const int j = x / CH;
-        if (cnt[j] != 0u)
-            atomicAdd(reinterpret_cast<unsigned long long *>(gs + (int64_t)j * kD + (x - j * CH)),
-                      static_cast<unsigned long long>(bins[x]));
-    }
-    if (slab == 0)
-        for (int j = threadIdx.x; j < p.C; j += kUpdThreads)
-            if (cnt[j] != 0u) atomicAdd(p.counts + h * p.C + j, (int)cnt[j]);
+    int *bh = p.blockoff + ((int64_t)h * p.nsb + b) * p.C;
+    for (int j = threadIdx.x; j < p.C; j += kSortBlock) bh[j] = hist[j];
 }
 
-template <int CPL>
-static cudaError_t launch_update_cpl(const QPlan &p, int t, int num_sms, cudaStream_t st) {
-    constexpr int CH = 32 * CPL;
-    const size_t smem = (size_t)p.C * CH * 8 + (size_t)p.C * 4;
-    const int slabs = kD / CH;
-    // one wave of CTAs (one per SM): few CTAs keep the final flush of the shared-memory
-    // bins to the global sums small; at least 512 tokens per CTA
-    const int64_t per_tensor = std::max<int64_t>(1, num_sms / ((int64_t)p.H * slabs));
-    int64_t toks = std::max<int64_t>(512, (p.N + per_tensor - 1) / per_tensor);
-    toks = (toks + 31) / 32 * 32;
-    const unsigned units = (unsigned)((p.N + toks - 1) / toks);
-    dim3 grid(units, slabs, p.H);
-    cudaError_t e;
-    if (t >= 2) {
-        e = cudaFuncSetAttribute(k_update<CPL, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        k_update<CPL, 2><<<grid, kUpdThreads, smem, st>>>(p, t, toks);
-    } else if (p.in_dtype == DT_F32) {
-        e = cudaFuncSetAttribute(k_update<CPL, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        k_update<CPL, 1><<<grid, kUpdThreads, smem, st>>>(p, t, toks);
-    } else {
-        e = cudaFuncSetAttribute(k_update<CPL, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        k_update<CPL, 0><<<grid, kUpdThreads, smem, st>>>(p, t, toks);
+__global__ void __launch_bounds__(kMaxC) k_sort_scan(QPlan p) {
+    // one block per tensor, thread j = cluster j
+    const int h = blockIdx.x, j = threadIdx.x;
+    __shared__ int buf[kMaxC];
+    int *bh = p.blockoff + (int64_t)h * p.nsb * p.C;
+    int total = 0;
+    if (j < p.C)
+        for (int b = 0; b < p.nsb; b++) total += bh[(int64_t)b * p.C + j];
+    buf[j] = j < p.C ? total : 0;
+    __syncthreads();
+    for (int o = 1; o < kMaxC; o <<= 1) {
+        const int a1 = j >= o ? buf[j - o] : 0;
+        __syncthreads();
+        buf[j] += a1;
+        __syncthreads();
     }
+    if (j < p.C) {
+        const int off = buf[j] - total;
+        p.counts[h * p.C + j] = total;
+        p.offs[h * p.C + j] = off;
+        int run = off;
+        for (int b = 0; b < p.nsb; b++) {
+            const int v = bh[(int64_t)b * p.C + j];
+            bh[(int64_t)b * p.C + j] = run;
+            run += v;
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kSortBlock) k_sort_scatter(QPlan p, int t) {
+    constexpr int NW = kSortBlock / 32;
+    __shared__ int wcnt[NW][kMaxC];  // tokens of each cluster in each warp
+    const int h = blockIdx.y, b = blockIdx.x;
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    for (int x = threadIdx.x; x < NW * kMaxC; x += kSortBlock) (&wcnt[0][0])[x] = 0;
+    __syncthreads();
+    const int64_t i = (int64_t)b * kSortBlock + threadIdx.x;
+    const uint8_t *pis = p.pi + (int64_t)(h * p.T + t - 1) * p.cap + p.tok_off;
+    int j = -1;
+    if (i < p.N) {
+        j = pis[i];
+        if (j >= p.C) j = -1;
+    }
+    const unsigned same = __match_any_sync(0xffffffffu, j);
+    const int rank = __popc(same & ((1u << lane) - 1u));  // earlier lanes, same cluster
+    if (j >= 0 && rank == 0) wcnt[w][j] = __popc(same);
+    __syncthreads();
+    if (j >= 0) {
+        int pos = p.blockoff[((int64_t)h * p.nsb + b) * p.C + j] + rank;
+        for (int w2 = 0; w2 < w; w2++) pos += wcnt[w2][j];
+        p.ids[(int64_t)h * p.N + pos] = (int)i;
+        p.cid[(int64_t)h * p.N + pos] = (uint8_t)j;
+    }
+}
+
+// Mean of S + E over n rows: the quotient of S corrected by the remainder and by E.
+__device__ __forceinline__ float mean_of(float S, float E, float n) {
+    const float q0 = __fdiv_rn(S, n);
+    const float r = __fadd_rn(__fmaf_rn(-q0, n, S), E);
+    return __fadd_rn(q0, __fdiv_rn(r, n));
+}
+
+// New centroid row j (lane l: channels 4l..4l+3), and its GEMM planes if requested.
+__device__ __forceinline__ void write_centroid(const QPlan &p, int h, int t, int j, int lane,
+                                               bool set, float4 cv, bool planes, float4 mu) {
+    float *c = p.cent + h * p.cent_tstride + p.cent_off + (int64_t)(t - 1) * p.C * kD +
+               (int64_t)j * kD + 4 * lane;
+    if (set)
+        *reinterpret_cast<float4 *>(c) = cv;
+    else
+        cv = *reinterpret_cast<float4 *>(c);
+    if (!planes) return;
+    const float ct[4] = {__fsub_rn(cv.x, mu.x), __fsub_rn(cv.y, mu.y), __fsub_rn(cv.z, mu.z),
+                         __fsub_rn(cv.w, mu.w)};
+    __align__(8) __nv_bfloat16 hi[4], lo[4];
+    float ss = 0.f;
+#pragma unroll
+    for (int k = 0; k < 4; k++) {
+        hi[k] = __float2bfloat16_rn(ct[k]);
+        lo[k] = __float2bfloat16_rn(__fsub_rn(ct[k], __bfloat162float(hi[k])));
+        ss = __fmaf_rn(ct[k], ct[k], ss);
+    }
+    *reinterpret_cast<uint2 *>(p.B + ((int64_t)(h * 2 + 0) * p.Cpad + j) * kD + 4 * lane) =
+        *reinterpret_cast<uint2 *>(hi);
+    *reinterpret_cast<uint2 *>(p.B + ((int64_t)(h * 2 + 1) * p.Cpad + j) * kD + 4 * lane) =
+        *reinterpret_cast<uint2 *>(lo);
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if (lane == 0) p.cn[(int64_t)h * p.Cpad + j] = ss;
+}
+
+// One warp per chunk of 64 cluster-sorted positions: the rows of each run (same cluster)
+// are added with TwoSum in sorted order, 16 rows in flight.  A run that is a whole cluster
+// leaves its (sum, error) in the cluster's slot; a run that crosses the chunk's start or end
+// leaves it in the chunk's first / last slot.  k_cluster_finalize turns them into means.
+template <int SRC>  // 0: X bf16, 1: X fp32, 2: R32, 3: X fp16
+__global__ void __launch_bounds__(256, 2) k_chunk_sums(QPlan p, int t) {
+    constexpr bool NARROW = SRC == 0 || SRC == 3;  // 16-bit input rows: 8 bytes a lane
+    constexpr int ROWS = NARROW ? 32 : 16;         // rows whose loads are in flight
+    const int lane = threadIdx.x & 31;
+    const int h = blockIdx.y;
+    const int k = blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (k >= p.nchunk) return;
+    const int64_t c0 = (int64_t)k * kChunk;
+    const int nk = (int)min((int64_t)kChunk, p.N - c0);
+    const int *ids = p.ids + (int64_t)h * p.N + c0;
+    const uint8_t *cid = p.cid + (int64_t)h * p.N + c0;
+    int idr[2], cr[2];
+#pragma unroll
+    for (int q = 0; q < 2; q++) {
+        const int pos = q * 32 + lane;
+        idr[q] = pos < nk ? ids[pos] : 0;
+        cr[q] = pos < nk ? (int)cid[pos] : -1;
+    }
+    // clusters just before and just after the chunk decide whether its first and last runs
+    // continue into the neighbouring chunks
+    const int c_prev = k > 0 ? (int)p.cid[(int64_t)h * p.N + c0 - 1] : -1;
+    const int c_next = c0 + nk < p.N ? (int)p.cid[(int64_t)h * p.N + c0 + nk] : -1;
+    float s[4] = {0.f, 0.f, 0.f, 0.f}, e[4] = {0.f, 0.f, 0.f, 0.f};
+    int run_c = -1, run_start = 0;
+    auto stash = [&](int end) {
+        const bool whole = (run_start > 0 || c_prev != run_c) && (end < nk || c_next != run_c);
+        float *dst = whole ? p.wsum + ((int64_t)h * p.C + run_c) * 2 * kD
+                           : p.psum + (((int64_t)h * p.nchunk + k) * 2 + (run_start == 0 ? 0 : 1)) * 2 * kD;
+        reinterpret_cast<float4 *>(dst)[lane] = make_float4(s[0], s[1], s[2], s[3]);
+        reinterpret_cast<float4 *>(dst + kD)[lane] = make_float4(e[0], e[1], e[2], e[3]);
+    };
+    for (int k1 = 0; k1 < nk; k1 += ROWS) {
+        // all loads of the batch are issued before any is used: raw words only here
+        float4 raw[NARROW ? 1 : ROWS];
+        uint2 raw16[NARROW ? ROWS : 1];
+#pragma unroll
+        for (int u = 0; u < ROWS; u++) {
+            const int q = k1 + u;
+            const int64_t row = q < 32 ? __shfl_sync(0xffffffffu, idr[0], q & 31)
+                                       : __shfl_sync(0xffffffffu, idr[1], q & 31);
+            if constexpr (NARROW) {
+                raw16[u] = make_uint2(0u, 0u);
+                if (q < nk)
+                    raw16[u] = __ldg(reinterpret_cast<const uint2 *>(
+                        static_cast<const uint16_t *>(p.X) + h * p.x_stride + row * kD) + lane);
+            } else {
+                raw[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (q < nk) {
+                    if constexpr (SRC == 2)
+                        raw[u] = __ldg(reinterpret_cast<const float4 *>(
+                            p.R32 + ((int64_t)h * p.N + row) * kD) + lane);
+                    else
+                        raw[u] = __ldg(reinterpret_cast<const float4 *>(
+                            static_cast<const float *>(p.X) + h * p.x_stride + row * kD) + lane);
+                }
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < ROWS; u++) {
+            const int q = k1 + u;
+            const int cu = q < 32 ? __shfl_sync(0xffffffffu, cr[0], q & 31)
+                                  : __shfl_sync(0xffffffffu, cr[1], q & 31);
+            if (q < nk) {
+                float v[4];
+                if constexpr (SRC == 0) {
+                    const uint32_t wx = raw16[u].x, wy = raw16[u].y;
+                    v[0] = __uint_as_float(wx << 16);
+                    v[1] = __uint_as_float(wx & 0xFFFF0000u);
+                    v[2] = __uint_as_float(wy << 16);
+                    v[3] = __uint_as_float(wy & 0xFFFF0000u);
+                } else if constexpr (SRC == 3) {
+                    const uint32_t wx = raw16[u].x, wy = raw16[u].y;
+                    const float2 f0 = __half22float2(*reinterpret_cast<const __half2 *>(&wx));
+                    const float2 f1 = __half22float2(*reinterpret_cast<const __half2 *>(&wy));
+                    v[0] = f0.x; v[1] = f0.y; v[2] = f1.x; v[3] = f1.y;
+                } else {
+                    v[0] = raw[u].x; v[1] = raw[u].y; v[2] = raw[u].z; v[3] = raw[u].w;
+                }
+                if (cu != run_c) {
+                    if (run_c >= 0) stash(q);
+                    run_c = cu;
+                    run_start = q;
+#pragma unroll
+                    for (int r = 0; r < 4; r++) s[r] = e[r] = 0.f;
+                }
+#pragma unroll
+                for (int r = 0; r < 4; r++) acc_two_sum(s[r], e[r], v[r]);
+            }
+        }
+    }
+    if (run_c >= 0) stash(nk);
+}
+
+// One warp per cluster: the mean from the cluster's own slot, or, for clusters spread over
+// several chunks, from their pieces added in chunk order; empty clusters keep their
+// centroid.  Then the centroid and its GEMM planes are written.
+__global__ void __launch_bounds__(256) k_cluster_finalize(QPlan p, int t, int planes) {
+    const int lane = threadIdx.x & 31;
+    const int j = blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int h = blockIdx.y;
+    if (j >= p.C) return;
+    const int cnt = p.counts[h * p.C + j];
+    const float4 mu = *reinterpret_cast<const float4 *>(p.mu + h * kD + 4 * lane);
+    if (cnt == 0) {
+        write_centroid(p, h, t, j, lane, false, make_float4(0.f, 0.f, 0.f, 0.f), planes != 0, mu);
+        return;
+    }
+    const int off = p.offs[h * p.C + j];
+    const int a = off / kChunk, b = (off + cnt - 1) / kChunk;
+    float S[4] = {0.f, 0.f, 0.f, 0.f}, E[4] = {0.f, 0.f, 0.f, 0.f};
+    if (a == b) {
+        // the whole cluster was one run of one chunk
+        const float *ws = p.wsum + ((int64_t)h * p.C + j) * 2 * kD;
+        const float4 sa = reinterpret_cast<const float4 *>(ws)[lane];
+        const float4 sb = reinterpret_cast<const float4 *>(ws + kD)[lane];
+        S[0] = sa.x; S[1] = sa.y; S[2] = sa.z; S[3] = sa.w;
+        E[0] = sb.x; E[1] = sb.y; E[2] = sb.z; E[3] = sb.w;
+    }
+    const int np = a == b ? 0 : b - a + 1;
+    for (int q0 = 0; q0 < np; q0 += 4) {
+        float4 sa[4], sb[4];  // 4 pieces' loads in flight, added in chunk order
+#pragma unroll
+        for (int u = 0; u < 4; u++)
+            if (q0 + u < np) {
+                const int kk = a + q0 + u;
+                // in its first chunk the cluster's run is the chunk's last run unless it
+                // starts exactly at the chunk start; in later chunks it is the first run
+                const int slot = (kk == a && off != (int64_t)a * kChunk) ? 1 : 0;
+                const float *ps = p.psum + (((int64_t)h * p.nchunk + kk) * 2 + slot) * 2 * kD;
+                sa[u] = reinterpret_cast<const float4 *>(ps)[lane];
+                sb[u] = reinterpret_cast<const float4 *>(ps + kD)[lane];
+            }
+#pragma unroll
+        for (int u = 0; u < 4; u++)
+            if (q0 + u < np) {
+                const float av[4] = {sa[u].x, sa[u].y, sa[u].z, sa[u].w};
+                const float bv[4] = {sb[u].x, sb[u].y, sb[u].z, sb[u].w};
+#pragma unroll
+                for (int k = 0; k < 4; k++) {
+                    acc_two_sum(S[k], E[k], av[k]);
+                    E[k] = __fadd_rn(E[k], bv[k]);
+                }
+            }
+    }
+    const float n = (float)cnt;
+    write_centroid(p, h, t, j, lane, true,
+                   make_float4(mean_of(S[0], E[0], n), mean_of(S[1], E[1], n), mean_of(S[2], E[2], n),
+                               mean_of(S[3], E[3], n)),
+                   planes != 0, mu);
+}
+
+cudaError_t launch_cluster_means(const QPlan &p, int t, bool planes, cudaStream_t st) {
+    const dim3 sgrid((unsigned)p.nsb, p.H);
+    k_sort_hist<<<sgrid, kSortBlock, 0, st>>>(p, t);
+    k_sort_scan<<<p.H, kMaxC, 0, st>>>(p);
+    k_sort_scatter<<<sgrid, kSortBlock, 0, st>>>(p, t);
+    const dim3 cgrid((unsigned)((p.nchunk + 7) / 8), p.H);
+    if (t >= 2)
+        k_chunk_sums<2><<<cgrid, 256, 0, st>>>(p, t);
+    else if (p.in_dtype == DT_F32)
+        k_chunk_sums<1><<<cgrid, 256, 0, st>>>(p, t);
+    else if (p.in_dtype == DT_F16)
+        k_chunk_sums<3><<<cgrid, 256, 0, st>>>(p, t);
+    else
+        k_chunk_sums<0><<<cgrid, 256, 0, st>>>(p, t);
+    k_cluster_finalize<<<dim3((unsigned)((p.C + 7) / 8), p.H), 256, 0, st>>>(p, t, planes ? 1 : 0);
     return cudaGetLastError();
-}
-
-cudaError_t launch_update(const QPlan &p, int t, int num_sms, cudaStream_t st) {
-    // 128-channel bins when they fit comfortably in shared memory, else 64-channel slabs.
-    if ((size_t)p.C * kD * 8 <= 100 * 1024) return launch_update_cpl<4>(p, t, num_sms, st);
-    return launch_update_cpl<2>(p, t, num_sms, st);
 }
 
 // --------------------------------------------------------------------------------------
@@ -436,19 +573,21 @@ cudaError_t launch_update(const QPlan &p, int t, int num_sms, cudaStream_t st) {
 //   finite), q = clamp(rne(r / s_q), -qmax, qmax), u = q + 2^(b-1); s_q == 0 gives u = 2^(b-1).
 // grid-stride over tokens, block 256 = 16 tokens x 16 chunks.
 // --------------------------------------------------------------------------------------
+constexpr int kEncTokens = 256;
+
 __global__ void __launch_bounds__(256) k_encode(QPlan p) {
+    const int h = blockIdx.y;
     const int c8 = threadIdx.x & 15;
     const int lpg = p.group >> 3;  // lanes per scale group (2, 4, 8)
     const int qmax = (1 << (p.bits - 1)) - 1, mid = 1 << (p.bits - 1);
-    const int64_t total = (int64_t)p.H * p.N;
+    const int64_t i0 = (int64_t)blockIdx.x * kEncTokens;
+    const int64_t i1 = min(p.N, i0 + kEncTokens);
     bool finite = true, bad_index = false;
-    for (int64_t rb = (int64_t)blockIdx.x * 16; rb < total; rb += (int64_t)gridDim.x * 16) {
+    for (int64_t ib = i0; ib < i1; ib += 16) {
         // the loop bound is uniform over the block, so every lane reaches the shuffles;
         // rows past the end compute on zeros and store nothing
-        const int64_t row = rb + (threadIdx.x >> 4);
-        const bool valid = row < total;
-        const int h = valid ? (int)(row / p.N) : 0;
-        const int64_t i = valid ? row - (int64_t)h * p.N : 0;
+        const int64_t i = ib + (threadIdx.x >> 4);
+        const bool valid = i < i1;
         float x[8], s[8], e[8];
         if (valid) {
             load_x8(p.X, p.in_dtype, h * p.x_stride + i * kD + c8 * 8, x);
@@ -471,11 +610,17 @@ __global__ void __launch_bounds__(256) k_encode(QPlan p) {
             float c[8];
             load_f8(p.cent + h * p.cent_tstride + p.cent_off + (int64_t)(st - 1) * p.C * kD +
                         (int64_t)pj * kD + c8 * 8, c);
+            if (p.T == 1) {
+                // one subtraction is already a single rounding of the exact residual
 #pragma unroll
-            for (int q = 0; q < 8; q++) {
-                float err;
-                two_sum(s[q], -c[q], s[q], err);
-                e[q] = __fadd_rn(e[q], err);
+                for (int q = 0; q < 8; q++) s[q] = __fsub_rn(s[q], c[q]);
+            } else {
+#pragma unroll
+                for (int q = 0; q < 8; q++) {
+                    float err;
+                    two_sum(s[q], -c[q], s[q], err);
+                    e[q] = __fadd_rn(e[q], err);
+                }
             }
         }
         float r[8], a = 0.f;
@@ -499,8 +644,7 @@ __global__ void __launch_bounds__(256) k_encode(QPlan p) {
             if (sq != 0.f) {
                 float v = __fmul_rn(r[q], inv);
                 if (fabsf(fabsf(v - rintf(v)) - 0.5f) < 0x1p-17f) v = __fdiv_rn(r[q], sq);
-                const float qq = fminf(fmaxf(rintf(v), (float)-qmax), (float)qmax);
-                u = (int)qq + mid;
+                u = __float2int_rn(fminf(fmaxf(v, (float)-qmax), (float)qmax)) + mid;
             }
             word |= (uint32_t)u << (q * p.bits);
         }
@@ -518,10 +662,8 @@ __global__ void __launch_bounds__(256) k_encode(QPlan p) {
 }
 
 cudaError_t launch_encode(const QPlan &p, cudaStream_t st) {
-    const int64_t rows = (int64_t)p.H * p.N;
-    int64_t blocks = (rows + 15) / 16;
-    if (blocks > 65535LL * 16) blocks = 65535LL * 16;
-    k_encode<<<(unsigned)blocks, 256, 0, st>>>(p);
+    dim3 grid((unsigned)((p.N + kEncTokens - 1) / kEncTokens), p.H);
+    k_encode<<<grid, 256, 0, st>>>(p);
     return cudaGetLastError();
 }
 

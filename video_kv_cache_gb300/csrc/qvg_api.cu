@@ -18,7 +18,9 @@ inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 
 inline int cpad_of(int C) { return C <= 16 ? 16 : (C + 15) / 16 * 16; }
 
 struct WsLayout {
-    size_t R32, A, rnorm, B, cn, mu, sums, counts, maxabs, init_idx, stats, rq_count, rq, total;
+    size_t R32, A, rnorm, B, cn, mu, counts, offs, blockoff, ids, cid, psum, wsum, maxabs, init_idx,
+        stats, rq_count, rq, total;
+    int nsb, nchunk;
 };
 
 WsLayout ws_layout(int64_t H, int64_t N, int C, int T) {
@@ -36,10 +38,17 @@ WsLayout ws_layout(int64_t H, int64_t N, int C, int T) {
         w.A = take((size_t)H * 2 * N * kD * 2);
         w.rnorm = take((size_t)H * N * 4);
         w.B = take((size_t)H * 2 * Cpad * kD * 2);
-        w.cn = take((size_t)H * Cpad * 4);
+        w.cn = take((size_t)H * Cpad * 4 + 32 * 4);  // 32-column TMEM reads may run past Cpad
         w.mu = take((size_t)H * kD * 4);
-        w.sums = take((size_t)H * C * kD * 8);
+        w.nsb = (int)((N + kSortBlock - 1) / kSortBlock);
+        w.nchunk = (int)((N + kChunk - 1) / kChunk);
         w.counts = take((size_t)H * C * 4);
+        w.offs = take((size_t)H * C * 4);
+        w.blockoff = take((size_t)H * w.nsb * C * 4);
+        w.ids = take((size_t)H * N * 4);
+        w.cid = take((size_t)H * N);
+        w.psum = take((size_t)H * w.nchunk * 4 * kD * 4);
+        w.wsum = take((size_t)H * C * 2 * kD * 4);
         w.maxabs = take((size_t)H * 4);
         w.init_idx = take((size_t)H * T * C * 4);
         w.rq_count = take(4);
@@ -98,8 +107,6 @@ qvg_status device_info(int *num_sms) {
 
 qvg_status run_quantize(QPlan &p, const qvg_quant_params *prm, int num_sms, cudaStream_t st) {
     if (p.T > 0) {
-        QVG_CUDA(cudaMemsetAsync(p.sums, 0, (size_t)p.H * p.C * kD * 8, st));
-        QVG_CUDA(cudaMemsetAsync(p.counts, 0, (size_t)p.H * p.C * 4, st));
         if (!p.warm) QVG_CUDA(launch_init_indices(p, prm->seed, prm->tensor_id_base, st));
         AssignMaps *maps = nullptr;
         QVG_CUDA(assign_prepare(p, &maps));
@@ -113,13 +120,12 @@ qvg_status run_quantize(QPlan &p, const qvg_quant_params *prm, int num_sms, cuda
             step(launch_centre(p, t, st));
             step(launch_prep(p, t, st));
             if (t >= 2) step(launch_init_centroids(p, t, st));
-            step(launch_centroid_planes(p, t, false, true, st));
+            step(launch_centroid_planes(p, t, st));
             for (int it = 1; it <= p.iters && rc == QVG_OK; it++) {
                 step(cudaMemsetAsync(p.rq_count, 0, 4, st));
                 step(launch_assign(p, maps, t, num_sms, st));
                 step(launch_refine(p, t, num_sms, st));
-                step(launch_update(p, t, num_sms, st));
-                step(launch_centroid_planes(p, t, true, it < p.iters, st));
+                step(launch_cluster_means(p, t, it < p.iters, st));
             }
         }
         assign_release(maps);
@@ -167,8 +173,15 @@ QPlan make_plan(const qvg_quant_params *prm, const void *X, const float *warm,
         p.B = reinterpret_cast<__nv_bfloat16 *>(ws + w.B);
         p.cn = reinterpret_cast<float *>(ws + w.cn);
         p.mu = reinterpret_cast<float *>(ws + w.mu);
-        p.sums = reinterpret_cast<long long *>(ws + w.sums);
         p.counts = reinterpret_cast<int *>(ws + w.counts);
+        p.offs = reinterpret_cast<int *>(ws + w.offs);
+        p.blockoff = reinterpret_cast<int *>(ws + w.blockoff);
+        p.ids = reinterpret_cast<int *>(ws + w.ids);
+        p.cid = reinterpret_cast<uint8_t *>(ws + w.cid);
+        p.psum = reinterpret_cast<float *>(ws + w.psum);
+        p.wsum = reinterpret_cast<float *>(ws + w.wsum);
+        p.nsb = w.nsb;
+        p.nchunk = w.nchunk;
         p.maxabs = reinterpret_cast<unsigned *>(ws + w.maxabs);
         p.init_idx = reinterpret_cast<int *>(ws + w.init_idx);
         p.rq_count = reinterpret_cast<int *>(ws + w.rq_count);
@@ -237,7 +250,7 @@ qvg_status qvg_reassign(const qvg_quant_params *prm, const void *X, const qvg_bu
         (void)cudaGetLastError();
         return QVG_ERR_CUDA;
     }
-    cudaError_t e = launch_centroid_planes(p, p.T, false, true, st);
+    cudaError_t e = launch_centroid_planes(p, p.T, st);
     if (e == cudaSuccess) e = cudaMemsetAsync(p.rq_count, 0, 4, st);
     if (e == cudaSuccess) e = launch_assign(p, maps, p.T, num_sms, st);
     if (e == cudaSuccess) e = launch_refine(p, p.T, num_sms, st);
