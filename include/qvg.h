@@ -25,7 +25,8 @@
  * Conventions for every call:
  *   - All data pointers are DEVICE pointers into memory the caller owns and keeps alive
  *     until the work on `stream` has finished.  The library allocates no device memory and
- *     keeps no mutable global state; scratch space is the caller's `workspace`.
+ *     keeps no mutable global state; scratch space is the caller's `workspace`.  The one
+ *     exception is qvg_quantize_static, whose scratch is a fixed area inside the library.
  *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).  Work
  *     is enqueued asynchronously; a call returns once it is enqueued.
  *   - Argument errors are detected on the host before anything is enqueued and returned as
@@ -55,7 +56,9 @@ typedef enum {
     QVG_ERR_UNSUPPORTED = 2, /* a value outside the supported shapes listed above */
     QVG_ERR_WORKSPACE = 3,   /* workspace NULL or smaller than qvg_quantize_workspace_bytes */
     QVG_ERR_CUDA = 4,        /* a CUDA runtime call failed while enqueuing (no device, launch) */
-    QVG_ERR_DEVICE = 5       /* the current device is not an sm_103 (GB300-class) GPU */
+    QVG_ERR_DEVICE = 5,      /* the current device is not an sm_103 (GB300-class) GPU */
+    QVG_ERR_SCRATCH_LIMIT = 6 /* qvg_quantize_static: the problem needs more scratch than
+                                 QVG_STATIC_SCRATCH_BYTES */
 } qvg_status;
 
 /* Bits OR-ed into *dev_status by the device. */
@@ -119,6 +122,48 @@ size_t qvg_quantize_workspace_bytes(const qvg_quant_params *params);
 qvg_status qvg_quantize(const qvg_quant_params *params, const void *X,
                         const float *warm_centroids, const qvg_buffers *out, void *workspace,
                         size_t workspace_bytes, uint32_t *dev_status, void *stream);
+
+/* Size of the fixed scratch area behind qvg_quantize_static: 64 MiB per device. */
+#define QVG_STATIC_SCRATCH_BYTES ((size_t)64 << 20)
+
+/* qvg_quantize without a workspace argument, for callers that cannot allocate.
+ *
+ * The paper has no counterpart to this call: it is a convenience of this library.  It
+ * runs the same kernels as qvg_quantize and gives the same results, but takes its scratch
+ * from one area of QVG_STATIC_SCRATCH_BYTES compiled into the library (a separate copy on
+ * each device) instead of from the caller, and allocates nothing itself: no cudaMalloc or
+ * cudaFree, no allocating library, no host heap.
+ *
+ * Who needs it: a caller that may not or cannot allocate device memory at the moment it
+ * compresses -- a server that has handed all free memory to its KV pool or to a caching
+ * allocator, a latency-bound loop in which cudaMalloc / cudaFree (which can synchronise
+ * the device) would stall the other streams, or a plain C host with no allocator of its
+ * own.
+ *
+ * Limit: qvg_quantize_workspace_bytes(params) must not exceed QVG_STATIC_SCRATCH_BYTES;
+ * otherwise the call returns QVG_ERR_SCRATCH_LIMIT before touching the device.  That is
+ * about 60 000 token rows (n_tensors * N) for T >= 2 and about 110 000 for T = 1.
+ *
+ * First call on a device: the first call made while a given device is current looks up
+ * the area's device address once (cudaGetSymbolAddress, which can load the library's
+ * device code on that device); if that fails the call returns QVG_ERR_CUDA.  Make this
+ * first call before any stream capture begins on that device.  Later calls reuse the
+ * address; after cudaDeviceReset it is stale, so do not call this function again in that
+ * process.
+ *
+ * Contents on entry do not matter: everything the path needs to start at zero is cleared
+ * by the call itself, on `stream`, before it is used.
+ *
+ * Races: all calls on one device share the one area.  Two calls whose device work can
+ * overlap -- on different streams with no event ordering them, e.g. from different host
+ * threads -- overwrite each other's scratch and both results are wrong.  Issue them on
+ * one stream, or order them with events.
+ *
+ * Arguments other than the workspace, layouts and the other errors are those of
+ * qvg_quantize. */
+qvg_status qvg_quantize_static(const qvg_quant_params *params, const void *X,
+                               const float *warm_centroids, const qvg_buffers *out,
+                               uint32_t *dev_status, void *stream);
 
 /* Assign every token's stage-T residual R^(T-1) to its nearest centroid of C^(T) as stored
  * in out->centroids (table slot table_index), writing pi^(T).  This is one assignment step

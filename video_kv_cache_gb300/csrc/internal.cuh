@@ -13,6 +13,7 @@
 //     direct fp32 sum of squared differences, ties going to the lowest cluster index.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -178,7 +179,14 @@ constexpr int kSortBlock = 256;  // tokens per block of the counting sort
 constexpr int kChunk = 64;       // sorted positions summed by one warp
 cudaError_t launch_encode(const QPlan &p, cudaStream_t st);
 
-struct AssignMaps;  // opaque: tensor maps for the assignment GEMM
+// TMA tensor maps of the assignment GEMM: A = residual planes, B = centroid planes.
+struct AssignMaps {
+    CUtensorMap a;
+    CUtensorMap b;
+};
+// Encodes the maps for plan p into caller-provided storage (no allocation).
+cudaError_t assign_encode(const QPlan &p, AssignMaps *maps);
+// Heap-allocates the maps and encodes them; free with assign_release.
 cudaError_t assign_prepare(const QPlan &p, AssignMaps **maps);
 void assign_release(AssignMaps *maps);
 cudaError_t launch_assign(const QPlan &p, const AssignMaps *maps, int t, int num_sms,

@@ -32,11 +32,6 @@
 
 namespace qvg {
 
-struct AssignMaps {
-    CUtensorMap a;
-    CUtensorMap b;
-};
-
 namespace {
 
 constexpr int kEpiGroups = 2;                      // epilogue groups of 8 warps
@@ -544,11 +539,9 @@ size_t assign_smem_bytes(int Cpad) {
            assign_tail_bytes(nslots, Cpad);
 }
 
-cudaError_t assign_prepare(const QPlan &p, AssignMaps **out) {
-    *out = nullptr;
+cudaError_t assign_encode(const QPlan &p, AssignMaps *m) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return cudaErrorNotSupported;
-    AssignMaps *m = new AssignMaps;
     const cuuint32_t estr[3] = {1, 1, 1};
     {
         const cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)p.N, (cuuint64_t)(2 * p.H)};
@@ -556,10 +549,8 @@ cudaError_t assign_prepare(const QPlan &p, AssignMaps **out) {
         const cuuint32_t box[3] = {64, (cuuint32_t)kTileM, 1};
         if (enc(&m->a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, p.A, dims, strides, box, estr,
                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS) {
-            delete m;
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
-        }
     }
     {
         const cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)p.C, (cuuint64_t)(2 * p.H)};
@@ -567,10 +558,20 @@ cudaError_t assign_prepare(const QPlan &p, AssignMaps **out) {
         const cuuint32_t box[3] = {64, (cuuint32_t)p.Cpad, 1};
         if (enc(&m->b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, p.B, dims, strides, box, estr,
                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS) {
-            delete m;
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
-        }
+    }
+    return cudaSuccess;
+}
+
+cudaError_t assign_prepare(const QPlan &p, AssignMaps **out) {
+    *out = nullptr;
+    if (!encode_fn()) return cudaErrorNotSupported;
+    AssignMaps *m = new AssignMaps;
+    const cudaError_t e = assign_encode(p, m);
+    if (e != cudaSuccess) {
+        delete m;
+        return e;
     }
     *out = m;
     return cudaSuccess;

@@ -3,6 +3,7 @@
 // are in include/qvg.h.
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 
 #include "internal.cuh"
 #include "qvg.h"
@@ -86,6 +87,16 @@ qvg_status check_quant(const qvg_quant_params *p) {
     return QVG_OK;
 }
 
+qvg_status check_quant_buffers(const qvg_quant_params *prm, const void *X, const float *warm,
+                               const qvg_buffers *out) {
+    if (!X || !out || !out->codes || !out->scales) return QVG_ERR_INVALID_ARG;
+    if (prm->T > 0 && (!out->pi || !out->centroids)) return QVG_ERR_INVALID_ARG;
+    if (!aligned16(X) || !aligned16(out->codes) || !aligned16(out->scales) ||
+        (prm->T > 0 && !aligned16(out->centroids)) || (warm && !aligned16(warm)))
+        return QVG_ERR_INVALID_ARG;
+    return QVG_OK;
+}
+
 qvg_status device_info(int *num_sms) {
     int dev = 0, major = 0, minor = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return QVG_ERR_CUDA;
@@ -105,29 +116,35 @@ qvg_status device_info(int *num_sms) {
         }                                             \
     } while (0)
 
+// The T smoothing stages: cold-start or warm centroids, then `iters` Lloyd rounds each.
+qvg_status run_stages(QPlan &p, const AssignMaps *maps, int num_sms, cudaStream_t st) {
+    qvg_status rc = QVG_OK;
+    for (int t = 1; t <= p.T && rc == QVG_OK; t++) {
+        auto step = [&](cudaError_t e) {
+            if (e != cudaSuccess && rc == QVG_OK) rc = QVG_ERR_CUDA;
+        };
+        step(cudaMemsetAsync(p.maxabs, 0, (size_t)p.H * 4, st));
+        if (t == 1) step(launch_init_centroids(p, t, st));
+        step(launch_centre(p, t, st));
+        step(launch_prep(p, t, st));
+        if (t >= 2) step(launch_init_centroids(p, t, st));
+        step(launch_centroid_planes(p, t, st));
+        for (int it = 1; it <= p.iters && rc == QVG_OK; it++) {
+            step(cudaMemsetAsync(p.rq_count, 0, 4, st));
+            step(launch_assign(p, maps, t, num_sms, st));
+            step(launch_refine(p, t, num_sms, st));
+            step(launch_cluster_means(p, t, it < p.iters, st));
+        }
+    }
+    return rc;
+}
+
 qvg_status run_quantize(QPlan &p, const qvg_quant_params *prm, int num_sms, cudaStream_t st) {
     if (p.T > 0) {
         if (!p.warm) QVG_CUDA(launch_init_indices(p, prm->seed, prm->tensor_id_base, st));
         AssignMaps *maps = nullptr;
         QVG_CUDA(assign_prepare(p, &maps));
-        qvg_status rc = QVG_OK;
-        for (int t = 1; t <= p.T && rc == QVG_OK; t++) {
-            auto step = [&](cudaError_t e) {
-                if (e != cudaSuccess && rc == QVG_OK) rc = QVG_ERR_CUDA;
-            };
-            step(cudaMemsetAsync(p.maxabs, 0, (size_t)p.H * 4, st));
-            if (t == 1) step(launch_init_centroids(p, t, st));
-            step(launch_centre(p, t, st));
-            step(launch_prep(p, t, st));
-            if (t >= 2) step(launch_init_centroids(p, t, st));
-            step(launch_centroid_planes(p, t, st));
-            for (int it = 1; it <= p.iters && rc == QVG_OK; it++) {
-                step(cudaMemsetAsync(p.rq_count, 0, 4, st));
-                step(launch_assign(p, maps, t, num_sms, st));
-                step(launch_refine(p, t, num_sms, st));
-                step(launch_cluster_means(p, t, it < p.iters, st));
-            }
-        }
+        const qvg_status rc = run_stages(p, maps, num_sms, st);
         assign_release(maps);
         if (rc != QVG_OK) {
             (void)cudaGetLastError();
@@ -191,6 +208,35 @@ QPlan make_plan(const qvg_quant_params *prm, const void *X, const float *warm,
     return p;
 }
 
+// Scratch area of qvg_quantize_static.  A __device__ variable exists once in every device
+// context that loads this module, so each device has its own copy.
+static __device__ __align__(256) unsigned char g_static_scratch[QVG_STATIC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_static_mu;
+void *g_static_addr[kMaxDevices];
+
+// Device address of g_static_scratch on the current device, looked up once per device.
+qvg_status static_scratch(void **addr) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return QVG_ERR_CUDA;
+    }
+    if (dev < 0 || dev >= kMaxDevices) return QVG_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_static_mu);
+    if (!g_static_addr[dev]) {
+        void *a = nullptr;
+        if (cudaGetSymbolAddress(&a, g_static_scratch) != cudaSuccess || !a) {
+            (void)cudaGetLastError();
+            return QVG_ERR_CUDA;
+        }
+        g_static_addr[dev] = a;
+    }
+    *addr = g_static_addr[dev];
+    return QVG_OK;
+}
+
 }  // namespace
 }  // namespace qvg
 
@@ -208,11 +254,8 @@ qvg_status qvg_quantize(const qvg_quant_params *prm, const void *X, const float 
                         uint32_t *dev_status, void *stream) {
     qvg_status rc = check_quant(prm);
     if (rc != QVG_OK) return rc;
-    if (!X || !out || !out->codes || !out->scales) return QVG_ERR_INVALID_ARG;
-    if (prm->T > 0 && (!out->pi || !out->centroids)) return QVG_ERR_INVALID_ARG;
-    if (!aligned16(X) || !aligned16(out->codes) || !aligned16(out->scales) ||
-        (prm->T > 0 && !aligned16(out->centroids)) || (warm && !aligned16(warm)))
-        return QVG_ERR_INVALID_ARG;
+    rc = check_quant_buffers(prm, X, warm, out);
+    if (rc != QVG_OK) return rc;
     const WsLayout w = ws_layout(prm->n_tensors, prm->N, prm->C, prm->T);
     if (!workspace || workspace_bytes < w.total) return QVG_ERR_WORKSPACE;
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return QVG_ERR_INVALID_ARG;
@@ -227,6 +270,38 @@ qvg_status qvg_quantize(const qvg_quant_params *prm, const void *X, const float 
         return QVG_ERR_CUDA;
     }
     return run_quantize(p, prm, num_sms, st);
+}
+
+qvg_status qvg_quantize_static(const qvg_quant_params *prm, const void *X, const float *warm,
+                               const qvg_buffers *out, uint32_t *dev_status, void *stream) {
+    qvg_status rc = check_quant(prm);
+    if (rc != QVG_OK) return rc;
+    const WsLayout w = ws_layout(prm->n_tensors, prm->N, prm->C, prm->T);
+    if (w.total > QVG_STATIC_SCRATCH_BYTES) return QVG_ERR_SCRATCH_LIMIT;
+    rc = check_quant_buffers(prm, X, warm, out);
+    if (rc != QVG_OK) return rc;
+    int num_sms = 0;
+    rc = device_info(&num_sms);
+    if (rc != QVG_OK) return rc;
+    void *workspace = nullptr;
+    rc = static_scratch(&workspace);
+    if (rc != QVG_OK) return rc;
+
+    QPlan p = make_plan(prm, X, warm, out, workspace, w, dev_status);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    QVG_CUDA(cudaMemsetAsync(p.stats, 0, 64, st));
+    if (p.T > 0) {
+        if (!p.warm) QVG_CUDA(launch_init_indices(p, prm->seed, prm->tensor_id_base, st));
+        AssignMaps maps;  // kernel parameters are copied at launch: stack storage is enough
+        QVG_CUDA(assign_encode(p, &maps));
+        rc = run_stages(p, &maps, num_sms, st);
+        if (rc != QVG_OK) {
+            (void)cudaGetLastError();
+            return rc;
+        }
+    }
+    QVG_CUDA(launch_encode(p, st));
+    return QVG_OK;
 }
 
 qvg_status qvg_reassign(const qvg_quant_params *prm, const void *X, const qvg_buffers *out,
@@ -323,6 +398,8 @@ const char *qvg_status_string(qvg_status s) {
         case QVG_ERR_WORKSPACE: return "workspace missing or too small";
         case QVG_ERR_CUDA: return "CUDA error while enqueuing work";
         case QVG_ERR_DEVICE: return "current device is not an sm_103 GPU";
+        case QVG_ERR_SCRATCH_LIMIT:
+            return "problem needs more scratch than qvg_quantize_static's fixed area holds";
     }
     return "unknown status";
 }

@@ -19,6 +19,8 @@ QVG_ERR_UNSUPPORTED = 2
 QVG_ERR_WORKSPACE = 3
 QVG_ERR_CUDA = 4
 QVG_ERR_DEVICE = 5
+QVG_ERR_SCRATCH_LIMIT = 6
+QVG_STATIC_SCRATCH_BYTES = 64 << 20
 
 QVG_DEV_NONFINITE = 0x1
 QVG_DEV_TIMEOUT = 0x2
@@ -82,6 +84,9 @@ SIGNATURES = {
                                      ctypes.c_void_p, ctypes.POINTER(qvg_buffers),
                                      ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p,
                                      ctypes.c_void_p]),
+    "qvg_quantize_static": (ctypes.c_int, [ctypes.POINTER(qvg_quant_params), ctypes.c_void_p,
+                                            ctypes.c_void_p, ctypes.POINTER(qvg_buffers),
+                                            ctypes.c_void_p, ctypes.c_void_p]),
     "qvg_reassign": (ctypes.c_int, [ctypes.POINTER(qvg_quant_params), ctypes.c_void_p,
                                     ctypes.POINTER(qvg_buffers), ctypes.c_void_p,
                                     ctypes.c_size_t, ctypes.c_void_p, ctypes.c_void_p]),
@@ -135,6 +140,12 @@ def qvg_quantize(params: qvg_quant_params, X: int, warm_centroids: int | None,
                  dev_status: int | None, stream: int | None) -> int:
     return int(load().qvg_quantize(_ref(params), X, warm_centroids, _ref(out),
                                    workspace, workspace_bytes, dev_status, stream))
+
+
+def qvg_quantize_static(params: qvg_quant_params, X: int, warm_centroids: int | None,
+                        out: qvg_buffers, dev_status: int | None, stream: int | None) -> int:
+    return int(load().qvg_quantize_static(_ref(params), X, warm_centroids, _ref(out),
+                                          dev_status, stream))
 
 
 def qvg_reassign(params: qvg_quant_params, X: int, out: qvg_buffers, workspace: int,
