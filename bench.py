@@ -58,7 +58,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "25"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
@@ -117,8 +117,8 @@ def shard(n_tensors: int, rank: int, world: int):
 def _max_over_ranks(x: float, world: int) -> float:
     if world == 1:
         return x
-    t = torch.tensor([x], dtype=torch.float64,
-                     device="cuda" if torch.cuda.is_available() else "cpu")
+    nccl = torch.distributed.get_backend() == "nccl"
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if nccl else "cpu")
     torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
     return float(t.item())
 
@@ -136,36 +136,56 @@ def dequant_bytes(H, N, C, T, bits, group, out_bytes=2, n_tables=1):
     return H * (N * per_tok + tables)
 
 
-def cpu_baseline(w, steps=1, budget_s=20.0):
-    """The oracle as it stands, on a bounded sample of the workload, on this host's cores."""
+def assign_flops(H, N, C):
+    """Useful flops of one assignment launch over H tensors: the [N x 128] x [128 x C]
+    product per tensor (the split-bf16 GEMM issues three times as many)."""
+    return 2.0 * H * N * C * 128
+
+
+def launches_per_step(w):
+    """Kernels of libqvg launched by one quantize + dequantize of the workload (cold start):
+    init_indices, then per stage init_centroids, centre, prep, [pad_cn], centroid_planes and
+    per Lloyd round assign, refine, sort hist / scan / scatter, chunk sums, finalize; then
+    encode; then the fused dequant."""
+    cpad = 16 if w.C <= 16 else (w.C + 15) // 16 * 16
+    per_stage = 4 + (1 if cpad > w.C else 0) + 7 * w.iters
+    return 1 + w.T * per_stage + 1 + 1
+
+
+# DRAM traffic of one k_assign launch on layer_1p3b_32760 (dram__bytes_read.sum +
+# dram__bytes_write.sum, ncu), valid while the kernel's sources hash to `sources_sha256`.
+ASSIGN_TRAFFIC = {"workload": "layer_1p3b_32760", "bytes": 415293696,
+                  "sources_sha256": "4c2841fa07c46313d0d35fcf6e33d7d5a2eef3be87ec4e0b66b1ead2eaf11c97"}
+ASSIGN_SOURCES = ("video_kv_cache_gb300/csrc/k_assign.cu", "video_kv_cache_gb300/csrc/internal.cuh")
+
+
+def _sources_sha256(paths):
+    import hashlib
+    h = hashlib.sha256()
+    for p in paths:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def cpu_baseline(w):
+    """The oracle as it stands, on a bounded sample of the workload, on this host's cores:
+    as many whole tensors (all N tokens, the full T stages and Lloyd rounds) as there are
+    cores, one thread each, quantized and reconstructed."""
     import oracle
     cores = oracle.num_cores()
-    X = w.make("cpu", tids=w.tids[:1])
+    n = max(1, min(w.H, cores))
+    X = w.make("cpu", tids=w.tids[:n])
     Xd = oracle.decode_input(X)
-    # sample: whole tensors (all N tokens), as many as there are cores, capped by a quick
-    # one-tensor timing so the run stays within the budget
     t0 = time.perf_counter()
-    r = oracle.quantize(Xd, w.C, w.T, w.bits, w.group, w.iters, w.seed, nthreads=1)
-    oracle.dequantize(r["codes"][0], r["scales"][0], r["pi"][0], r["centroids"][0], w.bits,
-                      w.group)
-    one = time.perf_counter() - t0
-    n = int(max(1, min(w.H, cores, budget_s / max(one, 1e-3) * cores)))
-    n = min(n, cores)
-    Xs = w.make("cpu", tids=w.tids[:n])
-    Xsd = oracle.decode_input(Xs)
-    times = []
-    for _ in range(steps):
-        t0 = time.perf_counter()
-        r = oracle.quantize(Xsd, w.C, w.T, w.bits, w.group, w.iters, w.seed, nthreads=cores)
-        for h in range(n):
-            oracle.dequantize(r["codes"][h], r["scales"][h], r["pi"][h], r["centroids"][h],
-                              w.bits, w.group)
-        times.append(time.perf_counter() - t0)
-    dt = statistics.median(times)
-    return {"value": n * w.N / dt / 1e6, "unit": "Mtokens/s", "cores": min(cores, n),
-            "kind": "oracle",
-            "sample": "%d of %d tensors, all %d tokens each, quantize + dequantize, %d thread(s)"
-                      % (n, w.H, w.N, min(cores, n)),
+    r = oracle.quantize(Xd, w.C, w.T, w.bits, w.group, w.iters, w.seed, nthreads=n)
+    for h in range(n):
+        oracle.dequantize(r["codes"][h], r["scales"][h], r["pi"][h], r["centroids"][h],
+                          w.bits, w.group)
+    dt = time.perf_counter() - t0
+    return {"value": n * w.N / dt / 1e6, "unit": "Mtokens/s", "cores": n, "kind": "oracle",
+            "sample": "%d of %d tensors, all %d tokens each, quantize + dequantize, "
+                      "%d thread(s)" % (n, w.H, w.N, n),
             "seconds_per_step": dt}
 
 
@@ -173,24 +193,46 @@ def run_reference(args, w):
     rank, world = _dist()
     if rank != 0:
         return
-    cb = None
-    times = []
+    times, cb = [], None
     for i in range(args.warmup + args.steps):
-        c = cpu_baseline(w, steps=1, budget_s=args.ref_budget)
+        c = cpu_baseline(w)
         if i >= args.warmup:
             times.append(c["seconds_per_step"])
             cb = c
-    v = cb["value"]
+    dt = statistics.median(times)
+    v = cb["value"] * cb["seconds_per_step"] / dt
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "Mtokens/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": 1e3 * statistics.median(times), "higher_is_better": True,
+            "ms_per_step": 1e3 * dt, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": w.name, "tensors": w.H, "tokens": w.N, "C": w.C, "T": w.T,
-                       "bits": w.bits, "group": w.group, "iters": w.iters},
-            "cpu_baseline": {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")},
+            "config": _config(w, 1),
+            "cpu_baseline": {"value": v, "unit": "Mtokens/s", "cores": cb["cores"],
+                             "kind": "oracle", "sample": cb["sample"]},
             "e2e": {"value": v, "unit": "Mtokens/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
+
+
+def _config(w, world):
+    return {"workload": w.name, "tensors": w.H, "tokens": w.N, "C": w.C, "T": w.T,
+            "bits": w.bits, "group": w.group, "iters": w.iters,
+            "parallelism": "dp%d (tensors sharded, no exchange)" % world,
+            "l2": "flushed (%d MiB write) before every timed step" % (L2_FLUSH_BYTES >> 20)}
+
+
+def _event_ms(st, fn, reps, flush=None):
+    """Mean device time of fn() on stream st over reps runs, CUDA events on that stream."""
+    pairs = []
+    for k in range(reps):
+        if flush is not None:
+            flush.fill_(k & 0xFF)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(st)
+        fn()
+        b.record(st)
+        pairs.append((a, b))
+    torch.cuda.synchronize()
+    return sum(a.elapsed_time(b) for a, b in pairs) / reps
 
 
 def run_ours(args, w):
@@ -226,15 +268,14 @@ def run_ours(args, w):
     torch.cuda.synchronize()
     assert int(status.item()) == 0, "device status %#x" % int(status.item())
 
-    # --- timed steps: L2 flushed before each step, each step timed with CUDA events
+    # --- timed region: K steps of quantize + dequantize, L2 flushed before each step (the
+    # flush is outside the per-step events), each step timed with CUDA events
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
            torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    deq_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(args.steps)]
-    _barrier(world)
-    torch.cuda.synchronize()
-    wall0 = time.perf_counter()
     with ClockSampler(local) as clocks:
+        _barrier(world)
+        torch.cuda.synchronize()
+        wall0 = time.perf_counter()
         for k in range(args.steps):
             flush.fill_(k & 0xFF)
             ev[k][0].record(st)
@@ -242,22 +283,23 @@ def run_ours(args, w):
             ev[k][1].record(st)
             dequantize()
             ev[k][2].record(st)
-        # dequant alone with a cold L2, for its HBM roofline
-        for k in range(args.steps):
-            flush.fill_((k + 7) & 0xFF)
-            deq_ev[k][0].record(st)
-            dequantize()
-            deq_ev[k][1].record(st)
         torch.cuda.synchronize()
-    wall = time.perf_counter() - wall0
-    _barrier(world)
+        _barrier(world)
+        wall = time.perf_counter() - wall0
     q_ms = [a.elapsed_time(b) for a, b, _ in ev]
     step_ms = [a.elapsed_time(c) for a, _, c in ev]
-    d_ms = [a.elapsed_time(b) for a, b in deq_ev]
     step_ms_avg = _max_over_ranks(sum(step_ms) / len(step_ms), world)
     q_ms_avg = _max_over_ranks(sum(q_ms) / len(q_ms), world)
-    d_ms_avg = _max_over_ranks(sum(d_ms) / len(d_ms), world)
     tokens_all = w.H * N  # whole job: every rank's tensors
+
+    # --- the dominant kernel and the dequant, each timed alone on the same data
+    reps = max(3, args.steps)
+    d_ms = _max_over_ranks(_event_ms(st, dequantize, reps, flush), world)
+    r_ms = _max_over_ranks(_event_ms(st, lambda: api.reassign(X, out, w.iters, ws, w.seed,
+                                                              status=status,
+                                                              tensor_id_base=lo), reps), world)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0, "device status %#x" % int(status.item())
 
     # --- end to end through the same API with host buffers (pinned), copies timed
     Xh = X.cpu().pin_memory()
@@ -265,28 +307,26 @@ def run_ours(args, w):
                               pin_memory=True) for k in ("codes", "scales", "pi", "centroids")}
     h2d = Xh.numel() * Xh.element_size()
     d2h = sum(t.numel() * t.element_size() for t in cache_h.values())
-    e2e_ms = []
-    for k in range(max(2, args.steps // 2)):
-        flush.fill_(k & 0xFF)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(st)
+
+    def e2e_step():
         X.copy_(Xh, non_blocking=True)
         quantize()
         dequantize()
         for key, t in cache_h.items():
             t.copy_(getattr(out, key), non_blocking=True)
-        e1.record(st)
-        torch.cuda.synchronize()
-        e2e_ms.append(e0.elapsed_time(e1))
-    e2e_avg = _max_over_ranks(sum(e2e_ms) / len(e2e_ms), world)
+
+    e2e_ms = _max_over_ranks(_event_ms(st, e2e_step, max(2, args.steps // 2), flush), world)
 
     hbm, tf_burst, tf_sus, src = _peaks()
-    dbytes = dequant_bytes(w.H, N, w.C, w.T, w.bits, w.group) / world * world
-    dq_gbs = dequant_bytes(H, N, w.C, w.T, w.bits, w.group) / (d_ms_avg * 1e-3) / 1e9
-    useful_flops = 2.0 * H * N * w.C * 128 * w.iters * w.T
-    n_launch_q = 1 + w.T * (4 + 3 * w.iters) + 1
+    dq_gbs = dequant_bytes(H, N, w.C, w.T, w.bits, w.group) / (d_ms * 1e-3) / 1e9
+    a_flops = assign_flops(H, N, w.C)
+    a_tflops = a_flops / (r_ms * 1e-3) / 1e12
+    traffic = None
+    if (ASSIGN_TRAFFIC["bytes"] and w.name == ASSIGN_TRAFFIC["workload"] and world == 1 and
+            _sources_sha256(ASSIGN_SOURCES) == ASSIGN_TRAFFIC["sources_sha256"]):
+        traffic = ASSIGN_TRAFFIC["bytes"]
+    useful_flops = assign_flops(H, N, w.C) * w.iters * w.T
     if rank == 0:
-        clk = clocks.summary()
         line = {
             "metric": METRIC,
             "value": tokens_all / (step_ms_avg * 1e-3) / 1e6,
@@ -294,24 +334,25 @@ def run_ours(args, w):
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": step_ms_avg, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": w.name, "tensors": w.H, "tokens": N, "C": w.C, "T": w.T,
-                       "bits": w.bits, "group": w.group, "iters": w.iters,
-                       "parallelism": "dp%d (tensors sharded, no exchange)" % world,
-                       "l2": "flushed (%d MiB write) before every timed step" % (L2_FLUSH_BYTES >> 20)},
+            "config": _config(w, world),
+            "roofline": {"kernel": "k_assign", "bound": "tensor", "achieved": a_tflops,
+                         "peak": tf_burst, "unit": "TFLOP/s", "frac": a_tflops / tf_burst,
+                         "traffic": traffic, "peak_source": src + " bf16 burst",
+                         "flops_per_launch": a_flops, "ms_per_launch": r_ms,
+                         "timed_as": "qvg_reassign (centroid planes + k_assign + k_refine)"},
             "quantize": {"ms": q_ms_avg, "mtokens_s": tokens_all / (q_ms_avg * 1e-3) / 1e6,
                          "useful_tflops": useful_flops * world / (q_ms_avg * 1e-3) / 1e12},
-            "dequant": {"ms": d_ms_avg, "gbs": dq_gbs, "pct_hbm": 100.0 * dq_gbs / hbm,
-                        "bytes": dbytes},
-            "roofline_dequant": {"bound": "hbm", "achieved": dq_gbs, "peak": hbm, "unit": "GB/s",
-                                 "frac": dq_gbs / hbm, "traffic": None, "peak_source": src},
-            "e2e": {"value": tokens_all / (e2e_avg * 1e-3) / 1e6, "unit": "Mtokens/s",
-                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms": e2e_avg},
-            "gpu_launches": args.steps * (n_launch_q + 1) + args.steps,
+            "dequant": {"ms": d_ms, "gbs": dq_gbs, "pct_hbm": 100.0 * dq_gbs / hbm,
+                        "bytes": dequant_bytes(H, N, w.C, w.T, w.bits, w.group),
+                        "peak_gbs": hbm, "peak_source": src},
+            "e2e": {"value": tokens_all / (e2e_ms * 1e-3) / 1e6, "unit": "Mtokens/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms": e2e_ms},
+            "gpu_launches": args.steps * launches_per_step(w),
             "wall_s_timed_region": wall,
-            "clocks": clk,
+            "clocks": clocks.summary(),
         }
         if not args.no_cpu_baseline and world == 1:
-            cb = cpu_baseline(w, budget_s=args.ref_budget)
+            cb = cpu_baseline(w)
             line["cpu_baseline"] = {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")}
         print(json.dumps(line), flush=True)
 
@@ -324,7 +365,6 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--ref-budget", type=float, default=20.0)
     args = ap.parse_args()
     w = synth.workload(args.workload)
     if args.impl == "reference":
