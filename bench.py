@@ -144,11 +144,10 @@ def assign_flops(H, N, C):
 
 def launches_per_step(w):
     """Kernels of libqvg launched by one quantize + dequantize of the workload (cold start):
-    init_indices, then per stage init_centroids, centre, prep, [pad_cn], centroid_planes and
-    per Lloyd round assign, refine, sort hist / scan / scatter, chunk sums, finalize; then
-    encode; then the fused dequant."""
-    cpad = 16 if w.C <= 16 else (w.C + 15) // 16 * 16
-    per_stage = 4 + (1 if cpad > w.C else 0) + 7 * w.iters
+    init_indices, then per stage init_centroids, centre, prep, centroid_planes and per Lloyd
+    round assign, refine, sort hist / scan / scatter, chunk sums, finalize; then encode; then
+    the fused dequant."""
+    per_stage = 4 + 7 * w.iters
     return 1 + w.T * per_stage + 1 + 1
 
 

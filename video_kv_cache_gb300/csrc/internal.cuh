@@ -3,14 +3,13 @@
 // Numerics used on the device (the oracle works in fp64; these are the GPU's choices):
 //   * Residuals r = x - C^(1)[pi^(1)] - ... are formed with an error-free TwoSum chain and
 //     rounded once to fp32, so r is the fp32 value nearest the exact residual.
-//   * Centroid sums are exact: every residual is turned into a 64-bit fixed-point integer
-//     with a per-(tensor, stage) power-of-two scale 2^Q chosen from max|r| and N, then added
-//     with integer atomics.  The result does not depend on summation order, and the mean
-//     is the exact sum divided by the count, rounded once to fp32.
-//   * Distances for the assignment come from a tensor-core GEMM on a two-term bf16 split of
-//     the centred operands (hi*hi + hi*lo + lo*hi, fp32 accumulate).  Every cluster whose
-//     GEMM score lies within a rigorous error margin of the best one is re-scored with a
-//     direct fp32 sum of squared differences, ties going to the lowest cluster index.
+//   * Centroid sums run in a fixed order over the tokens grouped by cluster (a stable
+//     counting sort), with TwoSum-compensated fp32 accumulation; the mean is rounded once
+//     to fp32.  Repeated runs give identical bits.
+//   * Distances for the assignment come from a tensor-core GEMM on fp16 copies of the
+//     centred operands (fp32 accumulate).  Every cluster whose GEMM score lies within a
+//     rigorous bound on the GEMM's error of the best one is re-scored with a direct fp32
+//     sum of squared differences, ties going to the lowest cluster index.
 #pragma once
 
 #include <cuda.h>
@@ -28,6 +27,12 @@ namespace qvg {
 constexpr int kD = 128;            // channels per token
 constexpr int kMaxT = 8;           // most smoothing stages
 constexpr int kMaxC = 256;         // most clusters (pi is uint8)
+// fp16 planes of the centroids in the assignment GEMM: 1 (one product per score) or 2
+// (hi + lo, two products, half the error bound)
+constexpr int kBPlanes = 2;
+// Largest |component| that the fp16 GEMM operands are trusted with; a residual row or a
+// centroid set with a larger norm sends every cluster of the row to the exact re-scoring.
+constexpr float kFp16Safe = 60000.f;
 
 enum : int { DT_F16 = 0, DT_BF16 = 1, DT_F32 = 2 };
 
@@ -35,7 +40,7 @@ enum : int { DT_F16 = 0, DT_BF16 = 1, DT_F32 = 2 };
 struct QPlan {
     int H;
     int64_t N;
-    int C, Cpad, T, bits, group, iters, in_dtype;
+    int C, Cpad, T, bits, group, iters, in_dtype;  // Cpad: C rounded up to a multiple of 32
     int64_t x_stride;      // elements between tensors of X
     int64_t cap, tok_off;  // token slots per tensor in codes/scales/pi, first slot written
     int64_t cent_tstride;  // floats between tensors in the centroid tables
@@ -47,9 +52,11 @@ struct QPlan {
     int64_t warm_stride;
     // workspace
     float *R32;            // [H][N][128] residual R^(t-1), stages t >= 2
-    __nv_bfloat16 *A;      // [H][2][N][128] bf16 hi / lo planes of the centred residual
-    float *rnorm;          // [H][N] norm of the centred residual row
-    __nv_bfloat16 *B;      // [H][2][Cpad][128] bf16 hi / lo planes of the centred centroids
+    __half *A;             // [H][N][128] fp16 copy of the centred residual r - mu
+    float *rnorm;          // [H][N] norm of the centred residual row (fp32)
+    float *dnorm;          // [H][N] norm of its fp16 rounding error, ||fp16(r - mu) - (r - mu)||
+    __half *B;             // [H][kBPlanes][Cpad][128] fp16 planes of the centred centroids
+                           // c - mu: plane 0 = fp16(c - mu), plane 1 = fp16 of its remainder
     float *cn;             // [H][Cpad] squared norm of the centred centroids
     float *mu;             // [H][128] centring vector of the current stage
     int *counts;           // [H][C] cluster sizes of the current assignment
@@ -61,7 +68,6 @@ struct QPlan {
                            // chunk boundary: [0] the run at the chunk start, [1] the last run
     float *wsum;           // [H][C][2][128] (sum, error) of clusters inside one chunk
     int nsb, nchunk;       // token blocks of the sort, 64-position chunks per tensor
-    unsigned *maxabs;      // [H] max |r| of the current stage, as float bits
     int *init_idx;         // [H][T][C] cold-start rows
     unsigned *stats;       // [16] counters (see kStat*)
     int *rq_count;         // number of queued near-tie re-scoring requests
@@ -126,40 +132,6 @@ __device__ __forceinline__ void load_f8(const float *p, float v[8]) {
     float4 b = __ldg(reinterpret_cast<const float4 *>(p) + 1);
     v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
     v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
-}
-
-// Fixed-point exponent for sums of n <= N values bounded by the float whose bits are
-// `maxabs_bits`: |sum * 2^Q| < 2^62.
-__device__ __forceinline__ int fixed_q(unsigned maxabs_bits, int64_t N) {
-    unsigned eb = (maxabs_bits >> 23) & 0xFFu;
-    if (maxabs_bits == 0u || eb == 0xFFu) return 0;
-    int e = (int)(eb < 1u ? 1u : eb) - 126;  // maxabs < 2^e
-    int L = 64 - __clzll((unsigned long long)N);  // N < 2^L
-    int q = 62 - L - e;
-    return q < -100 ? -100 : (q > 120 ? 120 : q);
-}
-
-__device__ __forceinline__ float pow2f(int q) { return __int_as_float((q + 127) << 23); }
-
-// x * 2^q rounded to nearest (ties to even) as a 64-bit integer, for |x * 2^q| < 2^62.
-// Integer-only: a float -> int64 conversion instruction would run on the FP64 pipe, which
-// is narrow on this GPU.
-__device__ __forceinline__ long long f2fix(float x, int q) {
-    const uint32_t b = __float_as_uint(x);
-    const int e = (int)((b >> 23) & 0xFFu);
-    const uint32_t m = (b & 0x7FFFFFu) | (e ? 0x800000u : 0u);
-    const int sh = (e ? e : 1) - 150 + q;  // |x| = m * 2^(e - 150) for normals
-    unsigned long long v;
-    if (sh >= 0) {
-        v = (unsigned long long)m << (sh < 63 ? sh : 63);
-    } else {
-        const int s = -sh < 31 ? -sh : 31;
-        const uint32_t kept = m >> s;
-        const uint32_t rem = m - (kept << s);
-        const uint32_t half = 1u << (s - 1);
-        v = kept + ((rem > half) || (rem == half && (kept & 1u)) ? 1u : 0u);
-    }
-    return (b >> 31) ? -(long long)v : (long long)v;
 }
 
 __device__ __forceinline__ void or_status(uint32_t *status, uint32_t bits) {

@@ -6,22 +6,40 @@
 //
 // Since ||R_i - C_j||^2 = ||R_i||^2 - 2 R_i.C_j + ||C_j||^2, the argmin only needs the
 // score s_ij = ||C_j||^2 - 2 R_i.C_j, and R.C^T is a [N x 128] x [128 x C] GEMM.  Both
-// operands are first shifted by a common centring vector mu (distances do not change) and
-// split into two bf16 terms, x = hi + lo.  The GEMM accumulates hi.hi + hi.lo + lo.hi in
-// fp32 TMEM, which carries ~16 significant bits of each operand.  The epilogue then finds
-// the best score; every cluster whose score is within a bound on the GEMM's error of the
-// best one is re-scored exactly (direct fp32 sum of squared differences on the fp32
-// residual and centroid), so the chosen index is that of the true nearest centroid up to
-// fp32 rounding.
+// operands are first shifted by a common centring vector mu (distances do not change):
+// r = R_i - mu and c = C_j - mu.  The GEMM multiplies fp16(r) by the fp16 planes of c
+// (kBPlanes = 1: fp16(c); 2: fp16(c) + fp16 of its remainder) with fp32 accumulation in
+// TMEM, and the epilogue forms s = ||c||^2 - 2 acc with ||c||^2 computed in fp32.
 //
-// Kernel structure (one persistent CTA per SM, 192 threads):
-//   warp 0   TMA producer: B (centroid planes, C x 128 x 2 planes) once per tensor, A
-//            (residual planes of 128 tokens, four 16 KB blocks of 64 channels per tile)
+// Error bound.  Let u = 2^-11 (fp16 unit roundoff) and e = 2^-25 (half the smallest fp16
+// subnormal), so |fp16(x) - x| <= u|x| + e.  The residual's rounding error is measured,
+// not bounded: dn = ||fp16(r) - r|| is computed exactly by the kernel that writes fp16(r)
+// (typically about 0.6 u ||r||).  The centroid side is off by |c^ - c| <= u|c| + e with one
+// plane and u^2|c| + 2e with two.  Over d = 128 channels, by Cauchy-Schwarz,
+//   |acc - r.c| <= dn ||c^|| + ||r|| ||c^ - c|| + (accumulation error),
+// and the fp32 accumulation of at most 256 exact products adds less than
+// 2^-15 ||r^|| ||c^||.  Collecting terms, with rn = ||r|| and cmax = max_j ||c_j||:
+//   |acc - r.c| <= 1.004 dn cmax + k rn cmax + 2^-20 (rn + dn),
+// k = 1.066 * 2^-11 (one plane) or 1.012 * 2^-15 (two planes).  ||c||^2 in fp32 and the
+// score's own rounding add at most 1.07 * 2^-17 cmax^2, so every score is within E of its
+// exact value, E = 2 |acc - r.c| bound + 1.07 * 2^-17 cmax^2, and any cluster whose score
+// is within 2E of the best score may be the true nearest one.  Those are re-scored exactly
+// (direct fp32 sum of squared differences on the fp32 residual and centroid, k_refine), so
+// the chosen index is that of the true nearest centroid up to fp32 rounding.  A row with
+// ||r|| >= 60000, or a centroid set with cmax >= 60000, could overflow fp16: all of its
+// clusters are re-scored.
+//
+// Kernel structure (one persistent CTA per SM, 576 threads):
+//   warp 0   TMA producer: B (kBPlanes fp16 planes of C x 128) once per tensor, then A
+//            (128 tokens x 128 channels fp16 per tile, as two 16 KB blocks of 64 channels)
 //            into a ring of smem slots.
-//   warp 1   TMEM allocator and MMA issuer (one thread): 3 x 8 tcgen05.mma of
+//   warp 1   TMEM allocator and MMA issuer (one thread): 2 x kBPlanes x 4 tcgen05.mma of
 //            M=128, N=Cpad, K=16 per tile into one of two TMEM accumulators.
-//   warps 2-5 epilogue: warp w reads TMEM lanes 32*(w%4).. (one token row per thread),
-//            computes the argmin, releases the accumulator, re-scores near ties, writes pi.
+//   warps 2-17 epilogue, two groups of 8 warps taking alternate tiles: a warp reads 32
+//            TMEM lanes (one token row per thread) and half of the columns; the pair of
+//            warps on the same rows merges its best / second-best scores, re-reads only
+//            the 32-column chunks that can hold a near tie, releases the accumulator,
+//            writes pi and queues near ties for k_refine.
 // Every mbarrier wait is bounded; on timeout the kernel sets QVG_DEV_TIMEOUT, stops, waits
 // for its own copies and MMAs, frees TMEM and returns.
 #include <cuda.h>
@@ -37,8 +55,14 @@ namespace {
 constexpr int kEpiGroups = 2;                      // epilogue groups of 8 warps
 constexpr int kThreads = 64 + kEpiGroups * 8 * 32;  // producer, MMA, 16 epilogue warps
 constexpr int kTileM = 128;
-constexpr uint32_t kKBlockBytes = kTileM * 64 * 2;  // 16 KB: 64 channels of that plane
+constexpr uint32_t kKBlockBytes = kTileM * 64 * 2;  // 16 KB: 64 fp16 channels of 128 rows
+constexpr int kABlocks = 2;                           // A blocks per tile (128 channels)
 constexpr uint32_t kSpinLimit = 1u << 22;
+constexpr uint32_t kSuspendHintNs = 20000;        // longest single suspension in a wait
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // a pipeline wait gives up after 2 s
+// coefficients of the bound on |acc - r.c| (see the error bound above)
+constexpr float kDnRel = 0x1.01p0f;
+constexpr float kRnRel = kBPlanes == 1 ? 0x1.11p-11f : 0x1.03p-15f;
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -66,13 +90,36 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
     return ok != 0u;
 }
 
-// Bounded wait on a phase.  Gives up when another role already gave up, or after the
-// spin limit (then it raises the abort flag itself).
+// try_wait that may suspend the thread until the phase completes, for at most the hinted
+// time (the hardware wakes it as soon as the phase completes).
+__device__ __forceinline__ bool mbar_try_suspend(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(kSuspendHintNs)
+        : "memory");
+    return ok != 0u;
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Bounded wait on a phase.  Gives up when another role already gave up, or after
+// kSpinLimit tries or kWaitLimitNs of wall time, whichever comes first (then it raises the
+// abort flag itself).
 __device__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag) {
+    if (mbar_try(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
     for (uint32_t n = 0; n < kSpinLimit; n++) {
-        if (mbar_try(bar, parity)) return true;
+        if (mbar_try_suspend(bar, parity)) return true;
         if (*abort_flag) return false;
-        if (n >= 1024) __nanosleep(128);
+        if ((n & 15u) == 15u && global_ns() - t0 > kWaitLimitNs) break;
     }
     *abort_flag = 1;
     return false;
@@ -134,7 +181,7 @@ __device__ __forceinline__ void tc_ld32(uint32_t taddr, float v[32]) {
 }
 
 // Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of 128 bytes,
-// 8-row groups 1024 bytes apart (the layout a TMA box of 64 bf16 x rows writes with
+// 8-row groups 1024 bytes apart (the layout a TMA box of 64 fp16 x rows writes with
 // CU_TENSOR_MAP_SWIZZLE_128B).
 __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
     return (uint64_t)((saddr & 0x3FFFFu) >> 4)   // start address
@@ -144,10 +191,10 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
            | ((uint64_t)2 << 61);                // 128-byte swizzle
 }
 
-// Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, both K-major.
+// Instruction descriptor, kind::f16: fp32 accumulator (bits 4-5 = 1), fp16 A and B (bits
+// 7-9 and 10-12 = 0), both K-major, N >> 3 at bit 17, M >> 4 at bit 24.
 __device__ __forceinline__ uint32_t make_idesc(int n) {
-    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) |
-           ((uint32_t)(kTileM >> 4) << 24);
+    return (1u << 4) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(kTileM >> 4) << 24);
 }
 
 }  // namespace
@@ -162,7 +209,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int Cpad = p.Cpad;
     const uint32_t bsub = (uint32_t)Cpad * 128u;  // one (plane, 64-channel block) of B
     unsigned char *sB = sm;
-    unsigned char *sA = sm + 4 * bsub;
+    unsigned char *sA = sm + 2 * kBPlanes * bsub;
     uint64_t *bars = reinterpret_cast<uint64_t *>(sA + (size_t)nslots * kKBlockBytes);
     uint64_t *a_full = bars, *a_empty = bars + nslots;
     uint64_t *b_full = bars + 2 * nslots, *b_empty = b_full + 1;
@@ -173,9 +220,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // 16-byte aligned: the epilogue reads it with 16-byte vector loads
     float *cn_s = reinterpret_cast<float *>(
         (reinterpret_cast<uintptr_t>(tmem_slot + 4) + 15) & ~static_cast<uintptr_t>(15));  // [kEpiGroups][Cpad]
-    float *x_best = cn_s + kEpiGroups * Cpad;                     // [kEpiGroups][128]
-    float *x_second = x_best + kEpiGroups * kTileM;
-    int *x_idx = reinterpret_cast<int *>(x_second + kEpiGroups * kTileM);
+    float *x_best = cn_s + kEpiGroups * Cpad;     // [kEpiGroups][2 halves][128 rows]
+    float *x_second = x_best + kEpiGroups * 2 * kTileM;
+    int *x_idx = reinterpret_cast<int *>(x_second + kEpiGroups * 2 * kTileM);
+    uint32_t *x_cand = reinterpret_cast<uint32_t *>(x_idx + kEpiGroups * 2 * kTileM);  // [kEpiGroups][128][4]
+
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t total = (int64_t)p.H * tiles_per_tensor;
@@ -221,25 +270,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int m0 = (int)(tile - (int64_t)h * tiles_per_tensor) * kTileM;
                 if (h != cur_h) {
                     if (nb > 0 && !mbar_wait(smem_u32(b_empty), (nb - 1) & 1, abort_flag)) break;
-                    mbar_expect_tx(smem_u32(b_full), 4 * bsub);
-                    for (int pl = 0; pl < 2; pl++)
+                    mbar_expect_tx(smem_u32(b_full), 2 * kBPlanes * bsub);
+                    for (int pl = 0; pl < kBPlanes; pl++)
                         for (int kb = 0; kb < 2; kb++)
                             tma_load_3d(smem_u32(sB + (pl * 2 + kb) * bsub), &tmB, kb * 64, 0,
-                                        2 * h + pl, smem_u32(b_full));
+                                        kBPlanes * h + pl, smem_u32(b_full));
                     nb++;
                     cur_h = h;
                 }
-                // four 16 KB loads per tile: hi plane channels 0-63, 64-127, then lo plane
+                // two 16 KB loads per tile: channels 0-63, then 64-127
                 bool ok = true;
-                for (int k = 0; k < 4; k++) {
-                    const uint32_t q = 4u * (uint32_t)lt + k, s = q % nslots, ph = (q / nslots) & 1u;
+                for (int k = 0; k < kABlocks; k++) {
+                    const uint32_t q = kABlocks * (uint32_t)lt + k, s = q % nslots,
+                                   ph = (q / nslots) & 1u;
                     if (!mbar_wait(smem_u32(a_empty + s), ph ^ 1u, abort_flag)) {
                         ok = false;
                         break;
                     }
                     mbar_expect_tx(smem_u32(a_full + s), kKBlockBytes);
-                    tma_load_3d(smem_u32(sA + s * kKBlockBytes), &tmA, (k & 1) * 64, m0,
-                                2 * h + (k >> 1), smem_u32(a_full + s));
+                    tma_load_3d(smem_u32(sA + s * kKBlockBytes), &tmA, k * 64, m0, h,
+                                smem_u32(a_full + s));
                     issued = q + 1;
                 }
                 if (!ok) break;
@@ -271,23 +321,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!mbar_wait(smem_u32(acc_empty + grp), (use & 1u) ^ 1u, abort_flag)) break;
                 tc_fence_after();
                 const uint32_t d = tmem + buf * acc_stride;
-                // k = 0, 1: hi plane blocks against B hi and B lo; k = 2, 3: lo plane against
-                // B hi.  Each A block's slot is released as soon as its MMAs complete.
+                // A block k (channels 64k..64k+63) against every B plane of the same
+                // channels; each A block's slot is released as soon as its MMAs complete.
                 bool ok = true;
-                for (int k = 0; k < 4 && ok; k++) {
-                    const uint32_t q = 4u * (uint32_t)lt + k, s = q % nslots;
+                for (int k = 0; k < kABlocks && ok; k++) {
+                    const uint32_t q = kABlocks * (uint32_t)lt + k, s = q % nslots;
                     if (!mbar_wait(smem_u32(a_full + s), (q / nslots) & 1u, abort_flag)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
                     const uint64_t dA = sw128_desc(smem_u32(sA + s * kKBlockBytes));
-                    const int kb = k & 1;
-                    const int nbp = k < 2 ? 2 : 1;
-                    for (int bp = 0; bp < nbp; bp++)
+                    for (int bp = 0; bp < kBPlanes; bp++)
                         for (int kk = 0; kk < 4; kk++)
                             tc_mma(d, dA + (uint64_t)((kk * 32) >> 4),
-                                   dB0 + (uint64_t)(((bp * 2 + kb) * bsub + kk * 32) >> 4), idesc,
+                                   dB0 + (uint64_t)(((bp * 2 + k) * bsub + kk * 32) >> 4), idesc,
                                    (k | bp | kk) != 0);
                     tc_commit(smem_u32(a_empty + s));
                 }
@@ -308,14 +356,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int grp = e >> 3, half = (e >> 2) & 1, quarter = warp & 3;
         const int row = quarter * 32 + lane;
         const int C = p.C;
-        const int nchunks = (Cpad + 31) >> 5;
+        const int nchunks = Cpad >> 5;  // Cpad is a multiple of 32
         const int split = (nchunks + 1) >> 1;
         const int ch_lo = half ? split : 0, ch_hi = half ? nchunks : split;
         const int pair_bar = 1 + grp * 4 + quarter;  // named barrier of the two warps of a row block
         const int grp_bar = 9 + grp;                  // named barrier of the group's 8 warps
         float *cns = cn_s + grp * Cpad;
-        float *xb = x_best + grp * kTileM, *xs = x_second + grp * kTileM;
-        int *xi = x_idx + grp * kTileM;
+        float *xb = x_best + grp * 2 * kTileM, *xs = x_second + grp * 2 * kTileM;
+        int *xi = x_idx + grp * 2 * kTileM;
+        uint32_t *xc = x_cand + grp * 4 * kTileM;
         int cur_h = -1;
         float cmax = 0.f, cmax2 = 0.f;
         unsigned n_ref_rows = 0;
@@ -324,7 +373,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int64_t i = (tile - (int64_t)h * tiles_per_tensor) * kTileM + row;
             const bool valid = i < p.N;
             const uint32_t buf = (uint32_t)grp, use = (uint32_t)lt >> 1;
-            const float rn = (half == 0 && valid) ? __ldg(p.rnorm + (int64_t)h * p.N + i) : 0.f;
+            const float rn = valid ? __ldg(p.rnorm + (int64_t)h * p.N + i) : 0.f;
+            const float dn = valid ? __ldg(p.dnorm + (int64_t)h * p.N + i) : 0.f;
             const bool ok = mbar_wait(smem_u32(acc_full + grp), use & 1u, abort_flag);
             // every warp of the group takes the same branch after the bounded wait; this is
             // also the group barrier that ends the previous tile's reads of ||c||^2
@@ -337,10 +387,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 : "memory");
             if (any_fail) break;
             if (h != cur_h) {
-                // the group's private copy of ||c||^2 for this tensor
+                // the group's private copy of ||c||^2 for this tensor; +inf in the padded
+                // columns (their B rows are zero-filled by TMA), whose scores never win
                 cur_h = h;
                 const float *cn = p.cn + (int64_t)h * Cpad;
-                for (int j = e * 32 + lane - grp * 256; j < Cpad; j += 256) cns[j] = __ldg(cn + j);
+                for (int j = e * 32 + lane - grp * 256; j < Cpad; j += 256)
+                    cns[j] = j < C ? __ldg(cn + j) : INFINITY;
                 asm volatile("bar.sync %0, 256;" ::"r"(grp_bar) : "memory");
                 cmax2 = 0.f;
                 for (int j = lane; j < C; j += 32) cmax2 = fmaxf(cmax2, cns[j]);
@@ -351,75 +403,129 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc_fence_after();
             const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + buf * acc_stride;
+            // Pass 1 over this warp's chunks of 32 columns: best score, second best, lowest
+            // index of the best, and each chunk's minimum (for the candidate pass).  Chunks
+            // are visited in increasing order and a chunk's best only replaces a strictly
+            // larger one, so ties keep the lowest index.
             float best = INFINITY, second = INFINITY;
             int bj = 0;
+            float cmin0 = INFINITY, cmin1 = INFINITY, cmin2 = INFINITY, cmin3 = INFINITY;
+            // one copy of the chunk body (a rolled loop keeps the kernel in the instruction
+            // cache); the chunk minima stay in named registers
 #pragma unroll 1
-            for (int cb = ch_lo; cb < ch_hi; cb++) {
+            for (int c = 0; c < ch_hi - ch_lo; c++) {
+                const int cb = ch_lo + c;
                 float v[32];
                 tc_ld32(taddr + cb * 32, v);
+                float b1 = INFINITY, s1 = INFINITY;
+                int j1 = 0;
 #pragma unroll
                 for (int q = 0; q < 32; q += 4) {
                     const float4 c4 = *reinterpret_cast<const float4 *>(cns + cb * 32 + q);
                     const float cc[4] = {c4.x, c4.y, c4.z, c4.w};
 #pragma unroll
                     for (int u = 0; u < 4; u++) {
-                        const int j = cb * 32 + q + u;
-                        const float s = j < C ? __fmaf_rn(-2.f, v[q + u], cc[u]) : INFINITY;
-                        second = fminf(second, fmaxf(s, best));
-                        if (s < best) bj = j;
-                        best = fminf(best, s);
+                        const float sc = __fmaf_rn(-2.f, v[q + u], cc[u]);
+                        s1 = fminf(s1, fmaxf(sc, b1));
+                        if (sc < b1) j1 = cb * 32 + q + u;
+                        b1 = fminf(b1, sc);
                     }
                 }
+                cmin0 = c == 0 ? b1 : cmin0;
+                cmin1 = c == 1 ? b1 : cmin1;
+                cmin2 = c == 2 ? b1 : cmin2;
+                cmin3 = c == 3 ? b1 : cmin3;
+                second = fminf(second, fminf(s1, fmaxf(best, b1)));
+                if (b1 < best) bj = j1;
+                best = fminf(best, b1);
             }
-            if (half == 1) {
-                xb[row] = best;
-                xs[row] = second;
-                xi[row] = bj;
-            }
+            // Both warps of the pair merge the two column halves the same way; the lower
+            // half's index wins ties.
+            xb[half * kTileM + row] = best;
+            xs[half * kTileM + row] = second;
+            xi[half * kTileM + row] = bj;
             asm volatile("bar.sync %0, 64;" ::"r"(pair_bar) : "memory");
-            if (half == 0) {
-                const float ob = xb[row], os = xs[row];
-                const int oj = xi[row];
+            {
+                const float ob = xb[(half ^ 1) * kTileM + row], os = xs[(half ^ 1) * kTileM + row];
+                const int oj = xi[(half ^ 1) * kTileM + row];
                 second = fminf(fminf(second, os), fmaxf(best, ob));
-                if (ob < best) bj = oj;  // the lower half wins ties: lowest cluster index
+                if (half == 0 ? ob < best : ob <= best) bj = oj;
                 best = fminf(best, ob);
             }
-            // |error of a score| <= 2^-12 ||r|| ||c_j|| + 2^-17 ||c_j||^2; two scores differ
-            // from their exact values by at most twice that.
-            const float margin = 2.f * (ldexpf(rn * cmax, -12) + ldexpf(cmax2, -17)) + 1e-30f;
-            const float lim = best + margin;
-            const bool need = half == 0 && valid && second <= lim;
-            uint32_t cand[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
-            if (half == 0 && __any_sync(0xffffffffu, need)) {
+            // Every cluster whose score is within twice the error bound of the best may be
+            // the nearest one (bound in the file header).
+            const float err = 2.f * (kDnRel * dn * cmax + kRnRel * rn * cmax +
+                                     0x1p-20f * (rn + dn)) +
+                              0x1.1p-17f * cmax2;
+            const bool trusted = rn < kFp16Safe && cmax < kFp16Safe;
+            const float lim = best + (trusted ? 2.f * err + 1e-30f : INFINITY);
+            const bool need = valid && second <= lim;
+            const bool any_need = __any_sync(0xffffffffu, need);  // the same in both warps
+            // Candidate pass: only chunks whose minimum is within the limit for some row.
+            uint32_t cand0 = 0u, cand1 = 0u, cand2 = 0u, cand3 = 0u;
+            if (any_need) {
+#pragma unroll 1
+                for (int c = 0; c < ch_hi - ch_lo; c++) {
+                    const float cm = c == 0 ? cmin0 : c == 1 ? cmin1 : c == 2 ? cmin2 : cmin3;
+                    if (!__any_sync(0xffffffffu, need && cm <= lim)) continue;
+                    const int cb = ch_lo + c;
+                    float v[32];
+                    tc_ld32(taddr + cb * 32, v);
+                    uint32_t w = 0u;
 #pragma unroll
-                for (int cb = 0; cb < 8; cb++) {
-                    if (cb < nchunks) {
-                        float v[32];
-                        tc_ld32(taddr + cb * 32, v);
+                    for (int q = 0; q < 32; q += 4) {
+                        const float4 c4 = *reinterpret_cast<const float4 *>(cns + cb * 32 + q);
+                        const float cc[4] = {c4.x, c4.y, c4.z, c4.w};
 #pragma unroll
-                        for (int q = 0; q < 32; q++) {
-                            const int j = cb * 32 + q;
-                            const float s = __fmaf_rn(-2.f, v[q], cns[j]);
-                            if (need && j < C && s <= lim) cand[cb] |= 1u << q;
+                        for (int u = 0; u < 4; u++) {
+                            const float sc = __fmaf_rn(-2.f, v[q + u], cc[u]);
+                            if (sc <= lim && cb * 32 + q + u < C) w |= 1u << (q + u);
                         }
                     }
+                    if (!need) w = 0u;
+                    cand0 = c == 0 ? w : cand0;
+                    cand1 = c == 1 ? w : cand1;
+                    cand2 = c == 2 ? w : cand2;
+                    cand3 = c == 3 ? w : cand3;
                 }
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(acc_empty + grp));
-            if (half == 0 && valid) {
-                p.pi[(int64_t)(h * p.T + t - 1) * p.cap + p.tok_off + i] = (uint8_t)bj;
-                if (need) {
-                    n_ref_rows++;
-                    const int slot = atomicAdd(p.rq_count, 1);
-                    RefineReq *rq = p.rq + slot;
-                    rq->h = h;
-                    rq->i = (int)i;
+            if (any_need) {
+                // the upper half hands its candidate words to the lower half, which queues
+                // the rows (one atomic per warp)
+                if (half == 1)
+                    *reinterpret_cast<uint4 *>(xc + row * 4) = make_uint4(cand0, cand1, cand2, cand3);
+                asm volatile("bar.sync %0, 64;" ::"r"(pair_bar) : "memory");
+                if (half == 0) {
+                    const unsigned m = __ballot_sync(0xffffffffu, need);
+                    int base = 0;
+                    if (lane == 0) base = atomicAdd(p.rq_count, __popc(m));
+                    base = __shfl_sync(0xffffffffu, base, 0);
+                    if (need) {
+                        n_ref_rows++;
+                        RefineReq *rq = p.rq + base + __popc(m & ((1u << lane) - 1u));
+                        rq->h = h;
+                        rq->i = (int)i;
+                        // chunk c belongs to the lower half when c < split
+                        const uint4 up = *reinterpret_cast<const uint4 *>(xc + row * 4);
+                        const uint32_t lo_w[4] = {cand0, cand1, cand2, cand3};
+                        const uint32_t up_w[4] = {up.x, up.y, up.z, up.w};
 #pragma unroll
-                    for (int cb = 0; cb < 8; cb++) rq->cand[cb] = cand[cb];
+                        for (int c = 0; c < 8; c++) {
+                            uint32_t w = 0u;
+#pragma unroll
+                            for (int k = 0; k < 4; k++) {
+                                if (c == k && c < split) w = lo_w[k];
+                                if (c == split + k && c < nchunks) w = up_w[k];
+                            }
+                            rq->cand[c] = w;
+                        }
+                    }
                 }
             }
+            if (half == 0 && valid) p.pi[(int64_t)(h * p.T + t - 1) * p.cap + p.tok_off + i] = (uint8_t)bj;
         }
         if (p.stats && half == 0) {
 #pragma unroll
@@ -522,12 +628,14 @@ static const int kMaxSmem = 232448;  // opt-in shared memory per block on sm_100
 // exchange (best, second, index per row)
 static size_t assign_tail_bytes(int nslots, int Cpad) {
     return (size_t)(2 * nslots + 3 + 2 * kEpiGroups) * 8 + 16 + 16 /* alignment */ +
-           (size_t)kEpiGroups * (Cpad + 3 * kTileM) * 4;
+           (size_t)kEpiGroups * (Cpad + 3 * 2 * kTileM + 4 * kTileM) * 4;
 }
+
+static size_t assign_b_bytes(int Cpad) { return (size_t)2 * kBPlanes * Cpad * 128; }
 
 static int assign_slots(int Cpad) {
     for (int n = 12; n >= 4; n--)
-        if ((size_t)1024 + 4 * (size_t)Cpad * 128 + (size_t)n * kKBlockBytes +
+        if ((size_t)1024 + assign_b_bytes(Cpad) + (size_t)n * kKBlockBytes +
                 assign_tail_bytes(n, Cpad) <= (size_t)kMaxSmem)
             return n;
     return 4;
@@ -535,7 +643,7 @@ static int assign_slots(int Cpad) {
 
 size_t assign_smem_bytes(int Cpad) {
     const int nslots = assign_slots(Cpad);
-    return (size_t)1024 + 4 * (size_t)Cpad * 128 + (size_t)nslots * kKBlockBytes +
+    return (size_t)1024 + assign_b_bytes(Cpad) + (size_t)nslots * kKBlockBytes +
            assign_tail_bytes(nslots, Cpad);
 }
 
@@ -544,19 +652,19 @@ cudaError_t assign_encode(const QPlan &p, AssignMaps *m) {
     if (!enc) return cudaErrorNotSupported;
     const cuuint32_t estr[3] = {1, 1, 1};
     {
-        const cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)p.N, (cuuint64_t)(2 * p.H)};
+        const cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)p.N, (cuuint64_t)p.H};
         const cuuint64_t strides[2] = {(cuuint64_t)kD * 2, (cuuint64_t)p.N * kD * 2};
         const cuuint32_t box[3] = {64, (cuuint32_t)kTileM, 1};
-        if (enc(&m->a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, p.A, dims, strides, box, estr,
+        if (enc(&m->a, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, p.A, dims, strides, box, estr,
                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
     }
     {
-        const cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)p.C, (cuuint64_t)(2 * p.H)};
+        const cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)p.C, (cuuint64_t)(kBPlanes * p.H)};
         const cuuint64_t strides[2] = {(cuuint64_t)kD * 2, (cuuint64_t)p.Cpad * kD * 2};
         const cuuint32_t box[3] = {64, (cuuint32_t)p.Cpad, 1};
-        if (enc(&m->b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, p.B, dims, strides, box, estr,
+        if (enc(&m->b, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, p.B, dims, strides, box, estr,
                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;

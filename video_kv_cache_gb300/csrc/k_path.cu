@@ -101,7 +101,7 @@ cudaError_t launch_init_centroids(const QPlan &p, int t, cudaStream_t st) {
 // --------------------------------------------------------------------------------------
 // Centring vector for the GEMM operands.  Squared distances do not change when both
 // operands are shifted by the same vector; shifting by a point near the data's centre
-// keeps the bf16 split's error small.  Stage 1 uses the mean of the initial centroids
+// keeps the fp16 operands small, and their rounding error is relative to their size.  Stage 1 uses the mean of the initial centroids
 // (C sample rows of X, or the warm-start table); later stages work on residuals whose
 // mean is already ~0 and use 0.   grid H, block 128.
 // --------------------------------------------------------------------------------------
@@ -126,9 +126,9 @@ cudaError_t launch_centre(const QPlan &p, int t, cudaStream_t st) {
 // Residual preparation for stage t.  One thread per (token, 8 channels).
 //   r      = fp32(x - sum_{s<t} C^(s)[pi^(s)_i]) via a TwoSum chain (one final rounding)
 //   R32    = r                           (stages t >= 2; stage 1 reads X directly)
-//   A hi/lo = bf16 split of r - mu       (tensor-core operand of the assignment)
-//   rnorm  = ||r - mu||                  (for the assignment's error margin)
-//   maxabs = max |r| over the tensor     (fixed-point scale of the centroid sums)
+//   A      = fp16(r - mu)                (tensor-core operand of the assignment)
+//   rnorm  = ||r - mu||, fp32            (for the assignment's error margin)
+//   dnorm  = ||A - (r - mu)||, fp32      (the same)
 // grid (blocks per tensor, H), block 256 = 16 tokens x 16 chunks of 8 channels.
 // --------------------------------------------------------------------------------------
 constexpr int kPrepTokens = 512;
@@ -140,7 +140,6 @@ __global__ void __launch_bounds__(256) k_prep(QPlan p, int t) {
     const int64_t i1 = min(p.N, i0 + kPrepTokens);
     float mu[8];
     load_f8(p.mu + h * kD + c8 * 8, mu);
-    float mx = 0.f;
     bool finite = true, bad_index = false;
     for (int64_t ib = i0; ib < i1; ib += 16) {
         // the loop bound is uniform over the block, so every lane reaches the shuffles
@@ -183,41 +182,37 @@ __global__ void __launch_bounds__(256) k_prep(QPlan p, int t) {
             dst[0] = make_float4(r[0], r[1], r[2], r[3]);
             dst[1] = make_float4(r[4], r[5], r[6], r[7]);
         }
-        float ss = 0.f;
-        __align__(16) __nv_bfloat16 hi[8], lo[8];
+        float ss = 0.f, dd = 0.f;
+        __align__(16) __half a16[8];
 #pragma unroll
         for (int q = 0; q < 8; q++) {
-            float v = __fsub_rn(r[q], mu[q]);
-            hi[q] = __float2bfloat16_rn(v);
-            lo[q] = __float2bfloat16_rn(__fsub_rn(v, __bfloat162float(hi[q])));
+            const float v = __fsub_rn(r[q], mu[q]);
+            a16[q] = __float2half_rn(v);
+            const float dv = __fsub_rn(v, __half2float(a16[q]));  // exact
             ss = __fmaf_rn(v, v, ss);
-            mx = fmaxf(mx, fabsf(r[q]));
+            dd = __fmaf_rn(dv, dv, dd);
         }
-        if (valid) {
-            *reinterpret_cast<uint4 *>(p.A + ((int64_t)(h * 2 + 0) * p.N + i) * kD + c8 * 8) =
-                *reinterpret_cast<uint4 *>(hi);
-            *reinterpret_cast<uint4 *>(p.A + ((int64_t)(h * 2 + 1) * p.N + i) * kD + c8 * 8) =
-                *reinterpret_cast<uint4 *>(lo);
-        }
+        if (valid)
+            *reinterpret_cast<uint4 *>(p.A + ((int64_t)h * p.N + i) * kD + c8 * 8) =
+                *reinterpret_cast<uint4 *>(a16);
 #pragma unroll
-        for (int o = 8; o >= 1; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-        if (valid && c8 == 0) p.rnorm[h * p.N + i] = sqrtf(ss);
+        for (int o = 8; o >= 1; o >>= 1) {
+            ss += __shfl_xor_sync(0xffffffffu, ss, o);
+            dd += __shfl_xor_sync(0xffffffffu, dd, o);
+        }
+        if (valid && c8 == 0) {
+            p.rnorm[h * p.N + i] = sqrtf(ss);
+            p.dnorm[h * p.N + i] = sqrtf(dd);
+        }
     }
-    // block max -> one atomic per block
-    __shared__ float red[8];
+    // one status update per block
     __shared__ int bad, bad_idx;
     if (threadIdx.x == 0) bad = 0, bad_idx = 0;
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
     __syncthreads();
     if (!finite) bad = 1;
     if (bad_index) bad_idx = 1;
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = mx;
     __syncthreads();
     if (threadIdx.x == 0) {
-        float m = red[0];
-        for (int w = 1; w < 8; w++) m = fmaxf(m, red[w]);
-        if (m == m) atomicMax(p.maxabs + h, __float_as_uint(m));
         if (bad) or_status(p.status, QVG_DEV_NONFINITE);
         if (bad_idx) or_status(p.status, QVG_DEV_BAD_INDEX);
     }
@@ -230,19 +225,24 @@ cudaError_t launch_prep(const QPlan &p, int t, cudaStream_t st) {
 }
 
 // --------------------------------------------------------------------------------------
-// GEMM planes of the stage's initial centroids: bf16 hi / lo split of C_j - mu and
-// ||C_j - mu||^2.   grid (C, H), block 128.
+// GEMM planes of the stage's initial centroids: fp16 planes of C_j - mu and
+// ||C_j - mu||^2 (fp32).   grid (C, H), block 128.
 // --------------------------------------------------------------------------------------
+__device__ __forceinline__ void store_planes(const QPlan &p, int h, int j, int k, float ct) {
+    const __half hi = __float2half_rn(ct);
+    p.B[((int64_t)h * kBPlanes * p.Cpad + j) * kD + k] = hi;
+    if (kBPlanes == 2)
+        p.B[((int64_t)(h * kBPlanes + 1) * p.Cpad + j) * kD + k] =
+            __float2half_rn(__fsub_rn(ct, __half2float(hi)));
+}
+
 __global__ void k_centroid_planes(QPlan p, int t) {
     const int j = blockIdx.x, h = blockIdx.y, k = threadIdx.x;
     const float v = p.cent[h * p.cent_tstride + p.cent_off + (int64_t)(t - 1) * p.C * kD +
                            (int64_t)j * kD + k];
     __shared__ float red[4];
     const float ct = __fsub_rn(v, p.mu[h * kD + k]);
-    const __nv_bfloat16 hi = __float2bfloat16_rn(ct);
-    const __nv_bfloat16 lo = __float2bfloat16_rn(__fsub_rn(ct, __bfloat162float(hi)));
-    p.B[((int64_t)(h * 2 + 0) * p.Cpad + j) * kD + k] = hi;
-    p.B[((int64_t)(h * 2 + 1) * p.Cpad + j) * kD + k] = lo;
+    store_planes(p, h, j, k, ct);
     float ss = ct * ct;
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
@@ -251,14 +251,7 @@ __global__ void k_centroid_planes(QPlan p, int t) {
     if (k == 0) p.cn[(int64_t)h * p.Cpad + j] = (red[0] + red[1]) + (red[2] + red[3]);
 }
 
-__global__ void k_pad_cn(QPlan p) {
-    // padded GEMM columns (C <= j < Cpad) never win the argmin
-    const int h = blockIdx.x;
-    for (int j = p.C + threadIdx.x; j < p.Cpad; j += blockDim.x) p.cn[(int64_t)h * p.Cpad + j] = INFINITY;
-}
-
 cudaError_t launch_centroid_planes(const QPlan &p, int t, cudaStream_t st) {
-    if (p.Cpad > p.C) k_pad_cn<<<p.H, 32, 0, st>>>(p);
     k_centroid_planes<<<dim3(p.C, p.H), kD, 0, st>>>(p, t);
     return cudaGetLastError();
 }
@@ -272,7 +265,7 @@ cudaError_t launch_centroid_planes(const QPlan &p, int t, cudaStream_t st) {
 //    cluster inside its chunk with error-free TwoSum accumulation (sum + running error,
 //    both fp32) in sorted order (lane l holds channels 4l..4l+3, 16 rows in flight).
 // 3. One warp per cluster adds its pieces (one, or one per chunk it spans) in chunk
-//    order, forms the mean, and writes the centroid with the bf16 hi / lo planes of
+//    order, forms the mean, and writes the centroid with the fp16 GEMM planes of
 //    C_j - mu and ||C_j - mu||^2 for the next assignment; empty clusters keep their
 //    centroid.
 // Every reduction has a fixed order, so repeated runs give identical bits; the
@@ -375,18 +368,19 @@ __device__ __forceinline__ void write_centroid(const QPlan &p, int h, int t, int
     if (!planes) return;
     const float ct[4] = {__fsub_rn(cv.x, mu.x), __fsub_rn(cv.y, mu.y), __fsub_rn(cv.z, mu.z),
                          __fsub_rn(cv.w, mu.w)};
-    __align__(8) __nv_bfloat16 hi[4], lo[4];
+    __align__(8) __half hi[4], lo[4];
     float ss = 0.f;
 #pragma unroll
     for (int k = 0; k < 4; k++) {
-        hi[k] = __float2bfloat16_rn(ct[k]);
-        lo[k] = __float2bfloat16_rn(__fsub_rn(ct[k], __bfloat162float(hi[k])));
+        hi[k] = __float2half_rn(ct[k]);
+        lo[k] = __float2half_rn(__fsub_rn(ct[k], __half2float(hi[k])));
         ss = __fmaf_rn(ct[k], ct[k], ss);
     }
-    *reinterpret_cast<uint2 *>(p.B + ((int64_t)(h * 2 + 0) * p.Cpad + j) * kD + 4 * lane) =
+    *reinterpret_cast<uint2 *>(p.B + ((int64_t)h * kBPlanes * p.Cpad + j) * kD + 4 * lane) =
         *reinterpret_cast<uint2 *>(hi);
-    *reinterpret_cast<uint2 *>(p.B + ((int64_t)(h * 2 + 1) * p.Cpad + j) * kD + 4 * lane) =
-        *reinterpret_cast<uint2 *>(lo);
+    if (kBPlanes == 2)
+        *reinterpret_cast<uint2 *>(p.B + ((int64_t)(h * kBPlanes + 1) * p.Cpad + j) * kD +
+                                   4 * lane) = *reinterpret_cast<uint2 *>(lo);
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
     if (lane == 0) p.cn[(int64_t)h * p.Cpad + j] = ss;

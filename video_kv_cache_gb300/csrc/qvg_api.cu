@@ -16,10 +16,12 @@ namespace {
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-inline int cpad_of(int C) { return C <= 16 ? 16 : (C + 15) / 16 * 16; }
+// GEMM columns: a multiple of 32, so that the MMA writes every TMEM column the epilogue's
+// 32-column loads read.
+inline int cpad_of(int C) { return (C + 31) / 32 * 32; }
 
 struct WsLayout {
-    size_t R32, A, rnorm, B, cn, mu, counts, offs, blockoff, ids, cid, psum, wsum, maxabs, init_idx,
+    size_t R32, A, rnorm, dnorm, B, cn, mu, counts, offs, blockoff, ids, cid, psum, wsum, init_idx,
         stats, rq_count, rq, total;
     int nsb, nchunk;
 };
@@ -36,10 +38,11 @@ WsLayout ws_layout(int64_t H, int64_t N, int C, int T) {
     if (T > 0) {
         const int Cpad = cpad_of(C);
         w.R32 = take(T >= 2 ? (size_t)H * N * kD * 4 : 0);
-        w.A = take((size_t)H * 2 * N * kD * 2);
+        w.A = take((size_t)H * N * kD * 2);
         w.rnorm = take((size_t)H * N * 4);
-        w.B = take((size_t)H * 2 * Cpad * kD * 2);
-        w.cn = take((size_t)H * Cpad * 4 + 32 * 4);  // 32-column TMEM reads may run past Cpad
+        w.dnorm = take((size_t)H * N * 4);
+        w.B = take((size_t)H * kBPlanes * Cpad * kD * 2);
+        w.cn = take((size_t)H * Cpad * 4);
         w.mu = take((size_t)H * kD * 4);
         w.nsb = (int)((N + kSortBlock - 1) / kSortBlock);
         w.nchunk = (int)((N + kChunk - 1) / kChunk);
@@ -50,7 +53,6 @@ WsLayout ws_layout(int64_t H, int64_t N, int C, int T) {
         w.cid = take((size_t)H * N);
         w.psum = take((size_t)H * w.nchunk * 4 * kD * 4);
         w.wsum = take((size_t)H * C * 2 * kD * 4);
-        w.maxabs = take((size_t)H * 4);
         w.init_idx = take((size_t)H * T * C * 4);
         w.rq_count = take(4);
         w.rq = take((size_t)H * N * sizeof(RefineReq));
@@ -123,7 +125,6 @@ qvg_status run_stages(QPlan &p, const AssignMaps *maps, int num_sms, cudaStream_
         auto step = [&](cudaError_t e) {
             if (e != cudaSuccess && rc == QVG_OK) rc = QVG_ERR_CUDA;
         };
-        step(cudaMemsetAsync(p.maxabs, 0, (size_t)p.H * 4, st));
         if (t == 1) step(launch_init_centroids(p, t, st));
         step(launch_centre(p, t, st));
         step(launch_prep(p, t, st));
@@ -185,9 +186,10 @@ QPlan make_plan(const qvg_quant_params *prm, const void *X, const float *warm,
     p.stats = reinterpret_cast<unsigned *>(ws + w.stats);
     if (p.T > 0) {
         p.R32 = p.T >= 2 ? reinterpret_cast<float *>(ws + w.R32) : nullptr;
-        p.A = reinterpret_cast<__nv_bfloat16 *>(ws + w.A);
+        p.A = reinterpret_cast<__half *>(ws + w.A);
         p.rnorm = reinterpret_cast<float *>(ws + w.rnorm);
-        p.B = reinterpret_cast<__nv_bfloat16 *>(ws + w.B);
+        p.dnorm = reinterpret_cast<float *>(ws + w.dnorm);
+        p.B = reinterpret_cast<__half *>(ws + w.B);
         p.cn = reinterpret_cast<float *>(ws + w.cn);
         p.mu = reinterpret_cast<float *>(ws + w.mu);
         p.counts = reinterpret_cast<int *>(ws + w.counts);
@@ -199,7 +201,6 @@ QPlan make_plan(const qvg_quant_params *prm, const void *X, const float *warm,
         p.wsum = reinterpret_cast<float *>(ws + w.wsum);
         p.nsb = w.nsb;
         p.nchunk = w.nchunk;
-        p.maxabs = reinterpret_cast<unsigned *>(ws + w.maxabs);
         p.init_idx = reinterpret_cast<int *>(ws + w.init_idx);
         p.rq_count = reinterpret_cast<int *>(ws + w.rq_count);
         p.rq = reinterpret_cast<RefineReq *>(ws + w.rq);
