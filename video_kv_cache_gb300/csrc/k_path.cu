@@ -101,9 +101,10 @@ cudaError_t launch_init_centroids(const QPlan &p, int t, cudaStream_t st) {
 // --------------------------------------------------------------------------------------
 // Centring vector for the GEMM operands.  Squared distances do not change when both
 // operands are shifted by the same vector; shifting by a point near the data's centre
-// keeps the fp16 operands small, and their rounding error is relative to their size.  Stage 1 uses the mean of the initial centroids
-// (C sample rows of X, or the warm-start table); later stages work on residuals whose
-// mean is already ~0 and use 0.   grid H, block 128.
+// keeps the fp16 operands small, and their rounding error is relative to their size.
+// Stage 1 uses the mean of the initial centroids (C sample rows of X, or the warm-start
+// table); later stages work on residuals whose mean is already ~0 and use 0.
+// grid H, block 128.
 // --------------------------------------------------------------------------------------
 __global__ void k_centre(QPlan p, int t) {
     const int h = blockIdx.x, k = threadIdx.x;
