@@ -51,10 +51,11 @@ def compare_codes(R, codes_gpu, scales_gpu, bits, group, eps=2.0 ** -20):
     band_group = sb_lo != sb_hi
     sq = oracle.e4m3_decode(scales_o)
     with np.errstate(divide="ignore", invalid="ignore"):
+        # groups with s_q == 0 give inf / nan here; np.where below leaves them out
         v = R / np.repeat(sq, group, axis=1)
-    frac = np.abs(np.abs(v - np.floor(v)) - 0.5)
-    band_elem = np.where(np.repeat(sq, group, axis=1) > 0,
-                         frac <= eps * np.maximum(np.abs(v), 1.0), False)
+        frac = np.abs(np.abs(v - np.floor(v)) - 0.5)
+        band_elem = np.where(np.repeat(sq, group, axis=1) > 0,
+                             frac <= eps * np.maximum(np.abs(v), 1.0), False)
     band_elem |= np.repeat(band_group, group, axis=1)
     scales_gpu = np.asarray(scales_gpu)
     bad_scales = (scales_gpu != scales_o) & ~band_group
