@@ -356,6 +356,62 @@ def run_ours(args, w):
         print(json.dumps(line), flush=True)
 
 
+def run_sweep(args):
+    """Precision sweep on the 1.3B layer's shapes: every (bits, group) of the sweep, T = 0
+    (plain group quantization, the naive baseline) and T = 1..3 at each C, reporting the
+    mean squared reconstruction error of the key and the value tensors and its reduction
+    against T = 0.  Also reported: the naive error with exact fp32 scales (no E4M3
+    rounding or saturation), and how many T = 0 groups saturate E4M3 (scale > 448)."""
+    from video_kv_cache_gb300 import api, qvg
+    from video_kv_cache_gb300 import build as qbuild
+    torch.cuda.set_device(0)
+    qbuild.build()
+    qvg.load()
+    w = synth.workload(DEFAULT_WORKLOAD)
+    dev = torch.device("cuda")
+    X = w.make(dev)
+    H, N = X.shape[:2]
+    Xf = X.float()
+    is_v = torch.tensor([t % 2 == 1 for t in w.tids], device=dev)
+    ws = api.new_workspace(H, N, max(synth.SWEEP_C), max(synth.SWEEP_T))
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def mse(xh):
+        e = ((xh - Xf) ** 2).mean(dim=(1, 2))
+        return float(e[~is_v].mean()), float(e[is_v].mean())
+
+    rows = []
+    for bits, group in synth.SWEEP_PRECISIONS:
+        qmax = (1 << (bits - 1)) - 1
+        g = Xf.view(H, N, 128 // group, group)
+        s = g.abs().amax(dim=3, keepdim=True) / qmax
+        q = torch.where(s > 0, torch.round(g / torch.where(s > 0, s, 1.0)), 0.0)
+        naive32 = mse((q.clamp(-qmax, qmax) * s).view(H, N, 128))
+        sat = int((s > 448).sum())
+        for C in synth.SWEEP_C:
+            for T in synth.SWEEP_T:
+                if T == 0 and C != synth.SWEEP_C[0]:
+                    continue
+                ckv = api.quantize(X, C, T, bits, group, w.iters, w.seed, workspace=ws,
+                                   status=status)
+                xh = api.dequantize(ckv, N, torch.float32, status=status)
+                mk, mv = mse(xh)
+                rows.append({"bits": bits, "group": group, "C": C if T else 0, "T": T,
+                             "mse_k": mk, "mse_v": mv})
+        base = [r for r in rows if r["bits"] == bits and r["group"] == group and r["T"] == 0][0]
+        for r in rows:
+            if r["bits"] == bits and r["group"] == group:
+                r["reduction_k"] = base["mse_k"] / r["mse_k"] if r["mse_k"] > 0 else None
+                r["reduction_v"] = base["mse_v"] / r["mse_v"] if r["mse_v"] > 0 else None
+        rows.append({"bits": bits, "group": group, "naive_fp32_scales_mse_k": naive32[0],
+                     "naive_fp32_scales_mse_v": naive32[1], "e4m3_saturated_groups_T0": sat})
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0, "device status %#x" % int(status.item())
+    print(json.dumps({"metric": "MSE reduction vs naive group quantization (K, V)",
+                      "workload": w.name, "tensors": H, "tokens": N, "iters": w.iters,
+                      "data": "synthetic", "rows": rows}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -364,9 +420,13 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sweep", action="store_true",
+                    help="print the precision sweep (MSE reduction) instead of the timing line")
     args = ap.parse_args()
     w = synth.workload(args.workload)
-    if args.impl == "reference":
+    if args.sweep:
+        run_sweep(args)
+    elif args.impl == "reference":
         run_reference(args, w)
     else:
         run_ours(args, w)
