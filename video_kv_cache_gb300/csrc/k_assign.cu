@@ -427,7 +427,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int u = 0; u < 4; u++) {
                         const float sc = __fmaf_rn(-2.f, v[q + u], cc[u]);
                         s1 = fminf(s1, fmaxf(sc, b1));
-                        if (sc < b1) j1 = cb * 32 + q + u;
+                        if (sc < b1) j1 = q + u;  // column within the chunk
                         b1 = fminf(b1, sc);
                     }
                 }
@@ -436,7 +436,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 cmin2 = c == 2 ? b1 : cmin2;
                 cmin3 = c == 3 ? b1 : cmin3;
                 second = fminf(second, fminf(s1, fmaxf(best, b1)));
-                if (b1 < best) bj = j1;
+                if (b1 < best) bj = cb * 32 + j1;
                 best = fminf(best, b1);
             }
             // Both warps of the pair merge the two column halves the same way; the lower

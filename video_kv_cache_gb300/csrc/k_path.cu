@@ -292,31 +292,49 @@ __global__ void __launch_bounds__(kSortBlock) k_sort_hist(QPlan p, int t) {
     }
     __syncthreads();
     int *bh = p.blockoff + ((int64_t)h * p.nsb + b) * p.C;
-    for (int j = threadIdx.x; j < p.C; j += kSortBlock) bh[j] = hist[j];
+    for (int j = threadIdx.x; j < p.C; j += kSortBlock) {
+        const int v = hist[j];
+        bh[j] = v;
+        if (v) atomicAdd(p.counts + h * p.C + j, v);  // cluster totals (zero on entry)
+    }
 }
 
-__global__ void __launch_bounds__(kMaxC) k_sort_scan(QPlan p) {
-    // one block per tensor, thread j = cluster j
-    const int h = blockIdx.x, j = threadIdx.x;
-    __shared__ int buf[kMaxC];
-    int *bh = p.blockoff + (int64_t)h * p.nsb * p.C;
-    int total = 0;
-    if (j < p.C)
-        for (int b = 0; b < p.nsb; b++) total += bh[(int64_t)b * p.C + j];
-    buf[j] = j < p.C ? total : 0;
+// Offsets of the counting sort.  grid (C/32 cluster groups, H), block 256: lane = cluster
+// of the group, warp w = a slice of the token blocks.  offs[j] = sum of the totals of the
+// clusters before j; blockoff[b][j] (in place, over the block histogram) = offs[j] + the
+// tokens of cluster j in the blocks before b.
+__global__ void __launch_bounds__(256) k_sort_scan(QPlan p) {
+    constexpr int NW = 8;
+    __shared__ int tot[kMaxC];
+    __shared__ int wsum[NW][32];
+    const int h = blockIdx.y, lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int j = blockIdx.x * 32 + lane;
+    // inclusive scan of the cluster totals of this tensor
+    const int x = threadIdx.x;
+    tot[x] = x < p.C ? p.counts[h * p.C + x] : 0;
     __syncthreads();
     for (int o = 1; o < kMaxC; o <<= 1) {
-        const int a1 = j >= o ? buf[j - o] : 0;
+        const int a1 = x >= o ? tot[x - o] : 0;
         __syncthreads();
-        buf[j] += a1;
+        tot[x] += a1;
         __syncthreads();
     }
+    int *bh = p.blockoff + (int64_t)h * p.nsb * p.C;
+    const int per = (p.nsb + NW - 1) / NW;
+    const int b0 = w * per, b1 = min(p.nsb, b0 + per);
+    int local = 0;
     if (j < p.C) {
-        const int off = buf[j] - total;
-        p.counts[h * p.C + j] = total;
-        p.offs[h * p.C + j] = off;
+#pragma unroll 8
+        for (int b = b0; b < b1; b++) local += bh[(int64_t)b * p.C + j];
+    }
+    wsum[w][lane] = local;
+    __syncthreads();
+    if (j < p.C) {
+        const int off = tot[j] - (j < p.C ? p.counts[h * p.C + j] : 0);
+        if (w == 0) p.offs[h * p.C + j] = off;
         int run = off;
-        for (int b = 0; b < p.nsb; b++) {
+        for (int w2 = 0; w2 < w; w2++) run += wsum[w2][lane];
+        for (int b = b0; b < b1; b++) {
             const int v = bh[(int64_t)b * p.C + j];
             bh[(int64_t)b * p.C + j] = run;
             run += v;
@@ -414,6 +432,17 @@ __global__ void __launch_bounds__(256, 2) k_chunk_sums(QPlan p, int t) {
     // continue into the neighbouring chunks
     const int c_prev = k > 0 ? (int)p.cid[(int64_t)h * p.N + c0 - 1] : -1;
     const int c_next = c0 + nk < p.N ? (int)p.cid[(int64_t)h * p.N + c0 + nk] : -1;
+    // run starts: bit q is set when sorted position q begins a new cluster run
+    uint32_t brk[2];
+    {
+        const int last0 = __shfl_sync(0xffffffffu, cr[0], 31);
+#pragma unroll
+        for (int q = 0; q < 2; q++) {
+            int pc = __shfl_up_sync(0xffffffffu, cr[q], 1);
+            if (lane == 0) pc = q == 0 ? -2 : last0;
+            brk[q] = __ballot_sync(0xffffffffu, q * 32 + lane < nk && cr[q] != pc);
+        }
+    }
     float s[4] = {0.f, 0.f, 0.f, 0.f}, e[4] = {0.f, 0.f, 0.f, 0.f};
     int run_c = -1, run_start = 0;
     auto stash = [&](int end) {
@@ -423,15 +452,17 @@ __global__ void __launch_bounds__(256, 2) k_chunk_sums(QPlan p, int t) {
         reinterpret_cast<float4 *>(dst)[lane] = make_float4(s[0], s[1], s[2], s[3]);
         reinterpret_cast<float4 *>(dst + kD)[lane] = make_float4(e[0], e[1], e[2], e[3]);
     };
-    for (int k1 = 0; k1 < nk; k1 += ROWS) {
+    // the positions of a batch are compile-time constants: row ids come from fixed lanes
+#pragma unroll
+    for (int k1 = 0; k1 < kChunk; k1 += ROWS) {
+        if (k1 >= nk) break;
         // all loads of the batch are issued before any is used: raw words only here
         float4 raw[NARROW ? 1 : ROWS];
         uint2 raw16[NARROW ? ROWS : 1];
 #pragma unroll
         for (int u = 0; u < ROWS; u++) {
             const int q = k1 + u;
-            const int64_t row = q < 32 ? __shfl_sync(0xffffffffu, idr[0], q & 31)
-                                       : __shfl_sync(0xffffffffu, idr[1], q & 31);
+            const int64_t row = __shfl_sync(0xffffffffu, idr[q >> 5], q & 31);
             if constexpr (NARROW) {
                 raw16[u] = make_uint2(0u, 0u);
                 if (q < nk)
@@ -452,8 +483,6 @@ __global__ void __launch_bounds__(256, 2) k_chunk_sums(QPlan p, int t) {
 #pragma unroll
         for (int u = 0; u < ROWS; u++) {
             const int q = k1 + u;
-            const int cu = q < 32 ? __shfl_sync(0xffffffffu, cr[0], q & 31)
-                                  : __shfl_sync(0xffffffffu, cr[1], q & 31);
             if (q < nk) {
                 float v[4];
                 if constexpr (SRC == 0) {
@@ -470,9 +499,9 @@ __global__ void __launch_bounds__(256, 2) k_chunk_sums(QPlan p, int t) {
                 } else {
                     v[0] = raw[u].x; v[1] = raw[u].y; v[2] = raw[u].z; v[3] = raw[u].w;
                 }
-                if (cu != run_c) {
+                if ((brk[q >> 5] >> (q & 31)) & 1u) {  // warp-uniform
                     if (run_c >= 0) stash(q);
-                    run_c = cu;
+                    run_c = __shfl_sync(0xffffffffu, cr[q >> 5], q & 31);
                     run_start = q;
 #pragma unroll
                     for (int r = 0; r < 4; r++) s[r] = e[r] = 0.f;
@@ -541,12 +570,16 @@ __global__ void __launch_bounds__(256) k_cluster_finalize(QPlan p, int t, int pl
                    make_float4(mean_of(S[0], E[0], n), mean_of(S[1], E[1], n), mean_of(S[2], E[2], n),
                                mean_of(S[3], E[3], n)),
                    planes != 0, mu);
+    // zero the total again for the next round's histogram (an empty cluster's is already
+    // zero); every lane has used cnt by now
+    __syncwarp();
+    if (lane == 0) p.counts[h * p.C + j] = 0;
 }
 
 cudaError_t launch_cluster_means(const QPlan &p, int t, bool planes, cudaStream_t st) {
     const dim3 sgrid((unsigned)p.nsb, p.H);
     k_sort_hist<<<sgrid, kSortBlock, 0, st>>>(p, t);
-    k_sort_scan<<<p.H, kMaxC, 0, st>>>(p);
+    k_sort_scan<<<dim3((unsigned)((p.C + 31) / 32), p.H), 256, 0, st>>>(p);
     k_sort_scatter<<<sgrid, kSortBlock, 0, st>>>(p, t);
     const dim3 cgrid((unsigned)((p.nchunk + 7) / 8), p.H);
     if (t >= 2)

@@ -121,6 +121,8 @@ qvg_status device_info(int *num_sms) {
 // The T smoothing stages: cold-start or warm centroids, then `iters` Lloyd rounds each.
 qvg_status run_stages(QPlan &p, const AssignMaps *maps, int num_sms, cudaStream_t st) {
     qvg_status rc = QVG_OK;
+    // the sort's cluster totals start at zero; each update leaves them at zero again
+    if (cudaMemsetAsync(p.counts, 0, (size_t)p.H * p.C * 4, st) != cudaSuccess) return QVG_ERR_CUDA;
     for (int t = 1; t <= p.T && rc == QVG_OK; t++) {
         auto step = [&](cudaError_t e) {
             if (e != cudaSuccess && rc == QVG_OK) rc = QVG_ERR_CUDA;
