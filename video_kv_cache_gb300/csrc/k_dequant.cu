@@ -6,63 +6,63 @@
 // "Quant VideoGen" notes page, sections Progressive Residual Quantization and
 // Algorithm-System Co-design, the fused dequantization kernel).
 //
-// Design (HBM-bound; the output write dominates the bytes):
-//   * Work unit = (tensor, centroid table, channel slice of W channels, token block).  The
-//     CTA stages the T tables' W-channel slices (T x C x W fp32) in shared memory once per
-//     unit, so centroid lookups never leave the SM in the token loop.
-//   * A thread reconstructs 16 channels of one token: four 4-channel chunks spread W/4
-//     channels apart, so the TPT = W/16 threads of a token cover the slice.  Per chunk it
-//     reads one 16-byte table row piece per stage (LDS.128) and writes 4 outputs at once.
-//   * Bank conflicts: one quarter-warp (8 threads) serves 8/TPT tokens whose table rows are
-//     random.  A token's chunk j sits in bank group (j mod 4 for W = 32, j mod 2 for
-//     W = 64); the token in quarter-warp slot k walks its chunks starting at j = k, so the
-//     tokens sharing a quarter-warp always hit disjoint banks.
-//   * The next token's codes, scales and cluster indices are loaded before the current
-//     token is computed, to keep reads in flight.
-//   * When even 32-channel slices of the tables do not fit in shared memory the kernel
-//     reads them through L1/L2 instead.
+// Design (HBM-bound: the output write is most of the bytes):
+//   * One CTA of 1024 threads per SM.  A work unit is (tensor, centroid table, channel
+//     slice of W channels, token block); the CTA stages that W-channel slice of all T
+//     tables (T x C x W fp32) in shared memory once per unit.  W is the widest of 128,
+//     64 and 32 whose slice fits in 200 KB (64 for T = 2, C = 256); beyond that the
+//     tables are read through L1 / L2.
+//   * A lane rebuilds 16 contiguous channels of a token: one 4- or 8-byte code load, one
+//     scale byte and T cluster-index bytes; the W / 16 lanes of a token write its W
+//     channels as one contiguous run.
+//   * Arithmetic per element: the code u is masked in place into the mantissa of the float
+//     2^23 (one logic op), one subtraction gives (u - 2^(b-1)) * 2^k exactly, and
+//     y = fma(s_q * 2^-k, that, C^(T)) (s_q * q is exact, so this equals adding C^(T) to
+//     the dequantized value); then one add per further stage, T - 1 down to 1, in fp32,
+//     rounded once to the output type.
+//   * A staged table row's 16-byte chunks are stored XOR-swizzled, so a quarter-warp's
+//     16-byte reads hit distinct bank groups.
+//   * The next token's codes, scale and indices are loaded before the current token is
+//     computed, to keep reads in flight.
 #include <cuda_fp8.h>
 
 #include <algorithm>
-#include <cstdlib>
 
 #include "internal.cuh"
 
 namespace qvg {
 
 namespace {
-constexpr int kDqThreads = 512;
+constexpr int kDqThreads = 1024;
+constexpr size_t kDqTableBytes = 200 * 1024;  // largest table slice staged by one CTA
+constexpr int kLaneCh = 16;                   // channels a lane rebuilds per token
 
-// Per-token state of one thread: the code bits of its 4 chunks (8 bits per chunk for INT2,
-// 16 for INT4), their 4 E4M3 scale bytes, and pi^(1..T) one byte per stage.
-template <int BITS>
-struct TokMeta {
-    uint32_t code[BITS / 2];
-    uint32_t sbytes;
-    uint64_t pk;
-};
+// Physical 16-byte chunk of logical chunk c in a staged table row: bits 3-4 of c are
+// XOR-ed into its low bits, so the lanes of a quarter-warp reading chunk 4l + k
+// (l = 0..7) hit 8 distinct bank groups.
+__device__ __forceinline__ int swz(int c) { return c ^ ((c >> 3) & 3); }
 }  // namespace
 
-// Two CTAs per SM where the state fits in 64 registers a thread; one otherwise.
 template <int BITS, int OUT, int TT>
-__global__ void __launch_bounds__(kDqThreads, (BITS == 2 && TT >= 0 && TT <= 2) ? 2 : 1)
+__global__ void __launch_bounds__(kDqThreads, 1)
     k_dequant(DPlan p, int W, int64_t n_chunks, int64_t blocks_per_chunk, int64_t blk,
-              int64_t total_units, int table_floats, int smem_tables) {
+              int64_t total_units, int smem_tables) {
     extern __shared__ __align__(16) float smem_f[];
     constexpr int MID = 1 << (BITS - 1);
+    constexpr int PER16 = 16 / BITS;  // codes in a 16-bit half-word
     const int T = TT >= 0 ? TT : p.T;
     const int C = p.C;
-    float *tab = smem_f;                  // [T][C][W]
-    float *lut = smem_f + table_floats;   // [256] E4M3 -> fp32
-    const int tid = threadIdx.x;
-    const int TPT = W >> 4;               // threads per token
-    const int q = tid & (TPT - 1);
-    const int slot = (tid & 7) / TPT;     // token position within the quarter-warp
-    const int tpc = kDqThreads / TPT;     // tokens per pass of the CTA
-    const int tok = tid / TPT;
+    float *lut = smem_f;        // [256] E4M3 -> fp32
+    float *tab = smem_f + 256;  // [T][C][W], swizzled 16-byte chunks
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int LPT = W / kLaneCh;  // lanes per token
+    const int TPW = 32 / LPT;     // tokens per warp and pass
+    const int sub = lane % LPT;
+    const int tpc = (kDqThreads / 32) * TPW;  // tokens per CTA pass
     const int slices = kD / W;
     const int row_bytes = kD * BITS / 8;
     const int ngroups = kD / p.group;
+    const int wq = W >> 2;  // 16-byte chunks per staged row
 
     if (tid < 256)
         lut[tid] = __half2float(__half(__nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)tid, __NV_E4M3)));
@@ -71,6 +71,7 @@ __global__ void __launch_bounds__(kDqThreads, (BITS == 2 && TT >= 0 && TT <= 2) 
     const int64_t ub = blockIdx.x * per + min((int64_t)blockIdx.x, rem);
     const int64_t ue = ub + per + ((int64_t)blockIdx.x < rem ? 1 : 0);
     int64_t staged = -1;
+    bool bad_index = false;
     __syncthreads();
 
     for (int64_t u = ub; u < ue; u++) {
@@ -83,11 +84,11 @@ __global__ void __launch_bounds__(kDqThreads, (BITS == 2 && TT >= 0 && TT <= 2) 
         const float *tbl = p.cent + ((int64_t)h * p.n_tables + c) * T * C * kD;
         if (smem_tables && T > 0 && hcs != staged) {
             __syncthreads();
-            const int nvec = T * C * (W / 4);
+            const int nvec = T * C * wq;
             for (int x = tid; x < nvec; x += kDqThreads) {
-                const int r = x / (W / 4), qq = x - r * (W / 4);
-                reinterpret_cast<float4 *>(tab)[x] =
-                    __ldg(reinterpret_cast<const float4 *>(tbl + (int64_t)r * kD + s * W) + qq);
+                const int r = x / wq, cc = x - r * wq;
+                reinterpret_cast<float4 *>(tab)[r * wq + swz(cc)] =
+                    __ldg(reinterpret_cast<const float4 *>(tbl + (int64_t)r * kD + s * W) + cc);
             }
             __syncthreads();
             staged = hcs;
@@ -95,111 +96,141 @@ __global__ void __launch_bounds__(kDqThreads, (BITS == 2 && TT >= 0 && TT <= 2) 
         const int64_t c_lo = c * p.chunk_len;
         const int64_t i0 = c_lo + b * blk;
         const int64_t i1 = min(min(c_lo + p.chunk_len, p.N), i0 + blk);
-        // this thread's chunks (first channels), in the bank-rotated order
-        int ch[4];
-#pragma unroll
-        for (int j = 0; j < 4; j++) ch[j] = s * W + 4 * (q + TPT * ((j + slot) & 3));
-        const int gshift = 31 - __clz(p.group);
-        const uint8_t *codes_h = p.codes + (int64_t)h * p.cap * row_bytes;
-        const uint8_t *scales_h = p.scales + (int64_t)h * p.cap * ngroups;
-        const uint8_t *pi_h = p.pi + (int64_t)h * T * p.cap;
-        float *out32 = static_cast<float *>(p.out) + (int64_t)h * p.out_stride;
-        uint16_t *out16 = static_cast<uint16_t *>(p.out) + (int64_t)h * p.out_stride;
+        const int ch0 = s * W + sub * kLaneCh;  // the lane's first channel
+        int64_t i = i0 + warp * TPW + lane / LPT;
+        // running pointers of token i; they advance by tpc tokens per pass
+        const uint8_t *cp = p.codes + ((int64_t)h * p.cap + i) * row_bytes + ch0 * BITS / 8;
+        const uint8_t *sp = p.scales + ((int64_t)h * p.cap + i) * ngroups + ch0 / p.group;
+        const uint8_t *pp = p.pi + (int64_t)h * T * p.cap + i;
+        char *op = static_cast<char *>(p.out) +
+                   ((int64_t)h * p.out_stride + i * kD + ch0) * (OUT == DT_F32 ? 4 : 2);
+        const int64_t cstep = (int64_t)tpc * row_bytes, sstep = (int64_t)tpc * ngroups;
+        const int64_t ostep = (int64_t)tpc * kD * (OUT == DT_F32 ? 4 : 2);
 
-        auto fetch = [&](int64_t i, TokMeta<BITS> &m) {
-            const uint8_t *cp = codes_h + i * row_bytes;
-            const uint8_t *sp = scales_h + i * ngroups;
-            m.sbytes = 0;
-#pragma unroll
-            for (int j = 0; j < 4; j++) {
-                m.sbytes |= (uint32_t)__ldg(sp + (ch[j] >> gshift)) << (8 * j);
-                if constexpr (BITS == 2) {
-                    const uint32_t v = __ldg(cp + (ch[j] >> 2));
-                    if (j == 0) m.code[0] = v; else m.code[0] |= v << (8 * j);
-                } else {
-                    const uint32_t v = __ldg(reinterpret_cast<const unsigned short *>(cp + (ch[j] >> 1)));
-                    if ((j & 1) == 0) m.code[j >> 1] = v; else m.code[j >> 1] |= v << 16;
-                }
+        struct Meta {
+            uint32_t code[BITS / 2];  // 16 codes, channel 0 in the low bits
+            uint32_t sbyte;
+            uint64_t pk;              // pi^(1..T), one byte per stage
+        };
+        auto fetch = [&](Meta &m) {
+            if constexpr (BITS == 2) {
+                m.code[0] = __ldg(reinterpret_cast<const uint32_t *>(cp));
+            } else {
+                const uint2 v = __ldg(reinterpret_cast<const uint2 *>(cp));
+                m.code[0] = v.x;
+                m.code[1] = v.y;
             }
+            m.sbyte = __ldg(sp);
             m.pk = 0;
             if (TT >= 0) {
 #pragma unroll
-                for (int t = 0; t < (TT > 0 ? TT : 1); t++)
-                    if (t < T) m.pk |= (uint64_t)__ldg(pi_h + (int64_t)t * p.cap + i) << (8 * t);
+                for (int t = 0; t < TT; t++) m.pk |= (uint64_t)__ldg(pp + (int64_t)t * p.cap) << (8 * t);
             } else {
-                for (int t = 0; t < T; t++)
-                    m.pk |= (uint64_t)__ldg(pi_h + (int64_t)t * p.cap + i) << (8 * t);
+                for (int t = 0; t < T; t++) m.pk |= (uint64_t)__ldg(pp + (int64_t)t * p.cap) << (8 * t);
+            }
+        };
+        auto stage_j = [&](const Meta &m, int t) {
+            int j = (int)((m.pk >> (8 * t)) & 0xFFu);
+            if (j >= C) {
+                j = C - 1;
+                bad_index = true;
+            }
+            return j;
+        };
+        // stage-t centroid values of this lane's 16 channels, cluster j, into 4 float4
+        auto table16 = [&](int t, int j, float4 (&a)[4]) {
+            if (smem_tables) {
+                const float4 *row = reinterpret_cast<const float4 *>(tab) + (t * C + j) * wq;
+#pragma unroll
+                for (int k = 0; k < 4; k++) a[k] = row[swz(4 * sub + k)];
+            } else {
+                const float4 *g =
+                    reinterpret_cast<const float4 *>(tbl + ((int64_t)t * C + j) * kD + ch0);
+#pragma unroll
+                for (int k = 0; k < 4; k++) a[k] = __ldg(g + k);
             }
         };
 
-        int64_t i = i0 + tok;
-        TokMeta<BITS> cur;
-        if (i < i1) fetch(i, cur);
+        Meta cur;
+        if (i < i1) fetch(cur);
         while (i < i1) {
             const int64_t inext = i + tpc;
-            TokMeta<BITS> nxt;
-            if (inext < i1) fetch(inext, nxt);
-            int rowoff[TT > 0 ? TT : 8];
-            if (TT >= 0) {
+            Meta nxt;
+            cp += cstep;
+            sp += sstep;
+            pp += tpc;
+            if (inext < i1) fetch(nxt);
+            // Code e of a 16-bit half-word sits at bits BITS*e; kept in place inside the
+            // mantissa of 2^23, the float is 2^23 + u * 2^(BITS*e), so subtracting
+            // 2^23 + MID * 2^(BITS*e) leaves (u - MID) * 2^(BITS*e) exactly, and
+            // sq * 2^-(BITS*e) (exact: a power-of-two rescaling) turns it into sq * q.
+            const float sq = lut[cur.sbyte & 0xFFu];
+            float se[PER16], ke[PER16];
 #pragma unroll
-                for (int t = 0; t < (TT > 0 ? TT : 1); t++)
-                    if (t < T) rowoff[t] = (t * C + min((int)((cur.pk >> (8 * t)) & 0xFFu), C - 1)) * W;
+            for (int e = 0; e < PER16; e++) {
+                se[e] = __fmul_rn(sq, __uint_as_float((uint32_t)(127 - BITS * e) << 23));
+                ke[e] = __uint_as_float(0x4B000000u) + (float)(MID << (BITS * e));
             }
+            float y[16];
 #pragma unroll
-            for (int j = 0; j < 4; j++) {
-                const float sq = lut[(cur.sbytes >> (8 * j)) & 0xFFu];
-                const uint32_t cbits = BITS == 2 ? (cur.code[0] >> (8 * j)) & 0xFFu
-                                                 : (cur.code[j >> 1] >> (16 * (j & 1))) & 0xFFFFu;
-                const float off = -sq * (float)MID;
-                float y[4];
+            for (int hw = 0; hw < 16 / PER16; hw++) {
+                const uint32_t word = cur.code[hw >> 1] >> (16 * (hw & 1));
 #pragma unroll
-                for (int e = 0; e < 4; e++)
-                    y[e] = __fmaf_rn(sq, (float)((cbits >> (e * BITS)) & ((1u << BITS) - 1u)), off);
-                const int cw = ch[j] - s * W;  // channel offset within the slice
-                if (TT >= 0) {
-#pragma unroll
-                    for (int t = (TT > 0 ? TT : 1) - 1; t >= 0; t--) {
-                        if (t < T) {
-                            float4 a;
-                            if (smem_tables) {
-                                a = *reinterpret_cast<const float4 *>(tab + rowoff[t] + cw);
-                            } else {
-                                const int pj = rowoff[t] / W - t * C;
-                                a = __ldg(reinterpret_cast<const float4 *>(tbl + ((int64_t)t * C + pj) * kD + ch[j]));
-                            }
-                            y[0] += a.x; y[1] += a.y; y[2] += a.z; y[3] += a.w;
-                        }
-                    }
-                } else {
-                    for (int t = T - 1; t >= 0; t--) {
-                        const int pj = min((int)((cur.pk >> (8 * t)) & 0xFFu), C - 1);
-                        const float4 a = smem_tables
-                            ? *reinterpret_cast<const float4 *>(tab + (t * C + pj) * W + cw)
-                            : __ldg(reinterpret_cast<const float4 *>(tbl + ((int64_t)t * C + pj) * kD + ch[j]));
-                        y[0] += a.x; y[1] += a.y; y[2] += a.z; y[3] += a.w;
-                    }
-                }
-                const int64_t o = i * kD + ch[j];
-                if constexpr (OUT == DT_F32) {
-                    *reinterpret_cast<float4 *>(out32 + o) = make_float4(y[0], y[1], y[2], y[3]);
-                } else if constexpr (OUT == DT_BF16) {
-                    const __nv_bfloat162 lo2 = __floats2bfloat162_rn(y[0], y[1]);
-                    const __nv_bfloat162 hi2 = __floats2bfloat162_rn(y[2], y[3]);
-                    *reinterpret_cast<uint2 *>(out16 + o) =
-                        make_uint2(*reinterpret_cast<const uint32_t *>(&lo2),
-                                   *reinterpret_cast<const uint32_t *>(&hi2));
-                } else {
-                    const __half2 lo2 = __floats2half2_rn(y[0], y[1]);
-                    const __half2 hi2 = __floats2half2_rn(y[2], y[3]);
-                    *reinterpret_cast<uint2 *>(out16 + o) =
-                        make_uint2(*reinterpret_cast<const uint32_t *>(&lo2),
-                                   *reinterpret_cast<const uint32_t *>(&hi2));
+                for (int e = 0; e < PER16; e++) {
+                    const uint32_t m = (word & (((1u << BITS) - 1u) << (BITS * e))) | 0x4B000000u;
+                    y[hw * PER16 + e] = __fsub_rn(__uint_as_float(m), ke[e]);
                 }
             }
+            if (T == 0) {
+#pragma unroll
+                for (int x = 0; x < 16; x++) y[x] = __fmul_rn(se[x % PER16], y[x]);
+            } else {
+                float4 a[4];
+                table16(T - 1, stage_j(cur, T - 1), a);
+#pragma unroll
+                for (int k = 0; k < 4; k++) {
+                    const float cv[4] = {a[k].x, a[k].y, a[k].z, a[k].w};
+#pragma unroll
+                    for (int q = 0; q < 4; q++)
+                        y[4 * k + q] = __fmaf_rn(se[(4 * k + q) % PER16], y[4 * k + q], cv[q]);
+                }
+                for (int t = T - 2; t >= 0; t--) {
+                    table16(t, stage_j(cur, t), a);
+#pragma unroll
+                    for (int k = 0; k < 4; k++) {
+                        const float cv[4] = {a[k].x, a[k].y, a[k].z, a[k].w};
+#pragma unroll
+                        for (int q = 0; q < 4; q++) y[4 * k + q] = __fadd_rn(y[4 * k + q], cv[q]);
+                    }
+                }
+            }
+            if constexpr (OUT == DT_F32) {
+                float4 *dst = reinterpret_cast<float4 *>(op);
+#pragma unroll
+                for (int k = 0; k < 4; k++)
+                    dst[k] = make_float4(y[4 * k], y[4 * k + 1], y[4 * k + 2], y[4 * k + 3]);
+            } else {
+                uint32_t w[8];
+#pragma unroll
+                for (int k = 0; k < 8; k++) {
+                    if constexpr (OUT == DT_BF16) {
+                        const __nv_bfloat162 v2 = __floats2bfloat162_rn(y[2 * k], y[2 * k + 1]);
+                        w[k] = *reinterpret_cast<const uint32_t *>(&v2);
+                    } else {
+                        const __half2 v2 = __floats2half2_rn(y[2 * k], y[2 * k + 1]);
+                        w[k] = *reinterpret_cast<const uint32_t *>(&v2);
+                    }
+                }
+                uint4 *dst = reinterpret_cast<uint4 *>(op);
+                dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+                dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+            }
+            op += ostep;
             cur = nxt;
             i = inext;
         }
     }
+    if (__any_sync(0xffffffffu, bad_index) && lane == 0) or_status(p.status, QVG_DEV_BAD_INDEX);
 }
 
 namespace {
@@ -208,27 +239,21 @@ template <int BITS, int OUT, int TT>
 cudaError_t launch_dq(const DPlan &p, int num_sms, int W, size_t table_bytes, bool smem_tables,
                       cudaStream_t st) {
     auto kern = k_dequant<BITS, OUT, TT>;
-    const size_t smem = (smem_tables ? table_bytes : 0) + 256 * 4;
+    const size_t smem = 256 * 4 + (smem_tables ? table_bytes : 0);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    int occ = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kDqThreads, smem);
-    if (e != cudaSuccess) return e;
-    occ = std::max(occ, 1);
-    const int64_t resident = (int64_t)num_sms * occ;
     const int64_t slices = kD / W;
     const int64_t n_chunks = (p.N + p.chunk_len - 1) / p.chunk_len;
     const int64_t base_units = (int64_t)p.H * n_chunks * slices;
-    // split chunks into token blocks until there are a couple of units per resident CTA
-    int64_t bpc = std::max<int64_t>(1, (resident * 2 + base_units - 1) / base_units);
+    // split chunks into token blocks until there are a couple of units per SM
+    int64_t bpc = std::max<int64_t>(1, ((int64_t)num_sms * 2 + base_units - 1) / base_units);
     const int64_t clen = std::min(p.chunk_len, p.N);
     int64_t blk = std::max<int64_t>(256, (clen + bpc - 1) / bpc);
     blk = (blk + 31) / 32 * 32;
     bpc = (clen + blk - 1) / blk;
     const int64_t total = base_units * bpc;
-    const int grid = (int)std::min<int64_t>(total, resident);
-    kern<<<grid, kDqThreads, smem, st>>>(p, W, n_chunks, bpc, blk, total,
-                                         smem_tables ? (int)(table_bytes / 4) : 0, smem_tables ? 1 : 0);
+    const int grid = (int)std::min<int64_t>(total, num_sms);
+    kern<<<grid, kDqThreads, smem, st>>>(p, W, n_chunks, bpc, blk, total, smem_tables ? 1 : 0);
     return cudaGetLastError();
 }
 
@@ -254,28 +279,20 @@ cudaError_t launch_dq_out(const DPlan &p, int num_sms, int W, size_t tb, bool sm
 }  // namespace
 
 cudaError_t launch_dequant(const DPlan &p, int num_sms, cudaStream_t st) {
-    // Slice width: the widest W whose T x C x W fp32 tables stay within the budget (so that
-    // several CTAs share an SM); 32-channel slices up to 160 KB of tables; tables through
-    // L1/L2 beyond that.
-    size_t budget = 64 * 1024;
-    if (const char *env = std::getenv("QVG_DQ_TABLE_BYTES")) budget = (size_t)std::atol(env);
+    // slice width: the widest whose T x C x W fp32 tables fit the staging budget
     const size_t per_ch = (size_t)p.T * p.C * 4;  // bytes per channel of all tables
     int W = 128;
     bool smem_tables = p.T > 0;
     if (smem_tables) {
         W = 0;
         for (int w : {128, 64, 32})
-            if (per_ch * w <= budget) {
+            if (per_ch * w <= kDqTableBytes) {
                 W = w;
                 break;
             }
         if (W == 0) {
-            if (per_ch * 32 <= 160 * 1024) {
-                W = 32;
-            } else {
-                W = 128;
-                smem_tables = false;
-            }
+            W = 128;
+            smem_tables = false;
         }
     }
     const size_t tb = smem_tables ? per_ch * W : 0;
