@@ -7,9 +7,10 @@
 // Algorithm-System Co-design, the fused dequantization kernel).
 //
 // Design (HBM-bound: the output write is most of the bytes):
-//   * One CTA of 1024 threads per SM.  A work unit is (tensor, centroid table, channel
-//     slice of W channels, token block); the CTA stages that W-channel slice of all T
-//     tables (T x C x W fp32) in shared memory once per unit.  W is the widest of 128,
+//   * One CTA of 1024 threads per SM, each taking an equal contiguous share of the
+//     flattened (tensor, centroid table, channel slice of W channels, token) space.  For
+//     each (tensor, table, slice) segment of its share the CTA stages that W-channel slice
+//     of all T tables (T x C x W fp32) in shared memory.  W is the widest of 128,
 //     64 and 32 whose slice fits in 200 KB (64 for T = 2, C = 256); beyond that the
 //     tables are read through L1 / L2.
 //   * A lane rebuilds 16 contiguous channels of a token: one 4- or 8-byte code load, one
@@ -22,8 +23,10 @@
 //     rounded once to the output type.
 //   * A staged table row's 16-byte chunks are stored XOR-swizzled, so a quarter-warp's
 //     16-byte reads hit distinct bank groups.
-//   * The next token's codes, scale and indices are loaded before the current token is
-//     computed, to keep reads in flight.
+//   * A lane writes its 16 outputs with one 32-byte store (two for fp32) when the output
+//     is 32-byte aligned, so every store instruction fills whole sectors.
+//   * The codes, scale and indices of the next two tokens are loaded before the current
+//     token is computed, to keep reads in flight.
 #include <cuda_fp8.h>
 
 #include <algorithm>
@@ -37,23 +40,34 @@ constexpr int kDqThreads = 1024;
 constexpr size_t kDqTableBytes = 200 * 1024;  // largest table slice staged by one CTA
 constexpr int kLaneCh = 16;                   // channels a lane rebuilds per token
 
-// Physical 16-byte chunk of logical chunk c in a staged table row: bits 3-4 of c are
-// XOR-ed into its low bits, so the lanes of a quarter-warp reading chunk 4l + k
-// (l = 0..7) hit 8 distinct bank groups.
-__device__ __forceinline__ int swz(int c) { return c ^ ((c >> 3) & 3); }
+// Physical 16-byte chunk of logical chunk c in staged table row r.  Bits 3-4 of c are
+// XOR-ed into its low bits, so the lanes of one token reading chunks 4l + k (l = 0..7)
+// hit distinct bank groups; bit 0 of the row flips bit 1, so two tokens of one
+// quarter-warp whose rows differ in parity also read disjoint groups.
+__device__ __forceinline__ int swz(int r, int c) { return c ^ ((c >> 3) & 3) ^ ((r & 1) << 1); }
+
+// 32-byte store (sm_100 and later), 32-byte aligned address.
+__device__ __forceinline__ void st_v8(void *ptr, const uint32_t (&w)[8]) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(ptr), "r"(w[0]),
+                 "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+                 : "memory");
+}
+
+__device__ __forceinline__ float e4m3_to_float(uint32_t b) {
+    const __half_raw h = __nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)b, __NV_E4M3);
+    return __half2float(__half(h));
+}
 }  // namespace
 
 template <int BITS, int OUT, int TT>
 __global__ void __launch_bounds__(kDqThreads, 1)
-    k_dequant(DPlan p, int W, int64_t n_chunks, int64_t blocks_per_chunk, int64_t blk,
-              int64_t total_units, int smem_tables) {
+    k_dequant(DPlan p, int W, int64_t n_chunks, int smem_tables, int wide_stores) {
     extern __shared__ __align__(16) float smem_f[];
     constexpr int MID = 1 << (BITS - 1);
     constexpr int PER16 = 16 / BITS;  // codes in a 16-bit half-word
     const int T = TT >= 0 ? TT : p.T;
     const int C = p.C;
-    float *lut = smem_f;        // [256] E4M3 -> fp32
-    float *tab = smem_f + 256;  // [T][C][W], swizzled 16-byte chunks
+    float *tab = smem_f;  // [T][C][W], swizzled 16-byte chunks
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int LPT = W / kLaneCh;  // lanes per token
     const int TPW = 32 / LPT;     // tokens per warp and pass
@@ -64,38 +78,40 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     const int ngroups = kD / p.group;
     const int wq = W >> 2;  // 16-byte chunks per staged row
 
-    if (tid < 256)
-        lut[tid] = __half2float(__half(__nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)tid, __NV_E4M3)));
-
-    const int64_t per = total_units / gridDim.x, rem = total_units % gridDim.x;
-    const int64_t ub = blockIdx.x * per + min((int64_t)blockIdx.x, rem);
-    const int64_t ue = ub + per + ((int64_t)blockIdx.x < rem ? 1 : 0);
+    // The work is the flattened (tensor, table chunk, slice, token) space; each CTA takes an
+    // equal contiguous share and walks it one (tensor, chunk, slice) segment at a time,
+    // staging that segment's tables when they change.
+    const int64_t per_tensor = p.N * slices;
+    const int64_t wb = per_tensor * p.H * blockIdx.x / gridDim.x;
+    const int64_t we = per_tensor * p.H * (blockIdx.x + 1) / gridDim.x;
     int64_t staged = -1;
     bool bad_index = false;
-    __syncthreads();
 
-    for (int64_t u = ub; u < ue; u++) {
-        const int64_t b = u % blocks_per_chunk;
-        const int64_t hcs = u / blocks_per_chunk;  // (h, chunk, slice)
-        const int s = (int)(hcs % slices);
-        const int64_t hc = hcs / slices;
-        const int64_t c = hc % n_chunks;
-        const int h = (int)(hc / n_chunks);
+    for (int64_t pos = wb; pos < we;) {
+        const int h = (int)(pos / per_tensor);
+        int64_t r = pos - (int64_t)h * per_tensor;
+        const int64_t c = min(r / (p.chunk_len * slices), n_chunks - 1);
+        r -= c * p.chunk_len * slices;
+        const int64_t len = min(p.chunk_len, p.N - c * p.chunk_len);  // tokens of this chunk
+        const int s = (int)(r / len);
+        const int64_t t0 = r - s * len;
+        const int64_t t1 = min(len, t0 + (we - pos));
+        pos += t1 - t0;
+        const int64_t hcs = ((int64_t)h * n_chunks + c) * slices + s;
         const float *tbl = p.cent + ((int64_t)h * p.n_tables + c) * T * C * kD;
         if (smem_tables && T > 0 && hcs != staged) {
             __syncthreads();
             const int nvec = T * C * wq;
             for (int x = tid; x < nvec; x += kDqThreads) {
-                const int r = x / wq, cc = x - r * wq;
-                reinterpret_cast<float4 *>(tab)[r * wq + swz(cc)] =
-                    __ldg(reinterpret_cast<const float4 *>(tbl + (int64_t)r * kD + s * W) + cc);
+                const int rr = x / wq, cc = x - rr * wq;
+                reinterpret_cast<float4 *>(tab)[rr * wq + swz(rr, cc)] =
+                    __ldg(reinterpret_cast<const float4 *>(tbl + (int64_t)rr * kD + s * W) + cc);
             }
             __syncthreads();
             staged = hcs;
         }
-        const int64_t c_lo = c * p.chunk_len;
-        const int64_t i0 = c_lo + b * blk;
-        const int64_t i1 = min(min(c_lo + p.chunk_len, p.N), i0 + blk);
+        const int64_t i0 = c * p.chunk_len + t0;
+        const int64_t i1 = c * p.chunk_len + t1;
         const int ch0 = s * W + sub * kLaneCh;  // the lane's first channel
         int64_t i = i0 + warp * TPW + lane / LPT;
         // running pointers of token i; they advance by tpc tokens per pass
@@ -140,9 +156,10 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         // stage-t centroid values of this lane's 16 channels, cluster j, into 4 float4
         auto table16 = [&](int t, int j, float4 (&a)[4]) {
             if (smem_tables) {
-                const float4 *row = reinterpret_cast<const float4 *>(tab) + (t * C + j) * wq;
+                const int r = t * C + j;
+                const float4 *row = reinterpret_cast<const float4 *>(tab) + r * wq;
 #pragma unroll
-                for (int k = 0; k < 4; k++) a[k] = row[swz(4 * sub + k)];
+                for (int k = 0; k < 4; k++) a[k] = row[swz(r, 4 * sub + k)];
             } else {
                 const float4 *g =
                     reinterpret_cast<const float4 *>(tbl + ((int64_t)t * C + j) * kD + ch0);
@@ -151,20 +168,25 @@ __global__ void __launch_bounds__(kDqThreads, 1)
             }
         };
 
-        Meta cur;
+        // two tokens of metadata in flight ahead of the one being computed
+        Meta cur, nxt;
         if (i < i1) fetch(cur);
+        cp += cstep;
+        sp += sstep;
+        pp += tpc;
+        if (i + tpc < i1) fetch(nxt);
         while (i < i1) {
             const int64_t inext = i + tpc;
-            Meta nxt;
+            Meta nxt2;
             cp += cstep;
             sp += sstep;
             pp += tpc;
-            if (inext < i1) fetch(nxt);
+            if (inext + tpc < i1) fetch(nxt2);
             // Code e of a 16-bit half-word sits at bits BITS*e; kept in place inside the
             // mantissa of 2^23, the float is 2^23 + u * 2^(BITS*e), so subtracting
             // 2^23 + MID * 2^(BITS*e) leaves (u - MID) * 2^(BITS*e) exactly, and
             // sq * 2^-(BITS*e) (exact: a power-of-two rescaling) turns it into sq * q.
-            const float sq = lut[cur.sbyte & 0xFFu];
+            const float sq = e4m3_to_float(cur.sbyte & 0xFFu);
             float se[PER16], ke[PER16];
 #pragma unroll
             for (int e = 0; e < PER16; e++) {
@@ -205,10 +227,20 @@ __global__ void __launch_bounds__(kDqThreads, 1)
                 }
             }
             if constexpr (OUT == DT_F32) {
-                float4 *dst = reinterpret_cast<float4 *>(op);
+                if (wide_stores) {
 #pragma unroll
-                for (int k = 0; k < 4; k++)
-                    dst[k] = make_float4(y[4 * k], y[4 * k + 1], y[4 * k + 2], y[4 * k + 3]);
+                    for (int k = 0; k < 2; k++) {
+                        uint32_t w[8];
+#pragma unroll
+                        for (int x = 0; x < 8; x++) w[x] = __float_as_uint(y[8 * k + x]);
+                        st_v8(op + 32 * k, w);
+                    }
+                } else {
+                    float4 *dst = reinterpret_cast<float4 *>(op);
+#pragma unroll
+                    for (int k = 0; k < 4; k++)
+                        dst[k] = make_float4(y[4 * k], y[4 * k + 1], y[4 * k + 2], y[4 * k + 3]);
+                }
             } else {
                 uint32_t w[8];
 #pragma unroll
@@ -221,12 +253,17 @@ __global__ void __launch_bounds__(kDqThreads, 1)
                         w[k] = *reinterpret_cast<const uint32_t *>(&v2);
                     }
                 }
-                uint4 *dst = reinterpret_cast<uint4 *>(op);
-                dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-                dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+                if (wide_stores) {
+                    st_v8(op, w);
+                } else {
+                    uint4 *dst = reinterpret_cast<uint4 *>(op);
+                    dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+                    dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+                }
             }
             op += ostep;
             cur = nxt;
+            nxt = nxt2;
             i = inext;
         }
     }
@@ -239,21 +276,15 @@ template <int BITS, int OUT, int TT>
 cudaError_t launch_dq(const DPlan &p, int num_sms, int W, size_t table_bytes, bool smem_tables,
                       cudaStream_t st) {
     auto kern = k_dequant<BITS, OUT, TT>;
-    const size_t smem = 256 * 4 + (smem_tables ? table_bytes : 0);
+    const size_t smem = smem_tables ? table_bytes : 16;
+    // 32-byte stores need a 32-byte aligned output and tensor stride
+    const size_t eb = p.out_dtype == DT_F32 ? 4 : 2;
+    const int wide = (reinterpret_cast<uintptr_t>(p.out) % 32 == 0 &&
+                      (p.out_stride * eb) % 32 == 0) ? 1 : 0;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    const int64_t slices = kD / W;
     const int64_t n_chunks = (p.N + p.chunk_len - 1) / p.chunk_len;
-    const int64_t base_units = (int64_t)p.H * n_chunks * slices;
-    // split chunks into token blocks until there are a couple of units per SM
-    int64_t bpc = std::max<int64_t>(1, ((int64_t)num_sms * 2 + base_units - 1) / base_units);
-    const int64_t clen = std::min(p.chunk_len, p.N);
-    int64_t blk = std::max<int64_t>(256, (clen + bpc - 1) / bpc);
-    blk = (blk + 31) / 32 * 32;
-    bpc = (clen + blk - 1) / blk;
-    const int64_t total = base_units * bpc;
-    const int grid = (int)std::min<int64_t>(total, num_sms);
-    kern<<<grid, kDqThreads, smem, st>>>(p, W, n_chunks, bpc, blk, total, smem_tables ? 1 : 0);
+    kern<<<num_sms, kDqThreads, smem, st>>>(p, W, n_chunks, smem_tables ? 1 : 0, wide);
     return cudaGetLastError();
 }
 
