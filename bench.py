@@ -44,13 +44,15 @@ def _peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle samples while the timed region runs."""
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi clock / throttle samples with their own timestamps; summary() keeps the
+    samples taken inside a wall-clock window (the timed region)."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, index: int):
+    def __init__(self, index: int, interval_ms: int = 10):
         self.index = index
+        self.interval_ms = interval_ms
         self.proc = None
         self.lines = []
 
@@ -58,7 +60,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
-                 "--format=csv,noheader,nounits", "-lms", "25"],
+                 "--format=csv,noheader,nounits", "-lms", str(self.interval_ms)],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
@@ -79,19 +81,31 @@ class ClockSampler:
                 self.proc.kill()
             self.thread.join(timeout=2)
 
-    def summary(self):
+    @staticmethod
+    def _epoch(ts: str):
+        import datetime
+        try:
+            return datetime.datetime.strptime(ts.strip(), "%Y/%m/%d %H:%M:%S.%f").timestamp()
+        except ValueError:
+            return None
+
+    def summary(self, t0: float, t1: float):
+        """Samples stamped within [t0, t1] (time.time() seconds)."""
         sm, mx, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for ln in self.lines:
-            parts = [p.strip() for p in ln.split(",")]
-            if len(parts) < 9:
+            parts = [q.strip() for q in ln.split(",")]
+            if len(parts) < 10:
+                continue
+            ts = self._epoch(parts[0])
+            if ts is None or ts < t0 or ts > t1:
                 continue
             try:
-                sm.append(float(parts[1]))
-                mx = float(parts[2])
+                sm.append(float(parts[2]))
+                mx = float(parts[3])
             except ValueError:
                 continue
-            for n, v in zip(names, parts[5:9]):
+            for n, v in zip(names, parts[6:10]):
                 if v.lower().startswith("active"):
                     reasons.add(n)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
@@ -153,8 +167,8 @@ def launches_per_step(w):
 
 # DRAM traffic of one k_assign launch on layer_1p3b_32760 (dram__bytes_read.sum +
 # dram__bytes_write.sum, ncu), valid while the kernel's sources hash to `sources_sha256`.
-ASSIGN_TRAFFIC = {"workload": "layer_1p3b_32760", "bytes": 415293696,
-                  "sources_sha256": "4c2841fa07c46313d0d35fcf6e33d7d5a2eef3be87ec4e0b66b1ead2eaf11c97"}
+ASSIGN_TRAFFIC = {"workload": "layer_1p3b_32760", "bytes": 218442752,
+                  "sources_sha256": "8360d7e03da245020f56a230fbc06293fd0637c1e27b4848aa40aecf0f8a22d7"}
 ASSIGN_SOURCES = ("video_kv_cache_gb300/csrc/k_assign.cu", "video_kv_cache_gb300/csrc/internal.cuh")
 
 
@@ -261,6 +275,7 @@ def run_ours(args, w):
     def dequantize():
         api.dequantize(out, N, torch.bfloat16, out=xhat, status=status)
 
+    clocks = ClockSampler(local).__enter__()  # sampling from before the warm-up
     for _ in range(args.warmup):
         quantize()
         dequantize()
@@ -271,20 +286,22 @@ def run_ours(args, w):
     # flush is outside the per-step events), each step timed with CUDA events
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
            torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    with ClockSampler(local) as clocks:
-        _barrier(world)
-        torch.cuda.synchronize()
-        wall0 = time.perf_counter()
-        for k in range(args.steps):
-            flush.fill_(k & 0xFF)
-            ev[k][0].record(st)
-            quantize()
-            ev[k][1].record(st)
-            dequantize()
-            ev[k][2].record(st)
-        torch.cuda.synchronize()
-        _barrier(world)
-        wall = time.perf_counter() - wall0
+    _barrier(world)
+    torch.cuda.synchronize()
+    epoch0, wall0 = time.time(), time.perf_counter()
+    for k in range(args.steps):
+        flush.fill_(k & 0xFF)
+        ev[k][0].record(st)
+        quantize()
+        ev[k][1].record(st)
+        dequantize()
+        ev[k][2].record(st)
+    torch.cuda.synchronize()
+    _barrier(world)
+    wall = time.perf_counter() - wall0
+    epoch1 = time.time()
+    time.sleep(0.05)  # let the last samples of the window arrive
+    clocks.__exit__(None, None, None)
     q_ms = [a.elapsed_time(b) for a, b, _ in ev]
     step_ms = [a.elapsed_time(c) for a, _, c in ev]
     step_ms_avg = _max_over_ranks(sum(step_ms) / len(step_ms), world)
@@ -348,7 +365,7 @@ def run_ours(args, w):
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms": e2e_ms},
             "gpu_launches": args.steps * launches_per_step(w),
             "wall_s_timed_region": wall,
-            "clocks": clocks.summary(),
+            "clocks": clocks.summary(epoch0, epoch1),
         }
         if not args.no_cpu_baseline and world == 1:
             cb = cpu_baseline(w)
@@ -415,7 +432,7 @@ def run_sweep(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
