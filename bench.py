@@ -429,6 +429,106 @@ def run_sweep(args):
                       "data": "synthetic", "rows": rows}), flush=True)
 
 
+def run_stream(args):
+    """The streaming workload: 60 chunks of 3 frames x 30x52 tokens appended to the caches
+    of 30 layers x 12 heads x K/V (720 tensors).  Chunk 0 is clustered from a cold start,
+    every later chunk is warm-started from the previous chunk's centroid tables, and after
+    every chunk each layer's whole cache so far is reconstructed into a reused buffer.
+    Reports chunk quantize times, the dequant throughput, and (on chunk 1) k-means time and
+    objective for a warm start against cold starts with 2, 6 and 10 rounds."""
+    from video_kv_cache_gb300 import api, qvg
+    from video_kv_cache_gb300 import build as qbuild
+    torch.cuda.set_device(0)
+    qbuild.build()
+    qvg.load()
+    w = synth.workload("stream_30x12_60chunk")
+    dev = torch.device("cuda")
+    L = w.chunk_frames * w.gh * w.gw
+    n_chunks = w.frames // w.chunk_frames
+    H, per_layer = w.H, w.heads * len(w.kinds)
+    cache = api.allocate(H, n_chunks * L, w.C, w.T, w.bits, w.group, n_tables=n_chunks,
+                         device=dev)
+    ws = api.new_workspace(H, L, w.C, w.T, dev)
+    xbuf = torch.empty((per_layer, n_chunks * L, 128), dtype=torch.bfloat16, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    st = torch.cuda.current_stream()
+    hbm = _peaks()[0]
+
+    def layer_view(l):
+        sl = slice(l * per_layer, (l + 1) * per_layer)
+        return api.CompressedKV(cache.codes[sl], cache.scales[sl], cache.pi[sl],
+                                cache.centroids[sl], w.C, w.T, w.bits, w.group)
+
+    layers = [layer_view(l) for l in range(w.layers)]
+    q_ms, d_ms, d_bytes, x1 = [], [], [], None
+    for c in range(n_chunks):
+        Xc = w.make(dev, f0=c * w.chunk_frames, nf=w.chunk_frames)
+        if c == 1:
+            x1 = Xc.clone()
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        e[0].record(st)
+        api.quantize(Xc, w.C, w.T, w.bits, w.group, w.iters if c == 0 else w.warm_iters,
+                     w.seed, warm=None if c == 0 else cache.centroids[:, c - 1],
+                     warm_stride=cache.centroids.stride(0), out=cache, token_offset=c * L,
+                     table_index=c, workspace=ws, status=status)
+        e[1].record(st)
+        n = (c + 1) * L
+        for lv in layers:
+            api.dequantize(lv, n, torch.bfloat16, chunk_len=L, out=xbuf[:, :n], status=status)
+        e[2].record(st)
+        torch.cuda.synchronize()
+        q_ms.append(e[0].elapsed_time(e[1]))
+        d_ms.append(e[1].elapsed_time(e[2]))
+        d_bytes.append(dequant_bytes(H, n, w.C, w.T, w.bits, w.group, n_tables=c + 1))
+        del Xc
+    assert int(status.item()) == 0, "device status %#x" % int(status.item())
+
+    # warm versus cold k-means on chunk 1, into a scratch cache
+    def objective(X, ck):
+        R = X.float()
+        J = []
+        for t in range(w.T):
+            pi = ck.pi[:, t].long()
+            g = torch.gather(ck.centroids[:, 0, t], 1, pi[..., None].expand(-1, -1, 128))
+            R = R - g
+            J.append(float((R.double() ** 2).sum()))
+        return J
+
+    scratch = api.allocate(H, L, w.C, w.T, w.bits, w.group, device=dev)
+    warm_cmp = []
+    for init, iters in (("warm", w.warm_iters), ("cold", 2), ("cold", 6), ("cold", 10)):
+        times = []
+        for _ in range(3):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(st)
+            api.quantize(x1, w.C, w.T, w.bits, w.group, iters, w.seed,
+                         warm=cache.centroids[:, 0] if init == "warm" else None,
+                         warm_stride=cache.centroids.stride(0), out=scratch, workspace=ws,
+                         status=status)
+            e1.record(st)
+            torch.cuda.synchronize()
+            times.append(e0.elapsed_time(e1))
+        warm_cmp.append({"init": init, "iters": iters, "ms": statistics.median(times),
+                         "J_per_stage": objective(x1, scratch)})
+    assert int(status.item()) == 0, "device status %#x" % int(status.item())
+    warm = q_ms[1:]
+    line = {
+        "metric": "streaming: chunk quantize Mtokens/s (warm start); full-cache fused dequant GB/s",
+        "workload": w.name, "tensors": H, "chunks": n_chunks, "tokens_per_chunk": L,
+        "C": w.C, "T": w.T, "bits": w.bits, "group": w.group, "data": "synthetic",
+        "cold_chunk": {"iters": w.iters, "ms": q_ms[0]},
+        "warm_chunk": {"iters": w.warm_iters, "ms_mean": statistics.mean(warm),
+                       "mtokens_s": H * L / (statistics.mean(warm) * 1e-3) / 1e6},
+        "dequant_all_chunks": {"bytes": sum(d_bytes), "ms": sum(d_ms),
+                               "gbs": sum(d_bytes) / (sum(d_ms) * 1e-3) / 1e9},
+        "dequant_last_chunk": {"tokens_per_tensor": n_chunks * L, "ms": d_ms[-1],
+                               "gbs": d_bytes[-1] / (d_ms[-1] * 1e-3) / 1e9,
+                               "pct_hbm": 100.0 * d_bytes[-1] / (d_ms[-1] * 1e-3) / 1e9 / hbm},
+        "kmeans_warm_vs_cold_chunk1": warm_cmp,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -439,10 +539,14 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sweep", action="store_true",
                     help="print the precision sweep (MSE reduction) instead of the timing line")
+    ap.add_argument("--stream", action="store_true",
+                    help="run the 60-chunk streaming workload and print its line")
     args = ap.parse_args()
     w = synth.workload(args.workload)
     if args.sweep:
         run_sweep(args)
+    elif args.stream:
+        run_stream(args)
     elif args.impl == "reference":
         run_reference(args, w)
     else:

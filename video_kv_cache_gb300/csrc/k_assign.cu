@@ -23,9 +23,12 @@
 // k = 1.066 * 2^-11 (one plane) or 1.012 * 2^-15 (two planes).  ||c||^2 in fp32 and the
 // score's own rounding add at most 1.07 * 2^-17 cmax^2, so every score is within E of its
 // exact value, E = 2 |acc - r.c| bound + 1.07 * 2^-17 cmax^2, and any cluster whose score
-// is within 2E of the best score may be the true nearest one.  Those are re-scored exactly
-// (direct fp32 sum of squared differences on the fp32 residual and centroid, k_refine), so
-// the chosen index is that of the true nearest centroid up to fp32 rounding.  A row with
+// is within 2E of the best score may be the true nearest one.  (The GEMM starts from the
+// fp32-rounded stage input, off the fp64 one by at most 2^-24 |r| per channel; that is
+// inside the slack of k.)  Those clusters are re-scored by k_refine, in fp64 on the stage
+// input rebuilt in fp64 wherever fp32 cannot separate them, so the chosen index is that of
+// the nearest centroid up to fp64 rounding: the same choice as an fp64 reference, ties to
+// the lowest index.  A row with
 // ||r|| >= 60000, or a centroid set with cmax >= 60000, could overflow fp16: all of its
 // clusters are re-scored.
 //
@@ -547,11 +550,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // --------------------------------------------------------------------------------------
-// Exact re-scoring of near ties.  One warp per queued token: lane l holds channels
-// 4l..4l+3 of the fp32 residual; each candidate's squared distance is a 4-term partial sum
-// per lane reduced over the warp in a fixed order.  Candidates are visited in increasing
-// cluster order and only a strictly smaller distance replaces the best, so ties go to the
-// lowest index.   grid-stride over the queue, block 256.
+// Re-scoring of near ties.  One warp per queued token; lane l holds channels 4l..4l+3.
+// First every candidate's squared distance is summed in fp32 on the fp32 stage input (a
+// 4-term partial sum per lane, reduced over the warp in a fixed order).  If the best two
+// are further apart than fp32 can blur, that decides.  Otherwise (a tie at fp32
+// resolution, rare) the stage input is rebuilt in fp64 from X and the earlier stages'
+// centroids, by the same subtraction chain as the fp64 reference, and the candidates are
+// scored again in fp64.  Candidates are visited in increasing cluster order and only a
+// strictly smaller distance replaces the best, so ties go to the lowest index.
+// grid-stride over the queue, block 256.
 // --------------------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) k_refine(QPlan p, int t) {
     const int lane = threadIdx.x & 31;
@@ -563,17 +570,20 @@ __global__ void __launch_bounds__(256) k_refine(QPlan p, int t) {
         const RefineReq rq = p.rq[r];
         const int h = rq.h;
         const int64_t i = rq.i;
+        const float *ct = p.cent + h * p.cent_tstride + p.cent_off;
+        const float *c0 = ct + (int64_t)(t - 1) * p.C * kD;
+        // fp32 pass on the fp32 stage input: channels 4*lane..4*lane+3
         float4 x;
         if (t == 1) {
             float v8[8];
             load_x8(p.X, p.in_dtype, h * p.x_stride + i * kD + (lane >> 1) * 8, v8);
-            const int o = (lane & 1) * 4;
-            x = make_float4(v8[o], v8[o + 1], v8[o + 2], v8[o + 3]);
+            const bool up = lane & 1;  // which half of the 8 loaded channels is this lane's
+            x = make_float4(up ? v8[4] : v8[0], up ? v8[5] : v8[1], up ? v8[6] : v8[2],
+                            up ? v8[7] : v8[3]);
         } else {
             x = __ldg(reinterpret_cast<const float4 *>(p.R32 + ((int64_t)h * p.N + i) * kD) + lane);
         }
-        const float *c0 = p.cent + h * p.cent_tstride + p.cent_off + (int64_t)(t - 1) * p.C * kD;
-        float bestD = INFINITY;
+        float bestD = INFINITY, secondD = INFINITY;
         int bestj = 0;
 #pragma unroll
         for (int cb = 0; cb < 8; cb++) {
@@ -589,8 +599,54 @@ __global__ void __launch_bounds__(256) k_refine(QPlan p, int t) {
 #pragma unroll
                 for (int o = 16; o >= 1; o >>= 1) D = __fadd_rn(D, __shfl_xor_sync(0xffffffffu, D, o));
                 if (D < bestD) {
+                    secondD = bestD;
                     bestD = D;
                     bestj = j;
+                } else {
+                    secondD = fminf(secondD, D);
+                }
+            }
+        }
+        // Each fp32 distance is within 2^-21 (relative) of the exact distance of the fp64
+        // stage input (the input's own rounding and the 128-term sum).  A gap wider than
+        // 2^-18 therefore decides; closer calls are settled in fp64 below.
+        if (secondD - bestD <= 0x1p-18f * secondD) {
+            // the stage input rebuilt in fp64: x - C^(1)[pi^(1)] - ... - C^(t-1)[pi^(t-1)],
+            // subtracted in that order
+            double xd[4];
+            {
+                float v8[8];
+                load_x8(p.X, p.in_dtype, h * p.x_stride + i * kD + (lane >> 1) * 8, v8);
+                const bool up = lane & 1;
+#pragma unroll
+                for (int k = 0; k < 4; k++) xd[k] = (double)(up ? v8[4 + k] : v8[k]);
+            }
+            for (int s2 = 1; s2 < t; s2++) {
+                const int js = min((int)p.pi[(int64_t)(h * p.T + s2 - 1) * p.cap + p.tok_off + i], p.C - 1);
+                const float4 c = __ldg(reinterpret_cast<const float4 *>(
+                    ct + ((int64_t)(s2 - 1) * p.C + js) * kD) + lane);
+                xd[0] -= (double)c.x;
+                xd[1] -= (double)c.y;
+                xd[2] -= (double)c.z;
+                xd[3] -= (double)c.w;
+            }
+            double bestDd = INFINITY;
+#pragma unroll
+            for (int cb = 0; cb < 8; cb++) {
+                uint32_t m = rq.cand[cb];
+                while (m) {
+                    const int j = cb * 32 + __ffs(m) - 1;
+                    m &= m - 1u;
+                    const float4 c = __ldg(reinterpret_cast<const float4 *>(c0 + (int64_t)j * kD) + lane);
+                    const double e0 = xd[0] - (double)c.x, e1 = xd[1] - (double)c.y;
+                    const double e2 = xd[2] - (double)c.z, e3 = xd[3] - (double)c.w;
+                    double D = __fma_rn(e3, e3, __fma_rn(e2, e2, __fma_rn(e1, e1, e0 * e0)));
+#pragma unroll
+                    for (int o = 16; o >= 1; o >>= 1) D += __shfl_xor_sync(0xffffffffu, D, o);
+                    if (D < bestDd) {
+                        bestDd = D;
+                        bestj = j;
+                    }
                 }
             }
         }

@@ -14,9 +14,10 @@ channels.  The field below has exactly that structure:
 
 with M = 32 random Fourier features of a squared-exponential kernel (w ~ N(0, I3),
 a ~ N(0, 1), phi ~ U[0, 2pi)), so every channel is marginally close to N(0, 1) and
-correlated over ls = 6 tokens in space and lt = 2 frames in time.  Every element gets
-iid N(0, 0.1^2) noise from a counter-based hash of (seed, tensor, token, channel), so a
-chunk of frames is the same slice of the same field whichever call produces it.  Four
+correlated over ls = 6 tokens in space and lt = 8 latent frames in time (a slowly
+changing scene: consecutive 3-frame chunks are about 0.93 correlated).  Every element
+gets iid N(0, 0.1^2) noise from a counter-based hash of (seed, tensor, token, channel), so
+a chunk of frames is the same slice of the same field whichever call produces it.  Four
 channels per tensor (chosen by the seed) are outliers: A_k + 10 z_k with
 A_k = +-U(60, 90), clipped to |x| <= 100.  Value tensors are the same construction
 scaled by 10 (clip 1000).  The result is cast to fp16 / bf16 with round-to-nearest-even.
@@ -34,7 +35,7 @@ import torch
 
 M_FEATURES = 32
 LEN_SPACE = 6.0
-LEN_TIME = 2.0
+LEN_TIME = 8.0
 D_HEAD = 128
 N_OUTLIERS = 4
 
@@ -69,11 +70,13 @@ def _mix(h: torch.Tensor) -> torch.Tensor:
     return h
 
 
-def _noise(seed: int, tid: int, gtok: torch.Tensor) -> torch.Tensor:
-    """iid N(0,1) per (token, channel) from a counter hash; gtok is [N] global token ids."""
+def _noise(seed: int, tids: Sequence[int], gtok: torch.Tensor) -> torch.Tensor:
+    """iid N(0,1) per (tensor, token, channel) from a counter hash; gtok is [N] global token
+    ids.  Returns [len(tids)][N][128]."""
     k = torch.arange(D_HEAD, device=gtok.device, dtype=torch.int64)
-    key = (gtok[:, None] * D_HEAD + k[None, :]) * 2
-    base = (int(seed) * 0x9E3779B1 + int(tid) * 0x85EBCA77) & ((1 << 62) - 1)
+    key = ((gtok[:, None] * D_HEAD + k[None, :]) * 2)[None]
+    base = torch.tensor([(int(seed) * 0x9E3779B1 + int(t) * 0x85EBCA77) & ((1 << 62) - 1)
+                         for t in tids], device=gtok.device, dtype=torch.int64)[:, None, None]
     h1 = _mix(key + base)
     h2 = _mix(key + 1 + base)
     u1 = (((h1 >> 8) & _MASK24).to(torch.float32) + 0.5) / float(1 << 24)
@@ -82,8 +85,10 @@ def _noise(seed: int, tid: int, gtok: torch.Tensor) -> torch.Tensor:
 
 
 def kv_tensor(seed: int, tids: Sequence[int], f0: int, nf: int, gh: int, gw: int,
-              dtype=torch.bfloat16, device="cpu") -> torch.Tensor:
-    """[len(tids)][nf*gh*gw][128] tensor of frames [f0, f0+nf) of the field, raster order."""
+              dtype=torch.bfloat16, device="cpu", batch: int = 32) -> torch.Tensor:
+    """[len(tids)][nf*gh*gw][128] tensor of frames [f0, f0+nf) of the field, raster order.
+    Tensors are generated `batch` at a time; each tensor's values depend only on (seed, its
+    id, the token), not on the batching."""
     dev = torch.device(device)
     f = torch.arange(f0, f0 + nf, device=dev, dtype=torch.float32)
     y = torch.arange(gh, device=dev, dtype=torch.float32)
@@ -92,19 +97,23 @@ def kv_tensor(seed: int, tids: Sequence[int], f0: int, nf: int, gh: int, gw: int
     pos = torch.stack([ff.reshape(-1) / LEN_TIME, yy.reshape(-1) / LEN_SPACE,
                        xx.reshape(-1) / LEN_SPACE], dim=1)
     gtok = torch.arange(f0 * gh * gw, (f0 + nf) * gh * gw, device=dev, dtype=torch.int64)
+    tids = list(tids)
     out = torch.empty((len(tids), pos.shape[0], D_HEAD), dtype=dtype, device=dev)
-    for n, tid in enumerate(tids):
-        omega, w, out_ch, amp = _params(seed, tid)
-        theta = pos @ torch.as_tensor(omega, dtype=torch.float32, device=dev).T
-        feats = torch.cat([torch.cos(theta), torch.sin(theta)], dim=1)
-        z = feats @ torch.as_tensor(w, dtype=torch.float32, device=dev)
-        v = z + 0.1 * _noise(seed, tid, gtok)
-        oc = torch.as_tensor(out_ch, device=dev, dtype=torch.int64)
-        v[:, oc] = torch.as_tensor(amp, dtype=torch.float32, device=dev) + 10.0 * v[:, oc]
+    for b0 in range(0, len(tids), batch):
+        bt = tids[b0:b0 + batch]
+        prm = [_params(seed, t) for t in bt]
+        omega = torch.as_tensor(np.stack([q[0] for q in prm]), dtype=torch.float32, device=dev)
+        w = torch.as_tensor(np.stack([q[1] for q in prm]), dtype=torch.float32, device=dev)
+        theta = torch.matmul(pos[None], omega.transpose(1, 2))          # [G][N][M]
+        feats = torch.cat([torch.cos(theta), torch.sin(theta)], dim=2)  # [G][N][2M]
+        v = torch.matmul(feats, w) + 0.1 * _noise(seed, bt, gtok)       # [G][N][128]
+        for g, q in enumerate(prm):
+            oc = torch.as_tensor(q[2], device=dev, dtype=torch.int64)
+            v[g, :, oc] = torch.as_tensor(q[3], dtype=torch.float32, device=dev) + 10.0 * v[g, :, oc]
         v = v.clamp(-100.0, 100.0)
-        if tid % 2 == 1:
-            v = v * 10.0
-        out[n] = v.to(dtype)
+        vk = torch.tensor([t % 2 == 1 for t in bt], device=dev)[:, None, None]
+        v = torch.where(vk, v * 10.0, v)
+        out[b0:b0 + len(bt)] = v.to(dtype)
     return out
 
 
