@@ -148,7 +148,7 @@ cudaError_t launch_prep(const QPlan &p, int t, cudaStream_t st);
 cudaError_t launch_centroid_planes(const QPlan &p, int t, cudaStream_t st);
 cudaError_t launch_cluster_means(const QPlan &p, int t, bool planes, cudaStream_t st);
 constexpr int kSortBlock = 256;  // tokens per block of the counting sort
-constexpr int kChunk = 64;       // sorted positions summed by one warp
+constexpr int kChunk = 32;       // sorted positions summed by one warp
 cudaError_t launch_encode(const QPlan &p, cudaStream_t st);
 
 // TMA tensor maps of the assignment GEMM: A = residual planes, B = centroid planes.

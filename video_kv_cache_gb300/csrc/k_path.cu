@@ -13,6 +13,8 @@
 //     Algorithm-System Co-design.
 #include <cuda_fp8.h>
 
+#include <type_traits>
+
 #include "internal.cuh"
 
 namespace qvg {
@@ -262,9 +264,9 @@ cudaError_t launch_centroid_planes(const QPlan &p, int t, cudaStream_t st) {
 //
 // 1. A stable counting sort groups the token indices by cluster, increasing within a
 //    cluster (histogram per block of 256 tokens, scans, scatter with in-block ranks).
-// 2. The sorted positions are cut into chunks of 64; one warp adds each run of equal
+// 2. The sorted positions are cut into chunks of 32; one warp adds each run of equal
 //    cluster inside its chunk with error-free TwoSum accumulation (sum + running error,
-//    both fp32) in sorted order (lane l holds channels 4l..4l+3, 16 rows in flight).
+//    both fp32) in sorted order (lane l holds channels 4l..4l+3).
 // 3. One warp per cluster adds its pieces (one, or one per chunk it spans) in chunk
 //    order, forms the mean, and writes the centroid with the fp16 GEMM planes of
 //    C_j - mu and ||C_j - mu||^2 for the next assignment; empty clusters keep their
@@ -405,14 +407,17 @@ __device__ __forceinline__ void write_centroid(const QPlan &p, int h, int t, int
     if (lane == 0) p.cn[(int64_t)h * p.Cpad + j] = ss;
 }
 
-// One warp per chunk of 64 cluster-sorted positions: the rows of each run (same cluster)
-// are added with TwoSum in sorted order, 16 rows in flight.  A run that is a whole cluster
+// One warp per chunk of 32 cluster-sorted positions: the rows of each run (same cluster)
+// are added with TwoSum in sorted order, the next batch's loads in flight.  A run that is a whole cluster
 // leaves its (sum, error) in the cluster's slot; a run that crosses the chunk's start or end
 // leaves it in the chunk's first / last slot.  k_cluster_finalize turns them into means.
+// Occupancy decides this kernel's speed (each warp's sum is a sequential chain), so the
+// batches are short and the CTAs per SM many: 4 for 16-bit rows (8-row batches), 6 for
+// fp32 rows (2-row batches).
 template <int SRC>  // 0: X bf16, 1: X fp32, 2: R32, 3: X fp16
-__global__ void __launch_bounds__(256, 2) k_chunk_sums(QPlan p, int t) {
+__global__ void __launch_bounds__(256, (SRC == 0 || SRC == 3) ? 4 : 6) k_chunk_sums(QPlan p, int t) {
     constexpr bool NARROW = SRC == 0 || SRC == 3;  // 16-bit input rows: 8 bytes a lane
-    constexpr int ROWS = NARROW ? 32 : 16;         // rows whose loads are in flight
+    constexpr int ROWS = NARROW ? 8 : 2;           // rows of a batch
     const int lane = threadIdx.x & 31;
     const int h = blockIdx.y;
     const int k = blockIdx.x * 8 + (threadIdx.x >> 5);
@@ -452,25 +457,21 @@ __global__ void __launch_bounds__(256, 2) k_chunk_sums(QPlan p, int t) {
         reinterpret_cast<float4 *>(dst)[lane] = make_float4(s[0], s[1], s[2], s[3]);
         reinterpret_cast<float4 *>(dst + kD)[lane] = make_float4(e[0], e[1], e[2], e[3]);
     };
-    // the positions of a batch are compile-time constants: row ids come from fixed lanes
-#pragma unroll
-    for (int k1 = 0; k1 < kChunk; k1 += ROWS) {
-        if (k1 >= nk) break;
-        // all loads of the batch are issued before any is used: raw words only here
-        float4 raw[NARROW ? 1 : ROWS];
-        uint2 raw16[NARROW ? ROWS : 1];
+    using Raw = typename std::conditional<NARROW, uint2, float4>::type;
+    // raw words of the ROWS rows starting at sorted position k1 (zero past the chunk)
+    auto load_batch = [&](int k1, Raw (&raw)[ROWS]) {
+        const int idsel = k1 < 32 ? idr[0] : idr[1];
 #pragma unroll
         for (int u = 0; u < ROWS; u++) {
-            const int q = k1 + u;
-            const int64_t row = __shfl_sync(0xffffffffu, idr[q >> 5], q & 31);
+            const int64_t row = __shfl_sync(0xffffffffu, idsel, (k1 + u) & 31);
             if constexpr (NARROW) {
-                raw16[u] = make_uint2(0u, 0u);
-                if (q < nk)
-                    raw16[u] = __ldg(reinterpret_cast<const uint2 *>(
+                raw[u] = make_uint2(0u, 0u);
+                if (k1 + u < nk)
+                    raw[u] = __ldg(reinterpret_cast<const uint2 *>(
                         static_cast<const uint16_t *>(p.X) + h * p.x_stride + row * kD) + lane);
             } else {
                 raw[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (q < nk) {
+                if (k1 + u < nk) {
                     if constexpr (SRC == 2)
                         raw[u] = __ldg(reinterpret_cast<const float4 *>(
                             p.R32 + ((int64_t)h * p.N + row) * kD) + lane);
@@ -480,29 +481,37 @@ __global__ void __launch_bounds__(256, 2) k_chunk_sums(QPlan p, int t) {
                 }
             }
         }
+    };
+    // one batch of raw words in registers, the next batch's loads already in flight
+    Raw cur[ROWS], nxt[ROWS];
+    load_batch(0, cur);
+#pragma unroll 1
+    for (int k1 = 0; k1 < nk; k1 += ROWS) {
+        if (k1 + ROWS < nk) load_batch(k1 + ROWS, nxt);
+        const uint32_t bm = (k1 < 32 ? brk[0] : brk[1]) >> (k1 & 31);
+        const int crsel = k1 < 32 ? cr[0] : cr[1];
 #pragma unroll
         for (int u = 0; u < ROWS; u++) {
-            const int q = k1 + u;
-            if (q < nk) {
+            if (k1 + u < nk) {
                 float v[4];
                 if constexpr (SRC == 0) {
-                    const uint32_t wx = raw16[u].x, wy = raw16[u].y;
+                    const uint32_t wx = cur[u].x, wy = cur[u].y;
                     v[0] = __uint_as_float(wx << 16);
                     v[1] = __uint_as_float(wx & 0xFFFF0000u);
                     v[2] = __uint_as_float(wy << 16);
                     v[3] = __uint_as_float(wy & 0xFFFF0000u);
                 } else if constexpr (SRC == 3) {
-                    const uint32_t wx = raw16[u].x, wy = raw16[u].y;
+                    const uint32_t wx = cur[u].x, wy = cur[u].y;
                     const float2 f0 = __half22float2(*reinterpret_cast<const __half2 *>(&wx));
                     const float2 f1 = __half22float2(*reinterpret_cast<const __half2 *>(&wy));
                     v[0] = f0.x; v[1] = f0.y; v[2] = f1.x; v[3] = f1.y;
                 } else {
-                    v[0] = raw[u].x; v[1] = raw[u].y; v[2] = raw[u].z; v[3] = raw[u].w;
+                    v[0] = cur[u].x; v[1] = cur[u].y; v[2] = cur[u].z; v[3] = cur[u].w;
                 }
-                if ((brk[q >> 5] >> (q & 31)) & 1u) {  // warp-uniform
-                    if (run_c >= 0) stash(q);
-                    run_c = __shfl_sync(0xffffffffu, cr[q >> 5], q & 31);
-                    run_start = q;
+                if ((bm >> u) & 1u) {  // warp-uniform
+                    if (run_c >= 0) stash(k1 + u);
+                    run_c = __shfl_sync(0xffffffffu, crsel, (k1 + u) & 31);
+                    run_start = k1 + u;
 #pragma unroll
                     for (int r = 0; r < 4; r++) s[r] = e[r] = 0.f;
                 }
@@ -510,6 +519,8 @@ __global__ void __launch_bounds__(256, 2) k_chunk_sums(QPlan p, int t) {
                 for (int r = 0; r < 4; r++) acc_two_sum(s[r], e[r], v[r]);
             }
         }
+#pragma unroll
+        for (int u = 0; u < ROWS; u++) cur[u] = nxt[u];
     }
     if (run_c >= 0) stash(nk);
 }
