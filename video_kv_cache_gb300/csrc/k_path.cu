@@ -134,7 +134,7 @@ cudaError_t launch_centre(const QPlan &p, int t, cudaStream_t st) {
 //   dnorm  = ||A - (r - mu)||, fp32      (the same)
 // grid (blocks per tensor, H), block 256 = 16 tokens x 16 chunks of 8 channels.
 // --------------------------------------------------------------------------------------
-constexpr int kPrepTokens = 512;
+constexpr int kPrepTokens = 64;
 
 __global__ void __launch_bounds__(256) k_prep(QPlan p, int t) {
     const int h = blockIdx.y;
@@ -612,16 +612,20 @@ cudaError_t launch_cluster_means(const QPlan &p, int t, bool planes, cudaStream_
 //   finite), q = clamp(rne(r / s_q), -qmax, qmax), u = q + 2^(b-1); s_q == 0 gives u = 2^(b-1).
 // grid-stride over tokens, block 256 = 16 tokens x 16 chunks.
 // --------------------------------------------------------------------------------------
-constexpr int kEncTokens = 256;
+constexpr int kEncTokens = 32;
 
+// TT: the number of stages when it is 0..4 (the stage loop unrolled), -1 for any T.
+template <int BITS, int TT>
 __global__ void __launch_bounds__(256) k_encode(QPlan p) {
+    constexpr int QMAX = (1 << (BITS - 1)) - 1, MID = 1 << (BITS - 1);
+    const int T = TT >= 0 ? TT : p.T;
     const int h = blockIdx.y;
     const int c8 = threadIdx.x & 15;
     const int lpg = p.group >> 3;  // lanes per scale group (2, 4, 8)
-    const int qmax = (1 << (p.bits - 1)) - 1, mid = 1 << (p.bits - 1);
     const int64_t i0 = (int64_t)blockIdx.x * kEncTokens;
     const int64_t i1 = min(p.N, i0 + kEncTokens);
-    bool finite = true, bad_index = false;
+    float nanprobe = 0.f;  // becomes NaN if any input is NaN or infinite (x * 0)
+    bool bad_index = false;
     for (int64_t ib = i0; ib < i1; ib += 16) {
         // the loop bound is uniform over the block, so every lane reaches the shuffles;
         // rows past the end compute on zeros and store nothing
@@ -636,12 +640,13 @@ __global__ void __launch_bounds__(256) k_encode(QPlan p) {
         }
 #pragma unroll
         for (int q = 0; q < 8; q++) {
-            finite &= isfinite(x[q]);
+            nanprobe = __fmaf_rn(x[q], 0.f, nanprobe);
             s[q] = x[q];
             e[q] = 0.f;
         }
-        for (int st = 1; valid && st <= p.T; st++) {
-            int pj = p.pi[(int64_t)(h * p.T + st - 1) * p.cap + p.tok_off + i];
+        // r = x - C^(1)[pi^(1)] - ... - C^(T)[pi^(T)] rounded once (TwoSum chain); the
+        // cluster indices are loaded first so that their loads overlap
+        auto subtract = [&](int st, int pj) {
             if (pj >= p.C) {
                 pj = p.C - 1;
                 bad_index = true;
@@ -649,17 +654,24 @@ __global__ void __launch_bounds__(256) k_encode(QPlan p) {
             float c[8];
             load_f8(p.cent + h * p.cent_tstride + p.cent_off + (int64_t)(st - 1) * p.C * kD +
                         (int64_t)pj * kD + c8 * 8, c);
-            if (p.T == 1) {
-                // one subtraction is already a single rounding of the exact residual
 #pragma unroll
-                for (int q = 0; q < 8; q++) s[q] = __fsub_rn(s[q], c[q]);
+            for (int q = 0; q < 8; q++) {
+                float err;
+                two_sum(s[q], -c[q], s[q], err);
+                e[q] = __fadd_rn(e[q], err);
+            }
+        };
+        if (valid) {
+            if constexpr (TT >= 0) {
+                int pjs[TT > 0 ? TT : 1];
+#pragma unroll
+                for (int st = 1; st <= TT; st++)
+                    pjs[st - 1] = p.pi[(int64_t)(h * p.T + st - 1) * p.cap + p.tok_off + i];
+#pragma unroll
+                for (int st = 1; st <= TT; st++) subtract(st, pjs[st - 1]);
             } else {
-#pragma unroll
-                for (int q = 0; q < 8; q++) {
-                    float err;
-                    two_sum(s[q], -c[q], s[q], err);
-                    e[q] = __fadd_rn(e[q], err);
-                }
+                for (int st = 1; st <= T; st++)
+                    subtract(st, p.pi[(int64_t)(h * p.T + st - 1) * p.cap + p.tok_off + i]);
             }
         }
         float r[8], a = 0.f;
@@ -669,41 +681,74 @@ __global__ void __launch_bounds__(256) k_encode(QPlan p) {
             a = fmaxf(a, fabsf(r[q]));
         }
         for (int o = 1; o < lpg; o <<= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
-        const float sc = __fdiv_rn(a, (float)qmax);
+        const float sc = QMAX == 1 ? a : __fdiv_rn(a, (float)QMAX);  // a / qmax, IEEE
         const __nv_fp8_storage_t sb = __nv_cvt_float_to_fp8(sc, __NV_SATFINITE, __NV_E4M3);
         const float sq = __half2float(__half(__nv_cvt_fp8_to_halfraw(sb, __NV_E4M3)));
-        // q = rne(r / s_q) with the IEEE quotient.  r * (1/s_q) is within 1.5 ulp of that
-        // quotient, so it gives the same rounding except within a few ulps of a half-integer;
-        // there the quotient is recomputed with a correctly rounded division.
-        const float inv = sq != 0.f ? __frcp_rn(sq) : 0.f;
+        // q = clamp(rne(r / s_q)) with the IEEE quotient.  r times an approximate
+        // reciprocal (a few ulps) gives the same rounding except close to a half-integer;
+        // there the quotient is recomputed with a correctly rounded division.  Adding
+        // 1.5 * 2^23 to the clamped quotient rounds it to an integer (half to even) and
+        // leaves that integer in the low mantissa bits.
         uint32_t word = 0;
+        if (sq != 0.f) {
+            constexpr float kRound = 12582912.f;  // 1.5 * 2^23
+            float inv;
+            asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(inv) : "f"(sq));
+            float tq[8];
+            uint32_t close = 0;  // elements whose quotient is near a half-integer
 #pragma unroll
-        for (int q = 0; q < 8; q++) {
-            int u = mid;
-            if (sq != 0.f) {
-                float v = __fmul_rn(r[q], inv);
-                if (fabsf(fabsf(v - rintf(v)) - 0.5f) < 0x1p-17f) v = __fdiv_rn(r[q], sq);
-                u = __float2int_rn(fminf(fmaxf(v, (float)-qmax), (float)qmax)) + mid;
+            for (int q = 0; q < 8; q++) {
+                const float v = fminf(fmaxf(__fmul_rn(r[q], inv), (float)-QMAX), (float)QMAX);
+                tq[q] = __fadd_rn(v, kRound);
+                const float d = __fsub_rn(v, __fsub_rn(tq[q], kRound));  // v - rne(v)
+                close |= (fabsf(d) > 0.5f - 0x1p-17f ? 1u : 0u) << q;
             }
-            word |= (uint32_t)u << (q * p.bits);
+            if (close) {  // rare
+#pragma unroll 1
+                for (int q = 0; q < 8; q++)
+                    if ((close >> q) & 1u)
+                        tq[q] = __fadd_rn(fminf(fmaxf(__fdiv_rn(r[q], sq), (float)-QMAX), (float)QMAX),
+                                          kRound);
+            }
+#pragma unroll
+            for (int q = 0; q < 8; q++) {
+                const int qi = (int)(__float_as_uint(tq[q]) - 0x4B400000u);  // rne(v)
+                word |= (uint32_t)(qi + MID) << (q * BITS);
+            }
+        } else {
+#pragma unroll
+            for (int q = 0; q < 8; q++) word |= (uint32_t)MID << (q * BITS);
         }
         if (valid) {
             const int64_t orow = (int64_t)h * p.cap + p.tok_off + i;
-            if (p.bits == 2)
+            if constexpr (BITS == 2)
                 *reinterpret_cast<uint16_t *>(p.codes + orow * (kD / 4) + c8 * 2) = (uint16_t)word;
             else
                 *reinterpret_cast<uint32_t *>(p.codes + orow * (kD / 2) + c8 * 4) = word;
             if ((c8 & (lpg - 1)) == 0) p.scales[orow * (kD / p.group) + c8 / lpg] = sb;
         }
     }
-    if (!finite) or_status(p.status, QVG_DEV_NONFINITE);
-    if (bad_index) or_status(p.status, QVG_DEV_BAD_INDEX);
+    if (__any_sync(0xffffffffu, nanprobe != nanprobe) && (threadIdx.x & 31) == 0)
+        or_status(p.status, QVG_DEV_NONFINITE);
+    if (__any_sync(0xffffffffu, bad_index) && (threadIdx.x & 31) == 0) or_status(p.status, QVG_DEV_BAD_INDEX);
+}
+
+template <int BITS>
+static cudaError_t launch_encode_b(const QPlan &p, cudaStream_t st) {
+    const dim3 grid((unsigned)((p.N + kEncTokens - 1) / kEncTokens), p.H);
+    switch (p.T) {
+        case 0: k_encode<BITS, 0><<<grid, 256, 0, st>>>(p); break;
+        case 1: k_encode<BITS, 1><<<grid, 256, 0, st>>>(p); break;
+        case 2: k_encode<BITS, 2><<<grid, 256, 0, st>>>(p); break;
+        case 3: k_encode<BITS, 3><<<grid, 256, 0, st>>>(p); break;
+        case 4: k_encode<BITS, 4><<<grid, 256, 0, st>>>(p); break;
+        default: k_encode<BITS, -1><<<grid, 256, 0, st>>>(p); break;
+    }
+    return cudaGetLastError();
 }
 
 cudaError_t launch_encode(const QPlan &p, cudaStream_t st) {
-    dim3 grid((unsigned)((p.N + kEncTokens - 1) / kEncTokens), p.H);
-    k_encode<<<grid, 256, 0, st>>>(p);
-    return cudaGetLastError();
+    return p.bits == 2 ? launch_encode_b<2>(p, st) : launch_encode_b<4>(p, st);
 }
 
 }  // namespace qvg
