@@ -24,7 +24,9 @@ namespace qvg {
 // shuffle of 0..N-1 driven by SplitMix64 (Steele, Lea and Flood, 2014, with the constants
 // Vigna published), state seed ^ (tensor_id * 0x9E3779B97F4A7C15) ^ t.  Only the touched
 // positions of the permutation are stored: positions < C directly, the others in a small
-// open-addressing table.   grid (T, H), one warp; lane 0 runs the sequential shuffle.
+// open-addressing table.  The k-th SplitMix64 output depends only on state + k * gamma, so
+// the warp draws all C picks and their modulo reductions in parallel first; lane 0 then
+// applies the swaps in order.   grid (T, H), one warp.
 // --------------------------------------------------------------------------------------
 __device__ __forceinline__ uint64_t splitmix64_next(uint64_t &state) {
     uint64_t z = (state += 0x9E3779B97F4A7C15ULL);
@@ -38,17 +40,22 @@ constexpr int kHashSlots = 1024;
 __global__ void k_init_indices(QPlan p, uint64_t seed, int64_t tid_base) {
     const int t = blockIdx.x + 1, h = blockIdx.y, lane = threadIdx.x;
     __shared__ int lo[kMaxC];
+    __shared__ int pick[kMaxC];  // position swapped with position j at step j
     __shared__ int keys[kHashSlots];
     __shared__ int vals[kHashSlots];
-    for (int x = lane; x < p.C; x += 32) lo[x] = x;
+    const uint64_t state0 = seed ^ ((uint64_t)(tid_base + h) * 0x9E3779B97F4A7C15ULL) ^ (uint64_t)t;
+    for (int x = lane; x < p.C; x += 32) {
+        lo[x] = x;
+        uint64_t st = state0 + (uint64_t)x * 0x9E3779B97F4A7C15ULL;  // state before draw x
+        const uint64_t r = splitmix64_next(st);
+        pick[x] = x + (int)(r % (uint64_t)(p.N - x));
+    }
     for (int x = lane; x < kHashSlots; x += 32) keys[x] = -1;
     __syncwarp();
     if (lane != 0) return;
-    uint64_t state = seed ^ ((uint64_t)(tid_base + h) * 0x9E3779B97F4A7C15ULL) ^ (uint64_t)t;
     int *out = p.init_idx + (int64_t)(h * p.T + (t - 1)) * p.C;
     for (int j = 0; j < p.C; j++) {
-        const uint64_t r = splitmix64_next(state);
-        const int k = j + (int)(r % (uint64_t)(p.N - j));
+        const int k = pick[j];
         int vk;
         int slot = -1;
         if (k < p.C) {
