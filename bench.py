@@ -167,8 +167,8 @@ def launches_per_step(w):
 
 # DRAM traffic of one k_assign launch on layer_1p3b_32760 (dram__bytes_read.sum +
 # dram__bytes_write.sum, ncu), valid while the kernel's sources hash to `sources_sha256`.
-ASSIGN_TRAFFIC = {"workload": "layer_1p3b_32760", "bytes": 218442752,
-                  "sources_sha256": "8360d7e03da245020f56a230fbc06293fd0637c1e27b4848aa40aecf0f8a22d7"}
+ASSIGN_TRAFFIC = {"workload": "layer_1p3b_32760", "bytes": 219088640,
+                  "sources_sha256": "3ae3c515f29fd1d66a028661c1caae99da8aac337caa96c4c3224039dd8f554c"}
 ASSIGN_SOURCES = ("video_kv_cache_gb300/csrc/k_assign.cu", "video_kv_cache_gb300/csrc/internal.cuh")
 
 
