@@ -7,7 +7,8 @@
   * every token identical: all distances tie, so every assignment must go to the lowest
     index, and every stage after the first sees a zero residual;
   * the largest cluster count with C = N = 256: each token is its own cluster, so the
-    residual and every scale are zero and the reconstruction is exact.
+    residual and every scale are zero and the reconstruction is exact;
+  * a stored cluster index >= C (a corrupted cache): flagged and clamped to C - 1.
 """
 import numpy as np
 import pytest
@@ -95,3 +96,21 @@ def test_max_clusters_equal_tokens_is_lossless():
     np.testing.assert_array_equal(x32, oracle.decode_input(X))
     for h in range(2):
         assert sorted(g["pi"][h, 0].tolist()) == list(range(256))
+
+
+def test_out_of_range_cluster_index_is_flagged_and_clamped():
+    X = synth.kv_tensor(44, [0], 0, 1, 10, 30, torch.bfloat16, "cpu")  # N = 300
+    C, T, bits, group = 16, 2, 2, 32
+    ckv, _, st = _run(X, C, T, bits, group, 2, 5)
+    assert st == 0
+    ckv.pi[0, 1, 7] = 200  # a stored index >= C, as a corrupted cache could hold
+    ckv.pi[0, 0, 9] = 255
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    x32 = api.dequantize(ckv, out_dtype=torch.float32, status=status).cpu().numpy()
+    torch.cuda.synchronize()
+    assert int(status.item()) & qvg.QVG_DEV_BAD_INDEX
+    g = _np(ckv)
+    pi = np.minimum(g["pi"][0], C - 1)  # the documented clamp
+    want = oracle.dequantize(g["codes"][0], g["scales"][0], pi, g["centroids"][0, 0], bits, group)
+    S = np.abs(want) + np.abs(g["centroids"][0, 0]).max()
+    assert np.all(np.abs(x32[0] - want) <= (T + 1) * np.spacing(S.astype(np.float32)))
