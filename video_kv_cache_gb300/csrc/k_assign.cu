@@ -460,11 +460,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float err = 2.f * (kDnRel * dn * cmax + kRnRel * rn * cmax +
                                      0x1p-20f * (rn + dn)) +
                               0x1.1p-17f * cmax2;
-            // an untrusted row (fp16 operands may have overflowed, its scores may be inf or
-            // NaN) re-scores every cluster, whatever its scores say
+            // An untrusted row (fp16 operands may have overflowed, so its scores may be inf
+            // or NaN) gets lim = +inf.  The tests below are written as !(x > lim), which is
+            // true for every score of such a row, NaN included, so it re-scores every
+            // cluster; for a trusted row (finite scores) it is x <= lim.
             const bool trusted = rn < kFp16Safe && cmax < kFp16Safe;
-            const float lim = best + (trusted ? 2.f * err + 1e-30f : INFINITY);
-            const bool need = valid && (!trusted || second <= lim);
+            const float lim = trusted ? best + (2.f * err + 1e-30f) : INFINITY;
+            const bool need = valid && !(second > lim);
             const bool any_need = __any_sync(0xffffffffu, need);  // the same in both warps
             // Candidate pass: only chunks whose minimum is within the limit for some row.
             uint32_t cand0 = 0u, cand1 = 0u, cand2 = 0u, cand3 = 0u;
@@ -472,7 +474,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
                 for (int c = 0; c < ch_hi - ch_lo; c++) {
                     const float cm = c == 0 ? cmin0 : c == 1 ? cmin1 : c == 2 ? cmin2 : cmin3;
-                    if (!__any_sync(0xffffffffu, need && (!trusted || cm <= lim))) continue;
+                    if (!__any_sync(0xffffffffu, need && !(cm > lim))) continue;
                     const int cb = ch_lo + c;
                     float v[32];
                     tc_ld32(taddr + cb * 32, v);
@@ -484,7 +486,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int u = 0; u < 4; u++) {
                             const float sc = __fmaf_rn(-2.f, v[q + u], cc[u]);
-                            if ((!trusted || sc <= lim) && cb * 32 + q + u < C) w |= 1u << (q + u);
+                            if (!(sc > lim) && cb * 32 + q + u < C) w |= 1u << (q + u);
                         }
                     }
                     if (!need) w = 0u;
@@ -765,7 +767,7 @@ cudaError_t launch_assign(const QPlan &p, const AssignMaps *maps, int t, int num
 }
 
 cudaError_t launch_refine(const QPlan &p, int t, int num_sms, cudaStream_t st) {
-    k_refine<<<num_sms * 2, 256, 0, st>>>(p, t);
+    k_refine<<<num_sms * 8, 256, 0, st>>>(p, t);
     return cudaGetLastError();
 }
 
