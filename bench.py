@@ -226,11 +226,15 @@ def run_reference(args, w):
     print(json.dumps(line), flush=True)
 
 
-def _config(w, world):
-    return {"workload": w.name, "tensors": w.H, "tokens": w.N, "C": w.C, "T": w.T,
-            "bits": w.bits, "group": w.group, "iters": w.iters,
-            "parallelism": "dp%d (tensors sharded, no exchange)" % world,
-            "l2": "flushed (%d MiB write) before every timed step" % (L2_FLUSH_BYTES >> 20)}
+def _config(w, world, graph=None):
+    cfg = {"workload": w.name, "tensors": w.H, "tokens": w.N, "C": w.C, "T": w.T,
+           "bits": w.bits, "group": w.group, "iters": w.iters,
+           "parallelism": "dp%d (tensors sharded, no exchange)" % world,
+           "l2": "flushed (%d MiB write) before every timed step" % (L2_FLUSH_BYTES >> 20)}
+    if graph is not None:
+        cfg["launch"] = ("CUDA graph replay of one quantize and one dequantize per step"
+                         if graph else "direct calls")
+    return cfg
 
 
 def _event_ms(st, fn, reps, flush=None):
@@ -276,9 +280,26 @@ def run_ours(args, w):
         api.dequantize(out, N, torch.bfloat16, out=xhat, status=status)
 
     clocks = ClockSampler(local).__enter__()  # sampling from before the warm-up
+    run_q, run_d = quantize, dequantize
+    if not args.no_graph:
+        # one quantize and one dequantize captured as CUDA graphs: the same kernels,
+        # replayed without the host launch gaps between the 151 launches of a step
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            quantize()
+            dequantize()
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        g_q, g_d = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_q):
+            quantize()
+        with torch.cuda.graph(g_d):
+            dequantize()
+        run_q, run_d = g_q.replay, g_d.replay
     for _ in range(args.warmup):
-        quantize()
-        dequantize()
+        run_q()
+        run_d()
     torch.cuda.synchronize()
     assert int(status.item()) == 0, "device status %#x" % int(status.item())
 
@@ -292,9 +313,9 @@ def run_ours(args, w):
     for k in range(args.steps):
         flush.fill_(k & 0xFF)
         ev[k][0].record(st)
-        quantize()
+        run_q()
         ev[k][1].record(st)
-        dequantize()
+        run_d()
         ev[k][2].record(st)
     torch.cuda.synchronize()
     _barrier(world)
@@ -350,7 +371,7 @@ def run_ours(args, w):
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": step_ms_avg, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": _config(w, world),
+            "config": _config(w, world, not args.no_graph),
             "roofline": {"kernel": "k_assign", "bound": "tensor", "achieved": a_tflops,
                          "peak": tf_burst, "unit": "TFLOP/s", "frac": a_tflops / tf_burst,
                          "traffic": traffic, "peak_source": src + " bf16 burst",
@@ -537,6 +558,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="time direct API calls instead of CUDA graph replays")
     ap.add_argument("--sweep", action="store_true",
                     help="print the precision sweep (MSE reduction) instead of the timing line")
     ap.add_argument("--stream", action="store_true",

@@ -28,7 +28,9 @@
  *     keeps no mutable global state; scratch space is the caller's `workspace`.  The one
  *     exception is qvg_quantize_static, whose scratch is a fixed area inside the library.
  *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).  Work
- *     is enqueued asynchronously; a call returns once it is enqueued.
+ *     is enqueued asynchronously; a call returns once it is enqueued.  qvg_quantize,
+ *     qvg_reassign and qvg_dequantize enqueue only kernels and memsets on `stream`, so a
+ *     caller may capture them in a CUDA graph and replay it with the same buffers.
  *   - Argument errors are detected on the host before anything is enqueued and returned as
  *     QVG_ERR_INVALID_ARG / QVG_ERR_UNSUPPORTED / QVG_ERR_WORKSPACE.  A CUDA error reported
  *     while enqueuing returns QVG_ERR_CUDA; work already enqueued may have run.

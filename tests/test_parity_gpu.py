@@ -288,3 +288,39 @@ def test_strided_input_and_token_offset():
     assert torch.equal(cache.codes[:, 300:812], ref.codes)
     assert torch.equal(cache.pi[:, :, 300:812], ref.pi)
     assert torch.equal(cache.centroids, ref.centroids)
+
+
+def test_graph_capture_replays_identical_results():
+    # qvg_quantize / qvg_dequantize enqueue only kernels and memsets on the given stream,
+    # so a caller may capture them in a CUDA graph; the replay must give the same bits
+    X = _make(13, 2, 2, 20, 30).cuda()
+    H, N = X.shape[:2]
+    C, T, bits, group, iters, seed = 32, 2, 2, 32, 3, 4
+    out = api.allocate(H, N, C, T, bits, group, device="cuda")
+    ws = api.new_workspace(H, N, C, T)
+    xh = torch.empty((H, N, 128), dtype=torch.bfloat16, device="cuda")
+
+    def step():
+        api.quantize(X, C, T, bits, group, iters, seed, out=out, workspace=ws)
+        api.dequantize(out, N, torch.bfloat16, out=xh)
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        step()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    ref = _to_np(out)
+    ref_x = xh.clone()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    for k in ("codes", "scales", "pi", "centroids"):
+        getattr(out, k).zero_()
+    xh.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    got = _to_np(out)
+    for k in ref:
+        assert np.array_equal(got[k], ref[k]), k
+    assert torch.equal(xh, ref_x)
