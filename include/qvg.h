@@ -144,7 +144,7 @@ qvg_status qvg_quantize(const qvg_quant_params *params, const void *X,
  *
  * Limit: qvg_quantize_workspace_bytes(params) must not exceed QVG_STATIC_SCRATCH_BYTES;
  * otherwise the call returns QVG_ERR_SCRATCH_LIMIT before touching the device.  That is
- * about 77 000 token rows (n_tensors * N) for T >= 2 and about 190 000 for T = 1.
+ * about 175 000 token rows (n_tensors * N), whatever T.
  *
  * First call on a device: the first call made while a given device is current looks up
  * the area's device address once (cudaGetSymbolAddress, which can load the library's

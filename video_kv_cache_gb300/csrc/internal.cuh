@@ -51,7 +51,6 @@ struct QPlan {
     const float *warm;
     int64_t warm_stride;
     // workspace
-    float *R32;            // [H][N][128] residual R^(t-1), stages t >= 2
     __half *A;             // [H][N][128] fp16 copy of the centred residual r - mu
     float *rnorm;          // [H][N] norm of the centred residual row (fp32)
     float *dnorm;          // [H][N] norm of its fp16 rounding error, ||fp16(r - mu) - (r - mu)||
@@ -139,6 +138,67 @@ __device__ __forceinline__ void or_status(uint32_t *status, uint32_t bits) {
 }
 
 // ------------------------------------------------------------------------------------
+// mbarrier and bulk-copy primitives (inline PTX)
+// ------------------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0u;
+}
+
+// try_wait that may suspend the thread until the phase completes, for at most the hinted
+// time (the hardware wakes it as soon as the phase completes).
+constexpr uint32_t kSuspendHintNs = 20000;  // longest single suspension in a wait
+__device__ __forceinline__ bool mbar_try_suspend(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(kSuspendHintNs)
+        : "memory");
+    return ok != 0u;
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Bulk copy (the TMA unit's untiled form) of `bytes` from global to shared memory, counted
+// on the mbarrier's transaction count.  Both addresses 16-byte aligned, bytes a multiple
+// of 16.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+// ------------------------------------------------------------------------------------
 // Launchers (each enqueues on `st`; returns the CUDA error of the launch)
 // ------------------------------------------------------------------------------------
 
@@ -146,7 +206,7 @@ cudaError_t launch_init_centroids(const QPlan &p, int t, cudaStream_t st);
 cudaError_t launch_centre(const QPlan &p, int t, cudaStream_t st);
 cudaError_t launch_prep(const QPlan &p, int t, cudaStream_t st);
 cudaError_t launch_centroid_planes(const QPlan &p, int t, cudaStream_t st);
-cudaError_t launch_cluster_means(const QPlan &p, int t, bool planes, cudaStream_t st);
+cudaError_t launch_cluster_means(const QPlan &p, int t, bool planes, int num_sms, cudaStream_t st);
 constexpr int kSortBlock = 256;  // tokens per block of the counting sort
 constexpr int kChunk = 32;       // sorted positions summed by one warp
 cudaError_t launch_encode(const QPlan &p, cudaStream_t st);

@@ -61,57 +61,10 @@ constexpr int kTileM = 128;
 constexpr uint32_t kKBlockBytes = kTileM * 64 * 2;  // 16 KB: 64 fp16 channels of 128 rows
 constexpr int kABlocks = 2;                           // A blocks per tile (128 channels)
 constexpr uint32_t kSpinLimit = 1u << 22;
-constexpr uint32_t kSuspendHintNs = 20000;        // longest single suspension in a wait
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // a pipeline wait gives up after 2 s
 // coefficients of the bound on |acc - r.c| (see the error bound above)
 constexpr float kDnRel = 0x1.01p0f;
 constexpr float kRnRel = kBPlanes == 1 ? 0x1.11p-11f : 0x1.03p-15f;
-
-__device__ __forceinline__ uint32_t smem_u32(const void *p) {
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-                 : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}\n"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0u;
-}
-
-// try_wait that may suspend the thread until the phase completes, for at most the hinted
-// time (the hardware wakes it as soon as the phase completes).
-__device__ __forceinline__ bool mbar_try_suspend(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}\n"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity), "r"(kSuspendHintNs)
-        : "memory");
-    return ok != 0u;
-}
-
-__device__ __forceinline__ uint64_t global_ns() {
-    uint64_t t;
-    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
-    return t;
-}
 
 // Bounded wait on a phase.  Gives up when another role already gave up, or after
 // kSpinLimit tries or kWaitLimitNs of wall time, whichever comes first (then it raises the
@@ -576,16 +529,34 @@ __global__ void __launch_bounds__(256) k_refine(QPlan p, int t) {
         const int64_t i = rq.i;
         const float *ct = p.cent + h * p.cent_tstride + p.cent_off;
         const float *c0 = ct + (int64_t)(t - 1) * p.C * kD;
-        // fp32 pass on the fp32 stage input: channels 4*lane..4*lane+3
-        float4 x;
-        if (t == 1) {
+        // X's channels 4*lane..4*lane+3
+        float xs[4];
+        {
             float v8[8];
             load_x8(p.X, p.in_dtype, h * p.x_stride + i * kD + (lane >> 1) * 8, v8);
             const bool up = lane & 1;  // which half of the 8 loaded channels is this lane's
-            x = make_float4(up ? v8[4] : v8[0], up ? v8[5] : v8[1], up ? v8[6] : v8[2],
-                            up ? v8[7] : v8[3]);
-        } else {
-            x = __ldg(reinterpret_cast<const float4 *>(p.R32 + ((int64_t)h * p.N + i) * kD) + lane);
+#pragma unroll
+            for (int k = 0; k < 4; k++) xs[k] = up ? v8[4 + k] : v8[k];
+        }
+        // fp32 pass on the fp32 stage input: X itself at stage 1, later the residual formed
+        // by the same TwoSum chain (one final rounding) as the GEMM operand's preparation
+        float4 x = make_float4(xs[0], xs[1], xs[2], xs[3]);
+        if (t > 1) {
+            float s[4] = {xs[0], xs[1], xs[2], xs[3]}, e[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int s2 = 1; s2 < t; s2++) {
+                const int js = min((int)p.pi[(int64_t)(h * p.T + s2 - 1) * p.cap + p.tok_off + i], p.C - 1);
+                const float4 c = __ldg(reinterpret_cast<const float4 *>(
+                    ct + ((int64_t)(s2 - 1) * p.C + js) * kD) + lane);
+                const float cc[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+                for (int k = 0; k < 4; k++) {
+                    float err;
+                    two_sum(s[k], -cc[k], s[k], err);
+                    e[k] = __fadd_rn(e[k], err);
+                }
+            }
+            x = make_float4(__fadd_rn(s[0], e[0]), __fadd_rn(s[1], e[1]), __fadd_rn(s[2], e[2]),
+                            __fadd_rn(s[3], e[3]));
         }
         float bestD = INFINITY, secondD = INFINITY;
         int bestj = 0;
@@ -618,13 +589,8 @@ __global__ void __launch_bounds__(256) k_refine(QPlan p, int t) {
             // the stage input rebuilt in fp64: x - C^(1)[pi^(1)] - ... - C^(t-1)[pi^(t-1)],
             // subtracted in that order
             double xd[4];
-            {
-                float v8[8];
-                load_x8(p.X, p.in_dtype, h * p.x_stride + i * kD + (lane >> 1) * 8, v8);
-                const bool up = lane & 1;
 #pragma unroll
-                for (int k = 0; k < 4; k++) xd[k] = (double)(up ? v8[4 + k] : v8[k]);
-            }
+            for (int k = 0; k < 4; k++) xd[k] = (double)xs[k];
             for (int s2 = 1; s2 < t; s2++) {
                 const int js = min((int)p.pi[(int64_t)(h * p.T + s2 - 1) * p.cap + p.tok_off + i], p.C - 1);
                 const float4 c = __ldg(reinterpret_cast<const float4 *>(

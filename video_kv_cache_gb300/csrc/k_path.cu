@@ -13,6 +13,7 @@
 //     Algorithm-System Co-design.
 #include <cuda_fp8.h>
 
+#include <atomic>
 #include <type_traits>
 
 #include "internal.cuh"
@@ -94,10 +95,20 @@ __global__ void k_init_centroids(QPlan p, int t) {
         v = __ldg(p.warm + h * p.warm_stride + (int64_t)(t - 1) * p.C * kD + (int64_t)j * kD + k);
     } else {
         const int64_t row = p.init_idx[(h * p.T + (t - 1)) * p.C + j];
-        if (t == 1)
-            v = load_x1(p.X, p.in_dtype, h * p.x_stride + row * kD + k);
-        else
-            v = p.R32[(h * p.N + row) * kD + k];
+        v = load_x1(p.X, p.in_dtype, h * p.x_stride + row * kD + k);
+        if (t > 1) {  // the row of R^(t-1), by the residual kernels' TwoSum chain
+            float e = 0.f;
+            for (int st = 1; st < t; st++) {
+                const int pj = min((int)p.pi[(int64_t)(h * p.T + st - 1) * p.cap + p.tok_off + row],
+                                   p.C - 1);
+                const float c = p.cent[h * p.cent_tstride + p.cent_off + (int64_t)(st - 1) * p.C * kD +
+                                       (int64_t)pj * kD + k];
+                float err;
+                two_sum(v, -c, v, err);
+                e = __fadd_rn(e, err);
+            }
+            v = __fadd_rn(v, e);
+        }
     }
     dst[k] = v;
 }
@@ -134,8 +145,8 @@ cudaError_t launch_centre(const QPlan &p, int t, cudaStream_t st) {
 
 // --------------------------------------------------------------------------------------
 // Residual preparation for stage t.  One thread per (token, 8 channels).
-//   r      = fp32(x - sum_{s<t} C^(s)[pi^(s)_i]) via a TwoSum chain (one final rounding)
-//   R32    = r                           (stages t >= 2; stage 1 reads X directly)
+//   r      = fp32(x - sum_{s<t} C^(s)[pi^(s)_i]) via a TwoSum chain (one final rounding);
+//            not stored: the kernels that need r again rebuild it by the same chain
 //   A      = fp16(r - mu)                (tensor-core operand of the assignment)
 //   rnorm  = ||r - mu||, fp32            (for the assignment's error margin)
 //   dnorm  = ||A - (r - mu)||, fp32      (the same)
@@ -187,11 +198,6 @@ __global__ void __launch_bounds__(256) k_prep(QPlan p, int t) {
         float r[8];
 #pragma unroll
         for (int q = 0; q < 8; q++) r[q] = __fadd_rn(s[q], e[q]);
-        if (valid && t >= 2) {
-            float4 *dst = reinterpret_cast<float4 *>(p.R32 + (h * p.N + i) * kD + c8 * 8);
-            dst[0] = make_float4(r[0], r[1], r[2], r[3]);
-            dst[1] = make_float4(r[4], r[5], r[6], r[7]);
-        }
         float ss = 0.f, dd = 0.f;
         __align__(16) __half a16[8];
 #pragma unroll
@@ -414,122 +420,261 @@ __device__ __forceinline__ void write_centroid(const QPlan &p, int h, int t, int
     if (lane == 0) p.cn[(int64_t)h * p.Cpad + j] = ss;
 }
 
-// One warp per chunk of 32 cluster-sorted positions: the rows of each run (same cluster)
-// are added with TwoSum in sorted order, the next batch's loads in flight.  A run that is a whole cluster
-// leaves its (sum, error) in the cluster's slot; a run that crosses the chunk's start or end
-// leaves it in the chunk's first / last slot.  k_cluster_finalize turns them into means.
-// Occupancy decides this kernel's speed (each warp's sum is a sequential chain), so the
-// batches are short and the CTAs per SM many: 4 for 16-bit rows (8-row batches), 6 for
-// fp32 rows (2-row batches).
-template <int SRC>  // 0: X bf16, 1: X fp32, 2: R32, 3: X fp16
-__global__ void __launch_bounds__(256, (SRC == 0 || SRC == 3) ? 4 : 6) k_chunk_sums(QPlan p, int t) {
-    constexpr bool NARROW = SRC == 0 || SRC == 3;  // 16-bit input rows: 8 bytes a lane
-    constexpr int ROWS = NARROW ? 8 : 2;           // rows of a batch
-    const int lane = threadIdx.x & 31;
-    const int h = blockIdx.y;
-    const int k = blockIdx.x * 8 + (threadIdx.x >> 5);
-    if (k >= p.nchunk) return;
-    const int64_t c0 = (int64_t)k * kChunk;
-    const int nk = (int)min((int64_t)kChunk, p.N - c0);
-    const int *ids = p.ids + (int64_t)h * p.N + c0;
-    const uint8_t *cid = p.cid + (int64_t)h * p.N + c0;
-    int idr[2], cr[2];
-#pragma unroll
-    for (int q = 0; q < 2; q++) {
-        const int pos = q * 32 + lane;
-        idr[q] = pos < nk ? ids[pos] : 0;
-        cr[q] = pos < nk ? (int)cid[pos] : -1;
+// Cluster sums over chunks of 32 cluster-sorted positions.  The rows of each run (same
+// cluster) are added with TwoSum in sorted order.  A run that is a whole cluster leaves its
+// (sum, error) in the cluster's slot; a run that crosses the chunk's start or end leaves it
+// in the chunk's first / last slot.  k_cluster_finalize turns them into means.
+//
+// The summed rows are the stage input R^(t-1): X itself at stage 1, later a residual that
+// is not stored but rebuilt here from X and the earlier stages' centroid rows (L2-resident)
+// by the TwoSum chain of k_prep, which gives the same fp32 value.  Reaching a row takes
+// three dependent loads (its id from the sort, its earlier clusters, then X and the
+// centroid rows), so the kernel is built to keep many of them in flight:
+//   * persistent warps, each striding over the chunks of all tensors; lane m holds sorted
+//     position m of a chunk (its token, cluster and earlier clusters), and the next chunk's
+//     ids and pi bytes are read while the current chunk is summed;
+//   * the rows reach shared memory by bulk copies that each lane issues for its own
+//     position, eight rows to a group on one mbarrier, two groups in flight ahead of the
+//     sums, running on from one chunk into the next.
+constexpr int kBulkGroup = 8;  // rows a group (one mbarrier phase)
+__host__ __device__ constexpr int bulk_xbytes(int src) { return src == 1 ? 512 : 256; }
+__host__ __device__ inline int bulk_row_bytes(int src, int tp) { return bulk_xbytes(src) + tp * 512; }
+// warps per CTA: as many as fit 96 KB of row slots (two groups a warp), at most 8
+__host__ __device__ inline int bulk_warps(int src, int tp) {
+    const int w = 98304 / (2 * kBulkGroup * bulk_row_bytes(src, tp));
+    return w > 8 ? 8 : (w < 1 ? 1 : w);
+}
+
+__device__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+    if (mbar_try(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    for (uint32_t n = 0; n < (1u << 22); n++) {
+        if (mbar_try_suspend(bar, parity)) return true;
+        if ((n & 15u) == 15u && global_ns() - t0 > 2000000000ull) break;
     }
-    // clusters just before and just after the chunk decide whether its first and last runs
-    // continue into the neighbouring chunks
-    const int c_prev = k > 0 ? (int)p.cid[(int64_t)h * p.N + c0 - 1] : -1;
-    const int c_next = c0 + nk < p.N ? (int)p.cid[(int64_t)h * p.N + c0 + nk] : -1;
-    // run starts: bit q is set when sorted position q begins a new cluster run
-    uint32_t brk[2];
-    {
-        const int last0 = __shfl_sync(0xffffffffu, cr[0], 31);
-#pragma unroll
-        for (int q = 0; q < 2; q++) {
-            int pc = __shfl_up_sync(0xffffffffu, cr[q], 1);
-            if (lane == 0) pc = q == 0 ? -2 : last0;
-            brk[q] = __ballot_sync(0xffffffffu, q * 32 + lane < nk && cr[q] != pc);
-        }
+    return false;
+}
+
+// one chunk as the warp holds it: lane m's values are those of sorted position m
+struct SumChunk {
+    int h, k, nk;           // tensor, chunk, positions in the chunk
+    int id, cl;             // the lane's token and cluster (cl = -1 past the end)
+    int c_prev, c_next;     // clusters just before and after the chunk (-1: none)
+    uint32_t pk0, pk1;      // the token's earlier clusters, 8 bits a stage
+    uint32_t brk;           // bit m: position m begins a new run
+};
+
+template <int SRC, int TP>  // SRC: X dtype (0 bf16, 1 fp32, 3 fp16); TP: t - 1 (0..3), or -1
+__global__ void __launch_bounds__(256, 2) k_chunk_sums(QPlan p, int t) {
+    static_assert(kChunk == 32, "one sorted position per lane");
+    constexpr int XB = bulk_xbytes(SRC);
+    extern __shared__ __align__(128) uint8_t bulk_smem[];
+    const int tp = TP >= 0 ? TP : t - 1;
+    const int row_bytes = XB + tp * 512;
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    const int wpc = blockDim.x >> 5;
+    const int total = p.H * p.nchunk;
+    const int nw = gridDim.x * wpc;
+    int ci = blockIdx.x * wpc + wid;
+    if (ci >= total) return;  // no CTA-wide barrier below
+    const uint32_t bars = smem_u32(bulk_smem) + wid * 16;  // group n waits on bars + 8 (n & 1)
+    const uint32_t ring = smem_u32(bulk_smem) + 128 + wid * 2 * kBulkGroup * row_bytes;
+    const uint8_t *ring_g = bulk_smem + 128 + wid * 2 * kBulkGroup * row_bytes;
+    if (lane == 0) {
+        mbar_init(bars, 1);
+        mbar_init(bars + 8, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    float s[4] = {0.f, 0.f, 0.f, 0.f}, e[4] = {0.f, 0.f, 0.f, 0.f};
-    int run_c = -1, run_start = 0;
-    auto stash = [&](int end) {
-        const bool whole = (run_start > 0 || c_prev != run_c) && (end < nk || c_next != run_c);
-        float *dst = whole ? p.wsum + ((int64_t)h * p.C + run_c) * 2 * kD
-                           : p.psum + (((int64_t)h * p.nchunk + k) * 2 + (run_start == 0 ? 0 : 1)) * 2 * kD;
-        reinterpret_cast<float4 *>(dst)[lane] = make_float4(s[0], s[1], s[2], s[3]);
-        reinterpret_cast<float4 *>(dst + kD)[lane] = make_float4(e[0], e[1], e[2], e[3]);
+    __syncwarp();
+
+    auto fetch = [&](int c, SumChunk &m) {
+        m.h = c / p.nchunk;
+        m.k = c - m.h * p.nchunk;
+        const int64_t c0 = (int64_t)m.k * kChunk;
+        m.nk = (int)min((int64_t)kChunk, p.N - c0);
+        const int64_t base = (int64_t)m.h * p.N + c0;
+        const bool mine = lane < m.nk;
+        m.id = mine ? p.ids[base + lane] : 0;
+        m.cl = mine ? (int)p.cid[base + lane] : -1;
+        m.c_prev = m.k > 0 ? (int)p.cid[base - 1] : -1;
+        m.c_next = c0 + m.nk < p.N ? (int)p.cid[base + m.nk] : -1;
     };
-    using Raw = typename std::conditional<NARROW, uint2, float4>::type;
-    // raw words of the ROWS rows starting at sorted position k1 (zero past the chunk)
-    auto load_batch = [&](int k1, Raw (&raw)[ROWS]) {
-        const int idsel = k1 < 32 ? idr[0] : idr[1];
-#pragma unroll
-        for (int u = 0; u < ROWS; u++) {
-            const int64_t row = __shfl_sync(0xffffffffu, idsel, (k1 + u) & 31);
-            if constexpr (NARROW) {
-                raw[u] = make_uint2(0u, 0u);
-                if (k1 + u < nk)
-                    raw[u] = __ldg(reinterpret_cast<const uint2 *>(
-                        static_cast<const uint16_t *>(p.X) + h * p.x_stride + row * kD) + lane);
-            } else {
-                raw[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (k1 + u < nk) {
-                    if constexpr (SRC == 2)
-                        raw[u] = __ldg(reinterpret_cast<const float4 *>(
-                            p.R32 + ((int64_t)h * p.N + row) * kD) + lane);
-                    else
-                        raw[u] = __ldg(reinterpret_cast<const float4 *>(
-                            static_cast<const float *>(p.X) + h * p.x_stride + row * kD) + lane);
-                }
+    auto fetch_pi = [&](SumChunk &m) {  // needs m.id; also finds the run starts
+        m.pk0 = m.pk1 = 0u;
+        if (lane < m.nk) {
+            for (int st = 0; st < tp; st++) {
+                const uint32_t b = p.pi[(int64_t)(m.h * p.T + st) * p.cap + p.tok_off + m.id];
+                if (st < 4) m.pk0 |= b << (8 * st);
+                else m.pk1 |= b << (8 * (st - 4));
             }
         }
+        int pc = __shfl_up_sync(0xffffffffu, m.cl, 1);
+        if (lane == 0) pc = -2;
+        m.brk = __ballot_sync(0xffffffffu, lane < m.nk && m.cl != pc);
     };
-    // one batch of raw words in registers, the next batch's loads already in flight
-    Raw cur[ROWS], nxt[ROWS];
-    load_batch(0, cur);
+    auto n_groups = [](const SumChunk &m) { return (m.nk + kBulkGroup - 1) / kBulkGroup; };
+
+    uint32_t n_issued = 0, n_done = 0;  // groups issued / summed by this warp so far
+    // copies of group g of chunk m (positions 8g..8g+7) into half (n_issued & 1) of the slots
+    auto issue = [&](const SumChunk &m, int g) {
+        const int n_rows = min(kBulkGroup, m.nk - g * kBulkGroup);
+        const int half = n_issued & 1;
+        const uint32_t bar = bars + 8 * half;
+        if (lane == 0) mbar_expect_tx(bar, (uint32_t)(n_rows * row_bytes));
+        __syncwarp();
+        if (lane >= g * kBulkGroup && lane < g * kBulkGroup + n_rows) {
+            const uint32_t dst = ring + (half * kBulkGroup + (lane & (kBulkGroup - 1))) * row_bytes;
+            bulk_g2s(dst,
+                     static_cast<const char *>(p.X) + (m.h * p.x_stride + (int64_t)m.id * kD) * (XB / kD),
+                     XB, bar);
+            const char *cb = reinterpret_cast<const char *>(p.cent + m.h * p.cent_tstride + p.cent_off);
+            for (int st = 0; st < tp; st++) {
+                const int pj = min((int)(((st < 4 ? m.pk0 : m.pk1) >> (8 * (st & 3))) & 255u), p.C - 1);
+                bulk_g2s(dst + XB + st * 512, cb + ((int64_t)st * p.C + pj) * kD * 4, 512, bar);
+            }
+        }
+        n_issued++;
+    };
+
+    SumChunk cur, nxt;
+    fetch(ci, cur);
+    fetch_pi(cur);
+    bool has_next = false;
+    // the issue pointer: group ip_g of the current (ip_next = 0) or the next chunk
+    int ip_next = 0, ip_g = 0;
+    auto issue_next = [&]() {
+        if (!ip_next) {
+            if (ip_g < n_groups(cur)) {
+                issue(cur, ip_g++);
+                return;
+            }
+            ip_next = 1;
+            ip_g = 0;
+        }
+        if (has_next && ip_g < n_groups(nxt)) issue(nxt, ip_g++);
+    };
+    issue_next();
+    issue_next();
+    for (;;) {
+        const int cn = ci + nw;
+        has_next = cn < total;
+        if (has_next) {
+            fetch(cn, nxt);
+            fetch_pi(nxt);
+        }
+        // keep two groups in flight (the current chunk may have had fewer than two)
+        while (n_issued < n_done + 2) {
+            const uint32_t before = n_issued;
+            issue_next();
+            if (n_issued == before) break;
+        }
+        float s[4] = {0.f, 0.f, 0.f, 0.f}, e[4] = {0.f, 0.f, 0.f, 0.f};
+        int run_c = -1, run_start = 0;
+        auto stash = [&](int end) {
+            const bool whole = (run_start > 0 || cur.c_prev != run_c) && (end < cur.nk || cur.c_next != run_c);
+            float *dst = whole ? p.wsum + ((int64_t)cur.h * p.C + run_c) * 2 * kD
+                               : p.psum + (((int64_t)cur.h * p.nchunk + cur.k) * 2 + (run_start == 0 ? 0 : 1)) * 2 * kD;
+            reinterpret_cast<float4 *>(dst)[lane] = make_float4(s[0], s[1], s[2], s[3]);
+            reinterpret_cast<float4 *>(dst + kD)[lane] = make_float4(e[0], e[1], e[2], e[3]);
+        };
+        const int ng = n_groups(cur);
+        for (int g = 0; g < ng; g++) {
+            const int half = n_done & 1;
+            if (!mbar_wait_bounded(bars + 8 * half, (n_done >> 1) & 1)) {
+                // a copy that never landed: report it, let the other group's copies finish
+                if (lane == 0) or_status(p.status, QVG_DEV_TIMEOUT);
+                if (n_issued > n_done + 1) mbar_wait_bounded(bars + 8 * (half ^ 1), ((n_done + 1) >> 1) & 1);
+                return;
+            }
+            const int n_rows = min(kBulkGroup, cur.nk - g * kBulkGroup);
 #pragma unroll 1
-    for (int k1 = 0; k1 < nk; k1 += ROWS) {
-        if (k1 + ROWS < nk) load_batch(k1 + ROWS, nxt);
-        const uint32_t bm = (k1 < 32 ? brk[0] : brk[1]) >> (k1 & 31);
-        const int crsel = k1 < 32 ? cr[0] : cr[1];
-#pragma unroll
-        for (int u = 0; u < ROWS; u++) {
-            if (k1 + u < nk) {
+            for (int u = 0; u < n_rows; u++) {
+                const int m = g * kBulkGroup + u;
+                const uint8_t *slot = ring_g + (half * kBulkGroup + u) * row_bytes;
                 float v[4];
                 if constexpr (SRC == 0) {
-                    const uint32_t wx = cur[u].x, wy = cur[u].y;
-                    v[0] = __uint_as_float(wx << 16);
-                    v[1] = __uint_as_float(wx & 0xFFFF0000u);
-                    v[2] = __uint_as_float(wy << 16);
-                    v[3] = __uint_as_float(wy & 0xFFFF0000u);
+                    const uint2 w = *reinterpret_cast<const uint2 *>(slot + lane * 8);
+                    v[0] = __uint_as_float(w.x << 16);
+                    v[1] = __uint_as_float(w.x & 0xFFFF0000u);
+                    v[2] = __uint_as_float(w.y << 16);
+                    v[3] = __uint_as_float(w.y & 0xFFFF0000u);
                 } else if constexpr (SRC == 3) {
-                    const uint32_t wx = cur[u].x, wy = cur[u].y;
-                    const float2 f0 = __half22float2(*reinterpret_cast<const __half2 *>(&wx));
-                    const float2 f1 = __half22float2(*reinterpret_cast<const __half2 *>(&wy));
+                    const uint2 w = *reinterpret_cast<const uint2 *>(slot + lane * 8);
+                    const float2 f0 = __half22float2(*reinterpret_cast<const __half2 *>(&w.x));
+                    const float2 f1 = __half22float2(*reinterpret_cast<const __half2 *>(&w.y));
                     v[0] = f0.x; v[1] = f0.y; v[2] = f1.x; v[3] = f1.y;
                 } else {
-                    v[0] = cur[u].x; v[1] = cur[u].y; v[2] = cur[u].z; v[3] = cur[u].w;
+                    const float4 w = *reinterpret_cast<const float4 *>(slot + lane * 16);
+                    v[0] = w.x; v[1] = w.y; v[2] = w.z; v[3] = w.w;
                 }
-                if ((bm >> u) & 1u) {  // warp-uniform
-                    if (run_c >= 0) stash(k1 + u);
-                    run_c = __shfl_sync(0xffffffffu, crsel, (k1 + u) & 31);
-                    run_start = k1 + u;
+                if (TP == 1) {
+                    // one earlier stage: the chain's fl(fl(x - c) + err) is fl(x - c) itself
+                    // for every finite result
+                    const float4 c = *reinterpret_cast<const float4 *>(slot + XB + lane * 16);
+                    v[0] = __fsub_rn(v[0], c.x);
+                    v[1] = __fsub_rn(v[1], c.y);
+                    v[2] = __fsub_rn(v[2], c.z);
+                    v[3] = __fsub_rn(v[3], c.w);
+                } else if (TP != 0) {
+                    float er[4] = {0.f, 0.f, 0.f, 0.f};
+                    for (int st = 0; st < tp; st++) {
+                        const float4 c = *reinterpret_cast<const float4 *>(slot + XB + st * 512 + lane * 16);
+                        const float cc[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+                        for (int r = 0; r < 4; r++) {
+                            float err;
+                            two_sum(v[r], -cc[r], v[r], err);
+                            er[r] = __fadd_rn(er[r], err);
+                        }
+                    }
+#pragma unroll
+                    for (int r = 0; r < 4; r++) v[r] = __fadd_rn(v[r], er[r]);
+                }
+                if ((cur.brk >> m) & 1u) {  // warp-uniform
+                    if (run_c >= 0) stash(m);
+                    run_c = __shfl_sync(0xffffffffu, cur.cl, m);
+                    run_start = m;
 #pragma unroll
                     for (int r = 0; r < 4; r++) s[r] = e[r] = 0.f;
                 }
 #pragma unroll
                 for (int r = 0; r < 4; r++) acc_two_sum(s[r], e[r], v[r]);
             }
+            n_done++;
+            __syncwarp();  // every lane has read the group's slots before they are refilled
+            issue_next();
         }
-#pragma unroll
-        for (int u = 0; u < ROWS; u++) cur[u] = nxt[u];
+        if (run_c >= 0) stash(cur.nk);
+        if (!has_next) break;
+        cur = nxt;
+        ci = cn;
+        if (!ip_next) ip_g = 0;  // every group of the old chunk was issued
+        ip_next = 0;
+        has_next = false;
     }
-    if (run_c >= 0) stash(nk);
+}
+
+template <int SRC, int TP>
+static cudaError_t launch_sums(const QPlan &p, int t, int num_sms, cudaStream_t st) {
+    const int tp = TP >= 0 ? TP : t - 1;
+    const int wpc = bulk_warps(SRC, tp);
+    const int smem = 128 + wpc * 2 * kBulkGroup * bulk_row_bytes(SRC, tp);
+    cudaError_t e = cudaFuncSetAttribute(k_chunk_sums<SRC, TP>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    // resident CTAs per SM, looked up once per stage count (the kernel's resources are fixed)
+    static std::atomic<int> per_sm_of[kMaxT];
+    int per_sm = per_sm_of[tp].load(std::memory_order_relaxed);
+    if (per_sm == 0) {
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_chunk_sums<SRC, TP>, 32 * wpc, smem);
+        if (e != cudaSuccess) return e;
+        per_sm = std::max(per_sm, 1);
+        per_sm_of[tp].store(per_sm, std::memory_order_relaxed);
+    }
+    const int64_t need = ((int64_t)p.H * p.nchunk + wpc - 1) / wpc;
+    const int grid = (int)std::min<int64_t>(need, (int64_t)per_sm * num_sms);
+    k_chunk_sums<SRC, TP><<<grid, 32 * wpc, smem, st>>>(p, t);
+    return cudaSuccess;
 }
 
 // One warp per cluster: the mean from the cluster's own slot, or, for clusters spread over
@@ -594,20 +739,25 @@ __global__ void __launch_bounds__(256) k_cluster_finalize(QPlan p, int t, int pl
     if (lane == 0) p.counts[h * p.C + j] = 0;
 }
 
-cudaError_t launch_cluster_means(const QPlan &p, int t, bool planes, cudaStream_t st) {
+cudaError_t launch_cluster_means(const QPlan &p, int t, bool planes, int num_sms, cudaStream_t st) {
     const dim3 sgrid((unsigned)p.nsb, p.H);
     k_sort_hist<<<sgrid, kSortBlock, 0, st>>>(p, t);
     k_sort_scan<<<dim3((unsigned)((p.C + 31) / 32), p.H), 256, 0, st>>>(p);
     k_sort_scatter<<<sgrid, kSortBlock, 0, st>>>(p, t);
-    const dim3 cgrid((unsigned)((p.nchunk + 7) / 8), p.H);
-    if (t >= 2)
-        k_chunk_sums<2><<<cgrid, 256, 0, st>>>(p, t);
-    else if (p.in_dtype == DT_F32)
-        k_chunk_sums<1><<<cgrid, 256, 0, st>>>(p, t);
-    else if (p.in_dtype == DT_F16)
-        k_chunk_sums<3><<<cgrid, 256, 0, st>>>(p, t);
-    else
-        k_chunk_sums<0><<<cgrid, 256, 0, st>>>(p, t);
+    auto sums = [&](auto src) {
+        constexpr int S = decltype(src)::value;
+        switch (t - 1) {
+            case 0: return launch_sums<S, 0>(p, t, num_sms, st);
+            case 1: return launch_sums<S, 1>(p, t, num_sms, st);
+            case 2: return launch_sums<S, 2>(p, t, num_sms, st);
+            case 3: return launch_sums<S, 3>(p, t, num_sms, st);
+            default: return launch_sums<S, -1>(p, t, num_sms, st);
+        }
+    };
+    const cudaError_t e = p.in_dtype == DT_F32   ? sums(std::integral_constant<int, 1>())
+                          : p.in_dtype == DT_F16 ? sums(std::integral_constant<int, 3>())
+                                                 : sums(std::integral_constant<int, 0>());
+    if (e != cudaSuccess) return e;
     k_cluster_finalize<<<dim3((unsigned)((p.C + 7) / 8), p.H), 256, 0, st>>>(p, t, planes ? 1 : 0);
     return cudaGetLastError();
 }

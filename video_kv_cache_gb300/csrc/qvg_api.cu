@@ -21,7 +21,7 @@ inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 
 inline int cpad_of(int C) { return (C + 31) / 32 * 32; }
 
 struct WsLayout {
-    size_t R32, A, rnorm, dnorm, B, cn, mu, counts, offs, blockoff, ids, cid, psum, wsum, init_idx,
+    size_t A, rnorm, dnorm, B, cn, mu, counts, offs, blockoff, ids, cid, psum, wsum, init_idx,
         stats, rq_count, rq, total;
     int nsb, nchunk;
 };
@@ -37,7 +37,6 @@ WsLayout ws_layout(int64_t H, int64_t N, int C, int T) {
     w.stats = take(64);
     if (T > 0) {
         const int Cpad = cpad_of(C);
-        w.R32 = take(T >= 2 ? (size_t)H * N * kD * 4 : 0);
         w.A = take((size_t)H * N * kD * 2);
         w.rnorm = take((size_t)H * N * 4);
         w.dnorm = take((size_t)H * N * 4);
@@ -136,7 +135,7 @@ qvg_status run_stages(QPlan &p, const AssignMaps *maps, int num_sms, cudaStream_
             step(cudaMemsetAsync(p.rq_count, 0, 4, st));
             step(launch_assign(p, maps, t, num_sms, st));
             step(launch_refine(p, t, num_sms, st));
-            step(launch_cluster_means(p, t, it < p.iters, st));
+            step(launch_cluster_means(p, t, it < p.iters, num_sms, st));
         }
     }
     return rc;
@@ -187,7 +186,6 @@ QPlan make_plan(const qvg_quant_params *prm, const void *X, const float *warm,
     p.warm_stride = prm->warm_stride ? prm->warm_stride : (int64_t)p.T * p.C * kD;
     p.stats = reinterpret_cast<unsigned *>(ws + w.stats);
     if (p.T > 0) {
-        p.R32 = p.T >= 2 ? reinterpret_cast<float *>(ws + w.R32) : nullptr;
         p.A = reinterpret_cast<__half *>(ws + w.A);
         p.rnorm = reinterpret_cast<float *>(ws + w.rnorm);
         p.dnorm = reinterpret_cast<float *>(ws + w.dnorm);
