@@ -293,6 +293,20 @@ __device__ __forceinline__ void acc_two_sum(float &s, float &e, float x) {
     e = __fadd_rn(e, err);
 }
 
+// Two lanes of fp32 at once (packed f32x2 instructions).  a - b is taken as fma(b, -1, a),
+// which rounds the same exact difference once, so every result equals the scalar form's.
+__device__ __forceinline__ float2 sub2(float2 a, float2 b) {
+    return __ffma2_rn(b, make_float2(-1.f, -1.f), a);
+}
+// acc_two_sum on a pair: s + x with its exact rounding error added to e
+__device__ __forceinline__ void acc_two_sum2(float2 &s, float2 &e, float2 x) {
+    const float2 sn = __fadd2_rn(s, x);
+    const float2 bb = sub2(sn, s);
+    const float2 err = __fadd2_rn(sub2(s, sub2(sn, bb)), sub2(x, bb));
+    e = __fadd2_rn(e, err);
+    s = sn;
+}
+
 __global__ void __launch_bounds__(kSortBlock) k_sort_hist(QPlan p, int t) {
     __shared__ int hist[kMaxC];
     const int h = blockIdx.y, b = blockIdx.x;
@@ -568,15 +582,54 @@ __global__ void __launch_bounds__(256, 2) k_chunk_sums(QPlan p, int t) {
             issue_next();
             if (n_issued == before) break;
         }
-        float s[4] = {0.f, 0.f, 0.f, 0.f}, e[4] = {0.f, 0.f, 0.f, 0.f};
-        int run_c = -1, run_start = 0;
+        // the running (sum, error) pair of the current run, channels (0,1) and (2,3)
+        float2 s01 = make_float2(0.f, 0.f), s23 = s01, e01 = s01, e23 = s01;
+        int run_c = __shfl_sync(0xffffffffu, cur.cl, 0), run_start = 0;
         auto stash = [&](int end) {
             const bool whole = (run_start > 0 || cur.c_prev != run_c) && (end < cur.nk || cur.c_next != run_c);
             float *dst = whole ? p.wsum + ((int64_t)cur.h * p.C + run_c) * 2 * kD
                                : p.psum + (((int64_t)cur.h * p.nchunk + cur.k) * 2 + (run_start == 0 ? 0 : 1)) * 2 * kD;
-            reinterpret_cast<float4 *>(dst)[lane] = make_float4(s[0], s[1], s[2], s[3]);
-            reinterpret_cast<float4 *>(dst + kD)[lane] = make_float4(e[0], e[1], e[2], e[3]);
+            reinterpret_cast<float4 *>(dst)[lane] = make_float4(s01.x, s01.y, s23.x, s23.y);
+            reinterpret_cast<float4 *>(dst + kD)[lane] = make_float4(e01.x, e01.y, e23.x, e23.y);
         };
+        // the lane's four channels of the row in a slot, as the stage input
+        auto row_of = [&](const uint8_t *slot, float2 &v01, float2 &v23) {
+            if constexpr (SRC == 0) {
+                const uint2 w = *reinterpret_cast<const uint2 *>(slot + lane * 8);
+                v01 = make_float2(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xFFFF0000u));
+                v23 = make_float2(__uint_as_float(w.y << 16), __uint_as_float(w.y & 0xFFFF0000u));
+            } else if constexpr (SRC == 3) {
+                const uint2 w = *reinterpret_cast<const uint2 *>(slot + lane * 8);
+                v01 = __half22float2(*reinterpret_cast<const __half2 *>(&w.x));
+                v23 = __half22float2(*reinterpret_cast<const __half2 *>(&w.y));
+            } else {
+                const float4 w = *reinterpret_cast<const float4 *>(slot + lane * 16);
+                v01 = make_float2(w.x, w.y);
+                v23 = make_float2(w.z, w.w);
+            }
+            if (TP == 1) {
+                // one earlier stage: the chain's fl(fl(x - c) + err) is fl(x - c) itself for
+                // every finite result
+                const float4 c = *reinterpret_cast<const float4 *>(slot + XB + lane * 16);
+                v01 = sub2(v01, make_float2(c.x, c.y));
+                v23 = sub2(v23, make_float2(c.z, c.w));
+            } else if (TP != 0) {
+                float v[4] = {v01.x, v01.y, v23.x, v23.y}, er[4] = {0.f, 0.f, 0.f, 0.f};
+                for (int st = 0; st < tp; st++) {
+                    const float4 c = *reinterpret_cast<const float4 *>(slot + XB + st * 512 + lane * 16);
+                    const float cc[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+                    for (int r = 0; r < 4; r++) {
+                        float err;
+                        two_sum(v[r], -cc[r], v[r], err);
+                        er[r] = __fadd_rn(er[r], err);
+                    }
+                }
+                v01 = make_float2(__fadd_rn(v[0], er[0]), __fadd_rn(v[1], er[1]));
+                v23 = make_float2(__fadd_rn(v[2], er[2]), __fadd_rn(v[3], er[3]));
+            }
+        };
+        const uint32_t starts = cur.brk & ~1u;  // position 0 opens the first run above
         const int ng = n_groups(cur);
         for (int g = 0; g < ng; g++) {
             const int half = n_done & 1;
@@ -587,64 +640,37 @@ __global__ void __launch_bounds__(256, 2) k_chunk_sums(QPlan p, int t) {
                 return;
             }
             const int n_rows = min(kBulkGroup, cur.nk - g * kBulkGroup);
+            const uint8_t *gslots = ring_g + half * kBulkGroup * row_bytes;
+            if (n_rows == kBulkGroup && ((starts >> (g * kBulkGroup)) & 0xFFu) == 0u) {
+                // a full group inside one run (the usual case)
+#pragma unroll
+                for (int u = 0; u < kBulkGroup; u++) {
+                    float2 v01, v23;
+                    row_of(gslots + u * row_bytes, v01, v23);
+                    acc_two_sum2(s01, e01, v01);
+                    acc_two_sum2(s23, e23, v23);
+                }
+            } else {
 #pragma unroll 1
-            for (int u = 0; u < n_rows; u++) {
-                const int m = g * kBulkGroup + u;
-                const uint8_t *slot = ring_g + (half * kBulkGroup + u) * row_bytes;
-                float v[4];
-                if constexpr (SRC == 0) {
-                    const uint2 w = *reinterpret_cast<const uint2 *>(slot + lane * 8);
-                    v[0] = __uint_as_float(w.x << 16);
-                    v[1] = __uint_as_float(w.x & 0xFFFF0000u);
-                    v[2] = __uint_as_float(w.y << 16);
-                    v[3] = __uint_as_float(w.y & 0xFFFF0000u);
-                } else if constexpr (SRC == 3) {
-                    const uint2 w = *reinterpret_cast<const uint2 *>(slot + lane * 8);
-                    const float2 f0 = __half22float2(*reinterpret_cast<const __half2 *>(&w.x));
-                    const float2 f1 = __half22float2(*reinterpret_cast<const __half2 *>(&w.y));
-                    v[0] = f0.x; v[1] = f0.y; v[2] = f1.x; v[3] = f1.y;
-                } else {
-                    const float4 w = *reinterpret_cast<const float4 *>(slot + lane * 16);
-                    v[0] = w.x; v[1] = w.y; v[2] = w.z; v[3] = w.w;
-                }
-                if (TP == 1) {
-                    // one earlier stage: the chain's fl(fl(x - c) + err) is fl(x - c) itself
-                    // for every finite result
-                    const float4 c = *reinterpret_cast<const float4 *>(slot + XB + lane * 16);
-                    v[0] = __fsub_rn(v[0], c.x);
-                    v[1] = __fsub_rn(v[1], c.y);
-                    v[2] = __fsub_rn(v[2], c.z);
-                    v[3] = __fsub_rn(v[3], c.w);
-                } else if (TP != 0) {
-                    float er[4] = {0.f, 0.f, 0.f, 0.f};
-                    for (int st = 0; st < tp; st++) {
-                        const float4 c = *reinterpret_cast<const float4 *>(slot + XB + st * 512 + lane * 16);
-                        const float cc[4] = {c.x, c.y, c.z, c.w};
-#pragma unroll
-                        for (int r = 0; r < 4; r++) {
-                            float err;
-                            two_sum(v[r], -cc[r], v[r], err);
-                            er[r] = __fadd_rn(er[r], err);
-                        }
+                for (int u = 0; u < n_rows; u++) {
+                    const int m = g * kBulkGroup + u;
+                    float2 v01, v23;
+                    row_of(gslots + u * row_bytes, v01, v23);
+                    if ((starts >> m) & 1u) {  // warp-uniform
+                        stash(m);
+                        run_c = __shfl_sync(0xffffffffu, cur.cl, m);
+                        run_start = m;
+                        s01 = s23 = e01 = e23 = make_float2(0.f, 0.f);
                     }
-#pragma unroll
-                    for (int r = 0; r < 4; r++) v[r] = __fadd_rn(v[r], er[r]);
+                    acc_two_sum2(s01, e01, v01);
+                    acc_two_sum2(s23, e23, v23);
                 }
-                if ((cur.brk >> m) & 1u) {  // warp-uniform
-                    if (run_c >= 0) stash(m);
-                    run_c = __shfl_sync(0xffffffffu, cur.cl, m);
-                    run_start = m;
-#pragma unroll
-                    for (int r = 0; r < 4; r++) s[r] = e[r] = 0.f;
-                }
-#pragma unroll
-                for (int r = 0; r < 4; r++) acc_two_sum(s[r], e[r], v[r]);
             }
             n_done++;
             __syncwarp();  // every lane has read the group's slots before they are refilled
             issue_next();
         }
-        if (run_c >= 0) stash(cur.nk);
+        stash(cur.nk);
         if (!has_next) break;
         cur = nxt;
         ci = cn;
