@@ -19,6 +19,7 @@
 #include <stdint.h>
 
 #include <algorithm>
+#include <utility>
 
 #include "qvg.h"
 
@@ -196,6 +197,35 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
         ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
         : "memory");
+}
+
+// ------------------------------------------------------------------------------------
+// Programmatic dependent launch.  Every kernel of the library is launched with
+// programmatic stream serialisation and begins with pdl_begin(): it lets the next kernel
+// in the stream launch (its CTAs take SM slots as this grid's CTAs retire) and then waits
+// until the previous kernel has completed and its writes are visible.  Kernel boundaries
+// then cost no launch latency and no empty ramp; the order of memory effects is that of
+// plain stream order.
+// ------------------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_begin() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+template <typename... Params, typename... Args>
+cudaError_t launch_kernel(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem,
+                          cudaStream_t st, Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
 // ------------------------------------------------------------------------------------

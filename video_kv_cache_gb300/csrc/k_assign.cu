@@ -159,6 +159,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     k_assign(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
              QPlan p, int t, int tiles_per_tensor, int nslots, uint32_t tmem_cols,
              uint32_t acc_stride) {
+    pdl_begin();
     extern __shared__ unsigned char smem_raw[];
     unsigned char *sm = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -518,6 +519,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // grid-stride over the queue, block 256.
 // --------------------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) k_refine(QPlan p, int t) {
+    pdl_begin();
     const int lane = threadIdx.x & 31;
     const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int nw = (gridDim.x * blockDim.x) >> 5;
@@ -728,13 +730,12 @@ cudaError_t launch_assign(const QPlan &p, const AssignMaps *maps, int t, int num
     cudaError_t e = cudaFuncSetAttribute(k_assign, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;
-    k_assign<<<grid, kThreads, smem, st>>>(maps->a, maps->b, p, t, tiles, nslots, cols, stride);
-    return cudaGetLastError();
+    return launch_kernel(k_assign, dim3(grid), dim3(kThreads), smem, st, maps->a, maps->b, p, t, tiles,
+                         nslots, cols, stride);
 }
 
 cudaError_t launch_refine(const QPlan &p, int t, int num_sms, cudaStream_t st) {
-    k_refine<<<num_sms * 8, 256, 0, st>>>(p, t);
-    return cudaGetLastError();
+    return launch_kernel(k_refine, dim3(num_sms * 8), dim3(256), 0, st, p, t);
 }
 
 }  // namespace qvg

@@ -62,6 +62,7 @@ __device__ __forceinline__ float e4m3_to_float(uint32_t b) {
 template <int BITS, int OUT, int TT>
 __global__ void __launch_bounds__(kDqThreads, 1)
     k_dequant(DPlan p, int W, int64_t n_chunks, int smem_tables, int wide_stores) {
+    pdl_begin();
     extern __shared__ __align__(16) float smem_f[];
     constexpr int MID = 1 << (BITS - 1);
     constexpr int PER16 = 16 / BITS;  // codes in a 16-bit half-word
@@ -284,8 +285,8 @@ cudaError_t launch_dq(const DPlan &p, int num_sms, int W, size_t table_bytes, bo
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const int64_t n_chunks = (p.N + p.chunk_len - 1) / p.chunk_len;
-    kern<<<num_sms, kDqThreads, smem, st>>>(p, W, n_chunks, smem_tables ? 1 : 0, wide);
-    return cudaGetLastError();
+    return launch_kernel(kern, dim3(num_sms), dim3(kDqThreads), smem, st, p, W, n_chunks,
+                         smem_tables ? 1 : 0, wide);
 }
 
 template <int BITS, int OUT>

@@ -39,6 +39,7 @@ __device__ __forceinline__ uint64_t splitmix64_next(uint64_t &state) {
 constexpr int kHashSlots = 1024;
 
 __global__ void k_init_indices(QPlan p, uint64_t seed, int64_t tid_base) {
+    pdl_begin();
     const int t = blockIdx.x + 1, h = blockIdx.y, lane = threadIdx.x;
     __shared__ int lo[kMaxC];
     __shared__ int pick[kMaxC];  // position swapped with position j at step j
@@ -78,8 +79,7 @@ __global__ void k_init_indices(QPlan p, uint64_t seed, int64_t tid_base) {
 }
 
 cudaError_t launch_init_indices(const QPlan &p, uint64_t seed, int64_t tid_base, cudaStream_t st) {
-    k_init_indices<<<dim3(p.T, p.H), 32, 0, st>>>(p, seed, tid_base);
-    return cudaGetLastError();
+    return launch_kernel(k_init_indices, dim3(p.T, p.H), dim3(32), 0, st, p, seed, tid_base);
 }
 
 // --------------------------------------------------------------------------------------
@@ -87,6 +87,7 @@ cudaError_t launch_init_indices(const QPlan &p, uint64_t seed, int64_t tid_base,
 // warm-start table.   grid (C, H), block 128 (one thread per channel).
 // --------------------------------------------------------------------------------------
 __global__ void k_init_centroids(QPlan p, int t) {
+    pdl_begin();
     const int j = blockIdx.x, h = blockIdx.y, k = threadIdx.x;
     float *dst = p.cent + h * p.cent_tstride + p.cent_off + (int64_t)(t - 1) * p.C * kD +
                  (int64_t)j * kD;
@@ -114,8 +115,7 @@ __global__ void k_init_centroids(QPlan p, int t) {
 }
 
 cudaError_t launch_init_centroids(const QPlan &p, int t, cudaStream_t st) {
-    k_init_centroids<<<dim3(p.C, p.H), kD, 0, st>>>(p, t);
-    return cudaGetLastError();
+    return launch_kernel(k_init_centroids, dim3(p.C, p.H), dim3(kD), 0, st, p, t);
 }
 
 // --------------------------------------------------------------------------------------
@@ -127,6 +127,7 @@ cudaError_t launch_init_centroids(const QPlan &p, int t, cudaStream_t st) {
 // grid H, block 128.
 // --------------------------------------------------------------------------------------
 __global__ void k_centre(QPlan p, int t) {
+    pdl_begin();
     const int h = blockIdx.x, k = threadIdx.x;
     float m = 0.f;
     if (t == 1) {
@@ -139,8 +140,7 @@ __global__ void k_centre(QPlan p, int t) {
 }
 
 cudaError_t launch_centre(const QPlan &p, int t, cudaStream_t st) {
-    k_centre<<<p.H, kD, 0, st>>>(p, t);
-    return cudaGetLastError();
+    return launch_kernel(k_centre, dim3(p.H), dim3(kD), 0, st, p, t);
 }
 
 // --------------------------------------------------------------------------------------
@@ -155,6 +155,7 @@ cudaError_t launch_centre(const QPlan &p, int t, cudaStream_t st) {
 constexpr int kPrepTokens = 64;
 
 __global__ void __launch_bounds__(256) k_prep(QPlan p, int t) {
+    pdl_begin();
     const int h = blockIdx.y;
     const int c8 = threadIdx.x & 15;
     const int64_t i0 = (int64_t)blockIdx.x * kPrepTokens;
@@ -236,8 +237,7 @@ __global__ void __launch_bounds__(256) k_prep(QPlan p, int t) {
 
 cudaError_t launch_prep(const QPlan &p, int t, cudaStream_t st) {
     dim3 grid((unsigned)((p.N + kPrepTokens - 1) / kPrepTokens), p.H);
-    k_prep<<<grid, 256, 0, st>>>(p, t);
-    return cudaGetLastError();
+    return launch_kernel(k_prep, grid, dim3(256), 0, st, p, t);
 }
 
 // --------------------------------------------------------------------------------------
@@ -253,6 +253,9 @@ __device__ __forceinline__ void store_planes(const QPlan &p, int h, int j, int k
 }
 
 __global__ void k_centroid_planes(QPlan p, int t) {
+    pdl_begin();
+    // the near-tie queue starts empty for the stage's first assignment
+    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *p.rq_count = 0;
     const int j = blockIdx.x, h = blockIdx.y, k = threadIdx.x;
     const float v = p.cent[h * p.cent_tstride + p.cent_off + (int64_t)(t - 1) * p.C * kD +
                            (int64_t)j * kD + k];
@@ -268,8 +271,7 @@ __global__ void k_centroid_planes(QPlan p, int t) {
 }
 
 cudaError_t launch_centroid_planes(const QPlan &p, int t, cudaStream_t st) {
-    k_centroid_planes<<<dim3(p.C, p.H), kD, 0, st>>>(p, t);
-    return cudaGetLastError();
+    return launch_kernel(k_centroid_planes, dim3(p.C, p.H), dim3(kD), 0, st, p, t);
 }
 
 // --------------------------------------------------------------------------------------
@@ -308,6 +310,7 @@ __device__ __forceinline__ void acc_two_sum2(float2 &s, float2 &e, float2 x) {
 }
 
 __global__ void __launch_bounds__(kSortBlock) k_sort_hist(QPlan p, int t) {
+    pdl_begin();
     __shared__ int hist[kMaxC];
     const int h = blockIdx.y, b = blockIdx.x;
     for (int j = threadIdx.x; j < p.C; j += kSortBlock) hist[j] = 0;
@@ -333,6 +336,7 @@ __global__ void __launch_bounds__(kSortBlock) k_sort_hist(QPlan p, int t) {
 // clusters before j; blockoff[b][j] (in place, over the block histogram) = offs[j] + the
 // tokens of cluster j in the blocks before b.
 __global__ void __launch_bounds__(256) k_sort_scan(QPlan p) {
+    pdl_begin();
     constexpr int NW = 8;
     __shared__ int tot[kMaxC];
     __shared__ int wsum[NW][32];
@@ -372,6 +376,7 @@ __global__ void __launch_bounds__(256) k_sort_scan(QPlan p) {
 }
 
 __global__ void __launch_bounds__(kSortBlock) k_sort_scatter(QPlan p, int t) {
+    pdl_begin();
     constexpr int NW = kSortBlock / 32;
     __shared__ int wcnt[NW][kMaxC];  // tokens of each cluster in each warp
     const int h = blockIdx.y, b = blockIdx.x;
@@ -480,6 +485,7 @@ struct SumChunk {
 
 template <int SRC, int TP>  // SRC: X dtype (0 bf16, 1 fp32, 3 fp16); TP: t - 1 (0..3), or -1
 __global__ void __launch_bounds__(256, 2) k_chunk_sums(QPlan p, int t) {
+    pdl_begin();
     static_assert(kChunk == 32, "one sorted position per lane");
     constexpr int XB = bulk_xbytes(SRC);
     extern __shared__ __align__(128) uint8_t bulk_smem[];
@@ -699,14 +705,16 @@ static cudaError_t launch_sums(const QPlan &p, int t, int num_sms, cudaStream_t 
     }
     const int64_t need = ((int64_t)p.H * p.nchunk + wpc - 1) / wpc;
     const int grid = (int)std::min<int64_t>(need, (int64_t)per_sm * num_sms);
-    k_chunk_sums<SRC, TP><<<grid, 32 * wpc, smem, st>>>(p, t);
-    return cudaSuccess;
+    return launch_kernel(k_chunk_sums<SRC, TP>, dim3(grid), dim3(32 * wpc), smem, st, p, t);
 }
 
 // One warp per cluster: the mean from the cluster's own slot, or, for clusters spread over
 // several chunks, from their pieces added in chunk order; empty clusters keep their
 // centroid.  Then the centroid and its GEMM planes are written.
 __global__ void __launch_bounds__(256) k_cluster_finalize(QPlan p, int t, int planes) {
+    pdl_begin();
+    // the near-tie queue of this round has been consumed: empty it for the next assignment
+    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *p.rq_count = 0;
     const int lane = threadIdx.x & 31;
     const int j = blockIdx.x * 8 + (threadIdx.x >> 5);
     const int h = blockIdx.y;
@@ -767,9 +775,11 @@ __global__ void __launch_bounds__(256) k_cluster_finalize(QPlan p, int t, int pl
 
 cudaError_t launch_cluster_means(const QPlan &p, int t, bool planes, int num_sms, cudaStream_t st) {
     const dim3 sgrid((unsigned)p.nsb, p.H);
-    k_sort_hist<<<sgrid, kSortBlock, 0, st>>>(p, t);
-    k_sort_scan<<<dim3((unsigned)((p.C + 31) / 32), p.H), 256, 0, st>>>(p);
-    k_sort_scatter<<<sgrid, kSortBlock, 0, st>>>(p, t);
+    cudaError_t e = launch_kernel(k_sort_hist, sgrid, dim3(kSortBlock), 0, st, p, t);
+    if (e == cudaSuccess)
+        e = launch_kernel(k_sort_scan, dim3((unsigned)((p.C + 31) / 32), p.H), dim3(256), 0, st, p);
+    if (e == cudaSuccess) e = launch_kernel(k_sort_scatter, sgrid, dim3(kSortBlock), 0, st, p, t);
+    if (e != cudaSuccess) return e;
     auto sums = [&](auto src) {
         constexpr int S = decltype(src)::value;
         switch (t - 1) {
@@ -780,12 +790,12 @@ cudaError_t launch_cluster_means(const QPlan &p, int t, bool planes, int num_sms
             default: return launch_sums<S, -1>(p, t, num_sms, st);
         }
     };
-    const cudaError_t e = p.in_dtype == DT_F32   ? sums(std::integral_constant<int, 1>())
-                          : p.in_dtype == DT_F16 ? sums(std::integral_constant<int, 3>())
-                                                 : sums(std::integral_constant<int, 0>());
+    e = p.in_dtype == DT_F32   ? sums(std::integral_constant<int, 1>())
+        : p.in_dtype == DT_F16 ? sums(std::integral_constant<int, 3>())
+                               : sums(std::integral_constant<int, 0>());
     if (e != cudaSuccess) return e;
-    k_cluster_finalize<<<dim3((unsigned)((p.C + 7) / 8), p.H), 256, 0, st>>>(p, t, planes ? 1 : 0);
-    return cudaGetLastError();
+    return launch_kernel(k_cluster_finalize, dim3((unsigned)((p.C + 7) / 8), p.H), dim3(256), 0, st, p, t,
+                         planes ? 1 : 0);
 }
 
 // --------------------------------------------------------------------------------------
@@ -800,6 +810,7 @@ constexpr int kEncTokens = 32;
 // TT: the number of stages when it is 0..4 (the stage loop unrolled), -1 for any T.
 template <int BITS, int TT>
 __global__ void __launch_bounds__(256) k_encode(QPlan p) {
+    pdl_begin();
     constexpr int QMAX = (1 << (BITS - 1)) - 1, MID = 1 << (BITS - 1);
     const int T = TT >= 0 ? TT : p.T;
     const int h = blockIdx.y;
@@ -920,14 +931,13 @@ template <int BITS>
 static cudaError_t launch_encode_b(const QPlan &p, cudaStream_t st) {
     const dim3 grid((unsigned)((p.N + kEncTokens - 1) / kEncTokens), p.H);
     switch (p.T) {
-        case 0: k_encode<BITS, 0><<<grid, 256, 0, st>>>(p); break;
-        case 1: k_encode<BITS, 1><<<grid, 256, 0, st>>>(p); break;
-        case 2: k_encode<BITS, 2><<<grid, 256, 0, st>>>(p); break;
-        case 3: k_encode<BITS, 3><<<grid, 256, 0, st>>>(p); break;
-        case 4: k_encode<BITS, 4><<<grid, 256, 0, st>>>(p); break;
-        default: k_encode<BITS, -1><<<grid, 256, 0, st>>>(p); break;
+        case 0: return launch_kernel(k_encode<BITS, 0>, grid, dim3(256), 0, st, p);
+        case 1: return launch_kernel(k_encode<BITS, 1>, grid, dim3(256), 0, st, p);
+        case 2: return launch_kernel(k_encode<BITS, 2>, grid, dim3(256), 0, st, p);
+        case 3: return launch_kernel(k_encode<BITS, 3>, grid, dim3(256), 0, st, p);
+        case 4: return launch_kernel(k_encode<BITS, 4>, grid, dim3(256), 0, st, p);
+        default: return launch_kernel(k_encode<BITS, -1>, grid, dim3(256), 0, st, p);
     }
-    return cudaGetLastError();
 }
 
 cudaError_t launch_encode(const QPlan &p, cudaStream_t st) {

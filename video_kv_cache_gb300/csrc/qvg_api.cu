@@ -132,7 +132,6 @@ qvg_status run_stages(QPlan &p, const AssignMaps *maps, int num_sms, cudaStream_
         if (t >= 2) step(launch_init_centroids(p, t, st));
         step(launch_centroid_planes(p, t, st));
         for (int it = 1; it <= p.iters && rc == QVG_OK; it++) {
-            step(cudaMemsetAsync(p.rq_count, 0, 4, st));
             step(launch_assign(p, maps, t, num_sms, st));
             step(launch_refine(p, t, num_sms, st));
             step(launch_cluster_means(p, t, it < p.iters, num_sms, st));
@@ -327,7 +326,6 @@ qvg_status qvg_reassign(const qvg_quant_params *prm, const void *X, const qvg_bu
         return QVG_ERR_CUDA;
     }
     cudaError_t e = launch_centroid_planes(p, p.T, st);
-    if (e == cudaSuccess) e = cudaMemsetAsync(p.rq_count, 0, 4, st);
     if (e == cudaSuccess) e = launch_assign(p, maps, p.T, num_sms, st);
     if (e == cudaSuccess) e = launch_refine(p, p.T, num_sms, st);
     assign_release(maps);
