@@ -62,6 +62,13 @@ constexpr uint32_t kKBlockBytes = kTileM * 64 * 2;  // 16 KB: 64 fp16 channels o
 constexpr int kABlocks = 2;                           // A blocks per tile (128 channels)
 constexpr uint32_t kSpinLimit = 1u << 22;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // a pipeline wait gives up after 2 s
+// minimum of three fp32 values (one instruction on sm_100-class GPUs; NaN inputs are
+// ignored unless all three are NaN, as with fminf)
+__device__ __forceinline__ float fmin3(float a, float b, float c) {
+    float r;
+    asm("min.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
 // coefficients of the bound on |acc - r.c| (see the error bound above)
 constexpr float kDnRel = 0x1.01p0f;
 constexpr float kRnRel = kBPlanes == 1 ? 0x1.11p-11f : 0x1.03p-15f;
@@ -178,9 +185,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float *cn_s = reinterpret_cast<float *>(
         (reinterpret_cast<uintptr_t>(tmem_slot + 4) + 15) & ~static_cast<uintptr_t>(15));  // [kEpiGroups][Cpad]
     float *x_best = cn_s + kEpiGroups * Cpad;     // [kEpiGroups][2 halves][128 rows]
-    float *x_second = x_best + kEpiGroups * 2 * kTileM;
-    int *x_idx = reinterpret_cast<int *>(x_second + kEpiGroups * 2 * kTileM);
-    uint32_t *x_cand = reinterpret_cast<uint32_t *>(x_idx + kEpiGroups * 2 * kTileM);  // [kEpiGroups][128][4]
+    uint32_t *x_cand = reinterpret_cast<uint32_t *>(x_best + kEpiGroups * 2 * kTileM);  // [kEpiGroups][128][4]
 
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -319,8 +324,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int pair_bar = 1 + grp * 4 + quarter;  // named barrier of the two warps of a row block
         const int grp_bar = 9 + grp;                  // named barrier of the group's 8 warps
         float *cns = cn_s + grp * Cpad;
-        float *xb = x_best + grp * 2 * kTileM, *xs = x_second + grp * 2 * kTileM;
-        int *xi = x_idx + grp * 2 * kTileM;
+        float *xb = x_best + grp * 2 * kTileM;
         uint32_t *xc = x_cand + grp * 4 * kTileM;
         int cur_h = -1;
         float cmax = 0.f, cmax2 = 0.f;
@@ -360,13 +364,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc_fence_after();
             const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + buf * acc_stride;
-            // Pass 1 over this warp's chunks of 32 columns: best score, second best, lowest
-            // index of the best, and each chunk's minimum (for the candidate pass).  Chunks
-            // are visited in increasing order and a chunk's best only replaces a strictly
-            // larger one, so ties keep the lowest index.
-            float best = INFINITY, second = INFINITY;
-            int bj = 0;
+            const float2 m2 = make_float2(-2.f, -2.f);
+            // Pass A over this warp's chunks of 32 columns: each chunk's minimum score.
             float cmin0 = INFINITY, cmin1 = INFINITY, cmin2 = INFINITY, cmin3 = INFINITY;
+            float own = INFINITY;
             // one copy of the chunk body (a rolled loop keeps the kernel in the instruction
             // cache); the chunk minima stay in named registers
 #pragma unroll 1
@@ -374,41 +375,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int cb = ch_lo + c;
                 float v[32];
                 tc_ld32(taddr + cb * 32, v);
-                float b1 = INFINITY, s1 = INFINITY;
-                int j1 = 0;
+                float ma = INFINITY, mb = INFINITY;
 #pragma unroll
                 for (int q = 0; q < 32; q += 4) {
                     const float4 c4 = *reinterpret_cast<const float4 *>(cns + cb * 32 + q);
-                    const float cc[4] = {c4.x, c4.y, c4.z, c4.w};
-#pragma unroll
-                    for (int u = 0; u < 4; u++) {
-                        const float sc = __fmaf_rn(-2.f, v[q + u], cc[u]);
-                        s1 = fminf(s1, fmaxf(sc, b1));
-                        if (sc < b1) j1 = q + u;  // column within the chunk
-                        b1 = fminf(b1, sc);
-                    }
+                    const float2 s01 = __ffma2_rn(m2, make_float2(v[q], v[q + 1]), make_float2(c4.x, c4.y));
+                    const float2 s23 = __ffma2_rn(m2, make_float2(v[q + 2], v[q + 3]), make_float2(c4.z, c4.w));
+                    ma = fmin3(ma, s01.x, s01.y);
+                    mb = fmin3(mb, s23.x, s23.y);
                 }
-                cmin0 = c == 0 ? b1 : cmin0;
-                cmin1 = c == 1 ? b1 : cmin1;
-                cmin2 = c == 2 ? b1 : cmin2;
-                cmin3 = c == 3 ? b1 : cmin3;
-                second = fminf(second, fminf(s1, fmaxf(best, b1)));
-                if (b1 < best) bj = cb * 32 + j1;
-                best = fminf(best, b1);
+                const float m = fminf(ma, mb);
+                cmin0 = c == 0 ? m : cmin0;
+                cmin1 = c == 1 ? m : cmin1;
+                cmin2 = c == 2 ? m : cmin2;
+                cmin3 = c == 3 ? m : cmin3;
+                own = fminf(own, m);
             }
-            // Both warps of the pair merge the two column halves the same way; the lower
-            // half's index wins ties.
-            xb[half * kTileM + row] = best;
-            xs[half * kTileM + row] = second;
-            xi[half * kTileM + row] = bj;
+            // the row's best score over both column halves
+            xb[half * kTileM + row] = own;
             asm volatile("bar.sync %0, 64;" ::"r"(pair_bar) : "memory");
-            {
-                const float ob = xb[(half ^ 1) * kTileM + row], os = xs[(half ^ 1) * kTileM + row];
-                const int oj = xi[(half ^ 1) * kTileM + row];
-                second = fminf(fminf(second, os), fmaxf(best, ob));
-                if (half == 0 ? ob < best : ob <= best) bj = oj;
-                best = fminf(best, ob);
-            }
+            const float best = fminf(own, xb[(half ^ 1) * kTileM + row]);
             // Every cluster whose score is within twice the error bound of the best may be
             // the nearest one (bound in the file header).
             const float err = 2.f * (kDnRel * dn * cmax + kRnRel * rn * cmax +
@@ -416,51 +402,78 @@ __global__ void __launch_bounds__(kThreads, 1)
                               0x1.1p-17f * cmax2;
             // An untrusted row (fp16 operands may have overflowed, so its scores may be inf
             // or NaN) gets lim = +inf.  The tests below are written as !(x > lim), which is
-            // true for every score of such a row, NaN included, so it re-scores every
-            // cluster; for a trusted row (finite scores) it is x <= lim.
+            // true for every score of such a row, NaN included, so every cluster becomes a
+            // candidate; for a trusted row (finite scores) it is x <= lim.
             const bool trusted = rn < kFp16Safe && cmax < kFp16Safe;
             const float lim = trusted ? best + (2.f * err + 1e-30f) : INFINITY;
-            const bool need = valid && !(second > lim);
-            const bool any_need = __any_sync(0xffffffffu, need);  // the same in both warps
-            // Candidate pass: only chunks whose minimum is within the limit for some row.
+            // Pass B: the candidate clusters (score within the limit), one bit per column,
+            // over the chunks that hold a candidate for some row of the warp.  The best
+            // score is always a candidate; a row with a single candidate has its nearest
+            // centroid, a row with several goes to exact re-scoring.
             uint32_t cand0 = 0u, cand1 = 0u, cand2 = 0u, cand3 = 0u;
-            if (any_need) {
 #pragma unroll 1
-                for (int c = 0; c < ch_hi - ch_lo; c++) {
-                    const float cm = c == 0 ? cmin0 : c == 1 ? cmin1 : c == 2 ? cmin2 : cmin3;
-                    if (!__any_sync(0xffffffffu, need && !(cm > lim))) continue;
-                    const int cb = ch_lo + c;
-                    float v[32];
-                    tc_ld32(taddr + cb * 32, v);
-                    uint32_t w = 0u;
+            for (int c = 0; c < ch_hi - ch_lo; c++) {
+                const float cm = c == 0 ? cmin0 : c == 1 ? cmin1 : c == 2 ? cmin2 : cmin3;
+                if (!__any_sync(0xffffffffu, !(cm > lim))) continue;
+                const int cb = ch_lo + c;
+                float v[32];
+                tc_ld32(taddr + cb * 32, v);
+                uint32_t w = 0u;
 #pragma unroll
-                    for (int q = 0; q < 32; q += 4) {
-                        const float4 c4 = *reinterpret_cast<const float4 *>(cns + cb * 32 + q);
-                        const float cc[4] = {c4.x, c4.y, c4.z, c4.w};
-#pragma unroll
-                        for (int u = 0; u < 4; u++) {
-                            const float sc = __fmaf_rn(-2.f, v[q + u], cc[u]);
-                            if (!(sc > lim) && cb * 32 + q + u < C) w |= 1u << (q + u);
-                        }
-                    }
-                    if (!need) w = 0u;
-                    cand0 = c == 0 ? w : cand0;
-                    cand1 = c == 1 ? w : cand1;
-                    cand2 = c == 2 ? w : cand2;
-                    cand3 = c == 3 ? w : cand3;
+                for (int q = 0; q < 32; q += 4) {
+                    const float4 c4 = *reinterpret_cast<const float4 *>(cns + cb * 32 + q);
+                    // the same roundings as pass A (a packed fma rounds each lane alone)
+                    const float2 s01 = make_float2(__fmaf_rn(-2.f, v[q], c4.x), __fmaf_rn(-2.f, v[q + 1], c4.y));
+                    const float2 s23 = make_float2(__fmaf_rn(-2.f, v[q + 2], c4.z), __fmaf_rn(-2.f, v[q + 3], c4.w));
+                    if (!(s01.x > lim)) w |= 1u << q;
+                    if (!(s01.y > lim)) w |= 2u << q;
+                    if (!(s23.x > lim)) w |= 4u << q;
+                    if (!(s23.y > lim)) w |= 8u << q;
                 }
+                // only real clusters (an untrusted row's padded columns pass the test)
+                const int live = C - cb * 32;
+                if (live < 32) w &= (1u << live) - 1u;
+                cand0 = c == 0 ? w : cand0;
+                cand1 = c == 1 ? w : cand1;
+                cand2 = c == 2 ? w : cand2;
+                cand3 = c == 3 ? w : cand3;
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(acc_empty + grp));
-            if (any_need) {
-                // the upper half hands its candidate words to the lower half, which queues
-                // the rows (one atomic per warp)
-                if (half == 1)
-                    *reinterpret_cast<uint4 *>(xc + row * 4) = make_uint4(cand0, cand1, cand2, cand3);
-                asm volatile("bar.sync %0, 64;" ::"r"(pair_bar) : "memory");
-                if (half == 0) {
-                    const unsigned m = __ballot_sync(0xffffffffu, need);
+            // the upper half hands its candidate words to the lower half, which decides
+            if (half == 1)
+                *reinterpret_cast<uint4 *>(xc + row * 4) = make_uint4(cand0, cand1, cand2, cand3);
+            asm volatile("bar.sync %0, 64;" ::"r"(pair_bar) : "memory");
+            if (half == 0) {
+                // candidate words in chunk order: chunk c belongs to the lower half when
+                // c < split
+                const uint4 up = *reinterpret_cast<const uint4 *>(xc + row * 4);
+                auto word_of = [&](int c) {  // c is a compile-time constant below
+                    const uint32_t lo_w[4] = {cand0, cand1, cand2, cand3};
+                    const uint32_t up_w[4] = {up.x, up.y, up.z, up.w};
+                    uint32_t w = 0u;
+#pragma unroll
+                    for (int k = 0; k < 4; k++) {
+                        if (c == k && c < split) w = lo_w[k];
+                        if (c == split + k && c < nchunks) w = up_w[k];
+                    }
+                    return w;
+                };
+                int n_cand = 0, bj = 0;
+                bool found = false;
+#pragma unroll
+                for (int c = 0; c < 8; c++) {
+                    const uint32_t w = word_of(c);
+                    n_cand += __popc(w);
+                    if (!found && w) {
+                        bj = c * 32 + __ffs(w) - 1;
+                        found = true;
+                    }
+                }
+                const bool need = valid && n_cand > 1;
+                const unsigned m = __ballot_sync(0xffffffffu, need);
+                if (m) {
                     int base = 0;
                     if (lane == 0) base = atomicAdd(p.rq_count, __popc(m));
                     base = __shfl_sync(0xffffffffu, base, 0);
@@ -469,24 +482,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                         RefineReq *rq = p.rq + base + __popc(m & ((1u << lane) - 1u));
                         rq->h = h;
                         rq->i = (int)i;
-                        // chunk c belongs to the lower half when c < split
-                        const uint4 up = *reinterpret_cast<const uint4 *>(xc + row * 4);
-                        const uint32_t lo_w[4] = {cand0, cand1, cand2, cand3};
-                        const uint32_t up_w[4] = {up.x, up.y, up.z, up.w};
 #pragma unroll
-                        for (int c = 0; c < 8; c++) {
-                            uint32_t w = 0u;
-#pragma unroll
-                            for (int k = 0; k < 4; k++) {
-                                if (c == k && c < split) w = lo_w[k];
-                                if (c == split + k && c < nchunks) w = up_w[k];
-                            }
-                            rq->cand[c] = w;
-                        }
+                        for (int c = 0; c < 8; c++) rq->cand[c] = word_of(c);
                     }
                 }
+                // a row with several candidates gets its lowest one here; k_refine
+                // overwrites it with the exact choice
+                if (valid) p.pi[(int64_t)(h * p.T + t - 1) * p.cap + p.tok_off + i] = (uint8_t)bj;
             }
-            if (half == 0 && valid) p.pi[(int64_t)(h * p.T + t - 1) * p.cap + p.tok_off + i] = (uint8_t)bj;
         }
         if (p.stats && half == 0) {
 #pragma unroll
@@ -653,10 +656,10 @@ static EncodeTiledFn encode_fn() {
 static const int kMaxSmem = 232448;  // opt-in shared memory per block on sm_100-class GPUs
 
 // barriers, TMEM slot, abort flag, and per epilogue group ||c||^2 and the column-half
-// exchange (best, second, index per row)
+// exchange (best score and candidate words per row)
 static size_t assign_tail_bytes(int nslots, int Cpad) {
     return (size_t)(2 * nslots + 3 + 2 * kEpiGroups) * 8 + 16 + 16 /* alignment */ +
-           (size_t)kEpiGroups * (Cpad + 3 * 2 * kTileM + 4 * kTileM) * 4;
+           (size_t)kEpiGroups * (Cpad + 2 * kTileM + 4 * kTileM) * 4;
 }
 
 static size_t assign_b_bytes(int Cpad) { return (size_t)2 * kBPlanes * Cpad * 128; }
