@@ -183,6 +183,18 @@ __device__ __forceinline__ bool mbar_try_suspend(uint32_t bar, uint32_t parity) 
     return ok != 0u;
 }
 
+// TMA gather of four rows (2D tensor map whose box is one row high) into consecutive
+// shared memory, counted on the mbarrier's transaction count.  col * element size must be
+// a multiple of 16 bytes.
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap *map, int col, int r0,
+                                            int r1, int r2, int r3, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(col), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar)
+        : "memory");
+}
+
 __device__ __forceinline__ uint64_t global_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
@@ -236,7 +248,9 @@ cudaError_t launch_init_centroids(const QPlan &p, int t, cudaStream_t st);
 cudaError_t launch_centre(const QPlan &p, int t, cudaStream_t st);
 cudaError_t launch_prep(const QPlan &p, int t, cudaStream_t st);
 cudaError_t launch_centroid_planes(const QPlan &p, int t, cudaStream_t st);
-cudaError_t launch_cluster_means(const QPlan &p, int t, bool planes, int num_sms, cudaStream_t st);
+struct AssignMaps;
+cudaError_t launch_cluster_means(const QPlan &p, const AssignMaps *maps, int t, bool planes,
+                                 int num_sms, cudaStream_t st);
 constexpr int kSortBlock = 256;  // tokens per block of the counting sort
 constexpr int kChunk = 32;       // sorted positions summed by one warp
 cudaError_t launch_encode(const QPlan &p, cudaStream_t st);
@@ -245,6 +259,12 @@ cudaError_t launch_encode(const QPlan &p, cudaStream_t st);
 struct AssignMaps {
     CUtensorMap a;
     CUtensorMap b;
+    // row views for the cluster sums' gathers: X as [rows][128] (when every tensor starts
+    // on a whole row, x_stride % 128 == 0; gather = 0 otherwise) and the centroid tables
+    // as [rows][128] fp32
+    CUtensorMap x_rows;
+    CUtensorMap c_rows;
+    int gather;
 };
 // Encodes the maps for plan p into caller-provided storage (no allocation).
 cudaError_t assign_encode(const QPlan &p, AssignMaps *maps);

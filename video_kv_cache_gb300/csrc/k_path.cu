@@ -154,6 +154,11 @@ cudaError_t launch_centre(const QPlan &p, int t, cudaStream_t st) {
 // --------------------------------------------------------------------------------------
 constexpr int kPrepTokens = 64;
 
+// G tokens per thread (16 threads per token, 8 channels each): all of a thread's loads are
+// issued before its arithmetic, so that G rows are in flight per thread.  CHAIN: the stage
+// subtracts earlier stages' centroids (t >= 2).  Stage 1 takes G = 4; the chained form
+// takes G = 1, where more tokens per thread cost more occupancy than they gain.
+template <int G, bool CHAIN>
 __global__ void __launch_bounds__(256) k_prep(QPlan p, int t) {
     pdl_begin();
     const int h = blockIdx.y;
@@ -163,63 +168,87 @@ __global__ void __launch_bounds__(256) k_prep(QPlan p, int t) {
     float mu[8];
     load_f8(p.mu + h * kD + c8 * 8, mu);
     bool finite = true, bad_index = false;
-    for (int64_t ib = i0; ib < i1; ib += 16) {
+#pragma unroll 1
+    for (int64_t ib = i0; ib < i1; ib += 16 * G) {
         // the loop bound is uniform over the block, so every lane reaches the shuffles
-        const int64_t i = ib + (threadIdx.x >> 4);
-        const bool valid = i < i1;
-        float x[8], s[8], e[8];
-        if (valid) {
-            load_x8(p.X, p.in_dtype, h * p.x_stride + i * kD + c8 * 8, x);
-        } else {
+        float s[G][8];
 #pragma unroll
-            for (int q = 0; q < 8; q++) x[q] = 0.f;
-        }
+        for (int g = 0; g < G; g++) {
+            const int64_t i = ib + 16 * g + (threadIdx.x >> 4);
+            if (i < i1) {
+                load_x8(p.X, p.in_dtype, h * p.x_stride + i * kD + c8 * 8, s[g]);
+            } else {
 #pragma unroll
-        for (int q = 0; q < 8; q++) {
-            finite &= isfinite(x[q]);
-            s[q] = x[q];
-            e[q] = 0.f;
-        }
-        for (int st = 1; valid && st < t; st++) {
-            int pj = p.pi[(int64_t)(h * p.T + st - 1) * p.cap + p.tok_off + i];
-            if (pj >= p.C) {
-                pj = p.C - 1;
-                bad_index = true;
+                for (int q = 0; q < 8; q++) s[g][q] = 0.f;
             }
-            float c[8];
-            load_f8(p.cent + h * p.cent_tstride + p.cent_off + (int64_t)(st - 1) * p.C * kD +
-                        (int64_t)pj * kD + c8 * 8, c);
+#pragma unroll
+            for (int q = 0; q < 8; q++) finite &= isfinite(s[g][q]);
+        }
+        if constexpr (CHAIN) {
+            float e[G][8];
+#pragma unroll
+            for (int g = 0; g < G; g++)
+#pragma unroll
+                for (int q = 0; q < 8; q++) e[g][q] = 0.f;
+            for (int st = 1; st < t; st++) {
+                int pj[G];
+#pragma unroll
+                for (int g = 0; g < G; g++) {
+                    const int64_t i = ib + 16 * g + (threadIdx.x >> 4);
+                    pj[g] = 0;
+                    if (i < i1) {
+                        pj[g] = p.pi[(int64_t)(h * p.T + st - 1) * p.cap + p.tok_off + i];
+                        if (pj[g] >= p.C) {
+                            pj[g] = p.C - 1;
+                            bad_index = true;
+                        }
+                    }
+                }
+                float c[G][8];
+#pragma unroll
+                for (int g = 0; g < G; g++)
+                    load_f8(p.cent + h * p.cent_tstride + p.cent_off + (int64_t)(st - 1) * p.C * kD +
+                                (int64_t)pj[g] * kD + c8 * 8, c[g]);
+#pragma unroll
+                for (int g = 0; g < G; g++)
+#pragma unroll
+                    for (int q = 0; q < 8; q++) {
+                        float err;
+                        two_sum(s[g][q], -c[g][q], s[g][q], err);
+                        e[g][q] = __fadd_rn(e[g][q], err);
+                    }
+            }
+#pragma unroll
+            for (int g = 0; g < G; g++)
+#pragma unroll
+                for (int q = 0; q < 8; q++) s[g][q] = __fadd_rn(s[g][q], e[g][q]);
+        }
+#pragma unroll
+        for (int g = 0; g < G; g++) {
+            const int64_t i = ib + 16 * g + (threadIdx.x >> 4);
+            const bool valid = i < i1;
+            float ss = 0.f, dd = 0.f;
+            __align__(16) __half a16[8];
 #pragma unroll
             for (int q = 0; q < 8; q++) {
-                float err;
-                two_sum(s[q], -c[q], s[q], err);
-                e[q] = __fadd_rn(e[q], err);
+                const float v = __fsub_rn(s[g][q], mu[q]);
+                a16[q] = __float2half_rn(v);
+                const float dv = __fsub_rn(v, __half2float(a16[q]));  // exact
+                ss = __fmaf_rn(v, v, ss);
+                dd = __fmaf_rn(dv, dv, dd);
             }
-        }
-        float r[8];
+            if (valid)
+                *reinterpret_cast<uint4 *>(p.A + ((int64_t)h * p.N + i) * kD + c8 * 8) =
+                    *reinterpret_cast<uint4 *>(a16);
 #pragma unroll
-        for (int q = 0; q < 8; q++) r[q] = __fadd_rn(s[q], e[q]);
-        float ss = 0.f, dd = 0.f;
-        __align__(16) __half a16[8];
-#pragma unroll
-        for (int q = 0; q < 8; q++) {
-            const float v = __fsub_rn(r[q], mu[q]);
-            a16[q] = __float2half_rn(v);
-            const float dv = __fsub_rn(v, __half2float(a16[q]));  // exact
-            ss = __fmaf_rn(v, v, ss);
-            dd = __fmaf_rn(dv, dv, dd);
-        }
-        if (valid)
-            *reinterpret_cast<uint4 *>(p.A + ((int64_t)h * p.N + i) * kD + c8 * 8) =
-                *reinterpret_cast<uint4 *>(a16);
-#pragma unroll
-        for (int o = 8; o >= 1; o >>= 1) {
-            ss += __shfl_xor_sync(0xffffffffu, ss, o);
-            dd += __shfl_xor_sync(0xffffffffu, dd, o);
-        }
-        if (valid && c8 == 0) {
-            p.rnorm[h * p.N + i] = sqrtf(ss);
-            p.dnorm[h * p.N + i] = sqrtf(dd);
+            for (int o = 8; o >= 1; o >>= 1) {
+                ss += __shfl_xor_sync(0xffffffffu, ss, o);
+                dd += __shfl_xor_sync(0xffffffffu, dd, o);
+            }
+            if (valid && c8 == 0) {
+                p.rnorm[h * p.N + i] = sqrtf(ss);
+                p.dnorm[h * p.N + i] = sqrtf(dd);
+            }
         }
     }
     // one status update per block
@@ -237,7 +266,8 @@ __global__ void __launch_bounds__(256) k_prep(QPlan p, int t) {
 
 cudaError_t launch_prep(const QPlan &p, int t, cudaStream_t st) {
     dim3 grid((unsigned)((p.N + kPrepTokens - 1) / kPrepTokens), p.H);
-    return launch_kernel(k_prep, grid, dim3(256), 0, st, p, t);
+    if (t == 1) return launch_kernel(k_prep<4, false>, grid, dim3(256), 0, st, p, t);
+    return launch_kernel(k_prep<1, true>, grid, dim3(256), 0, st, p, t);
 }
 
 // --------------------------------------------------------------------------------------
@@ -478,13 +508,16 @@ __device__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
 struct SumChunk {
     int h, k, nk;           // tensor, chunk, positions in the chunk
     int id, cl;             // the lane's token and cluster (cl = -1 past the end)
+    int xrow, crow;         // row of the token in the X row view; first row of the tables
     int c_prev, c_next;     // clusters just before and after the chunk (-1: none)
     uint32_t pk0, pk1;      // the token's earlier clusters, 8 bits a stage
     uint32_t brk;           // bit m: position m begins a new run
 };
 
 template <int SRC, int TP>  // SRC: X dtype (0 bf16, 1 fp32, 3 fp16); TP: t - 1 (0..3), or -1
-__global__ void __launch_bounds__(256, 2) k_chunk_sums(QPlan p, int t) {
+__global__ void __launch_bounds__(256, 2)
+    k_chunk_sums(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmC,
+                 QPlan p, int t, int gather) {
     pdl_begin();
     static_assert(kChunk == 32, "one sorted position per lane");
     constexpr int XB = bulk_xbytes(SRC);
@@ -516,6 +549,8 @@ __global__ void __launch_bounds__(256, 2) k_chunk_sums(QPlan p, int t) {
         const bool mine = lane < m.nk;
         m.id = mine ? p.ids[base + lane] : 0;
         m.cl = mine ? (int)p.cid[base + lane] : -1;
+        m.xrow = (int)(m.h * (p.x_stride / kD)) + m.id;
+        m.crow = (int)((m.h * p.cent_tstride + p.cent_off) / kD);
         m.c_prev = m.k > 0 ? (int)p.cid[base - 1] : -1;
         m.c_next = c0 + m.nk < p.N ? (int)p.cid[base + m.nk] : -1;
     };
@@ -535,22 +570,52 @@ __global__ void __launch_bounds__(256, 2) k_chunk_sums(QPlan p, int t) {
     auto n_groups = [](const SumChunk &m) { return (m.nk + kBulkGroup - 1) / kBulkGroup; };
 
     uint32_t n_issued = 0, n_done = 0;  // groups issued / summed by this warp so far
-    // copies of group g of chunk m (positions 8g..8g+7) into half (n_issued & 1) of the slots
+    // Group g of chunk m (positions 8g..8g+7) goes to half (n_issued & 1) of the warp's
+    // slots: its X rows at the half's start (XB bytes each), then for each earlier stage
+    // the 8 centroid rows (512 bytes each).
     auto issue = [&](const SumChunk &m, int g) {
         const int n_rows = min(kBulkGroup, m.nk - g * kBulkGroup);
         const int half = n_issued & 1;
         const uint32_t bar = bars + 8 * half;
-        if (lane == 0) mbar_expect_tx(bar, (uint32_t)(n_rows * row_bytes));
-        __syncwarp();
-        if (lane >= g * kBulkGroup && lane < g * kBulkGroup + n_rows) {
-            const uint32_t dst = ring + (half * kBulkGroup + (lane & (kBulkGroup - 1))) * row_bytes;
-            bulk_g2s(dst,
-                     static_cast<const char *>(p.X) + (m.h * p.x_stride + (int64_t)m.id * kD) * (XB / kD),
-                     XB, bar);
-            const char *cb = reinterpret_cast<const char *>(p.cent + m.h * p.cent_tstride + p.cent_off);
-            for (int st = 0; st < tp; st++) {
-                const int pj = min((int)(((st < 4 ? m.pk0 : m.pk1) >> (8 * (st & 3))) & 255u), p.C - 1);
-                bulk_g2s(dst + XB + st * 512, cb + ((int64_t)st * p.C + pj) * kD * 4, 512, bar);
+        const uint32_t hb = ring + half * kBulkGroup * row_bytes;
+        if (gather) {
+            // four rows per TMA gather; a short last group repeats its last row
+            const int n4 = (n_rows + 3) >> 2;
+            if (lane == 0) mbar_expect_tx(bar, (uint32_t)(n4 * 4 * row_bytes));
+            __syncwarp();
+            for (int u4 = 0; u4 < n4; u4++) {
+                int src[4];
+#pragma unroll
+                for (int k = 0; k < 4; k++) src[k] = min(g * kBulkGroup + 4 * u4 + k, m.nk - 1);
+                int r[4];
+#pragma unroll
+                for (int k = 0; k < 4; k++) r[k] = __shfl_sync(0xffffffffu, m.xrow, src[k]);
+                if (lane == 0) tma_gather4(hb + 4 * u4 * XB, &tmX, 0, r[0], r[1], r[2], r[3], bar);
+                for (int st = 0; st < tp; st++) {
+                    const int pj = min((int)(((st < 4 ? m.pk0 : m.pk1) >> (8 * (st & 3))) & 255u), p.C - 1);
+                    const int crow = m.crow + st * p.C + pj;
+#pragma unroll
+                    for (int k = 0; k < 4; k++) r[k] = __shfl_sync(0xffffffffu, crow, src[k]);
+                    if (lane == 0)
+                        tma_gather4(hb + kBulkGroup * XB + st * kBulkGroup * 512 + 4 * u4 * 512, &tmC, 0,
+                                    r[0], r[1], r[2], r[3], bar);
+                }
+            }
+        } else {
+            // one bulk copy per row, issued by the lane that holds the row
+            if (lane == 0) mbar_expect_tx(bar, (uint32_t)(n_rows * row_bytes));
+            __syncwarp();
+            if (lane >= g * kBulkGroup && lane < g * kBulkGroup + n_rows) {
+                const int u = lane & (kBulkGroup - 1);
+                bulk_g2s(hb + u * XB,
+                         static_cast<const char *>(p.X) + (m.h * p.x_stride + (int64_t)m.id * kD) * (XB / kD),
+                         XB, bar);
+                const char *cb = reinterpret_cast<const char *>(p.cent + m.h * p.cent_tstride + p.cent_off);
+                for (int st = 0; st < tp; st++) {
+                    const int pj = min((int)(((st < 4 ? m.pk0 : m.pk1) >> (8 * (st & 3))) & 255u), p.C - 1);
+                    bulk_g2s(hb + kBulkGroup * XB + st * kBulkGroup * 512 + u * 512,
+                             cb + ((int64_t)st * p.C + pj) * kD * 4, 512, bar);
+                }
             }
         }
         n_issued++;
@@ -599,7 +664,8 @@ __global__ void __launch_bounds__(256, 2) k_chunk_sums(QPlan p, int t) {
             reinterpret_cast<float4 *>(dst + kD)[lane] = make_float4(e01.x, e01.y, e23.x, e23.y);
         };
         // the lane's four channels of the row in a slot, as the stage input
-        auto row_of = [&](const uint8_t *slot, float2 &v01, float2 &v23) {
+        auto row_of = [&](const uint8_t *hs, int u, float2 &v01, float2 &v23) {
+            const uint8_t *slot = hs + u * XB;  // the X row; centroid rows follow all X rows
             if constexpr (SRC == 0) {
                 const uint2 w = *reinterpret_cast<const uint2 *>(slot + lane * 8);
                 v01 = make_float2(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xFFFF0000u));
@@ -616,13 +682,14 @@ __global__ void __launch_bounds__(256, 2) k_chunk_sums(QPlan p, int t) {
             if (TP == 1) {
                 // one earlier stage: the chain's fl(fl(x - c) + err) is fl(x - c) itself for
                 // every finite result
-                const float4 c = *reinterpret_cast<const float4 *>(slot + XB + lane * 16);
+                const float4 c = *reinterpret_cast<const float4 *>(hs + kBulkGroup * XB + u * 512 + lane * 16);
                 v01 = sub2(v01, make_float2(c.x, c.y));
                 v23 = sub2(v23, make_float2(c.z, c.w));
             } else if (TP != 0) {
                 float v[4] = {v01.x, v01.y, v23.x, v23.y}, er[4] = {0.f, 0.f, 0.f, 0.f};
                 for (int st = 0; st < tp; st++) {
-                    const float4 c = *reinterpret_cast<const float4 *>(slot + XB + st * 512 + lane * 16);
+                    const float4 c = *reinterpret_cast<const float4 *>(hs + kBulkGroup * XB + st * kBulkGroup * 512 +
+                                                                       u * 512 + lane * 16);
                     const float cc[4] = {c.x, c.y, c.z, c.w};
 #pragma unroll
                     for (int r = 0; r < 4; r++) {
@@ -652,7 +719,7 @@ __global__ void __launch_bounds__(256, 2) k_chunk_sums(QPlan p, int t) {
 #pragma unroll
                 for (int u = 0; u < kBulkGroup; u++) {
                     float2 v01, v23;
-                    row_of(gslots + u * row_bytes, v01, v23);
+                    row_of(gslots, u, v01, v23);
                     acc_two_sum2(s01, e01, v01);
                     acc_two_sum2(s23, e23, v23);
                 }
@@ -661,7 +728,7 @@ __global__ void __launch_bounds__(256, 2) k_chunk_sums(QPlan p, int t) {
                 for (int u = 0; u < n_rows; u++) {
                     const int m = g * kBulkGroup + u;
                     float2 v01, v23;
-                    row_of(gslots + u * row_bytes, v01, v23);
+                    row_of(gslots, u, v01, v23);
                     if ((starts >> m) & 1u) {  // warp-uniform
                         stash(m);
                         run_c = __shfl_sync(0xffffffffu, cur.cl, m);
@@ -687,7 +754,8 @@ __global__ void __launch_bounds__(256, 2) k_chunk_sums(QPlan p, int t) {
 }
 
 template <int SRC, int TP>
-static cudaError_t launch_sums(const QPlan &p, int t, int num_sms, cudaStream_t st) {
+static cudaError_t launch_sums(const QPlan &p, const AssignMaps *maps, int t, int num_sms,
+                               cudaStream_t st) {
     const int tp = TP >= 0 ? TP : t - 1;
     const int wpc = bulk_warps(SRC, tp);
     const int smem = 128 + wpc * 2 * kBulkGroup * bulk_row_bytes(SRC, tp);
@@ -705,7 +773,8 @@ static cudaError_t launch_sums(const QPlan &p, int t, int num_sms, cudaStream_t 
     }
     const int64_t need = ((int64_t)p.H * p.nchunk + wpc - 1) / wpc;
     const int grid = (int)std::min<int64_t>(need, (int64_t)per_sm * num_sms);
-    return launch_kernel(k_chunk_sums<SRC, TP>, dim3(grid), dim3(32 * wpc), smem, st, p, t);
+    return launch_kernel(k_chunk_sums<SRC, TP>, dim3(grid), dim3(32 * wpc), smem, st, maps->x_rows,
+                         maps->c_rows, p, t, maps->gather);
 }
 
 // One warp per cluster: the mean from the cluster's own slot, or, for clusters spread over
@@ -773,7 +842,8 @@ __global__ void __launch_bounds__(256) k_cluster_finalize(QPlan p, int t, int pl
     if (lane == 0) p.counts[h * p.C + j] = 0;
 }
 
-cudaError_t launch_cluster_means(const QPlan &p, int t, bool planes, int num_sms, cudaStream_t st) {
+cudaError_t launch_cluster_means(const QPlan &p, const AssignMaps *maps, int t, bool planes,
+                                 int num_sms, cudaStream_t st) {
     const dim3 sgrid((unsigned)p.nsb, p.H);
     cudaError_t e = launch_kernel(k_sort_hist, sgrid, dim3(kSortBlock), 0, st, p, t);
     if (e == cudaSuccess)
@@ -783,11 +853,11 @@ cudaError_t launch_cluster_means(const QPlan &p, int t, bool planes, int num_sms
     auto sums = [&](auto src) {
         constexpr int S = decltype(src)::value;
         switch (t - 1) {
-            case 0: return launch_sums<S, 0>(p, t, num_sms, st);
-            case 1: return launch_sums<S, 1>(p, t, num_sms, st);
-            case 2: return launch_sums<S, 2>(p, t, num_sms, st);
-            case 3: return launch_sums<S, 3>(p, t, num_sms, st);
-            default: return launch_sums<S, -1>(p, t, num_sms, st);
+            case 0: return launch_sums<S, 0>(p, maps, t, num_sms, st);
+            case 1: return launch_sums<S, 1>(p, maps, t, num_sms, st);
+            case 2: return launch_sums<S, 2>(p, maps, t, num_sms, st);
+            case 3: return launch_sums<S, 3>(p, maps, t, num_sms, st);
+            default: return launch_sums<S, -1>(p, maps, t, num_sms, st);
         }
     };
     e = p.in_dtype == DT_F32   ? sums(std::integral_constant<int, 1>())
@@ -806,6 +876,7 @@ cudaError_t launch_cluster_means(const QPlan &p, int t, bool planes, int num_sms
 // grid-stride over tokens, block 256 = 16 tokens x 16 chunks.
 // --------------------------------------------------------------------------------------
 constexpr int kEncTokens = 32;
+constexpr int kEncG = 1;  // tokens per thread whose loads are in flight together
 
 // TT: the number of stages when it is 0..4 (the stage loop unrolled), -1 for any T.
 template <int BITS, int TT>
@@ -820,27 +891,29 @@ __global__ void __launch_bounds__(256) k_encode(QPlan p) {
     const int64_t i1 = min(p.N, i0 + kEncTokens);
     float nanprobe = 0.f;  // becomes NaN if any input is NaN or infinite (x * 0)
     bool bad_index = false;
-    for (int64_t ib = i0; ib < i1; ib += 16) {
+#pragma unroll 1
+    for (int64_t ib = i0; ib < i1; ib += 16 * kEncG) {
         // the loop bound is uniform over the block, so every lane reaches the shuffles;
-        // rows past the end compute on zeros and store nothing
-        const int64_t i = ib + (threadIdx.x >> 4);
-        const bool valid = i < i1;
-        float x[8], s[8], e[8];
-        if (valid) {
-            load_x8(p.X, p.in_dtype, h * p.x_stride + i * kD + c8 * 8, x);
-        } else {
+        // rows past the end compute on zeros and store nothing.  The kEncG tokens of a
+        // thread load together: X, then their cluster indices, then the centroid rows.
+        float sg[kEncG][8], eg[kEncG][8];
 #pragma unroll
-            for (int q = 0; q < 8; q++) x[q] = 0.f;
-        }
+        for (int g = 0; g < kEncG; g++) {
+            const int64_t i = ib + 16 * g + (threadIdx.x >> 4);
+            if (i < i1) {
+                load_x8(p.X, p.in_dtype, h * p.x_stride + i * kD + c8 * 8, sg[g]);
+            } else {
 #pragma unroll
-        for (int q = 0; q < 8; q++) {
-            nanprobe = __fmaf_rn(x[q], 0.f, nanprobe);
-            s[q] = x[q];
-            e[q] = 0.f;
+                for (int q = 0; q < 8; q++) sg[g][q] = 0.f;
+            }
+#pragma unroll
+            for (int q = 0; q < 8; q++) {
+                nanprobe = __fmaf_rn(sg[g][q], 0.f, nanprobe);
+                eg[g][q] = 0.f;
+            }
         }
-        // r = x - C^(1)[pi^(1)] - ... - C^(T)[pi^(T)] rounded once (TwoSum chain); the
-        // cluster indices are loaded first so that their loads overlap
-        auto subtract = [&](int st, int pj) {
+        // r = x - C^(1)[pi^(1)] - ... - C^(T)[pi^(T)] rounded once (TwoSum chain)
+        auto subtract = [&](int g, int st, int pj) {
             if (pj >= p.C) {
                 pj = p.C - 1;
                 bad_index = true;
@@ -851,75 +924,91 @@ __global__ void __launch_bounds__(256) k_encode(QPlan p) {
 #pragma unroll
             for (int q = 0; q < 8; q++) {
                 float err;
-                two_sum(s[q], -c[q], s[q], err);
-                e[q] = __fadd_rn(e[q], err);
+                two_sum(sg[g][q], -c[q], sg[g][q], err);
+                eg[g][q] = __fadd_rn(eg[g][q], err);
             }
         };
-        if (valid) {
-            if constexpr (TT >= 0) {
-                int pjs[TT > 0 ? TT : 1];
+        if constexpr (TT >= 0) {
+            int pjs[kEncG][TT > 0 ? TT : 1];
+#pragma unroll
+            for (int g = 0; g < kEncG; g++) {
+                const int64_t i = ib + 16 * g + (threadIdx.x >> 4);
 #pragma unroll
                 for (int st = 1; st <= TT; st++)
-                    pjs[st - 1] = p.pi[(int64_t)(h * p.T + st - 1) * p.cap + p.tok_off + i];
-#pragma unroll
-                for (int st = 1; st <= TT; st++) subtract(st, pjs[st - 1]);
-            } else {
-                for (int st = 1; st <= T; st++)
-                    subtract(st, p.pi[(int64_t)(h * p.T + st - 1) * p.cap + p.tok_off + i]);
-            }
-        }
-        float r[8], a = 0.f;
-#pragma unroll
-        for (int q = 0; q < 8; q++) {
-            r[q] = __fadd_rn(s[q], e[q]);
-            a = fmaxf(a, fabsf(r[q]));
-        }
-        for (int o = 1; o < lpg; o <<= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
-        const float sc = QMAX == 1 ? a : __fdiv_rn(a, (float)QMAX);  // a / qmax, IEEE
-        const __nv_fp8_storage_t sb = __nv_cvt_float_to_fp8(sc, __NV_SATFINITE, __NV_E4M3);
-        const float sq = __half2float(__half(__nv_cvt_fp8_to_halfraw(sb, __NV_E4M3)));
-        // q = clamp(rne(r / s_q)) with the IEEE quotient.  r times an approximate
-        // reciprocal (a few ulps) gives the same rounding except close to a half-integer;
-        // there the quotient is recomputed with a correctly rounded division.  Adding
-        // 1.5 * 2^23 to the clamped quotient rounds it to an integer (half to even) and
-        // leaves that integer in the low mantissa bits.
-        uint32_t word = 0;
-        if (sq != 0.f) {
-            constexpr float kRound = 12582912.f;  // 1.5 * 2^23
-            float inv;
-            asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(inv) : "f"(sq));
-            float tq[8];
-            uint32_t close = 0;  // elements whose quotient is near a half-integer
-#pragma unroll
-            for (int q = 0; q < 8; q++) {
-                const float v = fminf(fmaxf(__fmul_rn(r[q], inv), (float)-QMAX), (float)QMAX);
-                tq[q] = __fadd_rn(v, kRound);
-                const float d = __fsub_rn(v, __fsub_rn(tq[q], kRound));  // v - rne(v)
-                close |= (fabsf(d) > 0.5f - 0x1p-17f ? 1u : 0u) << q;
-            }
-            if (close) {  // rare
-#pragma unroll 1
-                for (int q = 0; q < 8; q++)
-                    if ((close >> q) & 1u)
-                        tq[q] = __fadd_rn(fminf(fmaxf(__fdiv_rn(r[q], sq), (float)-QMAX), (float)QMAX),
-                                          kRound);
+                    pjs[g][st - 1] = i < i1 ? p.pi[(int64_t)(h * p.T + st - 1) * p.cap + p.tok_off + i] : 0;
             }
 #pragma unroll
-            for (int q = 0; q < 8; q++) {
-                const int qi = (int)(__float_as_uint(tq[q]) - 0x4B400000u);  // rne(v)
-                word |= (uint32_t)(qi + MID) << (q * BITS);
-            }
+            for (int st = 1; st <= TT; st++)
+#pragma unroll
+                for (int g = 0; g < kEncG; g++) subtract(g, st, pjs[g][st - 1]);
         } else {
 #pragma unroll
-            for (int q = 0; q < 8; q++) word |= (uint32_t)MID << (q * BITS);
+            for (int g = 0; g < kEncG; g++) {
+                const int64_t i = ib + 16 * g + (threadIdx.x >> 4);
+                if (i < i1)
+                    for (int st = 1; st <= T; st++)
+                        subtract(g, st, p.pi[(int64_t)(h * p.T + st - 1) * p.cap + p.tok_off + i]);
+            }
         }
-        if (valid) {
-            const int64_t orow = (int64_t)h * p.cap + p.tok_off + i;
-            if constexpr (BITS == 2)
-                *reinterpret_cast<uint16_t *>(p.codes + orow * (kD / 4) + c8 * 2) = (uint16_t)word;
-            else
-                *reinterpret_cast<uint32_t *>(p.codes + orow * (kD / 2) + c8 * 4) = word;
-            if ((c8 & (lpg - 1)) == 0) p.scales[orow * (kD / p.group) + c8 / lpg] = sb;
+#pragma unroll
+        for (int g = 0; g < kEncG; g++) {
+            const int64_t i = ib + 16 * g + (threadIdx.x >> 4);
+            const bool valid = i < i1;
+            const float (&s)[8] = sg[g];
+            const float (&e)[8] = eg[g];
+            float r[8], a = 0.f;
+#pragma unroll
+            for (int q = 0; q < 8; q++) {
+                r[q] = __fadd_rn(s[q], e[q]);
+                a = fmaxf(a, fabsf(r[q]));
+            }
+            for (int o = 1; o < lpg; o <<= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+            const float sc = QMAX == 1 ? a : __fdiv_rn(a, (float)QMAX);  // a / qmax, IEEE
+            const __nv_fp8_storage_t sb = __nv_cvt_float_to_fp8(sc, __NV_SATFINITE, __NV_E4M3);
+            const float sq = __half2float(__half(__nv_cvt_fp8_to_halfraw(sb, __NV_E4M3)));
+            // q = clamp(rne(r / s_q)) with the IEEE quotient.  r times an approximate
+            // reciprocal (a few ulps) gives the same rounding except close to a half-integer;
+            // there the quotient is recomputed with a correctly rounded division.  Adding
+            // 1.5 * 2^23 to the clamped quotient rounds it to an integer (half to even) and
+            // leaves that integer in the low mantissa bits.
+            uint32_t word = 0;
+            if (sq != 0.f) {
+                constexpr float kRound = 12582912.f;  // 1.5 * 2^23
+                float inv;
+                asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(inv) : "f"(sq));
+                float tq[8];
+                uint32_t close = 0;  // elements whose quotient is near a half-integer
+#pragma unroll
+                for (int q = 0; q < 8; q++) {
+                    const float v = fminf(fmaxf(__fmul_rn(r[q], inv), (float)-QMAX), (float)QMAX);
+                    tq[q] = __fadd_rn(v, kRound);
+                    const float d = __fsub_rn(v, __fsub_rn(tq[q], kRound));  // v - rne(v)
+                    close |= (fabsf(d) > 0.5f - 0x1p-17f ? 1u : 0u) << q;
+                }
+                if (close) {  // rare
+#pragma unroll 1
+                    for (int q = 0; q < 8; q++)
+                        if ((close >> q) & 1u)
+                            tq[q] = __fadd_rn(fminf(fmaxf(__fdiv_rn(r[q], sq), (float)-QMAX), (float)QMAX),
+                                              kRound);
+                }
+#pragma unroll
+                for (int q = 0; q < 8; q++) {
+                    const int qi = (int)(__float_as_uint(tq[q]) - 0x4B400000u);  // rne(v)
+                    word |= (uint32_t)(qi + MID) << (q * BITS);
+                }
+            } else {
+#pragma unroll
+                for (int q = 0; q < 8; q++) word |= (uint32_t)MID << (q * BITS);
+            }
+            if (valid) {
+                const int64_t orow = (int64_t)h * p.cap + p.tok_off + i;
+                if constexpr (BITS == 2)
+                    *reinterpret_cast<uint16_t *>(p.codes + orow * (kD / 4) + c8 * 2) = (uint16_t)word;
+                else
+                    *reinterpret_cast<uint32_t *>(p.codes + orow * (kD / 2) + c8 * 4) = word;
+                if ((c8 & (lpg - 1)) == 0) p.scales[orow * (kD / p.group) + c8 / lpg] = sb;
+            }
         }
     }
     if (__any_sync(0xffffffffu, nanprobe != nanprobe) && (threadIdx.x & 31) == 0)

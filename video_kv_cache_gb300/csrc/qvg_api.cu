@@ -134,7 +134,7 @@ qvg_status run_stages(QPlan &p, const AssignMaps *maps, int num_sms, cudaStream_
         for (int it = 1; it <= p.iters && rc == QVG_OK; it++) {
             step(launch_assign(p, maps, t, num_sms, st));
             step(launch_refine(p, t, num_sms, st));
-            step(launch_cluster_means(p, t, it < p.iters, num_sms, st));
+            step(launch_cluster_means(p, maps, t, it < p.iters, num_sms, st));
         }
     }
     return rc;
