@@ -472,7 +472,9 @@ __device__ __forceinline__ void write_centroid(const QPlan &p, int h, int t, int
 // Cluster sums over chunks of 32 cluster-sorted positions.  The rows of each run (same
 // cluster) are added with TwoSum in sorted order.  A run that is a whole cluster leaves its
 // (sum, error) in the cluster's slot; a run that crosses the chunk's start or end leaves it
-// in the chunk's first / last slot.  k_cluster_finalize turns them into means.
+// in the chunk's first / last slot.  k_cluster_finalize turns them into means.  Stage 1
+// (nothing to subtract) fits 64 registers, so four CTAs share an SM; later stages are bound
+// by their shared-memory row slots to two.
 //
 // The summed rows are the stage input R^(t-1): X itself at stage 1, later a residual that
 // is not stored but rebuilt here from X and the earlier stages' centroid rows (L2-resident)
@@ -515,7 +517,7 @@ struct SumChunk {
 };
 
 template <int SRC, int TP>  // SRC: X dtype (0 bf16, 1 fp32, 3 fp16); TP: t - 1 (0..3), or -1
-__global__ void __launch_bounds__(256, 2)
+__global__ void __launch_bounds__(256, TP == 0 ? 4 : 2)
     k_chunk_sums(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmC,
                  QPlan p, int t, int gather) {
     pdl_begin();
