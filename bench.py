@@ -167,8 +167,8 @@ def launches_per_step(w):
 
 # DRAM traffic of one k_assign launch on layer_1p3b_32760 (dram__bytes_read.sum +
 # dram__bytes_write.sum, ncu), valid while the kernel's sources hash to `sources_sha256`.
-ASSIGN_TRAFFIC = {"workload": "layer_1p3b_32760", "bytes": 219088640,
-                  "sources_sha256": "3ae3c515f29fd1d66a028661c1caae99da8aac337caa96c4c3224039dd8f554c"}
+ASSIGN_TRAFFIC = {"workload": "layer_1p3b_32760", "bytes": 216960768,
+                  "sources_sha256": "6a3c22ffc8983c0e433f87bbf1b487b6b3fe288143b7f20e3c6804c7237160c2"}
 ASSIGN_SOURCES = ("video_kv_cache_gb300/csrc/k_assign.cu", "video_kv_cache_gb300/csrc/internal.cuh")
 
 
