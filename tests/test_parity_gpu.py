@@ -290,6 +290,26 @@ def test_strided_input_and_token_offset():
     assert torch.equal(cache.centroids, ref.centroids)
 
 
+def test_tensor_stride_off_the_row_grid_gives_the_same_bits():
+    # A tensor stride that is not a whole number of 128-channel rows: the cluster sums
+    # cannot address X as one [rows][128] view for their TMA row gathers and copy row by
+    # row instead.  Both ways add the same values in the same order, so the results must
+    # be the bits of the contiguous case.  T = 2 covers both stages' sums (the second one
+    # also fetches the earlier stage's centroid rows).
+    for dtype in (torch.bfloat16, torch.float32):
+        X = _make(14, 3, 2, 18, 30, dtype)  # N = 1080
+        H, N, _ = X.shape
+        stride = N * 128 + 64  # 64 channels past a row boundary; 16-byte aligned
+        flat = torch.zeros(H * stride, dtype=X.dtype, device="cuda")
+        view = flat.as_strided((H, N, 128), (stride, 128, 1))
+        view.copy_(X.cuda())
+        args = (24, 2, 2, 32, 3, 6)
+        got = _to_np(_gpu_quantize(view, *args))
+        ref = _to_np(_gpu_quantize(X, *args))
+        for k in ("codes", "scales", "pi", "centroids"):
+            np.testing.assert_array_equal(got[k], ref[k], err_msg=k)
+
+
 def test_graph_capture_replays_identical_results():
     # qvg_quantize / qvg_dequantize enqueue only kernels and memsets on the given stream,
     # so a caller may capture them in a CUDA graph; the replay must give the same bits

@@ -790,13 +790,14 @@ __global__ void __launch_bounds__(256) k_cluster_finalize(QPlan p, int t, int pl
     const int j = blockIdx.x * 8 + (threadIdx.x >> 5);
     const int h = blockIdx.y;
     if (j >= p.C) return;
+    // the total and the offset load together (the offset is unused for an empty cluster)
     const int cnt = p.counts[h * p.C + j];
+    const int off = p.offs[h * p.C + j];
     const float4 mu = *reinterpret_cast<const float4 *>(p.mu + h * kD + 4 * lane);
     if (cnt == 0) {
         write_centroid(p, h, t, j, lane, false, make_float4(0.f, 0.f, 0.f, 0.f), planes != 0, mu);
         return;
     }
-    const int off = p.offs[h * p.C + j];
     const int a = off / kChunk, b = (off + cnt - 1) / kChunk;
     float S[4] = {0.f, 0.f, 0.f, 0.f}, E[4] = {0.f, 0.f, 0.f, 0.f};
     if (a == b) {
