@@ -167,8 +167,8 @@ def launches_per_step(w):
 
 # DRAM traffic of one k_assign launch on layer_1p3b_32760 (dram__bytes_read.sum +
 # dram__bytes_write.sum, ncu), valid while the kernel's sources hash to `sources_sha256`.
-ASSIGN_TRAFFIC = {"workload": "layer_1p3b_32760", "bytes": 216960768,
-                  "sources_sha256": "6a3c22ffc8983c0e433f87bbf1b487b6b3fe288143b7f20e3c6804c7237160c2"}
+ASSIGN_TRAFFIC = {"workload": "layer_1p3b_32760", "bytes": 217287424,
+                  "sources_sha256": "c7452dea8b04f946143f0b693819807e7a6206572fceb2689d175127965c9447"}
 ASSIGN_SOURCES = ("video_kv_cache_gb300/csrc/k_assign.cu", "video_kv_cache_gb300/csrc/internal.cuh")
 
 

@@ -460,16 +460,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     return w;
                 };
-                int n_cand = 0, bj = 0;
-                bool found = false;
-#pragma unroll
-                for (int c = 0; c < 8; c++) {
-                    const uint32_t w = word_of(c);
-                    n_cand += __popc(w);
-                    if (!found && w) {
-                        bj = c * 32 + __ffs(w) - 1;
-                        found = true;
-                    }
+                // words past a half's chunks are zero, so the count and the lowest candidate
+                // need no chunk mapping: the lower half's chunks come first
+                const int n_cand = __popc(cand0) + __popc(cand1) + __popc(cand2) + __popc(cand3) +
+                                   __popc(up.x) + __popc(up.y) + __popc(up.z) + __popc(up.w);
+                int bj;
+                if (cand0 | cand1 | cand2 | cand3) {
+                    const int c = cand0 ? 0 : cand1 ? 1 : cand2 ? 2 : 3;
+                    const uint32_t w = cand0 ? cand0 : cand1 ? cand1 : cand2 ? cand2 : cand3;
+                    bj = c * 32 + __ffs(w) - 1;
+                } else {
+                    const int k = up.x ? 0 : up.y ? 1 : up.z ? 2 : 3;
+                    const uint32_t w = up.x ? up.x : up.y ? up.y : up.z ? up.z : up.w;
+                    bj = (split + k) * 32 + __ffs(w) - 1;
                 }
                 const bool need = valid && n_cand > 1;
                 const unsigned m = __ballot_sync(0xffffffffu, need);
