@@ -67,7 +67,7 @@ struct QPlan {
     float *psum;           // [H][nchunk][2][2][128] (sum, error) of the runs that cross a
                            // chunk boundary: [0] the run at the chunk start, [1] the last run
     float *wsum;           // [H][C][2][128] (sum, error) of clusters inside one chunk
-    int nsb, nchunk;       // token blocks of the sort, 64-position chunks per tensor
+    int nsb, nchunk;       // token blocks of the sort, 32-position chunks per tensor
     int *init_idx;         // [H][T][C] cold-start rows
     unsigned *stats;       // [16] counters (see kStat*)
     int *rq_count;         // number of queued near-tie re-scoring requests

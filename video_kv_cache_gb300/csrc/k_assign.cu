@@ -39,10 +39,12 @@
 //   warp 1   TMEM allocator and MMA issuer (one thread): 2 x kBPlanes x 4 tcgen05.mma of
 //            M=128, N=Cpad, K=16 per tile into one of two TMEM accumulators.
 //   warps 2-17 epilogue, two groups of 8 warps taking alternate tiles: a warp reads 32
-//            TMEM lanes (one token row per thread) and half of the columns; the pair of
-//            warps on the same rows merges its best / second-best scores, re-reads only
-//            the 32-column chunks that can hold a near tie, releases the accumulator,
-//            writes pi and queues near ties for k_refine.
+//            TMEM lanes (one token row per thread) and half of the columns.  Pass A takes
+//            each 32-column chunk's minimum score; the pair of warps on the same rows
+//            exchanges them for the row's best, which fixes the near-tie margin.  Pass B
+//            re-reads the chunks that can hold a score within the margin and sets one
+//            candidate bit per score.  Then the accumulator is released; a row with one
+//            candidate gets it as pi, a row with several is queued for k_refine.
 // Every mbarrier wait is bounded; on timeout the kernel sets QVG_DEV_TIMEOUT, stops, waits
 // for its own copies and MMAs, frees TMEM and returns.
 #include <cuda.h>
