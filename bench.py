@@ -450,6 +450,75 @@ def run_sweep(args):
                       "data": "synthetic", "rows": rows}), flush=True)
 
 
+def run_presets(args):
+    """The two named settings on the 1.3B layer's tensors: quantize and dequantize time
+    (CUDA events, inputs resident, L2 flushed before each repetition), the mean squared
+    reconstruction error of K and V and its reduction against plain group quantization at
+    the same (bits, group), and the storage accounting: the compression ratio and the codes'
+    share with the fp32 centroids this library stores, and with 16-bit centroids as the
+    pages count them."""
+    from video_kv_cache_gb300 import api, qvg
+    from video_kv_cache_gb300 import build as qbuild
+    from video_kv_cache_gb300.presets import PRESETS, cache_bytes, storage_bits
+    torch.cuda.set_device(0)
+    qbuild.build()
+    qvg.load()
+    w = synth.workload(DEFAULT_WORKLOAD)
+    dev = torch.device("cuda")
+    X = w.make(dev)
+    H, N = X.shape[:2]
+    Xf = X.float()
+    is_v = torch.tensor([t % 2 == 1 for t in w.tids], device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    st = torch.cuda.current_stream()
+
+    def mse(xh):
+        e = ((xh - Xf) ** 2).mean(dim=(1, 2))
+        return float(e[~is_v].mean()), float(e[is_v].mean())
+
+    rows = []
+    for name, pr in PRESETS.items():
+        out = api.allocate(H, N, pr.C, pr.T, pr.bits, pr.group, device=dev)
+        ws = api.new_workspace(H, N, pr.C, pr.T, dev)
+        xh = torch.empty((H, N, 128), dtype=torch.float32, device=dev)
+
+        def quantize(T=pr.T, o=out, wsp=ws):
+            api.quantize(X, pr.C, T, pr.bits, pr.group, w.iters, w.seed, out=o, workspace=wsp,
+                         status=status)
+
+        def dequantize(o=out):
+            api.dequantize(o, N, torch.float32, out=xh, status=status)
+
+        quantize()
+        dequantize()
+        torch.cuda.synchronize()
+        q_ms = _event_ms(st, quantize, max(2, args.steps // 2), flush)
+        d_ms = _event_ms(st, dequantize, max(2, args.steps // 2), flush)
+        mk, mv = mse(xh)
+        base = api.allocate(H, N, pr.C, 0, pr.bits, pr.group, device=dev)
+        api.quantize(X, pr.C, 0, pr.bits, pr.group, w.iters, w.seed, out=base, workspace=ws,
+                     status=status)
+        bk, bv = mse(api.dequantize(base, N, torch.float32, status=status))
+        acc32 = storage_bits(pr.bits, pr.group, pr.T, pr.C, N, centroid_bits=32)
+        acc16 = storage_bits(pr.bits, pr.group, pr.T, pr.C, N, centroid_bits=16)
+        rows.append({
+            "preset": name, "C": pr.C, "T": pr.T, "bits": pr.bits, "group": pr.group,
+            "quantize_ms": q_ms, "quantize_mtokens_s": H * N / (q_ms * 1e-3) / 1e6,
+            "dequant_ms": d_ms, "mse_k": mk, "mse_v": mv,
+            "reduction_k": bk / mk if mk > 0 else None, "reduction_v": bv / mv if mv > 0 else None,
+            "cache_bytes": cache_bytes(out, N),
+            "compression_ratio_fp32_centroids": acc32["compression_ratio"],
+            "codes_share_fp32_centroids": acc32["codes_share"],
+            "compression_ratio_16bit_centroids": acc16["compression_ratio"],
+            "codes_share_16bit_centroids": acc16["codes_share"]})
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0, "device status %#x" % int(status.item())
+    print(json.dumps({"metric": "presets: quantize time, MSE reduction, compression ratio",
+                      "workload": w.name, "tensors": H, "tokens": N, "iters": w.iters,
+                      "data": "synthetic", "rows": rows}), flush=True)
+
+
 def run_stream(args):
     """The streaming workload: 60 chunks of 3 frames x 30x52 tokens appended to the caches
     of 30 layers x 12 heads x K/V (720 tensors).  Chunk 0 is clustered from a cold start,
@@ -564,12 +633,16 @@ def main():
                     help="print the precision sweep (MSE reduction) instead of the timing line")
     ap.add_argument("--stream", action="store_true",
                     help="run the 60-chunk streaming workload and print its line")
+    ap.add_argument("--presets", action="store_true",
+                    help="report the two named settings (time, MSE reduction, compression)")
     args = ap.parse_args()
     w = synth.workload(args.workload)
     if args.sweep:
         run_sweep(args)
     elif args.stream:
         run_stream(args)
+    elif args.presets:
+        run_presets(args)
     elif args.impl == "reference":
         run_reference(args, w)
     else:
