@@ -338,21 +338,60 @@ def run_ours(args, w):
     torch.cuda.synchronize()
     assert int(status.item()) == 0, "device status %#x" % int(status.item())
 
-    # --- end to end through the same API with host buffers (pinned), copies timed
+    # --- end to end through the same API with host buffers (pinned), copies timed.  Each
+    # step uploads its X, compresses and reconstructs it and downloads the compressed cache.
+    # As a streaming caller would, the steps overlap: step k+1's upload and step k-1's
+    # download run on their own streams while step k computes.  Inputs and outputs are
+    # double-buffered on the device, so a buffer is reused only after the step that read
+    # or wrote it.  The timed region spans all K steps, from the first upload to the last
+    # download; the inputs (larger than L2) stand in for the flush.
     Xh = X.cpu().pin_memory()
-    cache_h = {k: torch.empty(getattr(out, k).shape, dtype=getattr(out, k).dtype,
-                              pin_memory=True) for k in ("codes", "scales", "pi", "centroids")}
+    Xb = [X, torch.empty_like(X)]
+    outs = [out, api.allocate(H, N, w.C, w.T, w.bits, w.group, device=dev)]
+    cache_h = [{k: torch.empty(getattr(out, k).shape, dtype=getattr(out, k).dtype,
+                               pin_memory=True) for k in ("codes", "scales", "pi", "centroids")}
+               for _ in range(2)]
     h2d = Xh.numel() * Xh.element_size()
-    d2h = sum(t.numel() * t.element_size() for t in cache_h.values())
+    d2h = sum(t.numel() * t.element_size() for t in cache_h[0].values())
+    up, down = torch.cuda.Stream(), torch.cuda.Stream()
 
-    def e2e_step():
-        X.copy_(Xh, non_blocking=True)
-        quantize()
-        dequantize()
-        for key, t in cache_h.items():
-            t.copy_(getattr(out, key), non_blocking=True)
+    def e2e_run(K):
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        up_ev = [torch.cuda.Event() for _ in range(K)]
+        done_ev = [torch.cuda.Event() for _ in range(K)]
+        down_ev = [torch.cuda.Event() for _ in range(K)]
+        torch.cuda.synchronize()
+        start.record(st)
+        up.wait_event(start)
+        for k in range(K):
+            b = k & 1
+            with torch.cuda.stream(up):
+                if k >= 2:
+                    up.wait_event(done_ev[k - 2])  # the last reader of this input buffer
+                Xb[b].copy_(Xh, non_blocking=True)
+                up_ev[k].record(up)
+            st.wait_event(up_ev[k])
+            if k >= 2:
+                st.wait_event(down_ev[k - 2])  # this output buffer has been downloaded
+            api.quantize(Xb[b], w.C, w.T, w.bits, w.group, w.iters, w.seed, out=outs[b],
+                         workspace=ws, status=status, tensor_id_base=lo)
+            api.dequantize(outs[b], N, torch.bfloat16, out=xhat, status=status)
+            done_ev[k].record(st)
+            with torch.cuda.stream(down):
+                down.wait_event(done_ev[k])
+                for key, t in cache_h[b].items():
+                    t.copy_(getattr(outs[b], key), non_blocking=True)
+                down_ev[k].record(down)
+        st.wait_event(down_ev[K - 1])
+        end.record(st)
+        torch.cuda.synchronize()
+        return start.elapsed_time(end) / K
 
-    e2e_ms = _max_over_ranks(_event_ms(st, e2e_step, max(2, args.steps // 2), flush), world)
+    e2e_run(2)  # warm-up of the second buffer set
+    e2e_ms = _max_over_ranks(e2e_run(max(3, args.steps)), world)
+    assert int(status.item()) == 0, "device status %#x" % int(status.item())
+    # every step compresses the same X, so each downloaded cache holds the device's bits
+    assert all(torch.equal(cache_h[b]["pi"], outs[b].pi.cpu()) for b in range(2))
 
     hbm, tf_burst, tf_sus, src = _peaks()
     dq_gbs = dequant_bytes(H, N, w.C, w.T, w.bits, w.group) / (d_ms * 1e-3) / 1e9
@@ -383,7 +422,9 @@ def run_ours(args, w):
                         "bytes": dequant_bytes(H, N, w.C, w.T, w.bits, w.group),
                         "peak_gbs": hbm, "peak_source": src},
             "e2e": {"value": tokens_all / (e2e_ms * 1e-3) / 1e6, "unit": "Mtokens/s",
-                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms": e2e_ms},
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms": e2e_ms,
+                    "calls": "direct API calls, pinned host buffers",
+                    "overlap": "step k+1's upload and step k-1's download overlap step k"},
             "gpu_launches": args.steps * launches_per_step(w),
             "wall_s_timed_region": wall,
             "clocks": clocks.summary(epoch0, epoch1),
