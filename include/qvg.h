@@ -31,6 +31,13 @@
  *     is enqueued asynchronously; a call returns once it is enqueued.  qvg_quantize,
  *     qvg_reassign and qvg_dequantize enqueue only kernels and memsets on `stream`, so a
  *     caller may capture them in a CUDA graph and replay it with the same buffers.
+ *   - The kernels are launched with programmatic dependent launch: each one may become
+ *     resident before the previous kernel on `stream` has finished, and waits for it
+ *     (griddepcontrol.wait) before touching memory, so the order of memory effects is plain
+ *     stream order.  Each also lets its dependents launch early.  A kernel the caller
+ *     launches next with programmatic serialisation allowed must itself wait
+ *     (griddepcontrol.wait) before reading the results; one launched without it needs
+ *     nothing.
  *   - Argument errors are detected on the host before anything is enqueued and returned as
  *     QVG_ERR_INVALID_ARG / QVG_ERR_UNSUPPORTED / QVG_ERR_WORKSPACE.  A CUDA error reported
  *     while enqueuing returns QVG_ERR_CUDA; work already enqueued may have run.
