@@ -72,16 +72,19 @@ def _load():
         lib.orc_lloyd.restype = None
         lib.orc_lloyd.argtypes = [_f64p, c.c_int64, c.c_int, c.c_int, c.c_int, _f32p, _i32p]
         lib.orc_encode.restype = None
-        lib.orc_encode.argtypes = [_f64p, c.c_int64, c.c_int, c.c_int, c.c_int, _u8p, _u8p]
+        lib.orc_encode.argtypes = [_f64p, c.c_int64, c.c_int, c.c_int, c.c_int, c.c_int, _u8p,
+                                   _u8p]
         lib.orc_decode_codes.restype = None
-        lib.orc_decode_codes.argtypes = [_u8p, _u8p, c.c_int64, c.c_int, c.c_int, c.c_int, _f64p]
+        lib.orc_decode_codes.argtypes = [_u8p, _u8p, c.c_int64, c.c_int, c.c_int, c.c_int,
+                                         c.c_int, _f64p]
         lib.orc_dequantize.restype = None
         lib.orc_dequantize.argtypes = [_u8p, _u8p, _u8p, _f32p, c.c_int64, c.c_int, c.c_int,
-                                       c.c_int, c.c_int, c.c_int, _f64p]
+                                       c.c_int, c.c_int, c.c_int, c.c_int, _f64p]
         lib.orc_quantize.restype = c.c_int
         lib.orc_quantize.argtypes = [c.c_int64, c.c_int64, c.c_int, c.c_int, c.c_int, c.c_int,
                                      c.c_int, c.c_int, c.c_uint64, c.c_int64, _f64p,
-                                     c.c_void_p, _u8p, _u8p, _u8p, _f32p, _f64p, c.c_int]
+                                     c.c_void_p, _u8p, _u8p, _u8p, _f32p, _f64p, c.c_int,
+                                     c.c_int]
         lib.orc_num_cores.restype = c.c_int
         lib.orc_num_cores.argtypes = []
         _lib = lib
@@ -186,26 +189,27 @@ def lloyd(R, cent, iters: int):
     return out, pi
 
 
-def encode(R, bits: int, group: int):
-    """Q(R): (codes uint8 [N][d*bits/8], E4M3 scale bytes uint8 [N][d/group])."""
+def encode(R, bits: int, group: int, scheme: int = 0):
+    """Q(R): (codes uint8 [N][d*bits/8], E4M3 scale bytes uint8 [N][d/group]).
+    scheme 0: symmetric restricted grid; 1: mid-rise (levels at half-integers)."""
     R, N, d = _rows(R)
     codes = np.zeros((N, d * bits // 8), dtype=np.uint8)
     scales = np.zeros((N, d // group), dtype=np.uint8)
-    _load().orc_encode(R, N, d, bits, group, codes, scales)
+    _load().orc_encode(R, N, d, bits, group, scheme, codes, scales)
     return codes, scales
 
 
-def decode_codes(codes, scales, bits: int, group: int) -> np.ndarray:
+def decode_codes(codes, scales, bits: int, group: int, scheme: int = 0) -> np.ndarray:
     codes = np.ascontiguousarray(codes, dtype=np.uint8)
     scales = np.ascontiguousarray(scales, dtype=np.uint8)
     N = codes.shape[0]
     d = codes.shape[1] * 8 // bits
     out = np.zeros((N, d), dtype=np.float64)
-    _load().orc_decode_codes(codes, scales, N, d, bits, group, out)
+    _load().orc_decode_codes(codes, scales, N, d, bits, group, scheme, out)
     return out
 
 
-def dequantize(codes, scales, pi, cent, bits: int, group: int) -> np.ndarray:
+def dequantize(codes, scales, pi, cent, bits: int, group: int, scheme: int = 0) -> np.ndarray:
     """One tensor: codes [N][d*b/8], scales [N][d/B], pi [T][N] uint8, cent [T][C][d]."""
     codes = np.ascontiguousarray(codes, dtype=np.uint8)
     scales = np.ascontiguousarray(scales, dtype=np.uint8)
@@ -219,12 +223,12 @@ def dequantize(codes, scales, pi, cent, bits: int, group: int) -> np.ndarray:
         cent = np.zeros((1, 1, d), dtype=np.float32)
         pi = np.zeros((1, N), dtype=np.uint8)
     out = np.zeros((N, d), dtype=np.float64)
-    _load().orc_dequantize(codes, scales, pi, cent, N, d, C, T, bits, group, out)
+    _load().orc_dequantize(codes, scales, pi, cent, N, d, C, T, bits, group, scheme, out)
     return out
 
 
 def quantize(X, C: int, T: int, bits: int, group: int, iters: int, seed: int,
-             tensor_id_base: int = 0, warm=None, nthreads: int = 0) -> dict:
+             tensor_id_base: int = 0, warm=None, nthreads: int = 0, scheme: int = 0) -> dict:
     """The whole quantize path over a batch X [H][N][d] (float64, already decoded).
 
     Returns codes [H][N][d*b/8], scales [H][N][d/B], pi [H][T][N] (uint8),
@@ -246,7 +250,7 @@ def quantize(X, C: int, T: int, bits: int, group: int, iters: int, seed: int,
         warm_ptr = warm_arr.ctypes.data
     rc = _load().orc_quantize(H, N, d, Ce, T, bits, group, iters, seed & (2**64 - 1),
                               tensor_id_base, X, warm_ptr, codes, scales, pi, cent, J,
-                              nthreads)
+                              nthreads, scheme)
     if rc != 0:
         raise ValueError("orc_quantize rejected the arguments (%d)" % rc)
     return {"codes": codes, "scales": scales, "pi": pi[:, :T], "centroids": cent[:, :T],

@@ -40,6 +40,12 @@
  *     scale is E4M3(s), rounded to nearest even and saturated to +-448; q is r / s_q
  *     rounded half-to-even and clamped; the stored code is u = q + 2^(b-1).  When
  *     s_q == 0 every code is 2^(b-1).
+ *   - Scheme 1 (mid-rise, the reading of a critique's "only 4 quantization levels" at 2
+ *     bits): the 2^b levels sit at half-integers, x = s_q * (u - 2^(b-1) + 1/2) for
+ *     u = 0 .. 2^b - 1.  s = max|r| / (2^(b-1) - 1/2), so the largest |r| maps to the
+ *     outermost level; u = floor(r / s_q) + 2^(b-1), clamped to [0, 2^b - 1], the nearest
+ *     level (a value exactly between two levels takes the upper one).  When s_q == 0 every
+ *     code is 2^(b-1).
  *   - Codes are packed little-endian inside a byte: channel k sits at bit (k*b) mod 8 of
  *     byte (k*b)/8 of its token's row.
  *
@@ -207,9 +213,11 @@ void orc_lloyd(const double *R, int64_t N, int d, int C, int iters, float *cent,
 /* Q(.) of the final residual [review/pipeline], [notes/co-design], [explainer/steps].    */
 /* ------------------------------------------------------------------------------------ */
 
-void orc_encode(const double *R, int64_t N, int d, int bits, int group, uint8_t *codes,
-                uint8_t *scales) {
+void orc_encode(const double *R, int64_t N, int d, int bits, int group, int scheme,
+                uint8_t *codes, uint8_t *scales) {
     const int qmax = (1 << (bits - 1)) - 1, mid = 1 << (bits - 1);
+    /* the outermost level: qmax for the symmetric grid, 2^(b-1) - 1/2 for mid-rise */
+    const double top = scheme == 1 ? (double)mid - 0.5 : (double)qmax;
     const int row_bytes = d * bits / 8, ngroups = d / group;
     memset(codes, 0, (size_t)N * row_bytes);
     for (int64_t i = 0; i < N; i++) {
@@ -218,12 +226,17 @@ void orc_encode(const double *R, int64_t N, int d, int bits, int group, uint8_t 
             double a = 0.0;
             for (int k = g * group; k < (g + 1) * group; k++)
                 if (fabs(r[k]) > a) a = fabs(r[k]);
-            uint8_t sb = orc_e4m3_encode(a / (double)qmax);
+            uint8_t sb = orc_e4m3_encode(a / top);
             double sq = orc_e4m3_decode(sb);
             scales[i * ngroups + g] = sb;
             for (int k = g * group; k < (g + 1) * group; k++) {
                 int u = mid;
-                if (sq != 0.0) {
+                if (sq != 0.0 && scheme == 1) {
+                    double f = floor(r[k] / sq) + mid;
+                    if (f > 2 * mid - 1) f = 2 * mid - 1;
+                    if (f < 0) f = 0;
+                    u = (int)f;
+                } else if (sq != 0.0) {
                     double q = nearbyint(r[k] / sq); /* default rounding: half to even */
                     if (q > qmax) q = qmax;
                     if (q < -qmax) q = -qmax;
@@ -237,13 +250,14 @@ void orc_encode(const double *R, int64_t N, int d, int bits, int group, uint8_t 
 
 /* deQ(X_INT, S_x) in fp64. */
 void orc_decode_codes(const uint8_t *codes, const uint8_t *scales, int64_t N, int d, int bits,
-                      int group, double *out) {
+                      int group, int scheme, double *out) {
     const int mid = 1 << (bits - 1), row_bytes = d * bits / 8, ngroups = d / group;
+    const double off = scheme == 1 ? 0.5 : 0.0;
     for (int64_t i = 0; i < N; i++)
         for (int k = 0; k < d; k++) {
             int u = (codes[i * row_bytes + (k * bits) / 8] >> ((k * bits) % 8)) & ((1 << bits) - 1);
             double sq = orc_e4m3_decode(scales[i * ngroups + k / group]);
-            out[i * d + k] = sq * (double)(u - mid);
+            out[i * d + k] = sq * ((double)(u - mid) + off);
         }
 }
 
@@ -251,8 +265,8 @@ void orc_decode_codes(const uint8_t *codes, const uint8_t *scales, int64_t N, in
  * [review/pipeline], [notes/PRQ].  pi is [T][N], cent is [T][C][d]. */
 void orc_dequantize(const uint8_t *codes, const uint8_t *scales, const uint8_t *pi,
                     const float *cent, int64_t N, int d, int C, int T, int bits, int group,
-                    double *out) {
-    orc_decode_codes(codes, scales, N, d, bits, group, out);
+                    int scheme, double *out) {
+    orc_decode_codes(codes, scales, N, d, bits, group, scheme, out);
     for (int t = T; t >= 1; t--) {
         const uint8_t *p = pi + (int64_t)(t - 1) * N;
         const float *c = cent + (int64_t)(t - 1) * C * d;
@@ -269,6 +283,7 @@ typedef struct {
     int64_t N;
     int d, C, T, bits, group, iters;
     uint64_t seed;
+    int scheme; /* 0: symmetric restricted grid, 1: mid-rise */
 } orc_cfg;
 
 /* X [N][d] fp64 (decoded input); warm [T][C][d] or NULL; outputs codes [N][d*bits/8],
@@ -304,7 +319,7 @@ int orc_quantize_tensor(const orc_cfg *cfg, int64_t tensor_id, const double *X,
         for (int64_t i = 0; i < N; i++) pi[(int64_t)(t - 1) * N + i] = (uint8_t)p[i];
         orc_subtract(R, N, d, p, c); /* R^(t) */
     }
-    orc_encode(R, N, d, cfg->bits, cfg->group, codes, scales);
+    orc_encode(R, N, d, cfg->bits, cfg->group, cfg->scheme, codes, scales);
     if (Rfin) memcpy(Rfin, R, (size_t)N * d * sizeof(double));
     free(R), free(p), free(idx);
     return 0;
@@ -349,11 +364,12 @@ int orc_num_cores(void) {
 int orc_quantize(int64_t H, int64_t N, int d, int C, int T, int bits, int group, int iters,
                  uint64_t seed, int64_t tensor_id_base, const double *X, const float *warm,
                  uint8_t *codes, uint8_t *scales, uint8_t *pi, float *cent, double *J,
-                 int nthreads) {
+                 int nthreads, int scheme) {
     if (H < 0 || N < 1 || d < 1 || T < 0 || iters < 1) return -1;
     if (T > 0 && (C < 1 || C > 256 || C > N)) return -1;
     if ((bits != 2 && bits != 4) || group < 1 || d % group != 0 || (d * bits) % 8 != 0) return -1;
-    orc_cfg cfg = {N, d, C, T, bits, group, iters, seed};
+    if (scheme != 0 && scheme != 1) return -1;
+    orc_cfg cfg = {N, d, C, T, bits, group, iters, seed, scheme};
     if (nthreads <= 0) nthreads = orc_num_cores();
     if (nthreads > H) nthreads = (int)(H > 0 ? H : 1);
     orc_job *jobs = (orc_job *)calloc((size_t)nthreads, sizeof(orc_job));
