@@ -78,6 +78,17 @@ typedef enum {
 typedef enum { QVG_F16 = 0, QVG_BF16 = 1, QVG_F32 = 2 } qvg_dtype;
 
 /* Parameters of one qvg_quantize call: n_tensors independent tensors of N tokens each. */
+/* Integer grid of the codes.
+ *   QVG_QSCHEME_SYMMETRIC: q in [-qmax, qmax], qmax = 2^(bits-1) - 1 (INT2 is ternary);
+ *     s = max|r| / qmax; q = r / s_q rounded half to even and clamped; u = q + 2^(bits-1);
+ *     x = s_q * (u - 2^(bits-1)).
+ *   QVG_QSCHEME_MIDRISE: the 2^bits levels sit at half-integers (4 levels at INT2, the
+ *     reading of one critique page of the method); s = max|r| / (2^(bits-1) - 1/2);
+ *     u = floor(r / s_q) + 2^(bits-1) clamped to [0, 2^bits - 1] (a value exactly between
+ *     two levels takes the upper one); x = s_q * (u - 2^(bits-1) + 1/2).
+ * Either way s_q = E4M3(s) and s_q = 0 stores every code as 2^(bits-1). */
+typedef enum { QVG_QSCHEME_SYMMETRIC = 0, QVG_QSCHEME_MIDRISE = 1 } qvg_qscheme;
+
 typedef struct {
     int32_t n_tensors;      /* H >= 1: independent (layer, head, K/V) tensors in this call */
     int32_t d;              /* channels per token; must be 128 */
@@ -97,6 +108,7 @@ typedef struct {
     int32_t n_tables;       /* centroid-table slots per tensor (0 = 1) */
     int64_t warm_stride;    /* floats between consecutive tensors of warm_centroids
                                (0 = T*C*d) */
+    int32_t qscheme;        /* qvg_qscheme of the codes (zero-initialised = symmetric) */
 } qvg_quant_params;
 
 /* The compressed cache.  Layouts (all row-major, caller-owned device memory):
@@ -197,10 +209,12 @@ typedef struct {
     int64_t token_capacity; /* token slots per tensor in codes / scales / pi (0 = N) */
     int32_t n_tables;       /* centroid-table slots per tensor (0 = 1) */
     int64_t out_stride;     /* elements between consecutive tensors of X_hat (0 = N*d) */
+    int32_t qscheme;        /* qvg_qscheme the codes were written with */
 } qvg_dequant_params;
 
-/* Reconstruct X_hat[h][i] = s_q * (u - 2^(bits-1)) + C^(T)[pi^(T)_i] + ... + C^(1)[pi^(1)_i],
- * added in that order (stage T first) in fp32 registers, rounded once to out_dtype. */
+/* Reconstruct X_hat[h][i] = x(u) + C^(T)[pi^(T)_i] + ... + C^(1)[pi^(1)_i], x(u) the level
+ * of the code's scheme, added in that order (stage T first) in fp32 registers, rounded
+ * once to out_dtype. */
 qvg_status qvg_dequantize(const qvg_dequant_params *params, const qvg_buffers *in,
                           void *X_hat, uint32_t *dev_status, void *stream);
 

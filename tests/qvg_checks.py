@@ -3,7 +3,8 @@
 Tolerances (derived from the arithmetic; see the design notes for the derivations):
   * codes and E4M3 scales, given the same assignments and centroids: bit-exact, except
     groups whose exact scale max|r|/qmax lies within 2^-20 (relative) of an E4M3 rounding
-    midpoint and elements whose exact r/s_q lies within 2^-20 (relative) of a half-integer.
+    midpoint and elements whose exact r/s_q lies within 2^-20 (relative) of a half-integer
+    (of an integer for the mid-rise grid, whose codes change there).
     The GPU forms r as the fp32 value nearest the exact residual and divides in IEEE fp32,
     so it can only differ from the fp64 oracle inside those bands.  Band cases are counted.
   * centroids, given the same assignments: |C_gpu - C_exact| <= ulp32(C_exact) +
@@ -38,14 +39,17 @@ def unpack_codes(codes, bits):
     return u.reshape(*codes.shape[:-1], codes.shape[-1] * per).astype(np.int64)
 
 
-def compare_codes(R, codes_gpu, scales_gpu, bits, group, eps=2.0 ** -20):
-    """R: exact final residual [N][d] (fp64).  Returns counts; raises on a real mismatch."""
+def compare_codes(R, codes_gpu, scales_gpu, bits, group, eps=2.0 ** -20, scheme=0):
+    """R: exact final residual [N][d] (fp64).  Returns counts; raises on a real mismatch.
+    scheme 0: symmetric grid (codes change at half-integers of r/s_q); scheme 1: mid-rise
+    (codes change at integers)."""
     qmax = (1 << (bits - 1)) - 1
+    top = (1 << (bits - 1)) - 0.5 if scheme == 1 else qmax
     N, d = R.shape
     ng = d // group
-    codes_o, scales_o = oracle.encode(R, bits, group)
+    codes_o, scales_o = oracle.encode(R, bits, group, scheme)
     a = np.abs(R.reshape(N, ng, group)).max(axis=2)
-    s = a / qmax
+    s = a / top
     sb_lo = oracle.e4m3_encode(s * (1 - eps))
     sb_hi = oracle.e4m3_encode(s * (1 + eps))
     band_group = sb_lo != sb_hi
@@ -53,7 +57,10 @@ def compare_codes(R, codes_gpu, scales_gpu, bits, group, eps=2.0 ** -20):
     with np.errstate(divide="ignore", invalid="ignore"):
         # groups with s_q == 0 give inf / nan here; np.where below leaves them out
         v = R / np.repeat(sq, group, axis=1)
-        frac = np.abs(np.abs(v - np.floor(v)) - 0.5)
+        if scheme == 1:
+            frac = np.abs(v - np.rint(v))
+        else:
+            frac = np.abs(np.abs(v - np.floor(v)) - 0.5)
         band_elem = np.where(np.repeat(sq, group, axis=1) > 0,
                              frac <= eps * np.maximum(np.abs(v), 1.0), False)
     band_elem |= np.repeat(band_group, group, axis=1)
@@ -99,7 +106,7 @@ def check_centroids(R_in, pi_t, cent_gpu, stage):
             "entries": int(exact.size)}
 
 
-def forced_check(X, codes, scales, pi, cent, bits, group):
+def forced_check(X, codes, scales, pi, cent, bits, group, scheme=0):
     """One tensor's GPU outputs against the oracle given the GPU's own assignments.
     X [N][d] fp64; pi [T][N]; cent [T][C][d]."""
     T = pi.shape[0]
@@ -108,15 +115,15 @@ def forced_check(X, codes, scales, pi, cent, bits, group):
     for t in range(T):
         out["stages"].append(check_centroids(R, pi[t], cent[t], t + 1))
         R = oracle.subtract(R, pi[t].astype(np.int32), cent[t])
-    out["codes"] = compare_codes(R, codes, scales, bits, group)
+    out["codes"] = compare_codes(R, codes, scales, bits, group, scheme=scheme)
     return out
 
 
-def check_reconstruction(xhat_gpu, codes, scales, pi, cent, bits, group):
+def check_reconstruction(xhat_gpu, codes, scales, pi, cent, bits, group, scheme=0):
     """fp32 GPU reconstruction against the oracle's decode of the same compressed data."""
     T = pi.shape[0]
-    want = oracle.dequantize(codes, scales, pi, cent, bits, group)
-    deq = oracle.decode_codes(codes, scales, bits, group)
+    want = oracle.dequantize(codes, scales, pi, cent, bits, group, scheme)
+    deq = oracle.decode_codes(codes, scales, bits, group, scheme)
     S = np.abs(deq)
     for t in range(T):
         S = S + np.abs(cent[t][pi[t].astype(np.int64)])

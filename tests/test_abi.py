@@ -52,6 +52,7 @@ int main(void) {
   F(qvg_quant_params, N); F(qvg_quant_params, seed); F(qvg_quant_params, warm_stride);
   F(qvg_quant_params, table_index); F(qvg_dequant_params, chunk_len);
   F(qvg_dequant_params, out_stride); F(qvg_buffers, centroids);
+  F(qvg_quant_params, qscheme); F(qvg_dequant_params, qscheme);
   return 0;
 }
 """)
@@ -88,7 +89,7 @@ def test_workspace_bytes(lib):
     a = qvg.qvg_quantize_workspace_bytes(_qp())
     b = qvg.qvg_quantize_workspace_bytes(_qp(N=2000))
     assert 0 < a < b
-    # R^(t-1) is only materialised for stages t >= 2
+    # the cold-start index table grows with T
     assert qvg.qvg_quantize_workspace_bytes(_qp(T=1)) < a
     assert qvg.qvg_quantize_workspace_bytes(_qp(T=0)) <= 256
     for bad in (dict(d=64), dict(bits=3), dict(group=8), dict(C=0), dict(C=257), dict(T=9),
@@ -106,6 +107,7 @@ def test_workspace_bytes(lib):
     (dict(x_stride=128 * 999), qvg.QVG_ERR_INVALID_ARG),
     (dict(table_index=1), qvg.QVG_ERR_INVALID_ARG),
     (dict(n_tables=2, table_index=2), qvg.QVG_ERR_INVALID_ARG),
+    (dict(qscheme=2), qvg.QVG_ERR_UNSUPPORTED), (dict(qscheme=-1), qvg.QVG_ERR_UNSUPPORTED),
 ])
 def test_quantize_rejects_bad_arguments(lib, bad, code):
     buf = (ctypes.c_ubyte * 64)()
@@ -142,7 +144,8 @@ def test_dequantize_rejects_bad_arguments(lib):
                       (dict(out_dtype=5), qvg.QVG_ERR_UNSUPPORTED), (dict(N=0), qvg.QVG_ERR_INVALID_ARG),
                       (dict(token_capacity=50), qvg.QVG_ERR_INVALID_ARG),
                       (dict(chunk_len=10, n_tables=5), qvg.QVG_ERR_INVALID_ARG),
-                      (dict(out_stride=100), qvg.QVG_ERR_INVALID_ARG)):
+                      (dict(out_stride=100), qvg.QVG_ERR_INVALID_ARG),
+                      (dict(qscheme=3), qvg.QVG_ERR_UNSUPPORTED)):
         assert qvg.qvg_dequantize(dp(**bad), good, base, None, None) == code, bad
     assert qvg.qvg_dequantize(dp(), good, None, None, None) == qvg.QVG_ERR_INVALID_ARG
     assert qvg.qvg_dequantize(dp(), good, base + 4, None, None) == qvg.QVG_ERR_INVALID_ARG

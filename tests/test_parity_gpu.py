@@ -346,6 +346,73 @@ def test_presets_against_the_oracle(name):
             assert abs(J - ref["J"][h, t]) <= 1e-2 * ref["J"][h, t], (h, t, J, ref["J"][h, t])
 
 
+# --------------------------------------------------------------------------------------
+# The mid-rise grid (qscheme 1): 2^bits levels at half-integers of s_q
+# --------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("bits,group,T,C", [(2, 32, 2, 32), (4, 16, 1, 20), (2, 64, 0, 1),
+                                            (4, 64, 3, 7)])
+def test_midrise_dequant_matches_oracle(bits, group, T, C):
+    # the fused dequant on the oracle's own mid-rise cache
+    X = _make(22, 3, 2, 17, 30)  # N = 1020
+    Xd = oracle.decode_input(X)
+    ref = oracle.quantize(Xd, C, T, bits, group, 3, seed=5, scheme=1)
+    H, N = X.shape[:2]
+    ckv = api.allocate(H, N, C, T, bits, group, device="cuda")
+    ckv.qscheme = qvg.QVG_QSCHEME_MIDRISE
+    ckv.codes.copy_(torch.from_numpy(ref["codes"]))
+    ckv.scales.copy_(torch.from_numpy(ref["scales"]))
+    if T > 0:
+        ckv.pi.copy_(torch.from_numpy(ref["pi"]))
+        ckv.centroids.copy_(torch.from_numpy(ref["centroids"][:, None]))
+    x32 = api.dequantize(ckv, out_dtype=torch.float32).cpu().numpy()
+    x16 = api.dequantize(ckv, out_dtype=torch.bfloat16)
+    for h in range(H):
+        qc.check_reconstruction(x32[h], ref["codes"][h], ref["scales"][h], ref["pi"][h],
+                                ref["centroids"][h], bits, group, scheme=1)
+    qc.check_rounded_output(x16, x32, torch.bfloat16)
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("bits,group", [(2, 32), (2, 16), (4, 64)])
+def test_midrise_encode_T0_matches_oracle(dtype, bits, group):
+    X = _make(4, 2, 3, 11, 31, dtype)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ckv = api.quantize(X.cuda(), 1, 0, bits, group, 1, 0, status=status,
+                       qscheme=qvg.QVG_QSCHEME_MIDRISE)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    Xd = oracle.decode_input(X)
+    for h in range(X.shape[0]):
+        qc.compare_codes(Xd[h], ckv.codes[h].cpu().numpy(), ckv.scales[h].cpu().numpy(),
+                         bits, group, scheme=1)
+
+
+@pytest.mark.parametrize("bits,group,T", [(2, 32, 2), (4, 64, 1)])
+def test_midrise_end_to_end(bits, group, T):
+    X = _make(16, 2, 1, 24, 30)  # N = 720
+    C, iters, seed = 32, 3, 9
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ckv = api.quantize(X.cuda(), C, T, bits, group, iters, seed, status=status,
+                       qscheme=qvg.QVG_QSCHEME_MIDRISE)
+    x32 = api.dequantize(ckv, X.shape[1], torch.float32, status=status).cpu().numpy()
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    g = _to_np(ckv)
+    Xd = oracle.decode_input(X)
+    ref = oracle.quantize(Xd, C, T, bits, group, iters, seed, scheme=1)
+    for h in range(X.shape[0]):
+        cent = g["centroids"][h, 0]
+        qc.forced_check(Xd[h], g["codes"][h], g["scales"][h], g["pi"][h], cent, bits, group,
+                        scheme=1)
+        qc.check_reconstruction(x32[h], g["codes"][h], g["scales"][h], g["pi"][h], cent, bits,
+                                group, scheme=1)
+        assert (g["pi"][h][0] == ref["pi"][h][0]).mean() >= 0.999
+        # the assignments do not depend on the grid: the symmetric run clusters the same way
+        sym = oracle.quantize(Xd[h:h + 1], C, T, bits, group, iters, seed, tensor_id_base=h)
+        np.testing.assert_array_equal(sym["pi"][0], ref["pi"][h])
+
+
 def test_graph_capture_replays_identical_results():
     # qvg_quantize / qvg_dequantize enqueue only kernels and memsets on the given stream,
     # so a caller may capture them in a CUDA graph; the replay must give the same bits

@@ -42,6 +42,7 @@ struct QPlan {
     int H;
     int64_t N;
     int C, Cpad, T, bits, group, iters, in_dtype;  // Cpad: C rounded up to a multiple of 32
+    int qscheme;           // qvg_qscheme of the codes
     int64_t x_stride;      // elements between tensors of X
     int64_t cap, tok_off;  // token slots per tensor in codes/scales/pi, first slot written
     int64_t cent_tstride;  // floats between tensors in the centroid tables
@@ -279,7 +280,7 @@ size_t assign_smem_bytes(int Cpad);
 struct DPlan {
     int H;
     int64_t N;
-    int C, T, bits, group, out_dtype;
+    int C, T, bits, group, out_dtype, qscheme;
     int64_t chunk_len, cap;
     int n_tables;
     int64_t out_stride;

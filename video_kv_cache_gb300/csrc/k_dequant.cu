@@ -59,7 +59,7 @@ __device__ __forceinline__ float e4m3_to_float(uint32_t b) {
 }
 }  // namespace
 
-template <int BITS, int OUT, int TT>
+template <int BITS, int OUT, int TT, int SH>  // SH: 1 for the mid-rise grid, else 0
 __global__ void __launch_bounds__(kDqThreads, 1)
     k_dequant(DPlan p, int W, int64_t n_chunks, int smem_tables, int wide_stores) {
     pdl_begin();
@@ -69,6 +69,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     const int T = TT >= 0 ? TT : p.T;
     const int C = p.C;
     float *tab = smem_f;  // [T][C][W], swizzled 16-byte chunks
+    constexpr int sh = SH;  // code shift of the level trick
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int LPT = W / kLaneCh;  // lanes per token
     const int TPW = 32 / LPT;     // tokens per warp and pass
@@ -183,24 +184,26 @@ __global__ void __launch_bounds__(kDqThreads, 1)
             sp += sstep;
             pp += tpc;
             if (inext + tpc < i1) fetch(nxt2);
-            // Code e of a 16-bit half-word sits at bits BITS*e; kept in place inside the
-            // mantissa of 2^23, the float is 2^23 + u * 2^(BITS*e), so subtracting
-            // 2^23 + MID * 2^(BITS*e) leaves (u - MID) * 2^(BITS*e) exactly, and
-            // sq * 2^-(BITS*e) (exact: a power-of-two rescaling) turns it into sq * q.
+            // Code e of a 16-bit half-word sits at bits BITS*e; shifted left by sh (0, or 1
+            // for the mid-rise grid) and kept inside the mantissa of 2^23, the float is
+            // 2^23 + u * 2^(BITS*e + sh).  Subtracting 2^23 + (MID * 2^sh - sh) * 2^(BITS*e)
+            // leaves (u * 2^sh - MID * 2^sh + sh) * 2^(BITS*e) exactly, and
+            // sq * 2^-(BITS*e + sh) (exact: a power-of-two rescaling) turns it into the
+            // level: sq * (u - MID), or sq * (u - MID + 1/2) for the mid-rise grid.
             const float sq = e4m3_to_float(cur.sbyte & 0xFFu);
             float se[PER16], ke[PER16];
 #pragma unroll
             for (int e = 0; e < PER16; e++) {
-                se[e] = __fmul_rn(sq, __uint_as_float((uint32_t)(127 - BITS * e) << 23));
-                ke[e] = __uint_as_float(0x4B000000u) + (float)(MID << (BITS * e));
+                se[e] = __fmul_rn(sq, __uint_as_float((uint32_t)(127 - BITS * e - sh) << 23));
+                ke[e] = __uint_as_float(0x4B000000u) + (float)(((MID << sh) - sh) << (BITS * e));
             }
             float y[16];
 #pragma unroll
             for (int hw = 0; hw < 16 / PER16; hw++) {
-                const uint32_t word = cur.code[hw >> 1] >> (16 * (hw & 1));
+                const uint32_t word = (cur.code[hw >> 1] >> (16 * (hw & 1))) << sh;
 #pragma unroll
                 for (int e = 0; e < PER16; e++) {
-                    const uint32_t m = (word & (((1u << BITS) - 1u) << (BITS * e))) | 0x4B000000u;
+                    const uint32_t m = (word & (((1u << BITS) - 1u) << (BITS * e + sh))) | 0x4B000000u;
                     y[hw * PER16 + e] = __fsub_rn(__uint_as_float(m), ke[e]);
                 }
             }
@@ -276,7 +279,7 @@ namespace {
 template <int BITS, int OUT, int TT>
 cudaError_t launch_dq(const DPlan &p, int num_sms, int W, size_t table_bytes, bool smem_tables,
                       cudaStream_t st) {
-    auto kern = k_dequant<BITS, OUT, TT>;
+    auto kern = p.qscheme == QVG_QSCHEME_MIDRISE ? k_dequant<BITS, OUT, TT, 1> : k_dequant<BITS, OUT, TT, 0>;
     const size_t smem = smem_tables ? table_bytes : 16;
     // 32-byte stores need a 32-byte aligned output and tensor stride
     const size_t eb = p.out_dtype == DT_F32 ? 4 : 2;

@@ -890,6 +890,7 @@ __global__ void __launch_bounds__(256) k_encode(QPlan p) {
     const int h = blockIdx.y;
     const int c8 = threadIdx.x & 15;
     const int lpg = p.group >> 3;  // lanes per scale group (2, 4, 8)
+    const bool midrise = p.qscheme == QVG_QSCHEME_MIDRISE;
     const int64_t i0 = (int64_t)blockIdx.x * kEncTokens;
     const int64_t i1 = min(p.N, i0 + kEncTokens);
     float nanprobe = 0.f;  // becomes NaN if any input is NaN or infinite (x * 0)
@@ -966,7 +967,9 @@ __global__ void __launch_bounds__(256) k_encode(QPlan p) {
                 a = fmaxf(a, fabsf(r[q]));
             }
             for (int o = 1; o < lpg; o <<= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
-            const float sc = QMAX == 1 ? a : __fdiv_rn(a, (float)QMAX);  // a / qmax, IEEE
+            // a / (the outermost level), IEEE: qmax, or 2^(b-1) - 1/2 for the mid-rise grid
+            const float sc = midrise ? __fdiv_rn(a, (float)MID - 0.5f)
+                                     : (QMAX == 1 ? a : __fdiv_rn(a, (float)QMAX));
             const __nv_fp8_storage_t sb = __nv_cvt_float_to_fp8(sc, __NV_SATFINITE, __NV_E4M3);
             const float sq = __half2float(__half(__nv_cvt_fp8_to_halfraw(sb, __NV_E4M3)));
             // q = clamp(rne(r / s_q)) with the IEEE quotient.  r times an approximate
@@ -975,7 +978,31 @@ __global__ void __launch_bounds__(256) k_encode(QPlan p) {
             // 1.5 * 2^23 to the clamped quotient rounds it to an integer (half to even) and
             // leaves that integer in the low mantissa bits.
             uint32_t word = 0;
-            if (sq != 0.f) {
+            if (sq != 0.f && midrise) {
+                // u = floor(r / s_q) + 2^(b-1), clamped.  r times an approximate reciprocal
+                // (a few ulps) has the same floor except close to an integer; there the
+                // quotient is recomputed with a correctly rounded division.
+                float inv;
+                asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(inv) : "f"(sq));
+                float fq[8];
+                uint32_t close = 0;
+#pragma unroll
+                for (int q = 0; q < 8; q++) {
+                    const float v = __fmul_rn(r[q], inv);
+                    fq[q] = floorf(v);
+                    close |= (fabsf(__fsub_rn(v, rintf(v))) < 0x1p-17f * fmaxf(1.f, fabsf(v)) ? 1u : 0u) << q;
+                }
+                if (close) {  // rare
+#pragma unroll
+                    for (int q = 0; q < 8; q++)
+                        if ((close >> q) & 1u) fq[q] = floorf(__fdiv_rn(r[q], sq));
+                }
+#pragma unroll
+                for (int q = 0; q < 8; q++) {
+                    const float u = fminf(fmaxf(fq[q] + (float)MID, 0.f), (float)(2 * MID - 1));
+                    word |= (uint32_t)u << (q * BITS);
+                }
+            } else if (sq != 0.f) {
                 constexpr float kRound = 12582912.f;  // 1.5 * 2^23
                 float inv;
                 asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(inv) : "f"(sq));
@@ -989,7 +1016,7 @@ __global__ void __launch_bounds__(256) k_encode(QPlan p) {
                     close |= (fabsf(d) > 0.5f - 0x1p-17f ? 1u : 0u) << q;
                 }
                 if (close) {  // rare
-#pragma unroll 1
+#pragma unroll
                     for (int q = 0; q < 8; q++)
                         if ((close >> q) & 1u)
                             tq[q] = __fadd_rn(fminf(fmaxf(__fdiv_rn(r[q], sq), (float)-QMAX), (float)QMAX),

@@ -68,6 +68,8 @@ qvg_status check_quant(const qvg_quant_params *p) {
     if (p->d != kD) return QVG_ERR_UNSUPPORTED;
     if (p->bits != 2 && p->bits != 4) return QVG_ERR_UNSUPPORTED;
     if (p->group != 16 && p->group != 32 && p->group != 64) return QVG_ERR_UNSUPPORTED;
+    if (p->qscheme != QVG_QSCHEME_SYMMETRIC && p->qscheme != QVG_QSCHEME_MIDRISE)
+        return QVG_ERR_UNSUPPORTED;
     if (p->T < 0 || p->T > kMaxT) return QVG_ERR_UNSUPPORTED;
     if (p->in_dtype < QVG_F16 || p->in_dtype > QVG_F32) return QVG_ERR_UNSUPPORTED;
     if (p->T > 0) {
@@ -168,6 +170,7 @@ QPlan make_plan(const qvg_quant_params *prm, const void *X, const float *warm,
     p.T = prm->T;
     p.bits = prm->bits;
     p.group = prm->group;
+    p.qscheme = prm->qscheme;
     p.iters = prm->iters;
     p.in_dtype = prm->in_dtype;
     p.x_stride = prm->x_stride ? prm->x_stride : prm->N * kD;
@@ -345,6 +348,8 @@ qvg_status qvg_dequantize(const qvg_dequant_params *prm, const qvg_buffers *in, 
     if (prm->d != kD) return QVG_ERR_UNSUPPORTED;
     if (prm->bits != 2 && prm->bits != 4) return QVG_ERR_UNSUPPORTED;
     if (prm->group != 16 && prm->group != 32 && prm->group != 64) return QVG_ERR_UNSUPPORTED;
+    if (prm->qscheme != QVG_QSCHEME_SYMMETRIC && prm->qscheme != QVG_QSCHEME_MIDRISE)
+        return QVG_ERR_UNSUPPORTED;
     if (prm->T < 0 || prm->T > kMaxT) return QVG_ERR_UNSUPPORTED;
     if (prm->out_dtype < QVG_F16 || prm->out_dtype > QVG_F32) return QVG_ERR_UNSUPPORTED;
     if (prm->T > 0 && (prm->C < 1 || prm->C > kMaxC)) return QVG_ERR_UNSUPPORTED;
@@ -372,6 +377,7 @@ qvg_status qvg_dequantize(const qvg_dequant_params *prm, const qvg_buffers *in, 
     p.bits = prm->bits;
     p.group = prm->group;
     p.out_dtype = prm->out_dtype;
+    p.qscheme = prm->qscheme;
     p.chunk_len = chunk;
     p.cap = cap;
     p.n_tables = n_tables;

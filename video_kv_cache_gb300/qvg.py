@@ -27,6 +27,7 @@ QVG_DEV_TIMEOUT = 0x2
 QVG_DEV_BAD_INDEX = 0x4
 
 QVG_F16, QVG_BF16, QVG_F32 = 0, 1, 2
+QVG_QSCHEME_SYMMETRIC, QVG_QSCHEME_MIDRISE = 0, 1
 
 
 class qvg_quant_params(ctypes.Structure):
@@ -48,6 +49,7 @@ class qvg_quant_params(ctypes.Structure):
         ("table_index", ctypes.c_int32),
         ("n_tables", ctypes.c_int32),
         ("warm_stride", ctypes.c_int64),
+        ("qscheme", ctypes.c_int32),
     ]
 
 
@@ -74,6 +76,7 @@ class qvg_dequant_params(ctypes.Structure):
         ("token_capacity", ctypes.c_int64),
         ("n_tables", ctypes.c_int32),
         ("out_stride", ctypes.c_int64),
+        ("qscheme", ctypes.c_int32),
     ]
 
 
