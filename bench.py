@@ -440,7 +440,8 @@ def run_sweep(args):
     (plain group quantization, the naive baseline) and T = 1..3 at each C, reporting the
     mean squared reconstruction error of the key and the value tensors and its reduction
     against T = 0.  Also reported: the naive error with exact fp32 scales (no E4M3
-    rounding or saturation), and how many T = 0 groups saturate E4M3 (scale > 448)."""
+    rounding or saturation), how many T = 0 groups saturate E4M3 (scale > 448), and the
+    mid-rise grid at T = 0, 1, 2 (C = 256) against the symmetric grid's T = 0."""
     from video_kv_cache_gb300 import api, qvg
     from video_kv_cache_gb300 import build as qbuild
     torch.cuda.set_device(0)
@@ -484,6 +485,17 @@ def run_sweep(args):
                 r["reduction_v"] = base["mse_v"] / r["mse_v"] if r["mse_v"] > 0 else None
         rows.append({"bits": bits, "group": group, "naive_fp32_scales_mse_k": naive32[0],
                      "naive_fp32_scales_mse_v": naive32[1], "e4m3_saturated_groups_T0": sat})
+        # the same precision on the mid-rise grid (2^bits levels at half-integers), against
+        # the symmetric grid's T = 0 error
+        C = synth.SWEEP_C[-1]
+        for T in (0, 1, 2):
+            ckv = api.quantize(X, C, T, bits, group, w.iters, w.seed, workspace=ws, status=status,
+                               qscheme=qvg.QVG_QSCHEME_MIDRISE)
+            mk, mv = mse(api.dequantize(ckv, N, torch.float32, status=status))
+            rows.append({"bits": bits, "group": group, "qscheme": "midrise", "C": C if T else 0,
+                         "T": T, "mse_k": mk, "mse_v": mv,
+                         "reduction_k": base["mse_k"] / mk if mk > 0 else None,
+                         "reduction_v": base["mse_v"] / mv if mv > 0 else None})
     torch.cuda.synchronize()
     assert int(status.item()) == 0, "device status %#x" % int(status.item())
     print(json.dumps({"metric": "MSE reduction vs naive group quantization (K, V)",
