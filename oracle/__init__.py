@@ -84,7 +84,9 @@ def _load():
         lib.orc_quantize.argtypes = [c.c_int64, c.c_int64, c.c_int, c.c_int, c.c_int, c.c_int,
                                      c.c_int, c.c_int, c.c_uint64, c.c_int64, _f64p,
                                      c.c_void_p, _u8p, _u8p, _u8p, _f32p, _f64p, c.c_int,
-                                     c.c_int]
+                                     c.c_int, c.c_int]
+        lib.orc_store_n.restype = None
+        lib.orc_store_n.argtypes = [_f64p, c.c_int64, c.c_int, _f32p]
         lib.orc_num_cores.restype = c.c_int
         lib.orc_num_cores.argtypes = []
         _lib = lib
@@ -189,6 +191,15 @@ def lloyd(R, cent, iters: int):
     return out, pi
 
 
+def store_centroids(x, centroid_format: int) -> np.ndarray:
+    """The stored value of each x in a centroid storage format: 0 fp32, 1 IEEE binary16,
+    2 bfloat16 (round to nearest even once, from fp64)."""
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    out = np.zeros(x.shape, dtype=np.float32)
+    _load().orc_store_n(x.reshape(-1), x.size, centroid_format, out.reshape(-1))
+    return out
+
+
 def encode(R, bits: int, group: int, scheme: int = 0):
     """Q(R): (codes uint8 [N][d*bits/8], E4M3 scale bytes uint8 [N][d/group]).
     scheme 0: symmetric restricted grid; 1: mid-rise (levels at half-integers)."""
@@ -228,7 +239,8 @@ def dequantize(codes, scales, pi, cent, bits: int, group: int, scheme: int = 0) 
 
 
 def quantize(X, C: int, T: int, bits: int, group: int, iters: int, seed: int,
-             tensor_id_base: int = 0, warm=None, nthreads: int = 0, scheme: int = 0) -> dict:
+             tensor_id_base: int = 0, warm=None, nthreads: int = 0, scheme: int = 0,
+             centroid_format: int = 0) -> dict:
     """The whole quantize path over a batch X [H][N][d] (float64, already decoded).
 
     Returns codes [H][N][d*b/8], scales [H][N][d/B], pi [H][T][N] (uint8),
@@ -250,7 +262,7 @@ def quantize(X, C: int, T: int, bits: int, group: int, iters: int, seed: int,
         warm_ptr = warm_arr.ctypes.data
     rc = _load().orc_quantize(H, N, d, Ce, T, bits, group, iters, seed & (2**64 - 1),
                               tensor_id_base, X, warm_ptr, codes, scales, pi, cent, J,
-                              nthreads, scheme)
+                              nthreads, scheme, centroid_format)
     if rc != 0:
         raise ValueError("orc_quantize rejected the arguments (%d)" % rc)
     return {"codes": codes, "scales": scales, "pi": pi[:, :T], "centroids": cent[:, :T],

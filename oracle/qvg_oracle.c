@@ -30,7 +30,11 @@
  *     last assignment and the stored centroid is the mean under it.  An empty cluster
  *     keeps its previous centroid.
  *   - Centroids are stored as fp32, rounded to nearest even after every update.  Residuals
- *     are taken against those stored fp32 centroids, exactly (in fp64).
+ *     are taken against those stored fp32 centroids, exactly (in fp64).  The storage
+ *     variant of the survey's next row keeps them as IEEE binary16 or bfloat16 instead
+ *     (centroid_format 1 / 2): the exact mean, and the cold-start rows and warm tables,
+ *     are rounded once to that format, and the residuals are taken against the rounded
+ *     values.
  *   - Cold start: C distinct rows of R^(t-1), chosen by a partial Fisher-Yates shuffle
  *     driven by SplitMix64 (Steele, Lea, Flood 2014; Vigna's published constants), seeded
  *     with seed ^ (tensor_id * 0x9E3779B97F4A7C15) ^ t.  Warm start: the caller's
@@ -168,8 +172,46 @@ void orc_assign(const double *R, int64_t N, int d, const float *cent, int C, int
 
 /* (b) cent_j = fp32(mean of the rows assigned to j); empty clusters keep cent_j.
  * counts, if given, receives the cluster sizes. */
+/* ------------------------------------------------------------------------------------ */
+/* Centroid storage formats: 0 fp32, 1 IEEE binary16, 2 bfloat16.  A stored centroid is   */
+/* the exact mean rounded once to the format, to nearest even; residuals are then taken   */
+/* against that stored value.  The rounding is written from the formats' definitions:    */
+/* p significand bits, smallest normal exponent emin (subnormals keep emin's quantum),    */
+/* and values past the largest finite one rounding to infinity.                           */
+/* ------------------------------------------------------------------------------------ */
+
+static double orc_round_p(double x, int p, int emin, double maxfinite) {
+    if (x != x || x == 0.0 || isinf(x)) return x;
+    int ex;
+    frexp(fabs(x), &ex); /* |x| = m 2^ex, m in [0.5, 1): the leading bit has weight 2^(ex-1) */
+    int e = ex - 1;
+    if (e < emin) e = emin;
+    const double q = ldexp(1.0, e - (p - 1));
+    double r = nearbyint(fabs(x) / q) * q; /* exact scaling; nearest, ties to even */
+    if (r > maxfinite) r = INFINITY;
+    return copysign(r, x);
+}
+
+float orc_store(double v, int format) {
+    if (format == 1) return (float)orc_round_p(v, 11, -14, 65504.0);
+    if (format == 2) return (float)orc_round_p(v, 8, -126, ldexp(255.0, 120));
+    return (float)v;
+}
+
+void orc_store_n(const double *x, int64_t n, int format, float *out) {
+    for (int64_t i = 0; i < n; i++) out[i] = orc_store(x[i], format);
+}
+
+static void orc_update_fmt(const double *R, int64_t N, int d, const int32_t *pi, int C,
+                           float *cent, int64_t *counts, int format);
+
 void orc_update(const double *R, int64_t N, int d, const int32_t *pi, int C, float *cent,
                 int64_t *counts) {
+    orc_update_fmt(R, N, d, pi, C, cent, counts, 0);
+}
+
+static void orc_update_fmt(const double *R, int64_t N, int d, const int32_t *pi, int C,
+                           float *cent, int64_t *counts, int format) {
     double *sum = (double *)calloc((size_t)C * d, sizeof(double));
     int64_t *n = (int64_t *)calloc((size_t)C, sizeof(int64_t));
     for (int64_t i = 0; i < N; i++) {
@@ -180,7 +222,7 @@ void orc_update(const double *R, int64_t N, int d, const int32_t *pi, int C, flo
     for (int j = 0; j < C; j++) {
         if (n[j] == 0) continue;
         for (int k = 0; k < d; k++)
-            cent[(int64_t)j * d + k] = (float)(sum[(int64_t)j * d + k] / (double)n[j]);
+            cent[(int64_t)j * d + k] = orc_store(sum[(int64_t)j * d + k] / (double)n[j], format);
     }
     if (counts)
         for (int j = 0; j < C; j++) counts[j] = n[j];
@@ -202,11 +244,16 @@ void orc_subtract(double *R, int64_t N, int d, const int32_t *pi, const float *c
 }
 
 /* One smoothing stage: `iters` Lloyd rounds from the centroids already in `cent`. */
-void orc_lloyd(const double *R, int64_t N, int d, int C, int iters, float *cent, int32_t *pi) {
+static void orc_lloyd_fmt(const double *R, int64_t N, int d, int C, int iters, float *cent,
+                          int32_t *pi, int format) {
     for (int it = 0; it < iters; it++) {
         orc_assign(R, N, d, cent, C, pi, NULL);
-        orc_update(R, N, d, pi, C, cent, NULL);
+        orc_update_fmt(R, N, d, pi, C, cent, NULL, format);
     }
+}
+
+void orc_lloyd(const double *R, int64_t N, int d, int C, int iters, float *cent, int32_t *pi) {
+    orc_lloyd_fmt(R, N, d, C, iters, cent, pi, 0);
 }
 
 /* ------------------------------------------------------------------------------------ */
@@ -283,7 +330,8 @@ typedef struct {
     int64_t N;
     int d, C, T, bits, group, iters;
     uint64_t seed;
-    int scheme; /* 0: symmetric restricted grid, 1: mid-rise */
+    int scheme;          /* 0: symmetric restricted grid, 1: mid-rise */
+    int centroid_format; /* 0: fp32, 1: binary16, 2: bfloat16 (see orc_store) */
 } orc_cfg;
 
 /* X [N][d] fp64 (decoded input); warm [T][C][d] or NULL; outputs codes [N][d*bits/8],
@@ -305,16 +353,18 @@ int orc_quantize_tensor(const orc_cfg *cfg, int64_t tensor_id, const double *X,
     for (int t = 1; t <= cfg->T; t++) {
         float *c = cent + (int64_t)(t - 1) * C * d;
         if (warm) {
-            memcpy(c, warm + (int64_t)(t - 1) * C * d, (size_t)C * d * sizeof(float));
+            const float *w = warm + (int64_t)(t - 1) * C * d;
+            for (int64_t x = 0; x < (int64_t)C * d; x++) c[x] = orc_store((double)w[x], cfg->centroid_format);
         } else {
             if (orc_init_indices(cfg->seed, tensor_id, t, N, C, idx) != 0) {
                 free(R), free(p), free(idx);
                 return -1;
             }
             for (int j = 0; j < C; j++)
-                for (int k = 0; k < d; k++) c[(int64_t)j * d + k] = (float)R[idx[j] * d + k];
+                for (int k = 0; k < d; k++)
+                    c[(int64_t)j * d + k] = orc_store(R[idx[j] * d + k], cfg->centroid_format);
         }
-        orc_lloyd(R, N, d, C, cfg->iters, c, p);
+        orc_lloyd_fmt(R, N, d, C, cfg->iters, c, p, cfg->centroid_format);
         if (J) J[t - 1] = orc_objective(R, N, d, p, c);
         for (int64_t i = 0; i < N; i++) pi[(int64_t)(t - 1) * N + i] = (uint8_t)p[i];
         orc_subtract(R, N, d, p, c); /* R^(t) */
@@ -364,12 +414,13 @@ int orc_num_cores(void) {
 int orc_quantize(int64_t H, int64_t N, int d, int C, int T, int bits, int group, int iters,
                  uint64_t seed, int64_t tensor_id_base, const double *X, const float *warm,
                  uint8_t *codes, uint8_t *scales, uint8_t *pi, float *cent, double *J,
-                 int nthreads, int scheme) {
+                 int nthreads, int scheme, int centroid_format) {
     if (H < 0 || N < 1 || d < 1 || T < 0 || iters < 1) return -1;
     if (T > 0 && (C < 1 || C > 256 || C > N)) return -1;
     if ((bits != 2 && bits != 4) || group < 1 || d % group != 0 || (d * bits) % 8 != 0) return -1;
     if (scheme != 0 && scheme != 1) return -1;
-    orc_cfg cfg = {N, d, C, T, bits, group, iters, seed, scheme};
+    if (centroid_format < 0 || centroid_format > 2) return -1;
+    orc_cfg cfg = {N, d, C, T, bits, group, iters, seed, scheme, centroid_format};
     if (nthreads <= 0) nthreads = orc_num_cores();
     if (nthreads > H) nthreads = (int)(H > 0 ? H : 1);
     orc_job *jobs = (orc_job *)calloc((size_t)nthreads, sizeof(orc_job));
