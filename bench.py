@@ -152,7 +152,8 @@ def dequant_bytes(H, N, C, T, bits, group, out_bytes=2, n_tables=1):
 
 def assign_flops(H, N, C):
     """Useful flops of one assignment launch over H tensors: the [N x 128] x [128 x C]
-    product per tensor (the split-bf16 GEMM issues three times as many)."""
+    product per tensor (the GEMM issues twice as many: one fp16 plane of the residual
+    against two fp16 planes of the centroids)."""
     return 2.0 * H * N * C * 128
 
 

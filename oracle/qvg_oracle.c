@@ -30,11 +30,11 @@
  *     last assignment and the stored centroid is the mean under it.  An empty cluster
  *     keeps its previous centroid.
  *   - Centroids are stored as fp32, rounded to nearest even after every update.  Residuals
- *     are taken against those stored fp32 centroids, exactly (in fp64).  The storage
- *     variant of the survey's next row keeps them as IEEE binary16 or bfloat16 instead
- *     (centroid_format 1 / 2): the exact mean, and the cold-start rows and warm tables,
- *     are rounded once to that format, and the residuals are taken against the rounded
- *     values.
+ *     are taken against those stored fp32 centroids, exactly (in fp64).  A 16-bit storage
+ *     variant (the explainer page's compression ratios count centroids in 16 bits) keeps
+ *     them as IEEE binary16 or bfloat16 instead (centroid_format 1 / 2): the exact mean,
+ *     and the cold-start rows and warm tables, are rounded once to that format, and the
+ *     residuals are taken against the rounded values.
  *   - Cold start: C distinct rows of R^(t-1), chosen by a partial Fisher-Yates shuffle
  *     driven by SplitMix64 (Steele, Lea, Flood 2014; Vigna's published constants), seeded
  *     with seed ^ (tensor_id * 0x9E3779B97F4A7C15) ^ t.  Warm start: the caller's

@@ -1,9 +1,9 @@
 """Pins of the oracle's 16-bit centroid storage (centroid_format 1 = IEEE binary16,
 2 = bfloat16), on the CPU.
 
-The survey's first "next" row stores the centroids in 16 bits and takes the residuals
-against the rounded stored values; the storage accounting of the presets counts them that
-way (the explainer page's compression ratios).  The pins tie the oracle's rounding and its
+A 16-bit storage of the centroids takes the residuals against the rounded stored values;
+the explainer page's compression ratios count centroids that way, as does the storage
+accounting of the presets.  The pins tie the oracle's rounding and its
 use to things other than itself:
   * the rounding equals numpy's binary16 cast and torch's bfloat16 cast (both round to
     nearest even), over normal, subnormal, overflowing and tie values;
