@@ -89,6 +89,19 @@ typedef enum { QVG_F16 = 0, QVG_BF16 = 1, QVG_F32 = 2 } qvg_dtype;
  * Either way s_q = E4M3(s) and s_q = 0 stores every code as 2^(bits-1). */
 typedef enum { QVG_QSCHEME_SYMMETRIC = 0, QVG_QSCHEME_MIDRISE = 1 } qvg_qscheme;
 
+/* Value format of the stored centroids.  The tables stay float arrays; with a 16-bit format
+ * every stored value is exactly representable in it, so a consumer may narrow the tables
+ * without loss, and residuals, codes and reconstruction all use those rounded values.
+ *   QVG_CENTROIDS_F32:  the fp32 mean (the default).
+ *   QVG_CENTROIDS_F16:  IEEE binary16; QVG_CENTROIDS_BF16: bfloat16.  The cluster mean, a
+ *     cold-start row and a warm-start value are each rounded once to nearest even in the
+ *     format (the mean is carried to about twice fp32's precision, so the rounding is that
+ *     of the exact mean save within about 2^-40 relative of a tie).
+ * Quant VideoGen explainer page, compression and metadata overhead: the ratios it prints
+ * count centroids in a 16-bit format. */
+typedef enum { QVG_CENTROIDS_F32 = 0, QVG_CENTROIDS_F16 = 1, QVG_CENTROIDS_BF16 = 2 }
+    qvg_centroid_format;
+
 typedef struct {
     int32_t n_tensors;      /* H >= 1: independent (layer, head, K/V) tensors in this call */
     int32_t d;              /* channels per token; must be 128 */
@@ -109,6 +122,7 @@ typedef struct {
     int64_t warm_stride;    /* floats between consecutive tensors of warm_centroids
                                (0 = T*C*d) */
     int32_t qscheme;        /* qvg_qscheme of the codes (zero-initialised = symmetric) */
+    int32_t centroid_format; /* qvg_centroid_format of the stored centroids (0 = fp32) */
 } qvg_quant_params;
 
 /* The compressed cache.  Layouts (all row-major, caller-owned device memory):

@@ -106,6 +106,42 @@ def check_centroids(R_in, pi_t, cent_gpu, stage):
             "entries": int(exact.size)}
 
 
+def check_centroids_stored(R_in, pi_t, cent_gpu, stage, fmt):
+    """Centroids of one stage in a 16-bit storage format (1 binary16, 2 bfloat16) against the
+    oracle's rounding of the exact means of R_in over pi_t.  Each stored value must be
+    representable in the format; a non-empty cluster's value must equal the rounding of its
+    exact mean, except where the exact mean lies so close to a midpoint of two format values
+    that the GPU's fp32 mean could fall on either side: within two fp32 ulps (stage 1) plus
+    half an fp32 ulp of the cluster's largest member (later stages, whose members the GPU
+    holds in fp32).  There the value must be one of the two neighbours."""
+    C = cent_gpu.shape[0]
+    np.testing.assert_array_equal(oracle.store_centroids(cent_gpu.astype(np.float64), fmt),
+                                  cent_gpu)
+    pi_t = np.asarray(pi_t, dtype=np.int64)
+    counts = np.bincount(pi_t, minlength=C)
+    sums = np.zeros((C, R_in.shape[1]))
+    np.add.at(sums, pi_t, R_in)
+    nz = counts > 0
+    exact = sums[nz] / counts[nz, None]
+    want = oracle.store_centroids(exact, fmt)
+    slack = 2.0 * ulp32(exact)
+    if stage > 1:
+        maxabs = np.zeros(C)
+        np.maximum.at(maxabs, pi_t, np.abs(R_in).max(axis=1))
+        slack = slack + 0.5 * ulp32(maxabs)[nz, None]
+    lo = oracle.store_centroids(exact - slack, fmt)
+    hi = oracle.store_centroids(exact + slack, fmt)
+    got = cent_gpu[nz]
+    differ = got != want
+    ok = ~differ | ((lo != hi) & ((got == lo) | (got == hi)))
+    if not ok.all():
+        j, k = np.argwhere(~ok)[0]
+        raise AssertionError("stage %d stored centroid (row %d, channel %d): got %r, want %r "
+                             "(exact mean %r)" % (stage, j, k, got[j, k], want[j, k], exact[j, k]))
+    return {"clusters": int(nz.sum()), "entries": int(exact.size),
+            "tie_band": int(differ.sum())}
+
+
 def forced_check(X, codes, scales, pi, cent, bits, group, scheme=0):
     """One tensor's GPU outputs against the oracle given the GPU's own assignments.
     X [N][d] fp64; pi [T][N]; cent [T][C][d]."""

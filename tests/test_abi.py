@@ -53,6 +53,7 @@ int main(void) {
   F(qvg_quant_params, table_index); F(qvg_dequant_params, chunk_len);
   F(qvg_dequant_params, out_stride); F(qvg_buffers, centroids);
   F(qvg_quant_params, qscheme); F(qvg_dequant_params, qscheme);
+  F(qvg_quant_params, centroid_format);
   return 0;
 }
 """)
@@ -108,6 +109,8 @@ def test_workspace_bytes(lib):
     (dict(table_index=1), qvg.QVG_ERR_INVALID_ARG),
     (dict(n_tables=2, table_index=2), qvg.QVG_ERR_INVALID_ARG),
     (dict(qscheme=2), qvg.QVG_ERR_UNSUPPORTED), (dict(qscheme=-1), qvg.QVG_ERR_UNSUPPORTED),
+    (dict(centroid_format=3), qvg.QVG_ERR_UNSUPPORTED),
+    (dict(centroid_format=-1), qvg.QVG_ERR_UNSUPPORTED),
 ])
 def test_quantize_rejects_bad_arguments(lib, bad, code):
     buf = (ctypes.c_ubyte * 64)()

@@ -28,6 +28,7 @@ class CompressedKV:
     bits: int
     group: int
     qscheme: int = 0         # qvg_qscheme of the codes (set by quantize)
+    centroid_format: int = 0  # qvg_centroid_format of the stored centroids (set by quantize)
 
     @property
     def H(self):
@@ -65,13 +66,14 @@ def allocate(H: int, capacity: int, C: int, T: int, bits: int, group: int, n_tab
 
 def quant_params(H, N, C, T, bits, group, iters, dtype, seed=0, tensor_id_base=0, x_stride=0,
                  token_offset=0, token_capacity=0, table_index=0, n_tables=0, warm_stride=0,
-                 qscheme=0):
+                 qscheme=0, centroid_format=0):
     return _c.qvg_quant_params(n_tensors=H, d=D, N=N, C=C, T=T, bits=bits, group=group,
                                iters=iters, in_dtype=_DT[dtype], seed=seed & (2 ** 64 - 1),
                                tensor_id_base=tensor_id_base, x_stride=x_stride,
                                token_offset=token_offset, token_capacity=token_capacity,
                                table_index=table_index, n_tables=n_tables,
-                               warm_stride=warm_stride, qscheme=qscheme)
+                               warm_stride=warm_stride, qscheme=qscheme,
+                               centroid_format=centroid_format)
 
 
 def workspace_bytes(H: int, N: int, C: int, T: int, bits: int = 2, group: int = 32) -> int:
@@ -93,12 +95,14 @@ def quantize(X: torch.Tensor, C: int, T: int, bits: int, group: int, iters: int,
              *, warm: torch.Tensor | None = None, warm_stride: int = 0,
              out: CompressedKV | None = None, token_offset: int = 0, table_index: int = 0,
              workspace: torch.Tensor | None = None, status: torch.Tensor | None = None,
-             tensor_id_base: int = 0, stream=None, qscheme: int = 0) -> CompressedKV:
+             tensor_id_base: int = 0, stream=None, qscheme: int = 0,
+             centroid_format: int = 0) -> CompressedKV:
     """Compress X [H][N][128] (fp16 / bf16 / fp32 CUDA tensor; tensor stride may be larger
     than N*128).  With ``out`` given, writes tokens [token_offset, token_offset + N) and
     centroid table ``table_index`` of it; ``warm`` (fp32 [H][T][C][128] or a view with tensor
     stride ``warm_stride``) replaces the seeded cold start.  ``qscheme`` picks the integer
-    grid of the codes (qvg.QVG_QSCHEME_*) and is recorded in the returned cache."""
+    grid of the codes (qvg.QVG_QSCHEME_*) and ``centroid_format`` the value format of the
+    stored centroids (qvg.QVG_CENTROIDS_*); both are recorded in the returned cache."""
     assert X.is_cuda and X.dim() == 3 and X.shape[2] == D
     assert X.stride(2) == 1 and X.stride(1) == D
     H, N, _ = X.shape
@@ -108,7 +112,7 @@ def quantize(X: torch.Tensor, C: int, T: int, bits: int, group: int, iters: int,
         workspace = new_workspace(H, N, C, T, X.device)
     prm = quant_params(H, N, C, T, bits, group, iters, X.dtype, seed, tensor_id_base,
                        X.stride(0), token_offset, out.capacity, table_index, out.n_tables,
-                       warm_stride, qscheme)
+                       warm_stride, qscheme, centroid_format)
     rc = _c.qvg_quantize(prm, X.data_ptr(), warm.data_ptr() if warm is not None else None,
                          out.buffers(), workspace.data_ptr(), workspace.numel(),
                          status.data_ptr() if status is not None else None,
@@ -116,6 +120,7 @@ def quantize(X: torch.Tensor, C: int, T: int, bits: int, group: int, iters: int,
     if rc != _c.QVG_OK:
         raise _c.QVGError(rc, "qvg_quantize")
     out.qscheme = qscheme
+    out.centroid_format = centroid_format
     return out
 
 

@@ -43,6 +43,7 @@ struct QPlan {
     int64_t N;
     int C, Cpad, T, bits, group, iters, in_dtype;  // Cpad: C rounded up to a multiple of 32
     int qscheme;           // qvg_qscheme of the codes
+    int cfmt;              // qvg_centroid_format of the stored centroids
     int64_t x_stride;      // elements between tensors of X
     int64_t cap, tok_off;  // token slots per tensor in codes/scales/pi, first slot written
     int64_t cent_tstride;  // floats between tensors in the centroid tables

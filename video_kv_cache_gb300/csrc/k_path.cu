@@ -82,6 +82,28 @@ cudaError_t launch_init_indices(const QPlan &p, uint64_t seed, int64_t tid_base,
     return launch_kernel(k_init_indices, dim3(p.T, p.H), dim3(32), 0, st, p, seed, tid_base);
 }
 
+// A centroid value in the stored format (qvg_centroid_format): v + rem, with v a faithful
+// fp32 rounding of it, rounded once to nearest even in binary16 or bfloat16.  The midpoint
+// of the two format neighbours lo <= hi of v is an fp32 number, so v + rem lies on the same
+// side of it as v unless v is that midpoint; then the sign of rem decides.  The midpoint of two
+// neighbouring 16-bit values has at most 12 significant bits, so it is exact in fp32 (away
+// from fp32's subnormal range, which no centroid of these inputs reaches).
+__device__ __forceinline__ float store_centroid_value(float v, float rem, int fmt) {
+    if (fmt == QVG_CENTROIDS_F32) return v;
+    float lo, hi, rn;
+    if (fmt == QVG_CENTROIDS_F16) {
+        lo = __half2float(__float2half_rd(v));
+        hi = __half2float(__float2half_ru(v));
+        rn = __half2float(__float2half_rn(v));
+    } else {
+        lo = __bfloat162float(__float2bfloat16_rd(v));
+        hi = __bfloat162float(__float2bfloat16_ru(v));
+        rn = __bfloat162float(__float2bfloat16_rn(v));
+    }
+    if (lo == hi || isinf(lo) || isinf(hi) || v != 0.5f * (lo + hi) || rem == 0.f) return rn;
+    return rem > 0.f ? hi : lo;
+}
+
 // --------------------------------------------------------------------------------------
 // Stage-t initial centroids: rows of R^(t-1) picked by the seeded shuffle, or the caller's
 // warm-start table.   grid (C, H), block 128 (one thread per channel).
@@ -91,7 +113,7 @@ __global__ void k_init_centroids(QPlan p, int t) {
     const int j = blockIdx.x, h = blockIdx.y, k = threadIdx.x;
     float *dst = p.cent + h * p.cent_tstride + p.cent_off + (int64_t)(t - 1) * p.C * kD +
                  (int64_t)j * kD;
-    float v;
+    float v, rem = 0.f;
     if (p.warm) {
         v = __ldg(p.warm + h * p.warm_stride + (int64_t)(t - 1) * p.C * kD + (int64_t)j * kD + k);
     } else {
@@ -108,10 +130,12 @@ __global__ void k_init_centroids(QPlan p, int t) {
                 two_sum(v, -c, v, err);
                 e = __fadd_rn(e, err);
             }
-            v = __fadd_rn(v, e);
+            const float r = __fadd_rn(v, e);
+            rem = __fadd_rn(__fsub_rn(v, r), e);  // |e| is far below |v|: v - r is exact
+            v = r;
         }
     }
-    dst[k] = v;
+    dst[k] = store_centroid_value(v, rem, p.cfmt);
 }
 
 cudaError_t launch_init_centroids(const QPlan &p, int t, cudaStream_t st) {
@@ -437,6 +461,14 @@ __device__ __forceinline__ float mean_of(float S, float E, float n) {
     const float q0 = __fdiv_rn(S, n);
     const float r = __fadd_rn(__fmaf_rn(-q0, n, S), E);
     return __fadd_rn(q0, __fdiv_rn(r, n));
+}
+
+// The mean of a compensated sum (S, E) over n members in the stored format: the fp32 mean
+// and the sign of what it leaves out decide the rounding.
+__device__ __forceinline__ float stored_mean(float S, float E, float n, int fmt) {
+    const float m = mean_of(S, E, n);
+    if (fmt == QVG_CENTROIDS_F32) return m;
+    return store_centroid_value(m, __fadd_rn(__fmaf_rn(-m, n, S), E), fmt);
 }
 
 // New centroid row j (lane l: channels 4l..4l+3), and its GEMM planes if requested.
@@ -836,8 +868,8 @@ __global__ void __launch_bounds__(256) k_cluster_finalize(QPlan p, int t, int pl
     }
     const float n = (float)cnt;
     write_centroid(p, h, t, j, lane, true,
-                   make_float4(mean_of(S[0], E[0], n), mean_of(S[1], E[1], n), mean_of(S[2], E[2], n),
-                               mean_of(S[3], E[3], n)),
+                   make_float4(stored_mean(S[0], E[0], n, p.cfmt), stored_mean(S[1], E[1], n, p.cfmt),
+                               stored_mean(S[2], E[2], n, p.cfmt), stored_mean(S[3], E[3], n, p.cfmt)),
                    planes != 0, mu);
     // zero the total again for the next round's histogram (an empty cluster's is already
     // zero); every lane has used cnt by now

@@ -70,6 +70,8 @@ qvg_status check_quant(const qvg_quant_params *p) {
     if (p->group != 16 && p->group != 32 && p->group != 64) return QVG_ERR_UNSUPPORTED;
     if (p->qscheme != QVG_QSCHEME_SYMMETRIC && p->qscheme != QVG_QSCHEME_MIDRISE)
         return QVG_ERR_UNSUPPORTED;
+    if (p->centroid_format < QVG_CENTROIDS_F32 || p->centroid_format > QVG_CENTROIDS_BF16)
+        return QVG_ERR_UNSUPPORTED;
     if (p->T < 0 || p->T > kMaxT) return QVG_ERR_UNSUPPORTED;
     if (p->in_dtype < QVG_F16 || p->in_dtype > QVG_F32) return QVG_ERR_UNSUPPORTED;
     if (p->T > 0) {
@@ -171,6 +173,7 @@ QPlan make_plan(const qvg_quant_params *prm, const void *X, const float *warm,
     p.bits = prm->bits;
     p.group = prm->group;
     p.qscheme = prm->qscheme;
+    p.cfmt = prm->centroid_format;
     p.iters = prm->iters;
     p.in_dtype = prm->in_dtype;
     p.x_stride = prm->x_stride ? prm->x_stride : prm->N * kD;

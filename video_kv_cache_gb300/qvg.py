@@ -28,6 +28,7 @@ QVG_DEV_BAD_INDEX = 0x4
 
 QVG_F16, QVG_BF16, QVG_F32 = 0, 1, 2
 QVG_QSCHEME_SYMMETRIC, QVG_QSCHEME_MIDRISE = 0, 1
+QVG_CENTROIDS_F32, QVG_CENTROIDS_F16, QVG_CENTROIDS_BF16 = 0, 1, 2
 
 
 class qvg_quant_params(ctypes.Structure):
@@ -50,6 +51,7 @@ class qvg_quant_params(ctypes.Structure):
         ("n_tables", ctypes.c_int32),
         ("warm_stride", ctypes.c_int64),
         ("qscheme", ctypes.c_int32),
+        ("centroid_format", ctypes.c_int32),
     ]
 
 
