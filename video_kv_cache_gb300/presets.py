@@ -14,9 +14,11 @@ costs, in bits:
   * scales:    8 * d / group (one E4M3 byte per group)
   * pi:        8 * T (one cluster byte per stage)
   * centroids: T * C * d * centroid_bits, once per tensor, so N tokens share it
-The compression ratio is the 16-bit input over that total.  This library stores fp32
-centroids (centroid_bits = 32); the pages' ratios count a narrower centroid format, which
-the function takes as a parameter for comparison only.
+The compression ratio is the 16-bit input over that total.  The library keeps its centroid
+tables as fp32 arrays (centroid_bits = 32, what ``cache_bytes`` counts).  The pages' ratios
+count 16-bit centroids: with a 16-bit centroid format (qvg.QVG_CENTROIDS_F16 / _BF16) every
+stored value is representable in 16 bits, so a consumer that narrows the tables stores what
+``storage_bits(..., centroid_bits=16)`` counts.
 """
 from __future__ import annotations
 
