@@ -232,6 +232,44 @@ typedef struct {
 qvg_status qvg_dequantize(const qvg_dequant_params *params, const qvg_buffers *in,
                           void *X_hat, uint32_t *dev_status, void *stream);
 
+/* Parameters of one qvg_attention call. */
+typedef struct {
+    int32_t n_heads;        /* H: 1 .. 65535 */
+    int32_t d;              /* 128 */
+    int32_t M;              /* queries per head: 1 .. 16 */
+    int64_t N;              /* keys per head: cache slots [0, N) */
+    int32_t C, T, bits, group, qscheme;  /* of both caches, as they were quantized */
+    int64_t chunk_len;      /* tokens per centroid table (0 = N), as in qvg_dequant_params */
+    int64_t token_capacity; /* token slots per tensor of both caches (0 = N) */
+    int32_t n_tables;       /* centroid-table slots per tensor (0 = 1) */
+    int32_t q_dtype;        /* qvg_dtype of Q */
+    int32_t out_dtype;      /* qvg_dtype of O */
+    float scale;            /* multiplies q.k before the softmax, e.g. 1/sqrt(d); finite */
+    int64_t k_first;        /* head h reads key tensor k_first + h * tensor_step of k_cache */
+    int64_t v_first;        /* and value tensor v_first + h * tensor_step of v_cache */
+    int64_t tensor_step;    /* >= 0; keys and values interleaved in one cache: pass it as
+                               both caches with k_first 0, v_first 1, tensor_step 2 */
+} qvg_attention_params;
+
+/* Workspace bytes qvg_attention needs for these parameters (0 if they are invalid). */
+size_t qvg_attention_workspace_bytes(const qvg_attention_params *params);
+
+/* Softmax attention read straight from the compressed cache.  For head h and query m:
+ *   O[h][m] = sum_j p_j v_j,  p = softmax over j < N of (scale * Q[h][m] . k_j),
+ * where k_j and v_j are token j of the head's key and value tensors rebuilt exactly as
+ * qvg_dequantize writes them in fp32.  The rebuilt rows stay in registers and shared
+ * memory; nothing of size N x d is written (the notes page's fused reconstruction,
+ * section Algorithm-System Co-design, feeding attention on the fly).
+ * Layouts: Q [H][M][d] of q_dtype, O [H][M][d] of out_dtype, both contiguous and 16-byte
+ * aligned; the caches as qvg_buffers describes.  Scores, softmax and sums are fp32, the
+ * output rounded once to out_dtype.  Tensor indices are not checked against the caches'
+ * sizes: the caller guarantees them.  A cluster index >= C is clamped and reported as
+ * QVG_DEV_BAD_INDEX. */
+qvg_status qvg_attention(const qvg_attention_params *params, const void *Q,
+                         const qvg_buffers *k_cache, const qvg_buffers *v_cache, void *O,
+                         void *workspace, size_t workspace_bytes, uint32_t *dev_status,
+                         void *stream);
+
 /* Static description of a status code. */
 const char *qvg_status_string(qvg_status status);
 

@@ -173,6 +173,40 @@ def check_reconstruction(xhat_gpu, codes, scales, pi, cent, bits, group, scheme=
     return {"max_err_over_tol": float((err / tol).max())}
 
 
+def decode_with_slack(codes, scales, pi, cent, bits, group, scheme=0):
+    """The oracle's fp64 reconstruction of one tensor and, per element, the most an fp32
+    reconstruction can be off: (T + 1) * ulp32(|deQ| + sum_t |C^(t)[pi^(t)]|)."""
+    T = pi.shape[0]
+    x = oracle.dequantize(codes, scales, pi, cent, bits, group, scheme)
+    S = np.abs(oracle.decode_codes(codes, scales, bits, group, scheme))
+    for t in range(T):
+        S = S + np.abs(cent[t][pi[t].astype(np.int64)])
+    return x, (T + 1) * ulp32(S)
+
+
+def attention_tolerance(Q, K, V, eps_k, eps_v, scale):
+    """Bound on |O_fp32 - O_exact| per (query, channel) for attention computed in fp32 over
+    keys and values rebuilt in fp32 (each off by at most eps_k / eps_v from K / V):
+      * a score is a 128-term fp32 FMA chain times the scale:
+        |ds| <= scale * (|q|.eps_k + 2 * 128 u * |q|.|k|) + 2u |s|   (u = 2^-24);
+      * the softmax weights then move by a relative rho <= expm1(2 max|ds|) + 8u (two
+        exponentials of 2 ulps and the rescaling products), which moves the weighted mean
+        by at most 2 rho max|v| (the weights sum to one);
+      * the sums of weights and weighted values (N terms, one rescale per 32-key tile, one
+        per split when the splits are merged) add gamma = (N + N/16 + 4096) u relative to
+        max|v| each, the final division one more u;
+      * the values themselves are off by at most max eps_v."""
+    u = 2.0 ** -24
+    Q = np.asarray(Q, dtype=np.float64)
+    N = K.shape[0]
+    aq = np.abs(Q)
+    ds = scale * (aq @ eps_k.T + 2 * 128 * u * (aq @ np.abs(K).T)) + 2 * u * np.abs(scale * (Q @ K.T))
+    rho = np.expm1(2 * ds.max(axis=1)) + 8 * u
+    gamma = (N + N / 16 + 4096) * u
+    vmax = np.abs(V).max(axis=0)
+    return (2 * rho[:, None] + 2 * gamma + u) * vmax[None, :] + eps_v.max(axis=0)[None, :] + 1e-30
+
+
 def check_rounded_output(x16, x32, dtype):
     """A 16-bit output must be the round-to-nearest-even of the fp32 output."""
     import torch

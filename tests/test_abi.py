@@ -54,6 +54,10 @@ int main(void) {
   F(qvg_dequant_params, out_stride); F(qvg_buffers, centroids);
   F(qvg_quant_params, qscheme); F(qvg_dequant_params, qscheme);
   F(qvg_quant_params, centroid_format);
+  printf("qvg_attention_params %zu\\n", sizeof(qvg_attention_params));
+  F(qvg_attention_params, N); F(qvg_attention_params, chunk_len);
+  F(qvg_attention_params, scale); F(qvg_attention_params, k_first);
+  F(qvg_attention_params, tensor_step);
   return 0;
 }
 """)
@@ -65,9 +69,11 @@ int main(void) {
     assert int(got["qvg_quant_params"]) == ctypes.sizeof(qvg.qvg_quant_params)
     assert int(got["qvg_dequant_params"]) == ctypes.sizeof(qvg.qvg_dequant_params)
     assert int(got["qvg_buffers"]) == ctypes.sizeof(qvg.qvg_buffers)
+    assert int(got["qvg_attention_params"]) == ctypes.sizeof(qvg.qvg_attention_params)
     for key, st in (("qvg_quant_params", qvg.qvg_quant_params),
                     ("qvg_dequant_params", qvg.qvg_dequant_params),
-                    ("qvg_buffers", qvg.qvg_buffers)):
+                    ("qvg_buffers", qvg.qvg_buffers),
+                    ("qvg_attention_params", qvg.qvg_attention_params)):
         for k, v in got.items():
             if k.startswith(key + "."):
                 assert int(v) == getattr(st, k.split(".")[1]).offset, k
@@ -152,3 +158,46 @@ def test_dequantize_rejects_bad_arguments(lib):
         assert qvg.qvg_dequantize(dp(**bad), good, base, None, None) == code, bad
     assert qvg.qvg_dequantize(dp(), good, None, None, None) == qvg.QVG_ERR_INVALID_ARG
     assert qvg.qvg_dequantize(dp(), good, base + 4, None, None) == qvg.QVG_ERR_INVALID_ARG
+
+
+def _ap(**kw):
+    base = dict(n_heads=3, d=128, M=2, N=1000, C=64, T=2, bits=2, group=32,
+                q_dtype=qvg.QVG_BF16, out_dtype=qvg.QVG_F32, scale=0.088, tensor_step=1)
+    base.update(kw)
+    return qvg.qvg_attention_params(**base)
+
+
+def test_attention_workspace_bytes(lib):
+    a = qvg.qvg_attention_workspace_bytes(_ap())
+    # 4 splits of 256 keys, 3 heads x 2 queries: partial rows of 128 floats plus 2 floats
+    assert a == 3 * 4 * 2 * 128 * 4 + 256
+    assert qvg.qvg_attention_workspace_bytes(_ap(M=4)) > a
+    assert qvg.qvg_attention_workspace_bytes(_ap(N=100000)) > a
+    for bad in (dict(M=0), dict(M=17), dict(N=0), dict(d=64), dict(bits=3), dict(group=8),
+                dict(T=9), dict(C=0), dict(qscheme=2), dict(q_dtype=5), dict(out_dtype=-1),
+                dict(scale=float("inf")), dict(scale=float("nan")), dict(n_heads=0),
+                dict(tensor_step=-1), dict(k_first=-1), dict(token_capacity=10), dict(n_heads=65536),
+                dict(chunk_len=100, n_tables=2)):
+        assert qvg.qvg_attention_workspace_bytes(_ap(**bad)) == 0, bad
+
+
+def test_attention_rejects_bad_arguments(lib):
+    buf = (ctypes.c_ubyte * 64)()
+    base = ctypes.addressof(buf) + (-ctypes.addressof(buf)) % 16
+    good = qvg.qvg_buffers(base, base, base, base)
+    nocent = qvg.qvg_buffers(base, base, base, None)
+    big = 1 << 40
+    for prm, q, kc, vc, o, ws, code in (
+            (_ap(M=17), base, good, good, base, big, qvg.QVG_ERR_UNSUPPORTED),
+            (_ap(N=0), base, good, good, base, big, qvg.QVG_ERR_INVALID_ARG),
+            (_ap(), None, good, good, base, big, qvg.QVG_ERR_INVALID_ARG),
+            (_ap(), base, good, good, None, big, qvg.QVG_ERR_INVALID_ARG),
+            (_ap(), base + 2, good, good, base, big, qvg.QVG_ERR_INVALID_ARG),
+            (_ap(), base, good, nocent, base, big, qvg.QVG_ERR_INVALID_ARG),
+            (_ap(), base, None, good, base, big, qvg.QVG_ERR_INVALID_ARG),
+            (_ap(), base, good, good, base, 16, qvg.QVG_ERR_WORKSPACE)):
+        assert qvg.qvg_attention(prm, q, kc, vc, o, base, ws, None, None) == code
+    assert qvg.qvg_attention(None, base, good, good, base, base, big, None, None) == \
+        qvg.QVG_ERR_INVALID_ARG
+    assert qvg.qvg_attention(_ap(), base, good, good, base, None, big, None, None) == \
+        qvg.QVG_ERR_WORKSPACE

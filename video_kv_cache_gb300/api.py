@@ -160,3 +160,45 @@ def dequantize(ckv: CompressedKV, N: int | None = None, out_dtype=torch.bfloat16
     if rc != _c.QVG_OK:
         raise _c.QVGError(rc, "qvg_dequantize")
     return out
+
+
+def attention_params(ckv: CompressedKV, H: int, M: int, N: int, q_dtype, out_dtype, scale: float,
+                     chunk_len: int = 0, k_first: int = 0, v_first: int = 0,
+                     tensor_step: int = 1):
+    return _c.qvg_attention_params(
+        n_heads=H, d=D, M=M, N=N, C=ckv.C if ckv.T > 0 else 0, T=ckv.T, bits=ckv.bits,
+        group=ckv.group, qscheme=ckv.qscheme, chunk_len=chunk_len,
+        token_capacity=ckv.capacity, n_tables=ckv.n_tables, q_dtype=_DT[q_dtype],
+        out_dtype=_DT[out_dtype], scale=scale, k_first=k_first, v_first=v_first,
+        tensor_step=tensor_step)
+
+
+def attention(Q: torch.Tensor, k_cache: CompressedKV, v_cache: CompressedKV | None = None,
+              scale: float | None = None, N: int | None = None, *, out_dtype=torch.float32,
+              chunk_len: int = 0, k_first: int = 0, v_first: int = 0, tensor_step: int = 1,
+              out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+              status: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Softmax attention of Q [H][M][128] over tokens [0, N) of compressed keys and values
+    (qvg_attention): head h reads key tensor k_first + h * tensor_step of ``k_cache`` and
+    value tensor v_first + h * tensor_step of ``v_cache`` (the same cache when omitted).
+    ``scale`` defaults to 1 / sqrt(128)."""
+    v_cache = k_cache if v_cache is None else v_cache
+    assert Q.is_cuda and Q.dim() == 3 and Q.shape[2] == D and Q.is_contiguous()
+    H, M, _ = Q.shape
+    N = k_cache.capacity if N is None else N
+    scale = D ** -0.5 if scale is None else scale
+    if out is None:
+        out = torch.empty((H, M, D), dtype=out_dtype, device=Q.device)
+    assert out.is_contiguous() and out.shape == (H, M, D)
+    prm = attention_params(k_cache, H, M, N, Q.dtype, out.dtype, scale, chunk_len, k_first,
+                           v_first, tensor_step)
+    need = _c.qvg_attention_workspace_bytes(prm)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=Q.device)
+    rc = _c.qvg_attention(prm, Q.data_ptr(), k_cache.buffers(), v_cache.buffers(),
+                          out.data_ptr(), workspace.data_ptr(), workspace.numel(),
+                          status.data_ptr() if status is not None else None,
+                          _stream_handle(stream))
+    if rc != _c.QVG_OK:
+        raise _c.QVGError(rc, "qvg_attention")
+    return out

@@ -292,4 +292,36 @@ struct DPlan {
 };
 cudaError_t launch_dequant(const DPlan &p, int num_sms, cudaStream_t st);
 
+// Attention read straight from two compressed caches (keys and values).
+constexpr int kMaxAttnQ = 16;  // most queries per head
+struct APlan {
+    int H, M;                  // heads, queries per head
+    int64_t N;                 // keys per head
+    int C, T, bits, group, qscheme;
+    int64_t chunk_len, cap;
+    int n_tables;
+    int q_dtype, out_dtype;
+    float scale;
+    int64_t k_first, v_first, step;  // tensor of head h: first + h * step
+    int S;                     // key splits per head
+    int64_t split_len;         // keys per split (a multiple of 32)
+    const void *Q;             // [H][M][d]
+    const uint8_t *kc, *ks, *kp;
+    const float *kcent;
+    const uint8_t *vc, *vs, *vp;
+    const float *vcent;
+    float *part;               // [H][S][M][d] unnormalised partial outputs
+    float *ml;                 // [H][S][M][2] running maximum and weight sum of each split
+    void *O;                   // [H][M][d]
+    uint32_t *status;
+};
+// Keys per split: about N / 128 splits per head and at least 256 keys per split, a multiple
+// of the 32-key tile.  Every split s < S = ceil(N / split_len) holds at least one key.
+inline int64_t attn_split_len(int64_t N) {
+    const int64_t target = std::min<int64_t>(std::max<int64_t>((N + 255) / 256, 1), 128);
+    const int64_t len = (N + target - 1) / target;
+    return (len + 31) / 32 * 32;
+}
+cudaError_t launch_attention(const APlan &p, cudaStream_t st);
+
 }  // namespace qvg

@@ -1,0 +1,257 @@
+// Attention read straight from the compressed cache: keys and values are rebuilt in
+// registers from their codes, scales, cluster indices and centroid tables, used, and
+// dropped, so the reconstructed cache never goes to memory.
+//
+// Method step: the fused reconstruction X^(T) = deQ(X_INT, S_x), X^(t-1) = X^(t) + C^(t)_{pi_i}
+// ("Quant VideoGen" notes page, Algorithm-System Co-design, the fused dequantization that
+// feeds attention on the fly; review page "Quant VideoGen: 基于2-Bit KV缓存量化的自回归长视频生成",
+// pipeline paragraph).  Attention itself is the standard scaled dot-product softmax form:
+// o = sum_j p_j v_j, p = softmax_j(scale * q.k_j).
+//
+// Design (one query block per head, HBM reads of the compressed rows):
+//   * The N keys of a head are cut into S splits (a multiple of 32 keys each, about N / 128
+//     splits and at least 256 keys per split).  One warp takes one split and walks it in
+//     32-key tiles with a running maximum and weight sum per query (online softmax);
+//     k_attn_combine merges the splits of a head.
+//   * A rebuilt row is the value qvg_dequantize writes in fp32: the code's level times the
+//     E4M3 scale, plus the stage-T centroid, then stages T-1 .. 1, each add rounded in fp32.
+//     A lane rebuilds channels 4l .. 4l+3 of a row (one code byte at INT2, one 16-bit word
+//     at INT4, a float4 of each stage's table row).
+//   * Keys: the warp rebuilds the tile's 32 key rows into shared memory (rows padded to 132
+//     floats so that a quarter-warp's 16-byte reads of 8 different rows hit distinct bank
+//     groups); then lane j scores key j against every query (queries in shared memory,
+//     broadcast reads) with 128 sequential fp32 FMAs.
+//   * Values: lane l rebuilds channels 4l .. 4l+3 of each value row of the tile and adds
+//     them, weighted by the key's softmax numerator, into its M x 4 accumulators.
+#include <cuda_fp8.h>
+
+#include <algorithm>
+
+#include "internal.cuh"
+
+namespace qvg {
+
+namespace {
+constexpr int kAttnWarps = 4;   // warps (splits) per CTA
+constexpr int kAttnTile = 32;   // keys per tile
+constexpr int kKRow = 132;      // padded staged key row, floats
+
+__device__ __forceinline__ float e4m3_value(uint32_t b) {
+    const __half_raw h = __nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)b, __NV_E4M3);
+    return __half2float(__half(h));
+}
+
+// Channels 4*lane .. 4*lane+3 of token n of compressed tensor ti, as qvg_dequantize's fp32
+// output has them.
+template <int BITS, int SH>
+__device__ __forceinline__ float4 rebuild4(const APlan &p, const uint8_t *codes,
+                                           const uint8_t *scales, const uint8_t *pi,
+                                           const float *cent, int64_t ti, int64_t n, int lane,
+                                           bool &bad) {
+    constexpr int MID = 1 << (BITS - 1);
+    const int64_t row = ti * p.cap + n;
+    uint32_t cw;
+    if constexpr (BITS == 2)
+        cw = __ldg(codes + row * (kD * BITS / 8) + lane);
+    else
+        cw = __ldg(reinterpret_cast<const unsigned short *>(codes + row * (kD * BITS / 8)) + lane);
+    const float sq = e4m3_value(__ldg(scales + row * (kD / p.group) + (4 * lane) / p.group));
+    float y[4];
+#pragma unroll
+    for (int c = 0; c < 4; c++) {
+        const int u = (int)((cw >> (BITS * c)) & ((1u << BITS) - 1u));
+        // the level times s_q: at most 8 significant bits, exact in fp32
+        const float lv = SH ? __fadd_rn((float)(u - MID), 0.5f) : (float)(u - MID);
+        y[c] = __fmul_rn(sq, lv);
+    }
+    if (p.T > 0) {
+        const int64_t tbl = min(n / p.chunk_len, (int64_t)p.n_tables - 1);
+        const float *tb = cent + (ti * p.n_tables + tbl) * p.T * p.C * kD;
+        for (int t = p.T - 1; t >= 0; t--) {
+            int j = __ldg(pi + (ti * p.T + t) * p.cap + n);
+            if (j >= p.C) {
+                j = p.C - 1;
+                bad = true;
+            }
+            const float4 c4 =
+                __ldg(reinterpret_cast<const float4 *>(tb + ((int64_t)t * p.C + j) * kD) + lane);
+            y[0] = __fadd_rn(y[0], c4.x);
+            y[1] = __fadd_rn(y[1], c4.y);
+            y[2] = __fadd_rn(y[2], c4.z);
+            y[3] = __fadd_rn(y[3], c4.w);
+        }
+    }
+    return make_float4(y[0], y[1], y[2], y[3]);
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+}  // namespace
+
+// grid (ceil(S / kAttnWarps), H), block 32 * kAttnWarps; warp w of CTA x takes split
+// x * kAttnWarps + w of head blockIdx.y.  MQ >= M queries are held (the rest are zero).
+template <int BITS, int SH, int MQ>
+__global__ void __launch_bounds__(32 * kAttnWarps) k_attn_split(APlan p) {
+    pdl_begin();
+    extern __shared__ __align__(16) float sm_attn[];
+    float *sQ = sm_attn;  // [MQ][d]
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    float *sK = sm_attn + MQ * kD + warp * (kAttnTile * kKRow + MQ * kAttnTile);  // [32][132]
+    float *sP = sK + kAttnTile * kKRow;                                         // [MQ][32]
+    const int h = blockIdx.y;
+    for (int x = threadIdx.x; x < MQ * kD; x += blockDim.x) {
+        const int m = x / kD;
+        sQ[x] = m < p.M ? load_x1(p.Q, p.q_dtype, ((int64_t)h * p.M + m) * kD + (x - m * kD)) : 0.f;
+    }
+    __syncthreads();
+    const int s = blockIdx.x * kAttnWarps + warp;
+    if (s >= p.S) return;
+    const int64_t n0 = (int64_t)s * p.split_len;
+    const int64_t n1 = min(p.N, n0 + p.split_len);
+    const int64_t tk = p.k_first + (int64_t)h * p.step, tv = p.v_first + (int64_t)h * p.step;
+
+    float mrun[MQ], lrun[MQ], o[MQ][4];
+#pragma unroll
+    for (int m = 0; m < MQ; m++) {
+        mrun[m] = -INFINITY;
+        lrun[m] = 0.f;
+        o[m][0] = o[m][1] = o[m][2] = o[m][3] = 0.f;
+    }
+    bool bad = false;
+    for (int64_t t0 = n0; t0 < n1; t0 += kAttnTile) {
+        const int cnt = (int)min((int64_t)kAttnTile, n1 - t0);
+        for (int kk = 0; kk < cnt; kk++) {
+            const float4 k4 = rebuild4<BITS, SH>(p, p.kc, p.ks, p.kp, p.kcent, tk, t0 + kk, lane, bad);
+            *reinterpret_cast<float4 *>(sK + kk * kKRow + 4 * lane) = k4;
+        }
+        __syncwarp();
+        float sc[MQ];
+#pragma unroll
+        for (int m = 0; m < MQ; m++) sc[m] = 0.f;
+        if (lane < cnt) {
+            const float4 *kr = reinterpret_cast<const float4 *>(sK + lane * kKRow);
+            for (int c = 0; c < kD / 4; c++) {
+                const float4 kv = kr[c];
+#pragma unroll
+                for (int m = 0; m < MQ; m++) {
+                    const float4 qv = reinterpret_cast<const float4 *>(sQ + m * kD)[c];
+                    sc[m] = __fmaf_rn(qv.x, kv.x, sc[m]);
+                    sc[m] = __fmaf_rn(qv.y, kv.y, sc[m]);
+                    sc[m] = __fmaf_rn(qv.z, kv.z, sc[m]);
+                    sc[m] = __fmaf_rn(qv.w, kv.w, sc[m]);
+                }
+            }
+        }
+#pragma unroll
+        for (int m = 0; m < MQ; m++) {
+            const float sv = lane < cnt ? __fmul_rn(sc[m], p.scale) : -INFINITY;
+            const float mnew = fmaxf(mrun[m], warp_max(sv));  // finite: the tile has a key
+            const float corr = expf(mrun[m] - mnew);            // 0 on the first tile
+            const float pj = expf(sv - mnew);                   // 0 past the tile's keys
+            lrun[m] = __fmaf_rn(lrun[m], corr, warp_sum(pj));
+            mrun[m] = mnew;
+#pragma unroll
+            for (int c = 0; c < 4; c++) o[m][c] = __fmul_rn(o[m][c], corr);
+            sP[m * kAttnTile + lane] = pj;
+        }
+        __syncwarp();
+        for (int kk = 0; kk < cnt; kk++) {
+            const float4 v4 = rebuild4<BITS, SH>(p, p.vc, p.vs, p.vp, p.vcent, tv, t0 + kk, lane, bad);
+#pragma unroll
+            for (int m = 0; m < MQ; m++) {
+                const float w = sP[m * kAttnTile + kk];
+                o[m][0] = __fmaf_rn(w, v4.x, o[m][0]);
+                o[m][1] = __fmaf_rn(w, v4.y, o[m][1]);
+                o[m][2] = __fmaf_rn(w, v4.z, o[m][2]);
+                o[m][3] = __fmaf_rn(w, v4.w, o[m][3]);
+            }
+        }
+        __syncwarp();  // the next tile overwrites sK and sP
+    }
+#pragma unroll
+    for (int m = 0; m < MQ; m++) {
+        if (m < p.M) {
+            const int64_t r = ((int64_t)h * p.S + s) * p.M + m;
+            *reinterpret_cast<float4 *>(p.part + r * kD + 4 * lane) =
+                make_float4(o[m][0], o[m][1], o[m][2], o[m][3]);
+            if (lane == 0) {
+                p.ml[2 * r] = mrun[m];
+                p.ml[2 * r + 1] = lrun[m];
+            }
+        }
+    }
+    if (__any_sync(0xffffffffu, bad) && lane == 0) or_status(p.status, QVG_DEV_BAD_INDEX);
+}
+
+// One warp per (head, query): the splits' partial outputs rescaled to the largest maximum,
+// summed, and divided by the summed weights.  Lane l writes channels 4l .. 4l+3.
+__global__ void __launch_bounds__(256) k_attn_combine(APlan p) {
+    pdl_begin();
+    const int w = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+    if (w >= p.H * p.M) return;
+    const int h = w / p.M, m = w - h * p.M;
+    float mx = -INFINITY;
+    for (int s = lane; s < p.S; s += 32) mx = fmaxf(mx, p.ml[2 * (((int64_t)h * p.S + s) * p.M + m)]);
+    mx = warp_max(mx);
+    float l = 0.f, a[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int s = 0; s < p.S; s++) {
+        const int64_t r = ((int64_t)h * p.S + s) * p.M + m;
+        const float wgt = expf(p.ml[2 * r] - mx);
+        l = __fmaf_rn(wgt, p.ml[2 * r + 1], l);
+        const float4 po = *reinterpret_cast<const float4 *>(p.part + r * kD + 4 * lane);
+        a[0] = __fmaf_rn(wgt, po.x, a[0]);
+        a[1] = __fmaf_rn(wgt, po.y, a[1]);
+        a[2] = __fmaf_rn(wgt, po.z, a[2]);
+        a[3] = __fmaf_rn(wgt, po.w, a[3]);
+    }
+    const int64_t off = ((int64_t)h * p.M + m) * kD + 4 * lane;
+#pragma unroll
+    for (int c = 0; c < 4; c++) {
+        const float v = __fdiv_rn(a[c], l);
+        if (p.out_dtype == DT_F32)
+            static_cast<float *>(p.O)[off + c] = v;
+        else if (p.out_dtype == DT_BF16)
+            static_cast<__nv_bfloat16 *>(p.O)[off + c] = __float2bfloat16_rn(v);
+        else
+            static_cast<__half *>(p.O)[off + c] = __float2half_rn(v);
+    }
+}
+
+namespace {
+template <int BITS, int SH, int MQ>
+cudaError_t launch_split(const APlan &p, cudaStream_t st) {
+    const size_t smem = (size_t)(MQ * kD + kAttnWarps * (kAttnTile * kKRow + MQ * kAttnTile)) * sizeof(float);
+    cudaError_t e = cudaFuncSetAttribute(k_attn_split<BITS, SH, MQ>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    return launch_kernel(k_attn_split<BITS, SH, MQ>,
+                         dim3((unsigned)((p.S + kAttnWarps - 1) / kAttnWarps), p.H),
+                         dim3(32 * kAttnWarps), smem, st, p);
+}
+
+template <int BITS, int SH>
+cudaError_t launch_split_m(const APlan &p, cudaStream_t st) {
+    if (p.M <= 1) return launch_split<BITS, SH, 1>(p, st);
+    if (p.M <= 4) return launch_split<BITS, SH, 4>(p, st);
+    return launch_split<BITS, SH, kMaxAttnQ>(p, st);
+}
+}  // namespace
+
+cudaError_t launch_attention(const APlan &p, cudaStream_t st) {
+    const bool mr = p.qscheme == QVG_QSCHEME_MIDRISE;
+    cudaError_t e = p.bits == 2 ? (mr ? launch_split_m<2, 1>(p, st) : launch_split_m<2, 0>(p, st))
+                                : (mr ? launch_split_m<4, 1>(p, st) : launch_split_m<4, 0>(p, st));
+    if (e != cudaSuccess) return e;
+    return launch_kernel(k_attn_combine, dim3((unsigned)((p.H * p.M + 7) / 8)), dim3(256), 0, st, p);
+}
+
+}  // namespace qvg

@@ -1,6 +1,7 @@
 // C ABI of libqvg: argument checks, workspace layout and the stage / Lloyd-round loop of
-// the quantize path, plus the dequantize entry point.  Declarations and their contracts
+// the quantize path, plus the dequantize and attention entry points.  Declarations and their contracts
 // are in include/qvg.h.
+#include <cmath>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
@@ -392,6 +393,113 @@ qvg_status qvg_dequantize(const qvg_dequant_params *prm, const qvg_buffers *in, 
     p.out = X_hat;
     p.status = dev_status;
     if (launch_dequant(p, num_sms, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return QVG_ERR_CUDA;
+    }
+    return QVG_OK;
+}
+
+namespace {
+qvg_status check_attention(const qvg_attention_params *prm) {
+    if (!prm) return QVG_ERR_INVALID_ARG;
+    if (prm->n_heads < 1 || prm->N < 1 || prm->N >= (int64_t(1) << 31)) return QVG_ERR_INVALID_ARG;
+    if (prm->M < 1 || prm->M > kMaxAttnQ) return QVG_ERR_UNSUPPORTED;
+    if (prm->n_heads > 65535) return QVG_ERR_UNSUPPORTED;  // one grid row per head
+    if (prm->d != kD) return QVG_ERR_UNSUPPORTED;
+    if (prm->bits != 2 && prm->bits != 4) return QVG_ERR_UNSUPPORTED;
+    if (prm->group != 16 && prm->group != 32 && prm->group != 64) return QVG_ERR_UNSUPPORTED;
+    if (prm->qscheme != QVG_QSCHEME_SYMMETRIC && prm->qscheme != QVG_QSCHEME_MIDRISE)
+        return QVG_ERR_UNSUPPORTED;
+    if (prm->T < 0 || prm->T > kMaxT) return QVG_ERR_UNSUPPORTED;
+    if (prm->T > 0 && (prm->C < 1 || prm->C > kMaxC)) return QVG_ERR_UNSUPPORTED;
+    if (prm->q_dtype < QVG_F16 || prm->q_dtype > QVG_F32) return QVG_ERR_UNSUPPORTED;
+    if (prm->out_dtype < QVG_F16 || prm->out_dtype > QVG_F32) return QVG_ERR_UNSUPPORTED;
+    if (!std::isfinite(prm->scale)) return QVG_ERR_INVALID_ARG;
+    if (prm->chunk_len < 0 || prm->token_capacity < 0 || prm->n_tables < 0 ||
+        prm->k_first < 0 || prm->v_first < 0 || prm->tensor_step < 0)
+        return QVG_ERR_INVALID_ARG;
+    const int64_t cap = prm->token_capacity ? prm->token_capacity : prm->N;
+    const int64_t chunk = prm->chunk_len ? prm->chunk_len : prm->N;
+    const int n_tables = prm->n_tables ? prm->n_tables : 1;
+    if (cap < prm->N) return QVG_ERR_INVALID_ARG;
+    if (prm->T > 0 && (prm->N + chunk - 1) / chunk > n_tables) return QVG_ERR_INVALID_ARG;
+    return QVG_OK;
+}
+
+struct AttnWs {
+    size_t part, ml, total;
+};
+
+AttnWs attn_layout(const qvg_attention_params *prm) {
+    const int64_t L = attn_split_len(prm->N);
+    const int64_t S = (prm->N + L - 1) / L;
+    const size_t rows = (size_t)prm->n_heads * S * prm->M;
+    AttnWs w{};
+    w.part = 0;
+    w.ml = (rows * kD * sizeof(float) + 255) / 256 * 256;
+    w.total = w.ml + (rows * 2 * sizeof(float) + 255) / 256 * 256;
+    return w;
+}
+}  // namespace
+
+size_t qvg_attention_workspace_bytes(const qvg_attention_params *prm) {
+    if (check_attention(prm) != QVG_OK) return 0;
+    return attn_layout(prm).total;
+}
+
+qvg_status qvg_attention(const qvg_attention_params *prm, const void *Q,
+                         const qvg_buffers *k_cache, const qvg_buffers *v_cache, void *O,
+                         void *workspace, size_t ws_bytes, uint32_t *dev_status, void *stream) {
+    qvg_status rc = check_attention(prm);
+    if (rc != QVG_OK) return rc;
+    if (!Q || !O || !k_cache || !v_cache) return QVG_ERR_INVALID_ARG;
+    for (const qvg_buffers *b : {k_cache, v_cache}) {
+        if (!b->codes || !b->scales) return QVG_ERR_INVALID_ARG;
+        if (prm->T > 0 && (!b->pi || !b->centroids)) return QVG_ERR_INVALID_ARG;
+        if (!aligned16(b->codes) || !aligned16(b->scales) || (prm->T > 0 && !aligned16(b->centroids)))
+            return QVG_ERR_INVALID_ARG;
+    }
+    if (!aligned16(Q) || !aligned16(O)) return QVG_ERR_INVALID_ARG;
+    const AttnWs w = attn_layout(prm);
+    if (!workspace || ws_bytes < w.total || !aligned16(workspace)) return QVG_ERR_WORKSPACE;
+    int num_sms = 0;
+    rc = device_info(&num_sms);
+    if (rc != QVG_OK) return rc;
+    APlan p{};
+    p.H = prm->n_heads;
+    p.M = prm->M;
+    p.N = prm->N;
+    p.C = prm->T > 0 ? prm->C : 1;
+    p.T = prm->T;
+    p.bits = prm->bits;
+    p.group = prm->group;
+    p.qscheme = prm->qscheme;
+    p.chunk_len = prm->chunk_len ? prm->chunk_len : prm->N;
+    p.cap = prm->token_capacity ? prm->token_capacity : prm->N;
+    p.n_tables = prm->n_tables ? prm->n_tables : 1;
+    p.q_dtype = prm->q_dtype;
+    p.out_dtype = prm->out_dtype;
+    p.scale = prm->scale;
+    p.k_first = prm->k_first;
+    p.v_first = prm->v_first;
+    p.step = prm->tensor_step;
+    p.split_len = attn_split_len(prm->N);
+    p.S = (int)((prm->N + p.split_len - 1) / p.split_len);
+    p.Q = Q;
+    p.kc = k_cache->codes;
+    p.ks = k_cache->scales;
+    p.kp = k_cache->pi;
+    p.kcent = k_cache->centroids;
+    p.vc = v_cache->codes;
+    p.vs = v_cache->scales;
+    p.vp = v_cache->pi;
+    p.vcent = v_cache->centroids;
+    unsigned char *ws = static_cast<unsigned char *>(workspace);
+    p.part = reinterpret_cast<float *>(ws + w.part);
+    p.ml = reinterpret_cast<float *>(ws + w.ml);
+    p.O = O;
+    p.status = dev_status;
+    if (launch_attention(p, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
         (void)cudaGetLastError();
         return QVG_ERR_CUDA;
     }

@@ -82,6 +82,29 @@ class qvg_dequant_params(ctypes.Structure):
     ]
 
 
+class qvg_attention_params(ctypes.Structure):
+    _fields_ = [
+        ("n_heads", ctypes.c_int32),
+        ("d", ctypes.c_int32),
+        ("M", ctypes.c_int32),
+        ("N", ctypes.c_int64),
+        ("C", ctypes.c_int32),
+        ("T", ctypes.c_int32),
+        ("bits", ctypes.c_int32),
+        ("group", ctypes.c_int32),
+        ("qscheme", ctypes.c_int32),
+        ("chunk_len", ctypes.c_int64),
+        ("token_capacity", ctypes.c_int64),
+        ("n_tables", ctypes.c_int32),
+        ("q_dtype", ctypes.c_int32),
+        ("out_dtype", ctypes.c_int32),
+        ("scale", ctypes.c_float),
+        ("k_first", ctypes.c_int64),
+        ("v_first", ctypes.c_int64),
+        ("tensor_step", ctypes.c_int64),
+    ]
+
+
 # Every symbol include/qvg.h declares, with its ctypes signature.
 SIGNATURES = {
     "qvg_quantize_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(qvg_quant_params)]),
@@ -98,6 +121,11 @@ SIGNATURES = {
     "qvg_dequantize": (ctypes.c_int, [ctypes.POINTER(qvg_dequant_params),
                                       ctypes.POINTER(qvg_buffers), ctypes.c_void_p,
                                       ctypes.c_void_p, ctypes.c_void_p]),
+    "qvg_attention_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(qvg_attention_params)]),
+    "qvg_attention": (ctypes.c_int, [ctypes.POINTER(qvg_attention_params), ctypes.c_void_p,
+                                     ctypes.POINTER(qvg_buffers), ctypes.POINTER(qvg_buffers),
+                                     ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t,
+                                     ctypes.c_void_p, ctypes.c_void_p]),
     "qvg_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "qvg_version": (ctypes.c_uint32, []),
 }
@@ -163,6 +191,17 @@ def qvg_dequantize(params: qvg_dequant_params, inp: qvg_buffers, X_hat: int,
                    dev_status: int | None, stream: int | None) -> int:
     return int(load().qvg_dequantize(_ref(params), _ref(inp), X_hat,
                                      dev_status, stream))
+
+
+def qvg_attention_workspace_bytes(params: qvg_attention_params) -> int:
+    return int(load().qvg_attention_workspace_bytes(_ref(params)))
+
+
+def qvg_attention(params: qvg_attention_params, Q: int, k_cache: qvg_buffers,
+                  v_cache: qvg_buffers, O: int, workspace: int | None, workspace_bytes: int,
+                  dev_status: int | None, stream: int | None) -> int:
+    return int(load().qvg_attention(_ref(params), Q, _ref(k_cache), _ref(v_cache), O,
+                                    workspace, workspace_bytes, dev_status, stream))
 
 
 def qvg_status_string(code: int) -> str:
