@@ -150,6 +150,15 @@ def dequant_bytes(H, N, C, T, bits, group, out_bytes=2, n_tables=1):
     return H * (N * per_tok + tables)
 
 
+def attention_bytes(heads, N, C, T, bits, group, M, q_bytes=2, out_bytes=4):
+    """Algorithmic bytes of one qvg_attention launch: the codes, scales and pi of N keys and
+    N values per head, each tensor's centroid tables once, the queries read and the outputs
+    written."""
+    per_tok = 128 * bits / 8 + 128 / group + T
+    tables = T * C * 128 * 4
+    return 2 * heads * (N * per_tok + tables) + heads * M * 128 * (q_bytes + out_bytes)
+
+
 def assign_flops(H, N, C):
     """Useful flops of one assignment launch over H tensors: the [N x 128] x [128 x C]
     product per tensor (the GEMM issues twice as many: one fp16 plane of the residual
@@ -573,6 +582,77 @@ def run_presets(args):
                       "data": "synthetic", "rows": rows}), flush=True)
 
 
+def run_attention(args):
+    """Attention of a few queries per head over the 1.3B layer's compressed cache (12 heads,
+    keys and values interleaved, 32760 tokens), read straight from the compressed tensors
+    (qvg_attention), against two paths that materialise the cache: torch's
+    scaled_dot_product_attention over bf16 keys and values already in memory, and the fused
+    dequant to bf16 followed by it.  CUDA events on the launching stream, L2 flushed before
+    every repetition; the compressed cache (about 36 MB) would otherwise stay in L2."""
+    from video_kv_cache_gb300 import api, qvg
+    from video_kv_cache_gb300 import build as qbuild
+    torch.cuda.set_device(0)
+    qbuild.build()
+    qvg.load()
+    w = synth.workload(DEFAULT_WORKLOAD)
+    dev = torch.device("cuda")
+    X = w.make(dev)
+    H, N = X.shape[:2]
+    heads = H // 2
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    ckv = api.quantize(X, w.C, w.T, w.bits, w.group, w.iters, w.seed, status=status)
+    Xh = torch.empty((H, N, 128), dtype=torch.bfloat16, device=dev)
+    api.dequantize(ckv, N, torch.bfloat16, out=Xh, status=status)
+    K, V = Xh[0::2], Xh[1::2]
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    st = torch.cuda.current_stream()
+    hbm, _, _, src = _peaks()
+    reps = max(3, args.steps)
+    rows = []
+    for M in (1, 4, 16):
+        g = torch.Generator(device="cpu").manual_seed(M)
+        Q = torch.randn((heads, M, 128), generator=g).to(torch.bfloat16).to(dev)
+        O = torch.empty((heads, M, 128), dtype=torch.float32, device=dev)
+        prm = api.attention_params(ckv, heads, M, N, Q.dtype, O.dtype, 128 ** -0.5,
+                                   k_first=0, v_first=1, tensor_step=2)
+        ws = torch.empty(max(qvg.qvg_attention_workspace_bytes(prm), 256), dtype=torch.uint8,
+                         device=dev)
+
+        def ours():
+            api.attention(Q, ckv, N=N, k_first=0, v_first=1, tensor_step=2, out=O,
+                          workspace=ws, status=status)
+
+        def sdpa():
+            return torch.nn.functional.scaled_dot_product_attention(Q, K, V)
+
+        def dq_sdpa():
+            api.dequantize(ckv, N, torch.bfloat16, out=Xh, status=status)
+            return torch.nn.functional.scaled_dot_product_attention(Q, Xh[0::2], Xh[1::2])
+
+        for f in (ours, sdpa, dq_sdpa):
+            f()
+        torch.cuda.synchronize()
+        ref = torch.nn.functional.scaled_dot_product_attention(Q.float(), K.float(), V.float())
+        err = float((O - ref).abs().max() / V.float().abs().max())
+        t_ours = _event_ms(st, ours, reps, flush)
+        t_sdpa = _event_ms(st, sdpa, reps, flush)
+        t_dq = _event_ms(st, dq_sdpa, reps, flush)
+        nb = attention_bytes(heads, N, w.C, w.T, w.bits, w.group, M)
+        rows.append({"queries_per_head": M, "attention_us": 1e3 * t_ours,
+                     "gkeys_per_s": heads * N / (t_ours * 1e-3) / 1e9,
+                     "algorithmic_bytes": nb, "gb_s": nb / (t_ours * 1e-3) / 1e9,
+                     "hbm_frac": nb / (t_ours * 1e-3) / 1e9 / hbm,
+                     "sdpa_bf16_us": 1e3 * t_sdpa, "dequant_then_sdpa_us": 1e3 * t_dq,
+                     "max_err_vs_bf16_cache_over_max_v": err})
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0, "device status %#x" % int(status.item())
+    print(json.dumps({"metric": "attention over the compressed cache", "workload": w.name,
+                      "heads": heads, "keys": N, "C": w.C, "T": w.T, "bits": w.bits,
+                      "group": w.group, "peak_hbm_gbs": hbm, "peak_source": src,
+                      "l2": "flushed before every repetition", "data": "synthetic",
+                      "rows": rows}), flush=True)
+
+
 def run_stream(args):
     """The streaming workload: 60 chunks of 3 frames x 30x52 tokens appended to the caches
     of 30 layers x 12 heads x K/V (720 tensors).  Chunk 0 is clustered from a cold start,
@@ -689,9 +769,13 @@ def main():
                     help="run the 60-chunk streaming workload and print its line")
     ap.add_argument("--presets", action="store_true",
                     help="report the two named settings (time, MSE reduction, compression)")
+    ap.add_argument("--attention", action="store_true",
+                    help="time attention read straight from the compressed cache")
     args = ap.parse_args()
     w = synth.workload(args.workload)
-    if args.sweep:
+    if args.attention:
+        run_attention(args)
+    elif args.sweep:
         run_sweep(args)
     elif args.stream:
         run_stream(args)

@@ -5,6 +5,9 @@
     (INT2, B = 32, T = 2, C = 256) that is 294 B per token plus 8 B of tables amortised over
     32760 tokens, 302 B/token in all.
   * Useful assignment flops: 2 N C d per tensor.
+  * Attention over the compressed cache: per key, the key's and the value's codes, scales
+    and pi bytes (2 x 38 B at INT2, B = 32, T = 2), each tensor's tables once, the queries
+    read and the outputs written.
   * Launches per step: one seeded start, per stage four setup kernels and seven per Lloyd
     round, the encode and the fused dequant: 151 for the 1.3B layer, the count of the ncu
     launch list of one bench step.
@@ -41,3 +44,15 @@ def test_launches_per_step():
     assert bench.launches_per_step(w) == 151
     w4 = synth.workload("dit13b_65536")
     assert bench.launches_per_step(w4) == 1 + 4 * (4 + 7 * 8) + 2
+
+
+def test_attention_bytes_of_the_1p3b_layer():
+    w = synth.workload("layer_1p3b_32760")
+    heads, N = w.H // 2, w.N
+    b = bench.attention_bytes(heads, N, w.C, w.T, w.bits, w.group, 1)
+    per_key = 2 * (32 + 4 + 2)
+    assert per_key == 76
+    assert b == heads * (N * per_key + 2 * 2 * 256 * 128 * 4) + heads * 128 * (2 + 4)
+    # more queries only add their own rows
+    assert bench.attention_bytes(heads, N, w.C, w.T, w.bits, w.group, 16) - b == \
+        heads * 15 * 128 * 6
