@@ -273,7 +273,10 @@ qvg_status qvg_attention(const qvg_attention_params *params, const void *Q,
 /* Static description of a status code. */
 const char *qvg_status_string(qvg_status status);
 
-/* Library version, (major << 16) | minor. */
+/* Library version, (major << 16) | minor.
+ *   1.0  quantize, reassign, dequantize, the static-scratch quantize.
+ *   1.1  qvg_quant_params.qscheme and .centroid_format, qvg_dequant_params.qscheme (both
+ *        structs grew: rebuild callers), qvg_attention. */
 uint32_t qvg_version(void);
 
 #ifdef __cplusplus

@@ -89,7 +89,7 @@ def _qp(**kw):
 def test_status_strings(lib):
     for code in range(6):
         assert qvg.qvg_status_string(code)
-    assert qvg.qvg_version() >> 16 == 1
+    assert qvg.qvg_version() == (1 << 16) | 1
 
 
 def test_workspace_bytes(lib):

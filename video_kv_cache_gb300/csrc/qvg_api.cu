@@ -520,6 +520,6 @@ const char *qvg_status_string(qvg_status s) {
     return "unknown status";
 }
 
-uint32_t qvg_version(void) { return (1u << 16) | 0u; }
+uint32_t qvg_version(void) { return (1u << 16) | 1u; }
 
 }  // extern "C"
