@@ -201,3 +201,11 @@ def test_attention_rejects_bad_arguments(lib):
         qvg.QVG_ERR_INVALID_ARG
     assert qvg.qvg_attention(_ap(), base, good, good, base, None, big, None, None) == \
         qvg.QVG_ERR_WORKSPACE
+
+
+def test_attention_layout_defaults():
+    from video_kv_cache_gb300 import api
+    assert api.attention_layout(True) == (0, 1, 2)
+    assert api.attention_layout(False) == (0, 0, 1)
+    assert api.attention_layout(True, 4, 5, 6) == (4, 5, 6)
+    assert api.attention_layout(False, v_first=3) == (0, 3, 1)

@@ -173,15 +173,27 @@ def attention_params(ckv: CompressedKV, H: int, M: int, N: int, q_dtype, out_dty
         tensor_step=tensor_step)
 
 
+def attention_layout(one_cache: bool, k_first=None, v_first=None, tensor_step=None):
+    """(k_first, v_first, tensor_step) with the defaults of ``attention`` filled in: keys and
+    values interleaved in one cache (0, 1, 2), or tensor h of each of two caches (0, 0, 1)."""
+    return (0 if k_first is None else k_first,
+            (1 if one_cache else 0) if v_first is None else v_first,
+            (2 if one_cache else 1) if tensor_step is None else tensor_step)
+
+
 def attention(Q: torch.Tensor, k_cache: CompressedKV, v_cache: CompressedKV | None = None,
               scale: float | None = None, N: int | None = None, *, out_dtype=torch.float32,
-              chunk_len: int = 0, k_first: int = 0, v_first: int = 0, tensor_step: int = 1,
-              out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
-              status: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+              chunk_len: int = 0, k_first: int | None = None, v_first: int | None = None,
+              tensor_step: int | None = None, out: torch.Tensor | None = None,
+              workspace: torch.Tensor | None = None, status: torch.Tensor | None = None,
+              stream=None) -> torch.Tensor:
     """Softmax attention of Q [H][M][128] over tokens [0, N) of compressed keys and values
     (qvg_attention): head h reads key tensor k_first + h * tensor_step of ``k_cache`` and
-    value tensor v_first + h * tensor_step of ``v_cache`` (the same cache when omitted).
-    ``scale`` defaults to 1 / sqrt(128)."""
+    value tensor v_first + h * tensor_step of ``v_cache``.  With one cache (``v_cache``
+    omitted) the default layout is keys and values interleaved, tensors 2h and 2h + 1; with
+    two caches it is tensor h of each.  ``scale`` defaults to 1 / sqrt(128)."""
+    k_first, v_first, tensor_step = attention_layout(v_cache is None, k_first, v_first,
+                                                     tensor_step)
     v_cache = k_cache if v_cache is None else v_cache
     assert Q.is_cuda and Q.dim() == 3 and Q.shape[2] == D and Q.is_contiguous()
     H, M, _ = Q.shape
