@@ -178,7 +178,7 @@ def launches_per_step(w):
 # DRAM traffic of one k_assign launch on layer_1p3b_32760 (dram__bytes_read.sum +
 # dram__bytes_write.sum, ncu), valid while the kernel's sources hash to `sources_sha256`.
 ASSIGN_TRAFFIC = {"workload": "layer_1p3b_32760", "bytes": 217287424,
-                  "sources_sha256": "73e342b8456225c4a9099f14d17d7b914025e13d2df8537f496bbd3c726c5dd3"}
+                  "sources_sha256": "680b180614a7106ce8cae076bdb6dc7c5777bf7a184d6763313f4163a6f08d4f"}
 ASSIGN_SOURCES = ("video_kv_cache_gb300/csrc/k_assign.cu", "video_kv_cache_gb300/csrc/internal.cuh")
 
 
