@@ -31,25 +31,33 @@ _i64p = np.ctypeslib.ndpointer(np.int64, flags="C_CONTIGUOUS")
 _u8p = np.ctypeslib.ndpointer(np.uint8, flags="C_CONTIGUOUS")
 
 
+def compile_source(src: str, so: str) -> str:
+    """Compile a C source of the oracle into the shared library `so` (ISO C11, no FP
+    contraction, the flags every build of the oracle uses)."""
+    tmp = so + ".%d.tmp" % os.getpid()
+    cmd = ["gcc", "-std=c11", "-D_POSIX_C_SOURCE=200809L", "-O2", "-ffp-contract=off",
+           "-fPIC", "-shared", "-pthread", src, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, so)
+    return so
+
+
 def build(force: bool = False) -> str:
-    """Compile the oracle with gcc (ISO C11, no FP contraction) and return the .so path."""
+    """Compile the oracle and return the .so path."""
     if not force and os.path.exists(_SO) and os.path.getmtime(_SO) >= os.path.getmtime(_SRC):
         return _SO
     os.makedirs(_BUILD, exist_ok=True)
-    tmp = _SO + ".%d.tmp" % os.getpid()
-    cmd = ["gcc", "-std=c11", "-D_POSIX_C_SOURCE=200809L", "-O2", "-ffp-contract=off",
-           "-fPIC", "-shared", "-pthread", _SRC, "-o", tmp, "-lm"]
-    subprocess.run(cmd, check=True)
-    os.replace(tmp, _SO)
-    return _SO
+    return compile_source(_SRC, _SO)
 
 
 def _load():
+    """The oracle library.  QVG_ORACLE_LIB, if set, names a prebuilt copy to load instead:
+    the planted-mistake tests use it to run the pins against a mutated oracle."""
     global _lib
     with _lock:
         if _lib is not None:
             return _lib
-        lib = ctypes.CDLL(build())
+        lib = ctypes.CDLL(os.environ.get("QVG_ORACLE_LIB") or build())
         c = ctypes
         lib.orc_e4m3_decode.restype = c.c_double
         lib.orc_e4m3_decode.argtypes = [c.c_uint8]

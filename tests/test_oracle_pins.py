@@ -265,6 +265,28 @@ def test_T0_is_plain_group_rtn(bits, group):
     assert np.array_equal(unpacked.reshape(300, 128), ref_u)
 
 
+@pytest.mark.parametrize("bits,group", [(2, 32), (4, 16)])
+def test_T0_rtn_where_the_clamp_decides(bits, group):
+    # Groups whose scale saturates at 448 (|r| in the thousands) and, at INT4, groups whose
+    # scale falls among the subnormal E4M3 values and rounds down: there the nearest level
+    # lies past qmax and the clamp decides the code.
+    rng = np.random.default_rng(bits * 7 + group)
+    mag = rng.choice([1e-2, 1.3e-2, 1.7e-2, 1.0, 2e3, 5e3], size=(400, 1))
+    X = _bf16_round(rng.standard_normal((400, 128)) * mag)
+    codes, scales = oracle.encode(X, bits, group)
+    ref_s, ref_u, sq = _rtn_reference(X, bits, group)
+    assert np.array_equal(scales, ref_s)
+    per = 8 // bits
+    unpacked = np.stack([(codes >> (bits * k)) & (2 ** bits - 1) for k in range(per)],
+                        axis=2).reshape(400, 128)
+    assert np.array_equal(unpacked, ref_u)
+    qmax, mid = 2 ** (bits - 1) - 1, 2 ** (bits - 1)
+    assert unpacked.min() >= mid - qmax and unpacked.max() <= mid + qmax
+    with np.errstate(divide="ignore", invalid="ignore"):
+        ratio = np.abs(X.reshape(400, 128 // group, group)) / sq[..., None]
+    assert (ratio > qmax + 0.5).any()  # the case is exercised
+
+
 def test_code_packing_layout():
     # one token, d=16, INT2, group 16: values on the grid of scale 1.0 (E4M3 0x38)
     r = np.array([[1, 0, -1, 1, 0, 0, 1, -1, -1, -1, 0, 1, 1, 1, 1, 0]], np.float64)
