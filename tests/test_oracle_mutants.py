@@ -4,13 +4,15 @@ Each mutant is a copy of oracle/qvg_oracle.c with one plausible mistake: a flipp
 dropped or extra term, a wrong index, constant or rounding rule.  The oracle's pins (the
 CPU test files listed in PINS) run against every mutant through QVG_ORACLE_LIB and must
 fail; an unmodified copy built the same way must pass.  A mutant that no pin catches is a
-gap in the pins.  The mistakes are planted only in these copies, on the CPU.
+gap in the pins.  The attention oracle's mutants are numpy functions swapped in for it while
+its pins run.  The mistakes are planted only in these copies, on the CPU.
 """
 import concurrent.futures
 import os
 import subprocess
 import sys
 
+import numpy as np
 import pytest
 
 import oracle
@@ -100,3 +102,57 @@ def test_pins_catch_the_planted_mistake(results, name):
     r = results[name]
     # exit code 1: tests ran and one failed (not a crash, usage error or empty run)
     assert r.returncode == 1, "mutant %s: exit %d\n%s" % (name, r.returncode, r.stdout[-3000:])
+
+
+# Planted mistakes in the attention oracle (numpy): each replaces oracle.attention.attention
+# in this process while its pins run.
+def _attn_no_shift(Q, K, V, scale):
+    P = np.exp(float(scale) * (np.asarray(Q, float) @ np.asarray(K, float).T))
+    return (P @ V) / P.sum(axis=1, keepdims=True)
+
+
+def _attn_no_scale(Q, K, V, scale):
+    S = np.asarray(Q, float) @ np.asarray(K, float).T
+    P = np.exp(S - S.max(axis=1, keepdims=True))
+    return (P @ V) / P.sum(axis=1, keepdims=True)
+
+
+def _attn_keys_as_values(Q, K, V, scale):
+    S = float(scale) * (np.asarray(Q, float) @ np.asarray(K, float).T)
+    P = np.exp(S - S.max(axis=1, keepdims=True))
+    return (P @ K) / P.sum(axis=1, keepdims=True)
+
+
+def _attn_mean_not_weight_sum(Q, K, V, scale):
+    S = float(scale) * (np.asarray(Q, float) @ np.asarray(K, float).T)
+    P = np.exp(S - S.max(axis=1, keepdims=True))
+    return (P @ V) / P.shape[1]
+
+
+def _attn_shift_per_key(Q, K, V, scale):
+    S = float(scale) * (np.asarray(Q, float) @ np.asarray(K, float).T)
+    P = np.exp(S - S.max(axis=0, keepdims=True))
+    return (P @ V) / P.sum(axis=1, keepdims=True)
+
+
+ATTENTION_MUTANTS = [_attn_no_shift, _attn_no_scale, _attn_keys_as_values,
+                     _attn_mean_not_weight_sum, _attn_shift_per_key]
+
+
+@pytest.mark.parametrize("mutant", ATTENTION_MUTANTS, ids=lambda f: f.__name__[6:])
+def test_attention_pins_catch_the_planted_mistake(monkeypatch, mutant):
+    from oracle import attention as oatt
+    from tests import test_attention_oracle as pins
+    monkeypatch.setattr(oatt, "attention", mutant)
+    runs = [(pins.test_matches_torch_sdpa_in_fp64, (M, N)) for M, N in ((1, 1), (3, 50), (16, 700))]
+    runs += [(pins.test_one_key_gives_its_value, ()), (pins.test_equal_scores_give_the_mean_value, ()),
+             (pins.test_a_leading_key_takes_all_the_weight, ()), (pins.test_invariances, ()),
+             (pins.test_exact_cache_gives_attention_over_x, ())]
+    failed = 0
+    for fn, args in runs:
+        try:
+            with np.errstate(all="ignore"):
+                fn(*args)
+        except (AssertionError, ValueError, FloatingPointError):
+            failed += 1
+    assert failed > 0, mutant.__name__
