@@ -64,6 +64,16 @@ MUTANTS = [
     ("bfloat16_emin", "orc_round_p(v, 8, -126, ldexp(255.0, 120))",
      "orc_round_p(v, 8, -125, ldexp(255.0, 120))"),
     ("store_ties_away", "double r = nearbyint(fabs(x) / q) * q;", "double r = round(fabs(x) / q) * q;"),
+    ("stage_residual_not_updated", "orc_subtract(R, N, d, p, c); /* R^(t) */", "(void)0;"),
+    ("warm_table_of_stage_1_for_all", "const float *w = warm + (int64_t)(t - 1) * C * d;",
+     "const float *w = warm;"),
+    ("cold_start_rows_of_x", "c[(int64_t)j * d + k] = orc_store(R[idx[j] * d + k],",
+     "c[(int64_t)j * d + k] = orc_store(X[idx[j] * d + k],"),
+    ("pi_of_every_stage_in_slot_1", "pi[(int64_t)(t - 1) * N + i] = (uint8_t)p[i];",
+     "pi[i] = (uint8_t)p[i];"),
+    ("encodes_x_not_the_residual", "orc_encode(R, N, d, cfg->bits", "orc_encode(X, N, d, cfg->bits"),
+    ("packing_order_reversed", "(uint8_t)(u << ((k * bits) % 8));",
+     "(uint8_t)(u << (8 - bits - (k * bits) % 8));"),
 ]
 
 

@@ -287,6 +287,20 @@ def test_T0_rtn_where_the_clamp_decides(bits, group):
     assert (ratio > qmax + 0.5).any()  # the case is exercised
 
 
+def test_each_stage_starts_from_seeded_rows_of_its_input():
+    # With one Lloyd round, a seeded row sits at distance ~0 (its fp32 rounding) from its own
+    # starting centroid and far from the others, so it stays in that cluster: at every stage
+    # pi^(t)[idx_j] = j, where idx are the stage's seeded indices and the starting centroids
+    # are those rows of the stage input R^(t-1).
+    rng = np.random.default_rng(12)
+    X = _bf16_round(rng.standard_normal((1, 600, 128)) * 2 + rng.standard_normal(128) * 5)
+    C, T, seed = 24, 3, 77
+    ref = oracle.quantize(X, C, T, 2, 32, 1, seed)
+    for t in range(1, T + 1):
+        idx = oracle.init_indices(seed, 0, t, 600, C)
+        assert np.array_equal(ref["pi"][0][t - 1][idx], np.arange(C)), t
+
+
 def test_code_packing_layout():
     # one token, d=16, INT2, group 16: values on the grid of scale 1.0 (E4M3 0x38)
     r = np.array([[1, 0, -1, 1, 0, 0, 1, -1, -1, -1, 0, 1, 1, 1, 1, 0]], np.float64)
