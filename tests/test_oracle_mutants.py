@@ -74,6 +74,12 @@ MUTANTS = [
     ("encodes_x_not_the_residual", "orc_encode(R, N, d, cfg->bits", "orc_encode(X, N, d, cfg->bits"),
     ("packing_order_reversed", "(uint8_t)(u << ((k * bits) % 8));",
      "(uint8_t)(u << (8 - bits - (k * bits) % 8));"),
+    ("e4m3_drops_sign", "return sign ? -v : v;", "return v;"),
+    ("one_lloyd_round_short", "for (int it = 0; it < iters; it++) {",
+     "for (int it = 1; it < iters; it++) {"),
+    ("midrise_no_upper_clamp", "if (f > 2 * mid - 1) f = 2 * mid - 1;", ""),
+    ("store_no_overflow", "if (r > maxfinite) r = INFINITY;", ""),
+    ("tensor_id_ignored", "c, jb->tensor_id_base + h, jb->X", "c, jb->tensor_id_base, jb->X"),
 ]
 
 

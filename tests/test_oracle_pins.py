@@ -301,6 +301,21 @@ def test_each_stage_starts_from_seeded_rows_of_its_input():
         assert np.array_equal(ref["pi"][0][t - 1][idx], np.arange(C)), t
 
 
+def test_batch_equals_independent_tensors():
+    # tensors of a batch are independent problems: tensor h of a batch is the single-tensor
+    # call with tensor id h (its own seeded start), whatever else shares the batch
+    rng = np.random.default_rng(13)
+    X = _bf16_round(rng.standard_normal((3, 300, 128)) * 2 + rng.standard_normal((3, 1, 128)))
+    ref = oracle.quantize(X, 16, 2, 2, 32, 2, 5)
+    for h in range(3):
+        one = oracle.quantize(X[h:h + 1], 16, 2, 2, 32, 2, 5, tensor_id_base=h)
+        for k in ("codes", "scales", "pi", "centroids"):
+            assert np.array_equal(ref[k][h], one[k][0]), (h, k)
+    # and the seeded starts differ between tensor ids
+    assert not np.array_equal(oracle.init_indices(5, 0, 1, 300, 16),
+                              oracle.init_indices(5, 1, 1, 300, 16))
+
+
 def test_code_packing_layout():
     # one token, d=16, INT2, group 16: values on the grid of scale 1.0 (E4M3 0x38)
     r = np.array([[1, 0, -1, 1, 0, 0, 1, -1, -1, -1, 0, 1, 1, 1, 1, 0]], np.float64)
