@@ -315,8 +315,8 @@ struct APlan {
     void *O;                   // [H][M][d]
     uint32_t *status;
 };
-// Keys per split: about N / 128 splits per head and at least 256 keys per split, a multiple
-// of the 32-key tile.  Every split s < S = ceil(N / split_len) holds at least one key.
+// Keys per split: the N keys of a head in min(ceil(N / 256), 128) parts, each rounded up to a
+// multiple of the 32-key tile.  Every split s < S = ceil(N / split_len) holds a key.
 inline int64_t attn_split_len(int64_t N) {
     const int64_t target = std::min<int64_t>(std::max<int64_t>((N + 255) / 256, 1), 128);
     const int64_t len = (N + target - 1) / target;

@@ -9,10 +9,11 @@
 // o = sum_j p_j v_j, p = softmax_j(scale * q.k_j).
 //
 // Design (one query block per head, HBM reads of the compressed rows):
-//   * The N keys of a head are cut into S splits (a multiple of 32 keys each, about N / 128
-//     splits and at least 256 keys per split).  One warp takes one split and walks it in
-//     32-key tiles with a running maximum and weight sum per query (online softmax);
-//     k_attn_combine merges the splits of a head.
+//   * The N keys of a head are cut into S = min(ceil(N / 256), 128) splits of equal length
+//     rounded up to a multiple of 32 keys (at most 256 keys up to N = 32768, longer splits
+//     beyond).  One warp takes one split and walks it in 32-key tiles with a running
+//     maximum and weight sum per query (online softmax); k_attn_combine merges the splits
+//     of a head.
 //   * A rebuilt row is the value qvg_dequantize writes in fp32: the code's level times the
 //     E4M3 scale, plus the stage-T centroid, then stages T-1 .. 1, each add rounded in fp32.
 //     A lane rebuilds channels 4l .. 4l+3 of a row (one code byte at INT2, one 16-bit word
