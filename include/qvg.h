@@ -95,8 +95,9 @@ typedef enum { QVG_QSCHEME_SYMMETRIC = 0, QVG_QSCHEME_MIDRISE = 1 } qvg_qscheme;
  *   QVG_CENTROIDS_F32:  the fp32 mean (the default).
  *   QVG_CENTROIDS_F16:  IEEE binary16; QVG_CENTROIDS_BF16: bfloat16.  The cluster mean, a
  *     cold-start row and a warm-start value are each rounded once to nearest even in the
- *     format (the mean is carried to about twice fp32's precision, so the rounding is that
- *     of the exact mean save within about 2^-40 relative of a tie).
+ *     format.  The mean is carried to about twice fp32's precision, so it rounds as the
+ *     exact mean of the stage's fp32 inputs does, save within about 2^-40 relative of a
+ *     tie (from the second stage on, those inputs are the fp32 residuals).
  * Quant VideoGen explainer page, compression and metadata overhead: the ratios it prints
  * count centroids in a 16-bit format. */
 typedef enum { QVG_CENTROIDS_F32 = 0, QVG_CENTROIDS_F16 = 1, QVG_CENTROIDS_BF16 = 2 }
