@@ -24,13 +24,6 @@ def case():
     return X, ref
 
 
-def _mismatch_outside_band(R, codes, scales, bits, group):
-    """Index (token, channel) of an element whose code is not in a rounding band."""
-    res = qc.compare_codes(R, codes, scales, bits, group)
-    assert res["code_mismatch"] == 0
-    return 5, 7
-
-
 def test_compare_codes(case):
     X, ref = case
     R = oracle.residual(X[0], ref["pi"][0], ref["centroids"][0], 2)

@@ -13,7 +13,6 @@ Pins:
   * The accounting equals the bytes of the buffers the library actually allocates.
 """
 import pytest
-import torch
 
 from video_kv_cache_gb300 import api
 from video_kv_cache_gb300.presets import PRESETS, cache_bytes, storage_bits
