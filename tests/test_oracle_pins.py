@@ -397,3 +397,25 @@ def test_warm_start_uses_the_given_centroids():
     # and 0 iterations are not allowed: iters >= 1 always re-assigns
     with pytest.raises(ValueError):
         oracle.quantize(X, C=8, T=2, bits=2, group=32, iters=0, seed=1)
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
+def test_decode_input_is_exact_over_every_16_bit_pattern(dtype):
+    # the oracle reads the 16-bit inputs the GPU reads: every bit pattern decodes to the
+    # value torch's own widening gives (NaNs stay NaN, signed zeros keep their sign)
+    bits = torch.arange(-32768, 32768, dtype=torch.int32).to(torch.int16)
+    x = bits.view(dtype)
+    with np.errstate(invalid="ignore"):  # signalling-NaN patterns widen to quiet NaNs
+        got = oracle.decode_input(x)
+    want = x.double().numpy()
+    nan = np.isnan(want)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], want[~nan])
+    assert np.array_equal(np.signbit(got[~nan]), np.signbit(want[~nan]))
+
+
+def test_decode_input_keeps_fp32_and_float64_values():
+    x = torch.tensor([1.0, -2.5, 3.0e-39, 1.0e38], dtype=torch.float32)
+    assert np.array_equal(oracle.decode_input(x), x.double().numpy())
+    a = np.array([0.1, -7.25])
+    assert np.array_equal(oracle.decode_input(a), a)
