@@ -228,7 +228,7 @@ def run_reference(args, w):
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * dt, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": _config(w, 1),
+            "config": _config(w, 1, host=True),
             "cpu_baseline": {"value": v, "unit": "Mtokens/s", "cores": cb["cores"],
                              "kind": "oracle", "sample": cb["sample"]},
             "e2e": {"value": v, "unit": "Mtokens/s", "h2d_bytes_per_step": 0,
@@ -236,11 +236,12 @@ def run_reference(args, w):
     print(json.dumps(line), flush=True)
 
 
-def _config(w, world, graph=None):
+def _config(w, world, graph=None, host=False):
     cfg = {"workload": w.name, "tensors": w.H, "tokens": w.N, "C": w.C, "T": w.T,
            "bits": w.bits, "group": w.group, "iters": w.iters,
            "parallelism": "dp%d (tensors sharded, no exchange)" % world,
-           "l2": "flushed (%d MiB write) before every timed step" % (L2_FLUSH_BYTES >> 20)}
+           "l2": ("not applicable: host cores only" if host else
+                  "flushed (%d MiB write) before every timed step" % (L2_FLUSH_BYTES >> 20))}
     if graph is not None:
         cfg["launch"] = ("CUDA graph replay of one quantize and one dequantize per step"
                          if graph else "direct calls")
