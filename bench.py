@@ -178,7 +178,7 @@ def launches_per_step(w):
 # DRAM traffic of one k_assign launch on layer_1p3b_32760 (dram__bytes_read.sum +
 # dram__bytes_write.sum, ncu), valid while the kernel's sources hash to `sources_sha256`.
 ASSIGN_TRAFFIC = {"workload": "layer_1p3b_32760", "bytes": 217287424,
-                  "sources_sha256": "438490700d59909ee64aa7d43bdb48e1125ea2c4d2a60fc0d7a0369cbc2bb776"}
+                  "sources_sha256": "affc973d23933e4bf8c82320c0afdcf24c89e43950bcc7f40e68014a63c12dbf"}
 ASSIGN_SOURCES = ("video_kv_cache_gb300/csrc/k_assign.cu", "video_kv_cache_gb300/csrc/internal.cuh")
 
 

@@ -592,10 +592,25 @@ __global__ void __launch_bounds__(256) k_refine(QPlan p, int t) {
                 }
             }
         }
-        // Each fp32 distance is within 2^-21 (relative) of the exact distance of the fp64
-        // stage input (the input's own rounding and the 128-term sum).  A gap wider than
-        // 2^-18 therefore decides; closer calls are settled in fp64 below.
-        if (secondD - bestD <= 0x1p-18f * secondD) {
+        // Each fp32 distance is within about ten fp32 roundings (2^-20.6, relative: a sum of
+        // non-negative terms) of the exact distance of the fp32 stage input, so a gap wider
+        // than 2^-18 of the larger distance orders them as those exact distances are.  From
+        // the second stage on, the fp32 stage input is itself off the fp64 one by at most
+        // 2^-24 |x_k| per channel, which moves the difference of two distances by at most
+        // 2^-23 ||x|| (||x - c_1|| + ||x - c_2||) <= 2^-22 ||x|| sqrt(D_2); that is added to
+        // the margin (it dominates for a row far larger than its distances).  Closer calls
+        // are settled in fp64 below.
+        // (bestD and secondD are the same in every lane, so the branches are warp-uniform.)
+        bool close = secondD - bestD <= 0x1p-18f * secondD;
+        if (!close && t > 1) {
+            float xx = __fmaf_rn(x.w, x.w, __fmaf_rn(x.z, x.z, __fmaf_rn(x.y, x.y, __fmul_rn(x.x, x.x))));
+#pragma unroll
+            for (int o = 16; o >= 1; o >>= 1) xx = __fadd_rn(xx, __shfl_xor_sync(0xffffffffu, xx, o));
+            const float xn = sqrtf(xx);
+            if (xn > 0.f)
+                close = secondD - bestD <= 0x1p-18f * secondD + 0x1.1p-22f * xn * sqrtf(secondD);
+        }
+        if (close) {
             // the stage input rebuilt in fp64: x - C^(1)[pi^(1)] - ... - C^(t-1)[pi^(t-1)],
             // subtracted in that order
             double xd[4];
