@@ -9,10 +9,12 @@ Tolerances (derived from the arithmetic; see the design notes for the derivation
     so it can only differ from the fp64 oracle inside those bands.  Band cases are counted.
   * centroids, given the same assignments: |C_gpu - C_exact| <= ulp32(C_exact) +
     0.5 * max over the cluster of ulp32(r_i).  The GPU sums the fp32-rounded residuals r_i
-    with TwoSum-compensated fp32 accumulation (about twice fp32's precision, error far below
-    an fp32 ulp of the mean) and rounds the mean once, so it is off the exact mean by at most
-    the mean of the members' rounding errors plus one final rounding.  For stage 1 the
-    residual is X itself (exact in fp32) and the second term is zero.
+    with TwoSum-compensated fp32 accumulation (about twice fp32's precision: its error is
+    of order u^2 * sum |r_i|, far below an fp32 ulp of the mean unless the members cancel
+    to a mean some 10^5 times smaller than their size, which the test inputs do not do) and
+    rounds the mean once, so it is off the exact mean by at most the mean of the members'
+    rounding errors plus one final rounding.  For stage 1 the residual is X itself (exact in
+    fp32) and the second term is zero.
   * reconstruction into fp32: |x_gpu - x_oracle| <= max(1e-3 * s_q, (T + 1) * ulp32(S)) with
     S = |deQ| + sum_t |C^(t)[pi^(t)]|: the GPU adds T + 1 fp32 terms in sequence, each add
     rounding by at most half an ulp of a partial sum bounded by S.
