@@ -177,8 +177,10 @@ qvg_status qvg_quantize(const qvg_quant_params *params, const void *X,
  * own.
  *
  * Limit: qvg_quantize_workspace_bytes(params) must not exceed QVG_STATIC_SCRATCH_BYTES;
- * otherwise the call returns QVG_ERR_SCRATCH_LIMIT before touching the device.  That is
- * about 175 000 token rows (n_tensors * N), whatever T.
+ * otherwise the call returns QVG_ERR_SCRATCH_LIMIT before touching the device.  The
+ * scratch is about 380 bytes per token row plus about 390 KB per tensor, whatever T: one
+ * tensor of up to about 175 000 tokens fits, 24 tensors of up to about 6 300 each (152 000
+ * rows), 100 tensors of up to about 700 each.
  *
  * First call on a device: the first call made while a given device is current looks up
  * the area's device address once (cudaGetSymbolAddress, which can load the library's
