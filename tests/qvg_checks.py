@@ -7,14 +7,12 @@ Tolerances (derived from the arithmetic; see the design notes for the derivation
     (of an integer for the mid-rise grid, whose codes change there).
     The GPU forms r as the fp32 value nearest the exact residual and divides in IEEE fp32,
     so it can only differ from the fp64 oracle inside those bands.  Band cases are counted.
-  * centroids, given the same assignments: |C_gpu - C_exact| <= ulp32(C_exact) +
-    0.5 * max over the cluster of ulp32(r_i).  The GPU sums the fp32-rounded residuals r_i
-    with TwoSum-compensated fp32 accumulation (about twice fp32's precision: its error is
-    of order u^2 * sum |r_i|, far below an fp32 ulp of the mean unless the members cancel
-    to a mean some 10^5 times smaller than their size, which the test inputs do not do) and
-    rounds the mean once, so it is off the exact mean by at most the mean of the members'
-    rounding errors plus one final rounding.  For stage 1 the residual is X itself (exact in
-    fp32) and the second term is zero.
+  * centroids, given the same assignments: the fp32 rounding of the exact mean of the
+    exact stage input, except within the compensated sum's error bound of a rounding
+    midpoint (check_centroids gives the band); always within one fp32 ulp of the exact
+    mean.  The GPU adds each residual as its fp32 value plus the rounding error of the
+    chain that formed it, with TwoSum-compensated fp32 accumulation (about twice fp32's
+    precision), and rounds the mean once.
   * reconstruction into fp32: |x_gpu - x_oracle| <= max(1e-3 * s_q, (T + 1) * ulp32(S)) with
     S = |deQ| + sum_t |C^(t)[pi^(t)]|: the GPU adds T + 1 fp32 terms in sequence, each add
     rounding by at most half an ulp of a partial sum bounded by S.
@@ -81,30 +79,61 @@ def compare_codes(R, codes_gpu, scales_gpu, bits, group, eps=2.0 ** -20, scheme=
     return res
 
 
-def check_centroids(R_in, pi_t, cent_gpu, stage):
-    """Centroids of one stage against the exact means of R_in over pi_t."""
-    C = cent_gpu.shape[0]
+def cluster_means(R_in, pi_t, C):
+    """Exact (fp64) means of R_in's rows over each non-empty cluster of pi_t, and for each
+    the band within which the GPU's compensated sum may leave it on either side of a
+    rounding midpoint.
+
+    The GPU adds the exact stage input (from the second stage on, each residual as its fp32
+    value plus the rounding error of the chain that formed it) with TwoSum compensation, in
+    runs of at most 32 sorted positions whose pieces are then added in order, and divides
+    once.  With n members in p <= n/32 + 2 pieces and u = 2^-24, the error of its mean is at
+    most (2^-38 + p (32 + p) u^2) times the members' mean magnitude (the error terms of one
+    piece are added in fp32, at most 32 of them; those of the pieces, p of them), plus
+    2^-46 of the mean for the corrected division.  The fp64 reference sum here adds at most
+    n 2^-53 of the mean magnitude.  Returns (nonempty mask, exact means, band)."""
     pi_t = np.asarray(pi_t, dtype=np.int64)
     counts = np.bincount(pi_t, minlength=C)
     sums = np.zeros((C, R_in.shape[1]))
     np.add.at(sums, pi_t, R_in)
+    sabs = np.zeros((C, R_in.shape[1]))
+    np.add.at(sabs, pi_t, np.abs(R_in))
     nz = counts > 0
-    exact = sums[nz] / counts[nz, None]
-    if stage == 1:
-        slack = np.zeros(C)
-    else:
-        maxabs = np.zeros(C)
-        np.maximum.at(maxabs, pi_t, np.abs(R_in).max(axis=1))
-        slack = 0.5 * ulp32(maxabs)
-    tol = ulp32(exact) + slack[nz, None] + 1e-300
-    err = np.abs(cent_gpu[nz].astype(np.float64) - exact)
+    n = counts[nz, None].astype(np.float64)
+    exact = sums[nz] / n
+    pieces = np.floor(n / 32.0) + 2.0
+    band = (sabs[nz] / n) * (2.0 ** -38 + pieces * (32.0 + pieces) * 2.0 ** -48 + n * 2.0 ** -53) \
+        + 2.0 ** -46 * np.abs(exact)
+    return nz, exact, band
+
+
+def check_centroids(R_in, pi_t, cent_gpu, stage):
+    """fp32 centroids of one stage against the exact means of R_in over pi_t: the fp32
+    rounding of the exact mean, except where it lies within the band of cluster_means of an
+    fp32 rounding midpoint; everywhere within one fp32 ulp of the exact mean."""
+    C = cent_gpu.shape[0]
+    nz, exact, band = cluster_means(R_in, pi_t, C)
+    got = cent_gpu[nz]
+    err = np.abs(got.astype(np.float64) - exact)
+    tol = ulp32(exact) + 1e-300
     worst = float((err / tol).max()) if err.size else 0.0
     if worst > 1.0:
         j = np.argwhere(err > tol)[0]
-        raise AssertionError("stage %d centroid off by %.3g tolerances (cluster row %d, "
-                             "channel %d)" % (stage, worst, j[0], j[1]))
-    return {"clusters": int(nz.sum()), "empty": int((~nz).sum()), "worst_tol_frac": worst,
-            "exact_bits": int((cent_gpu[nz] == exact.astype(np.float32)).sum()),
+        raise AssertionError("stage %d centroid off by %.3g ulps (cluster row %d, channel %d)"
+                             % (stage, worst, j[0], j[1]))
+    want = exact.astype(np.float32)
+    f = want.astype(np.float64)
+    up = np.nextafter(want, np.float32(np.inf)).astype(np.float64)
+    down = np.nextafter(want, np.float32(-np.inf)).astype(np.float64)
+    near = (np.abs(exact - 0.5 * (f + up)) <= band) | (np.abs(exact - 0.5 * (f + down)) <= band)
+    off = (got != want) & ~near
+    if off.any():
+        j, k = np.argwhere(off)[0]
+        raise AssertionError("stage %d centroid (cluster row %d, channel %d) is %r, not the fp32 "
+                             "rounding %r of the exact mean %r" % (stage, j, k, got[j, k],
+                                                                  want[j, k], exact[j, k]))
+    return {"clusters": int(nz.sum()), "empty": int((~nz).sum()), "worst_ulp_frac": worst,
+            "exact_bits": int((got == want).sum()), "band": int(near.sum()),
             "entries": int(exact.size)}
 
 
@@ -112,27 +141,17 @@ def check_centroids_stored(R_in, pi_t, cent_gpu, stage, fmt):
     """Centroids of one stage in a 16-bit storage format (1 binary16, 2 bfloat16) against the
     oracle's rounding of the exact means of R_in over pi_t.  Each stored value must be
     representable in the format; a non-empty cluster's value must equal the rounding of its
-    exact mean, except where the exact mean lies so close to a midpoint of two format values
-    that the GPU's fp32 mean could fall on either side: within two fp32 ulps (stage 1) plus
-    half an fp32 ulp of the cluster's largest member (later stages, whose members the GPU
-    holds in fp32).  There the value must be one of the two neighbours."""
+    exact mean, except where the exact mean lies within the band of cluster_means of a
+    midpoint of two format values (the GPU rounds a faithful fp32 mean and settles a mean
+    exactly on a midpoint by the sign of what it leaves out, which is right outside that
+    band).  There the value must be one of the two neighbours."""
     C = cent_gpu.shape[0]
     np.testing.assert_array_equal(oracle.store_centroids(cent_gpu.astype(np.float64), fmt),
                                   cent_gpu)
-    pi_t = np.asarray(pi_t, dtype=np.int64)
-    counts = np.bincount(pi_t, minlength=C)
-    sums = np.zeros((C, R_in.shape[1]))
-    np.add.at(sums, pi_t, R_in)
-    nz = counts > 0
-    exact = sums[nz] / counts[nz, None]
+    nz, exact, band = cluster_means(R_in, pi_t, C)
     want = oracle.store_centroids(exact, fmt)
-    slack = 2.0 * ulp32(exact)
-    if stage > 1:
-        maxabs = np.zeros(C)
-        np.maximum.at(maxabs, pi_t, np.abs(R_in).max(axis=1))
-        slack = slack + 0.5 * ulp32(maxabs)[nz, None]
-    lo = oracle.store_centroids(exact - slack, fmt)
-    hi = oracle.store_centroids(exact + slack, fmt)
+    lo = oracle.store_centroids(exact - band, fmt)
+    hi = oracle.store_centroids(exact + band, fmt)
     got = cent_gpu[nz]
     differ = got != want
     ok = ~differ | ((lo != hi) & ((got == lo) | (got == hi)))
@@ -232,3 +251,29 @@ def assignment_agreement(pi_gpu, pi_orc, R_stage_inputs, cent_orc):
         res.append({"agree": float(eq.mean()), "mismatches": int((~eq).sum()),
                     "max_gap": float(max(gaps)) if gaps else 0.0})
     return res
+
+
+def check_oracle_run(Xd, pi_gpu, cent_gpu, ref_pi, ref_cent, ref_J, min_agree=0.999,
+                     max_gap=1e-3, j_rel=1e-3, stages=None):
+    """One tensor's GPU run against the oracle's own independent run, stage by stage:
+      * the assignments agree on at least `min_agree` of the tokens;
+      * every token assigned differently is a near tie: its GPU cluster is at most `max_gap`
+        farther (relative squared distance, on the oracle's stage input and centroids) than
+        the oracle's;
+      * the Lloyd objective J of the stage (the GPU's own assignment and centroids, on its
+        own fp64 stage input) is within `j_rel` of the oracle's (plus 1e-12 of ||X||^2, for
+        stages whose objective is zero).
+    Xd [N][d] fp64; pi_* [T][N]; cent_* [T][C][d]; ref_J [T].  Returns the per-stage
+    agreement records."""
+    T = pi_gpu.shape[0] if stages is None else stages
+    Rin = [oracle.residual(Xd, ref_pi, ref_cent, t) for t in range(T)]
+    agr = assignment_agreement(pi_gpu[:T], ref_pi[:T], Rin, ref_cent)
+    floor = 1e-12 * float((np.asarray(Xd, dtype=np.float64) ** 2).sum())
+    for t, a in enumerate(agr):
+        assert a["agree"] >= min_agree, ("stage", t + 1, a)
+        assert a["max_gap"] <= max_gap, ("stage", t + 1, a)
+        J = oracle.objective(oracle.residual(Xd, pi_gpu, cent_gpu, t),
+                             np.asarray(pi_gpu[t], dtype=np.int32), cent_gpu[t])
+        a["J_gpu"], a["J_oracle"] = J, float(ref_J[t])
+        assert abs(J - ref_J[t]) <= j_rel * ref_J[t] + floor, ("stage", t + 1, a)
+    return agr

@@ -56,3 +56,12 @@ def test_attention_bytes_of_the_1p3b_layer():
     # more queries only add their own rows
     assert bench.attention_bytes(heads, N, w.C, w.T, w.bits, w.group, 16) - b == \
         heads * 15 * 128 * 6
+
+
+def test_cpu_baseline_sample_is_whole_frames():
+    # whole frames, at most 8192 tokens a tensor: two of the 13B shape's sixteen 64x64
+    # frames, five of the 1.3B layer's 30x52 frames, all of the single-head tensor
+    assert bench.cpu_sample_frames(synth.workload("dit13b_65536")) == 2
+    assert bench.cpu_sample_frames(synth.workload("layer_1p3b_32760")) == 5
+    assert bench.cpu_sample_frames(synth.workload("single_head_4x32x32")) == 4
+    assert bench.DEFAULT_WORKLOAD == "dit13b_65536"

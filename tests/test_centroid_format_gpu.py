@@ -7,8 +7,9 @@ the residuals, codes and reconstruction are taken against those rounded values. 
     mean of its stage input (computed in fp64 from X and the stored centroids), and the codes
     and scales are the oracle's encoding of the final residual;
   * the fused dequant reconstructs from the rounded tables;
-  * end to end: the first stage's assignments agree with the oracle run in the same format,
-    and every stage's Lloyd objective is within 1e-3 relative of the oracle's;
+  * end to end, stage by stage, against the oracle run in the same format: assignments
+    agree on 99.9 % of tokens, every mismatch is a near tie (1e-3 relative distance gap),
+    and the Lloyd objective is within 1e-3 relative;
   * a warm-start table is rounded once into the format (clusters left empty keep it);
   * format 0 gives the same bits as a call that never names a format.
 """
@@ -66,11 +67,8 @@ def test_stored_centroids_match_oracle(fmt, H, fr, gh, gw, C, T, bits, group, it
         qc.compare_codes(R, g["codes"][h], g["scales"][h], bits, group)
         qc.check_reconstruction(x32[h], g["codes"][h], g["scales"][h], g["pi"][h], cent, bits,
                                 group)
-        assert (g["pi"][h][0] == ref["pi"][h][0]).mean() >= 0.999
-        for t in range(T):
-            J = oracle.objective(oracle.residual(Xd[h], g["pi"][h], cent, t),
-                                 g["pi"][h][t].astype(np.int32), cent[t])
-            assert abs(J - ref["J"][h, t]) <= 1e-3 * ref["J"][h, t], (t, J, ref["J"][h, t])
+        qc.check_oracle_run(Xd[h], g["pi"][h], cent, ref["pi"][h], ref["centroids"][h],
+                            ref["J"][h])
 
 
 @pytest.mark.parametrize("fmt", FORMATS)
@@ -90,7 +88,8 @@ def test_warm_table_is_rounded_once(fmt):
                                   oracle.store_centroids(warm[C // 2:].astype(np.float64), fmt))
     assert (g["pi"][0][0] < C // 2).all()
     ref = oracle.quantize(Xd, C, T, 2, 32, 1, 0, warm=warm[None, None], centroid_format=fmt)
-    assert (g["pi"][0] == ref["pi"][0]).mean() >= 0.999
+    qc.check_oracle_run(Xd[0], g["pi"][0], g["centroids"][0, 0], ref["pi"][0],
+                        ref["centroids"][0], ref["J"][0])
     qc.check_centroids_stored(Xd[0], g["pi"][0][0], cent, 1, fmt)
 
 

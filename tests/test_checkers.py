@@ -55,6 +55,23 @@ def test_check_centroids(case):
     bad[3, 4] = np.nextafter(np.nextafter(bad[3, 4], np.float32(np.inf)), np.float32(np.inf))
     with pytest.raises(AssertionError):
         qc.check_centroids(R, pi, bad, 1)
+    # one ulp off (the fp32 neighbour, not the rounding of the exact mean) fails too, at the
+    # first stage and on a later stage's residuals
+    R2 = oracle.residual(R, ref["pi"][0], ref["centroids"][0], 1)
+    for stage, Rs, pis in ((1, R, pi), (2, R2, ref["pi"][0][1])):
+        ns = np.bincount(pis, minlength=C)
+        sums = np.zeros((C, 128))
+        np.add.at(sums, pis.astype(np.int64), Rs)
+        want = np.where(ns[:, None] > 0, sums / np.maximum(ns, 1)[:, None], 0.0).astype(np.float32)
+        res = qc.check_centroids(Rs, pis, want, stage)
+        # only means far smaller than their members fall in the band
+        assert res["band"] <= 0.05 * res["entries"], res
+        bad = want.copy()
+        j = int(np.argmax(ns))
+        k = int(np.argmax(np.abs(want[j])))
+        bad[j, k] = np.nextafter(bad[j, k], np.float32(-np.inf))
+        with pytest.raises(AssertionError):
+            qc.check_centroids(Rs, pis, bad, stage)
 
 
 def test_check_centroids_stored():

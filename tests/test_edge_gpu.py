@@ -51,7 +51,8 @@ def _check_all(X, ckv, x32, C, T, bits, group, iters, seed, min_agree=0.999):
                         bits, group)
         qc.check_reconstruction(x32[h], g["codes"][h], g["scales"][h], g["pi"][h],
                                 g["centroids"][h, 0], bits, group)
-        assert (g["pi"][h] == ref["pi"][h]).mean() >= min_agree
+        qc.check_oracle_run(Xd[h], g["pi"][h], g["centroids"][h, 0], ref["pi"][h],
+                            ref["centroids"][h], ref["J"][h], min_agree=min_agree)
     return g, ref
 
 

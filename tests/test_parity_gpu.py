@@ -202,14 +202,8 @@ def test_end_to_end_matches_oracle(case):
                         bits, group)
         qc.check_reconstruction(x32[h], g["codes"][h], g["scales"][h], g["pi"][h],
                                 g["centroids"][h, 0], bits, group)
-        Rin = [oracle.residual(Xd[h], ref["pi"][h], ref["centroids"][h], t) for t in range(T)]
-        agr = qc.assignment_agreement(g["pi"][h], ref["pi"][h], Rin, ref["centroids"][h])
-        for t, a in enumerate(agr):
-            assert a["agree"] >= 0.999, (t, a)
-        for t in range(T):
-            J_gpu = oracle.objective(oracle.residual(Xd[h], g["pi"][h], g["centroids"][h, 0], t),
-                                     g["pi"][h][t].astype(np.int32), g["centroids"][h, 0, t])
-            assert abs(J_gpu - ref["J"][h, t]) <= 1e-3 * ref["J"][h, t]
+        qc.check_oracle_run(Xd[h], g["pi"][h], g["centroids"][h, 0], ref["pi"][h],
+                            ref["centroids"][h], ref["J"][h])
 
 
 def test_single_head_workload_matches_oracle():
@@ -219,7 +213,8 @@ def test_single_head_workload_matches_oracle():
     ckv = _gpu_quantize(X, w.C, w.T, w.bits, w.group, w.iters, w.seed)
     g = _to_np(ckv)
     ref = oracle.quantize(Xd, w.C, w.T, w.bits, w.group, w.iters, w.seed)
-    assert (g["pi"] == ref["pi"]).mean() >= 0.999
+    qc.check_oracle_run(Xd[0], g["pi"][0], g["centroids"][0, 0], ref["pi"][0],
+                        ref["centroids"][0], ref["J"][0])
     qc.forced_check(Xd[0], g["codes"][0], g["scales"][0], g["pi"][0], g["centroids"][0, 0],
                     w.bits, w.group)
     x32 = api.dequantize(ckv, out_dtype=torch.float32).cpu().numpy()
@@ -250,8 +245,9 @@ def test_streaming_chunks_warm_start_and_chunked_dequant():
         ref = oracle.quantize(Xd, C, T, bits, group, cold_iters if c == 0 else warm_iters, 3,
                               warm=warm_o)
         sl = slice(c * L, (c + 1) * L)
-        assert (g["pi"][:, :, sl] == ref["pi"]).mean() >= 0.999
         for h in range(H):
+            qc.check_oracle_run(Xd[h], g["pi"][h, :, sl], g["centroids"][h, c], ref["pi"][h],
+                                ref["centroids"][h], ref["J"][h])
             qc.forced_check(Xd[h], g["codes"][h, sl], g["scales"][h, sl], g["pi"][h, :, sl],
                             g["centroids"][h, c], bits, group)
             qc.check_reconstruction(x32[h, sl], g["codes"][h, sl], g["scales"][h, sl],
@@ -313,15 +309,11 @@ def test_tensor_stride_off_the_row_grid_gives_the_same_bits():
 @pytest.mark.parametrize("name", ["qvg", "qvg_pro"])
 def test_presets_against_the_oracle(name):
     # The two named settings (one stage with 64-channel groups; four stages with 16-channel
-    # groups) end to end against the oracle on a tensor pair of 4096 tokens.  Given the GPU's
-    # assignments every stage's centroids, codes and scales are the oracle's (forced mode)
-    # and the reconstruction matches.  Stage 1 clusters X itself, the same input on both
-    # sides, so its assignments must agree.  A later stage starts from a residual that
-    # differs from the oracle's by the last ulp of the stored fp32 centroids; on clusters
-    # of a dozen tokens one tie flipped by that ulp moves two centroids, and the next
-    # rounds follow another Lloyd trajectory (seen in the fourth stage of QVG-Pro: 3 % of
-    # its assignments, objective within 3e-4).  There each stage's objective must match the
-    # oracle's within 1 %.
+    # groups) end to end against the oracle on a tensor pair of 4096 tokens: given the GPU's
+    # assignments every stage's centroids, codes and scales are the oracle's (forced mode),
+    # the reconstruction matches, and against the oracle's own Lloyd run every stage's
+    # assignments agree on 99.9 % of tokens, every mismatch is a near tie and every stage's
+    # objective is within 1e-3.
     from video_kv_cache_gb300.presets import PRESETS
     pr = PRESETS[name]
     X = _make(15, 2, 4, 32, 32)  # N = 4096
@@ -339,11 +331,8 @@ def test_presets_against_the_oracle(name):
         qc.forced_check(Xd[h], g["codes"][h], g["scales"][h], g["pi"][h], cent, pr.bits, pr.group)
         qc.check_reconstruction(x32[h], g["codes"][h], g["scales"][h], g["pi"][h], cent,
                                 pr.bits, pr.group)
-        assert (g["pi"][h][0] == ref["pi"][h][0]).mean() >= 0.999
-        for t in range(pr.T):
-            J = oracle.objective(oracle.residual(Xd[h], g["pi"][h], cent, t),
-                                 g["pi"][h][t].astype(np.int32), cent[t])
-            assert abs(J - ref["J"][h, t]) <= 1e-2 * ref["J"][h, t], (h, t, J, ref["J"][h, t])
+        qc.check_oracle_run(Xd[h], g["pi"][h], cent, ref["pi"][h], ref["centroids"][h],
+                            ref["J"][h])
 
 
 # --------------------------------------------------------------------------------------
@@ -407,7 +396,8 @@ def test_midrise_end_to_end(bits, group, T):
                         scheme=1)
         qc.check_reconstruction(x32[h], g["codes"][h], g["scales"][h], g["pi"][h], cent, bits,
                                 group, scheme=1)
-        assert (g["pi"][h][0] == ref["pi"][h][0]).mean() >= 0.999
+        qc.check_oracle_run(Xd[h], g["pi"][h], cent, ref["pi"][h], ref["centroids"][h],
+                            ref["J"][h])
         # the assignments do not depend on the grid: the symmetric run clusters the same way
         sym = oracle.quantize(Xd[h:h + 1], C, T, bits, group, iters, seed, tensor_id_base=h)
         np.testing.assert_array_equal(sym["pi"][0], ref["pi"][h])

@@ -4,8 +4,10 @@
 //   * Residuals r = x - C^(1)[pi^(1)] - ... are formed with an error-free TwoSum chain and
 //     rounded once to fp32, so r is the fp32 value nearest the exact residual.
 //   * Centroid sums run in a fixed order over the tokens grouped by cluster (a stable
-//     counting sort), with TwoSum-compensated fp32 accumulation; the mean is rounded once
-//     to fp32.  Repeated runs give identical bits.
+//     counting sort), with TwoSum-compensated fp32 accumulation of the exact stage input
+//     (from the second stage on, each residual enters as its fp32 value plus the rounding
+//     error of the chain that formed it); the mean is rounded once to fp32.  Repeated runs
+//     give identical bits.
 //   * Distances for the assignment come from a tensor-core GEMM on fp16 copies of the
 //     centred operands (fp32 accumulate).  Every cluster whose GEMM score lies within a
 //     rigorous bound on the GEMM's error of the best one is re-scored with a direct fp32

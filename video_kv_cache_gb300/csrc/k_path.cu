@@ -362,6 +362,14 @@ __device__ __forceinline__ void acc_two_sum2(float2 &s, float2 &e, float2 x) {
     e = __fadd2_rn(e, err);
     s = sn;
 }
+// a - c on a pair with its exact rounding error: a - c = d + err exactly (TwoSum of a and
+// -c, the negation folded into the last step)
+__device__ __forceinline__ float2 two_diff2(float2 a, float2 c, float2 &err) {
+    const float2 d = sub2(a, c);
+    const float2 bb = sub2(d, a);
+    err = sub2(sub2(a, sub2(d, bb)), __fadd2_rn(c, bb));
+    return d;
+}
 
 __global__ void __launch_bounds__(kSortBlock) k_sort_hist(QPlan p, int t) {
     pdl_begin();
@@ -510,7 +518,10 @@ __device__ __forceinline__ void write_centroid(const QPlan &p, int h, int t, int
 //
 // The summed rows are the stage input R^(t-1): X itself at stage 1, later a residual that
 // is not stored but rebuilt here from X and the earlier stages' centroid rows (L2-resident)
-// by the TwoSum chain of k_prep, which gives the same fp32 value.  Reaching a row takes
+// by a TwoSum chain.  The chain's running difference and its collected rounding errors both
+// enter the compensated sum, so a mean is that of the exact residuals and rounds as the
+// fp64 reference's does (not the mean of fp32-rounded residuals, which is off by up to half
+// an fp32 ulp of the largest member and can flip a near tie).  Reaching a row takes
 // three dependent loads (its id from the sort, its earlier clusters, then X and the
 // centroid rows), so the kernel is built to keep many of them in flight:
 //   * persistent warps, each striding over the chunks of all tensors; lane m holds sorted
@@ -697,9 +708,15 @@ __global__ void __launch_bounds__(256, TP == 0 ? 4 : 2)
             reinterpret_cast<float4 *>(dst)[lane] = make_float4(s01.x, s01.y, s23.x, s23.y);
             reinterpret_cast<float4 *>(dst + kD)[lane] = make_float4(e01.x, e01.y, e23.x, e23.y);
         };
-        // the lane's four channels of the row in a slot, as the stage input
-        auto row_of = [&](const uint8_t *hs, int u, float2 &v01, float2 &v23) {
+        // Adds the lane's four channels of the row in slot u, as the stage input, to the
+        // running (sum, error) pair.  From the second stage on the stage input is
+        // x - C^(1)[pi^(1)] - ..., formed by a TwoSum chain as d + r with d the running
+        // fp32 difference and r the sum of the chain's rounding errors; d goes through the
+        // compensated sum and r is added to its error term, so the sum is that of the exact
+        // residuals (to about twice fp32's precision), not of their fp32 roundings.
+        auto add_row = [&](const uint8_t *hs, int u) {
             const uint8_t *slot = hs + u * XB;  // the X row; centroid rows follow all X rows
+            float2 v01, v23;
             if constexpr (SRC == 0) {
                 const uint2 w = *reinterpret_cast<const uint2 *>(slot + lane * 8);
                 v01 = make_float2(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xFFFF0000u));
@@ -713,27 +730,30 @@ __global__ void __launch_bounds__(256, TP == 0 ? 4 : 2)
                 v01 = make_float2(w.x, w.y);
                 v23 = make_float2(w.z, w.w);
             }
-            if (TP == 1) {
-                // one earlier stage: the chain's fl(fl(x - c) + err) is fl(x - c) itself for
-                // every finite result
-                const float4 c = *reinterpret_cast<const float4 *>(hs + kBulkGroup * XB + u * 512 + lane * 16);
-                v01 = sub2(v01, make_float2(c.x, c.y));
-                v23 = sub2(v23, make_float2(c.z, c.w));
-            } else if (TP != 0) {
-                float v[4] = {v01.x, v01.y, v23.x, v23.y}, er[4] = {0.f, 0.f, 0.f, 0.f};
-                for (int st = 0; st < tp; st++) {
-                    const float4 c = *reinterpret_cast<const float4 *>(hs + kBulkGroup * XB + st * kBulkGroup * 512 +
-                                                                       u * 512 + lane * 16);
-                    const float cc[4] = {c.x, c.y, c.z, c.w};
+            if constexpr (TP == 0) {
+                acc_two_sum2(s01, e01, v01);
+                acc_two_sum2(s23, e23, v23);
+            } else {
+                float2 r01 = make_float2(0.f, 0.f), r23 = r01;
+                auto chain = [&](int st) {  // subtract the row of stage st + 1
+                    const float4 c = *reinterpret_cast<const float4 *>(
+                        hs + kBulkGroup * XB + st * kBulkGroup * 512 + u * 512 + lane * 16);
+                    float2 t01, t23;
+                    v01 = two_diff2(v01, make_float2(c.x, c.y), t01);
+                    v23 = two_diff2(v23, make_float2(c.z, c.w), t23);
+                    r01 = __fadd2_rn(r01, t01);
+                    r23 = __fadd2_rn(r23, t23);
+                };
+                if constexpr (TP > 0) {
 #pragma unroll
-                    for (int r = 0; r < 4; r++) {
-                        float err;
-                        two_sum(v[r], -cc[r], v[r], err);
-                        er[r] = __fadd_rn(er[r], err);
-                    }
+                    for (int st = 0; st < TP; st++) chain(st);
+                } else {
+                    for (int st = 0; st < tp; st++) chain(st);
                 }
-                v01 = make_float2(__fadd_rn(v[0], er[0]), __fadd_rn(v[1], er[1]));
-                v23 = make_float2(__fadd_rn(v[2], er[2]), __fadd_rn(v[3], er[3]));
+                acc_two_sum2(s01, e01, v01);
+                acc_two_sum2(s23, e23, v23);
+                e01 = __fadd2_rn(e01, r01);
+                e23 = __fadd2_rn(e23, r23);
             }
         };
         const uint32_t starts = cur.brk & ~1u;  // position 0 opens the first run above
@@ -751,26 +771,18 @@ __global__ void __launch_bounds__(256, TP == 0 ? 4 : 2)
             if (n_rows == kBulkGroup && ((starts >> (g * kBulkGroup)) & 0xFFu) == 0u) {
                 // a full group inside one run (the usual case)
 #pragma unroll
-                for (int u = 0; u < kBulkGroup; u++) {
-                    float2 v01, v23;
-                    row_of(gslots, u, v01, v23);
-                    acc_two_sum2(s01, e01, v01);
-                    acc_two_sum2(s23, e23, v23);
-                }
+                for (int u = 0; u < kBulkGroup; u++) add_row(gslots, u);
             } else {
 #pragma unroll 1
                 for (int u = 0; u < n_rows; u++) {
                     const int m = g * kBulkGroup + u;
-                    float2 v01, v23;
-                    row_of(gslots, u, v01, v23);
                     if ((starts >> m) & 1u) {  // warp-uniform
                         stash(m);
                         run_c = __shfl_sync(0xffffffffu, cur.cl, m);
                         run_start = m;
                         s01 = s23 = e01 = e23 = make_float2(0.f, 0.f);
                     }
-                    acc_two_sum2(s01, e01, v01);
-                    acc_two_sum2(s23, e23, v23);
+                    add_row(gslots, u);
                 }
             }
             n_done++;
