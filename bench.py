@@ -167,8 +167,8 @@ def attention_bytes(heads, N, C, T, bits, group, M, q_bytes=2, out_bytes=4):
 
 def assign_flops(H, N, C):
     """Useful flops of one assignment launch over H tensors: the [N x 128] x [128 x C]
-    product per tensor (the GEMM issues twice as many: one fp16 plane of the residual
-    against two fp16 planes of the centroids)."""
+    product per tensor.  The tensor cores also run the per-centroid offset, one tf32 MMA of
+    K = 8 per 128-token tile, which is not counted."""
     return 2.0 * H * N * C * 128
 
 
@@ -359,6 +359,13 @@ def run_ours(args, w):
     q_ms_avg = _max_over_ranks(sum(q_ms) / len(q_ms), world)
     tokens_all = w.H * N  # whole job: every rank's tensors
 
+    # how often the tensor-core scores left a near tie to the exact re-scoring: the first
+    # two words of the workspace after a quantize (rows, candidate clusters)
+    quantize()
+    torch.cuda.synchronize()
+    ref_rows, ref_cands = (int(v) for v in ws[:8].view(torch.int32).cpu())
+    assign_rows = H * N * w.T * w.iters
+
     # --- the dominant kernel and the dequant, each timed alone on the same data
     reps = max(3, args.steps)
     d_ms = _max_over_ranks(_event_ms(st, dequantize, reps, flush), world)
@@ -445,7 +452,9 @@ def run_ours(args, w):
                          "peak": tf_burst, "unit": "TFLOP/s", "frac": a_tflops / tf_burst,
                          "traffic": traffic, "peak_source": src + " bf16 burst",
                          "flops_per_launch": a_flops, "ms_per_launch": r_ms,
-                         "timed_as": "qvg_reassign (centroid planes + k_assign + k_refine)"},
+                         "timed_as": "qvg_reassign (centroid planes + k_assign + k_refine)",
+                         "rescored_rows_frac": ref_rows / assign_rows,
+                         "rescored_cands_per_row": ref_cands / max(ref_rows, 1)},
             "quantize": {"ms": q_ms_avg, "mtokens_s": tokens_all / (q_ms_avg * 1e-3) / 1e6,
                          "useful_tflops": useful_flops * world / (q_ms_avg * 1e-3) / 1e12},
             "dequant": {"ms": d_ms, "gbs": dq_gbs, "pct_hbm": 100.0 * dq_gbs / hbm,

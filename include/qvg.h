@@ -96,8 +96,9 @@ typedef enum { QVG_QSCHEME_SYMMETRIC = 0, QVG_QSCHEME_MIDRISE = 1 } qvg_qscheme;
  *   QVG_CENTROIDS_F16:  IEEE binary16; QVG_CENTROIDS_BF16: bfloat16.  The cluster mean, a
  *     cold-start row and a warm-start value are each rounded once to nearest even in the
  *     format.  The mean is carried to about twice fp32's precision, so it rounds as the
- *     exact mean of the stage's fp32 inputs does, save within about 2^-40 relative of a
- *     tie (from the second stage on, those inputs are the fp32 residuals).
+ *     exact mean of the stage's inputs does (from the second stage on, the exact residuals
+ *     against the stored earlier centroids), save within about 2^-38 of the members' size
+ *     of a tie.
  * Quant VideoGen explainer page, compression and metadata overhead: the ratios it prints
  * count centroids in a 16-bit format. */
 typedef enum { QVG_CENTROIDS_F32 = 0, QVG_CENTROIDS_F16 = 1, QVG_CENTROIDS_BF16 = 2 }
@@ -153,7 +154,10 @@ size_t qvg_quantize_workspace_bytes(const qvg_quant_params *params);
  *                   used as stage t's initial centroids -- the streaming warm start.  It
  *                   may point into out->centroids (another table slot than table_index).
  *   workspace       >= qvg_quantize_workspace_bytes(params) bytes, 256-byte aligned; its
- *                   contents on entry do not matter.
+ *                   contents on entry do not matter.  Once the call's work has finished,
+ *                   its first two uint32 words count, over all stages and Lloyd rounds, the
+ *                   token rows whose nearest centroid the tensor-core scores could not
+ *                   settle and the candidate clusters re-scored exactly for them.
  * Calls that share a workspace must be ordered on one stream. */
 qvg_status qvg_quantize(const qvg_quant_params *params, const void *X,
                         const float *warm_centroids, const qvg_buffers *out, void *workspace,
@@ -178,9 +182,9 @@ qvg_status qvg_quantize(const qvg_quant_params *params, const void *X,
  *
  * Limit: qvg_quantize_workspace_bytes(params) must not exceed QVG_STATIC_SCRATCH_BYTES;
  * otherwise the call returns QVG_ERR_SCRATCH_LIMIT before touching the device.  The
- * scratch is about 380 bytes per token row plus about 390 KB per tensor, whatever T: one
- * tensor of up to about 175 000 tokens fits, 24 tensors of up to about 6 300 each (152 000
- * rows), 100 tensors of up to about 700 each.
+ * scratch is about 380 bytes per token row plus about 370 KB per tensor, whatever T: one
+ * tensor of up to about 175 000 tokens fits, 24 tensors of up to about 6 400 each (154 000
+ * rows), 100 tensors of up to about 780 each.
  *
  * First call on a device: the first call made while a given device is current looks up
  * the area's device address once (cudaGetSymbolAddress, which can load the library's

@@ -8,10 +8,10 @@
 //     (from the second stage on, each residual enters as its fp32 value plus the rounding
 //     error of the chain that formed it); the mean is rounded once to fp32.  Repeated runs
 //     give identical bits.
-//   * Distances for the assignment come from a tensor-core GEMM on fp16 copies of the
-//     centred operands (fp32 accumulate).  Every cluster whose GEMM score lies within a
-//     rigorous bound on the GEMM's error of the best one is re-scored with a direct fp32
-//     sum of squared differences, ties going to the lowest cluster index.
+//   * Distances for the assignment come from tensor-core MMAs: fp16 copies of the centred
+//     operands plus a tf32 per-centroid offset, accumulated in fp32.  Every cluster whose
+//     score lies within a rigorous bound on its error of the best one is re-scored exactly
+//     (fp32, then fp64 where fp32 cannot separate them), ties going to the lowest index.
 #pragma once
 
 #include <cuda.h>
@@ -30,9 +30,8 @@ namespace qvg {
 constexpr int kD = 128;            // channels per token
 constexpr int kMaxT = 8;           // most smoothing stages
 constexpr int kMaxC = 256;         // most clusters (pi is uint8)
-// fp16 planes of the centroids in the assignment GEMM: 1 (one product per score) or 2
-// (hi + lo, two products, half the error bound)
-constexpr int kBPlanes = 2;
+// fp32 values per row of the assignment's offset table (one 128-byte TMA row)
+constexpr int kOffsetRow = 32;
 // Largest |component| that the fp16 GEMM operands are trusted with; a residual row or a
 // centroid set with a larger norm sends every cluster of the row to the exact re-scoring.
 constexpr float kFp16Safe = 60000.f;
@@ -59,9 +58,10 @@ struct QPlan {
     __half *A;             // [H][N][128] fp16 copy of the centred residual r - mu
     float *rnorm;          // [H][N] norm of the centred residual row (fp32)
     float *dnorm;          // [H][N] norm of its fp16 rounding error, ||fp16(r - mu) - (r - mu)||
-    __half *B;             // [H][kBPlanes][Cpad][128] fp16 planes of the centred centroids
-                           // c - mu: plane 0 = fp16(c - mu), plane 1 = fp16 of its remainder
-    float *cn;             // [H][Cpad] squared norm of the centred centroids
+    __half *B;             // [H][Cpad][128] fp16(c - mu) of the centred centroids
+    float *Bx;             // [H][Cpad][kOffsetRow] the offset -||c - mu||^2 / 2 as three tf32
+                           // parts (h, m, l, 0, ...); -2^100 in the padded rows
+    float2 *cnd;           // [H][Cpad] (||c - mu||^2, ||fp16(c - mu) - (c - mu)||) per centroid
     float *mu;             // [H][128] centring vector of the current stage
     int *counts;           // [H][C] cluster sizes of the current assignment
     int *offs;             // [H][C] first position of each cluster in `ids`
@@ -97,6 +97,19 @@ __device__ __forceinline__ void two_sum(float a, float b, float &s, float &e) {
     s = __fadd_rn(a, b);
     float bb = __fsub_rn(s, a);
     e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+}
+
+// The fp32 value v as three tf32 parts, v = h + m + l exactly: h is v rounded to tf32
+// (11 significant bits), m the remainder rounded to tf32, l what is left (at most two
+// significant bits).  Each difference is exact in fp32.
+__device__ __forceinline__ float tf32_round(float x) {
+    return __uint_as_float((__float_as_uint(x) + 0x1000u) & 0xFFFFE000u);
+}
+__device__ __forceinline__ void tf32_split3(float v, float &h, float &m, float &l) {
+    h = tf32_round(v);
+    const float r = __fsub_rn(v, h);
+    m = tf32_round(r);
+    l = __fsub_rn(r, m);
 }
 
 // 8 consecutive input channels of X as fp32 (exact for fp16 / bf16).
@@ -263,6 +276,7 @@ cudaError_t launch_encode(const QPlan &p, cudaStream_t st);
 struct AssignMaps {
     CUtensorMap a;
     CUtensorMap b;
+    CUtensorMap bx;  // the offset rows
     // row views for the cluster sums' gathers: X as [rows][128] (when every tensor starts
     // on a whole row, x_stride % 128 == 0; gather = 0 otherwise) and the centroid tables
     // as [rows][128] fp32
@@ -278,7 +292,7 @@ void assign_release(AssignMaps *maps);
 cudaError_t launch_assign(const QPlan &p, const AssignMaps *maps, int t, int num_sms,
                           cudaStream_t st);
 cudaError_t launch_refine(const QPlan &p, int t, int num_sms, cudaStream_t st);
-size_t assign_smem_bytes(int Cpad);
+size_t assign_smem_bytes(int Cpad, int nslots);
 
 struct DPlan {
     int H;

@@ -295,15 +295,18 @@ cudaError_t launch_prep(const QPlan &p, int t, cudaStream_t st) {
 }
 
 // --------------------------------------------------------------------------------------
-// GEMM planes of the stage's initial centroids: fp16 planes of C_j - mu and
-// ||C_j - mu||^2 (fp32).   grid (C, H), block 128.
+// Assignment operands of the stage's initial centroids, per centroid j (c = C_j - mu):
+//   B[j]   = fp16(c), the tensor-core operand;
+//   Bx[j]  = the offset -||c||^2 / 2 as three tf32 parts (h, m, l, 0, ...);
+//   cnd[j] = (||c||^2, ||fp16(c) - c||), for the assignment's error bound.
+// The padded rows j in [C, Cpad) get the offset -2^100, so their scores never win.
+// grid (Cpad, H), block 128 (one thread per channel).
 // --------------------------------------------------------------------------------------
-__device__ __forceinline__ void store_planes(const QPlan &p, int h, int j, int k, float ct) {
-    const __half hi = __float2half_rn(ct);
-    p.B[((int64_t)h * kBPlanes * p.Cpad + j) * kD + k] = hi;
-    if (kBPlanes == 2)
-        p.B[((int64_t)(h * kBPlanes + 1) * p.Cpad + j) * kD + k] =
-            __float2half_rn(__fsub_rn(ct, __half2float(hi)));
+__device__ __forceinline__ void write_offset_row(const QPlan &p, int h, int j, int lane, float cn) {
+    float oh, om, ol;
+    tf32_split3(-0.5f * cn, oh, om, ol);
+    p.Bx[((int64_t)h * p.Cpad + j) * kOffsetRow + lane] =
+        lane == 0 ? oh : lane == 1 ? om : lane == 2 ? ol : 0.f;
 }
 
 __global__ void k_centroid_planes(QPlan p, int t) {
@@ -311,21 +314,39 @@ __global__ void k_centroid_planes(QPlan p, int t) {
     // the near-tie queue starts empty for the stage's first assignment
     if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *p.rq_count = 0;
     const int j = blockIdx.x, h = blockIdx.y, k = threadIdx.x;
+    if (j >= p.C) {  // a padded column (the whole block takes this branch)
+        if (k < kOffsetRow) p.Bx[((int64_t)h * p.Cpad + j) * kOffsetRow + k] = k == 0 ? -0x1p100f : 0.f;
+        return;
+    }
     const float v = p.cent[h * p.cent_tstride + p.cent_off + (int64_t)(t - 1) * p.C * kD +
                            (int64_t)j * kD + k];
-    __shared__ float red[4];
+    __shared__ float red[4][2];
     const float ct = __fsub_rn(v, p.mu[h * kD + k]);
-    store_planes(p, h, j, k, ct);
-    float ss = ct * ct;
+    const __half hi = __float2half_rn(ct);
+    p.B[((int64_t)h * p.Cpad + j) * kD + k] = hi;
+    const float dv = __fsub_rn(ct, __half2float(hi));  // exact
+    float ss = ct * ct, dd = dv * dv;
 #pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-    if ((k & 31) == 0) red[k >> 5] = ss;
+    for (int o = 16; o >= 1; o >>= 1) {
+        ss += __shfl_xor_sync(0xffffffffu, ss, o);
+        dd += __shfl_xor_sync(0xffffffffu, dd, o);
+    }
+    if ((k & 31) == 0) {
+        red[k >> 5][0] = ss;
+        red[k >> 5][1] = dd;
+    }
     __syncthreads();
-    if (k == 0) p.cn[(int64_t)h * p.Cpad + j] = (red[0] + red[1]) + (red[2] + red[3]);
+    if (k < 32) {
+        const float cn = (red[0][0] + red[1][0]) + (red[2][0] + red[3][0]);
+        write_offset_row(p, h, j, k, cn);
+        if (k == 0)
+            p.cnd[(int64_t)h * p.Cpad + j] =
+                make_float2(cn, sqrtf((red[0][1] + red[1][1]) + (red[2][1] + red[3][1])));
+    }
 }
 
 cudaError_t launch_centroid_planes(const QPlan &p, int t, cudaStream_t st) {
-    return launch_kernel(k_centroid_planes, dim3(p.C, p.H), dim3(kD), 0, st, p, t);
+    return launch_kernel(k_centroid_planes, dim3(p.Cpad, p.H), dim3(kD), 0, st, p, t);
 }
 
 // --------------------------------------------------------------------------------------
@@ -479,7 +500,8 @@ __device__ __forceinline__ float stored_mean(float S, float E, float n, int fmt)
     return store_centroid_value(m, __fadd_rn(__fmaf_rn(-m, n, S), E), fmt);
 }
 
-// New centroid row j (lane l: channels 4l..4l+3), and its GEMM planes if requested.
+// New centroid row j (lane l: channels 4l..4l+3), and its assignment operands (as
+// k_centroid_planes writes them) if requested.
 __device__ __forceinline__ void write_centroid(const QPlan &p, int h, int t, int j, int lane,
                                                bool set, float4 cv, bool planes, float4 mu) {
     float *c = p.cent + h * p.cent_tstride + p.cent_off + (int64_t)(t - 1) * p.C * kD +
@@ -491,22 +513,24 @@ __device__ __forceinline__ void write_centroid(const QPlan &p, int h, int t, int
     if (!planes) return;
     const float ct[4] = {__fsub_rn(cv.x, mu.x), __fsub_rn(cv.y, mu.y), __fsub_rn(cv.z, mu.z),
                          __fsub_rn(cv.w, mu.w)};
-    __align__(8) __half hi[4], lo[4];
-    float ss = 0.f;
+    __align__(8) __half hi[4];
+    float ss = 0.f, dd = 0.f;
 #pragma unroll
     for (int k = 0; k < 4; k++) {
         hi[k] = __float2half_rn(ct[k]);
-        lo[k] = __float2half_rn(__fsub_rn(ct[k], __half2float(hi[k])));
+        const float dv = __fsub_rn(ct[k], __half2float(hi[k]));  // exact
         ss = __fmaf_rn(ct[k], ct[k], ss);
+        dd = __fmaf_rn(dv, dv, dd);
     }
-    *reinterpret_cast<uint2 *>(p.B + ((int64_t)h * kBPlanes * p.Cpad + j) * kD + 4 * lane) =
+    *reinterpret_cast<uint2 *>(p.B + ((int64_t)h * p.Cpad + j) * kD + 4 * lane) =
         *reinterpret_cast<uint2 *>(hi);
-    if (kBPlanes == 2)
-        *reinterpret_cast<uint2 *>(p.B + ((int64_t)(h * kBPlanes + 1) * p.Cpad + j) * kD +
-                                   4 * lane) = *reinterpret_cast<uint2 *>(lo);
 #pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-    if (lane == 0) p.cn[(int64_t)h * p.Cpad + j] = ss;
+    for (int o = 16; o >= 1; o >>= 1) {
+        ss += __shfl_xor_sync(0xffffffffu, ss, o);
+        dd += __shfl_xor_sync(0xffffffffu, dd, o);
+    }
+    write_offset_row(p, h, j, lane, ss);
+    if (lane == 0) p.cnd[(int64_t)h * p.Cpad + j] = make_float2(ss, sqrtf(dd));
 }
 
 // Cluster sums over chunks of 32 cluster-sorted positions.  The rows of each run (same

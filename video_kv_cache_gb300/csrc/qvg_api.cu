@@ -22,7 +22,7 @@ inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 
 inline int cpad_of(int C) { return (C + 31) / 32 * 32; }
 
 struct WsLayout {
-    size_t A, rnorm, dnorm, B, cn, mu, counts, offs, blockoff, ids, cid, psum, wsum, init_idx,
+    size_t A, rnorm, dnorm, B, Bx, cnd, mu, counts, offs, blockoff, ids, cid, psum, wsum, init_idx,
         stats, rq_count, rq, total;
     int nsb, nchunk;
 };
@@ -41,8 +41,9 @@ WsLayout ws_layout(int64_t H, int64_t N, int C, int T) {
         w.A = take((size_t)H * N * kD * 2);
         w.rnorm = take((size_t)H * N * 4);
         w.dnorm = take((size_t)H * N * 4);
-        w.B = take((size_t)H * kBPlanes * Cpad * kD * 2);
-        w.cn = take((size_t)H * Cpad * 4);
+        w.B = take((size_t)H * Cpad * kD * 2);
+        w.Bx = take((size_t)H * Cpad * kOffsetRow * 4);
+        w.cnd = take((size_t)H * Cpad * 8);
         w.mu = take((size_t)H * kD * 4);
         w.nsb = (int)((N + kSortBlock - 1) / kSortBlock);
         w.nchunk = (int)((N + kChunk - 1) / kChunk);
@@ -196,7 +197,8 @@ QPlan make_plan(const qvg_quant_params *prm, const void *X, const float *warm,
         p.rnorm = reinterpret_cast<float *>(ws + w.rnorm);
         p.dnorm = reinterpret_cast<float *>(ws + w.dnorm);
         p.B = reinterpret_cast<__half *>(ws + w.B);
-        p.cn = reinterpret_cast<float *>(ws + w.cn);
+        p.Bx = reinterpret_cast<float *>(ws + w.Bx);
+        p.cnd = reinterpret_cast<float2 *>(ws + w.cnd);
         p.mu = reinterpret_cast<float *>(ws + w.mu);
         p.counts = reinterpret_cast<int *>(ws + w.counts);
         p.offs = reinterpret_cast<int *>(ws + w.offs);
