@@ -277,11 +277,9 @@ struct AssignMaps {
     CUtensorMap a;
     CUtensorMap b;
     CUtensorMap bx;  // the offset rows
-    // row views for the cluster sums' gathers: X as [rows][128] (when every tensor starts
-    // on a whole row, x_stride % 128 == 0; gather = 0 otherwise) and the centroid tables
-    // as [rows][128] fp32
+    // row view for the cluster sums' gathers: X as [rows][128] (when every tensor starts on
+    // a whole row, x_stride % 128 == 0; gather = 0 otherwise)
     CUtensorMap x_rows;
-    CUtensorMap c_rows;
     int gather;
 };
 // Encodes the maps for plan p into caller-provided storage (no allocation).

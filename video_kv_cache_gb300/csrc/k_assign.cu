@@ -815,7 +815,8 @@ cudaError_t assign_encode(const QPlan &p, AssignMaps *m) {
                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
     }
-    // row views for the cluster sums (a box of one row of 128 elements, as gathers need)
+    // the row view of X for the cluster sums (a box of one row of 128 elements, as gathers
+    // need)
     m->gather = 0;
     if (p.x_stride % kD == 0) {
         const size_t eb = p.in_dtype == DT_F32 ? 4 : 2;
@@ -823,16 +824,11 @@ cudaError_t assign_encode(const QPlan &p, AssignMaps *m) {
                                        : p.in_dtype == DT_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                                                : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
         const cuuint64_t xrows = (cuuint64_t)(p.H - 1) * (p.x_stride / kD) + (cuuint64_t)p.N;
-        const cuuint64_t crows = (cuuint64_t)p.H * (p.cent_tstride / kD);
         const cuuint32_t box[2] = {(cuuint32_t)kD, 1};
         const cuuint32_t estr2[2] = {1, 1};
         const cuuint64_t xdims[2] = {(cuuint64_t)kD, xrows}, xstr[1] = {(cuuint64_t)kD * eb};
-        const cuuint64_t cdims[2] = {(cuuint64_t)kD, crows}, cstr[1] = {(cuuint64_t)kD * 4};
-        if (xrows < (1ull << 31) && crows < (1ull << 31) && p.cent_tstride % kD == 0 &&
+        if (xrows < (1ull << 31) &&
             enc(&m->x_rows, dt, 2, const_cast<void *>(p.X), xdims, xstr, box, estr2,
-                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS &&
-            enc(&m->c_rows, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, p.cent, cdims, cstr, box, estr2,
                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS)
             m->gather = 1;

@@ -370,28 +370,6 @@ __device__ __forceinline__ void acc_two_sum(float &s, float &e, float x) {
     e = __fadd_rn(e, err);
 }
 
-// Two lanes of fp32 at once (packed f32x2 instructions).  a - b is taken as fma(b, -1, a),
-// which rounds the same exact difference once, so every result equals the scalar form's.
-__device__ __forceinline__ float2 sub2(float2 a, float2 b) {
-    return __ffma2_rn(b, make_float2(-1.f, -1.f), a);
-}
-// acc_two_sum on a pair: s + x with its exact rounding error added to e
-__device__ __forceinline__ void acc_two_sum2(float2 &s, float2 &e, float2 x) {
-    const float2 sn = __fadd2_rn(s, x);
-    const float2 bb = sub2(sn, s);
-    const float2 err = __fadd2_rn(sub2(s, sub2(sn, bb)), sub2(x, bb));
-    e = __fadd2_rn(e, err);
-    s = sn;
-}
-// a - c on a pair with its exact rounding error: a - c = d + err exactly (TwoSum of a and
-// -c, the negation folded into the last step)
-__device__ __forceinline__ float2 two_diff2(float2 a, float2 c, float2 &err) {
-    const float2 d = sub2(a, c);
-    const float2 bb = sub2(d, a);
-    err = sub2(sub2(a, sub2(d, bb)), __fadd2_rn(c, bb));
-    return d;
-}
-
 __global__ void __launch_bounds__(kSortBlock) k_sort_hist(QPlan p, int t) {
     pdl_begin();
     __shared__ int hist[kMaxC];
@@ -537,8 +515,8 @@ __device__ __forceinline__ void write_centroid(const QPlan &p, int h, int t, int
 // cluster) are added with TwoSum in sorted order.  A run that is a whole cluster leaves its
 // (sum, error) in the cluster's slot; a run that crosses the chunk's start or end leaves it
 // in the chunk's first / last slot.  k_cluster_finalize turns them into means.  Stage 1
-// (nothing to subtract) fits 64 registers, so four CTAs share an SM; later stages are bound
-// by their shared-memory row slots to two.
+// (nothing to subtract) fits 64 registers, so four CTAs share an SM; the second stage (one
+// subtraction) three, later ones, with the longer chain, two.
 //
 // The summed rows are the stage input R^(t-1): X itself at stage 1, later a residual that
 // is not stored but rebuilt here from X and the earlier stages' centroid rows (L2-resident)
@@ -551,15 +529,17 @@ __device__ __forceinline__ void write_centroid(const QPlan &p, int h, int t, int
 //   * persistent warps, each striding over the chunks of all tensors; lane m holds sorted
 //     position m of a chunk (its token, cluster and earlier clusters), and the next chunk's
 //     ids and pi bytes are read while the current chunk is summed;
-//   * the rows reach shared memory by bulk copies that each lane issues for its own
-//     position, eight rows to a group on one mbarrier, two groups in flight ahead of the
-//     sums, running on from one chunk into the next.
+//   * the X rows reach shared memory by TMA gathers (or bulk copies that each lane issues
+//     for its own position), eight rows to a group on one mbarrier, two groups in flight
+//     ahead of the sums, running on from one chunk into the next;
+//   * a lane reads its four channels of each earlier stage's centroid row (16 bytes, from
+//     L2, where the tables stay) with one vector load while it sums, so the shared-memory
+//     ring holds X rows only and more warps fit on an SM to keep those loads in flight.
 constexpr int kBulkGroup = 8;  // rows a group (one mbarrier phase)
 __host__ __device__ constexpr int bulk_xbytes(int src) { return src == 1 ? 512 : 256; }
-__host__ __device__ inline int bulk_row_bytes(int src, int tp) { return bulk_xbytes(src) + tp * 512; }
 // warps per CTA: as many as fit 96 KB of row slots (two groups a warp), at most 8
-__host__ __device__ inline int bulk_warps(int src, int tp) {
-    const int w = 98304 / (2 * kBulkGroup * bulk_row_bytes(src, tp));
+__host__ __device__ inline int bulk_warps(int src) {
+    const int w = 98304 / (2 * kBulkGroup * bulk_xbytes(src));
     return w > 8 ? 8 : (w < 1 ? 1 : w);
 }
 
@@ -584,15 +564,14 @@ struct SumChunk {
 };
 
 template <int SRC, int TP>  // SRC: X dtype (0 bf16, 1 fp32, 3 fp16); TP: t - 1 (0..3), or -1
-__global__ void __launch_bounds__(256, TP == 0 ? 4 : 2)
-    k_chunk_sums(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmC,
-                 QPlan p, int t, int gather) {
+__global__ void __launch_bounds__(256, TP == 0 ? 4 : (TP == 1 ? 3 : 2))
+    k_chunk_sums(const __grid_constant__ CUtensorMap tmX, QPlan p, int t, int gather) {
     pdl_begin();
     static_assert(kChunk == 32, "one sorted position per lane");
     constexpr int XB = bulk_xbytes(SRC);
     extern __shared__ __align__(128) uint8_t bulk_smem[];
     const int tp = TP >= 0 ? TP : t - 1;
-    const int row_bytes = XB + tp * 512;
+    constexpr int row_bytes = XB;
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
     const int wpc = blockDim.x >> 5;
     const int total = p.H * p.nchunk;
@@ -640,8 +619,7 @@ __global__ void __launch_bounds__(256, TP == 0 ? 4 : 2)
 
     uint32_t n_issued = 0, n_done = 0;  // groups issued / summed by this warp so far
     // Group g of chunk m (positions 8g..8g+7) goes to half (n_issued & 1) of the warp's
-    // slots: its X rows at the half's start (XB bytes each), then for each earlier stage
-    // the 8 centroid rows (512 bytes each).
+    // slots: its X rows (XB bytes each).
     auto issue = [&](const SumChunk &m, int g) {
         const int n_rows = min(kBulkGroup, m.nk - g * kBulkGroup);
         const int half = n_issued & 1;
@@ -660,15 +638,6 @@ __global__ void __launch_bounds__(256, TP == 0 ? 4 : 2)
 #pragma unroll
                 for (int k = 0; k < 4; k++) r[k] = __shfl_sync(0xffffffffu, m.xrow, src[k]);
                 if (lane == 0) tma_gather4(hb + 4 * u4 * XB, &tmX, 0, r[0], r[1], r[2], r[3], bar);
-                for (int st = 0; st < tp; st++) {
-                    const int pj = min((int)(((st < 4 ? m.pk0 : m.pk1) >> (8 * (st & 3))) & 255u), p.C - 1);
-                    const int crow = m.crow + st * p.C + pj;
-#pragma unroll
-                    for (int k = 0; k < 4; k++) r[k] = __shfl_sync(0xffffffffu, crow, src[k]);
-                    if (lane == 0)
-                        tma_gather4(hb + kBulkGroup * XB + st * kBulkGroup * 512 + 4 * u4 * 512, &tmC, 0,
-                                    r[0], r[1], r[2], r[3], bar);
-                }
             }
         } else {
             // one bulk copy per row, issued by the lane that holds the row
@@ -679,12 +648,6 @@ __global__ void __launch_bounds__(256, TP == 0 ? 4 : 2)
                 bulk_g2s(hb + u * XB,
                          static_cast<const char *>(p.X) + (m.h * p.x_stride + (int64_t)m.id * kD) * (XB / kD),
                          XB, bar);
-                const char *cb = reinterpret_cast<const char *>(p.cent + m.h * p.cent_tstride + p.cent_off);
-                for (int st = 0; st < tp; st++) {
-                    const int pj = min((int)(((st < 4 ? m.pk0 : m.pk1) >> (8 * (st & 3))) & 255u), p.C - 1);
-                    bulk_g2s(hb + kBulkGroup * XB + st * kBulkGroup * 512 + u * 512,
-                             cb + ((int64_t)st * p.C + pj) * kD * 4, 512, bar);
-                }
             }
         }
         n_issued++;
@@ -738,8 +701,8 @@ __global__ void __launch_bounds__(256, TP == 0 ? 4 : 2)
         // fp32 difference and r the sum of the chain's rounding errors; d goes through the
         // compensated sum and r is added to its error term, so the sum is that of the exact
         // residuals (to about twice fp32's precision), not of their fp32 roundings.
-        auto add_row = [&](const uint8_t *hs, int u) {
-            const uint8_t *slot = hs + u * XB;  // the X row; centroid rows follow all X rows
+        auto add_row = [&](const uint8_t *hs, int u, uint32_t q0, uint32_t q1) {
+            const uint8_t *slot = hs + u * XB;  // the X row
             float2 v01, v23;
             if constexpr (SRC == 0) {
                 const uint2 w = *reinterpret_cast<const uint2 *>(slot + lane * 8);
@@ -760,8 +723,9 @@ __global__ void __launch_bounds__(256, TP == 0 ? 4 : 2)
             } else {
                 float2 r01 = make_float2(0.f, 0.f), r23 = r01;
                 auto chain = [&](int st) {  // subtract the row of stage st + 1
-                    const float4 c = *reinterpret_cast<const float4 *>(
-                        hs + kBulkGroup * XB + st * kBulkGroup * 512 + u * 512 + lane * 16);
+                    const int pj = min((int)(((st < 4 ? q0 : q1) >> (8 * (st & 3))) & 255u), p.C - 1);
+                    const float4 c = __ldg(reinterpret_cast<const float4 *>(
+                        p.cent + (int64_t)(cur.crow + st * p.C + pj) * kD) + lane);
                     float2 t01, t23;
                     v01 = two_diff2(v01, make_float2(c.x, c.y), t01);
                     v23 = two_diff2(v23, make_float2(c.z, c.w), t23);
@@ -795,7 +759,11 @@ __global__ void __launch_bounds__(256, TP == 0 ? 4 : 2)
             if (n_rows == kBulkGroup && ((starts >> (g * kBulkGroup)) & 0xFFu) == 0u) {
                 // a full group inside one run (the usual case)
 #pragma unroll
-                for (int u = 0; u < kBulkGroup; u++) add_row(gslots, u);
+                for (int u = 0; u < kBulkGroup; u++) {
+                    const int m = g * kBulkGroup + u;
+                    add_row(gslots, u, TP != 0 ? __shfl_sync(0xffffffffu, cur.pk0, m) : 0u,
+                            TP < 0 ? __shfl_sync(0xffffffffu, cur.pk1, m) : 0u);
+                }
             } else {
 #pragma unroll 1
                 for (int u = 0; u < n_rows; u++) {
@@ -806,7 +774,8 @@ __global__ void __launch_bounds__(256, TP == 0 ? 4 : 2)
                         run_start = m;
                         s01 = s23 = e01 = e23 = make_float2(0.f, 0.f);
                     }
-                    add_row(gslots, u);
+                    add_row(gslots, u, TP != 0 ? __shfl_sync(0xffffffffu, cur.pk0, m) : 0u,
+                            TP < 0 ? __shfl_sync(0xffffffffu, cur.pk1, m) : 0u);
                 }
             }
             n_done++;
@@ -827,8 +796,8 @@ template <int SRC, int TP>
 static cudaError_t launch_sums(const QPlan &p, const AssignMaps *maps, int t, int num_sms,
                                cudaStream_t st) {
     const int tp = TP >= 0 ? TP : t - 1;
-    const int wpc = bulk_warps(SRC, tp);
-    const int smem = 128 + wpc * 2 * kBulkGroup * bulk_row_bytes(SRC, tp);
+    const int wpc = bulk_warps(SRC);
+    const int smem = 128 + wpc * 2 * kBulkGroup * bulk_xbytes(SRC);
     cudaError_t e = cudaFuncSetAttribute(k_chunk_sums<SRC, TP>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
@@ -844,7 +813,7 @@ static cudaError_t launch_sums(const QPlan &p, const AssignMaps *maps, int t, in
     const int64_t need = ((int64_t)p.H * p.nchunk + wpc - 1) / wpc;
     const int grid = (int)std::min<int64_t>(need, (int64_t)per_sm * num_sms);
     return launch_kernel(k_chunk_sums<SRC, TP>, dim3(grid), dim3(32 * wpc), smem, st, maps->x_rows,
-                         maps->c_rows, p, t, maps->gather);
+                         p, t, maps->gather);
 }
 
 // One warp per cluster: the mean from the cluster's own slot, or, for clusters spread over
