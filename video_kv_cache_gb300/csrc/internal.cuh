@@ -112,6 +112,28 @@ __device__ __forceinline__ void tf32_split3(float v, float &h, float &m, float &
     l = __fsub_rn(r, m);
 }
 
+// Two lanes of fp32 at once (packed f32x2 instructions).  a - b is taken as fma(b, -1, a),
+// which rounds the same exact difference once, so every result equals the scalar form's.
+__device__ __forceinline__ float2 sub2(float2 a, float2 b) {
+    return __ffma2_rn(b, make_float2(-1.f, -1.f), a);
+}
+// s + x on a pair, its exact rounding error added to e (compensated accumulation)
+__device__ __forceinline__ void acc_two_sum2(float2 &s, float2 &e, float2 x) {
+    const float2 sn = __fadd2_rn(s, x);
+    const float2 bb = sub2(sn, s);
+    const float2 err = __fadd2_rn(sub2(s, sub2(sn, bb)), sub2(x, bb));
+    e = __fadd2_rn(e, err);
+    s = sn;
+}
+// a - c on a pair with its exact rounding error: a - c = d + err exactly (TwoSum of a and
+// -c, the negation folded into the last step)
+__device__ __forceinline__ float2 two_diff2(float2 a, float2 c, float2 &err) {
+    const float2 d = sub2(a, c);
+    const float2 bb = sub2(d, a);
+    err = sub2(sub2(a, sub2(d, bb)), __fadd2_rn(c, bb));
+    return d;
+}
+
 // 8 consecutive input channels of X as fp32 (exact for fp16 / bf16).
 __device__ __forceinline__ void load_x8(const void *X, int dt, int64_t off, float v[8]) {
     if (dt == DT_F32) {

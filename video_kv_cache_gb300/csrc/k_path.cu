@@ -168,8 +168,98 @@ cudaError_t launch_centre(const QPlan &p, int t, cudaStream_t st) {
 }
 
 // --------------------------------------------------------------------------------------
+// The stage input of channels 8*c8 .. 8*c8+7 of G tokens: x minus the earlier stages'
+// assigned centroid rows C^(1)[pi^(1)_i], ..., C^(n)[pi^(n)_i], subtracted in that order by
+// a packed TwoSum chain whose collected rounding errors are added back at the end, so each
+// value is the fp32 number nearest the exact residual (the same value every kernel that
+// rebuilds the stage input forms).  v holds X's values on entry.  NST: the number of earlier
+// stages when it is fixed at compile time (every token's cluster indices, then every
+// centroid row, are loaded before any arithmetic), or -1 for n given at run time.  An index
+// >= C is clamped to C - 1 and reported through bad_index.
+// --------------------------------------------------------------------------------------
+template <int G, int NST>
+__device__ __forceinline__ void stage_input8(const QPlan &p, int h, const int64_t (&i)[G],
+                                             const bool (&valid)[G], int c8, int n,
+                                             float2 (&v)[G][4], bool &bad_index) {
+    if constexpr (NST != 0) {
+        const float *tab = p.cent + h * p.cent_tstride + p.cent_off + c8 * 8;
+        auto index = [&](int g, int st) {
+            int j = 0;
+            if (valid[g]) {
+                j = p.pi[(int64_t)(h * p.T + st) * p.cap + p.tok_off + i[g]];
+                if (j >= p.C) {
+                    j = p.C - 1;
+                    bad_index = true;
+                }
+            }
+            return j;
+        };
+        float2 e[G][4];
+#pragma unroll
+        for (int g = 0; g < G; g++)
+#pragma unroll
+            for (int q = 0; q < 4; q++) e[g][q] = make_float2(0.f, 0.f);
+        auto sub_row = [&](int g, float4 a, float4 b) {
+            const float2 c[4] = {make_float2(a.x, a.y), make_float2(a.z, a.w), make_float2(b.x, b.y),
+                                 make_float2(b.z, b.w)};
+#pragma unroll
+            for (int q = 0; q < 4; q++) {
+                float2 t;
+                v[g][q] = two_diff2(v[g][q], c[q], t);
+                e[g][q] = __fadd2_rn(e[g][q], t);
+            }
+        };
+        if constexpr (NST > 0) {
+            int pj[G][NST];
+#pragma unroll
+            for (int g = 0; g < G; g++)
+#pragma unroll
+                for (int st = 0; st < NST; st++) pj[g][st] = index(g, st);
+            float4 ca[G][NST], cb[G][NST];
+#pragma unroll
+            for (int g = 0; g < G; g++)
+#pragma unroll
+                for (int st = 0; st < NST; st++) {
+                    const float4 *r = reinterpret_cast<const float4 *>(tab + ((int64_t)st * p.C + pj[g][st]) * kD);
+                    ca[g][st] = __ldg(r);
+                    cb[g][st] = __ldg(r + 1);
+                }
+#pragma unroll
+            for (int st = 0; st < NST; st++)
+#pragma unroll
+                for (int g = 0; g < G; g++) sub_row(g, ca[g][st], cb[g][st]);
+        } else {
+            for (int st = 0; st < n; st++) {
+#pragma unroll
+                for (int g = 0; g < G; g++) {
+                    const float4 *r = reinterpret_cast<const float4 *>(tab + ((int64_t)st * p.C + index(g, st)) * kD);
+                    sub_row(g, __ldg(r), __ldg(r + 1));
+                }
+            }
+        }
+#pragma unroll
+        for (int g = 0; g < G; g++)
+#pragma unroll
+            for (int q = 0; q < 4; q++) v[g][q] = __fadd2_rn(v[g][q], e[g][q]);
+    }
+}
+
+// 8 channels of X as four pairs; false when one is not finite
+__device__ __forceinline__ bool load_x8_pairs(const QPlan &p, int64_t off, float2 (&v)[4]) {
+    float x[8];
+    load_x8(p.X, p.in_dtype, off, x);
+    bool fin = true;
+#pragma unroll
+    for (int q = 0; q < 4; q++) {
+        v[q] = make_float2(x[2 * q], x[2 * q + 1]);
+        fin &= isfinite(x[2 * q]) && isfinite(x[2 * q + 1]);
+    }
+    return fin;
+}
+
+// --------------------------------------------------------------------------------------
 // Residual preparation for stage t.  One thread per (token, 8 channels).
-//   r      = fp32(x - sum_{s<t} C^(s)[pi^(s)_i]) via a TwoSum chain (one final rounding);
+//   r      = fp32(x - sum_{s<t} C^(s)[pi^(s)_i]) via the TwoSum chain (one final rounding);
 //            not stored: the kernels that need r again rebuild it by the same chain
 //   A      = fp16(r - mu)                (tensor-core operand of the assignment)
 //   rnorm  = ||r - mu||, fp32            (for the assignment's error margin)
@@ -179,10 +269,9 @@ cudaError_t launch_centre(const QPlan &p, int t, cudaStream_t st) {
 constexpr int kPrepTokens = 64;
 
 // G tokens per thread (16 threads per token, 8 channels each): all of a thread's loads are
-// issued before its arithmetic, so that G rows are in flight per thread.  CHAIN: the stage
-// subtracts earlier stages' centroids (t >= 2).  Stage 1 takes G = 4; the chained form
-// takes G = 1, where more tokens per thread cost more occupancy than they gain.
-template <int G, bool CHAIN>
+// issued before its arithmetic, so that G rows are in flight per thread.  NST: earlier
+// stages (0 at stage 1), -1 when given at run time (t - 1).
+template <int G, int NST>
 __global__ void __launch_bounds__(256) k_prep(QPlan p, int t) {
     pdl_begin();
     const int h = blockIdx.y;
@@ -195,83 +284,45 @@ __global__ void __launch_bounds__(256) k_prep(QPlan p, int t) {
 #pragma unroll 1
     for (int64_t ib = i0; ib < i1; ib += 16 * G) {
         // the loop bound is uniform over the block, so every lane reaches the shuffles
-        float s[G][8];
+        float2 v[G][4];
+        int64_t ii[G];
+        bool valid[G];
 #pragma unroll
         for (int g = 0; g < G; g++) {
-            const int64_t i = ib + 16 * g + (threadIdx.x >> 4);
-            if (i < i1) {
-                load_x8(p.X, p.in_dtype, h * p.x_stride + i * kD + c8 * 8, s[g]);
+            ii[g] = ib + 16 * g + (threadIdx.x >> 4);
+            valid[g] = ii[g] < i1;
+            if (valid[g]) {
+                finite &= load_x8_pairs(p, h * p.x_stride + ii[g] * kD + c8 * 8, v[g]);
             } else {
 #pragma unroll
-                for (int q = 0; q < 8; q++) s[g][q] = 0.f;
+                for (int q = 0; q < 4; q++) v[g][q] = make_float2(0.f, 0.f);
             }
-#pragma unroll
-            for (int q = 0; q < 8; q++) finite &= isfinite(s[g][q]);
         }
-        if constexpr (CHAIN) {
-            float e[G][8];
-#pragma unroll
-            for (int g = 0; g < G; g++)
-#pragma unroll
-                for (int q = 0; q < 8; q++) e[g][q] = 0.f;
-            for (int st = 1; st < t; st++) {
-                int pj[G];
-#pragma unroll
-                for (int g = 0; g < G; g++) {
-                    const int64_t i = ib + 16 * g + (threadIdx.x >> 4);
-                    pj[g] = 0;
-                    if (i < i1) {
-                        pj[g] = p.pi[(int64_t)(h * p.T + st - 1) * p.cap + p.tok_off + i];
-                        if (pj[g] >= p.C) {
-                            pj[g] = p.C - 1;
-                            bad_index = true;
-                        }
-                    }
-                }
-                float c[G][8];
-#pragma unroll
-                for (int g = 0; g < G; g++)
-                    load_f8(p.cent + h * p.cent_tstride + p.cent_off + (int64_t)(st - 1) * p.C * kD +
-                                (int64_t)pj[g] * kD + c8 * 8, c[g]);
-#pragma unroll
-                for (int g = 0; g < G; g++)
-#pragma unroll
-                    for (int q = 0; q < 8; q++) {
-                        float err;
-                        two_sum(s[g][q], -c[g][q], s[g][q], err);
-                        e[g][q] = __fadd_rn(e[g][q], err);
-                    }
-            }
-#pragma unroll
-            for (int g = 0; g < G; g++)
-#pragma unroll
-                for (int q = 0; q < 8; q++) s[g][q] = __fadd_rn(s[g][q], e[g][q]);
-        }
+        stage_input8<G, NST>(p, h, ii, valid, c8, t - 1, v, bad_index);
 #pragma unroll
         for (int g = 0; g < G; g++) {
-            const int64_t i = ib + 16 * g + (threadIdx.x >> 4);
-            const bool valid = i < i1;
             float ss = 0.f, dd = 0.f;
             __align__(16) __half a16[8];
 #pragma unroll
             for (int q = 0; q < 8; q++) {
-                const float v = __fsub_rn(s[g][q], mu[q]);
-                a16[q] = __float2half_rn(v);
-                const float dv = __fsub_rn(v, __half2float(a16[q]));  // exact
-                ss = __fmaf_rn(v, v, ss);
-                dd = __fmaf_rn(dv, dv, dd);
+                const float s = q & 1 ? v[g][q >> 1].y : v[g][q >> 1].x;
+                const float x = __fsub_rn(s, mu[q]);
+                a16[q] = __float2half_rn(x);
+                const float dx = __fsub_rn(x, __half2float(a16[q]));  // exact
+                ss = __fmaf_rn(x, x, ss);
+                dd = __fmaf_rn(dx, dx, dd);
             }
-            if (valid)
-                *reinterpret_cast<uint4 *>(p.A + ((int64_t)h * p.N + i) * kD + c8 * 8) =
+            if (valid[g])
+                *reinterpret_cast<uint4 *>(p.A + ((int64_t)h * p.N + ii[g]) * kD + c8 * 8) =
                     *reinterpret_cast<uint4 *>(a16);
 #pragma unroll
             for (int o = 8; o >= 1; o >>= 1) {
                 ss += __shfl_xor_sync(0xffffffffu, ss, o);
                 dd += __shfl_xor_sync(0xffffffffu, dd, o);
             }
-            if (valid && c8 == 0) {
-                p.rnorm[h * p.N + i] = sqrtf(ss);
-                p.dnorm[h * p.N + i] = sqrtf(dd);
+            if (valid[g] && c8 == 0) {
+                p.rnorm[h * p.N + ii[g]] = sqrtf(ss);
+                p.dnorm[h * p.N + ii[g]] = sqrtf(dd);
             }
         }
     }
@@ -290,8 +341,13 @@ __global__ void __launch_bounds__(256) k_prep(QPlan p, int t) {
 
 cudaError_t launch_prep(const QPlan &p, int t, cudaStream_t st) {
     dim3 grid((unsigned)((p.N + kPrepTokens - 1) / kPrepTokens), p.H);
-    if (t == 1) return launch_kernel(k_prep<4, false>, grid, dim3(256), 0, st, p, t);
-    return launch_kernel(k_prep<1, true>, grid, dim3(256), 0, st, p, t);
+    switch (t - 1) {
+        case 0: return launch_kernel(k_prep<4, 0>, grid, dim3(256), 0, st, p, t);
+        case 1: return launch_kernel(k_prep<2, 1>, grid, dim3(256), 0, st, p, t);
+        case 2: return launch_kernel(k_prep<2, 2>, grid, dim3(256), 0, st, p, t);
+        case 3: return launch_kernel(k_prep<2, 3>, grid, dim3(256), 0, st, p, t);
+        default: return launch_kernel(k_prep<1, -1>, grid, dim3(256), 0, st, p, t);
+    }
 }
 
 // --------------------------------------------------------------------------------------
@@ -937,70 +993,36 @@ __global__ void __launch_bounds__(256) k_encode(QPlan p) {
         // the loop bound is uniform over the block, so every lane reaches the shuffles;
         // rows past the end compute on zeros and store nothing.  The kEncG tokens of a
         // thread load together: X, then their cluster indices, then the centroid rows.
-        float sg[kEncG][8], eg[kEncG][8];
+        float2 v[kEncG][4];
+        int64_t ii[kEncG];
+        bool ok[kEncG];
 #pragma unroll
         for (int g = 0; g < kEncG; g++) {
-            const int64_t i = ib + 16 * g + (threadIdx.x >> 4);
-            if (i < i1) {
-                load_x8(p.X, p.in_dtype, h * p.x_stride + i * kD + c8 * 8, sg[g]);
+            ii[g] = ib + 16 * g + (threadIdx.x >> 4);
+            ok[g] = ii[g] < i1;
+            if (ok[g]) {
+                float x[8];
+                load_x8(p.X, p.in_dtype, h * p.x_stride + ii[g] * kD + c8 * 8, x);
+#pragma unroll
+                for (int q = 0; q < 4; q++) {
+                    v[g][q] = make_float2(x[2 * q], x[2 * q + 1]);
+                    nanprobe = __fmaf_rn(x[2 * q], 0.f, __fmaf_rn(x[2 * q + 1], 0.f, nanprobe));
+                }
             } else {
 #pragma unroll
-                for (int q = 0; q < 8; q++) sg[g][q] = 0.f;
-            }
-#pragma unroll
-            for (int q = 0; q < 8; q++) {
-                nanprobe = __fmaf_rn(sg[g][q], 0.f, nanprobe);
-                eg[g][q] = 0.f;
+                for (int q = 0; q < 4; q++) v[g][q] = make_float2(0.f, 0.f);
             }
         }
-        // r = x - C^(1)[pi^(1)] - ... - C^(T)[pi^(T)] rounded once (TwoSum chain)
-        auto subtract = [&](int g, int st, int pj) {
-            if (pj >= p.C) {
-                pj = p.C - 1;
-                bad_index = true;
-            }
-            float c[8];
-            load_f8(p.cent + h * p.cent_tstride + p.cent_off + (int64_t)(st - 1) * p.C * kD +
-                        (int64_t)pj * kD + c8 * 8, c);
-#pragma unroll
-            for (int q = 0; q < 8; q++) {
-                float err;
-                two_sum(sg[g][q], -c[q], sg[g][q], err);
-                eg[g][q] = __fadd_rn(eg[g][q], err);
-            }
-        };
-        if constexpr (TT >= 0) {
-            int pjs[kEncG][TT > 0 ? TT : 1];
-#pragma unroll
-            for (int g = 0; g < kEncG; g++) {
-                const int64_t i = ib + 16 * g + (threadIdx.x >> 4);
-#pragma unroll
-                for (int st = 1; st <= TT; st++)
-                    pjs[g][st - 1] = i < i1 ? p.pi[(int64_t)(h * p.T + st - 1) * p.cap + p.tok_off + i] : 0;
-            }
-#pragma unroll
-            for (int st = 1; st <= TT; st++)
-#pragma unroll
-                for (int g = 0; g < kEncG; g++) subtract(g, st, pjs[g][st - 1]);
-        } else {
-#pragma unroll
-            for (int g = 0; g < kEncG; g++) {
-                const int64_t i = ib + 16 * g + (threadIdx.x >> 4);
-                if (i < i1)
-                    for (int st = 1; st <= T; st++)
-                        subtract(g, st, p.pi[(int64_t)(h * p.T + st - 1) * p.cap + p.tok_off + i]);
-            }
-        }
+        // r = x - C^(1)[pi^(1)] - ... - C^(T)[pi^(T)] rounded once (the TwoSum chain)
+        stage_input8<kEncG, TT>(p, h, ii, ok, c8, T, v, bad_index);
 #pragma unroll
         for (int g = 0; g < kEncG; g++) {
-            const int64_t i = ib + 16 * g + (threadIdx.x >> 4);
-            const bool valid = i < i1;
-            const float (&s)[8] = sg[g];
-            const float (&e)[8] = eg[g];
+            const int64_t i = ii[g];
+            const bool valid = ok[g];
             float r[8], a = 0.f;
 #pragma unroll
             for (int q = 0; q < 8; q++) {
-                r[q] = __fadd_rn(s[q], e[q]);
+                r[q] = q & 1 ? v[g][q >> 1].y : v[g][q >> 1].x;
                 a = fmaxf(a, fabsf(r[q]));
             }
             for (int o = 1; o < lpg; o <<= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
