@@ -163,7 +163,11 @@ qvg_status qvg_quantize(const qvg_quant_params *params, const void *X,
                         const float *warm_centroids, const qvg_buffers *out, void *workspace,
                         size_t workspace_bytes, uint32_t *dev_status, void *stream);
 
-/* Size of the fixed scratch area behind qvg_quantize_static: 64 MiB per device. */
+/* Size of the fixed scratch area behind qvg_quantize_static: 64 MiB per device.  The area is
+ * part of libqvg's device code, so it is reserved on every device (in every CUDA context)
+ * where that code is loaded -- whichever entry points the process calls, qvg_quantize,
+ * qvg_dequantize and qvg_attention included.  A caller sizing a KV pool to the last
+ * megabyte should count it. */
 #define QVG_STATIC_SCRATCH_BYTES ((size_t)64 << 20)
 
 /* qvg_quantize without a workspace argument, for callers that cannot allocate.
@@ -186,12 +190,14 @@ qvg_status qvg_quantize(const qvg_quant_params *params, const void *X,
  * tensor of up to about 175 000 tokens fits, 24 tensors of up to about 6 400 each (154 000
  * rows), 100 tensors of up to about 780 each.
  *
- * First call on a device: the first call made while a given device is current looks up
- * the area's device address once (cudaGetSymbolAddress, which can load the library's
- * device code on that device); if that fails the call returns QVG_ERR_CUDA.  Make this
- * first call before any stream capture begins on that device.  Later calls reuse the
- * address; after cudaDeviceReset it is stale, so do not call this function again in that
- * process.
+ * First call in a context: the area's device address belongs to the CUDA context whose
+ * copy of the library's device code holds it, so the first call made while a given context
+ * is current (a device's primary context, or one the caller created and made current) looks
+ * it up once (cudaGetSymbolAddress, which can load the library's device code in that
+ * context); if that fails the call returns QVG_ERR_CUDA.  Make this first call before any
+ * stream capture begins in that context.  Later calls in the same context reuse the
+ * address.  After cudaDeviceReset, or once a context is destroyed, the address kept for it
+ * is stale: do not call this function again in that process.
  *
  * Contents on entry do not matter: everything the path needs to start at zero is cleared
  * by the call itself, on `stream`, before it is used.
@@ -217,6 +223,18 @@ qvg_status qvg_quantize_static(const qvg_quant_params *params, const void *X,
 qvg_status qvg_reassign(const qvg_quant_params *params, const void *X, const qvg_buffers *out,
                         void *workspace, size_t workspace_bytes, uint32_t *dev_status,
                         void *stream);
+
+/* Self-test of the assignment kernel's failure handling; no step of the method.  It runs the
+ * tensor-core assignment of qvg_reassign once with the load of the centroid operand withheld
+ * and a wait limit of one millisecond (2 s in normal calls), so that the kernel's first wait
+ * on that operand never completes: the wait gives up, the kernel ORs QVG_DEV_TIMEOUT into
+ * *dev_status, waits for the copies it did issue, frees its tensor memory and returns.  The
+ * device stays usable, and later calls run normally.  Arguments as for qvg_reassign; pi^(T)
+ * is left unspecified.  The device is never faulted or trapped. */
+qvg_status qvg_selftest_assign_timeout(const qvg_quant_params *params, const void *X,
+                                       const qvg_buffers *out, void *workspace,
+                                       size_t workspace_bytes, uint32_t *dev_status,
+                                       void *stream);
 
 /* Parameters of one qvg_dequantize call. */
 typedef struct {

@@ -81,17 +81,28 @@ def test_static_matches_workspace_entry_on_consecutive_calls(lib):
     _assert_same(sa, ra, st_sa, st_ra)
     _assert_same(sb, rb, st_sb, st_rb)
 
-    # once set up, a repeat of the first problem takes no device memory
+    # Once set up, a repeat of the first problem takes no device memory.  Checked two ways
+    # around one call: the device's free memory (cudaMemGetInfo, device-wide, so another
+    # process allocating in the same window can disturb it: on a mismatch the measurement is
+    # taken once more) and torch's caching-allocator counters (allocations made through this
+    # process's torch).  Neither sees host memory; the header's promise of no host heap is
+    # not tested here.
     torch.cuda.synchronize()
     out = api.allocate(2, XA.shape[1], 64, 2, 2, 32, 1, XA.device)
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     prm = _params(2, XA.shape[1], 64, 2, 2, 32, 4, XA.dtype, 7)
-    torch.cuda.synchronize()
-    free_before = torch.cuda.mem_get_info()[0]
-    rc = qvg.qvg_quantize_static(prm, XA.data_ptr(), None, out.buffers(), status.data_ptr(),
-                                 torch.cuda.current_stream().cuda_stream)
-    torch.cuda.synchronize()
-    free_after = torch.cuda.mem_get_info()[0]
-    assert rc == qvg.QVG_OK
-    assert free_after == free_before
+
+    def one_call():
+        torch.cuda.synchronize()
+        allocs = torch.cuda.memory_stats().get("allocation.all.allocated", 0)
+        free_before = torch.cuda.mem_get_info()[0]
+        rc = qvg.qvg_quantize_static(prm, XA.data_ptr(), None, out.buffers(), status.data_ptr(),
+                                     torch.cuda.current_stream().cuda_stream)
+        torch.cuda.synchronize()
+        free_after = torch.cuda.mem_get_info()[0]
+        assert rc == qvg.QVG_OK
+        assert torch.cuda.memory_stats().get("allocation.all.allocated", 0) == allocs
+        return free_after == free_before
+
+    assert one_call() or one_call(), "free device memory changed across two calls"
     _assert_same(out, ra, status, st_ra)

@@ -309,8 +309,11 @@ cudaError_t assign_encode(const QPlan &p, AssignMaps *maps);
 // Heap-allocates the maps and encodes them; free with assign_release.
 cudaError_t assign_prepare(const QPlan &p, AssignMaps **maps);
 void assign_release(AssignMaps *maps);
+// A pipeline wait in the assignment kernel gives up after this long (then it sets
+// QVG_DEV_TIMEOUT and the kernel unwinds); withhold_b only for the failure self-test.
+constexpr uint64_t kAssignWaitNs = 2000000000ull;
 cudaError_t launch_assign(const QPlan &p, const AssignMaps *maps, int t, int num_sms,
-                          cudaStream_t st);
+                          cudaStream_t st, uint64_t wait_ns = kAssignWaitNs, int withhold_b = 0);
 cudaError_t launch_refine(const QPlan &p, int t, int num_sms, cudaStream_t st);
 size_t assign_smem_bytes(int Cpad, int nslots);
 

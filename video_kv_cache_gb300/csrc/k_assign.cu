@@ -14,7 +14,7 @@
 //     with B rows (h_j, m_j, l_j, 0, ...), the exact three-part tf32 split of the fp32 value
 //     -||c_j||^2 / 2, issued first (it initialises the accumulator);
 //   * the product: eight kind::f16 MMAs (K = 16) of fp16(a) with fp16(c_j), accumulated.
-// The epilogue reads finished scores: a maximum per 32-column chunk, then candidate bits.
+// The epilogue reads finished scores: a maximum per 32-column chunk and candidate bits.
 //
 // Error bound.  Let A^ = fp16(a), B^_j = fp16(c_j) and dn = ||A^ - a||, dc_j = ||B^_j - c_j||,
 // both measured exactly in fp32 by the kernels that write the fp16 copies (typically about
@@ -42,15 +42,18 @@
 //   warp 1   TMEM allocator and MMA issuer (one thread): per tile one tf32 MMA and 2 x 4
 //            f16 MMAs of M = 128, N = Cpad into one of two TMEM accumulators.
 //   warps 2-17 epilogue, two groups of 8 warps taking alternate tiles: a warp reads 32
-//            TMEM lanes (one token row per thread) and half of the columns.  Pass A takes
-//            each 32-column chunk's largest score (64 columns per TMEM load); the pair of
-//            warps on the same rows exchanges them for the row's best, which fixes the
-//            near-tie limit.  Pass B re-reads the chunks that can hold a score above the
-//            limit and sets one candidate bit per score (the sign of score - limit, shifted
-//            in).  Then the accumulator is released; a row with one candidate gets it as
-//            pi, a row with several is queued for k_refine.
-// Every mbarrier wait is bounded; on timeout the kernel sets QVG_DEV_TIMEOUT, stops, waits
-// for its own copies and MMAs, frees TMEM and returns.
+//            TMEM lanes (one token row per thread) and half of the columns, 64 columns per
+//            TMEM load, once.  For each 32-column chunk it takes the largest score, updates
+//            the row's running best and sets one candidate bit per score at or above the
+//            running limit best - 2E (the sign of score - limit, shifted in).  The pair of
+//            warps on the same rows exchanges their bests for the row's; chunks whose
+//            largest score is below the row's limit are cleared (see the epilogue for why
+//            the rest is exact where it matters).  Then the accumulator is released; a row
+//            with one candidate gets it as pi, a row with several is queued for k_refine.
+// Every mbarrier wait is bounded (2 s by default, a launch argument); on timeout the kernel
+// sets QVG_DEV_TIMEOUT, stops, waits for its own copies and MMAs, frees TMEM and returns.
+// A self-test withholds the centroid operand's load so that the MMA warp's first wait runs
+// out (qvg_selftest_assign_timeout).
 #include <cuda.h>
 
 #include <algorithm>
@@ -68,7 +71,6 @@ constexpr uint32_t kKBlockBytes = kTileM * 64 * 2;  // 16 KB: 64 fp16 channels o
 constexpr int kABlocks = 2;                           // A blocks per tile (128 channels)
 constexpr uint32_t kAuxABytes = kTileM * 128;         // the constant tf32 block: 128 rows of 128 B
 constexpr uint32_t kSpinLimit = 1u << 22;
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // a pipeline wait gives up after 2 s
 // maximum of three fp32 values (one instruction on sm_100-class GPUs; NaN inputs are
 // ignored unless all three are NaN, as with fmaxf)
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
@@ -81,15 +83,16 @@ constexpr float kDnRel = 0x1.03p0f;   // 1.01
 constexpr float kAccRel = 0x1p-15f;
 
 // Bounded wait on a phase.  Gives up when another role already gave up, or after
-// kSpinLimit tries or kWaitLimitNs of wall time, whichever comes first (then it raises the
+// kSpinLimit tries or limit_ns of wall time, whichever comes first (then it raises the
 // abort flag itself).
-__device__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag) {
+__device__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                          uint64_t limit_ns) {
     if (mbar_try(bar, parity)) return true;
     const uint64_t t0 = global_ns();
     for (uint32_t n = 0; n < kSpinLimit; n++) {
         if (mbar_try_suspend(bar, parity)) return true;
         if (*abort_flag) return false;
-        if ((n & 15u) == 15u && global_ns() - t0 > kWaitLimitNs) break;
+        if ((n & 15u) == 15u && global_ns() - t0 > limit_ns) break;
     }
     *abort_flag = 1;
     return false;
@@ -248,7 +251,8 @@ __device__ __forceinline__ uint32_t make_idesc_tf32(int n) {
 __global__ void __launch_bounds__(kThreads, 1)
     k_assign(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
              const __grid_constant__ CUtensorMap tmBx, QPlan p, int t, int tiles_per_tensor,
-             int nslots, uint32_t tmem_cols, uint32_t acc_stride) {
+             int nslots, uint32_t tmem_cols, uint32_t acc_stride, uint64_t wait_ns,
+             int withhold_b) {
     pdl_begin();
     extern __shared__ unsigned char smem_raw[];
     unsigned char *sm = reinterpret_cast<unsigned char *>(
@@ -321,11 +325,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int h = (int)(tile / tiles_per_tensor);
                 const int m0 = (int)(tile - (int64_t)h * tiles_per_tensor) * kTileM;
                 if (h != cur_h) {
-                    if (nb > 0 && !mbar_wait(smem_u32(b_empty), (nb - 1) & 1, abort_flag)) break;
-                    mbar_expect_tx(smem_u32(b_full), 3 * bsub);
-                    for (int kb = 0; kb < 2; kb++)
-                        tma_load_3d(smem_u32(sB + kb * bsub), &tmB, kb * 64, 0, h, smem_u32(b_full));
-                    tma_load_3d(smem_u32(sBx), &tmBx, 0, 0, h, smem_u32(b_full));
+                    if (nb > 0 && !mbar_wait(smem_u32(b_empty), (nb - 1) & 1, abort_flag, wait_ns)) break;
+                    // (withhold_b: the failure self-test; b_full then never completes)
+                    if (!withhold_b) {
+                        mbar_expect_tx(smem_u32(b_full), 3 * bsub);
+                        for (int kb = 0; kb < 2; kb++)
+                            tma_load_3d(smem_u32(sB + kb * bsub), &tmB, kb * 64, 0, h, smem_u32(b_full));
+                        tma_load_3d(smem_u32(sBx), &tmBx, 0, 0, h, smem_u32(b_full));
+                    }
                     nb++;
                     cur_h = h;
                 }
@@ -334,7 +341,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int k = 0; k < kABlocks; k++) {
                     const uint32_t q = kABlocks * (uint32_t)lt + k, s = q % nslots,
                                    ph = (q / nslots) & 1u;
-                    if (!mbar_wait(smem_u32(a_empty + s), ph ^ 1u, abort_flag)) {
+                    if (!mbar_wait(smem_u32(a_empty + s), ph ^ 1u, abort_flag, wait_ns)) {
                         ok = false;
                         break;
                     }
@@ -346,7 +353,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!ok) break;
             }
             // make sure every copy this CTA started has landed before the CTA can exit
-            if (nb > 0) mbar_wait_final(smem_u32(b_full), (nb - 1) & 1);
+            if (nb > 0 && !withhold_b) mbar_wait_final(smem_u32(b_full), (nb - 1) & 1);
             const uint32_t first = issued > (uint32_t)nslots ? issued - nslots : 0u;
             for (uint32_t q = first; q < issued; q++)
                 mbar_wait_final(smem_u32(a_full + q % nslots), (q / nslots) & 1u);
@@ -364,14 +371,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int h = (int)(tile / tiles_per_tensor);
                 if (h != cur_h) {
                     if (nb > 0) tc_commit(smem_u32(b_empty));
-                    if (!mbar_wait(smem_u32(b_full), nb & 1, abort_flag)) break;
+                    if (!mbar_wait(smem_u32(b_full), nb & 1, abort_flag, wait_ns)) break;
                     nb++;
                     cur_h = h;
                 }
                 // tile lt goes to accumulator and epilogue group lt % 2, free once the
                 // group released its previous tile
                 const uint32_t buf = (uint32_t)lt & 1u, grp = buf, use = (uint32_t)lt >> 1;
-                if (!mbar_wait(smem_u32(acc_empty + grp), (use & 1u) ^ 1u, abort_flag)) break;
+                if (!mbar_wait(smem_u32(acc_empty + grp), (use & 1u) ^ 1u, abort_flag, wait_ns)) break;
                 tc_fence_after();
                 const uint32_t d = tmem + buf * acc_stride;
                 // the per-column offset -||c_j||^2 / 2 first: it initialises the accumulator
@@ -381,7 +388,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 bool ok = true;
                 for (int k = 0; k < kABlocks && ok; k++) {
                     const uint32_t q = kABlocks * (uint32_t)lt + k, s = q % nslots;
-                    if (!mbar_wait(smem_u32(a_full + s), (q / nslots) & 1u, abort_flag)) {
+                    if (!mbar_wait(smem_u32(a_full + s), (q / nslots) & 1u, abort_flag, wait_ns)) {
                         ok = false;
                         break;
                     }
@@ -447,7 +454,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 cmax = sqrtf(m2) * 1.000001f;
                 dcmax = md;
             }
-            const bool ok = mbar_wait(smem_u32(acc_full + grp), use & 1u, abort_flag);
+            const bool ok = mbar_wait(smem_u32(acc_full + grp), use & 1u, abort_flag, wait_ns);
             // every warp of the group takes the same branch after the bounded wait
             uint32_t any_fail;
             asm volatile(
@@ -460,57 +467,72 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + buf * acc_stride +
                                    (uint32_t)(ch_lo * 32);
-            // Pass A: each chunk's largest score, two chunks per TMEM load.
+            // The row's margin: every cluster whose score is within twice the error bound of
+            // the best may be the nearest one (bound in the file header).
+            const float cm1 = cmax + dcmax;
+            const float two_err = 2.f * (kDnRel * dn * cm1 + kDnRel * rn * dcmax +
+                                         kAccRel * ((rn + dn) * cm1 + cmax2) + 0x1p-20f * (rn + dn)) +
+                                  1e-30f;
+            // An untrusted row (fp16 operands may have overflowed, so its scores may be inf
+            // or NaN) takes every cluster as a candidate.
+            const bool trusted = rn < kFp16Safe && cmax < kFp16Safe;
+            // One pass over this warp's chunks, two per TMEM load: each chunk's largest score,
+            // the running best of the row, and candidate bits against the running limit
+            // best - 2E.  A chunk read before the row's final best gets its bits against a
+            // lower limit, a superset of its true candidates; below, a chunk whose largest
+            // score is under the final limit is cleared, and one above it holds a true
+            // candidate, so its row goes to exact re-scoring anyway.  The chunk holding the
+            // best is always read with the final limit, so a row's single candidate is exact.
             float cm[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+            uint32_t cand[4] = {0u, 0u, 0u, 0u};
+            float own = -INFINITY;
             {
                 float v[64];
                 if (nc >= 2) {
                     tc_ld64(taddr, v);
                     cm[0] = chunk_max(v);
                     cm[1] = chunk_max(v + 32);
+                    own = fmaxf(cm[0], cm[1]);
+                    const float lim = own - two_err;
+                    cand[0] = chunk_cands(v, lim);
+                    cand[1] = chunk_cands(v + 32, lim);
                 }
                 if (nc == 4) {
                     tc_ld64(taddr + 64, v);
                     cm[2] = chunk_max(v);
                     cm[3] = chunk_max(v + 32);
-                } else if (nc == 3) {
-                    tc_ld32(taddr + 64, v);
-                    cm[2] = chunk_max(v);
-                } else if (nc == 1) {
-                    tc_ld32(taddr, v);
-                    cm[0] = chunk_max(v);
+                    own = fmax3(own, cm[2], cm[3]);
+                    const float lim = own - two_err;
+                    cand[2] = chunk_cands(v, lim);
+                    cand[3] = chunk_cands(v + 32, lim);
+                } else if (nc & 1) {
+                    const int c = nc - 1;  // 0 or 2
+                    tc_ld32(taddr + c * 32, v);
+                    const float m = chunk_max(v);
+                    own = fmaxf(own, m);
+                    const uint32_t w = chunk_cands(v, own - two_err);
+                    if (c == 0) {
+                        cm[0] = m;
+                        cand[0] = w;
+                    } else {
+                        cm[2] = m;
+                        cand[2] = w;
+                    }
                 }
             }
-            const float own = fmaxf(fmaxf(cm[0], cm[1]), fmaxf(cm[2], cm[3]));
             // the row's best score over both column halves
             xb[half * kTileM + row] = own;
             asm volatile("bar.sync %0, 64;" ::"r"(pair_bar) : "memory");
             const float best = fmaxf(own, xb[(half ^ 1) * kTileM + row]);
-            // Every cluster whose score is within twice the error bound of the best may be
-            // the nearest one (bound in the file header).
-            const float cm1 = cmax + dcmax;
-            const float err = kDnRel * dn * cm1 + kDnRel * rn * dcmax +
-                              kAccRel * ((rn + dn) * cm1 + cmax2) + 0x1p-20f * (rn + dn);
-            // An untrusted row (fp16 operands may have overflowed, so its scores may be inf
-            // or NaN) takes every cluster as a candidate.
-            const bool trusted = rn < kFp16Safe && cmax < kFp16Safe;
-            const float lim = trusted ? best - (2.f * err + 1e-30f) : -INFINITY;
-            // Pass B: the candidate clusters (score >= lim), one bit per column, over the
-            // chunks that hold a candidate for some row of the warp.  The best score is
-            // always a candidate; a row with a single candidate has its nearest centroid, a
-            // row with several goes to exact re-scoring.
-            uint32_t cand[4] = {0u, 0u, 0u, 0u};
+            const float lim = trusted ? best - two_err : -INFINITY;
 #pragma unroll
             for (int c = 0; c < 4; c++) {
-                if (c >= nc) break;
-                if (!__any_sync(0xffffffffu, !(cm[c] < lim))) continue;
-                float v[32];
-                tc_ld32(taddr + c * 32, v);
-                uint32_t w = trusted ? chunk_cands(v, lim) : 0xFFFFFFFFu;
+                uint32_t w = trusted ? (cm[c] < lim ? 0u : cand[c]) : 0xFFFFFFFFu;
                 // only real clusters (padded columns score -2^100, but an untrusted row's
                 // padded columns are set above)
                 const int live = C - (ch_lo + c) * 32;
-                if (live < 32) w &= (1u << live) - 1u;
+                if (c >= nc) w = 0u;
+                else if (live < 32) w &= (1u << live) - 1u;
                 cand[c] = w;
             }
             tc_fence_before();
@@ -852,7 +874,7 @@ cudaError_t assign_prepare(const QPlan &p, AssignMaps **out) {
 void assign_release(AssignMaps *maps) { delete maps; }
 
 cudaError_t launch_assign(const QPlan &p, const AssignMaps *maps, int t, int num_sms,
-                          cudaStream_t st) {
+                          cudaStream_t st, uint64_t wait_ns, int withhold_b) {
     const int tiles = (int)((p.N + kTileM - 1) / kTileM);
     const int64_t total = (int64_t)tiles * p.H;
     const int grid = (int)std::min<int64_t>(total, num_sms);
@@ -870,7 +892,7 @@ cudaError_t launch_assign(const QPlan &p, const AssignMaps *maps, int t, int num
     e = cudaFuncSetAttribute(k_assign, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     return launch_kernel(k_assign, dim3(grid), dim3(kThreads), smem, st, maps->a, maps->b, maps->bx,
-                         p, t, tiles, nslots, cols, stride);
+                         p, t, tiles, nslots, cols, stride, wait_ns, withhold_b);
 }
 
 cudaError_t launch_refine(const QPlan &p, int t, int num_sms, cudaStream_t st) {

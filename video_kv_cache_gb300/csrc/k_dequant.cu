@@ -20,7 +20,8 @@
 //     2^23 (one logic op), one subtraction gives (u - 2^(b-1)) * 2^k exactly, and
 //     y = fma(s_q * 2^-k, that, C^(T)) (s_q * q is exact, so this equals adding C^(T) to
 //     the dequantized value); then one add per further stage, T - 1 down to 1, in fp32,
-//     rounded once to the output type.
+//     rounded once to the output type.  The subtraction, the fma and the adds run on f32x2
+//     pairs of neighbouring channels (each half rounds as the scalar operation does).
 //   * A staged table row's 16-byte chunks are stored XOR-swizzled, so a quarter-warp's
 //     16-byte reads hit distinct bank groups.
 //   * A lane writes its 16 outputs with one 32-byte store (two for fp32) when the output
@@ -191,42 +192,53 @@ __global__ void __launch_bounds__(kDqThreads, 1)
             // sq * 2^-(BITS*e + sh) (exact: a power-of-two rescaling) turns it into the
             // level: sq * (u - MID), or sq * (u - MID + 1/2) for the mid-rise grid.
             const float sq = e4m3_to_float(cur.sbyte & 0xFFu);
-            float se[PER16], ke[PER16];
+            // per position e of a code in its half-word: the scale sq * 2^-(BITS*e + sh) and the
+            // offset -(2^23 + (MID * 2^sh - sh) * 2^(BITS*e)), as pairs of neighbouring positions
+            constexpr int NP = PER16 / 2;
+            float2 se[NP], nk[NP];
 #pragma unroll
-            for (int e = 0; e < PER16; e++) {
-                se[e] = __fmul_rn(sq, __uint_as_float((uint32_t)(127 - BITS * e - sh) << 23));
-                ke[e] = __uint_as_float(0x4B000000u) + (float)(((MID << sh) - sh) << (BITS * e));
+            for (int e2 = 0; e2 < NP; e2++) {
+                float s2[2], k2[2];
+#pragma unroll
+                for (int o = 0; o < 2; o++) {
+                    const int e = 2 * e2 + o;
+                    s2[o] = __fmul_rn(sq, __uint_as_float((uint32_t)(127 - BITS * e - sh) << 23));
+                    k2[o] = -(__uint_as_float(0x4B000000u) + (float)(((MID << sh) - sh) << (BITS * e)));
+                }
+                se[e2] = make_float2(s2[0], s2[1]);
+                nk[e2] = make_float2(k2[0], k2[1]);
             }
-            float y[16];
+            // y[p] holds channels 2p and 2p + 1 of the lane's 16; the arithmetic runs on
+            // f32x2 pairs, each lane of a pair rounding as the scalar operation would
+            float2 y[8];
 #pragma unroll
             for (int hw = 0; hw < 16 / PER16; hw++) {
                 const uint32_t word = (cur.code[hw >> 1] >> (16 * (hw & 1))) << sh;
 #pragma unroll
-                for (int e = 0; e < PER16; e++) {
-                    const uint32_t m = (word & (((1u << BITS) - 1u) << (BITS * e + sh))) | 0x4B000000u;
-                    y[hw * PER16 + e] = __fsub_rn(__uint_as_float(m), ke[e]);
+                for (int e = 0; e < PER16; e += 2) {
+                    const uint32_t m0 = (word & (((1u << BITS) - 1u) << (BITS * e + sh))) | 0x4B000000u;
+                    const uint32_t m1 = (word & (((1u << BITS) - 1u) << (BITS * (e + 1) + sh))) | 0x4B000000u;
+                    y[(hw * PER16 + e) / 2] =
+                        __fadd2_rn(make_float2(__uint_as_float(m0), __uint_as_float(m1)), nk[e / 2]);
                 }
             }
             if (T == 0) {
 #pragma unroll
-                for (int x = 0; x < 16; x++) y[x] = __fmul_rn(se[x % PER16], y[x]);
+                for (int x = 0; x < 8; x++) y[x] = __fmul2_rn(se[x % NP], y[x]);
             } else {
                 float4 a[4];
                 table16(T - 1, stage_j(cur, T - 1), a);
 #pragma unroll
                 for (int k = 0; k < 4; k++) {
-                    const float cv[4] = {a[k].x, a[k].y, a[k].z, a[k].w};
-#pragma unroll
-                    for (int q = 0; q < 4; q++)
-                        y[4 * k + q] = __fmaf_rn(se[(4 * k + q) % PER16], y[4 * k + q], cv[q]);
+                    y[2 * k] = __ffma2_rn(se[(2 * k) % NP], y[2 * k], make_float2(a[k].x, a[k].y));
+                    y[2 * k + 1] = __ffma2_rn(se[(2 * k + 1) % NP], y[2 * k + 1], make_float2(a[k].z, a[k].w));
                 }
                 for (int t = T - 2; t >= 0; t--) {
                     table16(t, stage_j(cur, t), a);
 #pragma unroll
                     for (int k = 0; k < 4; k++) {
-                        const float cv[4] = {a[k].x, a[k].y, a[k].z, a[k].w};
-#pragma unroll
-                        for (int q = 0; q < 4; q++) y[4 * k + q] = __fadd_rn(y[4 * k + q], cv[q]);
+                        y[2 * k] = __fadd2_rn(y[2 * k], make_float2(a[k].x, a[k].y));
+                        y[2 * k + 1] = __fadd2_rn(y[2 * k + 1], make_float2(a[k].z, a[k].w));
                     }
                 }
             }
@@ -236,24 +248,27 @@ __global__ void __launch_bounds__(kDqThreads, 1)
                     for (int k = 0; k < 2; k++) {
                         uint32_t w[8];
 #pragma unroll
-                        for (int x = 0; x < 8; x++) w[x] = __float_as_uint(y[8 * k + x]);
+                        for (int x = 0; x < 4; x++) {
+                            w[2 * x] = __float_as_uint(y[4 * k + x].x);
+                            w[2 * x + 1] = __float_as_uint(y[4 * k + x].y);
+                        }
                         st_v8(op + 32 * k, w);
                     }
                 } else {
                     float4 *dst = reinterpret_cast<float4 *>(op);
 #pragma unroll
                     for (int k = 0; k < 4; k++)
-                        dst[k] = make_float4(y[4 * k], y[4 * k + 1], y[4 * k + 2], y[4 * k + 3]);
+                        dst[k] = make_float4(y[2 * k].x, y[2 * k].y, y[2 * k + 1].x, y[2 * k + 1].y);
                 }
             } else {
                 uint32_t w[8];
 #pragma unroll
                 for (int k = 0; k < 8; k++) {
                     if constexpr (OUT == DT_BF16) {
-                        const __nv_bfloat162 v2 = __floats2bfloat162_rn(y[2 * k], y[2 * k + 1]);
+                        const __nv_bfloat162 v2 = __floats2bfloat162_rn(y[k].x, y[k].y);
                         w[k] = *reinterpret_cast<const uint32_t *>(&v2);
                     } else {
-                        const __half2 v2 = __floats2half2_rn(y[2 * k], y[2 * k + 1]);
+                        const __half2 v2 = __floats2half2_rn(y[k].x, y[k].y);
                         w[k] = *reinterpret_cast<const uint32_t *>(&v2);
                     }
                 }

@@ -217,32 +217,61 @@ QPlan make_plan(const qvg_quant_params *prm, const void *X, const float *warm,
     return p;
 }
 
-// Scratch area of qvg_quantize_static.  A __device__ variable exists once in every device
-// context that loads this module, so each device has its own copy.
+// Scratch area of qvg_quantize_static.  A __device__ variable exists once in every CUDA
+// context that loads this module, so each device (and each further context a caller
+// creates) has its own copy.
 static __device__ __align__(256) unsigned char g_static_scratch[QVG_STATIC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_static_mu;
-void *g_static_addr[kMaxDevices];
+typedef CUresult (*CtxGetCurrentFn)(CUcontext *);
 
-// Device address of g_static_scratch on the current device, looked up once per device.
+// cuCtxGetCurrent, resolved once through the runtime (no link-time dependence on libcuda).
+CtxGetCurrentFn ctx_get_current() {
+    static CtxGetCurrentFn fn = []() -> CtxGetCurrentFn {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &ptr, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return nullptr;
+        return reinterpret_cast<CtxGetCurrentFn>(ptr);
+    }();
+    return fn;
+}
+
+// The area's device address, looked up once per context: the address belongs to the context
+// whose copy of the module it points into, so it is keyed by the current context, not by the
+// device ordinal (a caller may make a context of its own current on a device).
+constexpr int kMaxContexts = 64;
+std::mutex g_static_mu;
+CUcontext g_static_ctx[kMaxContexts];
+void *g_static_addr[kMaxContexts];
+int g_static_n = 0;
+
 qvg_status static_scratch(void **addr) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) {
+    CtxGetCurrentFn get = ctx_get_current();
+    if (!get) return QVG_ERR_CUDA;
+    CUcontext ctx = nullptr;
+    if (get(&ctx) != CUDA_SUCCESS) return QVG_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_static_mu);
+    for (int k = 0; ctx && k < g_static_n; k++)
+        if (g_static_ctx[k] == ctx) {
+            *addr = g_static_addr[k];
+            return QVG_OK;
+        }
+    // not seen yet (or no context current: the runtime then binds the device's primary
+    // context on this lookup, and that is the one to key)
+    void *a = nullptr;
+    if (cudaGetSymbolAddress(&a, g_static_scratch) != cudaSuccess || !a) {
         (void)cudaGetLastError();
         return QVG_ERR_CUDA;
     }
-    if (dev < 0 || dev >= kMaxDevices) return QVG_ERR_UNSUPPORTED;
-    std::lock_guard<std::mutex> lock(g_static_mu);
-    if (!g_static_addr[dev]) {
-        void *a = nullptr;
-        if (cudaGetSymbolAddress(&a, g_static_scratch) != cudaSuccess || !a) {
-            (void)cudaGetLastError();
-            return QVG_ERR_CUDA;
-        }
-        g_static_addr[dev] = a;
+    if (!ctx && (get(&ctx) != CUDA_SUCCESS || !ctx)) return QVG_ERR_CUDA;
+    if (g_static_n < kMaxContexts) {  // beyond that, look the address up on every call
+        g_static_ctx[g_static_n] = ctx;
+        g_static_addr[g_static_n] = a;
+        g_static_n++;
     }
-    *addr = g_static_addr[dev];
+    *addr = a;
     return QVG_OK;
 }
 
@@ -346,6 +375,39 @@ qvg_status qvg_reassign(const qvg_quant_params *prm, const void *X, const qvg_bu
 }
 
 
+
+qvg_status qvg_selftest_assign_timeout(const qvg_quant_params *prm, const void *X,
+                                       const qvg_buffers *out, void *workspace,
+                                       size_t workspace_bytes, uint32_t *dev_status,
+                                       void *stream) {
+    qvg_status rc = check_quant(prm);
+    if (rc != QVG_OK) return rc;
+    if (prm->T < 1) return QVG_ERR_INVALID_ARG;
+    if (!X || !out || !out->pi || !out->centroids) return QVG_ERR_INVALID_ARG;
+    if (!aligned16(X) || !aligned16(out->centroids)) return QVG_ERR_INVALID_ARG;
+    const WsLayout w = ws_layout(prm->n_tensors, prm->N, prm->C, prm->T);
+    if (!workspace || workspace_bytes < w.total) return QVG_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return QVG_ERR_INVALID_ARG;
+    int num_sms = 0;
+    rc = device_info(&num_sms);
+    if (rc != QVG_OK) return rc;
+    QPlan p = make_plan(prm, X, nullptr, out, workspace, w, dev_status);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    AssignMaps *maps = nullptr;
+    if (assign_prepare(p, &maps) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return QVG_ERR_CUDA;
+    }
+    // the centroid operand's load withheld, a wait limit of one millisecond
+    cudaError_t e = launch_centroid_planes(p, p.T, st);
+    if (e == cudaSuccess) e = launch_assign(p, maps, p.T, num_sms, st, 1000000ull, 1);
+    assign_release(maps);
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        return QVG_ERR_CUDA;
+    }
+    return QVG_OK;
+}
 
 qvg_status qvg_dequantize(const qvg_dequant_params *prm, const qvg_buffers *in, void *X_hat,
                           uint32_t *dev_status, void *stream) {

@@ -118,6 +118,10 @@ SIGNATURES = {
     "qvg_reassign": (ctypes.c_int, [ctypes.POINTER(qvg_quant_params), ctypes.c_void_p,
                                     ctypes.POINTER(qvg_buffers), ctypes.c_void_p,
                                     ctypes.c_size_t, ctypes.c_void_p, ctypes.c_void_p]),
+    "qvg_selftest_assign_timeout": (ctypes.c_int, [ctypes.POINTER(qvg_quant_params),
+                                                   ctypes.c_void_p, ctypes.POINTER(qvg_buffers),
+                                                   ctypes.c_void_p, ctypes.c_size_t,
+                                                   ctypes.c_void_p, ctypes.c_void_p]),
     "qvg_dequantize": (ctypes.c_int, [ctypes.POINTER(qvg_dequant_params),
                                       ctypes.POINTER(qvg_buffers), ctypes.c_void_p,
                                       ctypes.c_void_p, ctypes.c_void_p]),
@@ -185,6 +189,13 @@ def qvg_reassign(params: qvg_quant_params, X: int, out: qvg_buffers, workspace: 
                  workspace_bytes: int, dev_status: int | None, stream: int | None) -> int:
     return int(load().qvg_reassign(_ref(params), X, _ref(out), workspace, workspace_bytes,
                                    dev_status, stream))
+
+
+def qvg_selftest_assign_timeout(params: qvg_quant_params, X: int, out: qvg_buffers,
+                                workspace: int, workspace_bytes: int, dev_status: int | None,
+                                stream: int | None) -> int:
+    return int(load().qvg_selftest_assign_timeout(_ref(params), X, _ref(out), workspace,
+                                                  workspace_bytes, dev_status, stream))
 
 
 def qvg_dequantize(params: qvg_dequant_params, inp: qvg_buffers, X_hat: int,
