@@ -74,12 +74,18 @@ struct QPlan {
     int nsb, nchunk;       // token blocks of the sort, 32-position chunks per tensor
     int *init_idx;         // [H][T][C] cold-start rows
     unsigned *stats;       // [16] counters (see kStat*)
-    int *rq_count;         // number of queued near-tie re-scoring requests
-    struct RefineReq *rq;  // [H*N] near-tie re-scoring requests
+    int *rq_cta;           // [2 * kMaxAssignCtas] per assignment CTA: first slot of its
+                           // region of rq, requests queued there
+    struct RefineReq *rq;  // [H * tiles * kAssignTileM] near-tie re-scoring requests
     uint32_t *status;      // caller's device status word (may be NULL)
 };
 
 enum { kStatRefineRows = 0, kStatRefineCands = 1 };
+// Most CTAs of one assignment launch (its grid is min(tiles, SMs), capped to this).
+constexpr int kMaxAssignCtas = 1024;
+// Tokens per assignment tile.  The near-tie queue has one slot per row of every tile (a
+// tensor's last tile may be ragged), and each assignment CTA owns the slots of its tiles.
+constexpr int kAssignTileM = 128;
 
 // A token whose GEMM scores leave more than one cluster within the error margin of the
 // best: cand holds one bit per cluster to re-score exactly.

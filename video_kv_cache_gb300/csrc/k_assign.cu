@@ -66,7 +66,7 @@ namespace {
 
 constexpr int kEpiGroups = 2;                      // epilogue groups of 8 warps
 constexpr int kThreads = 64 + kEpiGroups * 8 * 32;  // producer, MMA, 16 epilogue warps
-constexpr int kTileM = 128;
+constexpr int kTileM = kAssignTileM;
 constexpr uint32_t kKBlockBytes = kTileM * 64 * 2;  // 16 KB: 64 fp16 channels of 128 rows
 constexpr int kABlocks = 2;                           // A blocks per tile (128 channels)
 constexpr uint32_t kAuxABytes = kTileM * 128;         // the constant tf32 block: 128 rows of 128 B
@@ -269,6 +269,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *acc_full = b_full + 2, *acc_empty = acc_full + kEpiGroups, *fin = acc_empty + kEpiGroups;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(fin + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    int *q_count = reinterpret_cast<int *>(tmem_slot + 2);  // requests this CTA queued
     // per epilogue group: the column-half exchange (best score and candidate words per row)
     float *x_best = reinterpret_cast<float *>(
         (reinterpret_cast<uintptr_t>(tmem_slot + 4) + 15) & ~static_cast<uintptr_t>(15));  // [kEpiGroups][2][128]
@@ -301,6 +302,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_init(smem_u32(fin), 1);
         *abort_flag = 0;
+        *q_count = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
@@ -574,12 +576,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool need = valid && n_cand > 1;
                 const unsigned m = __ballot_sync(0xffffffffu, need);
                 if (m) {
+                    // this CTA's region of the queue: one slot per row of its tiles
                     int base = 0;
-                    if (lane == 0) base = atomicAdd(p.rq_count, __popc(m));
+                    if (lane == 0) base = atomicAdd(q_count, __popc(m));
                     base = __shfl_sync(0xffffffffu, base, 0);
                     if (need) {
                         n_ref_rows++;
-                        RefineReq *rq = p.rq + base + __popc(m & ((1u << lane) - 1u));
+                        RefineReq *rq = p.rq + tb * kTileM + base + __popc(m & ((1u << lane) - 1u));
                         rq->h = h;
                         rq->i = (int)i;
 #pragma unroll
@@ -601,7 +604,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     tc_fence_before();
     __syncthreads();
-    if (*abort_flag && threadIdx.x == 0) or_status(p.status, QVG_DEV_TIMEOUT);
+    if (threadIdx.x == 0) {
+        if (*abort_flag) or_status(p.status, QVG_DEV_TIMEOUT);
+        p.rq_cta[2 * blockIdx.x] = (int)(tb * kTileM);
+        p.rq_cta[2 * blockIdx.x + 1] = *q_count;
+    }
     if (warp == 1) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
@@ -620,17 +627,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 // centroids, by the same subtraction chain as the fp64 reference, and the candidates are
 // scored again in fp64.  Candidates are visited in increasing cluster order and only a
 // strictly smaller distance replaces the best, so ties go to the lowest index.
-// grid-stride over the queue, block 256.
+// Blocks of 256 threads; several blocks share each assignment CTA's region of the queue.
 // --------------------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) k_refine(QPlan p, int t) {
+__global__ void __launch_bounds__(256) k_refine(QPlan p, int t, int n_regions, int split) {
     pdl_begin();
     const int lane = threadIdx.x & 31;
-    const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const int nw = (gridDim.x * blockDim.x) >> 5;
-    const int count = *p.rq_count;
+    // blocks b, b + n_regions, ... share region b % n_regions of the queue (one region per
+    // assignment CTA); their warps stride over its requests
+    const int region = blockIdx.x % n_regions;
+    const int gw = (blockIdx.x / n_regions) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int nw = split * (blockDim.x >> 5);
+    const int first = p.rq_cta[2 * region], count = p.rq_cta[2 * region + 1];
     unsigned n_cands = 0;
     for (int r = gw; r < count; r += nw) {
-        const RefineReq rq = p.rq[r];
+        const RefineReq rq = p.rq[first + r];
         const int h = rq.h;
         const int64_t i = rq.i;
         const float *ct = p.cent + h * p.cent_tstride + p.cent_off;
@@ -877,7 +887,7 @@ cudaError_t launch_assign(const QPlan &p, const AssignMaps *maps, int t, int num
                           cudaStream_t st, uint64_t wait_ns, int withhold_b) {
     const int tiles = (int)((p.N + kTileM - 1) / kTileM);
     const int64_t total = (int64_t)tiles * p.H;
-    const int grid = (int)std::min<int64_t>(total, num_sms);
+    const int grid = (int)std::min<int64_t>(std::min<int64_t>(total, num_sms), kMaxAssignCtas);
     size_t max_smem = 0;
     cudaError_t e = max_smem_optin(&max_smem);
     if (e != cudaSuccess) return e;
@@ -895,8 +905,16 @@ cudaError_t launch_assign(const QPlan &p, const AssignMaps *maps, int t, int num
                          p, t, tiles, nslots, cols, stride, wait_ns, withhold_b);
 }
 
+// The assignment's grid for plan p (the number of queue regions it leaves).
+static int assign_grid(const QPlan &p, int num_sms) {
+    const int64_t total = (int64_t)((p.N + kTileM - 1) / kTileM) * p.H;
+    return (int)std::min<int64_t>(std::min<int64_t>(total, num_sms), kMaxAssignCtas);
+}
+
 cudaError_t launch_refine(const QPlan &p, int t, int num_sms, cudaStream_t st) {
-    return launch_kernel(k_refine, dim3(num_sms * 8), dim3(256), 0, st, p, t);
+    const int regions = assign_grid(p, num_sms);
+    const int split = std::max(1, (num_sms * 8 + regions - 1) / regions);
+    return launch_kernel(k_refine, dim3(regions * split), dim3(256), 0, st, p, t, regions, split);
 }
 
 }  // namespace qvg

@@ -367,8 +367,6 @@ __device__ __forceinline__ void write_offset_row(const QPlan &p, int h, int j, i
 
 __global__ void k_centroid_planes(QPlan p, int t) {
     pdl_begin();
-    // the near-tie queue starts empty for the stage's first assignment
-    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *p.rq_count = 0;
     const int j = blockIdx.x, h = blockIdx.y, k = threadIdx.x;
     if (j >= p.C) {  // a padded column (the whole block takes this branch)
         if (k < kOffsetRow) p.Bx[((int64_t)h * p.Cpad + j) * kOffsetRow + k] = k == 0 ? -0x1p100f : 0.f;
@@ -877,8 +875,6 @@ static cudaError_t launch_sums(const QPlan &p, const AssignMaps *maps, int t, in
 // centroid.  Then the centroid and its GEMM planes are written.
 __global__ void __launch_bounds__(256) k_cluster_finalize(QPlan p, int t, int planes) {
     pdl_begin();
-    // the near-tie queue of this round has been consumed: empty it for the next assignment
-    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *p.rq_count = 0;
     const int lane = threadIdx.x & 31;
     const int j = blockIdx.x * 8 + (threadIdx.x >> 5);
     const int h = blockIdx.y;

@@ -23,7 +23,7 @@ inline int cpad_of(int C) { return (C + 31) / 32 * 32; }
 
 struct WsLayout {
     size_t A, rnorm, dnorm, B, Bx, cnd, mu, counts, offs, blockoff, ids, cid, psum, wsum, init_idx,
-        stats, rq_count, rq, total;
+        stats, rq_cta, rq, total;
     int nsb, nchunk;
 };
 
@@ -55,8 +55,9 @@ WsLayout ws_layout(int64_t H, int64_t N, int C, int T) {
         w.psum = take((size_t)H * w.nchunk * 4 * kD * 4);
         w.wsum = take((size_t)H * C * 2 * kD * 4);
         w.init_idx = take((size_t)H * T * C * 4);
-        w.rq_count = take(4);
-        w.rq = take((size_t)H * N * sizeof(RefineReq));
+        w.rq_cta = take((size_t)2 * kMaxAssignCtas * 4);
+        w.rq = take((size_t)H * ((N + kAssignTileM - 1) / kAssignTileM) * kAssignTileM *
+                    sizeof(RefineReq));
     }
     w.total = off;
     return w;
@@ -210,7 +211,7 @@ QPlan make_plan(const qvg_quant_params *prm, const void *X, const float *warm,
         p.nsb = w.nsb;
         p.nchunk = w.nchunk;
         p.init_idx = reinterpret_cast<int *>(ws + w.init_idx);
-        p.rq_count = reinterpret_cast<int *>(ws + w.rq_count);
+        p.rq_cta = reinterpret_cast<int *>(ws + w.rq_cta);
         p.rq = reinterpret_cast<RefineReq *>(ws + w.rq);
     }
     p.status = dev_status;
