@@ -9,21 +9,21 @@ for the fp64 decision therefore adds 2^-22 ||x|| sqrt(D_2) to 2^-18 D_2.
 
 The model builds such rows on purpose (the second centroid displaced along the pattern of
 the input's rounding, the exact gap between 2^-18 and 2^-12 of the distance), computes the
-fp32 distances as the kernel does (a fused chain of 4 channels per lane, then a butterfly
-sum over 32 lanes) and checks that every wrongly ordered pair is sent to fp64 -- which the
-margin without the input term would not do."""
+fp32 distances as the kernel does (one half-warp per row: a fused chain of 8 channels per
+lane, then a butterfly sum over the 16 lanes) and checks that every wrongly ordered pair is
+sent to fp64 -- which the margin without the input term would not do."""
 import numpy as np
 
 f32 = np.float32
 
 
 def _d32(x32, c):
-    d = (x32 - c).astype(f32).reshape(32, 4).astype(np.float64)
+    d = (x32 - c).astype(f32).reshape(16, 8).astype(np.float64)
     lane = (d[:, 0] * d[:, 0]).astype(f32)
-    for k in range(1, 4):
+    for k in range(1, 8):
         lane = (d[:, k] * d[:, k] + lane.astype(np.float64)).astype(f32)   # fma: exact product
-    for o in (16, 8, 4, 2, 1):
-        lane = (lane + lane[np.arange(32) ^ o]).astype(f32)
+    for o in (8, 4, 2, 1):
+        lane = (lane + lane[np.arange(16) ^ o]).astype(f32)
     assert np.all(lane == lane[0])   # the butterfly leaves every lane with the same sum
     return lane[0]
 

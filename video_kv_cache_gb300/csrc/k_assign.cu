@@ -619,60 +619,66 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 
 // --------------------------------------------------------------------------------------
-// Re-scoring of near ties.  One warp per queued token; lane l holds channels 4l..4l+3.
-// First every candidate's squared distance is summed in fp32 on the fp32 stage input (a
-// 4-term partial sum per lane, reduced over the warp in a fixed order).  If the best two
-// are further apart than fp32 can blur, that decides.  Otherwise (a tie at fp32
-// resolution, rare) the stage input is rebuilt in fp64 from X and the earlier stages'
-// centroids, by the same subtraction chain as the fp64 reference, and the candidates are
-// scored again in fp64.  Candidates are visited in increasing cluster order and only a
-// strictly smaller distance replaces the best, so ties go to the lowest index.
-// Blocks of 256 threads; several blocks share each assignment CTA's region of the queue.
+// Re-scoring of near ties.  One half-warp per queued token, two tokens a warp; lane l of a
+// half holds channels 8l..8l+7.  First every candidate's squared distance is summed in fp32
+// on the fp32 stage input (an 8-term fused chain per lane, reduced over the half-warp in a
+// fixed order).  If the best two are further apart than fp32 can blur, that decides.
+// Otherwise (a tie at fp32 resolution, rare) the stage input is rebuilt in fp64 from X and
+// the earlier stages' centroids, by the same subtraction chain as the fp64 reference, and
+// the candidates are scored again in fp64.  Candidates are visited in increasing cluster
+// order and only a strictly smaller distance replaces the best, so ties go to the lowest
+// index.  Blocks of 256 threads; several blocks share each assignment CTA's region of the
+// queue.
 // --------------------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) k_refine(QPlan p, int t, int n_regions, int split) {
     pdl_begin();
-    const int lane = threadIdx.x & 31;
+    const int lane = threadIdx.x & 31, hl = lane & 15;
+    const unsigned hmask = lane < 16 ? 0x0000FFFFu : 0xFFFF0000u;  // this half-warp
     // blocks b, b + n_regions, ... share region b % n_regions of the queue (one region per
-    // assignment CTA); their warps stride over its requests
+    // assignment CTA); their half-warps stride over its requests
     const int region = blockIdx.x % n_regions;
-    const int gw = (blockIdx.x / n_regions) * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    const int nw = split * (blockDim.x >> 5);
+    const int gh = ((blockIdx.x / n_regions) * (blockDim.x >> 5) + (threadIdx.x >> 5)) * 2 + (lane >> 4);
+    const int nh = split * (blockDim.x >> 5) * 2;
     const int first = p.rq_cta[2 * region], count = p.rq_cta[2 * region + 1];
+    auto hsum = [&](float v) {  // the half-warp's sum, the same in every lane of it
+#pragma unroll
+        for (int o = 8; o >= 1; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(hmask, v, o));
+        return v;
+    };
     unsigned n_cands = 0;
-    for (int r = gw; r < count; r += nw) {
+    for (int r = gh; r < count; r += nh) {
         const RefineReq rq = p.rq[first + r];
         const int h = rq.h;
         const int64_t i = rq.i;
         const float *ct = p.cent + h * p.cent_tstride + p.cent_off;
         const float *c0 = ct + (int64_t)(t - 1) * p.C * kD;
-        // X's channels 4*lane..4*lane+3
-        float xs[4];
-        {
-            float v8[8];
-            load_x8(p.X, p.in_dtype, h * p.x_stride + i * kD + (lane >> 1) * 8, v8);
-            const bool up = lane & 1;  // which half of the 8 loaded channels is this lane's
-#pragma unroll
-            for (int k = 0; k < 4; k++) xs[k] = up ? v8[4 + k] : v8[k];
-        }
+        // X's channels 8*hl..8*hl+7
+        float xs[8];
+        load_x8(p.X, p.in_dtype, h * p.x_stride + i * kD + hl * 8, xs);
         // fp32 pass on the fp32 stage input: X itself at stage 1, later the residual formed
         // by the same TwoSum chain (one final rounding) as the GEMM operand's preparation
-        float4 x = make_float4(xs[0], xs[1], xs[2], xs[3]);
+        float2 x[4];
+#pragma unroll
+        for (int q = 0; q < 4; q++) x[q] = make_float2(xs[2 * q], xs[2 * q + 1]);
         if (t > 1) {
-            float s[4] = {xs[0], xs[1], xs[2], xs[3]}, e[4] = {0.f, 0.f, 0.f, 0.f};
+            float2 e[4];
+#pragma unroll
+            for (int q = 0; q < 4; q++) e[q] = make_float2(0.f, 0.f);
             for (int s2 = 1; s2 < t; s2++) {
                 const int js = min((int)p.pi[(int64_t)(h * p.T + s2 - 1) * p.cap + p.tok_off + i], p.C - 1);
-                const float4 c = __ldg(reinterpret_cast<const float4 *>(
-                    ct + ((int64_t)(s2 - 1) * p.C + js) * kD) + lane);
-                const float cc[4] = {c.x, c.y, c.z, c.w};
+                const float4 *cr = reinterpret_cast<const float4 *>(ct + ((int64_t)(s2 - 1) * p.C + js) * kD) + 2 * hl;
+                const float4 ca = __ldg(cr), cb = __ldg(cr + 1);
+                const float2 c[4] = {make_float2(ca.x, ca.y), make_float2(ca.z, ca.w), make_float2(cb.x, cb.y),
+                                     make_float2(cb.z, cb.w)};
 #pragma unroll
-                for (int k = 0; k < 4; k++) {
-                    float err;
-                    two_sum(s[k], -cc[k], s[k], err);
-                    e[k] = __fadd_rn(e[k], err);
+                for (int q = 0; q < 4; q++) {
+                    float2 err;
+                    x[q] = two_diff2(x[q], c[q], err);
+                    e[q] = __fadd2_rn(e[q], err);
                 }
             }
-            x = make_float4(__fadd_rn(s[0], e[0]), __fadd_rn(s[1], e[1]), __fadd_rn(s[2], e[2]),
-                            __fadd_rn(s[3], e[3]));
+#pragma unroll
+            for (int q = 0; q < 4; q++) x[q] = __fadd2_rn(x[q], e[q]);
         }
         float bestD = INFINITY, secondD = INFINITY;
         int bestj = 0;
@@ -683,12 +689,16 @@ __global__ void __launch_bounds__(256) k_refine(QPlan p, int t, int n_regions, i
                 const int j = cb * 32 + __ffs(m) - 1;
                 m &= m - 1u;
                 n_cands++;
-                const float4 c = __ldg(reinterpret_cast<const float4 *>(c0 + (int64_t)j * kD) + lane);
-                const float d0 = __fsub_rn(x.x, c.x), d1 = __fsub_rn(x.y, c.y);
-                const float d2 = __fsub_rn(x.z, c.z), d3 = __fsub_rn(x.w, c.w);
-                float D = __fmaf_rn(d3, d3, __fmaf_rn(d2, d2, __fmaf_rn(d1, d1, __fmul_rn(d0, d0))));
+                const float4 *cr = reinterpret_cast<const float4 *>(c0 + (int64_t)j * kD) + 2 * hl;
+                const float4 ca = __ldg(cr), cc = __ldg(cr + 1);
+                const float cv[8] = {ca.x, ca.y, ca.z, ca.w, cc.x, cc.y, cc.z, cc.w};
+                float D = 0.f;
 #pragma unroll
-                for (int o = 16; o >= 1; o >>= 1) D = __fadd_rn(D, __shfl_xor_sync(0xffffffffu, D, o));
+                for (int q = 0; q < 8; q++) {
+                    const float d = __fsub_rn(q & 1 ? x[q >> 1].y : x[q >> 1].x, cv[q]);
+                    D = q == 0 ? __fmul_rn(d, d) : __fmaf_rn(d, d, D);
+                }
+                D = hsum(D);
                 if (D < bestD) {
                     secondD = bestD;
                     bestD = D;
@@ -698,38 +708,38 @@ __global__ void __launch_bounds__(256) k_refine(QPlan p, int t, int n_regions, i
                 }
             }
         }
-        // Each fp32 distance is within about ten fp32 roundings (2^-20.6, relative: a sum of
-        // non-negative terms) of the exact distance of the fp32 stage input, so a gap wider
-        // than 2^-18 of the larger distance orders them as those exact distances are.  From
-        // the second stage on, the fp32 stage input is itself off the fp64 one by at most
-        // 2^-24 |x_k| per channel, which moves the difference of two distances by at most
-        // 2^-23 ||x|| (||x - c_1|| + ||x - c_2||) <= 2^-22 ||x|| sqrt(D_2); that is added to
-        // the margin (it dominates for a row far larger than its distances).  Closer calls
-        // are settled in fp64 below.
-        // (bestD and secondD are the same in every lane, so the branches are warp-uniform.)
+        // Each fp32 distance is within about twelve fp32 roundings (2^-20.4, relative: a sum
+        // of non-negative terms) of the exact distance of the fp32 stage input, so a gap
+        // wider than 2^-18 of the larger distance orders them as those exact distances are.
+        // From the second stage on, the fp32 stage input is itself off the fp64 one by at
+        // most 2^-24 |x_k| per channel, which moves the difference of two distances by at
+        // most 2^-23 ||x|| (||x - c_1|| + ||x - c_2||) <= 2^-22 ||x|| sqrt(D_2); that is added
+        // to the margin (it dominates for a row far larger than its distances to the
+        // candidates).  Closer calls are settled in fp64 below.
+        // (bestD and secondD are the same in every lane of the half, so the branches are
+        // uniform over it.)
         bool close = secondD - bestD <= 0x1p-18f * secondD;
         if (!close && t > 1) {
-            float xx = __fmaf_rn(x.w, x.w, __fmaf_rn(x.z, x.z, __fmaf_rn(x.y, x.y, __fmul_rn(x.x, x.x))));
+            float xx = 0.f;
 #pragma unroll
-            for (int o = 16; o >= 1; o >>= 1) xx = __fadd_rn(xx, __shfl_xor_sync(0xffffffffu, xx, o));
-            const float xn = sqrtf(xx);
+            for (int q = 0; q < 4; q++) xx = __fmaf_rn(x[q].y, x[q].y, __fmaf_rn(x[q].x, x[q].x, xx));
+            const float xn = sqrtf(hsum(xx));
             if (xn > 0.f)
                 close = secondD - bestD <= 0x1p-18f * secondD + 0x1.1p-22f * xn * sqrtf(secondD);
         }
         if (close) {
             // the stage input rebuilt in fp64: x - C^(1)[pi^(1)] - ... - C^(t-1)[pi^(t-1)],
             // subtracted in that order
-            double xd[4];
+            double xd[8];
 #pragma unroll
-            for (int k = 0; k < 4; k++) xd[k] = (double)xs[k];
+            for (int k = 0; k < 8; k++) xd[k] = (double)xs[k];
             for (int s2 = 1; s2 < t; s2++) {
                 const int js = min((int)p.pi[(int64_t)(h * p.T + s2 - 1) * p.cap + p.tok_off + i], p.C - 1);
-                const float4 c = __ldg(reinterpret_cast<const float4 *>(
-                    ct + ((int64_t)(s2 - 1) * p.C + js) * kD) + lane);
-                xd[0] -= (double)c.x;
-                xd[1] -= (double)c.y;
-                xd[2] -= (double)c.z;
-                xd[3] -= (double)c.w;
+                const float4 *cr = reinterpret_cast<const float4 *>(ct + ((int64_t)(s2 - 1) * p.C + js) * kD) + 2 * hl;
+                const float4 ca = __ldg(cr), cb = __ldg(cr + 1);
+                const float cv[8] = {ca.x, ca.y, ca.z, ca.w, cb.x, cb.y, cb.z, cb.w};
+#pragma unroll
+                for (int k = 0; k < 8; k++) xd[k] -= (double)cv[k];
             }
             double bestDd = INFINITY;
 #pragma unroll
@@ -738,12 +748,17 @@ __global__ void __launch_bounds__(256) k_refine(QPlan p, int t, int n_regions, i
                 while (m) {
                     const int j = cb * 32 + __ffs(m) - 1;
                     m &= m - 1u;
-                    const float4 c = __ldg(reinterpret_cast<const float4 *>(c0 + (int64_t)j * kD) + lane);
-                    const double e0 = xd[0] - (double)c.x, e1 = xd[1] - (double)c.y;
-                    const double e2 = xd[2] - (double)c.z, e3 = xd[3] - (double)c.w;
-                    double D = __fma_rn(e3, e3, __fma_rn(e2, e2, __fma_rn(e1, e1, e0 * e0)));
+                    const float4 *cr = reinterpret_cast<const float4 *>(c0 + (int64_t)j * kD) + 2 * hl;
+                    const float4 ca = __ldg(cr), cc = __ldg(cr + 1);
+                    const float cv[8] = {ca.x, ca.y, ca.z, ca.w, cc.x, cc.y, cc.z, cc.w};
+                    double D = 0.0;
 #pragma unroll
-                    for (int o = 16; o >= 1; o >>= 1) D += __shfl_xor_sync(0xffffffffu, D, o);
+                    for (int k = 0; k < 8; k++) {
+                        const double e = xd[k] - (double)cv[k];
+                        D = __fma_rn(e, e, D);
+                    }
+#pragma unroll
+                    for (int o = 8; o >= 1; o >>= 1) D += __shfl_xor_sync(hmask, D, o);
                     if (D < bestDd) {
                         bestDd = D;
                         bestj = j;
@@ -751,11 +766,10 @@ __global__ void __launch_bounds__(256) k_refine(QPlan p, int t, int n_regions, i
                 }
             }
         }
-        if (lane == 0) p.pi[(int64_t)(h * p.T + t - 1) * p.cap + p.tok_off + i] = (uint8_t)bestj;
+        if (hl == 0) p.pi[(int64_t)(h * p.T + t - 1) * p.cap + p.tok_off + i] = (uint8_t)bestj;
     }
-    if (p.stats && lane == 0 && n_cands) atomicAdd(p.stats + kStatRefineCands, n_cands);
+    if (p.stats && hl == 0 && n_cands) atomicAdd(p.stats + kStatRefineCands, n_cands);
 }
-
 
 // --------------------------------------------------------------------------------------
 // Host side

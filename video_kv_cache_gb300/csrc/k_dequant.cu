@@ -8,7 +8,7 @@
 //
 // Design (HBM-bound for one or two stages; bound by shared-memory reads of the tables
 // beyond that, since every output element reads T fp32 table values):
-//   * One CTA of 1024 threads per SM takes an equal contiguous share of the flattened
+//   * One CTA of 640 threads per SM takes an equal contiguous share of the flattened
 //     (tensor, token) space and walks it in blocks of up to kDqBlock tokens inside one
 //     centroid table.  The T tables are staged in shared memory one channel slice of W
 //     channels at a time (T x C x W fp32: W is the widest of 128, 64 and 32 that fits
@@ -30,6 +30,9 @@
 //     in an order rotated by the token's slot in its quarter-warp, so that the eight lanes
 //     of a quarter-warp (the unit of a 16-byte shared load) always read eight distinct
 //     bank groups, whichever rows their tokens' clusters select.
+//   * The lane puts its four groups back in channel order with two conditional swaps and
+//     writes its 16 outputs with one 32-byte store (two for fp32) when the output is
+//     32-byte aligned, so every store instruction fills whole sectors.
 //   * The codes, scale and indices of the next two tokens are loaded before the current
 //     token is computed, to keep reads in flight.
 #include <cuda_fp8.h>
@@ -41,10 +44,17 @@
 namespace qvg {
 
 namespace {
-constexpr int kDqThreads = 1024;
+constexpr int kDqThreads = 640;
 constexpr size_t kDqTableBytes = 200 * 1024;  // largest table slice staged by one CTA
 constexpr int kLaneCh = 16;                   // channels a lane rebuilds per token
 constexpr int64_t kDqBlock = 8192;            // tokens whose slices are done together
+
+// 32-byte store (sm_100 and later), 32-byte aligned address.
+__device__ __forceinline__ void st_v8(void *ptr, const uint32_t (&w)[8]) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(ptr), "r"(w[0]),
+                 "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+                 : "memory");
+}
 
 // Physical position of 16-byte chunk c in a staged table row.
 __device__ __forceinline__ int phys_chunk(int c) { return c ^ ((c >> 3) & 3); }
@@ -57,7 +67,7 @@ __device__ __forceinline__ float e4m3_to_float(uint32_t b) {
 
 template <int BITS, int OUT, int TT, int SH>  // SH: 1 for the mid-rise grid, else 0
 __global__ void __launch_bounds__(kDqThreads, 1)
-    k_dequant(DPlan p, int W, int64_t n_chunks, int smem_tables) {
+    k_dequant(DPlan p, int W, int64_t n_chunks, int smem_tables, int wide_stores) {
     pdl_begin();
     extern __shared__ __align__(16) float smem_f[];
     constexpr int MID = 1 << (BITS - 1);
@@ -196,6 +206,9 @@ __global__ void __launch_bounds__(kDqThreads, 1)
 #pragma unroll
                     for (int t = 0; t < TT; t++) js[t] = stage_j(cur, t);
                 }
+                // res[k] holds the 4 outputs of group k ^ xr, packed as the output type
+                constexpr int WPG = OUT == DT_F32 ? 4 : 2;  // 32-bit words per group
+                uint32_t res[4][WPG];
 #pragma unroll
                 for (int k = 0; k < 4; k++) {
                     const int g = k ^ xr;  // channels 4g .. 4g + 3 of the lane's 16
@@ -217,25 +230,69 @@ __global__ void __launch_bounds__(kDqThreads, 1)
                         float4 a = table4(T - 1, TT > 0 ? js[TT > 0 ? T - 1 : 0] : stage_j(cur, T - 1), k);
                         y0 = __ffma2_rn(se[0], y0, make_float2(a.x, a.y));
                         y1 = __ffma2_rn(se[1], y1, make_float2(a.z, a.w));
+#pragma unroll
                         for (int t = T - 2; t >= 0; t--) {
                             a = table4(t, TT > 0 ? js[TT > 0 ? t : 0] : stage_j(cur, t), k);
                             y0 = __fadd2_rn(y0, make_float2(a.x, a.y));
                             y1 = __fadd2_rn(y1, make_float2(a.z, a.w));
                         }
                     }
-                    char *dst = op + 4 * g * eb;
                     if constexpr (OUT == DT_F32) {
-                        *reinterpret_cast<float4 *>(dst) = make_float4(y0.x, y0.y, y1.x, y1.y);
+                        res[k][0] = __float_as_uint(y0.x);
+                        res[k][1] = __float_as_uint(y0.y);
+                        res[k][2] = __float_as_uint(y1.x);
+                        res[k][3] = __float_as_uint(y1.y);
                     } else if constexpr (OUT == DT_BF16) {
                         const __nv_bfloat162 v0 = __floats2bfloat162_rn(y0.x, y0.y);
                         const __nv_bfloat162 v1 = __floats2bfloat162_rn(y1.x, y1.y);
-                        *reinterpret_cast<uint2 *>(dst) = make_uint2(
-                            *reinterpret_cast<const uint32_t *>(&v0), *reinterpret_cast<const uint32_t *>(&v1));
+                        res[k][0] = *reinterpret_cast<const uint32_t *>(&v0);
+                        res[k][1] = *reinterpret_cast<const uint32_t *>(&v1);
                     } else {
                         const __half2 v0 = __floats2half2_rn(y0.x, y0.y);
                         const __half2 v1 = __floats2half2_rn(y1.x, y1.y);
-                        *reinterpret_cast<uint2 *>(dst) = make_uint2(
-                            *reinterpret_cast<const uint32_t *>(&v0), *reinterpret_cast<const uint32_t *>(&v1));
+                        res[k][0] = *reinterpret_cast<const uint32_t *>(&v0);
+                        res[k][1] = *reinterpret_cast<const uint32_t *>(&v1);
+                    }
+                }
+                // back to channel order: res[k] holds group k ^ xr, so swapping the pairs
+                // (k, k ^ 1) when bit 0 of xr is set and then (k, k ^ 2) when bit 1 is set
+                // leaves group k in res[k]
+#pragma unroll
+                for (int b = 1; b <= 2; b <<= 1) {
+                    const bool sw = (xr & b) != 0;
+#pragma unroll
+                    for (int k = 0; k < 4; k++) {
+                        if (k & b) continue;
+#pragma unroll
+                        for (int x = 0; x < WPG; x++) {
+                            const uint32_t lo = res[k][x], hi = res[k | b][x];
+                            res[k][x] = sw ? hi : lo;
+                            res[k | b][x] = sw ? lo : hi;
+                        }
+                    }
+                }
+                // 32-byte stores where the output allows them, else 16-byte ones
+                if constexpr (OUT == DT_F32) {
+#pragma unroll
+                    for (int half = 0; half < 2; half++) {
+                        const uint32_t w[8] = {res[2 * half][0], res[2 * half][1], res[2 * half][2],
+                                               res[2 * half][3], res[2 * half + 1][0], res[2 * half + 1][1],
+                                               res[2 * half + 1][2], res[2 * half + 1][3]};
+                        if (wide_stores) {
+                            st_v8(op + 32 * half, w);
+                        } else {
+                            reinterpret_cast<uint4 *>(op + 32 * half)[0] = make_uint4(w[0], w[1], w[2], w[3]);
+                            reinterpret_cast<uint4 *>(op + 32 * half)[1] = make_uint4(w[4], w[5], w[6], w[7]);
+                        }
+                    }
+                } else {
+                    const uint32_t w[8] = {res[0][0], res[0][1], res[1][0], res[1][1],
+                                           res[2][0], res[2][1], res[3][0], res[3][1]};
+                    if (wide_stores) {
+                        st_v8(op, w);
+                    } else {
+                        reinterpret_cast<uint4 *>(op)[0] = make_uint4(w[0], w[1], w[2], w[3]);
+                        reinterpret_cast<uint4 *>(op)[1] = make_uint4(w[4], w[5], w[6], w[7]);
                     }
                 }
                 op += ostep;
@@ -255,11 +312,14 @@ cudaError_t launch_dq(const DPlan &p, int num_sms, int W, size_t table_bytes, bo
                       cudaStream_t st) {
     auto kern = p.qscheme == QVG_QSCHEME_MIDRISE ? k_dequant<BITS, OUT, TT, 1> : k_dequant<BITS, OUT, TT, 0>;
     const size_t smem = smem_tables ? table_bytes : 16;
+    // 32-byte stores need a 32-byte aligned output and tensor stride
+    const size_t eb = p.out_dtype == DT_F32 ? 4 : 2;
+    const int wide = (reinterpret_cast<uintptr_t>(p.out) % 32 == 0 && (p.out_stride * eb) % 32 == 0) ? 1 : 0;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const int64_t n_chunks = (p.N + p.chunk_len - 1) / p.chunk_len;
     return launch_kernel(kern, dim3(num_sms), dim3(kDqThreads), smem, st, p, W, n_chunks,
-                         smem_tables ? 1 : 0);
+                         smem_tables ? 1 : 0, wide);
 }
 
 template <int BITS, int OUT>

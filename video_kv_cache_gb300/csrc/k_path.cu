@@ -1027,13 +1027,24 @@ __global__ void __launch_bounds__(256) k_encode(QPlan p) {
                                      : (QMAX == 1 ? a : __fdiv_rn(a, (float)QMAX));
             const __nv_fp8_storage_t sb = __nv_cvt_float_to_fp8(sc, __NV_SATFINITE, __NV_E4M3);
             const float sq = __half2float(__half(__nv_cvt_fp8_to_halfraw(sb, __NV_E4M3)));
-            // q = clamp(rne(r / s_q)) with the IEEE quotient.  r times an approximate
-            // reciprocal (a few ulps) gives the same rounding except close to a half-integer;
-            // there the quotient is recomputed with a correctly rounded division.  Adding
-            // 1.5 * 2^23 to the clamped quotient rounds it to an integer (half to even) and
-            // leaves that integer in the low mantissa bits.
             uint32_t word = 0;
-            if (sq != 0.f && midrise) {
+            if (BITS == 2 && sq != 0.f) {
+                // INT2: the code is decided by comparing r with exact multiples of s_q (s_q/2
+                // and s_q are exact in fp32), which is the code of the exact quotient r / s_q:
+                //   symmetric: q = clamp(rne(r / s_q), -1, 1) is 1 when r > s_q / 2, -1 when
+                //     r < -s_q / 2, else 0 (an exact half rounds to the even 0);
+                //   mid-rise: u = floor(r / s_q) + 2 clamped to [0, 3] steps at -s_q, 0, s_q.
+                const float hq = midrise ? sq : 0.5f * sq;
+#pragma unroll
+                for (int q = 0; q < 8; q++) {
+                    uint32_t u;
+                    if (midrise)
+                        u = r[q] >= 0.f ? (r[q] >= hq ? 3u : 2u) : (r[q] >= -hq ? 1u : 0u);
+                    else
+                        u = r[q] > hq ? 3u : (r[q] < -hq ? 1u : 2u);
+                    word |= u << (q * BITS);
+                }
+            } else if (sq != 0.f && midrise) {
                 // u = floor(r / s_q) + 2^(b-1), clamped.  r times an approximate reciprocal
                 // (a few ulps) has the same floor except close to an integer; there the
                 // quotient is recomputed with a correctly rounded division.
@@ -1058,6 +1069,11 @@ __global__ void __launch_bounds__(256) k_encode(QPlan p) {
                     word |= (uint32_t)u << (q * BITS);
                 }
             } else if (sq != 0.f) {
+                // q = clamp(rne(r / s_q)) with the IEEE quotient.  r times an approximate
+                // reciprocal (a few ulps) gives the same rounding except close to a
+                // half-integer; there the quotient is recomputed with a correctly rounded
+                // division.  Adding 1.5 * 2^23 to the clamped quotient rounds it to an
+                // integer (half to even) and leaves that integer in the low mantissa bits.
                 constexpr float kRound = 12582912.f;  // 1.5 * 2^23
                 float inv;
                 asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(inv) : "f"(sq));
