@@ -186,9 +186,9 @@ qvg_status qvg_quantize(const qvg_quant_params *params, const void *X,
  *
  * Limit: qvg_quantize_workspace_bytes(params) must not exceed QVG_STATIC_SCRATCH_BYTES;
  * otherwise the call returns QVG_ERR_SCRATCH_LIMIT before touching the device.  The
- * scratch is about 380 bytes per token row plus about 370 KB per tensor, whatever T: one
- * tensor of up to about 175 000 tokens fits, 24 tensors of up to about 6 400 each (154 000
- * rows), 100 tensors of up to about 780 each.
+ * scratch is about 450 bytes per token row plus about 630 KB per tensor, whatever T: one
+ * tensor of up to about 148 000 tokens fits, 24 tensors of up to about 4 800 each (116 000
+ * rows), 100 tensors of up to about 250 each.
  *
  * First call in a context: the area's device address belongs to the CUDA context whose
  * copy of the library's device code holds it, so the first call made while a given context

@@ -25,7 +25,7 @@ def _params(H, N, C, T, bits, group, iters, dtype, seed):
 
 
 def test_rejects_problem_larger_than_static_area(lib):
-    # about 0.38 KB of scratch per token row: 200 000 rows do not fit in 64 MiB.
+    # about 0.45 KB of scratch per token row: 200 000 rows do not fit in 64 MiB.
     prm = _params(1, 200000, 256, 2, 2, 32, 2, torch.bfloat16, 1)
     assert qvg.qvg_quantize_workspace_bytes(prm) > qvg.QVG_STATIC_SCRATCH_BYTES, "needs a larger N"
     bufs = qvg.qvg_buffers(16, 16, 16, 16)  # never dereferenced: the size check comes first

@@ -63,15 +63,27 @@ struct QPlan {
                            // parts (h, m, l, 0, ...); -2^100 in the padded rows
     float2 *cnd;           // [H][Cpad] (||c - mu||^2, ||fp16(c - mu) - (c - mu)||) per centroid
     float *mu;             // [H][128] centring vector of the current stage
-    int *counts;           // [H][C] cluster sizes of the current assignment
-    int *offs;             // [H][C] first position of each cluster in `ids`
+    // The mean update sorts items by cluster: in a stage's first round every token, in
+    // later rounds two events per token whose cluster changed (it leaves its old cluster,
+    // enters the new one), so the item capacity per tensor is icap = 2N.
+    int *counts;           // [H][C] items of each cluster this round
+    int *offs;             // [H][C] first position of each cluster's items in `ids`
     int *blockoff;         // [H][nsb][C] per token block: its first position per cluster
-    int *ids;              // [H][N] token indices grouped by cluster, increasing in a cluster
-    uint8_t *cid;          // [H][N] cluster of each sorted position
+    int *ids;              // [H][icap] token index of each sorted item, bit 31 set for an item
+                           // that leaves its cluster; increasing within a cluster's enters
+                           // (and leaves) of one token block
+    uint8_t *cid;          // [H][icap] cluster of each sorted item
+    int *items;            // [H] items sorted this round
     float *psum;           // [H][nchunk][2][2][128] (sum, error) of the runs that cross a
                            // chunk boundary: [0] the run at the chunk start, [1] the last run
     float *wsum;           // [H][C][2][128] (sum, error) of clusters inside one chunk
-    int nsb, nchunk;       // token blocks of the sort, 32-position chunks per tensor
+    float *tot;            // [H][C][2][128] (sum, error) of each cluster's members, kept
+                           // from round to round of a stage (renormalised: |error| <= ulp/2)
+    int *ccount;           // [H][C] members of each cluster, kept from round to round
+    int *dleave;           // [H][C] leave events of each cluster this round
+    uint8_t *pi_prev;      // [H][N] the previous round's assignment of the stage
+    int64_t icap;          // item capacity per tensor (2N)
+    int nsb, nchunk;       // token blocks of the sort, 32-position chunks per tensor (of icap)
     int *init_idx;         // [H][T][C] cold-start rows
     unsigned *stats;       // [16] counters (see kStat*)
     int *rq_cta;           // [2 * kMaxAssignCtas] per assignment CTA: first slot of its
@@ -294,8 +306,11 @@ cudaError_t launch_centre(const QPlan &p, int t, cudaStream_t st);
 cudaError_t launch_prep(const QPlan &p, int t, cudaStream_t st);
 cudaError_t launch_centroid_planes(const QPlan &p, int t, cudaStream_t st);
 struct AssignMaps;
+// Stage t's new centroids from its assignment; planes: also their assignment operands;
+// delta: fold the tokens whose cluster changed since the previous round into the cluster
+// totals that round kept (otherwise sum every member afresh).
 cudaError_t launch_cluster_means(const QPlan &p, const AssignMaps *maps, int t, bool planes,
-                                 int num_sms, cudaStream_t st);
+                                 bool delta, int num_sms, cudaStream_t st);
 constexpr int kSortBlock = 256;  // tokens per block of the counting sort
 constexpr int kChunk = 32;       // sorted positions summed by one warp
 cudaError_t launch_encode(const QPlan &p, cudaStream_t st);

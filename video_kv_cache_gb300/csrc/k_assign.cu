@@ -192,6 +192,20 @@ __device__ __forceinline__ void tc_ld64(uint32_t taddr, float v[64]) {
     for (int q = 0; q < 64; q++) v[q] = __uint_as_float(r[q]);
 }
 
+// 4-byte global-to-shared copy that completes asynchronously (waited on with
+// cp.async.wait_all by the issuing thread).
+__device__ __forceinline__ void cp_async4(uint32_t dst, const float *src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ float ld_shared_f32(uint32_t a) {
+    float v;
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(a) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_shared_f32(uint32_t a, float v) {
+    asm volatile("st.shared.f32 [%0], %1;" ::"r"(a), "f"(v) : "memory");
+}
+
 // Largest of 32 scores, in two independent chains.
 __device__ __forceinline__ float chunk_max(const float *v) {
     float ma = fmaxf(v[0], v[1]), mb = fmaxf(v[2], v[3]);
@@ -274,6 +288,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float *x_best = reinterpret_cast<float *>(
         (reinterpret_cast<uintptr_t>(tmem_slot + 4) + 15) & ~static_cast<uintptr_t>(15));  // [kEpiGroups][2][128]
     uint32_t *x_cand = reinterpret_cast<uint32_t *>(x_best + kEpiGroups * 2 * kTileM);  // [kEpiGroups][128][4]
+    float *x_norm = reinterpret_cast<float *>(x_cand + kEpiGroups * 4 * kTileM);  // [16 warps][2][64]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t total = (int64_t)p.H * tiles_per_tensor;
@@ -429,13 +444,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         int cur_h = -1;
         float cmax = 0.f, cmax2 = 0.f, dcmax = 0.f;
         unsigned n_ref_rows = 0;
+        // The row norms come from HBM while the tensor cores stream A at full rate, so each
+        // lane copies its row's pair into shared memory (cp.async) one tile ahead, off the
+        // path from the accumulator to the bits.  Two buffers a warp: [rn 32 | dn 32].
+        const uint32_t nb = smem_u32(x_norm) + (uint32_t)(e * 128 + lane) * 4u;
+        auto issue_norms = [&](int64_t tl, uint32_t b) {
+            const uint32_t dst = nb + b * 256u;
+            const int hh = (int)(tl / tiles_per_tensor);
+            const int64_t ii = (tl - (int64_t)hh * tiles_per_tensor) * kTileM + row;
+            if (tl < te && ii < p.N) {
+                cp_async4(dst, p.rnorm + (int64_t)hh * p.N + ii);
+                cp_async4(dst + 128u, p.dnorm + (int64_t)hh * p.N + ii);
+            } else {
+                st_shared_f32(dst, 0.f);
+                st_shared_f32(dst + 128u, 0.f);
+            }
+            asm volatile("cp.async.commit_group;" ::: "memory");
+        };
+        issue_norms(tb + grp, 0u);
+        uint32_t nbuf = 0u;
         for (int64_t tile = tb + grp, lt = grp; tile < te; tile += kEpiGroups, lt += kEpiGroups) {
             const int h = (int)(tile / tiles_per_tensor);
             const int64_t i = (tile - (int64_t)h * tiles_per_tensor) * kTileM + row;
             const bool valid = i < p.N;
             const uint32_t buf = (uint32_t)grp, use = (uint32_t)lt >> 1;
-            const float rn = valid ? __ldg(p.rnorm + (int64_t)h * p.N + i) : 0.f;
-            const float dn = valid ? __ldg(p.dnorm + (int64_t)h * p.N + i) : 0.f;
+            // this tile's pair (the only copies in flight), then the next tile's
+            asm volatile("cp.async.wait_all;" ::: "memory");
+            const float rn = ld_shared_f32(nb + nbuf * 256u), dn = ld_shared_f32(nb + nbuf * 256u + 128u);
+            nbuf ^= 1u;
+            issue_norms(tile + kEpiGroups, nbuf);
             if (h != cur_h) {
                 // the tensor's largest centroid norm and fp16 rounding error (each warp
                 // reduces them itself)
@@ -798,7 +835,7 @@ static EncodeTiledFn encode_fn() {
 // score and candidate words per row)
 static size_t assign_tail_bytes(int nslots) {
     return (size_t)(2 * nslots + 3 + 2 * kEpiGroups) * 8 + 16 + 16 /* alignment */ +
-           (size_t)kEpiGroups * (2 * kTileM + 4 * kTileM) * 4;
+           (size_t)kEpiGroups * (2 * kTileM + 4 * kTileM) * 4 + (size_t)kEpiGroups * 8 * 128 * 4;
 }
 
 // the fp16 centroid plane (two 64-channel blocks), the offset rows and the constant block

@@ -244,17 +244,16 @@ __device__ __forceinline__ void stage_input8(const QPlan &p, int h, const int64_
     }
 }
 
-// 8 channels of X as four pairs; false when one is not finite
-__device__ __forceinline__ bool load_x8_pairs(const QPlan &p, int64_t off, float2 (&v)[4]) {
+// 8 channels of X as four pairs; the probe becomes NaN if one of them is not finite
+// (x * 0 is NaN exactly for an infinity or a NaN)
+__device__ __forceinline__ void load_x8_pairs(const QPlan &p, int64_t off, float2 (&v)[4], float2 &probe) {
     float x[8];
     load_x8(p.X, p.in_dtype, off, x);
-    bool fin = true;
 #pragma unroll
     for (int q = 0; q < 4; q++) {
         v[q] = make_float2(x[2 * q], x[2 * q + 1]);
-        fin &= isfinite(x[2 * q]) && isfinite(x[2 * q + 1]);
+        probe = __ffma2_rn(v[q], make_float2(0.f, 0.f), probe);
     }
-    return fin;
 }
 
 // --------------------------------------------------------------------------------------
@@ -278,9 +277,15 @@ __global__ void __launch_bounds__(256) k_prep(QPlan p, int t) {
     const int c8 = threadIdx.x & 15;
     const int64_t i0 = (int64_t)blockIdx.x * kPrepTokens;
     const int64_t i1 = min(p.N, i0 + kPrepTokens);
-    float mu[8];
-    load_f8(p.mu + h * kD + c8 * 8, mu);
-    bool finite = true, bad_index = false;
+    float2 mu[4];
+    {
+        float m8[8];
+        load_f8(p.mu + h * kD + c8 * 8, m8);
+#pragma unroll
+        for (int q = 0; q < 4; q++) mu[q] = make_float2(m8[2 * q], m8[2 * q + 1]);
+    }
+    float2 probe = make_float2(0.f, 0.f);
+    bool bad_index = false;
 #pragma unroll 1
     for (int64_t ib = i0; ib < i1; ib += 16 * G) {
         // the loop bound is uniform over the block, so every lane reaches the shuffles
@@ -292,7 +297,7 @@ __global__ void __launch_bounds__(256) k_prep(QPlan p, int t) {
             ii[g] = ib + 16 * g + (threadIdx.x >> 4);
             valid[g] = ii[g] < i1;
             if (valid[g]) {
-                finite &= load_x8_pairs(p, h * p.x_stride + ii[g] * kD + c8 * 8, v[g]);
+                load_x8_pairs(p, h * p.x_stride + ii[g] * kD + c8 * 8, v[g], probe);
             } else {
 #pragma unroll
                 for (int q = 0; q < 4; q++) v[g][q] = make_float2(0.f, 0.f);
@@ -301,31 +306,33 @@ __global__ void __launch_bounds__(256) k_prep(QPlan p, int t) {
         stage_input8<G, NST>(p, h, ii, valid, c8, t - 1, v, bad_index);
 #pragma unroll
         for (int g = 0; g < G; g++) {
-            float ss = 0.f, dd = 0.f;
-            __align__(16) __half a16[8];
+            // a = r - mu, its fp16 copy and the fp16 rounding error (exact), on pairs
+            float2 ss = make_float2(0.f, 0.f), dd = ss;
+            __align__(16) __half2 a16[4];
 #pragma unroll
-            for (int q = 0; q < 8; q++) {
-                const float s = q & 1 ? v[g][q >> 1].y : v[g][q >> 1].x;
-                const float x = __fsub_rn(s, mu[q]);
-                a16[q] = __float2half_rn(x);
-                const float dx = __fsub_rn(x, __half2float(a16[q]));  // exact
-                ss = __fmaf_rn(x, x, ss);
-                dd = __fmaf_rn(dx, dx, dd);
+            for (int q = 0; q < 4; q++) {
+                const float2 x = sub2(v[g][q], mu[q]);
+                a16[q] = __float22half2_rn(x);
+                const float2 dx = sub2(x, __half22float2(a16[q]));
+                ss = __ffma2_rn(x, x, ss);
+                dd = __ffma2_rn(dx, dx, dd);
             }
             if (valid[g])
                 *reinterpret_cast<uint4 *>(p.A + ((int64_t)h * p.N + ii[g]) * kD + c8 * 8) =
                     *reinterpret_cast<uint4 *>(a16);
+            float sss = __fadd_rn(ss.x, ss.y), ddd = __fadd_rn(dd.x, dd.y);
 #pragma unroll
             for (int o = 8; o >= 1; o >>= 1) {
-                ss += __shfl_xor_sync(0xffffffffu, ss, o);
-                dd += __shfl_xor_sync(0xffffffffu, dd, o);
+                sss += __shfl_xor_sync(0xffffffffu, sss, o);
+                ddd += __shfl_xor_sync(0xffffffffu, ddd, o);
             }
             if (valid[g] && c8 == 0) {
-                p.rnorm[h * p.N + ii[g]] = sqrtf(ss);
-                p.dnorm[h * p.N + ii[g]] = sqrtf(dd);
+                p.rnorm[h * p.N + ii[g]] = sqrtf(sss);
+                p.dnorm[h * p.N + ii[g]] = sqrtf(ddd);
             }
         }
     }
+    const bool finite = probe.x == probe.x && probe.y == probe.y;
     // one status update per block
     __shared__ int bad, bad_idx;
     if (threadIdx.x == 0) bad = 0, bad_idx = 0;
@@ -424,18 +431,47 @@ __device__ __forceinline__ void acc_two_sum(float &s, float &e, float x) {
     e = __fadd_rn(e, err);
 }
 
-__global__ void __launch_bounds__(kSortBlock) k_sort_hist(QPlan p, int t) {
+// The sort's items.  delta = 0 (a stage's first round): every token, keyed by its cluster.
+// delta = 1 (later rounds): for every token whose cluster changed since the previous round,
+// a leave item keyed by its old cluster and an enter item keyed by its new one; within a
+// token block and cluster the leave items come first, each kind in token order, so the
+// order is fixed.
+struct SortKeys {
+    int leave, enter;  // cluster keys of the token's items (-1: none)
+    bool changed;
+};
+__device__ __forceinline__ SortKeys sort_keys(const QPlan &p, int h, int t, int64_t i, int delta) {
+    SortKeys k{-1, -1, false};
+    if (i >= p.N) return k;
+    const int j = p.pi[(int64_t)(h * p.T + t - 1) * p.cap + p.tok_off + i];
+    if (j >= p.C) return k;  // reported by the histogram; the token takes no part
+    if (!delta) {
+        k.enter = j;
+        return k;
+    }
+    const int jo = p.pi_prev[(int64_t)h * p.N + i];
+    if (jo != j) {
+        k.leave = jo;
+        k.enter = j;
+        k.changed = true;
+    }
+    return k;
+}
+
+__global__ void __launch_bounds__(kSortBlock) k_sort_hist(QPlan p, int t, int delta) {
     pdl_begin();
-    __shared__ int hist[kMaxC];
+    __shared__ int hist[kMaxC], lhist[kMaxC];
     const int h = blockIdx.y, b = blockIdx.x;
-    for (int j = threadIdx.x; j < p.C; j += kSortBlock) hist[j] = 0;
+    for (int j = threadIdx.x; j < p.C; j += kSortBlock) hist[j] = lhist[j] = 0;
     __syncthreads();
     const int64_t i = (int64_t)b * kSortBlock + threadIdx.x;
-    const uint8_t *pis = p.pi + (int64_t)(h * p.T + t - 1) * p.cap + p.tok_off;
-    if (i < p.N) {
-        const int j = pis[i];
-        if (j < p.C) atomicAdd(hist + j, 1);
-        else or_status(p.status, QVG_DEV_BAD_INDEX);
+    if (i < p.N && p.pi[(int64_t)(h * p.T + t - 1) * p.cap + p.tok_off + i] >= p.C)
+        or_status(p.status, QVG_DEV_BAD_INDEX);
+    const SortKeys k = sort_keys(p, h, t, i, delta);
+    if (k.enter >= 0) atomicAdd(hist + k.enter, 1);
+    if (k.leave >= 0) {
+        atomicAdd(hist + k.leave, 1);
+        atomicAdd(lhist + k.leave, 1);
     }
     __syncthreads();
     int *bh = p.blockoff + ((int64_t)h * p.nsb + b) * p.C;
@@ -443,13 +479,14 @@ __global__ void __launch_bounds__(kSortBlock) k_sort_hist(QPlan p, int t) {
         const int v = hist[j];
         bh[j] = v;
         if (v) atomicAdd(p.counts + h * p.C + j, v);  // cluster totals (zero on entry)
+        if (lhist[j]) atomicAdd(p.dleave + h * p.C + j, lhist[j]);
     }
 }
 
 // Offsets of the counting sort.  grid (C/32 cluster groups, H), block 256: lane = cluster
 // of the group, warp w = a slice of the token blocks.  offs[j] = sum of the totals of the
 // clusters before j; blockoff[b][j] (in place, over the block histogram) = offs[j] + the
-// tokens of cluster j in the blocks before b.
+// items of cluster j in the blocks before b; items = the tensor's total.
 __global__ void __launch_bounds__(256) k_sort_scan(QPlan p) {
     pdl_begin();
     constexpr int NW = 8;
@@ -467,6 +504,7 @@ __global__ void __launch_bounds__(256) k_sort_scan(QPlan p) {
         tot[x] += a1;
         __syncthreads();
     }
+    if (blockIdx.x == 0 && x == 0) p.items[h] = tot[kMaxC - 1];
     int *bh = p.blockoff + (int64_t)h * p.nsb * p.C;
     const int per = (p.nsb + NW - 1) / NW;
     const int b0 = w * per, b1 = min(p.nsb, b0 + per);
@@ -490,30 +528,41 @@ __global__ void __launch_bounds__(256) k_sort_scan(QPlan p) {
     }
 }
 
-__global__ void __launch_bounds__(kSortBlock) k_sort_scatter(QPlan p, int t) {
+// Writes the block's items to their sorted positions (the leave items of a cluster before
+// its enter items, each in token order), and the round's assignment into pi_prev.
+__global__ void __launch_bounds__(kSortBlock) k_sort_scatter(QPlan p, int t, int delta) {
     pdl_begin();
     constexpr int NW = kSortBlock / 32;
-    __shared__ int wcnt[NW][kMaxC];  // tokens of each cluster in each warp
+    __shared__ int wl[NW][kMaxC], we[NW][kMaxC];  // leave / enter items of each cluster per warp
     const int h = blockIdx.y, b = blockIdx.x;
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    for (int x = threadIdx.x; x < NW * kMaxC; x += kSortBlock) (&wcnt[0][0])[x] = 0;
+    for (int x = threadIdx.x; x < NW * kMaxC; x += kSortBlock) (&wl[0][0])[x] = (&we[0][0])[x] = 0;
     __syncthreads();
     const int64_t i = (int64_t)b * kSortBlock + threadIdx.x;
-    const uint8_t *pis = p.pi + (int64_t)(h * p.T + t - 1) * p.cap + p.tok_off;
-    int j = -1;
-    if (i < p.N) {
-        j = pis[i];
-        if (j >= p.C) j = -1;
-    }
-    const unsigned same = __match_any_sync(0xffffffffu, j);
-    const int rank = __popc(same & ((1u << lane) - 1u));  // earlier lanes, same cluster
-    if (j >= 0 && rank == 0) wcnt[w][j] = __popc(same);
+    const SortKeys k = sort_keys(p, h, t, i, delta);
+    const unsigned sl = __match_any_sync(0xffffffffu, k.leave);
+    const unsigned se = __match_any_sync(0xffffffffu, k.enter);
+    const unsigned below = (1u << lane) - 1u;
+    const int rl = __popc(sl & below), re = __popc(se & below);  // earlier lanes, same key
+    if (k.leave >= 0 && rl == 0) wl[w][k.leave] = __popc(sl);
+    if (k.enter >= 0 && re == 0) we[w][k.enter] = __popc(se);
     __syncthreads();
-    if (j >= 0) {
-        int pos = p.blockoff[((int64_t)h * p.nsb + b) * p.C + j] + rank;
-        for (int w2 = 0; w2 < w; w2++) pos += wcnt[w2][j];
-        p.ids[(int64_t)h * p.N + pos] = (int)i;
-        p.cid[(int64_t)h * p.N + pos] = (uint8_t)j;
+    const int *bo = p.blockoff + ((int64_t)h * p.nsb + b) * p.C;
+    int *ids = p.ids + (int64_t)h * p.icap;
+    uint8_t *cid = p.cid + (int64_t)h * p.icap;
+    if (k.leave >= 0) {
+        int pos = bo[k.leave] + rl;
+        for (int w2 = 0; w2 < w; w2++) pos += wl[w2][k.leave];
+        ids[pos] = (int)i | (int)0x80000000u;
+        cid[pos] = (uint8_t)k.leave;
+    }
+    if (k.enter >= 0) {
+        int pos = bo[k.enter] + re;
+        for (int w2 = 0; w2 < NW; w2++) pos += wl[w2][k.enter];  // the block's leave items first
+        for (int w2 = 0; w2 < w; w2++) pos += we[w2][k.enter];
+        ids[pos] = (int)i;
+        cid[pos] = (uint8_t)k.enter;
+        if (!delta || k.changed) p.pi_prev[(int64_t)h * p.N + i] = (uint8_t)k.enter;
     }
 }
 
@@ -565,8 +614,8 @@ __device__ __forceinline__ void write_centroid(const QPlan &p, int h, int t, int
     if (lane == 0) p.cnd[(int64_t)h * p.Cpad + j] = make_float2(ss, sqrtf(dd));
 }
 
-// Cluster sums over chunks of 32 cluster-sorted positions.  The rows of each run (same
-// cluster) are added with TwoSum in sorted order.  A run that is a whole cluster leaves its
+// Cluster sums over chunks of 32 cluster-sorted items.  The rows of each run (same
+// cluster) are added with TwoSum in sorted order, a leave item's row negated (exactly).  A run that is a whole cluster leaves its
 // (sum, error) in the cluster's slot; a run that crosses the chunk's start or end leaves it
 // in the chunk's first / last slot.  k_cluster_finalize turns them into means.  Stage 1
 // (nothing to subtract) fits 64 registers, so four CTAs share an SM; the second stage (one
@@ -611,6 +660,7 @@ __device__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
 struct SumChunk {
     int h, k, nk;           // tensor, chunk, positions in the chunk
     int id, cl;             // the lane's token and cluster (cl = -1 past the end)
+    uint32_t neg;           // bit m: position m is a leave item (its row is subtracted)
     int xrow, crow;         // row of the token in the X row view; first row of the tables
     int c_prev, c_next;     // clusters just before and after the chunk (-1: none)
     uint32_t pk0, pk1;      // the token's earlier clusters, 8 bits a stage
@@ -630,7 +680,17 @@ __global__ void __launch_bounds__(256, TP == 0 ? 4 : (TP == 1 ? 3 : 2))
     const int wpc = blockDim.x >> 5;
     const int total = p.H * p.nchunk;
     const int nw = gridDim.x * wpc;
-    int ci = blockIdx.x * wpc + wid;
+    // the warp's chunks: every nw-th of all tensors' chunk slots, skipping those past the
+    // tensor's item count (in a stage's first round half the slots, in later ones most)
+    auto next_chunk = [&](int c) {
+        while (c < total) {
+            const int h = c / p.nchunk;
+            if ((int64_t)(c - h * p.nchunk) * kChunk < (int64_t)p.items[h]) break;
+            c += nw;
+        }
+        return c;
+    };
+    int ci = next_chunk(blockIdx.x * wpc + wid);
     if (ci >= total) return;  // no CTA-wide barrier below
     const uint32_t bars = smem_u32(bulk_smem) + wid * 16;  // group n waits on bars + 8 (n & 1)
     const uint32_t ring = smem_u32(bulk_smem) + 128 + wid * 2 * kBulkGroup * row_bytes;
@@ -646,15 +706,18 @@ __global__ void __launch_bounds__(256, TP == 0 ? 4 : (TP == 1 ? 3 : 2))
         m.h = c / p.nchunk;
         m.k = c - m.h * p.nchunk;
         const int64_t c0 = (int64_t)m.k * kChunk;
-        m.nk = (int)min((int64_t)kChunk, p.N - c0);
-        const int64_t base = (int64_t)m.h * p.N + c0;
+        const int64_t n_items = p.items[m.h];
+        m.nk = (int)min((int64_t)kChunk, n_items - c0);
+        const int64_t base = (int64_t)m.h * p.icap + c0;
         const bool mine = lane < m.nk;
-        m.id = mine ? p.ids[base + lane] : 0;
+        const int raw = mine ? p.ids[base + lane] : 0;
+        m.id = raw & 0x7FFFFFFF;
+        m.neg = __ballot_sync(0xffffffffu, raw < 0);
         m.cl = mine ? (int)p.cid[base + lane] : -1;
         m.xrow = (int)(m.h * (p.x_stride / kD)) + m.id;
         m.crow = (int)((m.h * p.cent_tstride + p.cent_off) / kD);
         m.c_prev = m.k > 0 ? (int)p.cid[base - 1] : -1;
-        m.c_next = c0 + m.nk < p.N ? (int)p.cid[base + m.nk] : -1;
+        m.c_next = c0 + m.nk < n_items ? (int)p.cid[base + m.nk] : -1;
     };
     auto fetch_pi = [&](SumChunk &m) {  // needs m.id; also finds the run starts
         m.pk0 = m.pk1 = 0u;
@@ -727,7 +790,7 @@ __global__ void __launch_bounds__(256, TP == 0 ? 4 : (TP == 1 ? 3 : 2))
     issue_next();
     issue_next();
     for (;;) {
-        const int cn = ci + nw;
+        const int cn = next_chunk(ci + nw);
         has_next = cn < total;
         if (has_next) {
             fetch(cn, nxt);
@@ -755,7 +818,7 @@ __global__ void __launch_bounds__(256, TP == 0 ? 4 : (TP == 1 ? 3 : 2))
         // fp32 difference and r the sum of the chain's rounding errors; d goes through the
         // compensated sum and r is added to its error term, so the sum is that of the exact
         // residuals (to about twice fp32's precision), not of their fp32 roundings.
-        auto add_row = [&](const uint8_t *hs, int u, uint32_t q0, uint32_t q1) {
+        auto add_row = [&](const uint8_t *hs, int u, uint32_t q0, uint32_t q1, uint32_t sg) {
             const uint8_t *slot = hs + u * XB;  // the X row
             float2 v01, v23;
             if constexpr (SRC == 0) {
@@ -771,9 +834,13 @@ __global__ void __launch_bounds__(256, TP == 0 ? 4 : (TP == 1 ? 3 : 2))
                 v01 = make_float2(w.x, w.y);
                 v23 = make_float2(w.z, w.w);
             }
+            auto flip = [sg](float2 a) {  // negation of a leave item's values (exact)
+                return make_float2(__uint_as_float(__float_as_uint(a.x) ^ sg),
+                                   __uint_as_float(__float_as_uint(a.y) ^ sg));
+            };
             if constexpr (TP == 0) {
-                acc_two_sum2(s01, e01, v01);
-                acc_two_sum2(s23, e23, v23);
+                acc_two_sum2(s01, e01, flip(v01));
+                acc_two_sum2(s23, e23, flip(v23));
             } else {
                 float2 r01 = make_float2(0.f, 0.f), r23 = r01;
                 auto chain = [&](int st) {  // subtract the row of stage st + 1
@@ -792,10 +859,10 @@ __global__ void __launch_bounds__(256, TP == 0 ? 4 : (TP == 1 ? 3 : 2))
                 } else {
                     for (int st = 0; st < tp; st++) chain(st);
                 }
-                acc_two_sum2(s01, e01, v01);
-                acc_two_sum2(s23, e23, v23);
-                e01 = __fadd2_rn(e01, r01);
-                e23 = __fadd2_rn(e23, r23);
+                acc_two_sum2(s01, e01, flip(v01));
+                acc_two_sum2(s23, e23, flip(v23));
+                e01 = __fadd2_rn(e01, flip(r01));
+                e23 = __fadd2_rn(e23, flip(r23));
             }
         };
         const uint32_t starts = cur.brk & ~1u;  // position 0 opens the first run above
@@ -816,7 +883,8 @@ __global__ void __launch_bounds__(256, TP == 0 ? 4 : (TP == 1 ? 3 : 2))
                 for (int u = 0; u < kBulkGroup; u++) {
                     const int m = g * kBulkGroup + u;
                     add_row(gslots, u, TP != 0 ? __shfl_sync(0xffffffffu, cur.pk0, m) : 0u,
-                            TP < 0 ? __shfl_sync(0xffffffffu, cur.pk1, m) : 0u);
+                            TP < 0 ? __shfl_sync(0xffffffffu, cur.pk1, m) : 0u,
+                            ((cur.neg >> m) & 1u) << 31);
                 }
             } else {
 #pragma unroll 1
@@ -829,7 +897,8 @@ __global__ void __launch_bounds__(256, TP == 0 ? 4 : (TP == 1 ? 3 : 2))
                         s01 = s23 = e01 = e23 = make_float2(0.f, 0.f);
                     }
                     add_row(gslots, u, TP != 0 ? __shfl_sync(0xffffffffu, cur.pk0, m) : 0u,
-                            TP < 0 ? __shfl_sync(0xffffffffu, cur.pk1, m) : 0u);
+                            TP < 0 ? __shfl_sync(0xffffffffu, cur.pk1, m) : 0u,
+                            ((cur.neg >> m) & 1u) << 31);
                 }
             }
             n_done++;
@@ -870,77 +939,115 @@ static cudaError_t launch_sums(const QPlan &p, const AssignMaps *maps, int t, in
                          p, t, maps->gather);
 }
 
-// One warp per cluster: the mean from the cluster's own slot, or, for clusters spread over
-// several chunks, from their pieces added in chunk order; empty clusters keep their
-// centroid.  Then the centroid and its GEMM planes are written.
-__global__ void __launch_bounds__(256) k_cluster_finalize(QPlan p, int t, int planes) {
+// One warp per cluster.  The round's items of the cluster come from its own slot or, when
+// they span several chunks, from their pieces added in chunk order.  In a stage's first
+// round they are all its members; in a delta round they are the tokens that left (negated)
+// and entered it, added to the total the previous round kept.  The total is kept,
+// renormalised, for the next round, and the mean of the members written with its GEMM
+// operands.  A cluster with no members keeps its centroid.
+__global__ void __launch_bounds__(256) k_cluster_finalize(QPlan p, int t, int planes, int delta) {
     pdl_begin();
     const int lane = threadIdx.x & 31;
     const int j = blockIdx.x * 8 + (threadIdx.x >> 5);
     const int h = blockIdx.y;
     if (j >= p.C) return;
-    // the total and the offset load together (the offset is unused for an empty cluster)
-    const int cnt = p.counts[h * p.C + j];
-    const int off = p.offs[h * p.C + j];
+    const int64_t hj = (int64_t)h * p.C + j;
+    // the item count and offset load together (the offset is unused without items)
+    const int cnt = p.counts[hj];
+    const int off = p.offs[hj];
+    if (delta && cnt == 0) return;  // no member moved: the centroid and its operands stand
+    float S[4] = {0.f, 0.f, 0.f, 0.f}, E[4] = {0.f, 0.f, 0.f, 0.f};
+    float *tt = p.tot + hj * 2 * kD;
+    int n = cnt;
+    if (delta) {
+        n = p.ccount[hj] + cnt - 2 * p.dleave[hj];
+        const float4 ta = reinterpret_cast<const float4 *>(tt)[lane];
+        const float4 tb = reinterpret_cast<const float4 *>(tt + kD)[lane];
+        S[0] = ta.x; S[1] = ta.y; S[2] = ta.z; S[3] = ta.w;
+        E[0] = tb.x; E[1] = tb.y; E[2] = tb.z; E[3] = tb.w;
+    }
     const float4 mu = *reinterpret_cast<const float4 *>(p.mu + h * kD + 4 * lane);
-    if (cnt == 0) {
-        write_centroid(p, h, t, j, lane, false, make_float4(0.f, 0.f, 0.f, 0.f), planes != 0, mu);
+    if (cnt > 0) {
+        const int a = off / kChunk, b = (off + cnt - 1) / kChunk;
+        if (a == b) {
+            // all of the cluster's items were one run of one chunk
+            const float *ws = p.wsum + hj * 2 * kD;
+            const float4 sa = reinterpret_cast<const float4 *>(ws)[lane];
+            const float4 sb = reinterpret_cast<const float4 *>(ws + kD)[lane];
+            const float av[4] = {sa.x, sa.y, sa.z, sa.w}, bv[4] = {sb.x, sb.y, sb.z, sb.w};
+#pragma unroll
+            for (int k = 0; k < 4; k++) {
+                acc_two_sum(S[k], E[k], av[k]);
+                E[k] = __fadd_rn(E[k], bv[k]);
+            }
+        }
+        const int np = a == b ? 0 : b - a + 1;
+        for (int q0 = 0; q0 < np; q0 += 4) {
+            float4 sa[4], sb[4];  // 4 pieces' loads in flight, added in chunk order
+#pragma unroll
+            for (int u = 0; u < 4; u++)
+                if (q0 + u < np) {
+                    const int kk = a + q0 + u;
+                    // in its first chunk the cluster's run is the chunk's last run unless
+                    // it starts exactly at the chunk start; in later chunks it is the first
+                    const int slot = (kk == a && off != (int64_t)a * kChunk) ? 1 : 0;
+                    const float *ps = p.psum + (((int64_t)h * p.nchunk + kk) * 2 + slot) * 2 * kD;
+                    sa[u] = reinterpret_cast<const float4 *>(ps)[lane];
+                    sb[u] = reinterpret_cast<const float4 *>(ps + kD)[lane];
+                }
+#pragma unroll
+            for (int u = 0; u < 4; u++)
+                if (q0 + u < np) {
+                    const float av[4] = {sa[u].x, sa[u].y, sa[u].z, sa[u].w};
+                    const float bv[4] = {sb[u].x, sb[u].y, sb[u].z, sb[u].w};
+#pragma unroll
+                    for (int k = 0; k < 4; k++) {
+                        acc_two_sum(S[k], E[k], av[k]);
+                        E[k] = __fadd_rn(E[k], bv[k]);
+                    }
+                }
+        }
+    }
+    // every lane has read the counters; they restart at zero for the next round's sort
+    __syncwarp();
+    if (lane == 0) {
+        p.counts[hj] = 0;
+        p.dleave[hj] = 0;
+        p.ccount[hj] = n;
+    }
+    if (n <= 0) {
+        // no members: the total restarts at zero and the centroid stays (in the first
+        // round its operands are written again from it)
+        reinterpret_cast<float4 *>(tt)[lane] = make_float4(0.f, 0.f, 0.f, 0.f);
+        reinterpret_cast<float4 *>(tt + kD)[lane] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (!delta) write_centroid(p, h, t, j, lane, false, make_float4(0.f, 0.f, 0.f, 0.f), planes != 0, mu);
         return;
     }
-    const int a = off / kChunk, b = (off + cnt - 1) / kChunk;
-    float S[4] = {0.f, 0.f, 0.f, 0.f}, E[4] = {0.f, 0.f, 0.f, 0.f};
-    if (a == b) {
-        // the whole cluster was one run of one chunk
-        const float *ws = p.wsum + ((int64_t)h * p.C + j) * 2 * kD;
-        const float4 sa = reinterpret_cast<const float4 *>(ws)[lane];
-        const float4 sb = reinterpret_cast<const float4 *>(ws + kD)[lane];
-        S[0] = sa.x; S[1] = sa.y; S[2] = sa.z; S[3] = sa.w;
-        E[0] = sb.x; E[1] = sb.y; E[2] = sb.z; E[3] = sb.w;
+    // renormalise: S + E exactly as fl(S + E) plus its rounding error
+#pragma unroll
+    for (int k = 0; k < 4; k++) {
+        float sum = S[k], err = 0.f;
+        acc_two_sum(sum, err, E[k]);
+        S[k] = sum;
+        E[k] = err;
     }
-    const int np = a == b ? 0 : b - a + 1;
-    for (int q0 = 0; q0 < np; q0 += 4) {
-        float4 sa[4], sb[4];  // 4 pieces' loads in flight, added in chunk order
-#pragma unroll
-        for (int u = 0; u < 4; u++)
-            if (q0 + u < np) {
-                const int kk = a + q0 + u;
-                // in its first chunk the cluster's run is the chunk's last run unless it
-                // starts exactly at the chunk start; in later chunks it is the first run
-                const int slot = (kk == a && off != (int64_t)a * kChunk) ? 1 : 0;
-                const float *ps = p.psum + (((int64_t)h * p.nchunk + kk) * 2 + slot) * 2 * kD;
-                sa[u] = reinterpret_cast<const float4 *>(ps)[lane];
-                sb[u] = reinterpret_cast<const float4 *>(ps + kD)[lane];
-            }
-#pragma unroll
-        for (int u = 0; u < 4; u++)
-            if (q0 + u < np) {
-                const float av[4] = {sa[u].x, sa[u].y, sa[u].z, sa[u].w};
-                const float bv[4] = {sb[u].x, sb[u].y, sb[u].z, sb[u].w};
-#pragma unroll
-                for (int k = 0; k < 4; k++) {
-                    acc_two_sum(S[k], E[k], av[k]);
-                    E[k] = __fadd_rn(E[k], bv[k]);
-                }
-            }
-    }
-    const float n = (float)cnt;
+    reinterpret_cast<float4 *>(tt)[lane] = make_float4(S[0], S[1], S[2], S[3]);
+    reinterpret_cast<float4 *>(tt + kD)[lane] = make_float4(E[0], E[1], E[2], E[3]);
+    const float fn = (float)n;
     write_centroid(p, h, t, j, lane, true,
-                   make_float4(stored_mean(S[0], E[0], n, p.cfmt), stored_mean(S[1], E[1], n, p.cfmt),
-                               stored_mean(S[2], E[2], n, p.cfmt), stored_mean(S[3], E[3], n, p.cfmt)),
+                   make_float4(stored_mean(S[0], E[0], fn, p.cfmt), stored_mean(S[1], E[1], fn, p.cfmt),
+                               stored_mean(S[2], E[2], fn, p.cfmt), stored_mean(S[3], E[3], fn, p.cfmt)),
                    planes != 0, mu);
-    // zero the total again for the next round's histogram (an empty cluster's is already
-    // zero); every lane has used cnt by now
-    __syncwarp();
-    if (lane == 0) p.counts[h * p.C + j] = 0;
 }
 
 cudaError_t launch_cluster_means(const QPlan &p, const AssignMaps *maps, int t, bool planes,
-                                 int num_sms, cudaStream_t st) {
+                                 bool delta, int num_sms, cudaStream_t st) {
     const dim3 sgrid((unsigned)p.nsb, p.H);
-    cudaError_t e = launch_kernel(k_sort_hist, sgrid, dim3(kSortBlock), 0, st, p, t);
+    const int dl = delta ? 1 : 0;
+    cudaError_t e = launch_kernel(k_sort_hist, sgrid, dim3(kSortBlock), 0, st, p, t, dl);
     if (e == cudaSuccess)
         e = launch_kernel(k_sort_scan, dim3((unsigned)((p.C + 31) / 32), p.H), dim3(256), 0, st, p);
-    if (e == cudaSuccess) e = launch_kernel(k_sort_scatter, sgrid, dim3(kSortBlock), 0, st, p, t);
+    if (e == cudaSuccess) e = launch_kernel(k_sort_scatter, sgrid, dim3(kSortBlock), 0, st, p, t, dl);
     if (e != cudaSuccess) return e;
     auto sums = [&](auto src) {
         constexpr int S = decltype(src)::value;
@@ -957,7 +1064,7 @@ cudaError_t launch_cluster_means(const QPlan &p, const AssignMaps *maps, int t, 
                                : sums(std::integral_constant<int, 0>());
     if (e != cudaSuccess) return e;
     return launch_kernel(k_cluster_finalize, dim3((unsigned)((p.C + 7) / 8), p.H), dim3(256), 0, st, p, t,
-                         planes ? 1 : 0);
+                         planes ? 1 : 0, dl);
 }
 
 // --------------------------------------------------------------------------------------

@@ -22,8 +22,8 @@ inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 
 inline int cpad_of(int C) { return (C + 31) / 32 * 32; }
 
 struct WsLayout {
-    size_t A, rnorm, dnorm, B, Bx, cnd, mu, counts, offs, blockoff, ids, cid, psum, wsum, init_idx,
-        stats, rq_cta, rq, total;
+    size_t A, rnorm, dnorm, B, Bx, cnd, mu, counts, offs, blockoff, ids, cid, items, psum, wsum, tot,
+        ccount, dleave, pi_prev, init_idx, stats, rq_cta, rq, total;
     int nsb, nchunk;
 };
 
@@ -45,15 +45,21 @@ WsLayout ws_layout(int64_t H, int64_t N, int C, int T) {
         w.Bx = take((size_t)H * Cpad * kOffsetRow * 4);
         w.cnd = take((size_t)H * Cpad * 8);
         w.mu = take((size_t)H * kD * 4);
+        const int64_t icap = 2 * N;  // items: a token, or two events of a changed token
         w.nsb = (int)((N + kSortBlock - 1) / kSortBlock);
-        w.nchunk = (int)((N + kChunk - 1) / kChunk);
+        w.nchunk = (int)((icap + kChunk - 1) / kChunk);
         w.counts = take((size_t)H * C * 4);
         w.offs = take((size_t)H * C * 4);
         w.blockoff = take((size_t)H * w.nsb * C * 4);
-        w.ids = take((size_t)H * N * 4);
-        w.cid = take((size_t)H * N);
+        w.ids = take((size_t)H * icap * 4);
+        w.cid = take((size_t)H * icap);
+        w.items = take((size_t)H * 4);
         w.psum = take((size_t)H * w.nchunk * 4 * kD * 4);
         w.wsum = take((size_t)H * C * 2 * kD * 4);
+        w.tot = take((size_t)H * C * 2 * kD * 4);
+        w.ccount = take((size_t)H * C * 4);
+        w.dleave = take((size_t)H * C * 4);
+        w.pi_prev = take((size_t)H * N);
         w.init_idx = take((size_t)H * T * C * 4);
         w.rq_cta = take((size_t)2 * kMaxAssignCtas * 4);
         w.rq = take((size_t)H * ((N + kAssignTileM - 1) / kAssignTileM) * kAssignTileM *
@@ -127,8 +133,10 @@ qvg_status device_info(int *num_sms) {
 // The T smoothing stages: cold-start or warm centroids, then `iters` Lloyd rounds each.
 qvg_status run_stages(QPlan &p, const AssignMaps *maps, int num_sms, cudaStream_t st) {
     qvg_status rc = QVG_OK;
-    // the sort's cluster totals start at zero; each update leaves them at zero again
-    if (cudaMemsetAsync(p.counts, 0, (size_t)p.H * p.C * 4, st) != cudaSuccess) return QVG_ERR_CUDA;
+    // the sort's item and leave counts start at zero; each update leaves them at zero again
+    if (cudaMemsetAsync(p.counts, 0, (size_t)p.H * p.C * 4, st) != cudaSuccess ||
+        cudaMemsetAsync(p.dleave, 0, (size_t)p.H * p.C * 4, st) != cudaSuccess)
+        return QVG_ERR_CUDA;
     for (int t = 1; t <= p.T && rc == QVG_OK; t++) {
         auto step = [&](cudaError_t e) {
             if (e != cudaSuccess && rc == QVG_OK) rc = QVG_ERR_CUDA;
@@ -141,7 +149,10 @@ qvg_status run_stages(QPlan &p, const AssignMaps *maps, int num_sms, cudaStream_
         for (int it = 1; it <= p.iters && rc == QVG_OK; it++) {
             step(launch_assign(p, maps, t, num_sms, st));
             step(launch_refine(p, t, num_sms, st));
-            step(launch_cluster_means(p, maps, t, it < p.iters, num_sms, st));
+            // The first round sums every member; the ones between fold in the tokens that
+            // moved.  The last sums every member again, so the stage's centroids are means
+            // of a fresh compensated sum, with no rounding carried over from earlier rounds.
+            step(launch_cluster_means(p, maps, t, it < p.iters, it > 1 && it < p.iters, num_sms, st));
         }
     }
     return rc;
@@ -208,6 +219,12 @@ QPlan make_plan(const qvg_quant_params *prm, const void *X, const float *warm,
         p.cid = reinterpret_cast<uint8_t *>(ws + w.cid);
         p.psum = reinterpret_cast<float *>(ws + w.psum);
         p.wsum = reinterpret_cast<float *>(ws + w.wsum);
+        p.items = reinterpret_cast<int *>(ws + w.items);
+        p.tot = reinterpret_cast<float *>(ws + w.tot);
+        p.ccount = reinterpret_cast<int *>(ws + w.ccount);
+        p.dleave = reinterpret_cast<int *>(ws + w.dleave);
+        p.pi_prev = reinterpret_cast<uint8_t *>(ws + w.pi_prev);
+        p.icap = 2 * p.N;
         p.nsb = w.nsb;
         p.nchunk = w.nchunk;
         p.init_idx = reinterpret_cast<int *>(ws + w.init_idx);
