@@ -224,6 +224,20 @@ qvg_status qvg_reassign(const qvg_quant_params *params, const void *X, const qvg
                         void *workspace, size_t workspace_bytes, uint32_t *dev_status,
                         void *stream);
 
+/* The steps of qvg_reassign, for timing them one at a time: */
+#define QVG_STEP_PLANES 1 /* the centroids' GEMM operands (fp16 plane, offsets, norms) */
+#define QVG_STEP_GEMM 2   /* the tensor-core GEMM with its fused argmax epilogue: pi^(T)
+                             for every row with one candidate, the lowest candidate and a
+                             re-scoring request for the others */
+#define QVG_STEP_REFINE 4 /* the exact re-scoring of the requested rows */
+/* qvg_reassign with only the steps in the `steps` mask.  Each step reads what the earlier
+ * ones wrote in the workspace: run them in order, on one stream (the GEMM after the planes
+ * of the same centroids, the re-scoring after the GEMM).  QVG_ERR_INVALID_ARG for other
+ * bits; otherwise as qvg_reassign. */
+qvg_status qvg_reassign_steps(const qvg_quant_params *params, const void *X,
+                              const qvg_buffers *out, void *workspace, size_t workspace_bytes,
+                              int32_t steps, uint32_t *dev_status, void *stream);
+
 /* Self-test of the assignment kernel's failure handling; no step of the method.  It runs the
  * tensor-core assignment of qvg_reassign once with the load of the centroid operand withheld
  * and a wait limit of one millisecond (2 s in normal calls), so that the kernel's first wait

@@ -1,6 +1,6 @@
 """A numpy model of the arithmetic of libqvg's attention kernels, in fp32: the keys of a head
-cut into min(ceil(N / 256), 128) splits, each rounded up to a multiple of 32 keys,
-each split walked in 32-key tiles with a running maximum and weight sum per query, and the
+cut into splits of equal length (about 2048 splits over all heads, at least 64 keys and a
+multiple of 32 keys each), each split walked in 32-key tiles with a running maximum and weight sum per query, and the
 splits merged by rescaling to the largest maximum.  It stands in for the GPU output when the
 parity checkers are themselves tested on the CPU; it is not the oracle (oracle/attention.py
 is) and the library does not use it."""
@@ -9,16 +9,16 @@ import numpy as np
 f32 = np.float32
 
 
-def split_len(N: int) -> int:
-    target = min(max((N + 255) // 256, 1), 128)
-    length = (N + target - 1) // target
+def split_len(N: int, heads: int = 1) -> int:
+    target = max(2048 // max(heads, 1), 1)
+    length = max((N + target - 1) // target, 64)
     return (length + 31) // 32 * 32
 
 
-def attention_fp32(Q, K, V, scale):
+def attention_fp32(Q, K, V, scale, heads: int = 1):
     Q, K, V = (np.asarray(a, dtype=f32) for a in (Q, K, V))
     M, N = Q.shape[0], K.shape[0]
-    L = split_len(N)
+    L = split_len(N, heads)
     S = (N + L - 1) // L
     part = np.zeros((S, M, K.shape[1]), f32)
     ml = np.zeros((S, M, 2), f32)

@@ -139,6 +139,18 @@ def test_quantize_rejects_null_and_misaligned(lib):
     assert qvg.qvg_quantize(_qp(), base, None, good, None, 1 << 40, None, None) == qvg.QVG_ERR_WORKSPACE
 
 
+def test_reassign_steps_rejects_unknown_steps(lib):
+    buf = (ctypes.c_ubyte * 64)()
+    base = ctypes.addressof(buf) + (-ctypes.addressof(buf)) % 16
+    good = qvg.qvg_buffers(base, base, base, base)
+    for steps in (8, -1, qvg.QVG_STEP_GEMM | 16):
+        assert qvg.qvg_reassign_steps(_qp(), base, good, base, 1 << 40, steps, None,
+                                      None) == qvg.QVG_ERR_INVALID_ARG
+    # T = 0 has no assignment
+    assert qvg.qvg_reassign_steps(_qp(T=0), base, good, base, 1 << 40, qvg.QVG_STEP_GEMM,
+                                  None, None) == qvg.QVG_ERR_INVALID_ARG
+
+
 def test_dequantize_rejects_bad_arguments(lib):
     buf = (ctypes.c_ubyte * 64)()
     base = ctypes.addressof(buf) + (-ctypes.addressof(buf)) % 16
@@ -169,8 +181,9 @@ def _ap(**kw):
 
 def test_attention_workspace_bytes(lib):
     a = qvg.qvg_attention_workspace_bytes(_ap())
-    # 4 splits of 256 keys, 3 heads x 2 queries: partial rows of 128 floats plus 2 floats
-    assert a == 3 * 4 * 2 * 128 * 4 + 256
+    # 16 splits of 64 keys (about 2048 over the 3 heads, at least 64 keys each), 3 heads x 2
+    # queries: partial rows of 128 floats, then 2 floats each (256-byte aligned pieces)
+    assert a == 3 * 16 * 2 * 128 * 4 + (3 * 16 * 2 * 2 * 4 + 255) // 256 * 256
     assert qvg.qvg_attention_workspace_bytes(_ap(M=4)) > a
     assert qvg.qvg_attention_workspace_bytes(_ap(N=100000)) > a
     for bad in (dict(M=0), dict(M=17), dict(N=0), dict(d=64), dict(bits=3), dict(group=8),

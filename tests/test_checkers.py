@@ -119,14 +119,16 @@ def test_attention_tolerance(case):
 
 
 def test_model_splits_match_the_library_rule():
-    # the model cuts keys like the library: a multiple of 32 keys per split, at most 128
-    # splits, at most 256 keys per split while N <= 32768, every split non-empty
-    for N in (1, 31, 32, 255, 256, 257, 1000, 32760, 32768, 280800):
-        L = attention_model.split_len(N)
-        S = (N + L - 1) // L
-        assert L % 32 == 0 and 1 <= S <= 128 and (S - 1) * L < N
-        assert N > 32768 or L <= 256
-    assert attention_model.split_len(32760) == 256 and attention_model.split_len(280800) == 2208
+    # the model cuts keys like the library: a multiple of 32 keys per split, at least 64,
+    # about 2048 splits over all heads, every split non-empty
+    for heads in (1, 3, 12, 360):
+        for N in (1, 31, 32, 255, 256, 257, 1000, 32760, 32768, 280800):
+            L = attention_model.split_len(N, heads)
+            S = (N + L - 1) // L
+            assert L % 32 == 0 and L >= 64 and (S - 1) * L < N
+            assert S * heads <= max(2048, heads)
+    assert attention_model.split_len(32760, 12) == 224 and attention_model.split_len(32760, 1) == 64
+    assert attention_model.split_len(280800, 12) == 1664
 
 
 def test_assignment_agreement(case):

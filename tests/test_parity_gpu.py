@@ -160,6 +160,12 @@ def test_reassign_is_the_argmin_against_stored_centroids(T, C):
         R = oracle.residual(Xd[h], g["pi"][h], g["centroids"][h, 0], T - 1)
         pi_o, _ = oracle.assign(R, g["centroids"][h, 0, T - 1])
         assert (g["pi"][h, T - 1] == pi_o).mean() >= 0.9999
+    # the same steps one call at a time (qvg_reassign_steps) give the same bytes
+    ckv.pi[:, T - 1].fill_(255)
+    for step in (qvg.QVG_STEP_PLANES, qvg.QVG_STEP_GEMM, qvg.QVG_STEP_REFINE):
+        api.reassign(Xc, ckv, 3, ws, 5, steps=step)
+    torch.cuda.synchronize()
+    assert np.array_equal(ckv.pi.cpu().numpy(), g["pi"])
 
 
 def test_cold_start_indices_match_oracle():

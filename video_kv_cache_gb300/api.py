@@ -126,16 +126,22 @@ def quantize(X: torch.Tensor, C: int, T: int, bits: int, group: int, iters: int,
 
 def reassign(X: torch.Tensor, ckv: CompressedKV, iters: int, workspace: torch.Tensor,
              seed: int = 0, *, token_offset: int = 0, table_index: int = 0,
-             status: torch.Tensor | None = None, tensor_id_base: int = 0, stream=None):
+             status: torch.Tensor | None = None, tensor_id_base: int = 0, stream=None,
+             steps: int | None = None):
     """Re-run the last stage's assignment against the stored centroids (see qvg_reassign);
-    the arguments must match the preceding quantize call."""
+    the arguments must match the preceding quantize call.  ``steps``: a mask of
+    QVG_STEP_PLANES / QVG_STEP_GEMM / QVG_STEP_REFINE (qvg_reassign_steps); all by default."""
     H, N, _ = X.shape
     prm = quant_params(H, N, ckv.C, ckv.T, ckv.bits, ckv.group, iters, X.dtype, seed,
                        tensor_id_base, X.stride(0), token_offset, ckv.capacity, table_index,
                        ckv.n_tables)
-    rc = _c.qvg_reassign(prm, X.data_ptr(), ckv.buffers(), workspace.data_ptr(),
-                         workspace.numel(), status.data_ptr() if status is not None else None,
-                         _stream_handle(stream))
+    st = status.data_ptr() if status is not None else None
+    if steps is None:
+        rc = _c.qvg_reassign(prm, X.data_ptr(), ckv.buffers(), workspace.data_ptr(),
+                             workspace.numel(), st, _stream_handle(stream))
+    else:
+        rc = _c.qvg_reassign_steps(prm, X.data_ptr(), ckv.buffers(), workspace.data_ptr(),
+                                   workspace.numel(), steps, st, _stream_handle(stream))
     if rc != _c.QVG_OK:
         raise _c.QVGError(rc, "qvg_reassign")
 

@@ -377,9 +377,11 @@ struct APlan {
 };
 // Keys per split: the N keys of a head in min(ceil(N / 256), 128) parts, each rounded up to a
 // multiple of the 32-key tile.  Every split s < S = ceil(N / split_len) holds a key.
-inline int64_t attn_split_len(int64_t N) {
-    const int64_t target = std::min<int64_t>(std::max<int64_t>((N + 255) / 256, 1), 128);
-    const int64_t len = (N + target - 1) / target;
+// Keys per split: about 2048 splits over all heads (a warp each, enough to cover the SMs
+// with several warps apiece), at least 64 keys and a multiple of the 32-key tile.
+inline int64_t attn_split_len(int64_t N, int64_t heads) {
+    const int64_t target = std::max<int64_t>(2048 / std::max<int64_t>(heads, 1), 1);
+    const int64_t len = std::max<int64_t>((N + target - 1) / target, 64);
     return (len + 31) / 32 * 32;
 }
 cudaError_t launch_attention(const APlan &p, cudaStream_t st);

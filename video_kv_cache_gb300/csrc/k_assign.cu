@@ -192,20 +192,6 @@ __device__ __forceinline__ void tc_ld64(uint32_t taddr, float v[64]) {
     for (int q = 0; q < 64; q++) v[q] = __uint_as_float(r[q]);
 }
 
-// 4-byte global-to-shared copy that completes asynchronously (waited on with
-// cp.async.wait_all by the issuing thread).
-__device__ __forceinline__ void cp_async4(uint32_t dst, const float *src) {
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ float ld_shared_f32(uint32_t a) {
-    float v;
-    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(a) : "memory");
-    return v;
-}
-__device__ __forceinline__ void st_shared_f32(uint32_t a, float v) {
-    asm volatile("st.shared.f32 [%0], %1;" ::"r"(a), "f"(v) : "memory");
-}
-
 // Largest of 32 scores, in two independent chains.
 __device__ __forceinline__ float chunk_max(const float *v) {
     float ma = fmaxf(v[0], v[1]), mb = fmaxf(v[2], v[3]);
@@ -288,7 +274,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     float *x_best = reinterpret_cast<float *>(
         (reinterpret_cast<uintptr_t>(tmem_slot + 4) + 15) & ~static_cast<uintptr_t>(15));  // [kEpiGroups][2][128]
     uint32_t *x_cand = reinterpret_cast<uint32_t *>(x_best + kEpiGroups * 2 * kTileM);  // [kEpiGroups][128][4]
-    float *x_norm = reinterpret_cast<float *>(x_cand + kEpiGroups * 4 * kTileM);  // [16 warps][2][64]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t total = (int64_t)p.H * tiles_per_tensor;
@@ -444,35 +429,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         int cur_h = -1;
         float cmax = 0.f, cmax2 = 0.f, dcmax = 0.f;
         unsigned n_ref_rows = 0;
-        // The row norms come from HBM while the tensor cores stream A at full rate, so each
-        // lane copies its row's pair into shared memory (cp.async) one tile ahead, off the
-        // path from the accumulator to the bits.  Two buffers a warp: [rn 32 | dn 32].
-        const uint32_t nb = smem_u32(x_norm) + (uint32_t)(e * 128 + lane) * 4u;
-        auto issue_norms = [&](int64_t tl, uint32_t b) {
-            const uint32_t dst = nb + b * 256u;
-            const int hh = (int)(tl / tiles_per_tensor);
-            const int64_t ii = (tl - (int64_t)hh * tiles_per_tensor) * kTileM + row;
-            if (tl < te && ii < p.N) {
-                cp_async4(dst, p.rnorm + (int64_t)hh * p.N + ii);
-                cp_async4(dst + 128u, p.dnorm + (int64_t)hh * p.N + ii);
-            } else {
-                st_shared_f32(dst, 0.f);
-                st_shared_f32(dst + 128u, 0.f);
-            }
-            asm volatile("cp.async.commit_group;" ::: "memory");
-        };
-        issue_norms(tb + grp, 0u);
-        uint32_t nbuf = 0u;
         for (int64_t tile = tb + grp, lt = grp; tile < te; tile += kEpiGroups, lt += kEpiGroups) {
             const int h = (int)(tile / tiles_per_tensor);
             const int64_t i = (tile - (int64_t)h * tiles_per_tensor) * kTileM + row;
             const bool valid = i < p.N;
             const uint32_t buf = (uint32_t)grp, use = (uint32_t)lt >> 1;
-            // this tile's pair (the only copies in flight), then the next tile's
-            asm volatile("cp.async.wait_all;" ::: "memory");
-            const float rn = ld_shared_f32(nb + nbuf * 256u), dn = ld_shared_f32(nb + nbuf * 256u + 128u);
-            nbuf ^= 1u;
-            issue_norms(tile + kEpiGroups, nbuf);
+            const float rn = valid ? __ldg(p.rnorm + (int64_t)h * p.N + i) : 0.f;
+            const float dn = valid ? __ldg(p.dnorm + (int64_t)h * p.N + i) : 0.f;
             if (h != cur_h) {
                 // the tensor's largest centroid norm and fp16 rounding error (each warp
                 // reduces them itself)
@@ -667,7 +630,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 // index.  Blocks of 256 threads; several blocks share each assignment CTA's region of the
 // queue.
 // --------------------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) k_refine(QPlan p, int t, int n_regions, int split) {
+template <int TP>  // t - 1 (0..3), or -1: any stage, with the earlier rows read one at a time
+__global__ void __launch_bounds__(256, 3) k_refine(QPlan p, int t, int n_regions, int split) {
     pdl_begin();
     const int lane = threadIdx.x & 31, hl = lane & 15;
     const unsigned hmask = lane < 16 ? 0x0000FFFFu : 0xFFFF0000u;  // this half-warp
@@ -683,12 +647,22 @@ __global__ void __launch_bounds__(256) k_refine(QPlan p, int t, int n_regions, i
         return v;
     };
     unsigned n_cands = 0;
+    // A request's reads are issued together, not one after another: its X row and earlier
+    // clusters, then every earlier stage's centroid row at once, then the candidates' rows
+    // two at a time.
     for (int r = gh; r < count; r += nh) {
-        const RefineReq rq = p.rq[first + r];
-        const int h = rq.h;
-        const int64_t i = rq.i;
+        const RefineReq *rqp = p.rq + first + r;
+        const int h = rqp->h;
+        const int64_t i = rqp->i;
         const float *ct = p.cent + h * p.cent_tstride + p.cent_off;
         const float *c0 = ct + (int64_t)(t - 1) * p.C * kD;
+        constexpr int NB = TP > 0 ? TP : 1;  // earlier stages batched
+        auto earlier = [&](int s2) {            // cluster of stage s2 + 1
+            return min((int)p.pi[(int64_t)(h * p.T + s2) * p.cap + p.tok_off + i], p.C - 1);
+        };
+        int js[NB];
+#pragma unroll
+        for (int s2 = 0; s2 < NB; s2++) js[s2] = TP > 0 ? earlier(s2) : 0;
         // X's channels 8*hl..8*hl+7
         float xs[8];
         load_x8(p.X, p.in_dtype, h * p.x_stride + i * kD + hl * 8, xs);
@@ -697,21 +671,36 @@ __global__ void __launch_bounds__(256) k_refine(QPlan p, int t, int n_regions, i
         float2 x[4];
 #pragma unroll
         for (int q = 0; q < 4; q++) x[q] = make_float2(xs[2 * q], xs[2 * q + 1]);
-        if (t > 1) {
+        auto row8 = [&](int s2, int j, float4 &a, float4 &b) {  // stage s2 + 1's row j
+            const float4 *cr = reinterpret_cast<const float4 *>(ct + ((int64_t)s2 * p.C + j) * kD) + 2 * hl;
+            a = __ldg(cr);
+            b = __ldg(cr + 1);
+        };
+        if (TP != 0) {
             float2 e[4];
 #pragma unroll
             for (int q = 0; q < 4; q++) e[q] = make_float2(0.f, 0.f);
-            for (int s2 = 1; s2 < t; s2++) {
-                const int js = min((int)p.pi[(int64_t)(h * p.T + s2 - 1) * p.cap + p.tok_off + i], p.C - 1);
-                const float4 *cr = reinterpret_cast<const float4 *>(ct + ((int64_t)(s2 - 1) * p.C + js) * kD) + 2 * hl;
-                const float4 ca = __ldg(cr), cb = __ldg(cr + 1);
-                const float2 c[4] = {make_float2(ca.x, ca.y), make_float2(ca.z, ca.w), make_float2(cb.x, cb.y),
-                                     make_float2(cb.z, cb.w)};
+            auto sub_row = [&](const float4 &a, const float4 &b) {
+                const float2 c[4] = {make_float2(a.x, a.y), make_float2(a.z, a.w), make_float2(b.x, b.y),
+                                     make_float2(b.z, b.w)};
 #pragma unroll
                 for (int q = 0; q < 4; q++) {
                     float2 err;
                     x[q] = two_diff2(x[q], c[q], err);
                     e[q] = __fadd2_rn(e[q], err);
+                }
+            };
+            if (TP > 0) {
+                float4 cra[NB], crb[NB];
+#pragma unroll
+                for (int s2 = 0; s2 < NB; s2++) row8(s2, js[s2], cra[s2], crb[s2]);
+#pragma unroll
+                for (int s2 = 0; s2 < NB; s2++) sub_row(cra[s2], crb[s2]);
+            } else {
+                for (int s2 = 0; s2 + 1 < t; s2++) {
+                    float4 a, b;
+                    row8(s2, earlier(s2), a, b);
+                    sub_row(a, b);
                 }
             }
 #pragma unroll
@@ -719,42 +708,53 @@ __global__ void __launch_bounds__(256) k_refine(QPlan p, int t, int n_regions, i
         }
         float bestD = INFINITY, secondD = INFINITY;
         int bestj = 0;
+        int cb = 0;
+        uint32_t m = rqp->cand[0];
+        for (;;) {
+            // up to two candidates, in increasing cluster order
+            constexpr int KB = 2;
+            int jj[KB], nb = 0;
 #pragma unroll
-        for (int cb = 0; cb < 8; cb++) {
-            uint32_t m = rq.cand[cb];
-            while (m) {
-                const int j = cb * 32 + __ffs(m) - 1;
-                m &= m - 1u;
-                n_cands++;
-                const float4 *cr = reinterpret_cast<const float4 *>(c0 + (int64_t)j * kD) + 2 * hl;
-                const float4 ca = __ldg(cr), cc = __ldg(cr + 1);
-                const float cv[8] = {ca.x, ca.y, ca.z, ca.w, cc.x, cc.y, cc.z, cc.w};
-                float D = 0.f;
-#pragma unroll
-                for (int q = 0; q < 8; q++) {
-                    const float d = __fsub_rn(q & 1 ? x[q >> 1].y : x[q >> 1].x, cv[q]);
-                    D = q == 0 ? __fmul_rn(d, d) : __fmaf_rn(d, d, D);
-                }
-                D = hsum(D);
-                if (D < bestD) {
-                    secondD = bestD;
-                    bestD = D;
-                    bestj = j;
-                } else {
-                    secondD = fminf(secondD, D);
+            for (int u = 0; u < KB; u++) {
+                while (m == 0u && cb < 7) m = rqp->cand[++cb];
+                jj[u] = -1;
+                if (m) {
+                    jj[u] = cb * 32 + __ffs(m) - 1;
+                    m &= m - 1u;
+                    nb++;
                 }
             }
+            if (nb == 0) break;
+            float4 ca[KB], cc[KB];
+#pragma unroll
+            for (int u = 0; u < KB; u++)
+                if (jj[u] >= 0) {
+                    const float4 *cr = reinterpret_cast<const float4 *>(c0 + (int64_t)jj[u] * kD) + 2 * hl;
+                    ca[u] = __ldg(cr);
+                    cc[u] = __ldg(cr + 1);
+                }
+#pragma unroll
+            for (int u = 0; u < KB; u++)
+                if (jj[u] >= 0) {
+                    n_cands++;
+                    const float cv[8] = {ca[u].x, ca[u].y, ca[u].z, ca[u].w, cc[u].x, cc[u].y, cc[u].z, cc[u].w};
+                    float D = 0.f;
+#pragma unroll
+                    for (int q = 0; q < 8; q++) {
+                        const float d = __fsub_rn(q & 1 ? x[q >> 1].y : x[q >> 1].x, cv[q]);
+                        D = q == 0 ? __fmul_rn(d, d) : __fmaf_rn(d, d, D);
+                    }
+                    D = hsum(D);
+                    if (D < bestD) {
+                        secondD = bestD;
+                        bestD = D;
+                        bestj = jj[u];
+                    } else {
+                        secondD = fminf(secondD, D);
+                    }
+                }
+            if (nb < KB) break;
         }
-        // Each fp32 distance is within about twelve fp32 roundings (2^-20.4, relative: a sum
-        // of non-negative terms) of the exact distance of the fp32 stage input, so a gap
-        // wider than 2^-18 of the larger distance orders them as those exact distances are.
-        // From the second stage on, the fp32 stage input is itself off the fp64 one by at
-        // most 2^-24 |x_k| per channel, which moves the difference of two distances by at
-        // most 2^-23 ||x|| (||x - c_1|| + ||x - c_2||) <= 2^-22 ||x|| sqrt(D_2); that is added
-        // to the margin (it dominates for a row far larger than its distances to the
-        // candidates).  Closer calls are settled in fp64 below.
-        // (bestD and secondD are the same in every lane of the half, so the branches are
-        // uniform over it.)
         bool close = secondD - bestD <= 0x1p-18f * secondD;
         if (!close && t > 1) {
             float xx = 0.f;
@@ -768,23 +768,22 @@ __global__ void __launch_bounds__(256) k_refine(QPlan p, int t, int n_regions, i
             // the stage input rebuilt in fp64: x - C^(1)[pi^(1)] - ... - C^(t-1)[pi^(t-1)],
             // subtracted in that order
             double xd[8];
+            load_x8(p.X, p.in_dtype, h * p.x_stride + i * kD + hl * 8, xs);
 #pragma unroll
             for (int k = 0; k < 8; k++) xd[k] = (double)xs[k];
-            for (int s2 = 1; s2 < t; s2++) {
-                const int js = min((int)p.pi[(int64_t)(h * p.T + s2 - 1) * p.cap + p.tok_off + i], p.C - 1);
-                const float4 *cr = reinterpret_cast<const float4 *>(ct + ((int64_t)(s2 - 1) * p.C + js) * kD) + 2 * hl;
-                const float4 ca = __ldg(cr), cb = __ldg(cr + 1);
-                const float cv[8] = {ca.x, ca.y, ca.z, ca.w, cb.x, cb.y, cb.z, cb.w};
+            for (int s2 = 0; s2 + 1 < t; s2++) {
+                float4 ca, cb2;
+                row8(s2, earlier(s2), ca, cb2);
+                const float cv[8] = {ca.x, ca.y, ca.z, ca.w, cb2.x, cb2.y, cb2.z, cb2.w};
 #pragma unroll
                 for (int k = 0; k < 8; k++) xd[k] -= (double)cv[k];
             }
             double bestDd = INFINITY;
-#pragma unroll
-            for (int cb = 0; cb < 8; cb++) {
-                uint32_t m = rq.cand[cb];
-                while (m) {
-                    const int j = cb * 32 + __ffs(m) - 1;
-                    m &= m - 1u;
+            for (int cw = 0; cw < 8; cw++) {
+                uint32_t mm = rqp->cand[cw];
+                while (mm) {
+                    const int j = cw * 32 + __ffs(mm) - 1;
+                    mm &= mm - 1u;
                     const float4 *cr = reinterpret_cast<const float4 *>(c0 + (int64_t)j * kD) + 2 * hl;
                     const float4 ca = __ldg(cr), cc = __ldg(cr + 1);
                     const float cv[8] = {ca.x, ca.y, ca.z, ca.w, cc.x, cc.y, cc.z, cc.w};
@@ -835,7 +834,7 @@ static EncodeTiledFn encode_fn() {
 // score and candidate words per row)
 static size_t assign_tail_bytes(int nslots) {
     return (size_t)(2 * nslots + 3 + 2 * kEpiGroups) * 8 + 16 + 16 /* alignment */ +
-           (size_t)kEpiGroups * (2 * kTileM + 4 * kTileM) * 4 + (size_t)kEpiGroups * 8 * 128 * 4;
+           (size_t)kEpiGroups * (2 * kTileM + 4 * kTileM) * 4;
 }
 
 // the fp16 centroid plane (two 64-channel blocks), the offset rows and the constant block
@@ -965,7 +964,14 @@ static int assign_grid(const QPlan &p, int num_sms) {
 cudaError_t launch_refine(const QPlan &p, int t, int num_sms, cudaStream_t st) {
     const int regions = assign_grid(p, num_sms);
     const int split = std::max(1, (num_sms * 8 + regions - 1) / regions);
-    return launch_kernel(k_refine, dim3(regions * split), dim3(256), 0, st, p, t, regions, split);
+    const dim3 grid(regions * split);
+    switch (t - 1) {
+        case 0: return launch_kernel(k_refine<0>, grid, dim3(256), 0, st, p, t, regions, split);
+        case 1: return launch_kernel(k_refine<1>, grid, dim3(256), 0, st, p, t, regions, split);
+        case 2: return launch_kernel(k_refine<2>, grid, dim3(256), 0, st, p, t, regions, split);
+        case 3: return launch_kernel(k_refine<3>, grid, dim3(256), 0, st, p, t, regions, split);
+        default: return launch_kernel(k_refine<-1>, grid, dim3(256), 0, st, p, t, regions, split);
+    }
 }
 
 }  // namespace qvg

@@ -8,22 +8,24 @@
 // pipeline paragraph).  Attention itself is the standard scaled dot-product softmax form:
 // o = sum_j p_j v_j, p = softmax_j(scale * q.k_j).
 //
-// Design (one query block per head, HBM reads of the compressed rows):
-//   * The N keys of a head are cut into S = min(ceil(N / 256), 128) splits of equal length
-//     rounded up to a multiple of 32 keys (at most 256 keys up to N = 32768, longer splits
-//     beyond).  One warp takes one split and walks it in 32-key tiles with a running
-//     maximum and weight sum per query (online softmax); k_attn_combine merges the splits
-//     of a head.
+// Design (one query block per head; the reads of the compressed rows are latency-bound, so
+// the kernel is built to keep many of them in flight):
+//   * The N keys of a head are cut into S splits of equal length, a multiple of 32 keys and
+//     at least 64, chosen so that all heads together have about 2048 splits.  One warp
+//     takes one split and walks it in 32-key tiles with a running maximum and weight sum per
+//     query (online softmax); k_attn_combine merges the splits of a head.
 //   * A rebuilt row is the value qvg_dequantize writes in fp32: the code's level times the
 //     E4M3 scale, plus the stage-T centroid, then stages T-1 .. 1, each add rounded in fp32.
-//     A lane rebuilds channels 4l .. 4l+3 of a row (one code byte at INT2, one 16-bit word
-//     at INT4, a float4 of each stage's table row).
-//   * Keys: the warp rebuilds the tile's 32 key rows into shared memory (rows padded to 132
-//     floats so that a quarter-warp's 16-byte reads of 8 different rows hit distinct bank
-//     groups); then lane j scores key j against every query (queries in shared memory,
-//     broadcast reads) with 128 sequential fp32 FMAs.
-//   * Values: lane l rebuilds channels 4l .. 4l+3 of each value row of the tile and adds
-//     them, weighted by the key's softmax numerator, into its M x 4 accumulators.
+//     A tile's 32 rows are rebuilt together in shared memory (rows padded to 132 floats):
+//     lane k reads key k's codes, scale bytes and cluster indices (one pass of coalesced
+//     reads for the whole tile) and writes its dequantized row; then for each stage the
+//     warp adds the keys' centroid rows (lane l: channels 4l .. 4l+3), with the rows of 8
+//     keys loaded before any is added.
+//   * Keys: lane j scores key j against every query (queries in shared memory, broadcast
+//     reads) with 128 sequential fp32 FMAs.
+//   * Values: the tile's value rows are rebuilt the same way into the same buffer; lane l
+//     adds channels 4l .. 4l+3 of each, weighted by the key's softmax numerator, into its
+//     M x 4 accumulators.
 #include <cuda_fp8.h>
 
 #include <algorithm>
@@ -42,47 +44,92 @@ __device__ __forceinline__ float e4m3_value(uint32_t b) {
     return __half2float(__half(h));
 }
 
-// Channels 4*lane .. 4*lane+3 of token n of compressed tensor ti, as qvg_dequantize's fp32
-// output has them.
-template <int BITS, int SH>
-__device__ __forceinline__ float4 rebuild4(const APlan &p, const uint8_t *codes,
-                                           const uint8_t *scales, const uint8_t *pi,
-                                           const float *cent, int64_t ti, int64_t n, int lane,
-                                           bool &bad) {
+// Rows [t0, t0 + cnt) of compressed tensor ti, rebuilt as qvg_dequantize's fp32 output has
+// them, into rows[k * kKRow + c] (k < cnt).  The reads are issued in bulk, not one key at a
+// time: lane k first reads key t0 + k's codes, scale bytes and cluster indices (coalesced
+// across the warp) and writes its dequantized row; then, stage by stage from T down to 1,
+// the warp adds each key's centroid row (lane l: channels 4l .. 4l+3), the rows of KB keys
+// loaded together before they are added.  Each element gets the same fp32 operations, in
+// the same order, as in qvg_dequantize.
+// (Kept out of line: inlined twice into the split kernel it pushed that kernel's register
+// count past what fits several warps per SM.)  Returns true if a stored index was out of
+// range.
+template <int BITS, int SH, int KB>
+__device__ __noinline__ bool rebuild_tile(const APlan &p, const uint8_t *codes,
+                                          const uint8_t *scales, const uint8_t *pi,
+                                          const float *cent, int64_t ti, int64_t t0, int cnt,
+                                          int lane, float *rows) {
+    bool bad = false;
     constexpr int MID = 1 << (BITS - 1);
-    const int64_t row = ti * p.cap + n;
-    uint32_t cw;
-    if constexpr (BITS == 2)
-        cw = __ldg(codes + row * (kD * BITS / 8) + lane);
-    else
-        cw = __ldg(reinterpret_cast<const unsigned short *>(codes + row * (kD * BITS / 8)) + lane);
-    const float sq = e4m3_value(__ldg(scales + row * (kD / p.group) + (4 * lane) / p.group));
-    float y[4];
+    constexpr int WORDS = kD * BITS / 32;  // code words of a row
+    const int ngroups = kD / p.group;
+    uint64_t pk = 0;
+    int tbl = 0;
+    if (lane < cnt) {
+        const int64_t row = ti * p.cap + t0 + lane;
+        const uint32_t *cwp = reinterpret_cast<const uint32_t *>(codes + row * (kD * BITS / 8));
+        for (int t = 0; t < p.T; t++) pk |= (uint64_t)__ldg(pi + (ti * p.T + t) * p.cap + t0 + lane) << (8 * t);
+        tbl = (int)min((t0 + lane) / p.chunk_len, (int64_t)p.n_tables - 1);
+        // the row's scale bytes (ngroups = 8, 4 or 2 of them, naturally aligned)
+        const uint8_t *sr = scales + row * ngroups;
+        const uint64_t sw = ngroups == 8   ? __ldg(reinterpret_cast<const unsigned long long *>(sr))
+                            : ngroups == 4 ? (uint64_t)__ldg(reinterpret_cast<const uint32_t *>(sr))
+                                           : (uint64_t)__ldg(reinterpret_cast<const unsigned short *>(sr));
+        const int gsh = 31 - __clz(p.group);  // log2 of the group size
+        float *dst = rows + lane * kKRow;
+        // one code word at a time: 32 / BITS channels (its first sector read brings the
+        // row's others into L1)
+#pragma unroll 1
+        for (int w = 0; w < WORDS; w++) {
+            const uint32_t word = __ldg(cwp + w);
 #pragma unroll
-    for (int c = 0; c < 4; c++) {
-        const int u = (int)((cw >> (BITS * c)) & ((1u << BITS) - 1u));
-        // the level times s_q: at most 8 significant bits, exact in fp32
-        const float lv = SH ? __fadd_rn((float)(u - MID), 0.5f) : (float)(u - MID);
-        y[c] = __fmul_rn(sq, lv);
-    }
-    if (p.T > 0) {
-        const int64_t tbl = min(n / p.chunk_len, (int64_t)p.n_tables - 1);
-        const float *tb = cent + (ti * p.n_tables + tbl) * p.T * p.C * kD;
-        for (int t = p.T - 1; t >= 0; t--) {
-            int j = __ldg(pi + (ti * p.T + t) * p.cap + n);
-            if (j >= p.C) {
-                j = p.C - 1;
-                bad = true;
+            for (int c4 = 0; c4 < 32 / BITS; c4 += 4) {
+                const int c = w * (32 / BITS) + c4;
+                const float sq = e4m3_value((uint32_t)(sw >> (8 * (c >> gsh))) & 0xFFu);
+                float y[4];
+#pragma unroll
+                for (int k = 0; k < 4; k++) {
+                    const int u = (int)((word >> (BITS * (c4 + k))) & ((1u << BITS) - 1u));
+                    const float lv = SH ? __fadd_rn((float)(u - MID), 0.5f) : (float)(u - MID);
+                    y[k] = __fmul_rn(sq, lv);
+                }
+                *reinterpret_cast<float4 *>(dst + c) = make_float4(y[0], y[1], y[2], y[3]);
             }
-            const float4 c4 =
-                __ldg(reinterpret_cast<const float4 *>(tb + ((int64_t)t * p.C + j) * kD) + lane);
-            y[0] = __fadd_rn(y[0], c4.x);
-            y[1] = __fadd_rn(y[1], c4.y);
-            y[2] = __fadd_rn(y[2], c4.z);
-            y[3] = __fadd_rn(y[3], c4.w);
         }
     }
-    return make_float4(y[0], y[1], y[2], y[3]);
+    __syncwarp();
+    for (int t = p.T - 1; t >= 0; t--) {
+        for (int k0 = 0; k0 < cnt; k0 += KB) {
+            float4 c4[KB];
+#pragma unroll
+            for (int u = 0; u < KB; u++) {
+                const int k = k0 + u;
+                const uint64_t pku = __shfl_sync(0xffffffffu, pk, k & 31);
+                const int tb = __shfl_sync(0xffffffffu, tbl, k & 31);
+                if (k < cnt) {
+                    int j = (int)((pku >> (8 * t)) & 0xFFu);
+                    if (j >= p.C) {
+                        j = p.C - 1;
+                        bad = true;
+                    }
+                    const float *tr = cent + ((ti * p.n_tables + tb) * p.T + t) * p.C * kD;
+                    c4[u] = __ldg(reinterpret_cast<const float4 *>(tr + (int64_t)j * kD) + lane);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < KB; u++) {
+                const int k = k0 + u;
+                if (k < cnt) {
+                    float4 *r = reinterpret_cast<float4 *>(rows + k * kKRow + 4 * lane);
+                    const float4 y = *r;
+                    *r = make_float4(__fadd_rn(y.x, c4[u].x), __fadd_rn(y.y, c4[u].y),
+                                     __fadd_rn(y.z, c4[u].z), __fadd_rn(y.w, c4[u].w));
+                }
+            }
+        }
+    }
+    __syncwarp();
+    return bad;
 }
 
 __device__ __forceinline__ float warp_max(float v) {
@@ -101,7 +148,8 @@ __device__ __forceinline__ float warp_sum(float v) {
 // grid (ceil(S / kAttnWarps), H), block 32 * kAttnWarps; warp w of CTA x takes split
 // x * kAttnWarps + w of head blockIdx.y.  MQ >= M queries are held (the rest are zero).
 template <int BITS, int SH, int MQ>
-__global__ void __launch_bounds__(32 * kAttnWarps) k_attn_split(APlan p) {
+__global__ void __launch_bounds__(32 * kAttnWarps, MQ > 4 ? 2 : 4) k_attn_split(APlan p) {
+    constexpr int KB = 8;  // centroid rows in flight per lane
     pdl_begin();
     extern __shared__ __align__(16) float sm_attn[];
     float *sQ = sm_attn;  // [MQ][d]
@@ -130,11 +178,7 @@ __global__ void __launch_bounds__(32 * kAttnWarps) k_attn_split(APlan p) {
     bool bad = false;
     for (int64_t t0 = n0; t0 < n1; t0 += kAttnTile) {
         const int cnt = (int)min((int64_t)kAttnTile, n1 - t0);
-        for (int kk = 0; kk < cnt; kk++) {
-            const float4 k4 = rebuild4<BITS, SH>(p, p.kc, p.ks, p.kp, p.kcent, tk, t0 + kk, lane, bad);
-            *reinterpret_cast<float4 *>(sK + kk * kKRow + 4 * lane) = k4;
-        }
-        __syncwarp();
+        bad |= rebuild_tile<BITS, SH, KB>(p, p.kc, p.ks, p.kp, p.kcent, tk, t0, cnt, lane, sK);
         float sc[MQ];
 #pragma unroll
         for (int m = 0; m < MQ; m++) sc[m] = 0.f;
@@ -164,9 +208,10 @@ __global__ void __launch_bounds__(32 * kAttnWarps) k_attn_split(APlan p) {
             for (int c = 0; c < 4; c++) o[m][c] = __fmul_rn(o[m][c], corr);
             sP[m * kAttnTile + lane] = pj;
         }
-        __syncwarp();
+        __syncwarp();  // every lane has scored its key: the value rows can overwrite sK
+        bad |= rebuild_tile<BITS, SH, KB>(p, p.vc, p.vs, p.vp, p.vcent, tv, t0, cnt, lane, sK);
         for (int kk = 0; kk < cnt; kk++) {
-            const float4 v4 = rebuild4<BITS, SH>(p, p.vc, p.vs, p.vp, p.vcent, tv, t0 + kk, lane, bad);
+            const float4 v4 = *reinterpret_cast<const float4 *>(sK + kk * kKRow + 4 * lane);
 #pragma unroll
             for (int m = 0; m < MQ; m++) {
                 const float w = sP[m * kAttnTile + kk];

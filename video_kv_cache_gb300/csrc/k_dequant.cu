@@ -6,28 +6,35 @@
 // "Quant VideoGen" notes page, sections Progressive Residual Quantization and
 // Algorithm-System Co-design, the fused dequantization kernel).
 //
-// Design (HBM-bound: the output write is most of the bytes):
-//   * One CTA of 1024 threads per SM, each taking an equal contiguous share of the
-//     flattened (tensor, centroid table, channel slice of W channels, token) space.  For
-//     each (tensor, table, slice) segment of its share the CTA stages that W-channel slice
-//     of all T tables (T x C x W fp32) in shared memory.  W is the widest of 128,
-//     64 and 32 whose slice fits in 200 KB (64 for T = 2, C = 256); beyond that the
-//     tables are read through L1 / L2.
-//   * A lane rebuilds 16 contiguous channels of a token: one 4- or 8-byte code load, one
-//     scale byte and T cluster-index bytes; the W / 16 lanes of a token write its W
-//     channels as one contiguous run.
+// Design (HBM-bound for one or two stages; beyond that bound by the shared-memory reads of
+// the tables, T fp32 values per output element):
+//   * The T tables of a tensor are staged in shared memory one channel slice of W channels
+//     at a time (T x C x W fp32; W is the widest of 128, 64 and 32 that fits 200 KB: 64
+//     for T = 2, 32 for T = 4 with C = 256).  The S = 128 / W slices of a token range are
+//     taken by S CTAs side by side: CTA b holds slice b % S and the (b / S)-th equal share
+//     of the flattened (tensor, token) space, so the S CTAs of a share walk the same
+//     tokens at about the same time, and the code, scale and index sectors they share come
+//     from DRAM once (the others hit L2).  A CTA restages only when its share moves to
+//     another tensor or centroid table.
+//   * A lane rebuilds 16 contiguous channels of a token (four 4-channel chunks): one 4- or
+//     8-byte code load, one scale byte (the 16 channels lie in one scale group) and T
+//     cluster-index bytes, loaded two tokens ahead of the one being computed.
+//   * Conflict-free table reads without a swizzle: the 8 lanes of a quarter-warp read 16
+//     bytes each from up to 8 different table rows; a row's chunk c sits in bank group
+//     c mod 8.  Lane (token q of the quarter, part u of the token) reads its four chunks in
+//     the order k -> 4u + ((k + rot) mod 4), rot = (q * LPT / 2 + u / 2) mod 4 (LPT lanes
+//     per token), so at every step the 8 lanes hit 8 different bank groups whatever rows
+//     they read.  The codes are rotated the same way (a funnel shift), the arithmetic runs
+//     in that order, and two rounds of selects put the results back in channel order before
+//     the store.
 //   * Arithmetic per element: the code u is masked in place into the mantissa of the float
 //     2^23 (one logic op), one subtraction gives (u - 2^(b-1)) * 2^k exactly, and
 //     y = fma(s_q * 2^-k, that, C^(T)) (s_q * q is exact, so this equals adding C^(T) to
 //     the dequantized value); then one add per further stage, T - 1 down to 1, in fp32,
 //     rounded once to the output type.  The subtraction, the fma and the adds run on f32x2
 //     pairs of neighbouring channels (each half rounds as the scalar operation does).
-//   * A staged table row's 16-byte chunks are stored XOR-swizzled, so a quarter-warp's
-//     16-byte reads hit distinct bank groups.
 //   * A lane writes its 16 outputs with one 32-byte store (two for fp32) when the output
 //     is 32-byte aligned, so every store instruction fills whole sectors.
-//   * The codes, scale and indices of the next two tokens are loaded before the current
-//     token is computed, to keep reads in flight.
 #include <cuda_fp8.h>
 
 #include <algorithm>
@@ -39,13 +46,6 @@ namespace qvg {
 namespace {
 constexpr int kDqThreads = 1024;
 constexpr size_t kDqTableBytes = 200 * 1024;  // largest table slice staged by one CTA
-constexpr int kLaneCh = 16;                   // channels a lane rebuilds per token
-
-// Physical 16-byte chunk of logical chunk c in staged table row r.  Bits 3-4 of c are
-// XOR-ed into its low bits, so the lanes of one token reading chunks 4l + k (l = 0..7)
-// hit distinct bank groups; bit 0 of the row flips bit 1, so two tokens of one
-// quarter-warp whose rows differ in parity also read disjoint groups.
-__device__ __forceinline__ int swz(int r, int c) { return c ^ ((c >> 3) & 3) ^ ((r & 1) << 1); }
 
 // 32-byte store (sm_100 and later), 32-byte aligned address.
 __device__ __forceinline__ void st_v8(void *ptr, const uint32_t (&w)[8]) {
@@ -58,64 +58,65 @@ __device__ __forceinline__ float e4m3_to_float(uint32_t b) {
     const __half_raw h = __nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)b, __NV_E4M3);
     return __half2float(__half(h));
 }
+
+__device__ __forceinline__ uint32_t sel(bool c, uint32_t a, uint32_t b) { return c ? a : b; }
 }  // namespace
 
 template <int BITS, int OUT, int TT, int SH>  // SH: 1 for the mid-rise grid, else 0
 __global__ void __launch_bounds__(kDqThreads, 1)
-    k_dequant(DPlan p, int W, int64_t n_chunks, int smem_tables, int wide_stores) {
+    k_dequant(DPlan p, int W, int S, int64_t n_chunks, int smem_tables, int wide_stores) {
     pdl_begin();
     extern __shared__ __align__(16) float smem_f[];
     constexpr int MID = 1 << (BITS - 1);
     constexpr int PER16 = 16 / BITS;  // codes in a 16-bit half-word
+    constexpr int OW = OUT == DT_F32 ? 4 : 2;  // output words per 4-channel chunk
     const int T = TT >= 0 ? TT : p.T;
     const int C = p.C;
-    float *tab = smem_f;  // [T][C][W], swizzled 16-byte chunks
+    float *tab = smem_f;  // [T][C][W]
     constexpr int sh = SH;  // code shift of the level trick
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int LPT = W / kLaneCh;  // lanes per token
-    const int TPW = 32 / LPT;     // tokens per warp and pass
-    const int sub = lane % LPT;
+    const int LPT = W / 16;        // lanes per token
+    const int TPW = 32 / LPT;      // tokens per warp and pass
+    const int sub = lane % LPT;    // part of the token's slice
+    const int tq = (lane & 7) / LPT;  // token within the quarter-warp
+    const int rot = (tq * (LPT >> 1) + (sub >> 1)) & 3;
     const int tpc = (kDqThreads / 32) * TPW;  // tokens per CTA pass
-    const int slices = kD / W;
     const int row_bytes = kD * BITS / 8;
     const int ngroups = kD / p.group;
-    const int wq = W >> 2;  // 16-byte chunks per staged row
+    const int s = blockIdx.x % S;
+    const int G = gridDim.x / S, g = blockIdx.x / S;
+    const int ch0 = s * W + sub * 16;  // the lane's first channel
+    // float offsets in a staged row of the chunk read at step k
+    int roff[4];
+#pragma unroll
+    for (int k = 0; k < 4; k++) roff[k] = sub * 16 + 4 * ((k + rot) & 3);
 
-    // The work is the flattened (tensor, table chunk, slice, token) space; each CTA takes an
-    // equal contiguous share and walks it one (tensor, chunk, slice) segment at a time,
-    // staging that segment's tables when they change.
-    const int64_t per_tensor = p.N * slices;
-    const int64_t wb = per_tensor * p.H * blockIdx.x / gridDim.x;
-    const int64_t we = per_tensor * p.H * (blockIdx.x + 1) / gridDim.x;
+    const int64_t total = (int64_t)p.H * p.N;
+    const int64_t wb = total * g / G, we = total * (g + 1) / G;
     int64_t staged = -1;
     bool bad_index = false;
 
     for (int64_t pos = wb; pos < we;) {
-        const int h = (int)(pos / per_tensor);
-        int64_t r = pos - (int64_t)h * per_tensor;
-        const int64_t c = min(r / (p.chunk_len * slices), n_chunks - 1);
-        r -= c * p.chunk_len * slices;
-        const int64_t len = min(p.chunk_len, p.N - c * p.chunk_len);  // tokens of this chunk
-        const int s = (int)(r / len);
-        const int64_t t0 = r - s * len;
-        const int64_t t1 = min(len, t0 + (we - pos));
-        pos += t1 - t0;
-        const int64_t hcs = ((int64_t)h * n_chunks + c) * slices + s;
+        const int h = (int)(pos / p.N);
+        const int64_t i0 = pos - (int64_t)h * p.N;
+        const int64_t c = min(i0 / p.chunk_len, n_chunks - 1);
+        // the chunk's tokens (the last chunk's run to N), within the share
+        const int64_t i1 = min(min(p.N, (c + 1) * p.chunk_len), i0 + (we - pos));
+        pos += i1 - i0;
+        const int64_t hc = (int64_t)h * n_chunks + c;
         const float *tbl = p.cent + ((int64_t)h * p.n_tables + c) * T * C * kD;
-        if (smem_tables && T > 0 && hcs != staged) {
+        if (smem_tables && T > 0 && hc != staged) {
             __syncthreads();
+            const int wq = W >> 2;
             const int nvec = T * C * wq;
             for (int x = tid; x < nvec; x += kDqThreads) {
                 const int rr = x / wq, cc = x - rr * wq;
-                reinterpret_cast<float4 *>(tab)[rr * wq + swz(rr, cc)] =
+                reinterpret_cast<float4 *>(tab)[x] =
                     __ldg(reinterpret_cast<const float4 *>(tbl + (int64_t)rr * kD + s * W) + cc);
             }
             __syncthreads();
-            staged = hcs;
+            staged = hc;
         }
-        const int64_t i0 = c * p.chunk_len + t0;
-        const int64_t i1 = c * p.chunk_len + t1;
-        const int ch0 = s * W + sub * kLaneCh;  // the lane's first channel
         int64_t i = i0 + warp * TPW + lane / LPT;
         // running pointers of token i; they advance by tpc tokens per pass
         const uint8_t *cp = p.codes + ((int64_t)h * p.cap + i) * row_bytes + ch0 * BITS / 8;
@@ -156,18 +157,16 @@ __global__ void __launch_bounds__(kDqThreads, 1)
             }
             return j;
         };
-        // stage-t centroid values of this lane's 16 channels, cluster j, into 4 float4
+        // stage-t centroid values of the lane's four chunks, cluster j, in read order
         auto table16 = [&](int t, int j, float4 (&a)[4]) {
             if (smem_tables) {
-                const int r = t * C + j;
-                const float4 *row = reinterpret_cast<const float4 *>(tab) + r * wq;
+                const float *row = tab + (t * C + j) * W;
 #pragma unroll
-                for (int k = 0; k < 4; k++) a[k] = row[swz(r, 4 * sub + k)];
+                for (int k = 0; k < 4; k++) a[k] = *reinterpret_cast<const float4 *>(row + roff[k]);
             } else {
-                const float4 *g =
-                    reinterpret_cast<const float4 *>(tbl + ((int64_t)t * C + j) * kD + ch0);
+                const float *row = tbl + ((int64_t)t * C + j) * kD + s * W;
 #pragma unroll
-                for (int k = 0; k < 4; k++) a[k] = __ldg(g + k);
+                for (int k = 0; k < 4; k++) a[k] = __ldg(reinterpret_cast<const float4 *>(row + roff[k]));
             }
         };
 
@@ -185,6 +184,16 @@ __global__ void __launch_bounds__(kDqThreads, 1)
             sp += sstep;
             pp += tpc;
             if (inext + tpc < i1) fetch(nxt2);
+            // the codes in read order: chunk (k + rot) mod 4 at position k
+            uint32_t cw[BITS / 2];
+            if constexpr (BITS == 2) {
+                cw[0] = __funnelshift_r(cur.code[0], cur.code[0], 8 * rot);
+            } else {
+                const uint32_t a0 = sel(rot & 2, cur.code[1], cur.code[0]);
+                const uint32_t a1 = sel(rot & 2, cur.code[0], cur.code[1]);
+                cw[0] = sel(rot & 1, __funnelshift_r(a0, a1, 16), a0);
+                cw[1] = sel(rot & 1, __funnelshift_r(a1, a0, 16), a1);
+            }
             // Code e of a 16-bit half-word sits at bits BITS*e; shifted left by sh (0, or 1
             // for the mid-rise grid) and kept inside the mantissa of 2^23, the float is
             // 2^23 + u * 2^(BITS*e + sh).  Subtracting 2^23 + (MID * 2^sh - sh) * 2^(BITS*e)
@@ -192,8 +201,6 @@ __global__ void __launch_bounds__(kDqThreads, 1)
             // sq * 2^-(BITS*e + sh) (exact: a power-of-two rescaling) turns it into the
             // level: sq * (u - MID), or sq * (u - MID + 1/2) for the mid-rise grid.
             const float sq = e4m3_to_float(cur.sbyte & 0xFFu);
-            // per position e of a code in its half-word: the scale sq * 2^-(BITS*e + sh) and the
-            // offset -(2^23 + (MID * 2^sh - sh) * 2^(BITS*e)), as pairs of neighbouring positions
             constexpr int NP = PER16 / 2;
             float2 se[NP], nk[NP];
 #pragma unroll
@@ -208,12 +215,11 @@ __global__ void __launch_bounds__(kDqThreads, 1)
                 se[e2] = make_float2(s2[0], s2[1]);
                 nk[e2] = make_float2(k2[0], k2[1]);
             }
-            // y[p] holds channels 2p and 2p + 1 of the lane's 16; the arithmetic runs on
-            // f32x2 pairs, each lane of a pair rounding as the scalar operation would
+            // y[2k], y[2k + 1]: the four channels of the chunk read at step k
             float2 y[8];
 #pragma unroll
             for (int hw = 0; hw < 16 / PER16; hw++) {
-                const uint32_t word = (cur.code[hw >> 1] >> (16 * (hw & 1))) << sh;
+                const uint32_t word = (cw[hw >> 1] >> (16 * (hw & 1))) << sh;
 #pragma unroll
                 for (int e = 0; e < PER16; e += 2) {
                     const uint32_t m0 = (word & (((1u << BITS) - 1u) << (BITS * e + sh))) | 0x4B000000u;
@@ -242,43 +248,52 @@ __global__ void __launch_bounds__(kDqThreads, 1)
                     }
                 }
             }
-            if constexpr (OUT == DT_F32) {
-                if (wide_stores) {
+            // output words of the chunk read at step k, then back in channel order: chunk c
+            // was read at step (c - rot) mod 4
+            uint32_t w[4][OW];
 #pragma unroll
-                    for (int k = 0; k < 2; k++) {
-                        uint32_t w[8];
-#pragma unroll
-                        for (int x = 0; x < 4; x++) {
-                            w[2 * x] = __float_as_uint(y[4 * k + x].x);
-                            w[2 * x + 1] = __float_as_uint(y[4 * k + x].y);
-                        }
-                        st_v8(op + 32 * k, w);
-                    }
+            for (int k = 0; k < 4; k++) {
+                if constexpr (OUT == DT_F32) {
+                    w[k][0] = __float_as_uint(y[2 * k].x);
+                    w[k][1] = __float_as_uint(y[2 * k].y);
+                    w[k][2] = __float_as_uint(y[2 * k + 1].x);
+                    w[k][3] = __float_as_uint(y[2 * k + 1].y);
+                } else if constexpr (OUT == DT_BF16) {
+                    const __nv_bfloat162 v0 = __floats2bfloat162_rn(y[2 * k].x, y[2 * k].y);
+                    const __nv_bfloat162 v1 = __floats2bfloat162_rn(y[2 * k + 1].x, y[2 * k + 1].y);
+                    w[k][0] = *reinterpret_cast<const uint32_t *>(&v0);
+                    w[k][1] = *reinterpret_cast<const uint32_t *>(&v1);
                 } else {
-                    float4 *dst = reinterpret_cast<float4 *>(op);
+                    const __half2 v0 = __floats2half2_rn(y[2 * k].x, y[2 * k].y);
+                    const __half2 v1 = __floats2half2_rn(y[2 * k + 1].x, y[2 * k + 1].y);
+                    w[k][0] = *reinterpret_cast<const uint32_t *>(&v0);
+                    w[k][1] = *reinterpret_cast<const uint32_t *>(&v1);
+                }
+            }
+            uint32_t o[4 * OW];
 #pragma unroll
-                    for (int k = 0; k < 4; k++)
-                        dst[k] = make_float4(y[2 * k].x, y[2 * k].y, y[2 * k + 1].x, y[2 * k + 1].y);
+            for (int q = 0; q < OW; q++) {
+                const bool r2 = rot & 2, r1 = rot & 1;
+                const uint32_t a0 = sel(r2, w[2][q], w[0][q]), a1 = sel(r2, w[3][q], w[1][q]);
+                const uint32_t a2 = sel(r2, w[0][q], w[2][q]), a3 = sel(r2, w[1][q], w[3][q]);
+                o[0 * OW + q] = sel(r1, a3, a0);
+                o[1 * OW + q] = sel(r1, a0, a1);
+                o[2 * OW + q] = sel(r1, a1, a2);
+                o[3 * OW + q] = sel(r1, a2, a3);
+            }
+            if (wide_stores) {
+#pragma unroll
+                for (int k = 0; k < OW / 2; k++) {
+                    uint32_t v8[8];
+#pragma unroll
+                    for (int x = 0; x < 8; x++) v8[x] = o[8 * k + x];
+                    st_v8(op + 32 * k, v8);
                 }
             } else {
-                uint32_t w[8];
+                uint4 *dst = reinterpret_cast<uint4 *>(op);
 #pragma unroll
-                for (int k = 0; k < 8; k++) {
-                    if constexpr (OUT == DT_BF16) {
-                        const __nv_bfloat162 v2 = __floats2bfloat162_rn(y[k].x, y[k].y);
-                        w[k] = *reinterpret_cast<const uint32_t *>(&v2);
-                    } else {
-                        const __half2 v2 = __floats2half2_rn(y[k].x, y[k].y);
-                        w[k] = *reinterpret_cast<const uint32_t *>(&v2);
-                    }
-                }
-                if (wide_stores) {
-                    st_v8(op, w);
-                } else {
-                    uint4 *dst = reinterpret_cast<uint4 *>(op);
-                    dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-                    dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-                }
+                for (int k = 0; k < OW; k++)
+                    dst[k] = make_uint4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
             }
             op += ostep;
             cur = nxt;
@@ -303,7 +318,10 @@ cudaError_t launch_dq(const DPlan &p, int num_sms, int W, size_t table_bytes, bo
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const int64_t n_chunks = (p.N + p.chunk_len - 1) / p.chunk_len;
-    return launch_kernel(kern, dim3(num_sms), dim3(kDqThreads), smem, st, p, W, n_chunks,
+    // S CTAs (one per slice) per share of the tokens; at least one share
+    const int S = kD / W;
+    const int grid = std::max(1, num_sms / S) * S;
+    return launch_kernel(kern, dim3(grid), dim3(kDqThreads), smem, st, p, W, S, n_chunks,
                          smem_tables ? 1 : 0, wide);
 }
 

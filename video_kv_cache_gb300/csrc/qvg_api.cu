@@ -360,12 +360,14 @@ qvg_status qvg_quantize_static(const qvg_quant_params *prm, const void *X, const
     return QVG_OK;
 }
 
-qvg_status qvg_reassign(const qvg_quant_params *prm, const void *X, const qvg_buffers *out,
-                        void *workspace, size_t workspace_bytes, uint32_t *dev_status,
-                        void *stream) {
+qvg_status qvg_reassign_steps(const qvg_quant_params *prm, const void *X, const qvg_buffers *out,
+                              void *workspace, size_t workspace_bytes, int32_t steps,
+                              uint32_t *dev_status, void *stream) {
     qvg_status rc = check_quant(prm);
     if (rc != QVG_OK) return rc;
     if (prm->T < 1) return QVG_ERR_INVALID_ARG;
+    if ((steps & ~(QVG_STEP_PLANES | QVG_STEP_GEMM | QVG_STEP_REFINE)) != 0)
+        return QVG_ERR_INVALID_ARG;
     if (!X || !out || !out->pi || !out->centroids) return QVG_ERR_INVALID_ARG;
     if (!aligned16(X) || !aligned16(out->centroids)) return QVG_ERR_INVALID_ARG;
     const WsLayout w = ws_layout(prm->n_tensors, prm->N, prm->C, prm->T);
@@ -381,9 +383,10 @@ qvg_status qvg_reassign(const qvg_quant_params *prm, const void *X, const qvg_bu
         (void)cudaGetLastError();
         return QVG_ERR_CUDA;
     }
-    cudaError_t e = launch_centroid_planes(p, p.T, st);
-    if (e == cudaSuccess) e = launch_assign(p, maps, p.T, num_sms, st);
-    if (e == cudaSuccess) e = launch_refine(p, p.T, num_sms, st);
+    cudaError_t e = cudaSuccess;
+    if (steps & QVG_STEP_PLANES) e = launch_centroid_planes(p, p.T, st);
+    if (e == cudaSuccess && (steps & QVG_STEP_GEMM)) e = launch_assign(p, maps, p.T, num_sms, st);
+    if (e == cudaSuccess && (steps & QVG_STEP_REFINE)) e = launch_refine(p, p.T, num_sms, st);
     assign_release(maps);
     if (e != cudaSuccess) {
         (void)cudaGetLastError();
@@ -392,7 +395,12 @@ qvg_status qvg_reassign(const qvg_quant_params *prm, const void *X, const qvg_bu
     return QVG_OK;
 }
 
-
+qvg_status qvg_reassign(const qvg_quant_params *prm, const void *X, const qvg_buffers *out,
+                        void *workspace, size_t workspace_bytes, uint32_t *dev_status,
+                        void *stream) {
+    return qvg_reassign_steps(prm, X, out, workspace, workspace_bytes,
+                              QVG_STEP_PLANES | QVG_STEP_GEMM | QVG_STEP_REFINE, dev_status, stream);
+}
 
 qvg_status qvg_selftest_assign_timeout(const qvg_quant_params *prm, const void *X,
                                        const qvg_buffers *out, void *workspace,
@@ -513,7 +521,7 @@ struct AttnWs {
 };
 
 AttnWs attn_layout(const qvg_attention_params *prm) {
-    const int64_t L = attn_split_len(prm->N);
+    const int64_t L = attn_split_len(prm->N, prm->n_heads);
     const int64_t S = (prm->N + L - 1) / L;
     const size_t rows = (size_t)prm->n_heads * S * prm->M;
     AttnWs w{};
@@ -565,7 +573,7 @@ qvg_status qvg_attention(const qvg_attention_params *prm, const void *Q,
     p.k_first = prm->k_first;
     p.v_first = prm->v_first;
     p.step = prm->tensor_step;
-    p.split_len = attn_split_len(prm->N);
+    p.split_len = attn_split_len(prm->N, prm->n_heads);
     p.S = (int)((prm->N + p.split_len - 1) / p.split_len);
     p.Q = Q;
     p.kc = k_cache->codes;

@@ -28,6 +28,7 @@ QVG_DEV_BAD_INDEX = 0x4
 
 QVG_F16, QVG_BF16, QVG_F32 = 0, 1, 2
 QVG_QSCHEME_SYMMETRIC, QVG_QSCHEME_MIDRISE = 0, 1
+QVG_STEP_PLANES, QVG_STEP_GEMM, QVG_STEP_REFINE = 1, 2, 4
 QVG_CENTROIDS_F32, QVG_CENTROIDS_F16, QVG_CENTROIDS_BF16 = 0, 1, 2
 
 
@@ -118,6 +119,10 @@ SIGNATURES = {
     "qvg_reassign": (ctypes.c_int, [ctypes.POINTER(qvg_quant_params), ctypes.c_void_p,
                                     ctypes.POINTER(qvg_buffers), ctypes.c_void_p,
                                     ctypes.c_size_t, ctypes.c_void_p, ctypes.c_void_p]),
+    "qvg_reassign_steps": (ctypes.c_int, [ctypes.POINTER(qvg_quant_params), ctypes.c_void_p,
+                                          ctypes.POINTER(qvg_buffers), ctypes.c_void_p,
+                                          ctypes.c_size_t, ctypes.c_int32, ctypes.c_void_p,
+                                          ctypes.c_void_p]),
     "qvg_selftest_assign_timeout": (ctypes.c_int, [ctypes.POINTER(qvg_quant_params),
                                                    ctypes.c_void_p, ctypes.POINTER(qvg_buffers),
                                                    ctypes.c_void_p, ctypes.c_size_t,
@@ -189,6 +194,13 @@ def qvg_reassign(params: qvg_quant_params, X: int, out: qvg_buffers, workspace: 
                  workspace_bytes: int, dev_status: int | None, stream: int | None) -> int:
     return int(load().qvg_reassign(_ref(params), X, _ref(out), workspace, workspace_bytes,
                                    dev_status, stream))
+
+
+def qvg_reassign_steps(params: qvg_quant_params, X: int, out: qvg_buffers, workspace: int,
+                       workspace_bytes: int, steps: int, dev_status: int | None,
+                       stream: int | None) -> int:
+    return int(load().qvg_reassign_steps(_ref(params), X, _ref(out), workspace, workspace_bytes,
+                                         steps, dev_status, stream))
 
 
 def qvg_selftest_assign_timeout(params: qvg_quant_params, X: int, out: qvg_buffers,
