@@ -183,8 +183,13 @@ def launches_per_step(w):
 
 # DRAM traffic of one k_assign launch on layer_1p3b_32760 (dram__bytes_read.sum +
 # dram__bytes_write.sum, ncu), valid while the kernel's sources hash to `sources_sha256`.
-ASSIGN_TRAFFIC = {"workload": "layer_1p3b_32760", "bytes": 217287424,
-                  "sources_sha256": "affc973d23933e4bf8c82320c0afdcf24c89e43950bcc7f40e68014a63c12dbf"}
+# DRAM bytes (read + write) of one k_assign launch from ncu: a stage-4 launch of the profile
+# case (the first 8 of the 64 tensors, `bench.py --profile --tensors 8`), 143 326 464 B,
+# scaled by 8 to all 64 tensors (the traffic grows with the tiles processed).
+ASSIGN_TRAFFIC = {"workload": "dit13b_65536", "bytes": 143326464 * 8,
+                  "source": "ncu dram__bytes_read.sum + dram__bytes_write.sum of one stage-4 "
+                            "launch on the first 8 tensors, times 8",
+                  "sources_sha256": "89e0ad7415a6ed6a22136a326f9afaab8a1782f87e742124affd78198ae1a4e8"}
 ASSIGN_SOURCES = ("video_kv_cache_gb300/csrc/k_assign.cu", "video_kv_cache_gb300/csrc/internal.cuh")
 
 
@@ -467,7 +472,9 @@ def run_ours(args, w):
             "config": _config(w, world, not args.no_graph),
             "roofline": {"kernel": "k_assign", "bound": "tensor", "achieved": a_tflops,
                          "peak": tf_burst, "unit": "TFLOP/s", "frac": a_tflops / tf_burst,
-                         "traffic": traffic, "peak_source": src + " bf16 burst",
+                         "traffic": traffic,
+                         "traffic_source": ASSIGN_TRAFFIC["source"] if traffic else None,
+                         "peak_source": src + " bf16 burst",
                          "flops_per_launch": a_flops, "ms_per_launch": g_ms,
                          "timed_as": "k_assign alone (qvg_reassign_steps, the GEMM step), "
                                      "L2 flushed before each launch",
