@@ -458,13 +458,18 @@ __device__ __forceinline__ SortKeys sort_keys(const QPlan &p, int h, int t, int6
     return k;
 }
 
-__global__ void __launch_bounds__(kSortBlock) k_sort_hist(QPlan p, int t, int delta) {
+// Block histograms.  A CTA holds kHistGroups sort blocks of kSortBlock tokens, one per
+// group of kSortBlock threads (fewer, larger CTAs: the per-block work is short).
+constexpr int kHistGroups = 4;
+__global__ void __launch_bounds__(kSortBlock * kHistGroups) k_sort_hist(QPlan p, int t, int delta) {
     pdl_begin();
-    __shared__ int hist[kMaxC], lhist[kMaxC];
-    const int h = blockIdx.y, b = blockIdx.x;
-    for (int j = threadIdx.x; j < p.C; j += kSortBlock) hist[j] = lhist[j] = 0;
+    __shared__ int hist_s[kHistGroups][kMaxC], lhist_s[kHistGroups][kMaxC];
+    const int h = blockIdx.y, g = threadIdx.x / kSortBlock, tl = threadIdx.x % kSortBlock;
+    const int b = blockIdx.x * kHistGroups + g;
+    int *hist = hist_s[g], *lhist = lhist_s[g];
+    for (int j = tl; j < p.C; j += kSortBlock) hist[j] = lhist[j] = 0;
     __syncthreads();
-    const int64_t i = (int64_t)b * kSortBlock + threadIdx.x;
+    const int64_t i = (int64_t)b * kSortBlock + tl;  // >= N for a group past the last block
     if (i < p.N && p.pi[(int64_t)(h * p.T + t - 1) * p.cap + p.tok_off + i] >= p.C)
         or_status(p.status, QVG_DEV_BAD_INDEX);
     const SortKeys k = sort_keys(p, h, t, i, delta);
@@ -474,8 +479,9 @@ __global__ void __launch_bounds__(kSortBlock) k_sort_hist(QPlan p, int t, int de
         atomicAdd(lhist + k.leave, 1);
     }
     __syncthreads();
+    if (b >= p.nsb) return;
     int *bh = p.blockoff + ((int64_t)h * p.nsb + b) * p.C;
-    for (int j = threadIdx.x; j < p.C; j += kSortBlock) {
+    for (int j = tl; j < p.C; j += kSortBlock) {
         const int v = hist[j];
         bh[j] = v;
         if (v) atomicAdd(p.counts + h * p.C + j, v);  // cluster totals (zero on entry)
@@ -530,15 +536,20 @@ __global__ void __launch_bounds__(256) k_sort_scan(QPlan p) {
 
 // Writes the block's items to their sorted positions (the leave items of a cluster before
 // its enter items, each in token order), and the round's assignment into pi_prev.
-__global__ void __launch_bounds__(kSortBlock) k_sort_scatter(QPlan p, int t, int delta) {
+// A CTA holds kScatterGroups sort blocks, one per group of kSortBlock threads.
+constexpr int kScatterGroups = 2;
+__global__ void __launch_bounds__(kSortBlock * kScatterGroups) k_sort_scatter(QPlan p, int t, int delta) {
     pdl_begin();
     constexpr int NW = kSortBlock / 32;
-    __shared__ int wl[NW][kMaxC], we[NW][kMaxC];  // leave / enter items of each cluster per warp
-    const int h = blockIdx.y, b = blockIdx.x;
-    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    for (int x = threadIdx.x; x < NW * kMaxC; x += kSortBlock) (&wl[0][0])[x] = (&we[0][0])[x] = 0;
+    // leave / enter items of each cluster per warp, per group
+    __shared__ int wl_s[kScatterGroups][NW][kMaxC], we_s[kScatterGroups][NW][kMaxC];
+    const int h = blockIdx.y, g = threadIdx.x / kSortBlock, tl = threadIdx.x % kSortBlock;
+    const int b = blockIdx.x * kScatterGroups + g;
+    int (*wl)[kMaxC] = wl_s[g], (*we)[kMaxC] = we_s[g];
+    const int lane = tl & 31, w = tl >> 5;
+    for (int x = tl; x < NW * kMaxC; x += kSortBlock) (&wl[0][0])[x] = (&we[0][0])[x] = 0;
     __syncthreads();
-    const int64_t i = (int64_t)b * kSortBlock + threadIdx.x;
+    const int64_t i = (int64_t)b * kSortBlock + tl;  // >= N for a group past the last block
     const SortKeys k = sort_keys(p, h, t, i, delta);
     const unsigned sl = __match_any_sync(0xffffffffu, k.leave);
     const unsigned se = __match_any_sync(0xffffffffu, k.enter);
@@ -1042,12 +1053,14 @@ __global__ void __launch_bounds__(256) k_cluster_finalize(QPlan p, int t, int pl
 
 cudaError_t launch_cluster_means(const QPlan &p, const AssignMaps *maps, int t, bool planes,
                                  bool delta, int num_sms, cudaStream_t st) {
-    const dim3 sgrid((unsigned)p.nsb, p.H);
     const int dl = delta ? 1 : 0;
-    cudaError_t e = launch_kernel(k_sort_hist, sgrid, dim3(kSortBlock), 0, st, p, t, dl);
+    cudaError_t e = launch_kernel(k_sort_hist, dim3((unsigned)((p.nsb + kHistGroups - 1) / kHistGroups), p.H),
+                                  dim3(kSortBlock * kHistGroups), 0, st, p, t, dl);
     if (e == cudaSuccess)
         e = launch_kernel(k_sort_scan, dim3((unsigned)((p.C + 31) / 32), p.H), dim3(256), 0, st, p);
-    if (e == cudaSuccess) e = launch_kernel(k_sort_scatter, sgrid, dim3(kSortBlock), 0, st, p, t, dl);
+    if (e == cudaSuccess)
+        e = launch_kernel(k_sort_scatter, dim3((unsigned)((p.nsb + kScatterGroups - 1) / kScatterGroups), p.H),
+                          dim3(kSortBlock * kScatterGroups), 0, st, p, t, dl);
     if (e != cudaSuccess) return e;
     auto sums = [&](auto src) {
         constexpr int S = decltype(src)::value;
