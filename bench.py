@@ -184,12 +184,12 @@ def launches_per_step(w):
 # DRAM traffic of one k_assign launch on layer_1p3b_32760 (dram__bytes_read.sum +
 # dram__bytes_write.sum, ncu), valid while the kernel's sources hash to `sources_sha256`.
 # DRAM bytes (read + write) of one k_assign launch from ncu: a stage-4 launch of the profile
-# case (the first 8 of the 64 tensors, `bench.py --profile --tensors 8`), 143 326 464 B,
+# case (the first 8 of the 64 tensors, `bench.py --profile --tensors 8`), 144 054 784 B,
 # scaled by 8 to all 64 tensors (the traffic grows with the tiles processed).
-ASSIGN_TRAFFIC = {"workload": "dit13b_65536", "bytes": 143326464 * 8,
+ASSIGN_TRAFFIC = {"workload": "dit13b_65536", "bytes": 144054784 * 8,
                   "source": "ncu dram__bytes_read.sum + dram__bytes_write.sum of one stage-4 "
                             "launch on the first 8 tensors, times 8",
-                  "sources_sha256": "89e0ad7415a6ed6a22136a326f9afaab8a1782f87e742124affd78198ae1a4e8"}
+                  "sources_sha256": "042b3c209356462d2c732a0338b68203a0ac14f7b8b375ff79c79d8e66f6ad52"}
 ASSIGN_SOURCES = ("video_kv_cache_gb300/csrc/k_assign.cu", "video_kv_cache_gb300/csrc/internal.cuh")
 
 

@@ -192,6 +192,23 @@ __device__ __forceinline__ void tc_ld64(uint32_t taddr, float v[64]) {
     for (int q = 0; q < 64; q++) v[q] = __uint_as_float(r[q]);
 }
 
+// (tensor, tile within the tensor) of a flat tile index, advanced by a fixed step without a
+// 64-bit division per tile (one division when the walk starts).
+struct TileWalk {
+    int h, ti, tpt;
+    __device__ TileWalk(int64_t tile, int tiles_per_tensor) : tpt(tiles_per_tensor) {
+        h = (int)(tile / tiles_per_tensor);
+        ti = (int)(tile - (int64_t)h * tiles_per_tensor);
+    }
+    __device__ void advance(int step) {  // step <= tiles_per_tensor is not required
+        ti += step;
+        while (ti >= tpt) {
+            ti -= tpt;
+            h++;
+        }
+    }
+};
+
 // Largest of 32 scores, in two independent chains.
 __device__ __forceinline__ float chunk_max(const float *v) {
     float ma = fmaxf(v[0], v[1]), mb = fmaxf(v[2], v[3]);
@@ -323,9 +340,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             int cur_h = -1;
             uint32_t nb = 0, issued = 0;
-            for (int64_t tile = tb, lt = 0; tile < te && !*abort_flag; tile++, lt++) {
-                const int h = (int)(tile / tiles_per_tensor);
-                const int m0 = (int)(tile - (int64_t)h * tiles_per_tensor) * kTileM;
+            TileWalk tw(tb, tiles_per_tensor);
+            for (int64_t tile = tb, lt = 0; tile < te && !*abort_flag; tile++, lt++, tw.advance(1)) {
+                const int h = tw.h;
+                const int m0 = tw.ti * kTileM;
                 if (h != cur_h) {
                     if (nb > 0 && !mbar_wait(smem_u32(b_empty), (nb - 1) & 1, abort_flag, wait_ns)) break;
                     // (withhold_b: the failure self-test; b_full then never completes)
@@ -369,8 +387,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t dB0 = sw128_desc(smem_u32(sB));
             const uint64_t dBx = sw128_desc(smem_u32(sBx));
             const uint64_t dAx = sw128_desc(smem_u32(sAx));
-            for (int64_t tile = tb, lt = 0; tile < te; tile++, lt++) {
-                const int h = (int)(tile / tiles_per_tensor);
+            TileWalk tw(tb, tiles_per_tensor);
+            for (int64_t tile = tb, lt = 0; tile < te; tile++, lt++, tw.advance(1)) {
+                const int h = tw.h;
                 if (h != cur_h) {
                     if (nb > 0) tc_commit(smem_u32(b_empty));
                     if (!mbar_wait(smem_u32(b_full), nb & 1, abort_flag, wait_ns)) break;
@@ -429,9 +448,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         int cur_h = -1;
         float cmax = 0.f, cmax2 = 0.f, dcmax = 0.f;
         unsigned n_ref_rows = 0;
-        for (int64_t tile = tb + grp, lt = grp; tile < te; tile += kEpiGroups, lt += kEpiGroups) {
-            const int h = (int)(tile / tiles_per_tensor);
-            const int64_t i = (tile - (int64_t)h * tiles_per_tensor) * kTileM + row;
+        TileWalk tw(tb + grp, tiles_per_tensor);
+        for (int64_t tile = tb + grp, lt = grp; tile < te;
+             tile += kEpiGroups, lt += kEpiGroups, tw.advance(kEpiGroups)) {
+            const int h = tw.h;
+            const int64_t i = (int64_t)tw.ti * kTileM + row;
             const bool valid = i < p.N;
             const uint32_t buf = (uint32_t)grp, use = (uint32_t)lt >> 1;
             const float rn = valid ? __ldg(p.rnorm + (int64_t)h * p.N + i) : 0.f;

@@ -38,6 +38,7 @@
 #include <cuda_fp8.h>
 
 #include <algorithm>
+#include <type_traits>
 
 #include "internal.cuh"
 
@@ -126,11 +127,16 @@ __global__ void __launch_bounds__(kDqThreads, 1)
                    ((int64_t)h * p.out_stride + i * kD + ch0) * (OUT == DT_F32 ? 4 : 2);
         const int64_t cstep = (int64_t)tpc * row_bytes, sstep = (int64_t)tpc * ngroups;
         const int64_t ostep = (int64_t)tpc * kD * (OUT == DT_F32 ? 4 : 2);
+        int64_t poff[TT > 0 ? TT : 1];  // offsets of the stages' index planes
+#pragma unroll
+        for (int t = 0; t < (TT > 0 ? TT : 1); t++) poff[t] = (int64_t)t * p.cap;
 
+        // cluster indices of up to four stages fit one word
+        using PK = typename std::conditional<(TT >= 0 && TT <= 4), uint32_t, uint64_t>::type;
         struct Meta {
             uint32_t code[BITS / 2];  // 16 codes, channel 0 in the low bits
             uint32_t sbyte;
-            uint64_t pk;              // pi^(1..T), one byte per stage
+            PK pk;                    // pi^(1..T), one byte per stage
         };
         auto fetch = [&](Meta &m) {
             if constexpr (BITS == 2) {
@@ -144,18 +150,17 @@ __global__ void __launch_bounds__(kDqThreads, 1)
             m.pk = 0;
             if (TT >= 0) {
 #pragma unroll
-                for (int t = 0; t < TT; t++) m.pk |= (uint64_t)__ldg(pp + (int64_t)t * p.cap) << (8 * t);
+                for (int t = 0; t < TT; t++) m.pk |= (PK)__ldg(pp + poff[t]) << (8 * t);
             } else {
                 for (int t = 0; t < T; t++) m.pk |= (uint64_t)__ldg(pp + (int64_t)t * p.cap) << (8 * t);
             }
         };
+        // a stored index >= C is reported and clamped (one compare per stage for the flag,
+        // one min for the clamp)
         auto stage_j = [&](const Meta &m, int t) {
-            int j = (int)((m.pk >> (8 * t)) & 0xFFu);
-            if (j >= C) {
-                j = C - 1;
-                bad_index = true;
-            }
-            return j;
+            const int j = (int)((m.pk >> (8 * t)) & 0xFFu);
+            bad_index |= j >= C;
+            return min(j, C - 1);
         };
         // stage-t centroid values of the lane's four chunks, cluster j, in read order
         auto table16 = [&](int t, int j, float4 (&a)[4]) {

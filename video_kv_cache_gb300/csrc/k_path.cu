@@ -697,7 +697,8 @@ __global__ void __launch_bounds__(256, TP == 0 ? 4 : (TP == 1 ? 3 : 2))
         while (c < total) {
             const int h = c / p.nchunk;
             if ((int64_t)(c - h * p.nchunk) * kChunk < (int64_t)p.items[h]) break;
-            c += nw;
+            // the rest of tensor h is empty too: on to this warp's first slot in tensor h + 1
+            c += ((h + 1) * p.nchunk - c + nw - 1) / nw * nw;
         }
         return c;
     };
