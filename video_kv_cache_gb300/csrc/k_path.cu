@@ -346,13 +346,137 @@ __global__ void __launch_bounds__(256) k_prep(QPlan p, int t) {
     }
 }
 
+// Later stages: one token per 16-thread group and pass, passes software-pipelined: a pass
+// issues its tokens' earlier centroid rows (their cluster indices are already in registers)
+// together with the next pass's X rows and cluster indices, then does its own arithmetic,
+// so that each pass waits on one round of loads instead of two in a row.
+constexpr int kPrepPipeTokens = 256;
+
+template <int NST>
+__global__ void __launch_bounds__(256) k_prep_pipe(QPlan p, int t) {
+    pdl_begin();
+    static_assert(NST > 0, "stage 1 has nothing to subtract");
+    const int h = blockIdx.y;
+    const int c8 = threadIdx.x & 15;
+    const int64_t i0 = (int64_t)blockIdx.x * kPrepPipeTokens;
+    const int64_t i1 = min(p.N, i0 + kPrepPipeTokens);
+    float2 mu[4];
+    {
+        float m8[8];
+        load_f8(p.mu + h * kD + c8 * 8, m8);
+#pragma unroll
+        for (int q = 0; q < 4; q++) mu[q] = make_float2(m8[2 * q], m8[2 * q + 1]);
+    }
+    const float *tab = p.cent + h * p.cent_tstride + p.cent_off + c8 * 8;
+    float2 probe = make_float2(0.f, 0.f);
+    bool bad_index = false;
+    struct Pass {
+        int64_t i;
+        bool valid;
+        float2 x[4];
+        int pj[NST];
+    };
+    auto load_pass = [&](int64_t ib, Pass &q) {
+        q.i = ib + (threadIdx.x >> 4);
+        q.valid = q.i < i1;
+        if (q.valid) {
+            load_x8_pairs(p, h * p.x_stride + q.i * kD + c8 * 8, q.x, probe);
+        } else {
+#pragma unroll
+            for (int k = 0; k < 4; k++) q.x[k] = make_float2(0.f, 0.f);
+        }
+#pragma unroll
+        for (int st = 0; st < NST; st++) {
+            int j = 0;
+            if (q.valid) {
+                j = p.pi[(int64_t)(h * p.T + st) * p.cap + p.tok_off + q.i];
+                bad_index |= j >= p.C;
+                j = min(j, p.C - 1);
+            }
+            q.pj[st] = j;
+        }
+    };
+    Pass cur;
+    load_pass(i0, cur);
+#pragma unroll 1
+    for (int64_t ib = i0; ib < i1; ib += 16) {
+        // this pass's earlier centroid rows, then the next pass's inputs
+        float4 ca[NST], cb[NST];
+#pragma unroll
+        for (int st = 0; st < NST; st++) {
+            const float4 *r = reinterpret_cast<const float4 *>(tab + ((int64_t)st * p.C + cur.pj[st]) * kD);
+            ca[st] = __ldg(r);
+            cb[st] = __ldg(r + 1);
+        }
+        const bool more = ib + 16 < i1;  // uniform over the block
+        Pass nxt;
+        if (more) load_pass(ib + 16, nxt);
+        // r = x - C^(1)[pi^(1)] - ... by the TwoSum chain, one final rounding
+        float2 v[4], e[4];
+#pragma unroll
+        for (int k = 0; k < 4; k++) {
+            v[k] = cur.x[k];
+            e[k] = make_float2(0.f, 0.f);
+        }
+#pragma unroll
+        for (int st = 0; st < NST; st++) {
+            const float2 c[4] = {make_float2(ca[st].x, ca[st].y), make_float2(ca[st].z, ca[st].w),
+                                 make_float2(cb[st].x, cb[st].y), make_float2(cb[st].z, cb[st].w)};
+#pragma unroll
+            for (int k = 0; k < 4; k++) {
+                float2 tt;
+                v[k] = two_diff2(v[k], c[k], tt);
+                e[k] = __fadd2_rn(e[k], tt);
+            }
+        }
+        // a = r - mu, its fp16 copy and the fp16 rounding error (exact), on pairs
+        float2 ss = make_float2(0.f, 0.f), dd = ss;
+        __align__(16) __half2 a16[4];
+#pragma unroll
+        for (int k = 0; k < 4; k++) {
+            const float2 x = sub2(__fadd2_rn(v[k], e[k]), mu[k]);
+            a16[k] = __float22half2_rn(x);
+            const float2 dx = sub2(x, __half22float2(a16[k]));
+            ss = __ffma2_rn(x, x, ss);
+            dd = __ffma2_rn(dx, dx, dd);
+        }
+        if (cur.valid)
+            *reinterpret_cast<uint4 *>(p.A + ((int64_t)h * p.N + cur.i) * kD + c8 * 8) =
+                *reinterpret_cast<uint4 *>(a16);
+        float sss = __fadd_rn(ss.x, ss.y), ddd = __fadd_rn(dd.x, dd.y);
+#pragma unroll
+        for (int o = 8; o >= 1; o >>= 1) {
+            sss += __shfl_xor_sync(0xffffffffu, sss, o);
+            ddd += __shfl_xor_sync(0xffffffffu, ddd, o);
+        }
+        if (cur.valid && c8 == 0) {
+            p.rnorm[h * p.N + cur.i] = sqrtf(sss);
+            p.dnorm[h * p.N + cur.i] = sqrtf(ddd);
+        }
+        if (more) cur = nxt;
+    }
+    const bool finite = probe.x == probe.x && probe.y == probe.y;
+    // one status update per block
+    __shared__ int bad, bad_idx;
+    if (threadIdx.x == 0) bad = 0, bad_idx = 0;
+    __syncthreads();
+    if (!finite) bad = 1;
+    if (bad_index) bad_idx = 1;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        if (bad) or_status(p.status, QVG_DEV_NONFINITE);
+        if (bad_idx) or_status(p.status, QVG_DEV_BAD_INDEX);
+    }
+}
+
 cudaError_t launch_prep(const QPlan &p, int t, cudaStream_t st) {
-    dim3 grid((unsigned)((p.N + kPrepTokens - 1) / kPrepTokens), p.H);
+    const dim3 grid((unsigned)((p.N + kPrepTokens - 1) / kPrepTokens), p.H);
+    const dim3 pgrid((unsigned)((p.N + kPrepPipeTokens - 1) / kPrepPipeTokens), p.H);
     switch (t - 1) {
         case 0: return launch_kernel(k_prep<4, 0>, grid, dim3(256), 0, st, p, t);
-        case 1: return launch_kernel(k_prep<2, 1>, grid, dim3(256), 0, st, p, t);
-        case 2: return launch_kernel(k_prep<2, 2>, grid, dim3(256), 0, st, p, t);
-        case 3: return launch_kernel(k_prep<2, 3>, grid, dim3(256), 0, st, p, t);
+        case 1: return launch_kernel(k_prep_pipe<1>, pgrid, dim3(256), 0, st, p, t);
+        case 2: return launch_kernel(k_prep_pipe<2>, pgrid, dim3(256), 0, st, p, t);
+        case 3: return launch_kernel(k_prep_pipe<3>, pgrid, dim3(256), 0, st, p, t);
         default: return launch_kernel(k_prep<1, -1>, grid, dim3(256), 0, st, p, t);
     }
 }
@@ -482,56 +606,62 @@ __global__ void __launch_bounds__(kSortBlock * kHistGroups) k_sort_hist(QPlan p,
     if (b >= p.nsb) return;
     int *bh = p.blockoff + ((int64_t)h * p.nsb + b) * p.C;
     for (int j = tl; j < p.C; j += kSortBlock) {
-        const int v = hist[j];
-        bh[j] = v;
-        if (v) atomicAdd(p.counts + h * p.C + j, v);  // cluster totals (zero on entry)
+        bh[j] = hist[j];  // the cluster totals are the scan's column sums
         if (lhist[j]) atomicAdd(p.dleave + h * p.C + j, lhist[j]);
     }
 }
 
-// Offsets of the counting sort.  grid (C/32 cluster groups, H), block 256: lane = cluster
-// of the group, warp w = a slice of the token blocks.  offs[j] = sum of the totals of the
-// clusters before j; blockoff[b][j] (in place, over the block histogram) = offs[j] + the
-// items of cluster j in the blocks before b; items = the tensor's total.
-__global__ void __launch_bounds__(256) k_sort_scan(QPlan p) {
+// Offsets of the counting sort.  One CTA of 1024 threads per tensor: thread (w, j) takes
+// cluster j and the w-th quarter of the token blocks.  The cluster totals are the column
+// sums of the block histograms; offs[j] = the sum of the totals of the clusters before j;
+// blockoff[b][j] (in place, over the block histogram) = offs[j] + the items of cluster j
+// in the blocks before b; counts[j] = the total; items = the tensor's total.
+constexpr int kScanSlices = 4;
+__global__ void __launch_bounds__(kMaxC * kScanSlices) k_sort_scan(QPlan p) {
     pdl_begin();
-    constexpr int NW = 8;
-    __shared__ int tot[kMaxC];
-    __shared__ int wsum[NW][32];
-    const int h = blockIdx.y, lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    const int j = blockIdx.x * 32 + lane;
-    // inclusive scan of the cluster totals of this tensor
-    const int x = threadIdx.x;
-    tot[x] = x < p.C ? p.counts[h * p.C + x] : 0;
-    __syncthreads();
-    for (int o = 1; o < kMaxC; o <<= 1) {
-        const int a1 = x >= o ? tot[x - o] : 0;
-        __syncthreads();
-        tot[x] += a1;
-        __syncthreads();
-    }
-    if (blockIdx.x == 0 && x == 0) p.items[h] = tot[kMaxC - 1];
+    __shared__ int part[kScanSlices][kMaxC];  // column sums of each quarter
+    __shared__ int excl[kMaxC];               // exclusive scan of the cluster totals
+    const int h = blockIdx.x, j = threadIdx.x % kMaxC, w = threadIdx.x / kMaxC;
     int *bh = p.blockoff + (int64_t)h * p.nsb * p.C;
-    const int per = (p.nsb + NW - 1) / NW;
+    const int per = (p.nsb + kScanSlices - 1) / kScanSlices;
     const int b0 = w * per, b1 = min(p.nsb, b0 + per);
     int local = 0;
     if (j < p.C) {
 #pragma unroll 8
         for (int b = b0; b < b1; b++) local += bh[(int64_t)b * p.C + j];
     }
-    wsum[w][lane] = local;
+    part[w][j] = local;
     __syncthreads();
+    if (w == 0) {
+        int tot = 0;
+#pragma unroll
+        for (int w2 = 0; w2 < kScanSlices; w2++) tot += part[w2][j];
+        excl[j] = tot;  // inclusive scan below, then shifted
+    }
+    __syncthreads();
+    for (int o = 1; o < kMaxC; o <<= 1) {
+        int a1 = 0;
+        if (w == 0 && j >= o) a1 = excl[j - o];
+        __syncthreads();
+        if (w == 0) excl[j] += a1;
+        __syncthreads();
+    }
     if (j < p.C) {
-        const int off = tot[j] - (j < p.C ? p.counts[h * p.C + j] : 0);
-        if (w == 0) p.offs[h * p.C + j] = off;
+        const int total = (w == 0) ? excl[j] - (j > 0 ? excl[j - 1] : 0) : 0;
+        const int off = j > 0 ? excl[j - 1] : 0;
+        if (w == 0) {
+            p.offs[h * p.C + j] = off;
+            p.counts[h * p.C + j] = total;
+        }
         int run = off;
-        for (int w2 = 0; w2 < w; w2++) run += wsum[w2][lane];
+        for (int w2 = 0; w2 < w; w2++) run += part[w2][j];
         for (int b = b0; b < b1; b++) {
             const int v = bh[(int64_t)b * p.C + j];
             bh[(int64_t)b * p.C + j] = run;
             run += v;
         }
     }
+    if (threadIdx.x == 0) p.items[h] = excl[kMaxC - 1];
 }
 
 // Writes the block's items to their sorted positions (the leave items of a cluster before
@@ -541,13 +671,15 @@ constexpr int kScatterGroups = 2;
 __global__ void __launch_bounds__(kSortBlock * kScatterGroups) k_sort_scatter(QPlan p, int t, int delta) {
     pdl_begin();
     constexpr int NW = kSortBlock / 32;
-    // leave / enter items of each cluster per warp, per group
-    __shared__ int wl_s[kScatterGroups][NW][kMaxC], we_s[kScatterGroups][NW][kMaxC];
+    // leave / enter items of each cluster per warp, per group (at most 32: one byte each)
+    __shared__ __align__(16) uint8_t wl_s[kScatterGroups][NW][kMaxC], we_s[kScatterGroups][NW][kMaxC];
     const int h = blockIdx.y, g = threadIdx.x / kSortBlock, tl = threadIdx.x % kSortBlock;
     const int b = blockIdx.x * kScatterGroups + g;
-    int (*wl)[kMaxC] = wl_s[g], (*we)[kMaxC] = we_s[g];
+    uint8_t (*wl)[kMaxC] = wl_s[g], (*we)[kMaxC] = we_s[g];
     const int lane = tl & 31, w = tl >> 5;
-    for (int x = tl; x < NW * kMaxC; x += kSortBlock) (&wl[0][0])[x] = (&we[0][0])[x] = 0;
+    static_assert(2 * NW * kMaxC == kSortBlock * 16, "one 16-byte store per thread");
+    constexpr int kVec = NW * kMaxC / 16;  // 16-byte pieces of one array
+    reinterpret_cast<uint4 *>(tl < kVec ? &wl[0][0] : &we[0][0])[tl % kVec] = make_uint4(0u, 0u, 0u, 0u);
     __syncthreads();
     const int64_t i = (int64_t)b * kSortBlock + tl;  // >= N for a group past the last block
     const SortKeys k = sort_keys(p, h, t, i, delta);
@@ -555,8 +687,8 @@ __global__ void __launch_bounds__(kSortBlock * kScatterGroups) k_sort_scatter(QP
     const unsigned se = __match_any_sync(0xffffffffu, k.enter);
     const unsigned below = (1u << lane) - 1u;
     const int rl = __popc(sl & below), re = __popc(se & below);  // earlier lanes, same key
-    if (k.leave >= 0 && rl == 0) wl[w][k.leave] = __popc(sl);
-    if (k.enter >= 0 && re == 0) we[w][k.enter] = __popc(se);
+    if (k.leave >= 0 && rl == 0) wl[w][k.leave] = (uint8_t)__popc(sl);
+    if (k.enter >= 0 && re == 0) we[w][k.enter] = (uint8_t)__popc(se);
     __syncthreads();
     const int *bo = p.blockoff + ((int64_t)h * p.nsb + b) * p.C;
     int *ids = p.ids + (int64_t)h * p.icap;
@@ -1058,7 +1190,7 @@ cudaError_t launch_cluster_means(const QPlan &p, const AssignMaps *maps, int t, 
     cudaError_t e = launch_kernel(k_sort_hist, dim3((unsigned)((p.nsb + kHistGroups - 1) / kHistGroups), p.H),
                                   dim3(kSortBlock * kHistGroups), 0, st, p, t, dl);
     if (e == cudaSuccess)
-        e = launch_kernel(k_sort_scan, dim3((unsigned)((p.C + 31) / 32), p.H), dim3(256), 0, st, p);
+        e = launch_kernel(k_sort_scan, dim3((unsigned)p.H), dim3(kMaxC * kScanSlices), 0, st, p);
     if (e == cudaSuccess)
         e = launch_kernel(k_sort_scatter, dim3((unsigned)((p.nsb + kScatterGroups - 1) / kScatterGroups), p.H),
                           dim3(kSortBlock * kScatterGroups), 0, st, p, t, dl);
