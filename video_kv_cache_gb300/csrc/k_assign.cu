@@ -668,13 +668,25 @@ __global__ void __launch_bounds__(256, 3) k_refine(QPlan p, int t, int n_regions
         return v;
     };
     unsigned n_cands = 0;
-    // A request's reads are issued together, not one after another: its X row and earlier
-    // clusters, then every earlier stage's centroid row at once, then the candidates' rows
-    // two at a time.
+    // A request's reads are issued together, not one after another: the next request is
+    // read while this one is scored; this one's X row, earlier clusters and first two
+    // candidates' rows go out together, then every earlier stage's centroid row at once,
+    // then any further candidates two at a time.
+    int cur_h = 0, cur_i = 0;
+    if (gh < count) {
+        cur_h = p.rq[first + gh].h;
+        cur_i = p.rq[first + gh].i;
+    }
     for (int r = gh; r < count; r += nh) {
-        const RefineReq *rqp = p.rq + first + r;
-        const int h = rqp->h;
-        const int64_t i = rqp->i;
+        const RefineReq *rqp = p.rq + first + r;  // its candidate words are in L1 by now
+        const bool has_next = r + nh < count;
+        int nxt_h = 0, nxt_i = 0;
+        if (has_next) {
+            nxt_h = rqp[nh].h;
+            nxt_i = rqp[nh].i;
+        }
+        const int h = cur_h;
+        const int64_t i = cur_i;
         const float *ct = p.cent + h * p.cent_tstride + p.cent_off;
         const float *c0 = ct + (int64_t)(t - 1) * p.C * kD;
         constexpr int NB = TP > 0 ? TP : 1;  // earlier stages batched
@@ -687,6 +699,33 @@ __global__ void __launch_bounds__(256, 3) k_refine(QPlan p, int t, int n_regions
         // X's channels 8*hl..8*hl+7
         float xs[8];
         load_x8(p.X, p.in_dtype, h * p.x_stride + i * kD + hl * 8, xs);
+        // candidates in increasing cluster order, two at a time; the first two rows now
+        constexpr int KB = 2;
+        int cb = 0;
+        uint32_t m = rqp->cand[0];
+        int jj[KB], nb = 0;
+        float4 ca[KB], cc[KB];
+        auto next_batch = [&]() {
+            nb = 0;
+#pragma unroll
+            for (int u = 0; u < KB; u++) {
+                while (m == 0u && cb < 7) m = rqp->cand[++cb];
+                jj[u] = -1;
+                if (m) {
+                    jj[u] = cb * 32 + __ffs(m) - 1;
+                    m &= m - 1u;
+                    nb++;
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < KB; u++)
+                if (jj[u] >= 0) {
+                    const float4 *cr = reinterpret_cast<const float4 *>(c0 + (int64_t)jj[u] * kD) + 2 * hl;
+                    ca[u] = __ldg(cr);
+                    cc[u] = __ldg(cr + 1);
+                }
+        };
+        next_batch();
         // fp32 pass on the fp32 stage input: X itself at stage 1, later the residual formed
         // by the same TwoSum chain (one final rounding) as the GEMM operand's preparation
         float2 x[4];
@@ -729,31 +768,8 @@ __global__ void __launch_bounds__(256, 3) k_refine(QPlan p, int t, int n_regions
         }
         float bestD = INFINITY, secondD = INFINITY;
         int bestj = 0;
-        int cb = 0;
-        uint32_t m = rqp->cand[0];
         for (;;) {
-            // up to two candidates, in increasing cluster order
-            constexpr int KB = 2;
-            int jj[KB], nb = 0;
-#pragma unroll
-            for (int u = 0; u < KB; u++) {
-                while (m == 0u && cb < 7) m = rqp->cand[++cb];
-                jj[u] = -1;
-                if (m) {
-                    jj[u] = cb * 32 + __ffs(m) - 1;
-                    m &= m - 1u;
-                    nb++;
-                }
-            }
             if (nb == 0) break;
-            float4 ca[KB], cc[KB];
-#pragma unroll
-            for (int u = 0; u < KB; u++)
-                if (jj[u] >= 0) {
-                    const float4 *cr = reinterpret_cast<const float4 *>(c0 + (int64_t)jj[u] * kD) + 2 * hl;
-                    ca[u] = __ldg(cr);
-                    cc[u] = __ldg(cr + 1);
-                }
 #pragma unroll
             for (int u = 0; u < KB; u++)
                 if (jj[u] >= 0) {
@@ -775,6 +791,7 @@ __global__ void __launch_bounds__(256, 3) k_refine(QPlan p, int t, int n_regions
                     }
                 }
             if (nb < KB) break;
+            next_batch();
         }
         bool close = secondD - bestD <= 0x1p-18f * secondD;
         if (!close && t > 1) {
@@ -824,6 +841,8 @@ __global__ void __launch_bounds__(256, 3) k_refine(QPlan p, int t, int n_regions
             }
         }
         if (hl == 0) p.pi[(int64_t)(h * p.T + t - 1) * p.cap + p.tok_off + i] = (uint8_t)bestj;
+        cur_h = nxt_h;
+        cur_i = nxt_i;
     }
     if (p.stats && hl == 0 && n_cands) atomicAdd(p.stats + kStatRefineCands, n_cands);
 }

@@ -563,18 +563,24 @@ __device__ __forceinline__ void acc_two_sum(float &s, float &e, float x) {
 struct SortKeys {
     int leave, enter;  // cluster keys of the token's items (-1: none)
     bool changed;
+    bool bad;          // the stored index is out of range
 };
 __device__ __forceinline__ SortKeys sort_keys(const QPlan &p, int h, int t, int64_t i, int delta) {
-    SortKeys k{-1, -1, false};
+    SortKeys k{-1, -1, false, false};
     if (i >= p.N) return k;
     const int j = p.pi[(int64_t)(h * p.T + t - 1) * p.cap + p.tok_off + i];
-    if (j >= p.C) return k;  // reported by the histogram; the token takes no part
+    if (j >= p.C) {  // reported by the histogram; the token takes no part
+        k.bad = true;
+        return k;
+    }
     if (!delta) {
         k.enter = j;
         return k;
     }
     const int jo = p.pi_prev[(int64_t)h * p.N + i];
-    if (jo != j) {
+    // (an earlier round's index is < C unless that round had an out-of-range index, which
+    // is reported; keys stay < C so that no position leaves its tensor's items)
+    if (jo != j && jo < p.C) {
         k.leave = jo;
         k.enter = j;
         k.changed = true;
@@ -582,86 +588,94 @@ __device__ __forceinline__ SortKeys sort_keys(const QPlan &p, int h, int t, int6
     return k;
 }
 
-// Block histograms.  A CTA holds kHistGroups sort blocks of kSortBlock tokens, one per
-// group of kSortBlock threads (fewer, larger CTAs: the per-block work is short).
-constexpr int kHistGroups = 4;
-__global__ void __launch_bounds__(kSortBlock * kHistGroups) k_sort_hist(QPlan p, int t, int delta) {
+// Sort blocks per CTA of the histogram: each thread reads its token's indices in all of
+// them before any is counted, so those reads overlap.
+constexpr int kSortSB = 4;
+
+// Block histograms (one per sort block of kSortBlock tokens), and the cluster totals: one
+// atomic per cluster per CTA, the sum over its blocks.
+__global__ void __launch_bounds__(kSortBlock) k_sort_hist(QPlan p, int t, int delta) {
     pdl_begin();
-    __shared__ int hist_s[kHistGroups][kMaxC], lhist_s[kHistGroups][kMaxC];
-    const int h = blockIdx.y, g = threadIdx.x / kSortBlock, tl = threadIdx.x % kSortBlock;
-    const int b = blockIdx.x * kHistGroups + g;
-    int *hist = hist_s[g], *lhist = lhist_s[g];
-    for (int j = tl; j < p.C; j += kSortBlock) hist[j] = lhist[j] = 0;
-    __syncthreads();
-    const int64_t i = (int64_t)b * kSortBlock + tl;  // >= N for a group past the last block
-    if (i < p.N && p.pi[(int64_t)(h * p.T + t - 1) * p.cap + p.tok_off + i] >= p.C)
-        or_status(p.status, QVG_DEV_BAD_INDEX);
-    const SortKeys k = sort_keys(p, h, t, i, delta);
-    if (k.enter >= 0) atomicAdd(hist + k.enter, 1);
-    if (k.leave >= 0) {
-        atomicAdd(hist + k.leave, 1);
-        atomicAdd(lhist + k.leave, 1);
+    __shared__ int hist[kSortSB][kMaxC];
+    __shared__ int lsum[kMaxC];  // leave items of the CTA's blocks per cluster
+    const int h = blockIdx.y, tl = threadIdx.x;
+    const int bb = blockIdx.x * kSortSB;  // the CTA's first sort block
+    for (int x = tl; x < kSortSB * kMaxC; x += kSortBlock) (&hist[0][0])[x] = 0;
+    for (int j = tl; j < kMaxC; j += kSortBlock) lsum[j] = 0;
+    SortKeys k[kSortSB];
+    bool bad = false;
+#pragma unroll
+    for (int u = 0; u < kSortSB; u++) {
+        k[u] = sort_keys(p, h, t, (int64_t)(bb + u) * kSortBlock + tl, delta);
+        bad |= k[u].bad;
     }
     __syncthreads();
-    if (b >= p.nsb) return;
-    int *bh = p.blockoff + ((int64_t)h * p.nsb + b) * p.C;
+#pragma unroll
+    for (int u = 0; u < kSortSB; u++) {
+        if (k[u].enter >= 0) atomicAdd(&hist[u][k[u].enter], 1);
+        if (k[u].leave >= 0) {
+            atomicAdd(&hist[u][k[u].leave], 1);
+            atomicAdd(&lsum[k[u].leave], 1);
+        }
+    }
+    if (__any_sync(0xffffffffu, bad) && (tl & 31) == 0) or_status(p.status, QVG_DEV_BAD_INDEX);
+    __syncthreads();
     for (int j = tl; j < p.C; j += kSortBlock) {
-        bh[j] = hist[j];  // the cluster totals are the scan's column sums
-        if (lhist[j]) atomicAdd(p.dleave + h * p.C + j, lhist[j]);
+        int tot = 0;
+#pragma unroll
+        for (int u = 0; u < kSortSB; u++) {
+            const int v = hist[u][j];
+            if (bb + u < p.nsb) p.blockoff[((int64_t)h * p.nsb + bb + u) * p.C + j] = v;
+            tot += v;
+        }
+        if (tot) atomicAdd(p.counts + h * p.C + j, tot);  // cluster totals (zero on entry)
+        if (lsum[j]) atomicAdd(p.dleave + h * p.C + j, lsum[j]);
     }
 }
 
-// Offsets of the counting sort.  One CTA of 1024 threads per tensor: thread (w, j) takes
-// cluster j and the w-th quarter of the token blocks.  The cluster totals are the column
-// sums of the block histograms; offs[j] = the sum of the totals of the clusters before j;
-// blockoff[b][j] (in place, over the block histogram) = offs[j] + the items of cluster j
-// in the blocks before b; counts[j] = the total; items = the tensor's total.
-constexpr int kScanSlices = 4;
-__global__ void __launch_bounds__(kMaxC * kScanSlices) k_sort_scan(QPlan p) {
+// Offsets of the counting sort.  grid (C/32 cluster groups, H), block 256: lane = cluster
+// of the group, warp w = a slice of the token blocks.  offs[j] = sum of the totals of the
+// clusters before j; blockoff[b][j] (in place, over the block histogram) = offs[j] + the
+// items of cluster j in the blocks before b; items = the tensor's total.
+__global__ void __launch_bounds__(256) k_sort_scan(QPlan p) {
     pdl_begin();
-    __shared__ int part[kScanSlices][kMaxC];  // column sums of each quarter
-    __shared__ int excl[kMaxC];               // exclusive scan of the cluster totals
-    const int h = blockIdx.x, j = threadIdx.x % kMaxC, w = threadIdx.x / kMaxC;
+    constexpr int NW = 8;
+    __shared__ int tot[kMaxC];
+    __shared__ int wsum[NW][32];
+    const int h = blockIdx.y, lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int j = blockIdx.x * 32 + lane;
+    // inclusive scan of the cluster totals of this tensor
+    const int x = threadIdx.x;
+    tot[x] = x < p.C ? p.counts[h * p.C + x] : 0;
+    __syncthreads();
+    for (int o = 1; o < kMaxC; o <<= 1) {
+        const int a1 = x >= o ? tot[x - o] : 0;
+        __syncthreads();
+        tot[x] += a1;
+        __syncthreads();
+    }
+    if (blockIdx.x == 0 && x == 0) p.items[h] = tot[kMaxC - 1];
     int *bh = p.blockoff + (int64_t)h * p.nsb * p.C;
-    const int per = (p.nsb + kScanSlices - 1) / kScanSlices;
+    const int per = (p.nsb + NW - 1) / NW;
     const int b0 = w * per, b1 = min(p.nsb, b0 + per);
     int local = 0;
     if (j < p.C) {
 #pragma unroll 8
         for (int b = b0; b < b1; b++) local += bh[(int64_t)b * p.C + j];
     }
-    part[w][j] = local;
+    wsum[w][lane] = local;
     __syncthreads();
-    if (w == 0) {
-        int tot = 0;
-#pragma unroll
-        for (int w2 = 0; w2 < kScanSlices; w2++) tot += part[w2][j];
-        excl[j] = tot;  // inclusive scan below, then shifted
-    }
-    __syncthreads();
-    for (int o = 1; o < kMaxC; o <<= 1) {
-        int a1 = 0;
-        if (w == 0 && j >= o) a1 = excl[j - o];
-        __syncthreads();
-        if (w == 0) excl[j] += a1;
-        __syncthreads();
-    }
     if (j < p.C) {
-        const int total = (w == 0) ? excl[j] - (j > 0 ? excl[j - 1] : 0) : 0;
-        const int off = j > 0 ? excl[j - 1] : 0;
-        if (w == 0) {
-            p.offs[h * p.C + j] = off;
-            p.counts[h * p.C + j] = total;
-        }
+        const int off = tot[j] - (j < p.C ? p.counts[h * p.C + j] : 0);
+        if (w == 0) p.offs[h * p.C + j] = off;
         int run = off;
-        for (int w2 = 0; w2 < w; w2++) run += part[w2][j];
+        for (int w2 = 0; w2 < w; w2++) run += wsum[w2][lane];
         for (int b = b0; b < b1; b++) {
             const int v = bh[(int64_t)b * p.C + j];
             bh[(int64_t)b * p.C + j] = run;
             run += v;
         }
     }
-    if (threadIdx.x == 0) p.items[h] = excl[kMaxC - 1];
 }
 
 // Writes the block's items to their sorted positions (the leave items of a cluster before
@@ -1187,10 +1201,10 @@ __global__ void __launch_bounds__(256) k_cluster_finalize(QPlan p, int t, int pl
 cudaError_t launch_cluster_means(const QPlan &p, const AssignMaps *maps, int t, bool planes,
                                  bool delta, int num_sms, cudaStream_t st) {
     const int dl = delta ? 1 : 0;
-    cudaError_t e = launch_kernel(k_sort_hist, dim3((unsigned)((p.nsb + kHistGroups - 1) / kHistGroups), p.H),
-                                  dim3(kSortBlock * kHistGroups), 0, st, p, t, dl);
+    cudaError_t e = launch_kernel(k_sort_hist, dim3((unsigned)((p.nsb + kSortSB - 1) / kSortSB), p.H),
+                                  dim3(kSortBlock), 0, st, p, t, dl);
     if (e == cudaSuccess)
-        e = launch_kernel(k_sort_scan, dim3((unsigned)p.H), dim3(kMaxC * kScanSlices), 0, st, p);
+        e = launch_kernel(k_sort_scan, dim3((unsigned)((p.C + 31) / 32), p.H), dim3(256), 0, st, p);
     if (e == cudaSuccess)
         e = launch_kernel(k_sort_scatter, dim3((unsigned)((p.nsb + kScatterGroups - 1) / kScatterGroups), p.H),
                           dim3(kSortBlock * kScatterGroups), 0, st, p, t, dl);
