@@ -687,16 +687,19 @@ __global__ void __launch_bounds__(kSortBlock * kScatterGroups) k_sort_scatter(QP
     constexpr int NW = kSortBlock / 32;
     // leave / enter items of each cluster per warp, per group (at most 32: one byte each)
     __shared__ __align__(16) uint8_t wl_s[kScatterGroups][NW][kMaxC], we_s[kScatterGroups][NW][kMaxC];
+    __shared__ int bo_s[kScatterGroups][kMaxC];  // the block's first position per cluster
     const int h = blockIdx.y, g = threadIdx.x / kSortBlock, tl = threadIdx.x % kSortBlock;
     const int b = blockIdx.x * kScatterGroups + g;
     uint8_t (*wl)[kMaxC] = wl_s[g], (*we)[kMaxC] = we_s[g];
+    // the block's offsets, read beside its tokens' indices (neither waits for the other)
+    if (tl < p.C && b < p.nsb) bo_s[g][tl] = p.blockoff[((int64_t)h * p.nsb + b) * p.C + tl];
     const int lane = tl & 31, w = tl >> 5;
+    const int64_t i = (int64_t)b * kSortBlock + tl;  // >= N for a group past the last block
+    const SortKeys k = sort_keys(p, h, t, i, delta);
     static_assert(2 * NW * kMaxC == kSortBlock * 16, "one 16-byte store per thread");
     constexpr int kVec = NW * kMaxC / 16;  // 16-byte pieces of one array
     reinterpret_cast<uint4 *>(tl < kVec ? &wl[0][0] : &we[0][0])[tl % kVec] = make_uint4(0u, 0u, 0u, 0u);
     __syncthreads();
-    const int64_t i = (int64_t)b * kSortBlock + tl;  // >= N for a group past the last block
-    const SortKeys k = sort_keys(p, h, t, i, delta);
     const unsigned sl = __match_any_sync(0xffffffffu, k.leave);
     const unsigned se = __match_any_sync(0xffffffffu, k.enter);
     const unsigned below = (1u << lane) - 1u;
@@ -704,7 +707,7 @@ __global__ void __launch_bounds__(kSortBlock * kScatterGroups) k_sort_scatter(QP
     if (k.leave >= 0 && rl == 0) wl[w][k.leave] = (uint8_t)__popc(sl);
     if (k.enter >= 0 && re == 0) we[w][k.enter] = (uint8_t)__popc(se);
     __syncthreads();
-    const int *bo = p.blockoff + ((int64_t)h * p.nsb + b) * p.C;
+    const int *bo = bo_s[g];
     int *ids = p.ids + (int64_t)h * p.icap;
     uint8_t *cid = p.cid + (int64_t)h * p.icap;
     if (k.leave >= 0) {
