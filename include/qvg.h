@@ -45,6 +45,14 @@
  *     be NULL) as QVG_DEV_* bits; read it after synchronising the stream.  No call aborts
  *     the process or traps the device.
  *   - Pointers must be 16-byte aligned.
+ *   - Fault injection, for testing a caller's error handling without faulting a GPU (read
+ *     from the environment at every call): QVG_FAULT_INJECT=launch makes every call that
+ *     would enqueue device work return QVG_ERR_CUDA after its argument checks, with nothing
+ *     enqueued; =alloc does the same for qvg_quantize_static alone (its scratch lookup);
+ *     =timeout runs qvg_quantize's tensor-core assignments with their centroid operand
+ *     withheld and a 1 ms wait limit (as qvg_selftest_assign_timeout does), so the call
+ *     returns QVG_OK, the device status gets QVG_DEV_TIMEOUT and the results are
+ *     unspecified.  Unset, or any other value: no effect.
  *
  * Supported shapes: d = 128; group in {16, 32, 64}; bits in {2, 4}; 1 <= C <= 256 and
  * C <= N when T > 0; 0 <= T <= 8; iters >= 1; N >= 1.

@@ -151,6 +151,28 @@ def test_reassign_steps_rejects_unknown_steps(lib):
                                   None, None) == qvg.QVG_ERR_INVALID_ARG
 
 
+def test_fault_injection_comes_after_the_argument_checks(lib, monkeypatch):
+    # QVG_FAULT_INJECT fails calls as a launch error would, but only once their arguments
+    # passed: a bad argument is still reported as such (the device is never reached here)
+    buf = (ctypes.c_ubyte * 64)()
+    base = ctypes.addressof(buf) + (-ctypes.addressof(buf)) % 16
+    good = qvg.qvg_buffers(base, base, base, base)
+    for mode in ("launch", "alloc", "timeout"):
+        monkeypatch.setenv("QVG_FAULT_INJECT", mode)
+        assert qvg.qvg_quantize(_qp(bits=3), base, None, good, base, 1 << 40, None,
+                                None) == qvg.QVG_ERR_UNSUPPORTED
+        assert qvg.qvg_quantize_static(_qp(C=5000), base, None, good, None,
+                                       None) == qvg.QVG_ERR_UNSUPPORTED
+        assert qvg.qvg_quantize(_qp(), base, None, good, base, 16, None,
+                                None) == qvg.QVG_ERR_WORKSPACE
+    # with valid arguments an injected launch failure is QVG_ERR_CUDA
+    wbuf = (ctypes.c_ubyte * 512)()
+    ws = ctypes.addressof(wbuf) + (-ctypes.addressof(wbuf)) % 256  # the workspace's alignment
+    monkeypatch.setenv("QVG_FAULT_INJECT", "launch")
+    assert qvg.qvg_quantize(_qp(), base, None, good, ws, 1 << 40, None,
+                            None) == qvg.QVG_ERR_CUDA
+
+
 def test_dequantize_rejects_bad_arguments(lib):
     buf = (ctypes.c_ubyte * 64)()
     base = ctypes.addressof(buf) + (-ctypes.addressof(buf)) % 16

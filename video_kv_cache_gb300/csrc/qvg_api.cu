@@ -3,6 +3,7 @@
 // are in include/qvg.h.
 #include <cmath>
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -130,8 +131,26 @@ qvg_status device_info(int *num_sms) {
         }                                             \
     } while (0)
 
+// Host-side fault injection, for testing the callers' error paths without faulting a GPU:
+// QVG_FAULT_INJECT=launch makes every call that would enqueue device work return
+// QVG_ERR_CUDA once its arguments are checked, as a failed launch would (nothing is
+// enqueued); =alloc makes qvg_quantize_static's scratch lookup fail the same way;
+// =timeout runs every assignment launch of qvg_quantize with its centroid operand withheld
+// and a 1 ms wait limit, the path qvg_selftest_assign_timeout exercises: the device status
+// gets QVG_DEV_TIMEOUT and the results are unspecified.  Read at every call.
+enum FaultMode { kFaultNone = 0, kFaultAlloc, kFaultLaunch, kFaultTimeout };
+FaultMode fault_mode() {
+    const char *v = getenv("QVG_FAULT_INJECT");
+    if (!v) return kFaultNone;
+    if (!strcmp(v, "alloc")) return kFaultAlloc;
+    if (!strcmp(v, "launch")) return kFaultLaunch;
+    if (!strcmp(v, "timeout")) return kFaultTimeout;
+    return kFaultNone;
+}
+
 // The T smoothing stages: cold-start or warm centroids, then `iters` Lloyd rounds each.
 qvg_status run_stages(QPlan &p, const AssignMaps *maps, int num_sms, cudaStream_t st) {
+    const bool inject_timeout = fault_mode() == kFaultTimeout;
     qvg_status rc = QVG_OK;
     // the sort's item and leave counts start at zero; each update leaves them at zero again
     if (cudaMemsetAsync(p.counts, 0, (size_t)p.H * p.C * 4, st) != cudaSuccess ||
@@ -147,7 +166,8 @@ qvg_status run_stages(QPlan &p, const AssignMaps *maps, int num_sms, cudaStream_
         if (t >= 2) step(launch_init_centroids(p, t, st));
         step(launch_centroid_planes(p, t, st));
         for (int it = 1; it <= p.iters && rc == QVG_OK; it++) {
-            step(launch_assign(p, maps, t, num_sms, st));
+            step(inject_timeout ? launch_assign(p, maps, t, num_sms, st, 1000000ull, 1)
+                                : launch_assign(p, maps, t, num_sms, st));
             step(launch_refine(p, t, num_sms, st));
             // The first round sums every member; the ones between fold in the tokens that
             // moved.  The last sums every member again, so the stage's centroids are means
@@ -315,6 +335,7 @@ qvg_status qvg_quantize(const qvg_quant_params *prm, const void *X, const float 
     const WsLayout w = ws_layout(prm->n_tensors, prm->N, prm->C, prm->T);
     if (!workspace || workspace_bytes < w.total) return QVG_ERR_WORKSPACE;
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return QVG_ERR_INVALID_ARG;
+    if (fault_mode() == kFaultLaunch) return QVG_ERR_CUDA;
     int num_sms = 0;
     rc = device_info(&num_sms);
     if (rc != QVG_OK) return rc;
@@ -336,6 +357,8 @@ qvg_status qvg_quantize_static(const qvg_quant_params *prm, const void *X, const
     if (w.total > QVG_STATIC_SCRATCH_BYTES) return QVG_ERR_SCRATCH_LIMIT;
     rc = check_quant_buffers(prm, X, warm, out);
     if (rc != QVG_OK) return rc;
+    const FaultMode fm = fault_mode();
+    if (fm == kFaultLaunch || fm == kFaultAlloc) return QVG_ERR_CUDA;
     int num_sms = 0;
     rc = device_info(&num_sms);
     if (rc != QVG_OK) return rc;
@@ -373,6 +396,7 @@ qvg_status qvg_reassign_steps(const qvg_quant_params *prm, const void *X, const 
     const WsLayout w = ws_layout(prm->n_tensors, prm->N, prm->C, prm->T);
     if (!workspace || workspace_bytes < w.total) return QVG_ERR_WORKSPACE;
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return QVG_ERR_INVALID_ARG;
+    if (fault_mode() == kFaultLaunch) return QVG_ERR_CUDA;
     int num_sms = 0;
     rc = device_info(&num_sms);
     if (rc != QVG_OK) return rc;
@@ -414,6 +438,7 @@ qvg_status qvg_selftest_assign_timeout(const qvg_quant_params *prm, const void *
     const WsLayout w = ws_layout(prm->n_tensors, prm->N, prm->C, prm->T);
     if (!workspace || workspace_bytes < w.total) return QVG_ERR_WORKSPACE;
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return QVG_ERR_INVALID_ARG;
+    if (fault_mode() == kFaultLaunch) return QVG_ERR_CUDA;
     int num_sms = 0;
     rc = device_info(&num_sms);
     if (rc != QVG_OK) return rc;
@@ -460,6 +485,7 @@ qvg_status qvg_dequantize(const qvg_dequant_params *prm, const qvg_buffers *in, 
     if (!aligned16(X_hat) || !aligned16(in->codes) || !aligned16(in->scales) ||
         (prm->T > 0 && !aligned16(in->centroids)))
         return QVG_ERR_INVALID_ARG;
+    if (fault_mode() == kFaultLaunch) return QVG_ERR_CUDA;
     int num_sms = 0;
     qvg_status rc = device_info(&num_sms);
     if (rc != QVG_OK) return rc;
@@ -552,6 +578,7 @@ qvg_status qvg_attention(const qvg_attention_params *prm, const void *Q,
     if (!aligned16(Q) || !aligned16(O)) return QVG_ERR_INVALID_ARG;
     const AttnWs w = attn_layout(prm);
     if (!workspace || ws_bytes < w.total || !aligned16(workspace)) return QVG_ERR_WORKSPACE;
+    if (fault_mode() == kFaultLaunch) return QVG_ERR_CUDA;
     int num_sms = 0;
     rc = device_info(&num_sms);
     if (rc != QVG_OK) return rc;
