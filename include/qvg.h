@@ -52,7 +52,10 @@
  *     =timeout runs qvg_quantize's tensor-core assignments with their centroid operand
  *     withheld and a 1 ms wait limit (as qvg_selftest_assign_timeout does), so the call
  *     returns QVG_OK, the device status gets QVG_DEV_TIMEOUT and the results are
- *     unspecified.  Unset, or any other value: no effect.
+ *     unspecified; =assign makes qvg_quantize's first tensor-core assignment launch fail
+ *     after the kernels before it were enqueued, so the call returns QVG_ERR_CUDA from the
+ *     middle of its sequence (nothing after the failed launch is enqueued; the outputs are
+ *     unspecified).  Unset, or any other value: no effect.
  *
  * Supported shapes: d = 128; group in {16, 32, 64}; bits in {2, 4}; 1 <= C <= 256 and
  * C <= N when T > 0; 0 <= T <= 8; iters >= 1; N >= 1.
@@ -240,8 +243,10 @@ qvg_status qvg_reassign(const qvg_quant_params *params, const void *X, const qvg
 #define QVG_STEP_REFINE 4 /* the exact re-scoring of the requested rows */
 /* qvg_reassign with only the steps in the `steps` mask.  Each step reads what the earlier
  * ones wrote in the workspace: run them in order, on one stream (the GEMM after the planes
- * of the same centroids, the re-scoring after the GEMM).  QVG_ERR_INVALID_ARG for other
- * bits; otherwise as qvg_reassign. */
+ * of the same centroids, the re-scoring after the GEMM).  A re-scoring step whose queue no
+ * GEMM step wrote (a fresh workspace) reads no request outside the queue's capacity: it
+ * skips what is out of range and ORs QVG_DEV_BAD_INDEX into *dev_status.
+ * QVG_ERR_INVALID_ARG for other bits; otherwise as qvg_reassign. */
 qvg_status qvg_reassign_steps(const qvg_quant_params *params, const void *X,
                               const qvg_buffers *out, void *workspace, size_t workspace_bytes,
                               int32_t steps, uint32_t *dev_status, void *stream);

@@ -133,3 +133,58 @@ def test_injected_timeout_sets_the_status_and_the_next_call_is_exact(monkeypatch
     assert int(status.item()) == 0
     for k, v in ref_bits.items():
         assert torch.equal(getattr(again, k), v), k
+
+
+def test_a_launch_failing_mid_call_enqueues_nothing_after_it(monkeypatch):
+    """QVG_FAULT_INJECT=assign: the first assignment launch of qvg_quantize fails after the
+    preparation kernels were enqueued.  Nothing after it may run: in particular not the
+    re-scoring, whose queue no assignment wrote (the workspace is filled with 0xFF, which
+    the re-scoring would report as QVG_DEV_BAD_INDEX).  The call returns QVG_ERR_CUDA, the
+    status word stays clear, and a call without the injection gives the reference bytes."""
+    X, H, N, C, T, bits, group, iters, seed = _small_case()
+    ws = api.new_workspace(H, N, C, T)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ref = api.quantize(X, C, T, bits, group, iters, seed, workspace=ws, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    ref_bits = {k: getattr(ref, k).clone() for k in ("codes", "scales", "pi", "centroids")}
+    ws.fill_(0xFF)
+    out = api.allocate(H, N, C, T, bits, group, 1, X.device)
+    prm = api.quant_params(H, N, C, T, bits, group, iters, X.dtype, seed)
+    stream = torch.cuda.current_stream().cuda_stream
+    monkeypatch.setenv("QVG_FAULT_INJECT", "assign")
+    rc = qvg.qvg_quantize(prm, X.data_ptr(), None, out.buffers(), ws.data_ptr(), ws.numel(),
+                          status.data_ptr(), stream)
+    assert rc == qvg.QVG_ERR_CUDA
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    monkeypatch.delenv("QVG_FAULT_INJECT")
+    again = api.quantize(X, C, T, bits, group, iters, seed, workspace=ws, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    for k, v in ref_bits.items():
+        assert torch.equal(getattr(again, k), v), k
+
+
+def test_rescoring_alone_on_an_unwritten_queue_is_skipped_and_reported():
+    """qvg_reassign_steps with the re-scoring step only, on a workspace no assignment wrote
+    (every byte 0xFF, so the queue's first slot and count read as -1): no request is read,
+    QVG_DEV_BAD_INDEX is set, the stored assignments are untouched and the device stays
+    usable."""
+    X, H, N, C, T, bits, group, iters, seed = _small_case()
+    ws = api.new_workspace(H, N, C, T)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = api.quantize(X, C, T, bits, group, iters, seed, workspace=ws, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    pi = out.pi.clone()
+    ws.fill_(0xFF)
+    api.reassign(X, out, iters, ws, seed, status=status, steps=qvg.QVG_STEP_REFINE)
+    torch.cuda.synchronize()
+    assert int(status.item()) & qvg.QVG_DEV_BAD_INDEX
+    assert torch.equal(out.pi, pi)
+    status.zero_()
+    again = api.quantize(X, C, T, bits, group, iters, seed, workspace=ws, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert torch.equal(again.pi, pi)

@@ -661,7 +661,21 @@ __global__ void __launch_bounds__(256, 3) k_refine(QPlan p, int t, int n_regions
     const int region = blockIdx.x % n_regions;
     const int gh = ((blockIdx.x / n_regions) * (blockDim.x >> 5) + (threadIdx.x >> 5)) * 2 + (lane >> 4);
     const int nh = split * (blockDim.x >> 5) * 2;
-    const int first = p.rq_cta[2 * region], count = p.rq_cta[2 * region + 1];
+    int first = p.rq_cta[2 * region], count = p.rq_cta[2 * region + 1];
+    // The queue is the one the assignment of this call wrote.  A region outside the queue's
+    // capacity (the re-scoring step run with no assignment before it) is skipped and
+    // reported, and so is a request for a row outside the problem; candidate bits at or past
+    // C are ignored.  None of these occur when the steps run in order.
+    const int64_t rq_cap = (int64_t)p.H * ((p.N + kAssignTileM - 1) / kAssignTileM) * kAssignTileM;
+    if (first < 0 || count < 0 || (int64_t)first + count > rq_cap) {
+        if (threadIdx.x == 0 && blockIdx.x < n_regions) or_status(p.status, QVG_DEV_BAD_INDEX);
+        first = count = 0;
+    }
+    auto cand_word = [&](const RefineReq *rq, int w) {  // bits of clusters < C only
+        const int live = p.C - 32 * w;
+        const uint32_t keep = live >= 32 ? 0xFFFFFFFFu : (live <= 0 ? 0u : (1u << live) - 1u);
+        return rq->cand[w] & keep;
+    };
     auto hsum = [&](float v) {  // the half-warp's sum, the same in every lane of it
 #pragma unroll
         for (int o = 8; o >= 1; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(hmask, v, o));
@@ -687,6 +701,12 @@ __global__ void __launch_bounds__(256, 3) k_refine(QPlan p, int t, int n_regions
         }
         const int h = cur_h;
         const int64_t i = cur_i;
+        cur_h = nxt_h;
+        cur_i = nxt_i;
+        if ((unsigned)h >= (unsigned)p.H || i < 0 || i >= p.N) {  // the same in the half-warp
+            if (hl == 0) or_status(p.status, QVG_DEV_BAD_INDEX);
+            continue;
+        }
         const float *ct = p.cent + h * p.cent_tstride + p.cent_off;
         const float *c0 = ct + (int64_t)(t - 1) * p.C * kD;
         constexpr int NB = TP > 0 ? TP : 1;  // earlier stages batched
@@ -702,14 +722,14 @@ __global__ void __launch_bounds__(256, 3) k_refine(QPlan p, int t, int n_regions
         // candidates in increasing cluster order, two at a time; the first two rows now
         constexpr int KB = 2;
         int cb = 0;
-        uint32_t m = rqp->cand[0];
+        uint32_t m = cand_word(rqp, 0);
         int jj[KB], nb = 0;
         float4 ca[KB], cc[KB];
         auto next_batch = [&]() {
             nb = 0;
 #pragma unroll
             for (int u = 0; u < KB; u++) {
-                while (m == 0u && cb < 7) m = rqp->cand[++cb];
+                while (m == 0u && cb < 7) m = cand_word(rqp, ++cb);
                 jj[u] = -1;
                 if (m) {
                     jj[u] = cb * 32 + __ffs(m) - 1;
@@ -818,7 +838,7 @@ __global__ void __launch_bounds__(256, 3) k_refine(QPlan p, int t, int n_regions
             }
             double bestDd = INFINITY;
             for (int cw = 0; cw < 8; cw++) {
-                uint32_t mm = rqp->cand[cw];
+                uint32_t mm = cand_word(rqp, cw);
                 while (mm) {
                     const int j = cw * 32 + __ffs(mm) - 1;
                     mm &= mm - 1u;
@@ -841,8 +861,6 @@ __global__ void __launch_bounds__(256, 3) k_refine(QPlan p, int t, int n_regions
             }
         }
         if (hl == 0) p.pi[(int64_t)(h * p.T + t - 1) * p.cap + p.tok_off + i] = (uint8_t)bestj;
-        cur_h = nxt_h;
-        cur_i = nxt_i;
     }
     if (p.stats && hl == 0 && n_cands) atomicAdd(p.stats + kStatRefineCands, n_cands);
 }

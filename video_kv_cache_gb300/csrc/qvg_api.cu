@@ -137,42 +137,55 @@ qvg_status device_info(int *num_sms) {
 // enqueued); =alloc makes qvg_quantize_static's scratch lookup fail the same way;
 // =timeout runs every assignment launch of qvg_quantize with its centroid operand withheld
 // and a 1 ms wait limit, the path qvg_selftest_assign_timeout exercises: the device status
-// gets QVG_DEV_TIMEOUT and the results are unspecified.  Read at every call.
-enum FaultMode { kFaultNone = 0, kFaultAlloc, kFaultLaunch, kFaultTimeout };
+// gets QVG_DEV_TIMEOUT and the results are unspecified; =assign makes the first assignment
+// launch of qvg_quantize fail (it is not enqueued), after the kernels before it were
+// enqueued, so the call returns QVG_ERR_CUDA from the middle of its sequence.  Read at
+// every call.
+enum FaultMode { kFaultNone = 0, kFaultAlloc, kFaultLaunch, kFaultTimeout, kFaultAssign };
 FaultMode fault_mode() {
     const char *v = getenv("QVG_FAULT_INJECT");
     if (!v) return kFaultNone;
     if (!strcmp(v, "alloc")) return kFaultAlloc;
     if (!strcmp(v, "launch")) return kFaultLaunch;
     if (!strcmp(v, "timeout")) return kFaultTimeout;
+    if (!strcmp(v, "assign")) return kFaultAssign;
     return kFaultNone;
 }
 
 // The T smoothing stages: cold-start or warm centroids, then `iters` Lloyd rounds each.
 qvg_status run_stages(QPlan &p, const AssignMaps *maps, int num_sms, cudaStream_t st) {
-    const bool inject_timeout = fault_mode() == kFaultTimeout;
+    const FaultMode fm = fault_mode();
+    const bool inject_timeout = fm == kFaultTimeout, inject_assign = fm == kFaultAssign;
     qvg_status rc = QVG_OK;
     // the sort's item and leave counts start at zero; each update leaves them at zero again
     if (cudaMemsetAsync(p.counts, 0, (size_t)p.H * p.C * 4, st) != cudaSuccess ||
         cudaMemsetAsync(p.dleave, 0, (size_t)p.H * p.C * 4, st) != cudaSuccess)
         return QVG_ERR_CUDA;
+    // Each launch reads what the earlier ones wrote, so after a failed launch nothing more is
+    // enqueued (a re-scoring launched after a failed assignment would read a queue no kernel
+    // of this call wrote).
+    auto step = [&](auto &&launch) {
+        if (rc == QVG_OK && launch() != cudaSuccess) rc = QVG_ERR_CUDA;
+    };
     for (int t = 1; t <= p.T && rc == QVG_OK; t++) {
-        auto step = [&](cudaError_t e) {
-            if (e != cudaSuccess && rc == QVG_OK) rc = QVG_ERR_CUDA;
-        };
-        if (t == 1) step(launch_init_centroids(p, t, st));
-        step(launch_centre(p, t, st));
-        step(launch_prep(p, t, st));
-        if (t >= 2) step(launch_init_centroids(p, t, st));
-        step(launch_centroid_planes(p, t, st));
+        if (t == 1) step([&] { return launch_init_centroids(p, t, st); });
+        step([&] { return launch_centre(p, t, st); });
+        step([&] { return launch_prep(p, t, st); });
+        if (t >= 2) step([&] { return launch_init_centroids(p, t, st); });
+        step([&] { return launch_centroid_planes(p, t, st); });
         for (int it = 1; it <= p.iters && rc == QVG_OK; it++) {
-            step(inject_timeout ? launch_assign(p, maps, t, num_sms, st, 1000000ull, 1)
-                                : launch_assign(p, maps, t, num_sms, st));
-            step(launch_refine(p, t, num_sms, st));
+            step([&] {
+                if (inject_assign) return cudaErrorLaunchFailure;  // as if the launch failed
+                return inject_timeout ? launch_assign(p, maps, t, num_sms, st, 1000000ull, 1)
+                                      : launch_assign(p, maps, t, num_sms, st);
+            });
+            step([&] { return launch_refine(p, t, num_sms, st); });
             // The first round sums every member; the ones between fold in the tokens that
             // moved.  The last sums every member again, so the stage's centroids are means
             // of a fresh compensated sum, with no rounding carried over from earlier rounds.
-            step(launch_cluster_means(p, maps, t, it < p.iters, it > 1 && it < p.iters, num_sms, st));
+            step([&] {
+                return launch_cluster_means(p, maps, t, it < p.iters, it > 1 && it < p.iters, num_sms, st);
+            });
         }
     }
     return rc;
