@@ -249,15 +249,31 @@ __global__ void __launch_bounds__(256) k_attn_combine(APlan p) {
     for (int s = lane; s < p.S; s += 32) mx = fmaxf(mx, p.ml[2 * (((int64_t)h * p.S + s) * p.M + m)]);
     mx = warp_max(mx);
     float l = 0.f, a[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int s = 0; s < p.S; s++) {
-        const int64_t r = ((int64_t)h * p.S + s) * p.M + m;
-        const float wgt = expf(p.ml[2 * r] - mx);
-        l = __fmaf_rn(wgt, p.ml[2 * r + 1], l);
-        const float4 po = *reinterpret_cast<const float4 *>(p.part + r * kD + 4 * lane);
-        a[0] = __fmaf_rn(wgt, po.x, a[0]);
-        a[1] = __fmaf_rn(wgt, po.y, a[1]);
-        a[2] = __fmaf_rn(wgt, po.z, a[2]);
-        a[3] = __fmaf_rn(wgt, po.w, a[3]);
+    // the splits in order, eight at a time: their partial rows and (max, sum) pairs are read
+    // before any is added
+    constexpr int SB = 8;
+    for (int s0 = 0; s0 < p.S; s0 += SB) {
+        float2 ml[SB];
+        float4 po[SB];
+#pragma unroll
+        for (int u = 0; u < SB; u++) {
+            if (s0 + u < p.S) {
+                const int64_t r = ((int64_t)h * p.S + s0 + u) * p.M + m;
+                ml[u] = *reinterpret_cast<const float2 *>(p.ml + 2 * r);
+                po[u] = *reinterpret_cast<const float4 *>(p.part + r * kD + 4 * lane);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < SB; u++) {
+            if (s0 + u < p.S) {
+                const float wgt = expf(ml[u].x - mx);
+                l = __fmaf_rn(wgt, ml[u].y, l);
+                a[0] = __fmaf_rn(wgt, po[u].x, a[0]);
+                a[1] = __fmaf_rn(wgt, po[u].y, a[1]);
+                a[2] = __fmaf_rn(wgt, po[u].z, a[2]);
+                a[3] = __fmaf_rn(wgt, po[u].w, a[3]);
+            }
+        }
     }
     const int64_t off = ((int64_t)h * p.M + m) * kD + 4 * lane;
 #pragma unroll
