@@ -375,10 +375,9 @@ struct APlan {
     void *O;                   // [H][M][d]
     uint32_t *status;
 };
-// Keys per split: the N keys of a head in min(ceil(N / 256), 128) parts, each rounded up to a
-// multiple of the 32-key tile.  Every split s < S = ceil(N / split_len) holds a key.
 // Keys per split: about 2048 splits over all heads (a warp each, enough to cover the SMs
-// with several warps apiece), at least 64 keys and a multiple of the 32-key tile.
+// with several warps apiece), at least 64 keys and a multiple of the 32-key tile.  Every
+// split s < S = ceil(N / split_len) holds a key.
 inline int64_t attn_split_len(int64_t N, int64_t heads) {
     const int64_t target = std::max<int64_t>(2048 / std::max<int64_t>(heads, 1), 1);
     const int64_t len = std::max<int64_t>((N + target - 1) / target, 64);

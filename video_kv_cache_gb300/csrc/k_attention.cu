@@ -18,9 +18,10 @@
 //     E4M3 scale, plus the stage-T centroid, then stages T-1 .. 1, each add rounded in fp32.
 //     A tile's 32 rows are rebuilt together in shared memory (rows padded to 132 floats):
 //     lane k reads key k's codes, scale bytes and cluster indices (one pass of coalesced
-//     reads for the whole tile) and writes its dequantized row; then for each stage the
-//     warp adds the keys' centroid rows (lane l: channels 4l .. 4l+3), with the rows of 8
-//     keys loaded before any is added.
+//     reads for the whole tile), writes its dequantized row and looks up, once, where
+//     each stage's centroid row of the key lies (a small shared table); then for each
+//     stage the warp adds the keys' centroid rows (lane l: channels 4l .. 4l+3), with the
+//     rows of 8 keys loaded before any is added.
 //   * Keys: lane j scores key j against every query (queries in shared memory, broadcast
 //     reads) with 128 sequential fp32 FMAs.
 //   * Values: the tile's value rows are rebuilt the same way into the same buffer; lane l
@@ -47,10 +48,11 @@ __device__ __forceinline__ float e4m3_value(uint32_t b) {
 // Rows [t0, t0 + cnt) of compressed tensor ti, rebuilt as qvg_dequantize's fp32 output has
 // them, into rows[k * kKRow + c] (k < cnt).  The reads are issued in bulk, not one key at a
 // time: lane k first reads key t0 + k's codes, scale bytes and cluster indices (coalesced
-// across the warp) and writes its dequantized row; then, stage by stage from T down to 1,
-// the warp adds each key's centroid row (lane l: channels 4l .. 4l+3), the rows of KB keys
-// loaded together before they are added.  Each element gets the same fp32 operations, in
-// the same order, as in qvg_dequantize.
+// across the warp), writes its dequantized row and, for each stage, the index of the key's
+// centroid row within tensor ti's tables into srow[t * kAttnTile + k]; then, stage by
+// stage from T down to 1, the warp adds each key's centroid row (lane l: channels
+// 4l .. 4l+3), the rows of KB keys loaded together before they are added.  Each element
+// gets the same fp32 operations, in the same order, as in qvg_dequantize.
 // (Kept out of line: inlined twice into the split kernel it pushed that kernel's register
 // count past what fits several warps per SM.)  Returns true if a stored index was out of
 // range.
@@ -58,18 +60,22 @@ template <int BITS, int SH, int KB>
 __device__ __noinline__ bool rebuild_tile(const APlan &p, const uint8_t *codes,
                                           const uint8_t *scales, const uint8_t *pi,
                                           const float *cent, int64_t ti, int64_t t0, int cnt,
-                                          int lane, float *rows) {
+                                          int lane, float *rows, int *srow) {
     bool bad = false;
     constexpr int MID = 1 << (BITS - 1);
     constexpr int WORDS = kD * BITS / 32;  // code words of a row
+    constexpr int PER = 32 / BITS;         // codes in a word
     const int ngroups = kD / p.group;
-    uint64_t pk = 0;
-    int tbl = 0;
     if (lane < cnt) {
         const int64_t row = ti * p.cap + t0 + lane;
         const uint32_t *cwp = reinterpret_cast<const uint32_t *>(codes + row * (kD * BITS / 8));
-        for (int t = 0; t < p.T; t++) pk |= (uint64_t)__ldg(pi + (ti * p.T + t) * p.cap + t0 + lane) << (8 * t);
-        tbl = (int)min((t0 + lane) / p.chunk_len, (int64_t)p.n_tables - 1);
+        const int tbl = (int)min((t0 + lane) / p.chunk_len, (int64_t)p.n_tables - 1);
+        for (int t = 0; t < p.T; t++) {
+            int j = __ldg(pi + (ti * p.T + t) * p.cap + t0 + lane);
+            bad |= j >= p.C;
+            j = min(j, p.C - 1);
+            srow[t * kAttnTile + lane] = (tbl * p.T + t) * p.C + j;
+        }
         // the row's scale bytes (ngroups = 8, 4 or 2 of them, naturally aligned)
         const uint8_t *sr = scales + row * ngroups;
         const uint64_t sw = ngroups == 8   ? __ldg(reinterpret_cast<const unsigned long long *>(sr))
@@ -77,20 +83,24 @@ __device__ __noinline__ bool rebuild_tile(const APlan &p, const uint8_t *codes,
                                            : (uint64_t)__ldg(reinterpret_cast<const unsigned short *>(sr));
         const int gsh = 31 - __clz(p.group);  // log2 of the group size
         float *dst = rows + lane * kKRow;
-        // one code word at a time: 32 / BITS channels (its first sector read brings the
-        // row's others into L1)
-#pragma unroll 1
-        for (int w = 0; w < WORDS; w++) {
-            const uint32_t word = __ldg(cwp + w);
+        // Every code word is read first; code u of a word goes into the mantissa of 2^23
+        // (one logic op) and one subtraction leaves u - MID exactly, the level of the
+        // symmetric grid (plus 1/2 on the mid-rise grid).
+        uint32_t cw[WORDS];
 #pragma unroll
-            for (int c4 = 0; c4 < 32 / BITS; c4 += 4) {
-                const int c = w * (32 / BITS) + c4;
+        for (int w = 0; w < WORDS; w++) cw[w] = __ldg(cwp + w);
+#pragma unroll
+        for (int w = 0; w < WORDS; w++) {
+#pragma unroll
+            for (int c4 = 0; c4 < PER; c4 += 4) {
+                const int c = w * PER + c4;
                 const float sq = e4m3_value((uint32_t)(sw >> (8 * (c >> gsh))) & 0xFFu);
                 float y[4];
 #pragma unroll
                 for (int k = 0; k < 4; k++) {
-                    const int u = (int)((word >> (BITS * (c4 + k))) & ((1u << BITS) - 1u));
-                    const float lv = SH ? __fadd_rn((float)(u - MID), 0.5f) : (float)(u - MID);
+                    const uint32_t u = (cw[w] >> (BITS * (c4 + k))) & ((1u << BITS) - 1u);
+                    float lv = __fsub_rn(__uint_as_float(0x4B000000u | u), 8388608.0f + (float)MID);
+                    if (SH) lv = __fadd_rn(lv, 0.5f);
                     y[k] = __fmul_rn(sq, lv);
                 }
                 *reinterpret_cast<float4 *>(dst + c) = make_float4(y[0], y[1], y[2], y[3]);
@@ -99,22 +109,14 @@ __device__ __noinline__ bool rebuild_tile(const APlan &p, const uint8_t *codes,
     }
     __syncwarp();
     for (int t = p.T - 1; t >= 0; t--) {
+        const float *tbase = cent + ti * p.n_tables * p.T * p.C * kD + 4 * lane;  // tensor ti
+        const int *sr = srow + t * kAttnTile;
         for (int k0 = 0; k0 < cnt; k0 += KB) {
             float4 c4[KB];
 #pragma unroll
             for (int u = 0; u < KB; u++) {
                 const int k = k0 + u;
-                const uint64_t pku = __shfl_sync(0xffffffffu, pk, k & 31);
-                const int tb = __shfl_sync(0xffffffffu, tbl, k & 31);
-                if (k < cnt) {
-                    int j = (int)((pku >> (8 * t)) & 0xFFu);
-                    if (j >= p.C) {
-                        j = p.C - 1;
-                        bad = true;
-                    }
-                    const float *tr = cent + ((ti * p.n_tables + tb) * p.T + t) * p.C * kD;
-                    c4[u] = __ldg(reinterpret_cast<const float4 *>(tr + (int64_t)j * kD) + lane);
-                }
+                if (k < cnt) c4[u] = __ldg(reinterpret_cast<const float4 *>(tbase + (int64_t)sr[k] * kD));
             }
 #pragma unroll
             for (int u = 0; u < KB; u++) {
@@ -154,8 +156,9 @@ __global__ void __launch_bounds__(32 * kAttnWarps, MQ > 4 ? 2 : 4) k_attn_split(
     extern __shared__ __align__(16) float sm_attn[];
     float *sQ = sm_attn;  // [MQ][d]
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    float *sK = sm_attn + MQ * kD + warp * (kAttnTile * kKRow + MQ * kAttnTile);  // [32][132]
-    float *sP = sK + kAttnTile * kKRow;                                         // [MQ][32]
+    float *sK = sm_attn + MQ * kD + warp * (kAttnTile * kKRow + MQ * kAttnTile + p.T * kAttnTile);
+    float *sP = sK + kAttnTile * kKRow;                                     // [MQ][32]
+    int *sRow = reinterpret_cast<int *>(sP + MQ * kAttnTile);               // [T][32]
     const int h = blockIdx.y;
     for (int x = threadIdx.x; x < MQ * kD; x += blockDim.x) {
         const int m = x / kD;
@@ -178,7 +181,7 @@ __global__ void __launch_bounds__(32 * kAttnWarps, MQ > 4 ? 2 : 4) k_attn_split(
     bool bad = false;
     for (int64_t t0 = n0; t0 < n1; t0 += kAttnTile) {
         const int cnt = (int)min((int64_t)kAttnTile, n1 - t0);
-        bad |= rebuild_tile<BITS, SH, KB>(p, p.kc, p.ks, p.kp, p.kcent, tk, t0, cnt, lane, sK);
+        bad |= rebuild_tile<BITS, SH, KB>(p, p.kc, p.ks, p.kp, p.kcent, tk, t0, cnt, lane, sK, sRow);
         float sc[MQ];
 #pragma unroll
         for (int m = 0; m < MQ; m++) sc[m] = 0.f;
@@ -209,7 +212,7 @@ __global__ void __launch_bounds__(32 * kAttnWarps, MQ > 4 ? 2 : 4) k_attn_split(
             sP[m * kAttnTile + lane] = pj;
         }
         __syncwarp();  // every lane has scored its key: the value rows can overwrite sK
-        bad |= rebuild_tile<BITS, SH, KB>(p, p.vc, p.vs, p.vp, p.vcent, tv, t0, cnt, lane, sK);
+        bad |= rebuild_tile<BITS, SH, KB>(p, p.vc, p.vs, p.vp, p.vcent, tv, t0, cnt, lane, sK, sRow);
         for (int kk = 0; kk < cnt; kk++) {
             const float4 v4 = *reinterpret_cast<const float4 *>(sK + kk * kKRow + 4 * lane);
 #pragma unroll
@@ -291,7 +294,8 @@ __global__ void __launch_bounds__(256) k_attn_combine(APlan p) {
 namespace {
 template <int BITS, int SH, int MQ>
 cudaError_t launch_split(const APlan &p, cudaStream_t st) {
-    const size_t smem = (size_t)(MQ * kD + kAttnWarps * (kAttnTile * kKRow + MQ * kAttnTile)) * sizeof(float);
+    const size_t smem =
+        (size_t)(MQ * kD + kAttnWarps * (kAttnTile * kKRow + MQ * kAttnTile + p.T * kAttnTile)) * sizeof(float);
     cudaError_t e = cudaFuncSetAttribute(k_attn_split<BITS, SH, MQ>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
