@@ -213,7 +213,27 @@ __global__ void __launch_bounds__(32 * kAttnWarps, MQ > 4 ? 2 : 4) k_attn_split(
         }
         __syncwarp();  // every lane has scored its key: the value rows can overwrite sK
         bad |= rebuild_tile<BITS, SH, KB>(p, p.vc, p.vs, p.vp, p.vcent, tv, t0, cnt, lane, sK, sRow);
-        for (int kk = 0; kk < cnt; kk++) {
+        // four keys at a time (their weights read as one vector per query), then the rest
+        // one by one; each accumulator adds the keys in order
+        int kk = 0;
+        for (; kk + 4 <= cnt; kk += 4) {
+            float4 v4[4];
+#pragma unroll
+            for (int u = 0; u < 4; u++) v4[u] = *reinterpret_cast<const float4 *>(sK + (kk + u) * kKRow + 4 * lane);
+#pragma unroll
+            for (int m = 0; m < MQ; m++) {
+                const float4 w4 = *reinterpret_cast<const float4 *>(sP + m * kAttnTile + kk);
+                const float w[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+                for (int u = 0; u < 4; u++) {
+                    o[m][0] = __fmaf_rn(w[u], v4[u].x, o[m][0]);
+                    o[m][1] = __fmaf_rn(w[u], v4[u].y, o[m][1]);
+                    o[m][2] = __fmaf_rn(w[u], v4[u].z, o[m][2]);
+                    o[m][3] = __fmaf_rn(w[u], v4[u].w, o[m][3]);
+                }
+            }
+        }
+        for (; kk < cnt; kk++) {
             const float4 v4 = *reinterpret_cast<const float4 *>(sK + kk * kKRow + 4 * lane);
 #pragma unroll
             for (int m = 0; m < MQ; m++) {
